@@ -1,0 +1,115 @@
+"""An independent, pure-Python reader of the blob format, for tests.
+
+Written from the format description (header, chunk table, grouped-chunk
+directory, rANS record), not from the oracle's code, and sharing nothing with
+either implementation. It decodes small blobs (tens of KiB) only. A blob that
+this reader and the oracle both turn back into the input is a valid encoding
+of the documented format, which pins the oracle's layout choices from the
+outside.
+
+Bit-level conventions it reads (ZipNN note, Method 1-2 readings): for the
+float dtypes the permuted word holds exponent | sign | mantissa from the top;
+stream j is byte j counted from the most significant byte.
+"""
+from __future__ import annotations
+
+import struct
+import zlib
+
+WORD = {1: 1, 2: 2, 3: 4, 4: 2, 5: 2, 6: 4}
+EXP = {4: 8, 5: 5, 6: 8}
+
+
+class SpecError(ValueError):
+    pass
+
+
+def _unpermute(p: int, dtype: int) -> int:
+    E = EXP.get(dtype)
+    if E is None:
+        return p
+    B = 8 * WORD[dtype]
+    e = p >> (B - E)
+    s = (p >> (B - E - 1)) & 1
+    m = p & ((1 << (B - 1 - E)) - 1)
+    return (s << (B - 1)) | (e << (B - 1 - E)) | m
+
+
+def _rans(rec: bytes, n: int) -> list[int]:
+    states = list(struct.unpack_from("<32I", rec, 0))
+    bitmap = rec[128:160]
+    present = [s for s in range(256) if bitmap[s // 8] >> (s % 8) & 1]
+    k = len(present)
+    freqs = struct.unpack_from(f"<{k}H", rec, 160)
+    words_at = 160 + (2 * k + 15) // 16 * 16
+    words = struct.unpack_from(f"<{(len(rec) - words_at) // 2}H", rec, words_at)
+    # slot -> symbol map, built by laying the symbols' slot ranges end to end
+    slot_sym, start = [], {}
+    for s, f in zip(present, freqs):
+        start[s] = len(slot_sym)
+        slot_sym += [s] * f
+    if len(slot_sym) != 4096:
+        raise SpecError("frequencies do not sum to 4096")
+    freq = dict(zip(present, freqs))
+    out = [0] * n
+    nxt = len(words)  # the words are consumed from the last one backwards
+    for i in range(n):
+        lane = i % 32
+        x = states[lane]
+        slot = x % 4096
+        s = slot_sym[slot]
+        x = freq[s] * (x // 4096) + slot - start[s]
+        if x < 65536:
+            nxt -= 1
+            if nxt < 0:
+                raise SpecError("ran out of words")
+            x = x * 65536 + words[nxt]
+        states[lane] = x
+        out[i] = s
+    if nxt != 0 or any(x != 65536 for x in states):
+        raise SpecError("bad final state")
+    return out
+
+
+def decode(blob: bytes) -> bytes:
+    if blob[:4] != b"ZCNN" or struct.unpack_from("<H", blob, 4)[0] != 1:
+        raise SpecError("magic/version")
+    dtype, ndim = blob[6], blob[7]
+    chunk_bytes, = struct.unpack_from("<I", blob, 8)
+    nbytes, = struct.unpack_from("<Q", blob, 16)
+    n_chunks, hcrc = struct.unpack_from("<II", blob, 24)
+    table_end = 96 + 16 * n_chunks
+    head = bytearray(blob[:table_end])
+    head[28:32] = b"\0\0\0\0"
+    if zlib.crc32(bytes(head)) != hcrc:
+        raise SpecError("header crc")
+    W = WORD[dtype]
+    out = bytearray()
+    for c in range(n_chunks):
+        off, sm, crc = struct.unpack_from("<QII", blob, 96 + 16 * c)
+        stored, raw = sm & 0x7FFFFFFF, sm >> 31
+        payload = blob[off:off + stored]
+        if zlib.crc32(payload) != crc:
+            raise SpecError(f"chunk {c} crc")
+        length = min(chunk_bytes, nbytes - c * chunk_bytes)
+        if raw:
+            out += payload
+            continue
+        n = length // W
+        pos = (4 * W + 15) // 16 * 16
+        streams = []
+        for j in range(W):
+            entry, = struct.unpack_from("<I", payload, 4 * j)
+            mode, v = entry >> 30, entry & 0x3FFFFFFF
+            if mode == 2:
+                streams.append([v] * n)
+                continue
+            rec = payload[pos:pos + v]
+            streams.append(list(rec) if mode == 0 else _rans(rec, n))
+            pos += (v + 15) // 16 * 16
+        for i in range(n):
+            p = 0
+            for j in range(W):
+                p = (p << 8) | streams[j][i]
+            out += _unpermute(p, dtype).to_bytes(W, "little")
+    return bytes(out)
