@@ -1,1 +1,222 @@
-"""GB300-native lossless compression of float model tensors (placeholder)."""
+"""GB300-native lossless compression of float model tensors.
+
+ZipNN-style pipeline (nucleation NOTE-241: ZipNN, Method): exponent
+extraction and byte grouping, per-chunk order-0 12-bit frequency tables,
+32-lane interleaved rANS with raw passthrough (cuZipNN 0.1.0 API:
+passthrough_threshold), a chunk-offset prefix scan and per-chunk zlib CRC-32.
+Every step runs in the CUDA kernels of ``libzc.so`` (include/zc.h); this
+module only marshals arguments through ctypes and uses PyTorch for device
+memory and streams. There is no CPU fallback: without the library every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+from .workloads import BF16, FP16, FP32, U8, U16, U32
+
+__all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspace_size",
+           "compress_into", "decompress_into", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
+           "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
+
+OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
+NO_VERIFY = 1
+DEFAULT_CHUNK = 131072
+DEFAULT_THRESHOLD = 0.95
+
+_TORCH_TO_CODE = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32,
+                  torch.uint8: U8, torch.int8: U8, torch.bool: U8,
+                  torch.int16: U16, torch.int32: U32}
+for _n, _c in (("uint16", U16), ("uint32", U32)):
+    if hasattr(torch, _n):
+        _TORCH_TO_CODE[getattr(torch, _n)] = _c
+_CODE_TO_TORCH = {BF16: torch.bfloat16, FP16: torch.float16, FP32: torch.float32,
+                  U8: torch.uint8, U16: torch.int16, U32: torch.int32}
+_WORD = {U8: 1, U16: 2, U32: 4, BF16: 2, FP16: 2, FP32: 4}
+
+
+class ZcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        names = [n for n, b in (("EINVAL", EINVAL), ("EFORMAT", EFORMAT), ("ECRC", ECRC),
+                                ("ECORRUPT", ECORRUPT), ("ETIMEOUT", ETIMEOUT),
+                                ("ECAPACITY", ECAPACITY), ("ECUDA", ECUDA)) if status & b]
+        super().__init__(f"{what}: status {status} ({'|'.join(names) or 'OK'})")
+        self.status = status
+
+
+class _Info(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * 8),
+                ("nbytes", ctypes.c_uint64), ("blob_bytes", ctypes.c_uint64),
+                ("n_chunks", ctypes.c_uint32), ("chunk_bytes", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libzc.so (built with nvcc on first use if absent)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            vp, u64, u32, i32, dbl = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, ctypes.c_double
+            L.zc_blob_size.restype = u64
+            L.zc_blob_size.argtypes = [u64, i32, u32, dbl]
+            L.zc_workspace_size.restype = u64
+            L.zc_workspace_size.argtypes = [u64, i32, u32]
+            L.zc_blob_info.restype = i32
+            L.zc_blob_info.argtypes = [vp, u64, ctypes.POINTER(_Info)]
+            L.zc_compress.restype = i32
+            L.zc_compress.argtypes = [vp, u64, i32, i32, ctypes.POINTER(ctypes.c_int64), u32, dbl,
+                                      vp, u64, vp, vp, u64, vp, vp]
+            L.zc_decompress.restype = i32
+            L.zc_decompress.argtypes = [vp, ctypes.POINTER(_Info), vp, u64, u32, vp, vp]
+            L.zc_crc32.restype = i32
+            L.zc_crc32.argtypes = [vp, u64, u64, vp, vp]
+            _lib = L
+    return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _TORCH_TO_CODE[t.dtype]
+    except KeyError:
+        raise ZcError(EINVAL, f"unsupported dtype {t.dtype}") from None
+
+
+def blob_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD) -> int:
+    return int(lib().zc_blob_size(nbytes, dtype, chunk_bytes, threshold))
+
+
+def workspace_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK) -> int:
+    return int(lib().zc_workspace_size(nbytes, dtype, chunk_bytes))
+
+
+def _check(st: int, what: str):
+    if st:
+        raise ZcError(st, what)
+
+
+def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tensor, workspace: torch.Tensor,
+                  status: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK,
+                  threshold: float = DEFAULT_THRESHOLD, stream=None, dtype: int | None = None,
+                  shape=None) -> None:
+    """Launch compression into caller buffers; no allocation, no sync.
+
+    ``blob_bytes`` is a 1-element int64 CUDA tensor that receives the blob
+    length; ``status`` a 1-element int32 CUDA tensor the caller zeroes."""
+    code = dtype_code(src) if dtype is None else dtype
+    shape = tuple(src.shape) if shape is None else tuple(shape)
+    shp = (ctypes.c_int64 * max(1, len(shape)))(*shape)
+    nbytes = src.numel() * src.element_size()
+    st = lib().zc_compress(src.data_ptr() if nbytes else None, nbytes, code, len(shape), shp, chunk_bytes,
+                           threshold, blob.data_ptr(), blob.numel(), blob_bytes.data_ptr(),
+                           workspace.data_ptr(), workspace.numel(), status.data_ptr(), _stream(stream))
+    _check(st, "zc_compress")
+
+
+def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
+             stream=None) -> torch.Tensor:
+    """Compress a CUDA tensor into a self-describing blob (1-D uint8 CUDA tensor).
+
+    Synchronises once, to read the blob length."""
+    if not t.is_cuda:
+        raise ZcError(EINVAL, "compress expects a CUDA tensor")
+    src = t.contiguous()
+    code = dtype_code(src)
+    nbytes = src.numel() * src.element_size()
+    cap = blob_size(nbytes, code, chunk_bytes, threshold)
+    if cap == 0:
+        raise ZcError(EINVAL, "invalid compression parameters")
+    dev = src.device
+    blob = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, workspace_size(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flat = src.view(-1).view(torch.uint8) if src.dtype != torch.bool else src.view(-1).view(torch.uint8)
+    compress_into(flat, blob, nb, ws, status, chunk_bytes, threshold, stream, dtype=code, shape=tuple(t.shape))
+    st, n = int(status.item()), int(nb.item())
+    _check(st, "zc_compress (device)")
+    return blob[:n]
+
+
+def blob_info(prefix) -> dict:
+    """Header and chunk table of a blob, from host bytes (or a CPU tensor)."""
+    if isinstance(prefix, torch.Tensor):
+        prefix = prefix.detach().cpu().contiguous().numpy().tobytes()
+    buf = ctypes.create_string_buffer(bytes(prefix), len(prefix))
+    info = _Info()
+    _check(lib().zc_blob_info(buf, len(prefix), ctypes.byref(info)), "zc_blob_info")
+    return _info_dict(info)
+
+
+def _info_dict(info: _Info) -> dict:
+    return dict(dtype=info.dtype, ndim=info.ndim, shape=tuple(info.shape[: info.ndim]),
+                nbytes=info.nbytes, blob_bytes=info.blob_bytes, n_chunks=info.n_chunks,
+                chunk_bytes=info.chunk_bytes)
+
+
+def _info_struct(d: dict) -> _Info:
+    info = _Info()
+    info.dtype, info.ndim = d["dtype"], d["ndim"]
+    for i, v in enumerate(d["shape"]):
+        info.shape[i] = v
+    info.nbytes, info.blob_bytes = d["nbytes"], d["blob_bytes"]
+    info.n_chunks, info.chunk_bytes = d["n_chunks"], d["chunk_bytes"]
+    return info
+
+
+def read_info(blob: torch.Tensor) -> dict:
+    """blob_info of a device blob (copies the header and table to the host)."""
+    head = blob[:96].cpu()
+    n_chunks = int.from_bytes(bytes(head[24:28].numpy()), "little")
+    return blob_info(blob[: 96 + 16 * n_chunks].cpu())
+
+
+def decompress_into(blob: torch.Tensor, info: dict, out: torch.Tensor, status: torch.Tensor,
+                    verify: bool = True, stream=None) -> None:
+    """Launch decompression into a caller buffer; no allocation, no sync."""
+    st = lib().zc_decompress(blob.data_ptr(), ctypes.byref(_info_struct(info)), out.data_ptr(),
+                             out.numel() * out.element_size(), 0 if verify else NO_VERIFY,
+                             status.data_ptr(), _stream(stream))
+    _check(st, "zc_decompress")
+
+
+def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True, stream=None) -> torch.Tensor:
+    """Restore the exact tensor (dtype and shape from the blob header)."""
+    if not blob.is_cuda:
+        raise ZcError(EINVAL, "decompress expects a CUDA blob")
+    info = read_info(blob) if info is None else info
+    dt = _CODE_TO_TORCH[info["dtype"]]
+    out = torch.empty(info["shape"], dtype=dt, device=blob.device)
+    status = torch.zeros(1, dtype=torch.int32, device=blob.device)
+    decompress_into(blob, info, out, status, verify, stream)
+    _check(int(status.item()), "zc_decompress (device)")
+    return out
+
+
+def crc32(t: torch.Tensor, piece_bytes: int = 16384, stream=None) -> torch.Tensor:
+    """zlib CRC-32 of every piece_bytes piece of a CUDA tensor's bytes
+    (int64 CUDA tensor of values in [0, 2^32)); piece_bytes=0: one CRC."""
+    if not t.is_cuda:
+        raise ZcError(EINVAL, "crc32 expects a CUDA tensor")
+    src = t.contiguous()
+    nbytes = src.numel() * src.element_size()
+    pieces = (nbytes + piece_bytes - 1) // piece_bytes if piece_bytes else 1
+    out = torch.empty(max(1, pieces), dtype=torch.int32, device=src.device)
+    _check(lib().zc_crc32(src.data_ptr() if nbytes else None, nbytes, piece_bytes, out.data_ptr(),
+                          _stream(stream)), "zc_crc32")
+    return out[:pieces].to(torch.int64) & 0xFFFFFFFF

@@ -1,0 +1,500 @@
+// encode.cu — single-pass compression kernel.
+//
+// One warp compresses one chunk at a time (ZipNN note, Method 5: fixed-size
+// chunks coded independently). Warps take chunk indices from a global ticket
+// counter, so every chunk below a warp's chunk is already owned by a running
+// warp. Per chunk a warp:
+//   1. builds one 256-bin histogram per byte stream (order-0 statistics, ZipNN
+//      note Key insight) from the exponent-extracted words;
+//   2. quantises each histogram to a 12-bit table;
+//   3. skips streams that provably cannot shrink below the threshold, and
+//      rANS-codes the others (32 interleaved lanes) into its workspace slot;
+//   4. applies the passthrough rule per stream and per chunk (cuZipNN API,
+//      passthrough_threshold);
+//   5. publishes its padded payload size and finds its blob offset with a
+//      decoupled look-back over the chunks before it (an exclusive prefix
+//      scan of the metadata map, ZipNN note Method 5);
+//   6. writes its payload, its CRC-32 and its chunk table entry.
+// The last warp to finish writes the header and its CRC.
+#include "zc_kernels.cuh"
+
+namespace zc {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int W>
+__device__ __forceinline__ uint32_t load_word(const uint8_t *p) {
+    if (W == 4) return *reinterpret_cast<const uint32_t *>(p);
+    if (W == 2) return *reinterpret_cast<const uint16_t *>(p);
+    return *p;
+}
+
+template <int W>
+__device__ __forceinline__ uint32_t stream_byte(uint32_t perm, int j) {
+    return (perm >> (8 * (W - 1 - j))) & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+    return __shfl_sync(kFull, v, 0);
+}
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+    return __shfl_sync(kFull, v, 0);
+}
+__device__ __forceinline__ float warp_sum_f32(float v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+    return __shfl_sync(kFull, v, 0);
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+// exclusive prefix sum over lanes
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+    uint32_t inc = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += t;
+    }
+    return inc - v;
+}
+
+// Histogram of the W byte streams of one chunk into h[W][256].
+template <int DT>
+__device__ void chunk_histograms(const uint8_t *src, uint32_t len, uint32_t (*h)[256]) {
+    constexpr int W = WordOf<DT>::W;
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < W * 256; i += 32) h[i >> 8][i & 255] = 0;
+    __syncwarp();
+    uint32_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
+    for (uint32_t v = lane; v < nvec; v += 32) {
+        uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+        uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int e = 0; e < 4 / W; e++) {
+                uint32_t w = (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+                uint32_t p = Perm<DT>::fwd(w);
+#pragma unroll
+                for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
+            }
+        }
+    }
+    for (uint32_t i = nvec * 16 / W + lane; i < len / W; i += 32) {
+        uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
+#pragma unroll
+        for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
+    }
+    __syncwarp();
+}
+
+// 12-bit table from counts held as 8 bins per lane (symbol 8*lane + k).
+// Same rule as the format's definition: floor share with a floor of 1,
+// shortfall to the most frequent symbol, excess taken from the largest
+// frequencies (lowest symbol on ties); runs of decrements on a unique maximum
+// are taken at once, which gives the same result as one at a time.
+__device__ void normalize_warp(const uint32_t cnt[8], uint32_t n, uint32_t f[8]) {
+    const int lane = threadIdx.x & 31;
+    uint32_t local = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        f[k] = cnt[k] ? max(1u, (cnt[k] * kM) / n) : 0u;
+        local += f[k];
+    }
+    uint32_t sum = warp_sum_u32(local);
+    if (sum < kM) {
+        uint32_t key = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            uint32_t s = 8 * lane + k;
+            key = max(key, (cnt[k] << 8) | (255u - s));
+        }
+        key = warp_max_u32(key);
+        uint32_t sb = 255u - (key & 0xFFu);
+        if ((sb >> 3) == uint32_t(lane)) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (k == int(sb & 7)) f[k] += kM - sum;
+        }
+    }
+    while (sum > kM) {
+        uint32_t key = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            uint32_t s = 8 * lane + k;
+            if (f[k] > 1) key = max(key, (f[k] << 8) | (255u - s));
+        }
+        key = warp_max_u32(key);
+        uint32_t f1 = key >> 8, s1 = 255u - (key & 0xFFu);
+        uint32_t key2 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            uint32_t s = 8 * lane + k;
+            if (f[k] > 1 && s != s1) key2 = max(key2, f[k]);
+        }
+        uint32_t m2 = max(warp_max_u32(key2), 1u);
+        uint32_t dec = (f1 > m2) ? min(sum - kM, f1 - m2) : 1u;
+        if ((s1 >> 3) == uint32_t(lane)) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (k == int(s1 & 7)) f[k] -= dec;
+        }
+        sum -= dec;
+    }
+}
+
+// Exclusive prefix of this chunk's padded size over the chunks before it
+// (decoupled look-back). Every wait is bounded; a timeout sets ZC_ETIMEOUT.
+__device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, int32_t *d_status) {
+    const int lane = threadIdx.x & 31;
+    if (c == 0) {
+        if (lane == 0) st_release(&st[0], kFlagPre | agg);
+        return 0;
+    }
+    if (lane == 0) st_release(&st[c], kFlagAgg | agg);
+    uint64_t excl = 0;
+    int64_t j = int64_t(c) - 1;
+    for (;;) {
+        int64_t idx = j - lane;
+        unsigned long long v = kFlagPre;  // before chunk 0: prefix 0
+        bool timed_out = false;
+        if (idx >= 0) {
+            uint32_t spins = 0;
+            v = ld_acquire(&st[idx]);
+            while ((v >> 62) == 0) {
+                if (++spins > kSpinLimit) { timed_out = true; break; }
+                __nanosleep(64);
+                v = ld_acquire(&st[idx]);
+            }
+        }
+        if (__any_sync(kFull, timed_out)) {
+            if (lane == 0) status_or(d_status, ZC_ETIMEOUT);
+            return excl;
+        }
+        uint32_t pre = __ballot_sync(kFull, (v >> 62) == 2);
+        int first = pre ? __ffs(pre) - 1 : 31;
+        excl += warp_sum_u64(lane <= first ? (v & kValMask) : 0ull);
+        if (pre) break;
+        j -= 32;
+    }
+    if (lane == 0) st_release(&st[c], kFlagPre | (excl + agg));
+    return excl;
+}
+
+struct ChunkPlan {
+    uint32_t mode[4];
+    uint32_t val[4];   // RAW: n, RANS: record bytes, CONST: symbol
+};
+
+// Code stream j of the chunk into rec (the workspace record area). Returns
+// the record's unpadded size. f/cum are the lane's 8 table entries.
+template <int DT>
+__device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, const uint32_t f[8],
+                                       uint2 *etab, uint8_t *rec) {
+    constexpr int W = WordOf<DT>::W;
+    const int lane = threadIdx.x & 31;
+    // table: bitmap byte per lane, frequencies in symbol order, encoder entries
+    uint32_t present = 0, fsum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        present += f[k] ? 1u : 0u;
+        fsum += f[k];
+    }
+    uint32_t rank = warp_excl_scan(present);
+    uint32_t cum = warp_excl_scan(fsum);
+    uint32_t k_total = __shfl_sync(kFull, rank + present, 31);
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        uint32_t s = 8 * lane + k;
+        uint32_t fs = f[k];
+        if (fs) {
+            bits |= 1u << k;
+            reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
+            uint32_t l = 32 - __clz(fs - 1);  // ceil(log2 fs); 0 for fs = 1
+            // Granlund & Montgomery (1994), division by invariant integers:
+            // m = floor(2^32 (2^l - d) / d) + 1 gives floor(x/d) =
+            // (mulhi(m, x) + x) >> l for every 32-bit x.
+            uint32_t m = uint32_t((((1ull << l) - fs) << 32) / fs + 1);
+            etab[s] = make_uint2(m, fs | (cum << 12) | (l << 24));
+        }
+        cum += fs;
+    }
+    rec[128 + lane] = uint8_t(bits);
+    uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
+    for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
+    __syncwarp();
+
+    uint16_t *wout = reinterpret_cast<uint16_t *>(rec + words_at);
+    const uint32_t gt = lanemask_gt();
+    uint32_t x = kRansL;
+    uint32_t wc = 0;
+    const int T = int((n + 31) / 32);
+    constexpr int B = 8;
+    uint32_t buf[B];
+#pragma unroll
+    for (int k = 0; k < B; k++) {
+        int t = T - 1 - k;
+        uint32_t i = uint32_t(t) * 32 + lane;
+        buf[k] = (t >= 0 && i < n) ? load_word<W>(src + uint64_t(i) * W) : 0u;
+    }
+    for (int t0 = T - 1; t0 >= 0; t0 -= B) {
+        uint32_t nxt[B];
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            int t = t0 - B - k;
+            uint32_t i = uint32_t(t) * 32 + lane;
+            nxt[k] = (t >= 0 && i < n) ? load_word<W>(src + uint64_t(i) * W) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            int t = t0 - k;
+            if (t < 0) break;
+            bool active = uint32_t(t) * 32 + lane < n;
+            uint32_t s = stream_byte<W>(Perm<DT>::fwd(buf[k]), j);
+            uint2 e = etab[s];
+            uint32_t fs = e.y & 0xFFFu, cs = (e.y >> 12) & 0xFFFu, l = e.y >> 24;
+            bool emit = active && x >= (fs << 20);
+            uint32_t bal = __ballot_sync(kFull, emit);
+            if (emit) {
+                wout[wc + __popc(bal & gt)] = uint16_t(x & 0xFFFFu);
+                x >>= 16;
+            }
+            wc += __popc(bal);
+            if (active) {
+                uint32_t q = uint32_t((uint64_t(__umulhi(x, e.x)) + x) >> l);
+                x = (q << kProbBits) + (x - q * fs) + cs;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < B; k++) buf[k] = nxt[k];
+    }
+    reinterpret_cast<uint32_t *>(rec)[lane] = x;
+    uint32_t rec_bytes = words_at + 2 * wc;
+    for (uint32_t b = rec_bytes + lane; b < pad16(rec_bytes); b += 32) rec[b] = 0;
+    __syncwarp();
+    return rec_bytes;
+}
+
+// Write raw stream j (its n bytes, zero-padded to 16) at dst (16-aligned).
+template <int DT>
+__device__ void write_raw_stream(const uint8_t *src, uint32_t n, int j, uint8_t *dst) {
+    constexpr int W = WordOf<DT>::W;
+    const int lane = threadIdx.x & 31;
+    uint32_t groups = (n + 15) / 16;
+    for (uint32_t g = lane; g < groups; g += 32) {
+        uint32_t b[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            uint32_t i = g * 16 + k;
+            b[k] = i < n ? stream_byte<W>(Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W)), j) : 0u;
+        }
+        uint4 v;
+        v.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        v.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+        v.z = b[8] | (b[9] << 8) | (b[10] << 16) | (b[11] << 24);
+        v.w = b[12] | (b[13] << 8) | (b[14] << 16) | (b[15] << 24);
+        reinterpret_cast<uint4 *>(dst)[g] = v;
+    }
+}
+
+__device__ void copy_bytes(const uint8_t *src, uint64_t len, uint8_t *dst /*16-aligned*/) {
+    const int lane = threadIdx.x & 31;
+    uint64_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
+    for (uint64_t v = lane; v < nvec; v += 32)
+        reinterpret_cast<uint4 *>(dst)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+    for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? src[i] : 0;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kWarps * 32) encode_kernel(EncodeArgs a) {
+    constexpr int W = WordOf<DT>::W;
+    __shared__ uint32_t crc_tab[8][256];
+    __shared__ uint32_t hist[kWarps][W][256];
+    __shared__ uint2 etab[kWarps][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    load_crc_smem(crc_tab);
+    __syncthreads();
+
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
+    uint8_t *slot = a.ws_slots + (uint64_t(blockIdx.x) * kWarps + warp) * a.slot_bytes;
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
+
+    for (;;) {
+        uint32_t c = 0;
+        if (lane == 0) c = atomicAdd(&ctrl[0], 1u);
+        c = __shfl_sync(kFull, c, 0);
+        if (c >= a.n_chunks) break;
+
+        const uint8_t *src = a.src + uint64_t(c) * a.chunk_bytes;
+        const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
+        const uint32_t n = len / W;
+
+        chunk_histograms<DT>(src, len, hist[warp]);
+
+        ChunkPlan plan;
+        uint64_t grouped = 16;  // pad16(4W) for W <= 4
+        const uint64_t rec_stride = pad16(kRecHead + kMaxTable + 2ull * (a.chunk_bytes / W));
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            uint32_t cnt[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) cnt[k] = hist[warp][j][8 * lane + k];
+            uint32_t pres = 0, only = 0;
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (cnt[k]) { pres++; only = 8 * lane + k; }
+            uint32_t k_total = warp_sum_u32(pres);
+            if (k_total == 1) {
+                uint32_t who = __ballot_sync(kFull, pres != 0);
+                plan.mode[j] = kModeConst;
+                plan.val[j] = __shfl_sync(kFull, only, __ffs(who) - 1);
+                continue;
+            }
+            uint32_t f[8];
+            normalize_warp(cnt, n, f);
+            // Lower bound on the coded size from the table's information
+            // content: every coded symbol adds at least log2(4096/f_s) +
+            // log2(15/16) bits to its lane's state, every word removes at most
+            // 16.1 bits, and 32 states of at most 32 bits remain.
+            float info = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (cnt[k]) info += float(cnt[k]) * (12.0f - __log2f(float(f[k])));
+            info = warp_sum_f32(info);
+            float words_lb = (info * (1.0f - 1.0f / 1024) - 0.0932f * float(n) - 512.0f - 64.0f) / 16.1f;
+            uint64_t rec_lb = kRecHead + pad16(2 * k_total) + 2ull * uint64_t(words_lb > 0.f ? words_lb : 0.f);
+            if (double(rec_lb) >= a.threshold * double(n)) {
+                plan.mode[j] = kModeRaw;
+                plan.val[j] = n;
+                grouped += pad16(n);
+                continue;
+            }
+            uint8_t *rec = slot + uint64_t(j) * rec_stride;
+            uint32_t rb = rans_encode_stream<DT>(src, n, j, f, etab[warp], rec);
+            if (double(rb) < a.threshold * double(n)) {
+                plan.mode[j] = kModeRans;
+                plan.val[j] = rb;
+                grouped += pad16(rb);
+            } else {
+                plan.mode[j] = kModeRaw;
+                plan.val[j] = n;
+                grouped += pad16(n);
+            }
+        }
+        const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
+        const uint64_t stored = raw_chunk ? len : grouped;
+
+        const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status);
+        const bool fits = off + pad16(stored) <= a.cap;
+        if (!fits && lane == 0) status_or(a.d_status, ZC_ECAPACITY);
+
+        uint32_t crc = 0;
+        if (fits) {
+            uint8_t *out = a.blob + off;
+            if (raw_chunk) {
+                copy_bytes(src, len, out);
+            } else {
+                if (lane < 4) {
+                    uint32_t e = 0;
+#pragma unroll
+                    for (int j = 0; j < W; j++)
+                        if (lane == j) e = (plan.mode[j] << 30) | plan.val[j];
+                    reinterpret_cast<uint32_t *>(out)[lane] = e;
+                }
+                uint64_t pos = 16;
+#pragma unroll
+                for (int j = 0; j < W; j++) {
+                    if (plan.mode[j] == kModeRaw) {
+                        write_raw_stream<DT>(src, n, j, out + pos);
+                        pos += pad16(n);
+                    } else if (plan.mode[j] == kModeRans) {
+                        copy_bytes(slot + uint64_t(j) * rec_stride, pad16(plan.val[j]), out + pos);
+                        pos += pad16(plan.val[j]);
+                    }
+                }
+            }
+            __syncwarp();
+            __threadfence_block();
+            crc = warp_crc_raw<true>(out, stored, 0xFFFFFFFFu, crc_tab) ^ 0xFFFFFFFFu;
+            if (lane == 0) {
+                uint4 ent;
+                ent.x = uint32_t(off);
+                ent.y = uint32_t(off >> 32);
+                ent.z = uint32_t(stored) | (raw_chunk ? 0x80000000u : 0u);
+                ent.w = crc;
+                reinterpret_cast<uint4 *>(a.blob + ZC_HEADER_BYTES)[c] = ent;
+                // header CRC = shift(crc(header), 16 n) ^ XOR_c shift(crc(entry_c), 16 (n-1-c))
+                uint32_t ec = 0xFFFFFFFFu;
+                uint32_t words[4] = {ent.x, ent.y, ent.z, ent.w};
+                for (int q = 0; q < 4; q += 2) ec = crc_step8(ec, words[q], words[q + 1], crc_tab);
+                ec ^= 0xFFFFFFFFu;
+                uint32_t contrib = gf2_mulmod(ec, gf2_xpow8(16ull * (a.n_chunks - 1 - c)));
+                atomicXor(&ctrl[2], contrib);
+            }
+        }
+        if (lane == 0) {
+            __threadfence();
+            uint32_t done = atomicAdd(&ctrl[1], 1u);
+            if (done == a.n_chunks - 1) {
+                __threadfence();
+                uint32_t acc = atomicXor(&ctrl[2], 0u);
+                unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
+                uint64_t total = table_end + (last & kValMask);
+                uint32_t hc = 0xFFFFFFFFu;
+                for (int q = 0; q < 24; q += 2) hc = crc_step8(hc, a.header[q], a.header[q + 1], crc_tab);
+                hc ^= 0xFFFFFFFFu;
+                uint32_t hcrc = gf2_mulmod(hc, gf2_xpow8(16ull * a.n_chunks)) ^ acc;
+                uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
+                for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : a.header[q];
+                *a.d_blob_bytes = total;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// A blob of an empty tensor is its header alone (its CRC made on the host).
+__global__ void empty_blob_kernel(EncodeArgs a) {
+    if (threadIdx.x < 24) reinterpret_cast<uint32_t *>(a.blob)[threadIdx.x] = a.header[threadIdx.x];
+    if (threadIdx.x == 0) *a.d_blob_bytes = ZC_HEADER_BYTES;
+}
+
+} // namespace
+
+int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s) {
+    if (a.n_chunks == 0) {
+        empty_blob_kernel<<<1, 32, 0, s>>>(a);
+        return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+    }
+    switch (dtype) {
+    case ZC_U8: encode_kernel<ZC_U8><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_U16: encode_kernel<ZC_U16><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_U32: encode_kernel<ZC_U32><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_BF16: encode_kernel<ZC_BF16><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_FP16: encode_kernel<ZC_FP16><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_FP32: encode_kernel<ZC_FP32><<<grid, kWarps * 32, 0, s>>>(a); break;
+    default: return ZC_EINVAL;
+    }
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
+
+int encode_warps_per_cta() { return kWarps; }
+
+} // namespace zc

@@ -1,0 +1,253 @@
+// zc_api.cu — the C ABI (include/zc.h): argument checks, workspace layout,
+// header construction and kernel launches. No entry point allocates memory or
+// synchronises; device-side errors are reported through *d_status.
+#include <cmath>
+#include <cstring>
+
+#include "zc_kernels.cuh"
+
+namespace {
+
+using namespace zc;
+
+constexpr uint32_t kWorkersPerSM = 8;   // encoder warps resident per SM
+constexpr uint64_t kCtrlBytes = 256;    // ticket, done counter, header CRC accumulator
+constexpr uint64_t kCrcUnit = 32768;    // bytes per warp in zc_crc32
+
+uint64_t pad256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+bool valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
+    int W = word_bytes(dtype);
+    if (W == 0 || nbytes % uint64_t(W)) return false;
+    if (chunk_bytes < ZC_MIN_CHUNK || chunk_bytes > ZC_MAX_CHUNK || chunk_bytes % 64) return false;
+    if (!(threshold > 0.0) || !(threshold <= 1e9)) return false;
+    if ((nbytes + chunk_bytes - 1) / chunk_bytes > 0xFFFFFFFFull) return false;
+    return true;
+}
+
+uint64_t chunks_of(uint64_t nbytes, uint32_t chunk_bytes) { return (nbytes + chunk_bytes - 1) / chunk_bytes; }
+
+// Staging for one warp: room for a coded record of every stream of a chunk.
+uint64_t slot_bytes(uint32_t chunk_bytes, int W) {
+    return pad256(uint64_t(W) * pad16(kRecHead + kMaxTable + 2ull * (chunk_bytes / W)));
+}
+
+uint32_t host_crc_table[256];
+bool host_crc_ready = false;
+
+uint32_t host_crc32(const uint8_t *p, uint64_t n, uint32_t reg = 0xFFFFFFFFu) {
+    if (!host_crc_ready) {  // idempotent; a race only recomputes the same values
+        for (uint32_t b = 0; b < 256; b++) {
+            uint32_t r = b;
+            for (int k = 0; k < 8; k++) r = gf2_mul_x(r);
+            host_crc_table[b] = r;
+        }
+        host_crc_ready = true;
+    }
+    for (uint64_t i = 0; i < n; i++) reg = host_crc_table[(reg ^ p[i]) & 0xFF] ^ (reg >> 8);
+    return reg;
+}
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+uint64_t worker_count(uint64_t n_chunks) {
+    const uint64_t per = uint64_t(encode_warps_per_cta());
+    uint64_t want = (n_chunks + per - 1) / per * per;
+    uint64_t most = uint64_t(sm_count()) * kWorkersPerSM;
+    most = most / per * per;
+    if (most < per) most = per;
+    return want < most ? want : most;
+}
+
+uint32_t get32(const uint8_t *p) { return uint32_t(p[0]) | uint32_t(p[1]) << 8 | uint32_t(p[2]) << 16 | uint32_t(p[3]) << 24; }
+uint64_t get64(const uint8_t *p) { return uint64_t(get32(p)) | uint64_t(get32(p + 4)) << 32; }
+void put32(uint8_t *p, uint32_t v) { for (int i = 0; i < 4; i++) p[i] = uint8_t(v >> (8 * i)); }
+void put64(uint8_t *p, uint64_t v) { for (int i = 0; i < 8; i++) p[i] = uint8_t(v >> (8 * i)); }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+} // namespace
+
+extern "C" uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
+    if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return 0;
+    const int W = word_bytes(dtype);
+    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
+    uint64_t total = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc;
+    if (nc == 0) return total;
+    const uint64_t full = nc - 1, last = nbytes - full * chunk_bytes;
+    auto worst = [&](uint64_t len) {
+        uint64_t w = pad16(len);
+        if (threshold > 1.0 && max_grouped(len, W) > w) w = max_grouped(len, W);
+        return w;
+    };
+    return total + full * worst(chunk_bytes) + worst(last);
+}
+
+extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes) {
+    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95)) return 0;
+    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
+    if (nc == 0) return kCtrlBytes;
+    return kCtrlBytes + pad256(8 * nc) + worker_count(nc) * slot_bytes(chunk_bytes, word_bytes(dtype));
+}
+
+extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out) {
+    const uint8_t *b = static_cast<const uint8_t *>(h_blob_prefix);
+    if (!b || !out || avail < ZC_HEADER_BYTES) return ZC_EFORMAT;
+    if (std::memcmp(b, "ZCNN", 4) != 0 || (b[4] | b[5] << 8) != 1) return ZC_EFORMAT;
+    const int dtype = b[6], ndim = b[7];
+    const uint32_t chunk_bytes = get32(b + 8);
+    const uint64_t nbytes = get64(b + 16);
+    const uint32_t nc = get32(b + 24);
+    const int W = word_bytes(dtype);
+    if (W == 0 || ndim > 8 || b[12] != kLanes || b[13] != kProbBits || b[14] || b[15]) return ZC_EFORMAT;
+    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95) || chunks_of(nbytes, chunk_bytes) != nc) return ZC_EFORMAT;
+    uint64_t elems = 1;
+    for (int d = 0; d < 8; d++) {
+        int64_t v = int64_t(get64(b + 32 + 8 * d));
+        if (d >= ndim) {
+            if (v != 0) return ZC_EFORMAT;
+            continue;
+        }
+        if (v < 0) return ZC_EFORMAT;
+        if (v && elems > UINT64_MAX / uint64_t(v)) return ZC_EFORMAT;
+        elems *= uint64_t(v);
+    }
+    if (elems * uint64_t(W) != nbytes) return ZC_EFORMAT;
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc;
+    if (avail < table_end) return ZC_EFORMAT;
+    uint8_t head[ZC_HEADER_BYTES];
+    std::memcpy(head, b, ZC_HEADER_BYTES);
+    put32(head + 28, 0);
+    uint32_t reg = host_crc32(head, ZC_HEADER_BYTES);
+    reg = host_crc32(b + ZC_HEADER_BYTES, table_end - ZC_HEADER_BYTES, reg);
+    if ((reg ^ 0xFFFFFFFFu) != get32(b + 28)) return ZC_ECRC;
+    uint64_t off = table_end;
+    for (uint32_t c = 0; c < nc; c++) {
+        const uint8_t *e = b + ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * c;
+        const uint64_t len = (c + 1 < nc) ? chunk_bytes : nbytes - uint64_t(c) * chunk_bytes;
+        const uint32_t sm = get32(e + 8), stored = sm & 0x7FFFFFFFu;
+        if (get64(e) != off) return ZC_EFORMAT;
+        if ((sm >> 31) ? stored != len : (stored % 16 || stored > max_grouped(len, W))) return ZC_EFORMAT;
+        off += pad16(stored);
+    }
+    out->dtype = dtype;
+    out->ndim = ndim;
+    for (int d = 0; d < 8; d++) out->shape[d] = int64_t(get64(b + 32 + 8 * d));
+    out->nbytes = nbytes;
+    out->blob_bytes = off;
+    out->n_chunks = nc;
+    out->chunk_bytes = chunk_bytes;
+    return ZC_OK;
+}
+
+extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                           uint32_t chunk_bytes, double threshold,
+                           void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                           void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZC_EINVAL;
+    if (ndim < 0 || ndim > 8 || (ndim > 0 && !h_shape)) return ZC_EINVAL;
+    const int W = word_bytes(dtype);
+    uint64_t elems = 1;
+    for (int d = 0; d < ndim; d++) {
+        if (h_shape[d] < 0) return ZC_EINVAL;
+        if (h_shape[d] && elems > UINT64_MAX / uint64_t(h_shape[d])) return ZC_EINVAL;
+        elems *= uint64_t(h_shape[d]);
+    }
+    if (elems * uint64_t(W) != nbytes) return ZC_EINVAL;
+    if (!d_blob || !d_blob_bytes || !d_status || !d_ws || (nbytes && !d_src)) return ZC_EINVAL;
+    if (!aligned(d_src, W) || !aligned(d_blob, 16) || !aligned(d_ws, 16) || !aligned(d_blob_bytes, 8))
+        return ZC_EINVAL;
+    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc;
+    if (blob_capacity < table_end) return ZC_ECAPACITY;
+
+    EncodeArgs a{};
+    a.src = static_cast<const uint8_t *>(d_src);
+    a.nbytes = nbytes;
+    a.chunk_bytes = chunk_bytes;
+    a.n_chunks = uint32_t(nc);
+    a.threshold = threshold;
+    a.blob = static_cast<uint8_t *>(d_blob);
+    a.cap = blob_capacity;
+    a.d_blob_bytes = d_blob_bytes;
+    a.d_status = d_status;
+
+    uint8_t head[ZC_HEADER_BYTES] = {};
+    std::memcpy(head, "ZCNN", 4);
+    head[4] = 1;
+    head[6] = uint8_t(dtype);
+    head[7] = uint8_t(ndim);
+    put32(head + 8, chunk_bytes);
+    head[12] = uint8_t(kLanes);
+    head[13] = uint8_t(kProbBits);
+    put64(head + 16, nbytes);
+    put32(head + 24, uint32_t(nc));
+    for (int d = 0; d < ndim; d++) put64(head + 32 + 8 * d, uint64_t(h_shape[d]));
+    if (nc == 0) put32(head + 28, host_crc32(head, ZC_HEADER_BYTES) ^ 0xFFFFFFFFu);
+    std::memcpy(a.header, head, ZC_HEADER_BYTES);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int grid = 1;
+    if (nc) {
+        const uint64_t fixed = kCtrlBytes + pad256(8 * nc);
+        const uint64_t slot = slot_bytes(chunk_bytes, W);
+        const uint64_t per = uint64_t(encode_warps_per_cta());
+        if (ws_bytes < fixed + per * slot) return ZC_ECAPACITY;
+        uint64_t workers = worker_count(nc);
+        uint64_t fit = (ws_bytes - fixed) / slot / per * per;
+        if (workers > fit) workers = fit;
+        a.ws_ctrl = static_cast<uint8_t *>(d_ws);
+        a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + kCtrlBytes);
+        a.ws_slots = a.ws_ctrl + fixed;
+        a.slot_bytes = slot;
+        grid = int(workers / per);
+        if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
+    }
+    return launch_encode(dtype, a, grid, s);
+}
+
+extern "C" int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
+                             uint32_t flags, int32_t *d_status, void *stream) {
+    if (!info || !d_status || !d_blob) return ZC_EINVAL;
+    const int W = word_bytes(info->dtype);
+    if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
+    if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
+    if (info->blob_bytes < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks) return ZC_EINVAL;
+    if (dst_capacity < info->nbytes || (info->nbytes && !d_dst)) return ZC_ECAPACITY;
+    if (!aligned(d_blob, 16) || !aligned(d_dst, W)) return ZC_EINVAL;
+    if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
+    DecodeArgs a{};
+    a.blob = static_cast<const uint8_t *>(d_blob);
+    a.blob_bytes = info->blob_bytes;
+    a.nbytes = info->nbytes;
+    a.chunk_bytes = info->chunk_bytes;
+    a.n_chunks = info->n_chunks;
+    a.dst = static_cast<uint8_t *>(d_dst);
+    a.flags = flags;
+    a.d_status = d_status;
+    return launch_decode(info->dtype, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream) {
+    if (!d_out || (nbytes && !d_data)) return ZC_EINVAL;
+    const uint64_t piece = piece_bytes ? piece_bytes : (nbytes ? nbytes : 1);
+    const uint64_t pieces = piece_bytes ? (nbytes + piece - 1) / piece : 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pieces == 0) return ZC_OK;
+    if (cudaMemsetAsync(d_out, 0, pieces * 4, s) != cudaSuccess) return ZC_ECUDA;
+    if (nbytes == 0) return ZC_OK;
+    CrcArgs a{};
+    a.data = static_cast<const uint8_t *>(d_data);
+    a.nbytes = nbytes;
+    a.piece = piece;
+    a.unit = kCrcUnit;
+    a.units_per_piece = (piece + kCrcUnit - 1) / kCrcUnit;
+    a.n_units = pieces * a.units_per_piece;
+    a.out = d_out;
+    return launch_crc(a, s);
+}

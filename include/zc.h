@@ -1,0 +1,149 @@
+/*
+ * zc.h — C ABI of the GB300 (sm_103a) lossless compressor for float model
+ * tensors: exponent extraction + byte grouping, per-chunk order-0 12-bit
+ * frequency tables, 32-lane interleaved rANS with raw passthrough, a chunk
+ * offset prefix scan, and per-chunk CRC-32.
+ *
+ * Sources (web pages, cited by title and section):
+ *   cuZipNN 0.1.0 (PyPI): Usage (tensor in, blob out, torch.equal round trip;
+ *     the blob records dtype and shape), API (chunk_bytes, passthrough
+ *     threshold, CRC-32 helpers that match zlib.crc32), Blob format (a format
+ *     version that other versions reject).
+ *   nucleation NOTE-241: ZipNN — Method 1-5 (exponent extraction, byte
+ *     grouping, entropy-only coding, all-constant streams stored as a header,
+ *     fixed chunks with a metadata map of variable compressed sizes).
+ *   lmzip 1.3.0 (PyPI metadata) — "Building on lmz": the device entry point
+ *     takes the caller's device pointers and stream, allocates nothing,
+ *     creates no context and does not synchronise; interleaved rANS lanes.
+ *
+ * Conventions for every entry point:
+ *   - "d_" pointers are device pointers on the current CUDA device; "h_"
+ *     pointers are host pointers. The caller owns every buffer, the stream and
+ *     the context. No entry point allocates memory, creates streams, or
+ *     synchronises.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - The return value reports argument errors found on the host before any
+ *     launch, and launch errors (ZC_ECUDA). Errors only the device can see
+ *     are OR-ed into *d_status, which the caller zeroes before the call;
+ *     results and *d_status are valid once the stream has been synchronised.
+ *   - Blob format v1 (byte layout): 96-byte header ("ZCNN", version 1,
+ *     dtype, ndim, chunk_bytes, lanes = 32, prob_bits = 12, nbytes,
+ *     n_chunks, header CRC-32 over header + chunk table, shape[8]); a chunk
+ *     table of 16-byte entries {u64 offset, u32 stored | raw << 31, u32
+ *     CRC-32 of the stored bytes}; then the chunk payloads, each zero-padded
+ *     to 16 bytes. All integers little-endian.
+ */
+#ifndef ZC_H
+#define ZC_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZC_API __attribute__((visibility("default")))
+#else
+#define ZC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the tensor. The float types get exponent extraction
+ * (exponent byte first, then sign, then mantissa); the integer types are
+ * byte-grouped as they are. */
+enum zc_dtype { ZC_U8 = 1, ZC_U16 = 2, ZC_U32 = 3, ZC_BF16 = 4, ZC_FP16 = 5, ZC_FP32 = 6 };
+
+/* Status bits; several may be OR-ed together. */
+enum zc_status {
+    ZC_OK = 0,
+    ZC_EINVAL = 1,     /* bad argument (host) */
+    ZC_EFORMAT = 2,    /* not a v1 blob, or a malformed header/table */
+    ZC_ECRC = 4,       /* a CRC-32 did not match */
+    ZC_ECORRUPT = 8,   /* payload structure or rANS stream invalid */
+    ZC_ETIMEOUT = 16,  /* a bounded device wait gave up */
+    ZC_ECAPACITY = 32, /* an output or workspace buffer is too small */
+    ZC_ECUDA = 64      /* a CUDA launch or memset failed */
+};
+
+/* zc_decompress flag: skip the per-chunk CRC-32 check. */
+#define ZC_NO_VERIFY 1u
+
+/* Parameter limits of format v1. */
+#define ZC_MIN_CHUNK 64u
+#define ZC_MAX_CHUNK 131072u   /* chunk_bytes: a multiple of 64 in [64, 131072] */
+#define ZC_HEADER_BYTES 96u
+#define ZC_ENTRY_BYTES 16u
+
+/* What a blob header and chunk table say (filled by zc_blob_info). */
+typedef struct {
+    int32_t dtype;
+    int32_t ndim;
+    int64_t shape[8];
+    uint64_t nbytes;      /* original tensor bytes */
+    uint64_t blob_bytes;  /* total blob length */
+    uint32_t n_chunks;
+    uint32_t chunk_bytes;
+} zc_info;
+
+/* Worst-case blob length for compressing nbytes of dtype with these
+ * parameters (cuZipNN API: a chunk is kept coded only if it shrinks below
+ * threshold x its size, so for threshold <= 1 no chunk grows beyond its raw
+ * size; threshold > 1, a test setting that forces coding, allows growth).
+ * Returns 0 if the parameters are invalid. Host only, no CUDA call. */
+ZC_API uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold);
+
+/* Device workspace zc_compress needs for these parameters on the current
+ * device (chunk status words for the offset scan plus per-worker staging
+ * for coded words). Returns 0 for invalid parameters. Queries the device's
+ * SM count; no allocation, no synchronisation. */
+ZC_API uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes);
+
+/* Parse and check a blob's header and chunk table from a host copy of its
+ * first `avail` bytes (at least 96 + 16 * n_chunks). Checks magic, version,
+ * field ranges, the header CRC-32 and that the table describes the packed
+ * layout exactly. Returns ZC_OK, ZC_EFORMAT or ZC_ECRC. Host only. */
+ZC_API int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out);
+
+/* Compress a contiguous row-major tensor (cuZipNN Usage: tensor in,
+ * self-describing blob out).
+ *   d_src        nbytes of input, aligned to the element size
+ *   dtype, ndim, shape[ndim]  recorded in the header; prod(shape) * element
+ *                size must equal nbytes; 0 <= ndim <= 8
+ *   chunk_bytes  multiple of 64 in [64, 131072] (ZipNN Method 5 chunks;
+ *                cuZipNN default 131072)
+ *   threshold    > 0 (cuZipNN passthrough_threshold; 0.95 by default)
+ *   d_blob       output, blob_capacity >= zc_blob_size(...)
+ *   d_blob_bytes receives the blob length (device u64)
+ *   d_ws         workspace of ws_bytes >= zc_workspace_size(...); its
+ *                contents are scratch and need no initialisation
+ *   d_status     device int32, OR-ed with ZC_ETIMEOUT / ZC_ECAPACITY
+ * The output is byte-identical to the format's CPU definition. */
+ZC_API int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                uint32_t chunk_bytes, double threshold,
+                void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream);
+
+/* Decompress a device-resident blob whose header was read with zc_blob_info
+ * into `info` (cuZipNN API decompress_tensor: decoding runs on the GPU).
+ *   d_blob       the blob (info->blob_bytes bytes)
+ *   d_dst        output, dst_capacity >= info->nbytes, aligned to the
+ *                element size
+ *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check)
+ *   d_status     device int32, OR-ed with ZC_ECRC / ZC_ECORRUPT / ZC_EFORMAT
+ * Chunks that fail a check are not written (their output bytes are
+ * unspecified). Every device read is bounds-checked against the blob. */
+ZC_API int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
+                  uint32_t flags, int32_t *d_status, void *stream);
+
+/* zlib-compatible CRC-32 of each piece_bytes-byte piece of a device buffer,
+ * the last piece possibly shorter (cuZipNN API hash_tensor_with_crc32,
+ * checksum_chunk_bytes). piece_bytes = 0 means one CRC of the whole buffer.
+ * d_out receives ceil(nbytes / piece_bytes) uint32 values (1 for
+ * piece_bytes = 0; none for nbytes = 0 with pieces); it is zeroed on the
+ * stream by this call before the kernel runs. */
+ZC_API int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
