@@ -105,6 +105,8 @@ def test_crc32_large_whole_buffer():
 def _rand_tensor(rng, dtype, n):
     W = W_OF[dtype]
     kind = int(rng.integers(0, 6))
+    if n == 0:
+        return np.zeros(0, np.uint8)
     if kind == 0:
         return rng.integers(0, 256, n * W, dtype=np.uint8)
     if kind == 1:
@@ -123,7 +125,8 @@ def _rand_tensor(rng, dtype, n):
         x = x.half()
     elif kind == 5:
         x = x.bfloat16().float()
-    return x.view(torch.uint8).numpy().copy() if dtype == 6 else x.view(torch.int16).numpy().view(np.uint8).copy()
+    x = x.contiguous()
+    return x.numpy().view(np.uint8).copy() if dtype == 6 else x.view(torch.int16).numpy().view(np.uint8).copy()
 
 
 def test_random_small_tensors(zco):
