@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark: encode and decode throughput (GB/s of original bytes) of the
+compressor on one GB300, with the HBM roofline fraction and the size ratio.
+
+A step is one pass of the whole hot path over one tensor: compression (byte
+grouping, per-chunk tables, rANS with passthrough, offset scan, CRC-32) and
+decompression of the blob it made (CRC check, rANS decode, merge). Inputs are
+device-resident when the timed region starts; they are larger than the L2
+cache (no flush needed). `value` = original bytes of all ranks / (encode +
+decode time); encode and decode are also reported on their own.
+
+`--impl reference` times the CPU oracle (plain C, one thread) on a bounded
+sample of the same workload, as the reference arm.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one independent replica per GPU (the path shards by
+tensor and needs no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="fp32_64m",
+                   choices=["fp32_64m", "bf16_1m", "fp32clean_64m", "fp16_16m", "bf16_delta", "bf16_llama_gate"])
+    p.add_argument("--chunk-bytes", type=int, default=131072)
+    p.add_argument("--threshold", type=float, default=0.95)
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-verify", action="store_true", help="decode without the CRC check")
+    return p.parse_args()
+
+
+def make_workload(name: str, device):
+    from entropy_coding_gb300 import workloads as wl
+    if name == "fp32_64m":
+        return wl.fp32_64m(device), "FP32 8192x8192 N(0,0.02) seed 1"
+    if name == "bf16_1m":
+        return wl.bf16_1m(device), "BF16 1024x1024 N(0,0.02) seed 0"
+    if name == "fp32clean_64m":
+        return wl.fp32clean_64m(device), "clean FP32 8192x8192 (BF16-rounded) seed 2"
+    if name == "fp16_16m":
+        return wl.fp16_16m(device), "FP16 4096x4096 N(0,0.05) seed 3"
+    if name == "bf16_delta":
+        return wl.bf16_delta(device)[1], "U16 XOR of two BF16 4096x14336 checkpoints, seed 4"
+    if name == "bf16_llama_gate":
+        specs = wl.llama8b_specs()
+        nm, shape = specs[5]
+        return wl.llama8b_tensor(5, nm, shape, device), "Llama-3.1-8B layer-0 gate_proj BF16 14336x4096"
+    raise ValueError(name)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if k in d:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "entropy_coding_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    from the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            d = json.load(fh)
+        e = d[f"{kernel}:{workload}"]
+        if e.get("source_hash") == kernel_source_hash():
+            return int(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--id={self.index}",
+               "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[0]) for r in self.rows if r and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) > 1 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 3 + i and r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+def run_reference(a):
+    """The CPU oracle on a bounded sample of the workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from entropy_coding_gb300 import workloads as wl
+    oracle.build()
+    t, desc = make_workload(a.workload, "cpu")
+    raw = wl.as_bytes(t).numpy()
+    code = wl.dtype_code(t)
+    W = raw.size // max(1, t.numel())
+    sample = min(raw.size, 16 * a.chunk_bytes)     # 2 MiB per step: a few seconds of CPU work
+    part = raw[:sample]
+    blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold)   # warm-up
+    oracle.decompress(blob)
+    t_enc = t_dec = 0.0
+    size = 0
+    for _ in range(a.steps):
+        t0 = time.perf_counter()
+        blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold)
+        t1 = time.perf_counter()
+        out = oracle.decompress(blob)
+        t2 = time.perf_counter()
+        t_enc += t1 - t0
+        t_dec += t2 - t1
+        size = len(blob)
+    assert out.tobytes() == part.tobytes()
+    n = sample * a.steps
+    value = n / (t_enc + t_dec) / 1e9
+    line = {"metric": "round-trip GB/s (original bytes; encode + decode)", "value": round(value, 4),
+            "unit": "GB/s", "impl": "reference", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": round(1e3 * (t_enc + t_dec) / a.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": a.workload, "desc": desc, "chunk_bytes": a.chunk_bytes,
+                       "threshold": a.threshold},
+            "encode_gbs": round(n / t_enc / 1e9, 4), "decode_gbs": round(n / t_dec / 1e9, 4),
+            "size_pct": round(100.0 * size / sample, 3),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {sample} bytes ({sample // a.chunk_bytes} chunks) of the "
+                                       f"workload per step, single-threaded C oracle"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(t, code, a):
+    """Single-thread oracle on a bounded sample (about ten seconds)."""
+    import oracle
+    from entropy_coding_gb300 import workloads as wl
+    oracle.build()
+    raw = wl.as_bytes(t.cpu()).numpy()
+    W = raw.size // max(1, t.numel())
+    budget, done, t_total, chunks = 8.0, 0, 0.0, 0
+    step = min(raw.size, 8 * a.chunk_bytes)
+    while t_total < budget and done < raw.size:
+        part = raw[done:done + step]
+        t0 = time.perf_counter()
+        blob = oracle.compress(part, code, (part.size // W,), a.chunk_bytes, a.threshold)
+        out = oracle.decompress(blob)
+        t_total += time.perf_counter() - t0
+        assert out.tobytes() == part.tobytes()
+        done += part.size
+        chunks += (part.size + a.chunk_bytes - 1) // a.chunk_bytes
+    return {"value": round(done / t_total / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} bytes ({chunks} chunks) from the start of the workload, compressed and "
+                      f"decompressed once, single-threaded C oracle, {t_total:.1f} s"}
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+        return
+    import torch
+    import torch.distributed as dist
+    import entropy_coding_gb300 as zc
+    from entropy_coding_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    t, desc = make_workload(a.workload, dev)
+    code = wl.dtype_code(t)
+    src = wl.as_bytes(t)
+    N = src.numel()
+    C, thr = a.chunk_bytes, a.threshold
+    cap = zc.blob_size(N, code, C, thr)
+    blob = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ws = torch.empty(zc.workspace_size(N, code, C), dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(N, dtype=torch.uint8, device=dev)
+    shape = tuple(t.shape)
+
+    # first pass outside timing: blob length, header, correctness
+    with torch.cuda.stream(stream):
+        zc.compress_into(src, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+    stream.synchronize()
+    S = int(nb.item())
+    assert int(st.item()) == 0
+    info = zc.blob_info(blob[: 96 + 16 * ((N + C - 1) // C)].cpu())
+    with torch.cuda.stream(stream):
+        zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+    stream.synchronize()
+    assert int(st.item()) == 0 and torch.equal(out, src), "round trip failed"
+
+    def one_step(ev):
+        zc.compress_into(src, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+        ev[1].record(stream)
+        zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+        ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            one_step([None, torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)])
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for ev in evs:
+                ev[0].record(stream)
+                one_step(ev)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    t_enc = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    assert int(st.item()) == 0 and int(nb.item()) == S
+    total = t_enc + t_dec
+    if world > 1:
+        tt = torch.tensor([total, t_enc, t_dec], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total, t_enc, t_dec = tt.tolist()
+        dist.barrier()
+
+    # end to end through the public calls, host (pinned) buffers in and out
+    h_src = torch.empty(N, dtype=torch.uint8, pin_memory=True)
+    h_src.copy_(src.cpu())
+    h_blob = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(N, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty_like(src)
+    h2d = d2h = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(a.e2e_steps):
+        with torch.cuda.stream(stream):
+            d_in.copy_(h_src, non_blocking=True)
+            zc.compress_into(d_in, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+            s_bytes = int(nb.item())
+            h_blob[:s_bytes].copy_(blob[:s_bytes], non_blocking=True)
+            blob[:s_bytes].copy_(h_blob[:s_bytes], non_blocking=True)
+            zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+            h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        h2d += N + s_bytes
+        d2h += s_bytes + 8 + N
+    t_e2e = time.perf_counter() - t0
+    assert torch.equal(h_out, h_src)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    hbm, peak_kind = peaks()
+    enc_gbs = N * a.steps / t_enc / 1e9
+    dec_gbs = N * a.steps / t_dec / 1e9
+    enc_ach = (N + S) * a.steps / t_enc / 1e9
+    dec_ach = (N + S) * a.steps / t_dec / 1e9
+    dominant = "encode_kernel" if t_enc >= t_dec else "decode_kernel"
+    ach = enc_ach if t_enc >= t_dec else dec_ach
+    traffic = profiled_traffic(dominant, a.workload)
+    line = {
+        "metric": "round-trip GB/s (original bytes; encode + decode)",
+        "value": round(world * N * a.steps / total / 1e9, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": a.workload, "desc": desc, "nbytes": N, "chunk_bytes": C, "threshold": thr,
+                   "verify_crc_on_decode": not a.no_verify, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "encode": {"gbs": round(enc_gbs, 2), "roofline_frac": round(enc_ach / hbm, 4),
+                   "ms": round(1e3 * t_enc / a.steps, 4)},
+        "decode": {"gbs": round(dec_gbs, 2), "roofline_frac": round(dec_ach / hbm, 4),
+                   "ms": round(1e3 * t_dec / a.steps, 4)},
+        "size_pct": round(100.0 * S / N, 3),
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": N + S},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(N * a.e2e_steps / t_e2e / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d // a.e2e_steps, "d2h_bytes_per_step": d2h // a.e2e_steps},
+        "gpu_launches": 2 * a.steps,
+    }
+    line["cpu_baseline"] = cpu_baseline(t, code, a)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

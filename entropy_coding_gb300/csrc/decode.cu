@@ -5,24 +5,34 @@
 //   1. reads and bounds-checks the chunk table entry;
 //   2. checks the CRC-32 of the stored bytes (cuZipNN: verify a blob before
 //      decoding it), unless the caller asked not to;
-//   3. copies a RAW chunk, or parses a grouped chunk's directory and, for
-//      every rANS stream, its frequency table into a slot -> symbol lookup
+//   3. copies a RAW chunk, or parses a grouped chunk's directory and, for up
+//      to two rANS streams, its frequency table into a slot -> symbol lookup
 //      table in shared memory;
-//   4. runs the 32 interleaved rANS lanes of all coded streams forward in
-//      step with the raw and constant streams, merges the W stream bytes of
-//      each element back into its word (inverse exponent extraction) and
-//      stores the 32 consecutive words of each step with one coalesced store.
-// Renormalisation words are consumed from the end of each record backwards;
-// they are staged in a 4-block shared-memory ring filled by cp.async.
+//   4. runs the 32 interleaved rANS lanes forward four steps at a time,
+//      staging the decoded symbols of the 128 elements of those steps in
+//      shared memory, then lets each lane gather the bytes of 4 consecutive
+//      elements from every stream (coded, raw or constant), transpose them
+//      into words, undo the exponent extraction and store them with one
+//      vector store.
+// Renormalisation words are consumed from the end of each record backwards
+// and staged in a two-block shared-memory ring filled by cp.async. Chunks
+// with more than two coded streams first decode the extra streams into the
+// tail of their own output range (one byte per element and stream,
+// interleaved); the main pass reads them from there before any store can
+// reach them (the write front advances W bytes per element, the read front
+// q < W bytes per element from (W - q) n onward, and they meet only at the
+// end).
 #include "zc_kernels.cuh"
 
 namespace zc {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024, kRingBytes = 2 * kRingWords;
-constexpr uint32_t kStreamSmem = kLutBytes + kSymBytes + kRingBytes;  // 7 KB per coded stream
+constexpr int kWarps = 8;
+constexpr int kSlots = 2;  // coded streams decoded by the main pass
+constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 512, kRingBytes = 2 * kRingWords,
+                   kStageBytes = 128;
+constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
 constexpr uint32_t kCrcSmem = 8 * 256 * 4;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
@@ -31,25 +41,126 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Fetch 256-word block b of a record's word area into its ring slot.
-__device__ __forceinline__ void fetch_block(uint16_t *ring, const uint8_t *wbase, uint32_t padded_bytes, int b) {
-    const int lane = threadIdx.x & 31;
-    uint32_t byte = uint32_t(b) * 512u + 16u * lane;
-    if (byte < padded_bytes) cp_async16(reinterpret_cast<uint8_t *>(ring) + (b & 3) * 512 + 16 * lane, wbase + byte);
-}
-
-struct RansStream {
+struct Rans {
     uint32_t x;          // this lane's state
-    int32_t ptr;         // words left (warp-uniform)
-    int32_t next_block;  // next 256-word block to fetch, < 0 when done
+    int32_t ptr;         // words left to consume (warp-uniform)
+    int32_t next_block;  // next 256-word block to fetch, < 0 when all fetched
     const uint8_t *wbase;
     uint32_t padded;     // pad16(2 * nwords)
     const uint8_t *lut;
     const uint32_t *sym;
     uint16_t *ring;
+    uint8_t *stage;
 };
+
+// Fetch 256-word block b of a record's word area into its ring slot.
+__device__ __forceinline__ void fetch_block(const Rans &r, int b) {
+    const int lane = threadIdx.x & 31;
+    uint32_t byte = uint32_t(b) * 512u + 16u * lane;
+    if (byte < r.padded) cp_async16(reinterpret_cast<uint8_t *>(r.ring) + (b & 1) * 512 + 16 * lane, r.wbase + byte);
+}
+
+// Parse a rANS record (val bytes) into lookup tables in `slot` and load the
+// lane states and the last two word blocks. Returns false if malformed.
+__device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, Rans &r) {
+    const int lane = threadIdx.x & 31;
+    uint8_t *lut = slot;
+    uint32_t *sym = reinterpret_cast<uint32_t *>(slot + kLutBytes);
+    uint32_t bits = rec[128 + lane];
+    uint32_t present = __popc(bits);
+    uint32_t k = __reduce_add_sync(kFull, present);
+    uint32_t inc = present;
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += t;
+    }
+    uint32_t rank = inc - present;
+    const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k));
+    bool bad = k < 2 || val < words_at || ((val - words_at) & 1u);
+    const uint16_t *freqs = reinterpret_cast<const uint16_t *>(rec + kRecHead);
+    uint32_t f8[8], fsum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        f8[q] = 0;
+        if (!bad && ((bits >> q) & 1u)) {
+            f8[q] = freqs[rank++];
+            bad |= f8[q] == 0 || f8[q] >= kM;
+        }
+        fsum += f8[q];
+    }
+    for (uint32_t b = kRecHead + 2 * k + lane; !bad && b < words_at; b += 32) bad |= rec[b] != 0;
+    inc = fsum;
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += t;
+    }
+    uint32_t cum = inc - fsum;
+    bad |= __shfl_sync(kFull, inc, 31) != kM;
+    r.x = reinterpret_cast<const uint32_t *>(rec)[lane];
+    bad |= r.x < kRansL;
+    if (__any_sync(kFull, bad)) return false;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        uint32_t s = 8 * lane + q;
+        if (f8[q]) {
+            sym[s] = f8[q] | (cum << 12);
+            uint32_t a = cum, e = cum + f8[q];
+            for (; a < e && (a & 3); a++) lut[a] = uint8_t(s);
+            for (; a + 4 <= e; a += 4) *reinterpret_cast<uint32_t *>(lut + a) = s * 0x01010101u;
+            for (; a < e; a++) lut[a] = uint8_t(s);
+        }
+        cum += f8[q];
+    }
+    const uint32_t nwords = (val - words_at) / 2;
+    r.ptr = int32_t(nwords);
+    r.wbase = rec + words_at;
+    r.padded = uint32_t(pad16(2 * nwords));
+    r.lut = lut;
+    r.sym = sym;
+    r.ring = reinterpret_cast<uint16_t *>(slot + kLutBytes + kSymBytes);
+    r.stage = slot + kLutBytes + kSymBytes + kRingBytes;
+    int top = nwords ? int((nwords - 1) >> 8) : -1;
+    if (top >= 0) fetch_block(r, top);
+    if (top >= 1) fetch_block(r, top - 1);
+    r.next_block = top - 2;
+    cp_async_commit();
+    return true;
+}
+
+// One rANS decode step of the warp: returns this lane's symbol.
+__device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt) {
+    uint32_t slot = r.x & (kM - 1);
+    uint32_t s = r.lut[slot];
+    uint32_t e = r.sym[s];
+    uint32_t xn = (e & 0xFFFu) * (r.x >> kProbBits) + slot - (e >> 12);
+    bool need = active && xn < kRansL;
+    uint32_t bal = __ballot_sync(kFull, need);
+    if (need) {
+        int32_t idx = r.ptr - 1 - int32_t(__popc(bal & lt));
+        xn = (xn << 16) | r.ring[uint32_t(idx) & (kRingWords - 1)];
+    }
+    if (active) r.x = xn;
+    r.ptr -= int32_t(__popc(bal));
+    if (r.next_block >= 0 && r.ptr <= 256 * (r.next_block + 2)) {
+        __syncwarp();
+        fetch_block(r, r.next_block);
+        cp_async_commit();
+        r.next_block--;
+        if (r.next_block < 0) cp_async_wait_all();
+        else cp_async_wait1();
+        __syncwarp();
+    }
+    return s;
+}
+
+__device__ __forceinline__ bool rans_final_ok(const Rans &r) {
+    return !__any_sync(kFull, r.x != kRansL || r.ptr != 0);
+}
+
+// Stream kinds in the main pass.
+constexpr uint32_t kKConst = 0, kKRaw = 1, kKMain = 2, kKStaged = 3;
 
 template <int DT>
 __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t (*crc_tab)[256]) {
@@ -95,23 +206,30 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     // directory: W entries of mode << 30 | value, zero-padded to 16 bytes
     uint32_t dir = lane < 4 ? reinterpret_cast<const uint32_t *>(p)[lane] : 0u;
     bool bad = __any_sync(kFull, lane >= W && lane < 4 && dir != 0);
-    uint32_t mode[W], val[W], roff[W];
-    uint32_t pos = 16;
+    uint32_t kind[W], val[W], roff[W], sub[W];
+    uint32_t pos = 16, coded = 0;
 #pragma unroll
     for (int j = 0; j < W; j++) {
         uint32_t e = __shfl_sync(kFull, dir, j);
-        mode[j] = e >> 30;
+        uint32_t mode = e >> 30;
         val[j] = e & 0x3FFFFFFFu;
         roff[j] = pos;
-        if (mode[j] == kModeConst) {
+        sub[j] = 0;
+        if (mode == kModeConst) {
+            kind[j] = kKConst;
             bad |= val[j] > 255;
-        } else if (mode[j] == kModeRaw) {
+        } else if (mode == kModeRaw) {
+            kind[j] = kKRaw;
             bad |= val[j] != n;
             pos += uint32_t(pad16(n));
-        } else if (mode[j] == kModeRans) {
+        } else if (mode == kModeRans) {
+            kind[j] = coded < uint32_t(kSlots) ? kKMain : kKStaged;
+            sub[j] = coded < uint32_t(kSlots) ? coded : coded - kSlots;
+            coded++;
             bad |= val[j] < kRecHead || val[j] > stored;
             pos += uint32_t(pad16(val[j]));
         } else {
+            kind[j] = kKConst;
             bad = true;
         }
         if (pos > stored) bad = true;
@@ -120,129 +238,143 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
         if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
         return;
     }
+    const uint32_t lt = lanemask_lt();
+    const uint32_t T = (n + 31) / 32;
 
-    // tables of the coded streams
-    RansStream rs[W];
-    bool tbad = false;
+    // extra coded streams: decode into the output tail, q bytes per element
+    const uint32_t q = coded > uint32_t(kSlots) ? coded - kSlots : 0;
+    uint8_t *tail = out + (len - q * n);
+    if (q) {
 #pragma unroll
-    for (int j = 0; j < W; j++) {
-        if (mode[j] != kModeRans) continue;
-        const uint8_t *rec = p + roff[j];
-        uint8_t *lut = wsm + j * kStreamSmem;
-        uint32_t *sym = reinterpret_cast<uint32_t *>(lut + kLutBytes);
-        uint16_t *ring = reinterpret_cast<uint16_t *>(lut + kLutBytes + kSymBytes);
-        uint32_t bits = rec[128 + lane];
-        uint32_t present = __popc(bits);
-        uint32_t k = __reduce_add_sync(kFull, present);
-        uint32_t rank = 0;
-        {   // exclusive prefix of present symbols over lanes
-            uint32_t inc = present;
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t t = __shfl_up_sync(kFull, inc, o);
-                if (lane >= o) inc += t;
+        for (int j = 0; j < W; j++) {
+            if (kind[j] != kKStaged) continue;
+            Rans r;
+            if (!rans_setup(p + roff[j], val[j], wsm, r)) bad = true;
+            cp_async_wait_all();
+            __syncwarp();
+            if (bad) break;
+            for (uint32_t t = 0; t < T; t++) {
+                uint32_t i = t * 32 + lane;
+                bool active = i < n;
+                uint32_t s = rans_step(r, active, lt);
+                if (active) tail[uint64_t(i) * q + sub[j]] = uint8_t(s);
             }
-            rank = inc - present;
+            bad |= !rans_final_ok(r);
+            __syncwarp();
         }
-        const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k));
-        bool lbad = k < 2 || val[j] < words_at || ((val[j] - words_at) & 1u);
-        const uint16_t *freqs = reinterpret_cast<const uint16_t *>(rec + kRecHead);
-        uint32_t f8[8], fsum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            f8[q] = 0;
-            if (!lbad && ((bits >> q) & 1u)) {
-                f8[q] = freqs[rank++];
-                lbad |= f8[q] == 0 || f8[q] >= kM;
-            }
-            fsum += f8[q];
-        }
-        for (uint32_t b = kRecHead + 2 * k + lane; !lbad && b < words_at; b += 32) lbad |= rec[b] != 0;
-        uint32_t cum;
-        {
-            uint32_t inc = fsum;
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t t = __shfl_up_sync(kFull, inc, o);
-                if (lane >= o) inc += t;
-            }
-            cum = inc - fsum;
-            lbad |= __shfl_sync(kFull, inc, 31) != kM;
-        }
-        if (__any_sync(kFull, lbad)) {
-            tbad = true;
-            break;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            uint32_t s = 8 * lane + q;
-            if (f8[q]) {
-                sym[s] = f8[q] | (cum << 12);
-                for (uint32_t sl = cum; sl < cum + f8[q]; sl++) lut[sl] = uint8_t(s);
-            }
-            cum += f8[q];
-        }
-        rs[j].x = reinterpret_cast<const uint32_t *>(rec)[lane];
-        const uint32_t nwords = (val[j] - words_at) / 2;
-        rs[j].ptr = int32_t(nwords);
-        rs[j].wbase = rec + words_at;
-        rs[j].padded = uint32_t(pad16(2 * nwords));
-        rs[j].lut = lut;
-        rs[j].sym = sym;
-        rs[j].ring = ring;
-        int top = nwords ? int((nwords - 1) >> 8) : -1;
-        for (int b = top; b >= 0 && b > top - 4; b--) fetch_block(ring, rs[j].wbase, rs[j].padded, b);
-        rs[j].next_block = top - 4;
-        if (__any_sync(kFull, rs[j].x < kRansL)) {
-            tbad = true;
-            break;
+        __syncwarp();
+        if (bad) {
+            if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+            return;
         }
     }
-    cp_async_commit();
+
+    Rans rs[kSlots];  // indexed only with compile-time indices (stays in registers)
+#pragma unroll
+    for (int j = 0; j < W; j++) {
+        if (kind[j] != kKMain) continue;
+        bool ok_j = sub[j] == 0 ? rans_setup(p + roff[j], val[j], wsm, rs[0])
+                                : rans_setup(p + roff[j], val[j], wsm + kSlotSmem, rs[kSlots - 1]);
+        if (!ok_j) bad = true;
+    }
     cp_async_wait_all();
     __syncwarp();
-    if (tbad) {
+    if (bad) {
         if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
         return;
     }
+    const int nmain = int(coded < uint32_t(kSlots) ? coded : kSlots);
 
-    const uint32_t lt = lanemask_lt();
-    const uint32_t T = (n + 31) / 32;
-    for (uint32_t t = 0; t < T; t++) {
+    const uint32_t groups = n / 128;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & (4 * W - 1)) == 0;
+    uint32_t rawnext[W];
+#pragma unroll
+    for (int j = 0; j < W; j++)
+        rawnext[j] = (kind[j] == kKRaw && groups) ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j]) + lane) : 0u;
+    for (uint32_t g = 0; g < groups; g++) {
+        uint32_t col[W];
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            col[j] = rawnext[j];
+            if (kind[j] == kKRaw && g + 1 < groups)
+                rawnext[j] = __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128 * (g + 1)) + lane);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+#pragma unroll
+            for (int m = 0; m < kSlots; m++)
+                if (m < nmain) rs[m].stage[32 * k + lane] = uint8_t(rans_step(rs[m], true, lt));
+        }
+        __syncwarp();
+        const uint32_t e0 = 128 * g + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            if (kind[j] == kKConst) {
+                col[j] = val[j] * 0x01010101u;
+            } else if (kind[j] == kKMain) {
+                const uint8_t *stg = sub[j] == 0 ? rs[0].stage : rs[kSlots - 1].stage;
+                col[j] = *reinterpret_cast<const uint32_t *>(stg + 4 * lane);
+            } else if (kind[j] == kKStaged) {
+                uint32_t v = 0;
+                for (int e = 0; e < 4; e++) v |= uint32_t(__ldcg(tail + uint64_t(e0 + e) * q + sub[j])) << (8 * e);
+                col[j] = v;
+            }
+        }
+        __syncwarp();
+        if constexpr (W == 4) {
+            uint32_t lo32 = __byte_perm(col[W - 1], col[W - 2 < 0 ? 0 : W - 2], 0x5140);
+            uint32_t hi32 = __byte_perm(col[W - 1], col[W - 2 < 0 ? 0 : W - 2], 0x7362);
+            uint32_t lo10 = __byte_perm(col[1 % W], col[0], 0x5140);
+            uint32_t hi10 = __byte_perm(col[1 % W], col[0], 0x7362);
+            uint4 v;
+            v.x = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x5410));
+            v.y = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x7632));
+            v.z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
+            v.w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
+            if (vec_ok) {
+                *reinterpret_cast<uint4 *>(out + 4ull * e0) = v;
+            } else {
+                uint32_t *o = reinterpret_cast<uint32_t *>(out) + e0;
+                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+            }
+        } else if constexpr (W == 2) {
+            uint2 v;
+            v.x = Perm<DT>::inv2(__byte_perm(col[1 % W], col[0], 0x5140));
+            v.y = Perm<DT>::inv2(__byte_perm(col[1 % W], col[0], 0x7362));
+            if (vec_ok) {
+                *reinterpret_cast<uint2 *>(out + 2ull * e0) = v;
+            } else {
+                uint16_t *o = reinterpret_cast<uint16_t *>(out) + e0;
+                o[0] = uint16_t(v.x); o[1] = uint16_t(v.x >> 16); o[2] = uint16_t(v.y); o[3] = uint16_t(v.y >> 16);
+            }
+        } else {
+            if (vec_ok) {
+                *reinterpret_cast<uint32_t *>(out + e0) = col[0];
+            } else {
+                for (int e = 0; e < 4; e++) out[e0 + e] = uint8_t(col[0] >> (8 * e));
+            }
+        }
+    }
+    // the last < 128 elements, one step at a time
+    for (uint32_t t = groups * 4; t < T; t++) {
         const uint32_t i = t * 32 + lane;
         const bool active = i < n;
+        uint32_t sm[kSlots];
+#pragma unroll
+        for (int m = 0; m < kSlots; m++) sm[m] = (m < nmain) ? rans_step(rs[m], active, lt) : 0u;
         uint32_t word = 0;
 #pragma unroll
         for (int j = 0; j < W; j++) {
-            uint32_t b;
-            if (mode[j] == kModeConst) {
-                b = val[j];
-            } else if (mode[j] == kModeRaw) {
-                b = active ? __ldg(p + roff[j] + i) : 0u;
-            } else {
-                RansStream &r = rs[j];
-                uint32_t slot = r.x & (kM - 1);
-                b = r.lut[slot];
-                uint32_t e = r.sym[b];
-                uint32_t xn = (e & 0xFFFu) * (r.x >> kProbBits) + slot - (e >> 12);
-                bool need = active && xn < kRansL;
-                uint32_t bal = __ballot_sync(kFull, need);
-                if (need) {
-                    int32_t idx = r.ptr - 1 - int32_t(__popc(bal & lt));
-                    xn = (xn << 16) | r.ring[uint32_t(idx) & (kRingWords - 1)];
-                }
-                if (active) r.x = xn;
-                r.ptr -= int32_t(__popc(bal));
-                if (r.next_block >= 0 && r.ptr <= 256 * (r.next_block + 4)) {
-                    __syncwarp();
-                    fetch_block(r.ring, r.wbase, r.padded, r.next_block);
-                    cp_async_commit();
-                    r.next_block--;
-                    if (r.next_block < 0) cp_async_wait_all();
-                    else cp_async_wait2();
-                    __syncwarp();
-                }
+            uint32_t b = 0;
+            if (active) {
+                if (kind[j] == kKConst) b = val[j];
+                else if (kind[j] == kKRaw) b = __ldg(p + roff[j] + i);
+                else if (kind[j] == kKMain) b = sub[j] == 0 ? sm[0] : sm[kSlots - 1];
+                else b = __ldcg(tail + uint64_t(i) * q + sub[j]);
             }
             word = (word << 8) | b;
         }
+        __syncwarp();
         if (active) {
             uint32_t w = Perm<DT>::inv(word);
             if (W == 4) reinterpret_cast<uint32_t *>(out)[i] = w;
@@ -252,14 +384,16 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     }
     bool fin_bad = false;
 #pragma unroll
-    for (int j = 0; j < W; j++)
-        if (mode[j] == kModeRans) fin_bad |= rs[j].x != kRansL || rs[j].ptr != 0;
-    if (__any_sync(kFull, fin_bad) && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+    for (int m = 0; m < kSlots; m++)
+        if (m < nmain) fin_bad |= !rans_final_ok(rs[m]);
+    if (fin_bad && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
 }
 
 template <int DT>
+constexpr int slots_of() { return WordOf<DT>::W < kSlots ? WordOf<DT>::W : kSlots; }
+
+template <int DT>
 __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
-    constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t(*crc_tab)[256] = reinterpret_cast<uint32_t(*)[256]>(smem);
     const int warp = threadIdx.x >> 5;
@@ -267,13 +401,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
     __syncthreads();
     uint32_t c = blockIdx.x * kWarps + warp;
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * W * kStreamSmem, crc_tab);
+    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * slots_of<DT>() * kSlotSmem, crc_tab);
 }
 
 template <int DT>
 int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
-    constexpr int W = WordOf<DT>::W;
-    const size_t smem = kCrcSmem + size_t(kWarps) * W * kStreamSmem;
+    const size_t smem = kCrcSmem + size_t(kWarps) * slots_of<DT>() * kSlotSmem;
     if (cudaFuncSetAttribute(decode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return ZC_ECUDA;
     const int grid = int((a.n_chunks + kWarps - 1) / kWarps);
