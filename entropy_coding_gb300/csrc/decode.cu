@@ -287,17 +287,22 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
 
     const uint32_t groups = n / 128;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & (4 * W - 1)) == 0;
-    uint32_t rawnext[W];
+    // raw columns are loaded two groups ahead
+    uint32_t rawnext[W], rawnext2[W];
 #pragma unroll
-    for (int j = 0; j < W; j++)
-        rawnext[j] = (kind[j] == kKRaw && groups) ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j]) + lane) : 0u;
+    for (int j = 0; j < W; j++) {
+        rawnext[j] = (kind[j] == kKRaw && groups > 0) ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j]) + lane) : 0u;
+        rawnext2[j] = (kind[j] == kKRaw && groups > 1)
+                          ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128) + lane) : 0u;
+    }
     for (uint32_t g = 0; g < groups; g++) {
         uint32_t col[W];
 #pragma unroll
         for (int j = 0; j < W; j++) {
             col[j] = rawnext[j];
-            if (kind[j] == kKRaw && g + 1 < groups)
-                rawnext[j] = __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128 * (g + 1)) + lane);
+            rawnext[j] = rawnext2[j];
+            if (kind[j] == kKRaw && g + 2 < groups)
+                rawnext2[j] = __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128 * (g + 2)) + lane);
         }
 #pragma unroll
         for (int k = 0; k < 4; k++) {

@@ -1,30 +1,75 @@
 // encode.cu — single-pass compression kernel.
 //
-// One warp compresses one chunk at a time (ZipNN note, Method 5: fixed-size
-// chunks coded independently). Warps take chunk indices from a global ticket
-// counter, so every chunk below a warp's chunk is already owned by a running
-// warp. Per chunk a warp:
-//   1. builds one 256-bin histogram per byte stream (order-0 statistics, ZipNN
-//      note Key insight) from the exponent-extracted words;
-//   2. quantises each histogram to a 12-bit table;
-//   3. skips streams that provably cannot shrink below the threshold, and
-//      rANS-codes the others (32 interleaved lanes) into its workspace slot;
-//   4. applies the passthrough rule per stream and per chunk (cuZipNN API,
-//      passthrough_threshold);
-//   5. publishes its padded payload size and finds its blob offset with a
-//      decoupled look-back over the chunks before it (an exclusive prefix
-//      scan of the metadata map, ZipNN note Method 5);
-//   6. writes its payload, its CRC-32 and its chunk table entry.
-// The last warp to finish writes the header and its CRC.
+// One CTA compresses one chunk at a time (ZipNN note, Method 5: fixed-size
+// chunks coded independently); CTAs are persistent and take chunk indices
+// from a global ticket counter, so every chunk below a CTA's chunk is already
+// owned by a running CTA. Per chunk:
+//   1. all warps build one 256-bin histogram per byte stream (order-0
+//      statistics, ZipNN note Key insight) of the exponent-extracted words;
+//   2. warp j takes stream j: a constant stream needs no record; otherwise it
+//      quantises the histogram to a 12-bit table, skips the stream if it
+//      provably cannot shrink below the threshold, and else rANS-codes it
+//      (32 interleaved lanes) into the CTA's workspace slot;
+//   3. warp 0 applies the passthrough rule per stream and per chunk (cuZipNN
+//      API, passthrough_threshold), publishes the chunk's padded size and
+//      finds its blob offset with a decoupled look-back over the chunks
+//      before it (an exclusive prefix scan of the metadata map, ZipNN note
+//      Method 5);
+//   4. all warps write the payload: the directory, the raw streams (one pass
+//      over the input for all of them), the coded records; then compute its
+//      CRC-32 together and write the chunk table entry.
+// The last CTA to finish writes the header and its CRC.
 #include "zc_kernels.cuh"
 
 namespace zc {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kCtasPerSM = 3;
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Exact division by a table frequency f in [1, 4095] for every dividend the
+// encoder can see (x < 2^20 f, since larger states are renormalised first):
+// floor(x / f) = (x * m + a) >> k with a 32-bit m and a in {0, m}. This is
+// the round-up reciprocal (a = 0, m = ceil(2^k / f)) or the round-down one
+// with increment (a = m, m = floor(2^k / f)) of Granlund & Montgomery (1994)
+// and Robison (2005); for each f the first k >= 32 whose error term e
+// satisfies e (2^20 f - 1) < 2^k (round-up) or e 2^20 f <= 2^k (round-down)
+// is taken. Built at compile time.
+struct Recip {
+    uint32_t m[4096];
+    uint32_t ka[4096];  // k | round-down flag << 8
+};
+
+constexpr Recip make_recip() {
+    Recip r{};
+    using u128 = unsigned __int128;
+    const u128 X = u128(1) << 20;
+    for (uint32_t f = 1; f < 4096; f++) {
+        for (uint32_t k = 32; k < 64; k++) {
+            const u128 p = u128(1) << k;
+            const u128 mu = (p + f - 1) / f;
+            if (mu < (u128(1) << 32) && (mu * f - p) * (X * f - 1) < p) {
+                r.m[f] = uint32_t(mu);
+                r.ka[f] = k;
+                break;
+            }
+            u128 md = p / f;
+            if (md > 0xFFFFFFFFu) md = 0xFFFFFFFFu;
+            if ((p - md * f) * X * f <= p) {
+                r.m[f] = uint32_t(md);
+                r.ka[f] = k | 0x100u;
+                break;
+            }
+        }
+    }
+    return r;
+}
+
+__device__ constexpr Recip kRecip = make_recip();
 
 __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -63,7 +108,6 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
     for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
     return v;
 }
-// exclusive prefix sum over lanes
 __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
     const int lane = threadIdx.x & 31;
     uint32_t inc = v;
@@ -74,15 +118,15 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
     return inc - v;
 }
 
-// Histogram of the W byte streams of one chunk into h[W][256].
+// Histogram of the W byte streams of one chunk into h[W][256], by the CTA.
 template <int DT>
 __device__ void chunk_histograms(const uint8_t *src, uint32_t len, uint32_t (*h)[256]) {
     constexpr int W = WordOf<DT>::W;
-    const int lane = threadIdx.x & 31;
-    for (int i = lane; i < W * 256; i += 32) h[i >> 8][i & 255] = 0;
-    __syncwarp();
-    uint32_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    for (uint32_t v = lane; v < nvec; v += 32) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < W * 256; i += kThreads) h[i >> 8][i & 255] = 0;
+    __syncthreads();
+    const uint32_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
+    for (uint32_t v = tid; v < nvec; v += kThreads) {
         uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + v);
         uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -96,12 +140,12 @@ __device__ void chunk_histograms(const uint8_t *src, uint32_t len, uint32_t (*h)
             }
         }
     }
-    for (uint32_t i = nvec * 16 / W + lane; i < len / W; i += 32) {
+    for (uint32_t i = nvec * 16 / W + tid; i < len / W; i += kThreads) {
         uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
 #pragma unroll
         for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
     }
-    __syncwarp();
+    __syncthreads();
 }
 
 // 12-bit table from counts held as 8 bins per lane (symbol 8*lane + k).
@@ -121,10 +165,7 @@ __device__ void normalize_warp(const uint32_t cnt[8], uint32_t n, uint32_t f[8])
     if (sum < kM) {
         uint32_t key = 0;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            uint32_t s = 8 * lane + k;
-            key = max(key, (cnt[k] << 8) | (255u - s));
-        }
+        for (int k = 0; k < 8; k++) key = max(key, (cnt[k] << 8) | (255u - (8 * lane + k)));
         key = warp_max_u32(key);
         uint32_t sb = 255u - (key & 0xFFu);
         if ((sb >> 3) == uint32_t(lane)) {
@@ -136,18 +177,14 @@ __device__ void normalize_warp(const uint32_t cnt[8], uint32_t n, uint32_t f[8])
     while (sum > kM) {
         uint32_t key = 0;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            uint32_t s = 8 * lane + k;
-            if (f[k] > 1) key = max(key, (f[k] << 8) | (255u - s));
-        }
+        for (int k = 0; k < 8; k++)
+            if (f[k] > 1) key = max(key, (f[k] << 8) | (255u - (8 * lane + k)));
         key = warp_max_u32(key);
         uint32_t f1 = key >> 8, s1 = 255u - (key & 0xFFu);
         uint32_t key2 = 0;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            uint32_t s = 8 * lane + k;
-            if (f[k] > 1 && s != s1) key2 = max(key2, f[k]);
-        }
+        for (int k = 0; k < 8; k++)
+            if (f[k] > 1 && 8 * lane + k != s1) key2 = max(key2, f[k]);
         uint32_t m2 = max(warp_max_u32(key2), 1u);
         uint32_t dec = (f1 > m2) ? min(sum - kM, f1 - m2) : 1u;
         if ((s1 >> 3) == uint32_t(lane)) {
@@ -160,9 +197,11 @@ __device__ void normalize_warp(const uint32_t cnt[8], uint32_t n, uint32_t f[8])
 }
 
 // Exclusive prefix of this chunk's padded size over the chunks before it
-// (decoupled look-back). Every wait is bounded; a timeout sets ZC_ETIMEOUT.
-__device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, int32_t *d_status) {
+// (decoupled look-back, one warp). Every wait is bounded; a timeout sets
+// ZC_ETIMEOUT and the chunk is not placed.
+__device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, int32_t *d_status, bool *timed) {
     const int lane = threadIdx.x & 31;
+    *timed = false;
     if (c == 0) {
         if (lane == 0) st_release(&st[0], kFlagPre | agg);
         return 0;
@@ -178,13 +217,17 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
             uint32_t spins = 0;
             v = ld_acquire(&st[idx]);
             while ((v >> 62) == 0) {
-                if (++spins > kSpinLimit) { timed_out = true; break; }
+                if (++spins > kSpinLimit) {
+                    timed_out = true;
+                    break;
+                }
                 __nanosleep(64);
                 v = ld_acquire(&st[idx]);
             }
         }
         if (__any_sync(kFull, timed_out)) {
             if (lane == 0) status_or(d_status, ZC_ETIMEOUT);
+            *timed = true;
             return excl;
         }
         uint32_t pre = __ballot_sync(kFull, (v >> 62) == 2);
@@ -197,13 +240,8 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
     return excl;
 }
 
-struct ChunkPlan {
-    uint32_t mode[4];
-    uint32_t val[4];   // RAW: n, RANS: record bytes, CONST: symbol
-};
-
-// Code stream j of the chunk into rec (the workspace record area). Returns
-// the record's unpadded size. f/cum are the lane's 8 table entries.
+// Code stream j of the chunk into rec (the workspace record area), one warp.
+// Returns the record's unpadded size. f holds the lane's 8 table entries.
 template <int DT>
 __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, const uint32_t f[8],
                                        uint2 *etab, uint8_t *rec) {
@@ -218,26 +256,21 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, co
     }
     uint32_t rank = warp_excl_scan(present);
     uint32_t cum = warp_excl_scan(fsum);
-    uint32_t k_total = __shfl_sync(kFull, rank + present, 31);
+    const uint32_t k_total = __shfl_sync(kFull, rank + present, 31);
     uint32_t bits = 0;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
-        uint32_t s = 8 * lane + k;
-        uint32_t fs = f[k];
+        const uint32_t s = 8 * lane + k, fs = f[k];
         if (fs) {
             bits |= 1u << k;
             reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
-            uint32_t l = 32 - __clz(fs - 1);  // ceil(log2 fs); 0 for fs = 1
-            // Granlund & Montgomery (1994), division by invariant integers:
-            // m = floor(2^32 (2^l - d) / d) + 1 gives floor(x/d) =
-            // (mulhi(m, x) + x) >> l for every 32-bit x.
-            uint32_t m = uint32_t((((1ull << l) - fs) << 32) / fs + 1);
-            etab[s] = make_uint2(m, fs | (cum << 12) | (l << 24));
+            const uint32_t ka = kRecip.ka[fs];
+            etab[s] = make_uint2(kRecip.m[fs], fs | (cum << 12) | ((ka & 0xFFu) - 32) << 24 | (ka >> 8) << 28);
         }
         cum += fs;
     }
     rec[128 + lane] = uint8_t(bits);
-    uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
+    const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
     for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
     __syncwarp();
 
@@ -266,207 +299,262 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, co
         for (int k = 0; k < B; k++) {
             int t = t0 - k;
             if (t < 0) break;
-            bool active = uint32_t(t) * 32 + lane < n;
-            uint32_t s = stream_byte<W>(Perm<DT>::fwd(buf[k]), j);
-            uint2 e = etab[s];
-            uint32_t fs = e.y & 0xFFFu, cs = (e.y >> 12) & 0xFFFu, l = e.y >> 24;
-            bool emit = active && x >= (fs << 20);
-            uint32_t bal = __ballot_sync(kFull, emit);
+            const bool active = uint32_t(t) * 32 + lane < n;
+            const uint32_t s = stream_byte<W>(Perm<DT>::fwd(buf[k]), j);
+            const uint2 e = etab[s];
+            const uint32_t fs = e.y & 0xFFFu, cs = (e.y >> 12) & 0xFFFu, kk = (e.y >> 24) & 0xFu;
+            const bool emit = active && x >= (fs << 20);
+            const uint32_t bal = __ballot_sync(kFull, emit);
             if (emit) {
                 wout[wc + __popc(bal & gt)] = uint16_t(x & 0xFFFFu);
                 x >>= 16;
             }
             wc += __popc(bal);
             if (active) {
-                uint32_t q = uint32_t((uint64_t(__umulhi(x, e.x)) + x) >> l);
-                x = (q << kProbBits) + (x - q * fs) + cs;
+                const uint64_t prod = uint64_t(x) * e.x + ((e.y >> 28) ? e.x : 0u);
+                const uint32_t q = uint32_t(prod >> 32) >> kk;
+                x = x + q * (kM - fs) + cs;
             }
         }
 #pragma unroll
         for (int k = 0; k < B; k++) buf[k] = nxt[k];
     }
     reinterpret_cast<uint32_t *>(rec)[lane] = x;
-    uint32_t rec_bytes = words_at + 2 * wc;
+    const uint32_t rec_bytes = words_at + 2 * wc;
     for (uint32_t b = rec_bytes + lane; b < pad16(rec_bytes); b += 32) rec[b] = 0;
     __syncwarp();
     return rec_bytes;
 }
 
-// Write raw stream j (its n bytes, zero-padded to 16) at dst (16-aligned).
+struct Plan {
+    uint32_t mode[4];
+    uint32_t val[4];   // RAW: n, RANS: record bytes, CONST: symbol
+    uint32_t roff[4];  // record offset within the payload
+    uint64_t off;      // payload offset in the blob
+    uint64_t stored;
+    uint32_t raw_chunk;
+    uint32_t write;    // 0 when the chunk is not placed (capacity or timeout)
+    uint32_t c;
+    uint32_t crc_reg[kWarps];
+};
+
+// Per-stream decision, by warp j for stream j.
 template <int DT>
-__device__ void write_raw_stream(const uint8_t *src, uint32_t n, int j, uint8_t *dst) {
-    constexpr int W = WordOf<DT>::W;
+__device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n, int j, const uint32_t (*h)[256],
+                            uint2 *etab, uint8_t *rec, Plan &pl) {
     const int lane = threadIdx.x & 31;
-    uint32_t groups = (n + 15) / 16;
-    for (uint32_t g = lane; g < groups; g += 32) {
-        uint32_t b[16];
+    uint32_t cnt[8];
 #pragma unroll
-        for (int k = 0; k < 16; k++) {
-            uint32_t i = g * 16 + k;
-            b[k] = i < n ? stream_byte<W>(Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W)), j) : 0u;
+    for (int k = 0; k < 8; k++) cnt[k] = h[j][8 * lane + k];
+    uint32_t pres = 0, only = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        if (cnt[k]) {
+            pres++;
+            only = 8 * lane + k;
         }
-        uint4 v;
-        v.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-        v.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-        v.z = b[8] | (b[9] << 8) | (b[10] << 16) | (b[11] << 24);
-        v.w = b[12] | (b[13] << 8) | (b[14] << 16) | (b[15] << 24);
-        reinterpret_cast<uint4 *>(dst)[g] = v;
+    const uint32_t k_total = warp_sum_u32(pres);
+    uint32_t mode, val;
+    if (k_total == 1) {
+        const uint32_t who = __ballot_sync(kFull, pres != 0);
+        mode = kModeConst;
+        val = __shfl_sync(kFull, only, __ffs(who) - 1);
+    } else {
+        uint32_t f[8];
+        normalize_warp(cnt, n, f);
+        // Lower bound on the coded size from the table's information content:
+        // every coded symbol adds at least log2(4096/f_s) + log2(15/16) bits
+        // to its lane's state, every word removes at most 16.1 bits, and 32
+        // states of at most 32 bits remain. A stream whose bound already
+        // reaches threshold x n cannot be kept coded, so it is not coded.
+        float info = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (cnt[k]) info += float(cnt[k]) * (12.0f - __log2f(float(f[k])));
+        info = warp_sum_f32(info);
+        const float words_lb = (info * (1.0f - 1.0f / 1024) - 0.0932f * float(n) - 512.0f - 64.0f) / 16.1f;
+        const uint64_t rec_lb = kRecHead + pad16(2 * k_total) + 2ull * uint64_t(words_lb > 0.f ? words_lb : 0.f);
+        mode = kModeRaw;
+        val = n;
+        if (double(rec_lb) < a.threshold * double(n)) {
+            const uint32_t rb = rans_encode_stream<DT>(src, n, j, f, etab, rec);
+            if (double(rb) < a.threshold * double(n)) {
+                mode = kModeRans;
+                val = rb;
+            }
+        }
+    }
+    if (lane == 0) {
+        pl.mode[j] = mode;
+        pl.val[j] = val;
     }
 }
 
-__device__ void copy_bytes(const uint8_t *src, uint64_t len, uint8_t *dst /*16-aligned*/) {
-    const int lane = threadIdx.x & 31;
-    uint64_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    for (uint64_t v = lane; v < nvec; v += 32)
-        reinterpret_cast<uint4 *>(dst)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-    for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? src[i] : 0;
+// All raw streams of a grouped chunk in one pass over the input: each thread
+// takes 16 consecutive elements and writes 16 bytes to every raw stream.
+template <int DT>
+__device__ void write_raw_streams(const uint8_t *src, uint32_t n, const Plan &pl, uint8_t *out) {
+    constexpr int W = WordOf<DT>::W;
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < W; j++) any |= pl.mode[j] == kModeRaw;
+    if (!any) return;
+    const uint32_t groups = (n + 15) / 16;
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    for (uint32_t g = threadIdx.x; g < groups; g += kThreads) {
+        uint32_t wd[16];
+        if (vec && 16 * (g + 1) <= n) {
+#pragma unroll
+            for (int v = 0; v < W; v++) {
+                uint4 q = __ldcs(reinterpret_cast<const uint4 *>(src + uint64_t(g) * 16 * W) + v);
+                uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+#pragma unroll
+                    for (int e = 0; e < 4 / W; e++)
+                        wd[(v * 4 + k) * (4 / W) + e] =
+                            (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; k++) {
+                uint32_t i = g * 16 + k;
+                wd[k] = i < n ? load_word<W>(src + uint64_t(i) * W) : 0u;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; k++) wd[k] = Perm<DT>::fwd(wd[k]);
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            if (pl.mode[j] != kModeRaw) continue;
+            uint32_t b[16];
+#pragma unroll
+            for (int k = 0; k < 16; k++) b[k] = (g * 16 + k < n) ? stream_byte<W>(wd[k], j) : 0u;
+            uint4 v;
+            v.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+            v.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+            v.z = b[8] | (b[9] << 8) | (b[10] << 16) | (b[11] << 24);
+            v.w = b[12] | (b[13] << 8) | (b[14] << 16) | (b[15] << 24);
+            reinterpret_cast<uint4 *>(out + pl.roff[j])[g] = v;
+        }
+    }
+}
+
+// Copy len bytes (zero-padded to 16) by the CTA; dst is 16-aligned.
+__device__ void block_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
+    const uint64_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
+    for (uint64_t v = threadIdx.x; v < nvec; v += kThreads)
+        reinterpret_cast<uint4 *>(dst)[v] = __ldcs(reinterpret_cast<const uint4 *>(src) + v);
+    for (uint64_t i = nvec * 16 + threadIdx.x; i < pad16(len); i += kThreads) dst[i] = i < len ? src[i] : 0;
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kWarps * 32) encode_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     __shared__ uint32_t crc_tab[8][256];
-    __shared__ uint32_t hist[kWarps][W][256];
-    __shared__ uint2 etab[kWarps][256];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ uint32_t hist[W][256];
+    __shared__ uint2 etab[W][256];
+    __shared__ Plan pl;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     load_crc_smem(crc_tab);
-    __syncthreads();
 
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
-    uint8_t *slot = a.ws_slots + (uint64_t(blockIdx.x) * kWarps + warp) * a.slot_bytes;
+    uint8_t *slot = a.ws_slots + uint64_t(blockIdx.x) * a.slot_bytes;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
+    const uint64_t rec_stride = pad16(kRecHead + kMaxTable + 2ull * (a.chunk_bytes / W));
 
     for (;;) {
-        uint32_t c = 0;
-        if (lane == 0) c = atomicAdd(&ctrl[0], 1u);
-        c = __shfl_sync(kFull, c, 0);
+        if (tid == 0) pl.c = atomicAdd(&ctrl[0], 1u);
+        __syncthreads();
+        const uint32_t c = pl.c;
         if (c >= a.n_chunks) break;
-
         const uint8_t *src = a.src + uint64_t(c) * a.chunk_bytes;
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
 
-        chunk_histograms<DT>(src, len, hist[warp]);
+        chunk_histograms<DT>(src, len, hist);
 
-        ChunkPlan plan;
-        uint64_t grouped = 16;  // pad16(4W) for W <= 4
-        const uint64_t rec_stride = pad16(kRecHead + kMaxTable + 2ull * (a.chunk_bytes / W));
+        if (warp < W) plan_stream<DT>(a, src, n, warp, hist, etab[warp], slot + uint64_t(warp) * rec_stride, pl);
+        __syncthreads();
+
+        if (warp == 0) {
+            uint64_t grouped = 16;  // pad16(4W) for W <= 4
+            uint32_t roff[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int j = 0; j < W; j++) {
-            uint32_t cnt[8];
-#pragma unroll
-            for (int k = 0; k < 8; k++) cnt[k] = hist[warp][j][8 * lane + k];
-            uint32_t pres = 0, only = 0;
-#pragma unroll
-            for (int k = 0; k < 8; k++)
-                if (cnt[k]) { pres++; only = 8 * lane + k; }
-            uint32_t k_total = warp_sum_u32(pres);
-            if (k_total == 1) {
-                uint32_t who = __ballot_sync(kFull, pres != 0);
-                plan.mode[j] = kModeConst;
-                plan.val[j] = __shfl_sync(kFull, only, __ffs(who) - 1);
-                continue;
+            for (int j = 0; j < W; j++) {
+                roff[j] = uint32_t(grouped);
+                if (pl.mode[j] != kModeConst) grouped += pad16(pl.val[j]);
             }
-            uint32_t f[8];
-            normalize_warp(cnt, n, f);
-            // Lower bound on the coded size from the table's information
-            // content: every coded symbol adds at least log2(4096/f_s) +
-            // log2(15/16) bits to its lane's state, every word removes at most
-            // 16.1 bits, and 32 states of at most 32 bits remain.
-            float info = 0.f;
+            const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
+            const uint64_t stored = raw_chunk ? len : grouped;
+            bool timed;
+            const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status, &timed);
+            const bool fits = off + pad16(stored) <= a.cap;
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < 8; k++)
-                if (cnt[k]) info += float(cnt[k]) * (12.0f - __log2f(float(f[k])));
-            info = warp_sum_f32(info);
-            float words_lb = (info * (1.0f - 1.0f / 1024) - 0.0932f * float(n) - 512.0f - 64.0f) / 16.1f;
-            uint64_t rec_lb = kRecHead + pad16(2 * k_total) + 2ull * uint64_t(words_lb > 0.f ? words_lb : 0.f);
-            if (double(rec_lb) >= a.threshold * double(n)) {
-                plan.mode[j] = kModeRaw;
-                plan.val[j] = n;
-                grouped += pad16(n);
-                continue;
-            }
-            uint8_t *rec = slot + uint64_t(j) * rec_stride;
-            uint32_t rb = rans_encode_stream<DT>(src, n, j, f, etab[warp], rec);
-            if (double(rb) < a.threshold * double(n)) {
-                plan.mode[j] = kModeRans;
-                plan.val[j] = rb;
-                grouped += pad16(rb);
-            } else {
-                plan.mode[j] = kModeRaw;
-                plan.val[j] = n;
-                grouped += pad16(n);
+                for (int j = 0; j < W; j++) pl.roff[j] = roff[j];
+                pl.off = off;
+                pl.stored = stored;
+                pl.raw_chunk = raw_chunk;
+                pl.write = fits && !timed;
+                if (!fits) status_or(a.d_status, ZC_ECAPACITY);
             }
         }
-        const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
-        const uint64_t stored = raw_chunk ? len : grouped;
+        __syncthreads();
 
-        const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status);
-        const bool fits = off + pad16(stored) <= a.cap;
-        if (!fits && lane == 0) status_or(a.d_status, ZC_ECAPACITY);
-
-        uint32_t crc = 0;
-        if (fits) {
-            uint8_t *out = a.blob + off;
-            if (raw_chunk) {
-                copy_bytes(src, len, out);
+        if (pl.write) {
+            uint8_t *out = a.blob + pl.off;
+            if (pl.raw_chunk) {
+                block_copy(src, len, out);
             } else {
-                if (lane < 4) {
+                if (tid < 4) {
                     uint32_t e = 0;
 #pragma unroll
                     for (int j = 0; j < W; j++)
-                        if (lane == j) e = (plan.mode[j] << 30) | plan.val[j];
-                    reinterpret_cast<uint32_t *>(out)[lane] = e;
+                        if (tid == j) e = (pl.mode[j] << 30) | pl.val[j];
+                    reinterpret_cast<uint32_t *>(out)[tid] = e;
                 }
-                uint64_t pos = 16;
+                write_raw_streams<DT>(src, n, pl, out);
 #pragma unroll
-                for (int j = 0; j < W; j++) {
-                    if (plan.mode[j] == kModeRaw) {
-                        write_raw_stream<DT>(src, n, j, out + pos);
-                        pos += pad16(n);
-                    } else if (plan.mode[j] == kModeRans) {
-                        copy_bytes(slot + uint64_t(j) * rec_stride, pad16(plan.val[j]), out + pos);
-                        pos += pad16(plan.val[j]);
-                    }
-                }
+                for (int j = 0; j < W; j++)
+                    if (pl.mode[j] == kModeRans)
+                        block_copy(slot + uint64_t(j) * rec_stride, pad16(pl.val[j]), out + pl.roff[j]);
             }
-            __syncwarp();
-            __threadfence_block();
-            crc = warp_crc_raw<true>(out, stored, 0xFFFFFFFFu, crc_tab) ^ 0xFFFFFFFFu;
-            if (lane == 0) {
+            __syncthreads();
+            const uint32_t crc = block_crc_raw<kWarps>(out, pl.stored, 0xFFFFFFFFu, crc_tab, pl.crc_reg) ^ 0xFFFFFFFFu;
+            if (tid == 0) {
                 uint4 ent;
-                ent.x = uint32_t(off);
-                ent.y = uint32_t(off >> 32);
-                ent.z = uint32_t(stored) | (raw_chunk ? 0x80000000u : 0u);
+                ent.x = uint32_t(pl.off);
+                ent.y = uint32_t(pl.off >> 32);
+                ent.z = uint32_t(pl.stored) | (pl.raw_chunk ? 0x80000000u : 0u);
                 ent.w = crc;
                 reinterpret_cast<uint4 *>(a.blob + ZC_HEADER_BYTES)[c] = ent;
                 // header CRC = shift(crc(header), 16 n) ^ XOR_c shift(crc(entry_c), 16 (n-1-c))
                 uint32_t ec = 0xFFFFFFFFu;
-                uint32_t words[4] = {ent.x, ent.y, ent.z, ent.w};
-                for (int q = 0; q < 4; q += 2) ec = crc_step8(ec, words[q], words[q + 1], crc_tab);
+                ec = crc_step8(ec, ent.x, ent.y, crc_tab);
+                ec = crc_step8(ec, ent.z, ent.w, crc_tab);
                 ec ^= 0xFFFFFFFFu;
-                uint32_t contrib = gf2_mulmod(ec, gf2_xpow8(16ull * (a.n_chunks - 1 - c)));
-                atomicXor(&ctrl[2], contrib);
+                atomicXor(&ctrl[2], gf2_mulmod(ec, gf2_xpow8(16ull * (a.n_chunks - 1 - c))));
             }
         }
-        if (lane == 0) {
+        if (tid == 0) {
             __threadfence();
-            uint32_t done = atomicAdd(&ctrl[1], 1u);
+            const uint32_t done = atomicAdd(&ctrl[1], 1u);
             if (done == a.n_chunks - 1) {
                 __threadfence();
-                uint32_t acc = atomicXor(&ctrl[2], 0u);
-                unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
-                uint64_t total = table_end + (last & kValMask);
+                const uint32_t acc = atomicXor(&ctrl[2], 0u);
+                const unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
+                const uint64_t total = table_end + (last & kValMask);
                 uint32_t hc = 0xFFFFFFFFu;
                 for (int q = 0; q < 24; q += 2) hc = crc_step8(hc, a.header[q], a.header[q + 1], crc_tab);
                 hc ^= 0xFFFFFFFFu;
-                uint32_t hcrc = gf2_mulmod(hc, gf2_xpow8(16ull * a.n_chunks)) ^ acc;
+                const uint32_t hcrc = gf2_mulmod(hc, gf2_xpow8(16ull * a.n_chunks)) ^ acc;
                 uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
                 for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : a.header[q];
                 *a.d_blob_bytes = total;
             }
         }
-        __syncwarp();
+        __syncthreads();
     }
 }
 
@@ -484,17 +572,17 @@ int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s) {
         return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
     }
     switch (dtype) {
-    case ZC_U8: encode_kernel<ZC_U8><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case ZC_U16: encode_kernel<ZC_U16><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case ZC_U32: encode_kernel<ZC_U32><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case ZC_BF16: encode_kernel<ZC_BF16><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case ZC_FP16: encode_kernel<ZC_FP16><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case ZC_FP32: encode_kernel<ZC_FP32><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case ZC_U8: encode_kernel<ZC_U8><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_U16: encode_kernel<ZC_U16><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_U32: encode_kernel<ZC_U32><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_BF16: encode_kernel<ZC_BF16><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_FP16: encode_kernel<ZC_FP16><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_FP32: encode_kernel<ZC_FP32><<<grid, kThreads, 0, s>>>(a); break;
     default: return ZC_EINVAL;
     }
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
-int encode_warps_per_cta() { return kWarps; }
+int encode_ctas_per_sm() { return kCtasPerSM; }
 
 } // namespace zc

@@ -10,7 +10,6 @@ namespace {
 
 using namespace zc;
 
-constexpr uint32_t kWorkersPerSM = 8;   // encoder warps resident per SM
 constexpr uint64_t kCtrlBytes = 256;    // ticket, done counter, header CRC accumulator
 constexpr uint64_t kCrcUnit = 32768;    // bytes per warp in zc_crc32
 
@@ -27,7 +26,7 @@ bool valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double thres
 
 uint64_t chunks_of(uint64_t nbytes, uint32_t chunk_bytes) { return (nbytes + chunk_bytes - 1) / chunk_bytes; }
 
-// Staging for one warp: room for a coded record of every stream of a chunk.
+// Staging for one CTA: room for a coded record of every stream of a chunk.
 uint64_t slot_bytes(uint32_t chunk_bytes, int W) {
     return pad256(uint64_t(W) * pad16(kRecHead + kMaxTable + 2ull * (chunk_bytes / W)));
 }
@@ -55,13 +54,11 @@ int sm_count() {
     return sms;
 }
 
+// Persistent compression CTAs: a few per SM (each holds one chunk in flight).
 uint64_t worker_count(uint64_t n_chunks) {
-    const uint64_t per = uint64_t(encode_warps_per_cta());
-    uint64_t want = (n_chunks + per - 1) / per * per;
-    uint64_t most = uint64_t(sm_count()) * kWorkersPerSM;
-    most = most / per * per;
-    if (most < per) most = per;
-    return want < most ? want : most;
+    uint64_t most = uint64_t(sm_count()) * uint64_t(encode_ctas_per_sm());
+    if (most < 1) most = 1;
+    return n_chunks < most ? n_chunks : most;
 }
 
 uint32_t get32(const uint8_t *p) { return uint32_t(p[0]) | uint32_t(p[1]) << 8 | uint32_t(p[2]) << 16 | uint32_t(p[3]) << 24; }
@@ -196,16 +193,15 @@ extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int nd
     if (nc) {
         const uint64_t fixed = kCtrlBytes + pad256(8 * nc);
         const uint64_t slot = slot_bytes(chunk_bytes, W);
-        const uint64_t per = uint64_t(encode_warps_per_cta());
-        if (ws_bytes < fixed + per * slot) return ZC_ECAPACITY;
+        if (ws_bytes < fixed + slot) return ZC_ECAPACITY;
         uint64_t workers = worker_count(nc);
-        uint64_t fit = (ws_bytes - fixed) / slot / per * per;
+        const uint64_t fit = (ws_bytes - fixed) / slot;
         if (workers > fit) workers = fit;
         a.ws_ctrl = static_cast<uint8_t *>(d_ws);
         a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + kCtrlBytes);
         a.ws_slots = a.ws_ctrl + fixed;
         a.slot_bytes = slot;
-        grid = int(workers / per);
+        grid = int(workers);
         if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
     }
     return launch_encode(dtype, a, grid, s);

@@ -155,9 +155,22 @@ __device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t
         int64_t e = s + int64_t(seg);
         uint32_t c = (s <= 0 && e > 0) ? init : 0u;
         if (s < 0) s = 0;
-        for (int64_t off = s; off < e; off += 16) {
+        int64_t off = s;
+        for (; off + 64 <= e; off += 64) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                v[u] = kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p + off) + u)
+                             : __ldg(reinterpret_cast<const uint4 *>(p + off) + u);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                c = crc_step8(c, v[u].x, v[u].y, T);
+                c = crc_step8(c, v[u].z, v[u].w, T);
+            }
+        }
+        for (; off < e; off += 16) {
             uint4 v = kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p + off))
-                            : *reinterpret_cast<const uint4 *>(p + off);
+                            : __ldg(reinterpret_cast<const uint4 *>(p + off));
             c = crc_step8(c, v.x, v.y, T);
             c = crc_step8(c, v.z, v.w, T);
         }
@@ -171,6 +184,65 @@ __device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t
         reg = __shfl_sync(kFull, c, 0);
     }
     for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, kLdcg ? __ldcg(p + i) : p[i], T);
+    return reg;
+}
+
+// Raw CRC register over [p, p + len) computed by a whole CTA of NW warps, the
+// same way as warp_crc_raw but with 32 * NW runs: each warp folds its 32
+// lanes, then warp 0 folds the NW warp registers (through s_reg[NW] in shared
+// memory). Every thread of the CTA must call it; the result is valid in all
+// threads. p must be 16-byte aligned; reads go through L2 only.
+template <int NW>
+__device__ inline uint32_t block_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
+                                         uint32_t *s_reg) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kRuns = 32 * NW;
+    const uint64_t main = len & ~uint64_t(15);
+    uint32_t reg = init;
+    if (main) {
+        const uint64_t seg = ((main / 16 + kRuns - 1) / kRuns) * 16;
+        int64_t s = int64_t(main) - int64_t(kRuns - tid) * int64_t(seg);
+        const int64_t e = s + int64_t(seg);
+        uint32_t c = (s <= 0 && e > 0) ? init : 0u;
+        if (s < 0) s = 0;
+        int64_t off = s;
+        for (; off + 32 <= e; off += 32) {
+            uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(p + off));
+            uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(p + off + 16));
+            c = crc_step8(c, v0.x, v0.y, T);
+            c = crc_step8(c, v0.z, v0.w, T);
+            c = crc_step8(c, v1.x, v1.y, T);
+            c = crc_step8(c, v1.z, v1.w, T);
+        }
+        if (off < e) {
+            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(p + off));
+            c = crc_step8(c, v.x, v.y, T);
+            c = crc_step8(c, v.z, v.w, T);
+        }
+        uint32_t K = (seg / 16 <= 1024) ? kCrc.seg16[seg / 16] : gf2_xpow8(seg);
+#pragma unroll
+        for (int k = 0; k < 5; k++) {
+            uint32_t right = __shfl_down_sync(kFull, c, 1 << k);
+            c = gf2_mulmod(c, K) ^ right;
+            K = gf2_mulmod(K, K);
+        }
+        if (lane == 0) s_reg[warp] = c;
+        __syncthreads();
+        if (warp == 0) {
+            c = lane < NW ? s_reg[lane] : 0u;
+#pragma unroll
+            for (int k = 1; k < NW; k <<= 1) {
+                uint32_t right = __shfl_down_sync(kFull, c, k);
+                c = gf2_mulmod(c, K) ^ right;
+                K = gf2_mulmod(K, K);
+            }
+            if (lane == 0) s_reg[0] = c;
+        }
+        __syncthreads();
+        reg = s_reg[0];
+        __syncthreads();
+    }
+    for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, __ldcg(p + i), T);
     return reg;
 }
 

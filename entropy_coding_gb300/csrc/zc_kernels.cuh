@@ -19,7 +19,7 @@ struct EncodeArgs {
     int32_t *d_status;
     uint8_t *ws_ctrl;               // u32 ticket, u32 done, u32 header-CRC accumulator
     unsigned long long *ws_status;  // per chunk: flag << 62 | padded size or prefix
-    uint8_t *ws_slots;              // per-warp staging for coded records
+    uint8_t *ws_slots;              // per-CTA staging for coded records
     uint64_t slot_bytes;
     uint32_t header[24];            // the 96-byte header, CRC field zero (final CRC if empty)
 };
@@ -46,7 +46,7 @@ struct CrcArgs {
 };
 
 int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s);
-int encode_warps_per_cta();
+int encode_ctas_per_sm();
 int launch_decode(int dtype, const DecodeArgs &a, cudaStream_t s);
 int launch_crc(const CrcArgs &a, cudaStream_t s);
 
