@@ -143,6 +143,28 @@ ZC_API int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, u
  * stream by this call before the kernel runs. */
 ZC_API int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream);
 
+/* Compression without any device allocation: the same work and the same
+ * output as zc_compress, but the workspace comes from a fixed 64 MiB scratch
+ * array that the library keeps in device memory (none of the source pages
+ * has a counterpart to this entry point). It is for callers that cannot
+ * allocate device memory, such as a service whose memory is all owned by
+ * another allocator, or a runtime that forbids allocations after start-up;
+ * the caller still provides the input, the blob, d_blob_bytes and d_status
+ * exactly as for zc_compress.
+ *   Limit: at most 1,048,576 chunks (nbytes <= 2^20 * chunk_bytes);
+ *   larger tensors are rejected with ZC_ECAPACITY before any launch.
+ *   The scratch array occupies 64 MiB on every device where this part of the
+ *   library is loaded, until the process exits.
+ *   All calls share the array: calls that may overlap on the GPU (different
+ *   streams, or unordered host threads) race and must be ordered by the
+ *   caller.
+ *   The first call on a device looks up the array's address on that device;
+ *   make that first call before starting any stream capture. */
+ZC_API int zc_compress_noalloc(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                               uint32_t chunk_bytes, double threshold,
+                               void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                               int32_t *d_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
