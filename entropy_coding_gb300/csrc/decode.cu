@@ -5,18 +5,18 @@
 //   1. reads and bounds-checks the chunk table entry;
 //   2. checks the CRC-32 of the stored bytes (cuZipNN: verify a blob before
 //      decoding it), unless the caller asked not to;
-//   3. copies a RAW chunk, or parses a grouped chunk's directory and, for up
-//      to two rANS streams, its frequency table into a slot -> symbol lookup
+//   3. copies a RAW chunk, or parses a grouped chunk's directory and the
+//      frequency table of its first rANS stream into a slot -> symbol lookup
 //      table in shared memory;
-//   4. runs the 32 interleaved rANS lanes forward four steps at a time,
-//      staging the decoded symbols of the 128 elements of those steps in
-//      shared memory, then lets each lane gather the bytes of 4 consecutive
+//   4. runs the 32 interleaved rANS lanes forward eight steps at a time,
+//      staging the decoded symbols of the 256 elements of those steps in
+//      shared memory, then lets each lane gather the bytes of 8 consecutive
 //      elements from every stream (coded, raw or constant), transpose them
-//      into words, undo the exponent extraction and store them with one
-//      vector store.
+//      into words, undo the exponent extraction and store them with vector
+//      stores.
 // Renormalisation words are consumed from the end of each record backwards
 // and staged in a two-block shared-memory ring filled by cp.async. Chunks
-// with more than two coded streams first decode the extra streams into the
+// with more than one coded stream first decode the other ones into the
 // tail of their own output range (one byte per element and stream,
 // interleaved); the main pass reads them from there before any store can
 // reach them (the write front advances W bytes per element, the read front
@@ -29,9 +29,8 @@ namespace zc {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kSlots = 2;  // coded streams decoded by the main pass
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 512, kRingBytes = 2 * kRingWords,
-                   kStageBytes = 128;
+                   kStageBytes = 256;
 constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
 constexpr uint32_t kCrcSmem = 8 * 256 * 4;
 
@@ -162,6 +161,12 @@ __device__ __forceinline__ bool rans_final_ok(const Rans &r) {
 // Stream kinds in the main pass.
 constexpr uint32_t kKConst = 0, kKRaw = 1, kKMain = 2, kKStaged = 3;
 
+// 8 consecutive elements' bytes of stream j packed in two words (element e
+// of the eight in byte e of the pair), from each kind of stream.
+struct Col8 {
+    uint32_t lo, hi;
+};
+
 template <int DT>
 __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t (*crc_tab)[256]) {
     constexpr int W = WordOf<DT>::W;
@@ -223,8 +228,8 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             bad |= val[j] != n;
             pos += uint32_t(pad16(n));
         } else if (mode == kModeRans) {
-            kind[j] = coded < uint32_t(kSlots) ? kKMain : kKStaged;
-            sub[j] = coded < uint32_t(kSlots) ? coded : coded - kSlots;
+            kind[j] = coded == 0 ? kKMain : kKStaged;
+            sub[j] = coded == 0 ? 0 : coded - 1;
             coded++;
             bad |= val[j] < kRecHead || val[j] > stored;
             pos += uint32_t(pad16(val[j]));
@@ -241,8 +246,9 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     const uint32_t lt = lanemask_lt();
     const uint32_t T = (n + 31) / 32;
 
-    // extra coded streams: decode into the output tail, q bytes per element
-    const uint32_t q = coded > uint32_t(kSlots) ? coded - kSlots : 0;
+    // coded streams after the first: decode into the output tail first, q
+    // bytes per element
+    const uint32_t q = coded > 1 ? coded - 1 : 0;
     uint8_t *tail = out + (len - q * n);
     if (q) {
 #pragma unroll
@@ -269,13 +275,13 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
         }
     }
 
-    Rans rs[kSlots];  // indexed only with compile-time indices (stays in registers)
+    Rans rs;
+    bool have_main = false;
 #pragma unroll
     for (int j = 0; j < W; j++) {
         if (kind[j] != kKMain) continue;
-        bool ok_j = sub[j] == 0 ? rans_setup(p + roff[j], val[j], wsm, rs[0])
-                                : rans_setup(p + roff[j], val[j], wsm + kSlotSmem, rs[kSlots - 1]);
-        if (!ok_j) bad = true;
+        have_main = true;
+        if (!rans_setup(p + roff[j], val[j], wsm, rs)) bad = true;
     }
     cp_async_wait_all();
     __syncwarp();
@@ -283,90 +289,102 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
         if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
         return;
     }
-    const int nmain = int(coded < uint32_t(kSlots) ? coded : kSlots);
 
-    const uint32_t groups = n / 128;
-    const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & (4 * W - 1)) == 0;
-    // raw columns are loaded two groups ahead
-    uint32_t rawnext[W], rawnext2[W];
+    // groups of 8 steps = 256 elements; each lane then owns 8 consecutive
+    // elements 256 g + 8 lane .. + 7
+    const uint32_t groups = n / 256;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    uint2 rn1[W], rn2[W];  // raw columns of the next two groups
 #pragma unroll
     for (int j = 0; j < W; j++) {
-        rawnext[j] = (kind[j] == kKRaw && groups > 0) ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j]) + lane) : 0u;
-        rawnext2[j] = (kind[j] == kKRaw && groups > 1)
-                          ? __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128) + lane) : 0u;
+        const uint2 *src = reinterpret_cast<const uint2 *>(p + roff[j]) + lane;
+        rn1[j] = (kind[j] == kKRaw && groups > 0) ? __ldg(src) : make_uint2(0, 0);
+        rn2[j] = (kind[j] == kKRaw && groups > 1) ? __ldg(src + 32) : make_uint2(0, 0);
     }
     for (uint32_t g = 0; g < groups; g++) {
-        uint32_t col[W];
+        Col8 col[W];
 #pragma unroll
         for (int j = 0; j < W; j++) {
-            col[j] = rawnext[j];
-            rawnext[j] = rawnext2[j];
+            col[j].lo = rn1[j].x;
+            col[j].hi = rn1[j].y;
+            rn1[j] = rn2[j];
             if (kind[j] == kKRaw && g + 2 < groups)
-                rawnext2[j] = __ldg(reinterpret_cast<const uint32_t *>(p + roff[j] + 128 * (g + 2)) + lane);
+                rn2[j] = __ldg(reinterpret_cast<const uint2 *>(p + roff[j] + 256 * (g + 2)) + lane);
         }
+        if (have_main) {
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-#pragma unroll
-            for (int m = 0; m < kSlots; m++)
-                if (m < nmain) rs[m].stage[32 * k + lane] = uint8_t(rans_step(rs[m], true, lt));
+            for (int k = 0; k < 8; k++) rs.stage[32 * k + lane] = uint8_t(rans_step(rs, true, lt));
+            __syncwarp();
         }
-        __syncwarp();
-        const uint32_t e0 = 128 * g + 4 * lane;
+        const uint32_t e0 = 256 * g + 8 * lane;
 #pragma unroll
         for (int j = 0; j < W; j++) {
             if (kind[j] == kKConst) {
-                col[j] = val[j] * 0x01010101u;
+                col[j].lo = col[j].hi = val[j] * 0x01010101u;
             } else if (kind[j] == kKMain) {
-                const uint8_t *stg = sub[j] == 0 ? rs[0].stage : rs[kSlots - 1].stage;
-                col[j] = *reinterpret_cast<const uint32_t *>(stg + 4 * lane);
+                const uint2 v = *reinterpret_cast<const uint2 *>(rs.stage + 8 * lane);
+                col[j].lo = v.x;
+                col[j].hi = v.y;
             } else if (kind[j] == kKStaged) {
-                uint32_t v = 0;
-                for (int e = 0; e < 4; e++) v |= uint32_t(__ldcg(tail + uint64_t(e0 + e) * q + sub[j])) << (8 * e);
-                col[j] = v;
+                uint32_t v[2] = {0, 0};
+                for (int e = 0; e < 8; e++)
+                    v[e >> 2] |= uint32_t(__ldcg(tail + uint64_t(e0 + e) * q + sub[j])) << (8 * (e & 3));
+                col[j].lo = v[0];
+                col[j].hi = v[1];
             }
         }
         __syncwarp();
         if constexpr (W == 4) {
-            uint32_t lo32 = __byte_perm(col[W - 1], col[W - 2 < 0 ? 0 : W - 2], 0x5140);
-            uint32_t hi32 = __byte_perm(col[W - 1], col[W - 2 < 0 ? 0 : W - 2], 0x7362);
-            uint32_t lo10 = __byte_perm(col[1 % W], col[0], 0x5140);
-            uint32_t hi10 = __byte_perm(col[1 % W], col[0], 0x7362);
-            uint4 v;
-            v.x = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x5410));
-            v.y = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x7632));
-            v.z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
-            v.w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
+            uint4 v[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint32_t c0 = h ? col[0].hi : col[0].lo, c1 = h ? col[1].hi : col[1].lo;
+                const uint32_t c2 = h ? col[2].hi : col[2].lo, c3 = h ? col[3].hi : col[3].lo;
+                const uint32_t lo32 = __byte_perm(c3, c2, 0x5140), hi32 = __byte_perm(c3, c2, 0x7362);
+                const uint32_t lo10 = __byte_perm(c1, c0, 0x5140), hi10 = __byte_perm(c1, c0, 0x7362);
+                v[h].x = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x5410));
+                v[h].y = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x7632));
+                v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
+                v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
+            }
             if (vec_ok) {
-                *reinterpret_cast<uint4 *>(out + 4ull * e0) = v;
+                uint4 *o = reinterpret_cast<uint4 *>(out + 4ull * e0);
+                o[0] = v[0];
+                o[1] = v[1];
             } else {
                 uint32_t *o = reinterpret_cast<uint32_t *>(out) + e0;
-                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+                o[0] = v[0].x; o[1] = v[0].y; o[2] = v[0].z; o[3] = v[0].w;
+                o[4] = v[1].x; o[5] = v[1].y; o[6] = v[1].z; o[7] = v[1].w;
             }
         } else if constexpr (W == 2) {
-            uint2 v;
-            v.x = Perm<DT>::inv2(__byte_perm(col[1 % W], col[0], 0x5140));
-            v.y = Perm<DT>::inv2(__byte_perm(col[1 % W], col[0], 0x7362));
+            uint4 v;
+            v.x = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x5140));
+            v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
+            v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
+            v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
             if (vec_ok) {
-                *reinterpret_cast<uint2 *>(out + 2ull * e0) = v;
+                *reinterpret_cast<uint4 *>(out + 2ull * e0) = v;
             } else {
                 uint16_t *o = reinterpret_cast<uint16_t *>(out) + e0;
-                o[0] = uint16_t(v.x); o[1] = uint16_t(v.x >> 16); o[2] = uint16_t(v.y); o[3] = uint16_t(v.y >> 16);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int e = 0; e < 4; e++) {
+                    o[2 * e] = uint16_t(w4[e]);
+                    o[2 * e + 1] = uint16_t(w4[e] >> 16);
+                }
             }
         } else {
-            if (vec_ok) {
-                *reinterpret_cast<uint32_t *>(out + e0) = col[0];
+            if ((reinterpret_cast<uintptr_t>(out) & 7) == 0) {
+                *reinterpret_cast<uint2 *>(out + e0) = make_uint2(col[0].lo, col[0].hi);
             } else {
-                for (int e = 0; e < 4; e++) out[e0 + e] = uint8_t(col[0] >> (8 * e));
+                for (int e = 0; e < 8; e++) out[e0 + e] = uint8_t((e < 4 ? col[0].lo : col[0].hi) >> (8 * (e & 3)));
             }
         }
     }
-    // the last < 128 elements, one step at a time
-    for (uint32_t t = groups * 4; t < T; t++) {
+    // the last < 256 elements, one step at a time
+    for (uint32_t t = groups * 8; t < T; t++) {
         const uint32_t i = t * 32 + lane;
         const bool active = i < n;
-        uint32_t sm[kSlots];
-#pragma unroll
-        for (int m = 0; m < kSlots; m++) sm[m] = (m < nmain) ? rans_step(rs[m], active, lt) : 0u;
+        const uint32_t sm = have_main ? rans_step(rs, active, lt) : 0u;
         uint32_t word = 0;
 #pragma unroll
         for (int j = 0; j < W; j++) {
@@ -374,7 +392,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             if (active) {
                 if (kind[j] == kKConst) b = val[j];
                 else if (kind[j] == kKRaw) b = __ldg(p + roff[j] + i);
-                else if (kind[j] == kKMain) b = sub[j] == 0 ? sm[0] : sm[kSlots - 1];
+                else if (kind[j] == kKMain) b = sm;
                 else b = __ldcg(tail + uint64_t(i) * q + sub[j]);
             }
             word = (word << 8) | b;
@@ -387,18 +405,11 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             else out[i] = uint8_t(w);
         }
     }
-    bool fin_bad = false;
-#pragma unroll
-    for (int m = 0; m < kSlots; m++)
-        if (m < nmain) fin_bad |= !rans_final_ok(rs[m]);
-    if (fin_bad && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+    if (have_main && !rans_final_ok(rs) && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
 }
 
 template <int DT>
-constexpr int slots_of() { return WordOf<DT>::W < kSlots ? WordOf<DT>::W : kSlots; }
-
-template <int DT>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t(*crc_tab)[256] = reinterpret_cast<uint32_t(*)[256]>(smem);
     const int warp = threadIdx.x >> 5;
@@ -406,12 +417,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
     __syncthreads();
     uint32_t c = blockIdx.x * kWarps + warp;
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * slots_of<DT>() * kSlotSmem, crc_tab);
+    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_tab);
 }
 
 template <int DT>
 int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
-    const size_t smem = kCrcSmem + size_t(kWarps) * slots_of<DT>() * kSlotSmem;
+    const size_t smem = kCrcSmem + size_t(kWarps) * kSlotSmem;
     if (cudaFuncSetAttribute(decode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return ZC_ECUDA;
     const int grid = int((a.n_chunks + kWarps - 1) / kWarps);

@@ -126,17 +126,26 @@ __device__ void chunk_histograms(const uint8_t *src, uint32_t len, uint32_t (*h)
     for (int i = tid; i < W * 256; i += kThreads) h[i >> 8][i & 255] = 0;
     __syncthreads();
     const uint32_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    for (uint32_t v = tid; v < nvec; v += kThreads) {
-        uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-        uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    constexpr int U = 4;  // loads in flight per thread
+    for (uint32_t v0 = tid; v0 < nvec; v0 += U * kThreads) {
+        uint4 qv[U];
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
+        for (int u = 0; u < U; u++)
+            qv[u] = (v0 + u * kThreads < nvec) ? __ldg(reinterpret_cast<const uint4 *>(src) + v0 + u * kThreads)
+                                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int e = 0; e < 4 / W; e++) {
-                uint32_t w = (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
-                uint32_t p = Perm<DT>::fwd(w);
+        for (int u = 0; u < U; u++) {
+            if (v0 + u * kThreads >= nvec) break;
+            uint32_t uu[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
 #pragma unroll
-                for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
+            for (int k = 0; k < 4; k++) {
+#pragma unroll
+                for (int e = 0; e < 4 / W; e++) {
+                    uint32_t w = (W == 4) ? uu[k] : (uu[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+                    uint32_t p = Perm<DT>::fwd(w);
+#pragma unroll
+                    for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
+                }
             }
         }
     }
@@ -240,14 +249,15 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
     return excl;
 }
 
-// Code stream j of the chunk into rec (the workspace record area), one warp.
+// Code stream J of the chunk into rec (the workspace record area), one warp.
 // Returns the record's unpadded size. f holds the lane's 8 table entries.
-template <int DT>
-__device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, const uint32_t f[8],
-                                       uint2 *etab, uint8_t *rec) {
+// Per symbol the table keeps {m, a, 2^20 f, (4096 - f) | cum << 13 | (k-32) << 25}
+// so that a step is: renormalise if x >= 2^20 f, q = (x m + a) >> k,
+// x += q (4096 - f) + cum.
+template <int DT, int J>
+__device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uint32_t f[8], uint4 *etab, uint8_t *rec) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
-    // table: bitmap byte per lane, frequencies in symbol order, encoder entries
     uint32_t present = 0, fsum = 0;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
@@ -264,8 +274,8 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, co
         if (fs) {
             bits |= 1u << k;
             reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
-            const uint32_t ka = kRecip.ka[fs];
-            etab[s] = make_uint2(kRecip.m[fs], fs | (cum << 12) | ((ka & 0xFFu) - 32) << 24 | (ka >> 8) << 28);
+            const uint32_t ka = kRecip.ka[fs], m = kRecip.m[fs];
+            etab[s] = make_uint4(m, (ka >> 8) ? m : 0u, fs << 20, (kM - fs) | (cum << 13) | (((ka & 0xFFu) - 32) << 25));
         }
         cum += fs;
     }
@@ -279,42 +289,50 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, int j, co
     uint32_t x = kRansL;
     uint32_t wc = 0;
     const int T = int((n + 31) / 32);
-    constexpr int B = 8;
+
+    auto step = [&](uint32_t word, bool active) {
+        const uint32_t s = stream_byte<W>(Perm<DT>::fwd(word), J);
+        const uint4 e = etab[s];
+        const bool emit = active && x >= e.z;
+        const uint32_t bal = __ballot_sync(kFull, emit);
+        if (emit) {
+            wout[wc + __popc(bal & gt)] = uint16_t(x & 0xFFFFu);
+            x >>= 16;
+        }
+        wc += __popc(bal);
+        const uint32_t q = uint32_t((uint64_t(x) * e.x + e.y) >> 32) >> ((e.w >> 25) & 0xFu);
+        const uint32_t xn = x + q * (e.w & 0x1FFFu) + ((e.w >> 13) & 0xFFFu);
+        if (active) x = xn;
+    };
+
+    // the last step first (the only one that may be partial)
+    {
+        const uint32_t i = uint32_t(T - 1) * 32 + lane;
+        const bool active = i < n;
+        step(active ? load_word<W>(src + uint64_t(i) * W) : 0u, active);
+    }
+    // then the full steps T-2 .. 0, 16 at a time, the next 16 words in flight
+    constexpr int B = 16;
     uint32_t buf[B];
 #pragma unroll
     for (int k = 0; k < B; k++) {
-        int t = T - 1 - k;
-        uint32_t i = uint32_t(t) * 32 + lane;
-        buf[k] = (t >= 0 && i < n) ? load_word<W>(src + uint64_t(i) * W) : 0u;
+        const int t = T - 2 - k;
+        buf[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
     }
-    for (int t0 = T - 1; t0 >= 0; t0 -= B) {
+    for (int t0 = T - 2; t0 >= 0; t0 -= B) {
         uint32_t nxt[B];
 #pragma unroll
         for (int k = 0; k < B; k++) {
-            int t = t0 - B - k;
-            uint32_t i = uint32_t(t) * 32 + lane;
-            nxt[k] = (t >= 0 && i < n) ? load_word<W>(src + uint64_t(i) * W) : 0u;
+            const int t = t0 - B - k;
+            nxt[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
         }
+        if (t0 >= B - 1) {
 #pragma unroll
-        for (int k = 0; k < B; k++) {
-            int t = t0 - k;
-            if (t < 0) break;
-            const bool active = uint32_t(t) * 32 + lane < n;
-            const uint32_t s = stream_byte<W>(Perm<DT>::fwd(buf[k]), j);
-            const uint2 e = etab[s];
-            const uint32_t fs = e.y & 0xFFFu, cs = (e.y >> 12) & 0xFFFu, kk = (e.y >> 24) & 0xFu;
-            const bool emit = active && x >= (fs << 20);
-            const uint32_t bal = __ballot_sync(kFull, emit);
-            if (emit) {
-                wout[wc + __popc(bal & gt)] = uint16_t(x & 0xFFFFu);
-                x >>= 16;
-            }
-            wc += __popc(bal);
-            if (active) {
-                const uint64_t prod = uint64_t(x) * e.x + ((e.y >> 28) ? e.x : 0u);
-                const uint32_t q = uint32_t(prod >> 32) >> kk;
-                x = x + q * (kM - fs) + cs;
-            }
+            for (int k = 0; k < B; k++) step(buf[k], true);
+        } else {
+#pragma unroll
+            for (int k = 0; k < B; k++)
+                if (t0 - k >= 0) step(buf[k], true);
         }
 #pragma unroll
         for (int k = 0; k < B; k++) buf[k] = nxt[k];
@@ -339,9 +357,10 @@ struct Plan {
 };
 
 // Per-stream decision, by warp j for stream j.
-template <int DT>
-__device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n, int j, const uint32_t (*h)[256],
-                            uint2 *etab, uint8_t *rec, Plan &pl) {
+template <int DT, int J>
+__device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n, const uint32_t (*h)[256],
+                            uint4 *etab, uint8_t *rec, Plan &pl) {
+    constexpr int j = J;
     const int lane = threadIdx.x & 31;
     uint32_t cnt[8];
 #pragma unroll
@@ -377,7 +396,7 @@ __device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n,
         mode = kModeRaw;
         val = n;
         if (double(rec_lb) < a.threshold * double(n)) {
-            const uint32_t rb = rans_encode_stream<DT>(src, n, j, f, etab, rec);
+            const uint32_t rb = rans_encode_stream<DT, J>(src, n, f, etab, rec);
             if (double(rb) < a.threshold * double(n)) {
                 mode = kModeRans;
                 val = rb;
@@ -453,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
     constexpr int W = WordOf<DT>::W;
     __shared__ uint32_t crc_tab[8][256];
     __shared__ uint32_t hist[W][256];
-    __shared__ uint2 etab[W][256];
+    __shared__ uint4 etab[W][256];
     __shared__ Plan pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     load_crc_smem(crc_tab);
@@ -474,7 +493,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
 
         chunk_histograms<DT>(src, len, hist);
 
-        if (warp < W) plan_stream<DT>(a, src, n, warp, hist, etab[warp], slot + uint64_t(warp) * rec_stride, pl);
+        if (warp == 0) plan_stream<DT, 0>(a, src, n, hist, etab[0], slot, pl);
+        if constexpr (W > 1) {
+            if (warp == 1) plan_stream<DT, 1>(a, src, n, hist, etab[1], slot + rec_stride, pl);
+        }
+        if constexpr (W > 2) {
+            if (warp == 2) plan_stream<DT, 2>(a, src, n, hist, etab[2], slot + 2 * rec_stride, pl);
+            if (warp == 3) plan_stream<DT, 3>(a, src, n, hist, etab[3], slot + 3 * rec_stride, pl);
+        }
         __syncthreads();
 
         if (warp == 0) {
