@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/zc.h"
+#include "zc.h"  // from include/ (on the -I path)
 
 namespace zc {
 
