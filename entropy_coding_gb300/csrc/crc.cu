@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kWarps * 32) crc_kernel(CrcArgs a) {
         uint64_t b1 = min(b0 + a.unit, p1);
         uint32_t reg = warp_crc_raw_any(a.data + b0, b1 - b0, k == 0 ? 0xFFFFFFFFu : 0u, tab);
         if (lane == 0) {
-            uint32_t term = gf2_mulmod(reg, gf2_xpow8(p1 - b1));
+            uint32_t term = shift_bytes(reg, p1 - b1);
             if (k == 0) term ^= 0xFFFFFFFFu;
             atomicXor(&a.out[piece], term);
         }

@@ -134,12 +134,12 @@ __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt)
     uint32_t s = r.lut[slot];
     uint32_t e = r.sym[s];
     uint32_t xn = (e & 0xFFFu) * (r.x >> kProbBits) + slot - (e >> 12);
-    bool need = active && xn < kRansL;
-    uint32_t bal = __ballot_sync(kFull, need);
-    if (need) {
-        int32_t idx = r.ptr - 1 - int32_t(__popc(bal & lt));
-        xn = (xn << 16) | r.ring[uint32_t(idx) & (kRingWords - 1)];
-    }
+    const bool need = active && xn < kRansL;
+    const uint32_t bal = __ballot_sync(kFull, need);
+    // every lane reads its candidate word (in bounds of the ring), so no branch
+    const int32_t idx = r.ptr - 1 - int32_t(__popc(bal & lt));
+    const uint32_t w = r.ring[uint32_t(idx) & (kRingWords - 1)];
+    xn = need ? ((xn << 16) | w) : xn;
     if (active) r.x = xn;
     r.ptr -= int32_t(__popc(bal));
     if (r.next_block >= 0 && r.ptr <= 256 * (r.next_block + 2)) {

@@ -295,10 +295,12 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uin
         const uint4 e = etab[s];
         const bool emit = active && x >= e.z;
         const uint32_t bal = __ballot_sync(kFull, emit);
-        if (emit) {
-            wout[wc + __popc(bal & gt)] = uint16_t(x & 0xFFFFu);
-            x >>= 16;
-        }
+        // the store reads its own copy of x, so updating x need not wait for it
+        uint32_t wv;
+        asm volatile("mov.b32 %0, %1;" : "=r"(wv) : "r"(x));
+        const uint32_t pos = wc + __popc(bal & gt);
+        if (emit) wout[pos] = uint16_t(wv);
+        x = emit ? x >> 16 : x;
         wc += __popc(bal);
         const uint32_t q = uint32_t((uint64_t(x) * e.x + e.y) >> 32) >> ((e.w >> 25) & 0xFu);
         const uint32_t xn = x + q * (e.w & 0x1FFFu) + ((e.w >> 13) & 0xFFFu);
@@ -560,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 ec = crc_step8(ec, ent.x, ent.y, crc_tab);
                 ec = crc_step8(ec, ent.z, ent.w, crc_tab);
                 ec ^= 0xFFFFFFFFu;
-                atomicXor(&ctrl[2], gf2_mulmod(ec, gf2_xpow8(16ull * (a.n_chunks - 1 - c))));
+                atomicXor(&ctrl[2], shift_bytes(ec, 16ull * (a.n_chunks - 1 - c)));
             }
         }
         if (tid == 0) {
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 uint32_t hc = 0xFFFFFFFFu;
                 for (int q = 0; q < 24; q += 2) hc = crc_step8(hc, a.header[q], a.header[q + 1], crc_tab);
                 hc ^= 0xFFFFFFFFu;
-                const uint32_t hcrc = gf2_mulmod(hc, gf2_xpow8(16ull * a.n_chunks)) ^ acc;
+                const uint32_t hcrc = shift_bytes(hc, 16ull * a.n_chunks) ^ acc;
                 uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
                 for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : a.header[q];
                 *a.d_blob_bytes = total;

@@ -89,8 +89,6 @@ __host__ __device__ constexpr uint32_t gf2_mulmod(uint32_t a, uint32_t b) {
 
 struct CrcTables {
     uint32_t t[8][256];   // t[k][b]: register contribution of byte b followed by k zero bytes
-    uint32_t pow2[64];    // x^(8 * 2^j) mod P: shifting a register by 2^j bytes
-    uint32_t seg16[1025]; // x^(8 * 16 * m) mod P for m = 0..1024
 };
 
 constexpr CrcTables make_crc_tables() {
@@ -102,23 +100,72 @@ constexpr CrcTables make_crc_tables() {
     }
     for (int k = 1; k < 8; k++)
         for (uint32_t b = 0; b < 256; b++) c.t[k][b] = (c.t[k - 1][b] >> 8) ^ c.t[0][c.t[k - 1][b] & 0xFFu];
-    uint32_t x8 = 0x80000000u;                 // x^0
-    for (int k = 0; k < 8; k++) x8 = gf2_mul_x(x8);  // x^8
-    c.pow2[0] = x8;
-    for (int j = 1; j < 64; j++) c.pow2[j] = gf2_mulmod(c.pow2[j - 1], c.pow2[j - 1]);
-    c.seg16[0] = 0x80000000u;
-    for (int m = 1; m <= 1024; m++) c.seg16[m] = gf2_mulmod(c.seg16[m - 1], c.pow2[4]);
     return c;
 }
 
 __device__ constexpr CrcTables kCrc = make_crc_tables();
 
-// x^(8n) mod P by square-and-multiply over the bits of n.
-__device__ inline uint32_t gf2_xpow8(uint64_t n) {
-    uint32_t r = 0x80000000u;
+// Multiplying a CRC register by a fixed x^(8n) mod P ("appending n zero
+// bytes") is linear in the register, so it is four table lookups, one per
+// register byte. Tables: kShPow + j shifts by 2^j bytes (j = 0..39), then the
+// stride gaps 248, 496 and 4080 bytes used by the strided CRCs below.
+constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh4080 = 42, kShCount = 43;
+
+struct ShiftTables {
+    uint32_t t[kShCount][4][256];
+};
+
+constexpr ShiftTables make_shift_tables() {
+    ShiftTables s{};
+    uint32_t pw[kShPowCount] = {};
+    uint32_t x8 = 0x80000000u;  // x^0
+    for (int k = 0; k < 8; k++) x8 = gf2_mul_x(x8);
+    pw[0] = x8;
+    for (int j = 1; j < kShPowCount; j++) pw[j] = gf2_mulmod(pw[j - 1], pw[j - 1]);
+    auto xpow8 = [&](uint32_t n) {
+        uint32_t r = 0x80000000u;
+        for (int j = 0; n; j++, n >>= 1)
+            if (n & 1u) r = gf2_mulmod(r, pw[j]);
+        return r;
+    };
+    uint32_t K[kShCount] = {};
+    for (int j = 0; j < kShPowCount; j++) K[kShPow + j] = pw[j];
+    K[kSh248] = xpow8(248);
+    K[kSh496] = xpow8(496);
+    K[kSh4080] = xpow8(4080);
+    for (int c = 0; c < kShCount; c++) {
+        // register bit m is the coefficient of x^(31-m); its image is K x^(31-m)
+        uint32_t basis[32] = {};
+        uint32_t v = K[c];
+        for (int m = 31; m >= 0; m--) {
+            basis[m] = v;
+            v = gf2_mul_x(v);
+        }
+        for (int i = 0; i < 4; i++) {
+            s.t[c][i][0] = 0;
+            for (uint32_t b = 1; b < 256; b++) {
+                int low = 0;
+                while (!((b >> low) & 1u)) low++;
+                s.t[c][i][b] = s.t[c][i][b & (b - 1)] ^ basis[8 * i + low];
+            }
+        }
+    }
+    return s;
+}
+
+__device__ constexpr ShiftTables kShift = make_shift_tables();
+
+__device__ __forceinline__ uint32_t shift_by(uint32_t c, int table) {
+    const uint32_t(*t)[256] = kShift.t[table];
+    return __ldg(&t[0][c & 0xFF]) ^ __ldg(&t[1][(c >> 8) & 0xFF]) ^ __ldg(&t[2][(c >> 16) & 0xFF]) ^
+           __ldg(&t[3][c >> 24]);
+}
+
+// Register shifted by n bytes (n < 2^40): one table multiply per set bit.
+__device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
     for (int j = 0; n; j++, n >>= 1)
-        if (n & 1u) r = gf2_mulmod(r, kCrc.pow2[j]);
-    return r;
+        if (n & 1u) c = shift_by(c, kShPow + j);
+    return c;
 }
 
 // Shared-memory copy of the slicing tables (8 KB), filled once per CTA.
@@ -133,117 +180,94 @@ __device__ __forceinline__ uint32_t crc_step8(uint32_t c, uint32_t lo, uint32_t 
            T[3][hi & 0xFF] ^ T[2][(hi >> 8) & 0xFF] ^ T[1][(hi >> 16) & 0xFF] ^ T[0][hi >> 24];
 }
 
+__device__ __forceinline__ uint32_t crc_step16(uint32_t c, uint4 v, const uint32_t (*T)[256]) {
+    return crc_step8(crc_step8(c, v.x, v.y, T), v.z, v.w, T);
+}
+
 __device__ __forceinline__ uint32_t crc_step1(uint32_t c, uint32_t byte, const uint32_t (*T)[256]) {
     return T[0][(c ^ byte) & 0xFF] ^ (c >> 8);
 }
 
-// Raw CRC register over [p, p + len) starting from register `init`, computed
-// by the whole warp: each lane takes an equal run of 16-byte blocks (the runs
-// are aligned to the end of the range, so the first lane's run may start
-// before p and only its real bytes are read), then the lanes' registers are
-// combined pairwise with shifts of 1, 2, 4, 8, 16 runs. The < 16-byte tail is
-// finished by one lane. p must be 16-byte aligned. Returns the register (no
-// final complement) on every lane. `ldcg` reads through L2 only.
 template <bool kLdcg>
-__device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256]) {
-    const int lane = threadIdx.x & 31;
-    uint64_t main = len & ~uint64_t(15);
+__device__ __forceinline__ uint4 load16(const uint8_t *p) {
+    return kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p)) : __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Raw CRC register (no final complement) over [p, p + len) from register
+// `init`, computed by NT = 32 * NW threads with coalesced loads: the
+// 16-byte pieces are dealt round-robin, aligned to the end of the range so
+// that only the first round can be short. Each thread keeps the register of
+// its own pieces with everything between them taken as zero bytes (after
+// each round it shifts by the NT*16-16 bytes of the other threads' pieces);
+// CRC-32 is linear, so the range's register is the XOR of the threads'
+// registers, each shifted by the bytes that follow its last piece: a tree
+// over threads with shifts of 16, 32, ... bytes. The last len % 16 bytes
+// are added by one thread. p must be 16-byte aligned. Every thread of the
+// group must call it (NW > 1: the whole CTA, with s_reg[NW] shared memory);
+// the result is returned in every thread.
+template <int NW, bool kLdcg>
+__device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
+                                       uint32_t *s_reg) {
+    constexpr int NT = 32 * NW;
+    constexpr int kGap = NT == 32 ? kSh496 : kSh4080;
+    static_assert(NT == 32 || NT == 256, "strided CRC runs on one warp or on 8 warps");
+    const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
+    const int lane = threadIdx.x & 31, warp = tid >> 5;
+    const uint64_t main = len & ~uint64_t(15);
+    const uint64_t pieces = main / 16;
     uint32_t reg = init;
-    if (main) {
-        uint64_t seg = ((main / 16 + 31) / 32) * 16;  // bytes per lane
-        int64_t s = int64_t(main) - int64_t(32 - lane) * int64_t(seg);
-        int64_t e = s + int64_t(seg);
-        uint32_t c = (s <= 0 && e > 0) ? init : 0u;
-        if (s < 0) s = 0;
-        int64_t off = s;
-        for (; off + 64 <= e; off += 64) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; u++)
-                v[u] = kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p + off) + u)
-                             : __ldg(reinterpret_cast<const uint4 *>(p + off) + u);
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                c = crc_step8(c, v[u].x, v[u].y, T);
-                c = crc_step8(c, v[u].z, v[u].w, T);
-            }
+    if (pieces) {
+        const uint64_t rounds = (pieces + NT - 1) / NT;
+        const uint64_t v0 = rounds * NT - pieces;  // empty slots before the first piece
+        uint32_t R = 0;
+        int64_t pidx = int64_t(tid) - int64_t(v0);
+        uint4 cur = pidx >= 0 ? load16<kLdcg>(p + 16 * pidx) : make_uint4(0, 0, 0, 0);
+        for (uint64_t r = 0; r < rounds; r++) {
+            uint4 nxt = make_uint4(0, 0, 0, 0);
+            if (r + 1 < rounds) nxt = load16<kLdcg>(p + 16 * (pidx + NT));
+            uint32_t c = r == 0 ? (pidx == 0 ? init : 0u) : shift_by(R, kGap);
+            if (pidx >= 0) c = crc_step16(c, cur, T);
+            R = c;
+            cur = nxt;
+            pidx += NT;
         }
-        for (; off < e; off += 16) {
-            uint4 v = kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p + off))
-                            : __ldg(reinterpret_cast<const uint4 *>(p + off));
-            c = crc_step8(c, v.x, v.y, T);
-            c = crc_step8(c, v.z, v.w, T);
-        }
-        uint32_t K = (seg / 16 <= 1024) ? kCrc.seg16[seg / 16] : gf2_xpow8(seg);
 #pragma unroll
         for (int k = 0; k < 5; k++) {
-            uint32_t right = __shfl_down_sync(kFull, c, 1 << k);
-            c = gf2_mulmod(c, K) ^ right;
-            K = gf2_mulmod(K, K);
+            const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
+            R = shift_by(R, kShPow + 4 + k) ^ right;
         }
-        reg = __shfl_sync(kFull, c, 0);
+        if constexpr (NW > 1) {
+            if (lane == 0) s_reg[warp] = R;
+            __syncthreads();
+            if (warp == 0) {
+                R = lane < NW ? s_reg[lane] : 0u;
+#pragma unroll
+                for (int k = 0; (1 << k) < NW; k++) {
+                    const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
+                    R = shift_by(R, kShPow + 9 + k) ^ right;
+                }
+                if (lane == 0) s_reg[0] = R;
+            }
+            __syncthreads();
+            reg = s_reg[0];
+            __syncthreads();
+        } else {
+            reg = __shfl_sync(kFull, R, 0);
+        }
     }
-    for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, kLdcg ? __ldcg(p + i) : p[i], T);
+    for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), T);
     return reg;
 }
 
-// Raw CRC register over [p, p + len) computed by a whole CTA of NW warps, the
-// same way as warp_crc_raw but with 32 * NW runs: each warp folds its 32
-// lanes, then warp 0 folds the NW warp registers (through s_reg[NW] in shared
-// memory). Every thread of the CTA must call it; the result is valid in all
-// threads. p must be 16-byte aligned; reads go through L2 only.
+template <bool kLdcg>
+__device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256]) {
+    return crc_strided<1, kLdcg>(p, len, init, T, nullptr);
+}
+
 template <int NW>
 __device__ inline uint32_t block_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
                                          uint32_t *s_reg) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kRuns = 32 * NW;
-    const uint64_t main = len & ~uint64_t(15);
-    uint32_t reg = init;
-    if (main) {
-        const uint64_t seg = ((main / 16 + kRuns - 1) / kRuns) * 16;
-        int64_t s = int64_t(main) - int64_t(kRuns - tid) * int64_t(seg);
-        const int64_t e = s + int64_t(seg);
-        uint32_t c = (s <= 0 && e > 0) ? init : 0u;
-        if (s < 0) s = 0;
-        int64_t off = s;
-        for (; off + 32 <= e; off += 32) {
-            uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(p + off));
-            uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(p + off + 16));
-            c = crc_step8(c, v0.x, v0.y, T);
-            c = crc_step8(c, v0.z, v0.w, T);
-            c = crc_step8(c, v1.x, v1.y, T);
-            c = crc_step8(c, v1.z, v1.w, T);
-        }
-        if (off < e) {
-            uint4 v = __ldcg(reinterpret_cast<const uint4 *>(p + off));
-            c = crc_step8(c, v.x, v.y, T);
-            c = crc_step8(c, v.z, v.w, T);
-        }
-        uint32_t K = (seg / 16 <= 1024) ? kCrc.seg16[seg / 16] : gf2_xpow8(seg);
-#pragma unroll
-        for (int k = 0; k < 5; k++) {
-            uint32_t right = __shfl_down_sync(kFull, c, 1 << k);
-            c = gf2_mulmod(c, K) ^ right;
-            K = gf2_mulmod(K, K);
-        }
-        if (lane == 0) s_reg[warp] = c;
-        __syncthreads();
-        if (warp == 0) {
-            c = lane < NW ? s_reg[lane] : 0u;
-#pragma unroll
-            for (int k = 1; k < NW; k <<= 1) {
-                uint32_t right = __shfl_down_sync(kFull, c, k);
-                c = gf2_mulmod(c, K) ^ right;
-                K = gf2_mulmod(K, K);
-            }
-            if (lane == 0) s_reg[0] = c;
-        }
-        __syncthreads();
-        reg = s_reg[0];
-        __syncthreads();
-    }
-    for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, __ldcg(p + i), T);
-    return reg;
+    return crc_strided<NW, true>(p, len, init, T, s_reg);
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() { uint32_t m; asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m)); return m; }
