@@ -32,7 +32,7 @@ constexpr int kWarps = 8;
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 512, kRingBytes = 2 * kRingWords,
                    kStageBytes = 256;
 constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
-constexpr uint32_t kCrcSmem = 8 * 256 * 4;
+constexpr uint32_t kCrcSmem = 8 * 256 * 4 + 4 * 256 * 4;  // slicing tables + stride gap table
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
@@ -168,7 +168,8 @@ struct Col8 {
 };
 
 template <int DT>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t (*crc_tab)[256]) {
+__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t (*crc_tab)[256],
+                             const uint32_t (*gap)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
@@ -193,7 +194,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     }
     const uint8_t *p = a.blob + off;
     if (!(a.flags & ZC_NO_VERIFY)) {
-        uint32_t crc = warp_crc_raw<false>(p, stored, 0xFFFFFFFFu, crc_tab) ^ 0xFFFFFFFFu;
+        uint32_t crc = warp_crc_raw<false>(p, stored, 0xFFFFFFFFu, crc_tab, gap) ^ 0xFFFFFFFFu;
         if (crc != ent.w) {
             if (lane == 0) status_or(a.d_status, ZC_ECRC);
             return;
@@ -412,12 +413,16 @@ template <int DT>
 __global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t(*crc_tab)[256] = reinterpret_cast<uint32_t(*)[256]>(smem);
+    uint32_t(*gap)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + 8 * 256 * 4);
     const int warp = threadIdx.x >> 5;
-    if (!(a.flags & ZC_NO_VERIFY)) load_crc_smem(crc_tab);
+    if (!(a.flags & ZC_NO_VERIFY)) {
+        load_crc_smem(crc_tab);
+        load_shift_smem(gap, gap_table<32>());
+    }
     __syncthreads();
     uint32_t c = blockIdx.x * kWarps + warp;
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_tab);
+    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_tab, gap);
 }
 
 template <int DT>

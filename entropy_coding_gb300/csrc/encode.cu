@@ -25,9 +25,9 @@ namespace zc {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSM = 3;
+constexpr int kCtasPerSM = 6;
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
@@ -290,9 +290,8 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uin
     uint32_t wc = 0;
     const int T = int((n + 31) / 32);
 
-    auto step = [&](uint32_t word, bool active) {
-        const uint32_t s = stream_byte<W>(Perm<DT>::fwd(word), J);
-        const uint4 e = etab[s];
+    auto sym_of = [&](uint32_t word) { return stream_byte<W>(Perm<DT>::fwd(word), J); };
+    auto step = [&](const uint4 &e, bool active) {
         const bool emit = active && x >= e.z;
         const uint32_t bal = __ballot_sync(kFull, emit);
         // the store reads its own copy of x, so updating x need not wait for it
@@ -311,9 +310,10 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uin
     {
         const uint32_t i = uint32_t(T - 1) * 32 + lane;
         const bool active = i < n;
-        step(active ? load_word<W>(src + uint64_t(i) * W) : 0u, active);
+        step(etab[sym_of(active ? load_word<W>(src + uint64_t(i) * W) : 0u)], active);
     }
-    // then the full steps T-2 .. 0, 16 at a time, the next 16 words in flight
+    // then the full steps T-2 .. 0, 16 at a time with the next 16 words in
+    // flight; each step's table entry is read one step ahead
     constexpr int B = 16;
     uint32_t buf[B];
 #pragma unroll
@@ -321,6 +321,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uin
         const int t = T - 2 - k;
         buf[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
     }
+    uint4 e_next = etab[sym_of(buf[0])];
     for (int t0 = T - 2; t0 >= 0; t0 -= B) {
         uint32_t nxt[B];
 #pragma unroll
@@ -328,13 +329,12 @@ __device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uin
             const int t = t0 - B - k;
             nxt[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
         }
-        if (t0 >= B - 1) {
+        const bool full = t0 >= B - 1;
 #pragma unroll
-            for (int k = 0; k < B; k++) step(buf[k], true);
-        } else {
-#pragma unroll
-            for (int k = 0; k < B; k++)
-                if (t0 - k >= 0) step(buf[k], true);
+        for (int k = 0; k < B; k++) {
+            const uint4 e = e_next;
+            e_next = etab[sym_of(k + 1 < B ? buf[k + 1] : nxt[0])];
+            if (full || t0 - k >= 0) step(e, true);
         }
 #pragma unroll
         for (int k = 0; k < B; k++) buf[k] = nxt[k];
@@ -473,11 +473,13 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     __shared__ uint32_t crc_tab[8][256];
+    __shared__ uint32_t gap_tab[4][256];
     __shared__ uint32_t hist[W][256];
     __shared__ uint4 etab[W][256];
     __shared__ Plan pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     load_crc_smem(crc_tab);
+    load_shift_smem(gap_tab, gap_table<kThreads>());
 
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
     uint8_t *slot = a.ws_slots + uint64_t(blockIdx.x) * a.slot_bytes;
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                         block_copy(slot + uint64_t(j) * rec_stride, pad16(pl.val[j]), out + pl.roff[j]);
             }
             __syncthreads();
-            const uint32_t crc = block_crc_raw<kWarps>(out, pl.stored, 0xFFFFFFFFu, crc_tab, pl.crc_reg) ^ 0xFFFFFFFFu;
+            const uint32_t crc = block_crc_raw<kWarps>(out, pl.stored, 0xFFFFFFFFu, crc_tab, gap_tab, pl.crc_reg) ^ 0xFFFFFFFFu;
             if (tid == 0) {
                 uint4 ent;
                 ent.x = uint32_t(pl.off);

@@ -108,8 +108,8 @@ __device__ constexpr CrcTables kCrc = make_crc_tables();
 // Multiplying a CRC register by a fixed x^(8n) mod P ("appending n zero
 // bytes") is linear in the register, so it is four table lookups, one per
 // register byte. Tables: kShPow + j shifts by 2^j bytes (j = 0..39), then the
-// stride gaps 248, 496 and 4080 bytes used by the strided CRCs below.
-constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh4080 = 42, kShCount = 43;
+// stride gaps 248, 496, 2032 and 4080 bytes used by the strided CRCs below.
+constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh2032 = 42, kSh4080 = 43, kShCount = 44;
 
 struct ShiftTables {
     uint32_t t[kShCount][4][256];
@@ -132,6 +132,7 @@ constexpr ShiftTables make_shift_tables() {
     for (int j = 0; j < kShPowCount; j++) K[kShPow + j] = pw[j];
     K[kSh248] = xpow8(248);
     K[kSh496] = xpow8(496);
+    K[kSh2032] = xpow8(2032);
     K[kSh4080] = xpow8(4080);
     for (int c = 0; c < kShCount; c++) {
         // register bit m is the coefficient of x^(31-m); its image is K x^(31-m)
@@ -160,6 +161,18 @@ __device__ __forceinline__ uint32_t shift_by(uint32_t c, int table) {
     return __ldg(&t[0][c & 0xFF]) ^ __ldg(&t[1][(c >> 8) & 0xFF]) ^ __ldg(&t[2][(c >> 16) & 0xFF]) ^
            __ldg(&t[3][c >> 24]);
 }
+
+__device__ __forceinline__ uint32_t shift_smem(uint32_t c, const uint32_t (*t)[256]) {
+    return t[0][c & 0xFF] ^ t[1][(c >> 8) & 0xFF] ^ t[2][(c >> 16) & 0xFF] ^ t[3][c >> 24];
+}
+
+// Shared-memory copy of one shift table (4 KB), filled once per CTA.
+__device__ inline void load_shift_smem(uint32_t (*dst)[256], int table) {
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) dst[i >> 8][i & 255] = kShift.t[table][i >> 8][i & 255];
+}
+
+template <int NT>
+constexpr int gap_table() { return NT == 32 ? kSh496 : NT == 128 ? kSh2032 : kSh4080; }
 
 // Register shifted by n bytes (n < 2^40): one table multiply per set bit.
 __device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
@@ -202,15 +215,15 @@ __device__ __forceinline__ uint4 load16(const uint8_t *p) {
 // CRC-32 is linear, so the range's register is the XOR of the threads'
 // registers, each shifted by the bytes that follow its last piece: a tree
 // over threads with shifts of 16, 32, ... bytes. The last len % 16 bytes
-// are added by one thread. p must be 16-byte aligned. Every thread of the
-// group must call it (NW > 1: the whole CTA, with s_reg[NW] shared memory);
-// the result is returned in every thread.
+// are added by one thread. p must be 16-byte aligned; G is the shared-memory
+// copy of the gap table gap_table<32 * NW>(). Every thread of the group must
+// call it (NW > 1: the whole CTA, with s_reg[NW] shared memory); the result
+// is returned in every thread.
 template <int NW, bool kLdcg>
 __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
-                                       uint32_t *s_reg) {
+                                       const uint32_t (*G)[256], uint32_t *s_reg) {
     constexpr int NT = 32 * NW;
-    constexpr int kGap = NT == 32 ? kSh496 : kSh4080;
-    static_assert(NT == 32 || NT == 256, "strided CRC runs on one warp or on 8 warps");
+    static_assert(NT == 32 || NT == 128 || NT == 256, "strided CRC runs on 1, 4 or 8 warps");
     const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
     const int lane = threadIdx.x & 31, warp = tid >> 5;
     const uint64_t main = len & ~uint64_t(15);
@@ -225,7 +238,7 @@ __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t 
         for (uint64_t r = 0; r < rounds; r++) {
             uint4 nxt = make_uint4(0, 0, 0, 0);
             if (r + 1 < rounds) nxt = load16<kLdcg>(p + 16 * (pidx + NT));
-            uint32_t c = r == 0 ? (pidx == 0 ? init : 0u) : shift_by(R, kGap);
+            uint32_t c = r == 0 ? (pidx == 0 ? init : 0u) : shift_smem(R, G);
             if (pidx >= 0) c = crc_step16(c, cur, T);
             R = c;
             cur = nxt;
@@ -260,14 +273,15 @@ __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t 
 }
 
 template <bool kLdcg>
-__device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256]) {
-    return crc_strided<1, kLdcg>(p, len, init, T, nullptr);
+__device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
+                                        const uint32_t (*G)[256]) {
+    return crc_strided<1, kLdcg>(p, len, init, T, G, nullptr);
 }
 
 template <int NW>
 __device__ inline uint32_t block_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
-                                         uint32_t *s_reg) {
-    return crc_strided<NW, true>(p, len, init, T, s_reg);
+                                         const uint32_t (*G)[256], uint32_t *s_reg) {
+    return crc_strided<NW, true>(p, len, init, T, G, s_reg);
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() { uint32_t m; asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m)); return m; }
