@@ -24,7 +24,7 @@
  *              field read as zero
  *   32   64    shape[8] as int64, unused dims zero
  *   96   16*n  chunk table: u64 offset, u32 stored | raw_flag << 31,
- *              u32 CRC-32 of the stored payload bytes
+ *              u32 CRC-32 of the chunk's original (uncompressed) bytes
  *   then each chunk's payload in chunk order, zero-padded to 16 bytes;
  *   offset_0 = 96 + 16n, offset_{c+1} = offset_c + pad16(stored_c).
  *
@@ -462,7 +462,10 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
     /* ZipNN Method 5: fixed-size chunks; a metadata map records each
      * chunk's variable compressed size so chunks decode independently. The
      * map here holds offsets, which are the running sum of the padded sizes
-     * of the chunks before. */
+     * of the chunks before. Each entry also carries the zlib CRC-32 of the
+     * chunk's original bytes (cuZipNN: checksums match zlib.crc32; reading:
+     * the chunk CRC checks the decoded result end to end, while whole-blob
+     * checks before decoding use the CRC of the blob's own bytes). */
     uint64_t off = table_end;
     for (uint64_t c = 0; c < nc; c++) {
         uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - c * chunk_bytes);
@@ -475,7 +478,7 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
         uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * c;
         put64(e, off);
         put32(e + 8, (uint32_t)stored | ((uint32_t)raw << 31));
-        put32(e + 12, zco_crc32(blob + off, stored));
+        put32(e + 12, zco_crc32(src + c * (uint64_t)chunk_bytes, len));
         off += pad16(stored);
     }
     put32(blob + 28, zco_crc32(blob, table_end));
@@ -598,13 +601,13 @@ int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_
         uint32_t stored = sm & 0x7FFFFFFFu;
         uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - (uint64_t)c * chunk_bytes);
         uint8_t *out = dst + (uint64_t)c * chunk_bytes;
-        /* cuZipNN: verify a blob's CRCs before trusting it */
-        if (!(flags & ZCO_NO_VERIFY) && zco_crc32(blob + off, stored) != get32(e + 12)) {
-            status |= ZCO_ECRC;
-            continue;
-        }
+        int cst = ZCO_OK;
         if (sm >> 31) memcpy(out, blob + off, len);
-        else status |= decode_grouped(blob + off, stored, len, dtype, out);
+        else cst = decode_grouped(blob + off, stored, len, dtype, out);
+        status |= cst;
+        /* the chunk CRC covers the original bytes: check what was decoded */
+        if (cst == ZCO_OK && !(flags & ZCO_NO_VERIFY) && zco_crc32(out, len) != get32(e + 12))
+            status |= ZCO_ECRC;
     }
     return status;
 }

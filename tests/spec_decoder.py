@@ -83,33 +83,40 @@ def decode(blob: bytes) -> bytes:
     head[28:32] = b"\0\0\0\0"
     if zlib.crc32(bytes(head)) != hcrc:
         raise SpecError("header crc")
-    W = WORD[dtype]
     out = bytearray()
     for c in range(n_chunks):
         off, sm, crc = struct.unpack_from("<QII", blob, 96 + 16 * c)
         stored, raw = sm & 0x7FFFFFFF, sm >> 31
         payload = blob[off:off + stored]
-        if zlib.crc32(payload) != crc:
-            raise SpecError(f"chunk {c} crc")
         length = min(chunk_bytes, nbytes - c * chunk_bytes)
+        start = len(out)
         if raw:
             out += payload
+        else:
+            out += _grouped(payload, length, dtype)
+        if zlib.crc32(bytes(out[start:])) != crc:   # CRC of the original bytes
+            raise SpecError(f"chunk {c} crc")
+    return bytes(out)
+
+
+def _grouped(payload: bytes, length: int, dtype: int) -> bytes:
+    W = WORD[dtype]
+    n = length // W
+    pos = (4 * W + 15) // 16 * 16
+    streams = []
+    for j in range(W):
+        entry, = struct.unpack_from("<I", payload, 4 * j)
+        mode, v = entry >> 30, entry & 0x3FFFFFFF
+        if mode == 2:
+            streams.append([v] * n)
             continue
-        n = length // W
-        pos = (4 * W + 15) // 16 * 16
-        streams = []
+        rec = payload[pos:pos + v]
+        streams.append(list(rec) if mode == 0 else _rans(rec, n))
+        pos += (v + 15) // 16 * 16
+    out = bytearray()
+    for i in range(n):
+        p = 0
         for j in range(W):
-            entry, = struct.unpack_from("<I", payload, 4 * j)
-            mode, v = entry >> 30, entry & 0x3FFFFFFF
-            if mode == 2:
-                streams.append([v] * n)
-                continue
-            rec = payload[pos:pos + v]
-            streams.append(list(rec) if mode == 0 else _rans(rec, n))
-            pos += (v + 15) // 16 * 16
-        for i in range(n):
-            p = 0
-            for j in range(W):
-                p = (p << 8) | streams[j][i]
-            out += _unpermute(p, dtype).to_bytes(W, "little")
+            p = (p << 8) | streams[j][i]
+        out += _unpermute(p, dtype).to_bytes(W, "little")
     return bytes(out)

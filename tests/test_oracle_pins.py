@@ -226,7 +226,8 @@ def test_tiny_blob_golden(zco):
     payload = struct.pack("<I", int(g["dir0"], 16)) + bytes(12) + rec
     assert len(payload) == int(g["chunk0_stored"])
     entry = struct.pack("<QII", int(g["chunk0_offset"]),
-                        int(g["chunk0_stored"]) | (int(g["chunk0_raw"]) << 31), zlib.crc32(payload))
+                        int(g["chunk0_stored"]) | (int(g["chunk0_raw"]) << 31),
+                        zlib.crc32(bytes.fromhex(g["chunk0_original"])))
     table = bytes(head) + entry
     assert len(table) == table_end
     hcrc = zlib.crc32(table)
