@@ -18,19 +18,20 @@ constexpr int kWarps = 8;
 
 // Raw register over an arbitrarily aligned range: bytes up to the first
 // 16-byte boundary are taken one at a time, the rest by the warp.
-__device__ uint32_t warp_crc_raw_any(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
+__device__ uint32_t warp_crc_raw_any(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
                                      const uint32_t (*G)[256]) {
     uint64_t head = (16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15;
     if (head > len) head = len;
     uint32_t reg = init;
-    for (uint64_t i = 0; i < head; i++) reg = crc_step1(reg, __ldg(p + i), T);
-    return warp_crc_raw<false>(p + head, len - head, reg, T, G);
+    const uint32_t *row = T + (threadIdx.x & 31);
+    for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, __ldg(p + i), row);
+    return crc_strided<1, false>(p + head, len - head, reg, T, G, nullptr);
 }
 
 __global__ void __launch_bounds__(kWarps * 32) crc_kernel(CrcArgs a) {
-    __shared__ uint32_t tab[8][256];
+    __shared__ uint32_t tab[kCrcRepWords];
     __shared__ uint32_t gap[4][256];
-    load_crc_smem(tab);
+    load_crc_rep(tab);
     load_shift_smem(gap, gap_table<32>());
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

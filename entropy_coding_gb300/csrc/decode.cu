@@ -32,7 +32,8 @@ constexpr int kWarps = 8;
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 512, kRingBytes = 2 * kRingWords,
                    kStageBytes = 256;
 constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
-constexpr uint32_t kCrcSmem = 8 * 256 * 4 + 4 * 256 * 4;  // slicing tables + stride gap table
+// replicated CRC byte table + the gap table of the output pieces + the 496-byte gap table
+constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
@@ -168,8 +169,8 @@ struct Col8 {
 };
 
 template <int DT>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t (*crc_tab)[256],
-                             const uint32_t (*gap)[256]) {
+__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t *crc_rep,
+                             const uint32_t (*gap_out)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
@@ -193,19 +194,18 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
         return;
     }
     const uint8_t *p = a.blob + off;
-    if (!(a.flags & ZC_NO_VERIFY)) {
-        uint32_t crc = warp_crc_raw<false>(p, stored, 0xFFFFFFFFu, crc_tab, gap) ^ 0xFFFFFFFFu;
-        if (crc != ent.w) {
-            if (lane == 0) status_or(a.d_status, ZC_ECRC);
-            return;
-        }
-    }
+    const bool verify = !(a.flags & ZC_NO_VERIFY);
+    const uint32_t *row = crc_rep + lane;
     uint8_t *out = a.dst + uint64_t(c) * a.chunk_bytes;
     if (raw) {
         uint32_t nvec = (reinterpret_cast<uintptr_t>(out) & 15) ? 0 : len / 16;
         for (uint32_t v = lane; v < nvec; v += 32)
             reinterpret_cast<uint4 *>(out)[v] = __ldg(reinterpret_cast<const uint4 *>(p) + v);
         for (uint32_t i = nvec * 16 + lane; i < len; i += 32) out[i] = p[i];
+        // a RAW chunk stores the original bytes, so its CRC is the payload's
+        if (verify && (crc_strided<1, false>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
+            lane == 0)
+            status_or(a.d_status, ZC_ECRC);
         return;
     }
 
@@ -295,6 +295,11 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     // elements 256 g + 8 lane .. + 7
     const uint32_t groups = n / 256;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    // CRC of the decoded bytes: lane l's 8 elements of each group form one
+    // 8W-byte piece; pieces of a group are consecutive, so each lane keeps the
+    // register of its own pieces and shifts it over the others' (256 W - 8 W
+    // bytes) between groups, then the lanes are folded (crc_fold).
+    uint32_t Rl = 0;
     uint2 rn1[W], rn2[W];  // raw columns of the next two groups
 #pragma unroll
     for (int j = 0; j < W; j++) {
@@ -335,6 +340,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             }
         }
         __syncwarp();
+        const uint32_t cin = g == 0 ? (lane == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(Rl, gap_out);
         if constexpr (W == 4) {
             uint4 v[2];
 #pragma unroll
@@ -348,6 +354,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
                 v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
                 v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
             }
+            if (verify) Rl = crc_rep16(crc_rep16(cin, v[0], row), v[1], row);
             if (vec_ok) {
                 uint4 *o = reinterpret_cast<uint4 *>(out + 4ull * e0);
                 o[0] = v[0];
@@ -363,6 +370,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
             v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
             v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
+            if (verify) Rl = crc_rep16(cin, v, row);
             if (vec_ok) {
                 *reinterpret_cast<uint4 *>(out + 2ull * e0) = v;
             } else {
@@ -374,6 +382,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
                 }
             }
         } else {
+            if (verify) Rl = crc_rep_word(crc_rep_word(cin, col[0].lo, row), col[0].hi, row);
             if ((reinterpret_cast<uintptr_t>(out) & 7) == 0) {
                 *reinterpret_cast<uint2 *>(out + e0) = make_uint2(col[0].lo, col[0].hi);
             } else {
@@ -406,23 +415,35 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
             else out[i] = uint8_t(w);
         }
     }
-    if (have_main && !rans_final_ok(rs) && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+    bool bad_end = have_main && !rans_final_ok(rs);
+    if (verify) {
+        constexpr int kLogPiece = W == 4 ? 5 : W == 2 ? 4 : 3;
+        uint32_t reg = groups ? crc_fold<1>(Rl, kLogPiece, nullptr) : 0xFFFFFFFFu;
+        __syncwarp();
+        const uint32_t done = groups * 256 * W;
+        reg = crc_any<1, true>(out + done, len - done, reg, crc_rep, gap496, nullptr);
+        if ((reg ^ 0xFFFFFFFFu) != ent.w && lane == 0) status_or(a.d_status, ZC_ECRC);
+    }
+    if (bad_end && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t(*crc_tab)[256] = reinterpret_cast<uint32_t(*)[256]>(smem);
-    uint32_t(*gap)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + 8 * 256 * 4);
+    constexpr int W = WordOf<DT>::W;
+    uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
+    uint32_t(*gap_out)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
-        load_crc_smem(crc_tab);
-        load_shift_smem(gap, gap_table<32>());
+        load_crc_rep(crc_rep);
+        load_shift_smem(gap_out, W == 4 ? kSh992 : W == 2 ? kSh496 : kSh248);
+        load_shift_smem(gap496, kSh496);
     }
     __syncthreads();
     uint32_t c = blockIdx.x * kWarps + warp;
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_tab, gap);
+    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_rep, gap_out, gap496);
 }
 
 template <int DT>

@@ -25,9 +25,9 @@ namespace zc {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSM = 6;
+constexpr int kCtasPerSM = 3;
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
@@ -118,43 +118,72 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
     return inc - v;
 }
 
-// Histogram of the W byte streams of one chunk into h[W][256], by the CTA.
+// Histogram of the W byte streams of one chunk into h[W][256], by the CTA,
+// and the raw CRC register of the chunk's bytes (the chunk table's check of
+// the original data) from the same loads: the 16-byte pieces are dealt to
+// the threads as in crc_strided, so each thread's register only needs the
+// gap shift between its pieces. Returns the raw register in every thread.
 template <int DT>
-__device__ void chunk_histograms(const uint8_t *src, uint32_t len, uint32_t (*h)[256]) {
+__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, uint32_t (*h)[256], const uint32_t *crc_rep,
+                                const uint32_t (*gap)[256], uint32_t *s_reg) {
     constexpr int W = WordOf<DT>::W;
     const int tid = threadIdx.x;
+    const uint32_t *row = crc_rep + (tid & 31);
     for (int i = tid; i < W * 256; i += kThreads) h[i >> 8][i & 255] = 0;
     __syncthreads();
-    const uint32_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    constexpr int U = 4;  // loads in flight per thread
-    for (uint32_t v0 = tid; v0 < nvec; v0 += U * kThreads) {
-        uint4 qv[U];
-#pragma unroll
-        for (int u = 0; u < U; u++)
-            qv[u] = (v0 + u * kThreads < nvec) ? __ldg(reinterpret_cast<const uint4 *>(src) + v0 + u * kThreads)
-                                               : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            if (v0 + u * kThreads >= nvec) break;
-            uint32_t uu[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-#pragma unroll
-                for (int e = 0; e < 4 / W; e++) {
-                    uint32_t w = (W == 4) ? uu[k] : (uu[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
-                    uint32_t p = Perm<DT>::fwd(w);
-#pragma unroll
-                    for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
-                }
-            }
-        }
-    }
-    for (uint32_t i = nvec * 16 / W + tid; i < len / W; i += kThreads) {
-        uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
+    auto count = [&](uint32_t w) {
+        const uint32_t p = Perm<DT>::fwd(w);
 #pragma unroll
         for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
+    };
+    uint32_t reg;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint32_t main = len & ~15u;
+        const Strided sp(main, kThreads);
+        uint32_t R = 0;
+        int64_t pidx = int64_t(tid) - int64_t(sp.v0);
+        constexpr int U = 4;  // pieces in flight per thread
+        for (uint64_t r0 = 0; r0 < sp.rounds; r0 += U) {
+            uint4 q[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t pi = pidx + int64_t(u) * kThreads;
+                q[u] = (r0 + u < sp.rounds && pi >= 0) ? __ldg(reinterpret_cast<const uint4 *>(src) + pi)
+                                                      : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                if (r0 + u >= sp.rounds) break;
+                const int64_t pi = pidx + int64_t(u) * kThreads;
+                uint32_t c = (r0 + u == 0) ? (pi == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, gap);
+                if (pi >= 0) {
+                    c = crc_rep16(c, q[u], row);
+                    const uint32_t uu[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+#pragma unroll
+                        for (int e = 0; e < 4 / W; e++)
+                            count(W == 4 ? uu[k] : (uu[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u));
+                }
+                R = c;
+            }
+            pidx += int64_t(U) * kThreads;
+        }
+        reg = sp.pieces ? crc_fold<kWarps>(R, 4, s_reg) : 0xFFFFFFFFu;
+        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, __ldg(src + i), row);
+        for (uint32_t i = main / W + tid; i < len / W; i += kThreads) count(load_word<W>(src + uint64_t(i) * W));
+    } else {
+        // unaligned input: words one at a time; the CRC takes the bytes up to
+        // the first 16-byte boundary one by one, then the aligned rest
+        for (uint32_t i = tid; i < len / W; i += kThreads) count(load_word<W>(src + uint64_t(i) * W));
+        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15);
+        if (head > len) head = len;
+        uint32_t c = 0xFFFFFFFFu;
+        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, __ldg(src + i), row);
+        reg = crc_strided<kWarps, false>(src + head, len - head, c, crc_rep, gap, s_reg);
     }
     __syncthreads();
+    return reg;
 }
 
 // 12-bit table from counts held as 8 bins per lane (symbol 8*lane + k).
@@ -355,6 +384,7 @@ struct Plan {
     uint32_t raw_chunk;
     uint32_t write;    // 0 when the chunk is not placed (capacity or timeout)
     uint32_t c;
+    uint32_t crc;      // CRC-32 of the chunk's original bytes
     uint32_t crc_reg[kWarps];
 };
 
@@ -469,17 +499,26 @@ __device__ void block_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
     for (uint64_t i = nvec * 16 + threadIdx.x; i < pad16(len); i += kThreads) dst[i] = i < len ? src[i] : 0;
 }
 
+// Dynamic shared memory of the compression CTA.
+template <int W>
+struct EncodeSmem {
+    uint32_t crc_rep[kCrcRepWords];  // replicated CRC byte table (32 KB)
+    uint32_t gap[4][256];            // register shift over the other threads' pieces
+    uint32_t hist[W][256];
+    uint4 etab[W][256];
+    Plan pl;
+};
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
-    __shared__ uint32_t crc_tab[8][256];
-    __shared__ uint32_t gap_tab[4][256];
-    __shared__ uint32_t hist[W][256];
-    __shared__ uint4 etab[W][256];
-    __shared__ Plan pl;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    EncodeSmem<W> &sm = *reinterpret_cast<EncodeSmem<W> *>(smem_raw);
+    Plan &pl = sm.pl;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    load_crc_smem(crc_tab);
-    load_shift_smem(gap_tab, gap_table<kThreads>());
+    load_crc_rep(sm.crc_rep);
+    load_shift_smem(sm.gap, gap_table<kThreads>());
+    const uint32_t *row = sm.crc_rep + lane;
 
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
     uint8_t *slot = a.ws_slots + uint64_t(blockIdx.x) * a.slot_bytes;
@@ -495,15 +534,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
 
-        chunk_histograms<DT>(src, len, hist);
+        const uint32_t crc = chunk_stats<DT>(src, len, sm.hist, sm.crc_rep, sm.gap, pl.crc_reg) ^ 0xFFFFFFFFu;
 
-        if (warp == 0) plan_stream<DT, 0>(a, src, n, hist, etab[0], slot, pl);
+        if (warp == 0) plan_stream<DT, 0>(a, src, n, sm.hist, sm.etab[0], slot, pl);
         if constexpr (W > 1) {
-            if (warp == 1) plan_stream<DT, 1>(a, src, n, hist, etab[1], slot + rec_stride, pl);
+            if (warp == 1) plan_stream<DT, 1>(a, src, n, sm.hist, sm.etab[1], slot + rec_stride, pl);
         }
         if constexpr (W > 2) {
-            if (warp == 2) plan_stream<DT, 2>(a, src, n, hist, etab[2], slot + 2 * rec_stride, pl);
-            if (warp == 3) plan_stream<DT, 3>(a, src, n, hist, etab[3], slot + 3 * rec_stride, pl);
+            if (warp == 2) plan_stream<DT, 2>(a, src, n, sm.hist, sm.etab[2], slot + 2 * rec_stride, pl);
+            if (warp == 3) plan_stream<DT, 3>(a, src, n, sm.hist, sm.etab[3], slot + 3 * rec_stride, pl);
         }
         __syncthreads();
 
@@ -550,8 +589,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                     if (pl.mode[j] == kModeRans)
                         block_copy(slot + uint64_t(j) * rec_stride, pad16(pl.val[j]), out + pl.roff[j]);
             }
-            __syncthreads();
-            const uint32_t crc = block_crc_raw<kWarps>(out, pl.stored, 0xFFFFFFFFu, crc_tab, gap_tab, pl.crc_reg) ^ 0xFFFFFFFFu;
             if (tid == 0) {
                 uint4 ent;
                 ent.x = uint32_t(pl.off);
@@ -560,10 +597,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 ent.w = crc;
                 reinterpret_cast<uint4 *>(a.blob + ZC_HEADER_BYTES)[c] = ent;
                 // header CRC = shift(crc(header), 16 n) ^ XOR_c shift(crc(entry_c), 16 (n-1-c))
-                uint32_t ec = 0xFFFFFFFFu;
-                ec = crc_step8(ec, ent.x, ent.y, crc_tab);
-                ec = crc_step8(ec, ent.z, ent.w, crc_tab);
-                ec ^= 0xFFFFFFFFu;
+                const uint32_t ec = crc_rep16(0xFFFFFFFFu, ent, row) ^ 0xFFFFFFFFu;
                 atomicXor(&ctrl[2], shift_bytes(ec, 16ull * (a.n_chunks - 1 - c)));
             }
         }
@@ -576,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 const unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
                 const uint64_t total = table_end + (last & kValMask);
                 uint32_t hc = 0xFFFFFFFFu;
-                for (int q = 0; q < 24; q += 2) hc = crc_step8(hc, a.header[q], a.header[q + 1], crc_tab);
+                for (int q = 0; q < 24; q++) hc = crc_rep_word(hc, a.header[q], row);
                 hc ^= 0xFFFFFFFFu;
                 const uint32_t hcrc = shift_bytes(hc, 16ull * a.n_chunks) ^ acc;
                 uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
@@ -594,6 +628,15 @@ __global__ void empty_blob_kernel(EncodeArgs a) {
     if (threadIdx.x == 0) *a.d_blob_bytes = ZC_HEADER_BYTES;
 }
 
+template <int DT>
+int launch_encode_t(const EncodeArgs &a, int grid, cudaStream_t s) {
+    const size_t smem = sizeof(EncodeSmem<WordOf<DT>::W>);
+    if (cudaFuncSetAttribute(encode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return ZC_ECUDA;
+    encode_kernel<DT><<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
+
 } // namespace
 
 int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s) {
@@ -602,15 +645,14 @@ int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s) {
         return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
     }
     switch (dtype) {
-    case ZC_U8: encode_kernel<ZC_U8><<<grid, kThreads, 0, s>>>(a); break;
-    case ZC_U16: encode_kernel<ZC_U16><<<grid, kThreads, 0, s>>>(a); break;
-    case ZC_U32: encode_kernel<ZC_U32><<<grid, kThreads, 0, s>>>(a); break;
-    case ZC_BF16: encode_kernel<ZC_BF16><<<grid, kThreads, 0, s>>>(a); break;
-    case ZC_FP16: encode_kernel<ZC_FP16><<<grid, kThreads, 0, s>>>(a); break;
-    case ZC_FP32: encode_kernel<ZC_FP32><<<grid, kThreads, 0, s>>>(a); break;
+    case ZC_U8: return launch_encode_t<ZC_U8>(a, grid, s);
+    case ZC_U16: return launch_encode_t<ZC_U16>(a, grid, s);
+    case ZC_U32: return launch_encode_t<ZC_U32>(a, grid, s);
+    case ZC_BF16: return launch_encode_t<ZC_BF16>(a, grid, s);
+    case ZC_FP16: return launch_encode_t<ZC_FP16>(a, grid, s);
+    case ZC_FP32: return launch_encode_t<ZC_FP32>(a, grid, s);
     default: return ZC_EINVAL;
     }
-    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
 int encode_ctas_per_sm() { return kCtasPerSM; }

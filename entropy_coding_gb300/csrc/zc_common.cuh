@@ -108,8 +108,9 @@ __device__ constexpr CrcTables kCrc = make_crc_tables();
 // Multiplying a CRC register by a fixed x^(8n) mod P ("appending n zero
 // bytes") is linear in the register, so it is four table lookups, one per
 // register byte. Tables: kShPow + j shifts by 2^j bytes (j = 0..39), then the
-// stride gaps 248, 496, 2032 and 4080 bytes used by the strided CRCs below.
-constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh2032 = 42, kSh4080 = 43, kShCount = 44;
+// stride gaps 248, 496, 992, 2032 and 4080 bytes used by the strided CRCs.
+constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh992 = 42, kSh2032 = 43, kSh4080 = 44,
+              kShCount = 45;
 
 struct ShiftTables {
     uint32_t t[kShCount][4][256];
@@ -132,6 +133,7 @@ constexpr ShiftTables make_shift_tables() {
     for (int j = 0; j < kShPowCount; j++) K[kShPow + j] = pw[j];
     K[kSh248] = xpow8(248);
     K[kSh496] = xpow8(496);
+    K[kSh992] = xpow8(992);
     K[kSh2032] = xpow8(2032);
     K[kSh4080] = xpow8(4080);
     for (int c = 0; c < kShCount; c++) {
@@ -181,24 +183,34 @@ __device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
     return c;
 }
 
-// Shared-memory copy of the slicing tables (8 KB), filled once per CTA.
-__device__ inline void load_crc_smem(uint32_t (*tab)[256]) {
-    for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) tab[i >> 8][i & 255] = kCrc.t[i >> 8][i & 255];
+// The byte table of the CRC (Sarwate's method: one lookup per byte) held in
+// shared memory once per lane: entry b of lane l is word b * 32 + l, so the
+// 32 lanes of a warp always read 32 different banks. 32 KB per CTA.
+constexpr uint32_t kCrcRepWords = 256 * 32;
+
+__device__ inline void load_crc_rep(uint32_t *t) {
+    for (uint32_t i = threadIdx.x; i < kCrcRepWords; i += blockDim.x) t[i] = kCrc.t[0][i >> 5];
 }
 
-// Register update over 8 bytes given as two little-endian words (slicing by 8).
-__device__ __forceinline__ uint32_t crc_step8(uint32_t c, uint32_t lo, uint32_t hi, const uint32_t (*T)[256]) {
-    uint32_t v = c ^ lo;
-    return T[7][v & 0xFF] ^ T[6][(v >> 8) & 0xFF] ^ T[5][(v >> 16) & 0xFF] ^ T[4][v >> 24] ^
-           T[3][hi & 0xFF] ^ T[2][(hi >> 8) & 0xFF] ^ T[1][(hi >> 16) & 0xFF] ^ T[0][hi >> 24];
+// row = table + lane
+__device__ __forceinline__ uint32_t crc_rep_byte(uint32_t c, uint32_t byte, const uint32_t *row) {
+    return row[((c ^ byte) & 0xFFu) << 5] ^ (c >> 8);
 }
 
-__device__ __forceinline__ uint32_t crc_step16(uint32_t c, uint4 v, const uint32_t (*T)[256]) {
-    return crc_step8(crc_step8(c, v.x, v.y, T), v.z, v.w, T);
+// Register update over a little-endian 32-bit word: with u = c ^ w the
+// remaining data bytes ride down in u, so each step is u = T[u & 255] ^ u >> 8.
+__device__ __forceinline__ uint32_t crc_rep_word(uint32_t c, uint32_t w, const uint32_t *row) {
+    uint32_t u = c ^ w;
+#pragma unroll
+    for (int k = 0; k < 4; k++) u = row[(u & 0xFFu) << 5] ^ (u >> 8);
+    return u;
 }
 
-__device__ __forceinline__ uint32_t crc_step1(uint32_t c, uint32_t byte, const uint32_t (*T)[256]) {
-    return T[0][(c ^ byte) & 0xFF] ^ (c >> 8);
+__device__ __forceinline__ uint32_t crc_rep16(uint32_t c, uint4 v, const uint32_t *row) {
+    c = crc_rep_word(c, v.x, row);
+    c = crc_rep_word(c, v.y, row);
+    c = crc_rep_word(c, v.z, row);
+    return crc_rep_word(c, v.w, row);
 }
 
 template <bool kLdcg>
@@ -206,82 +218,102 @@ __device__ __forceinline__ uint4 load16(const uint8_t *p) {
     return kLdcg ? __ldcg(reinterpret_cast<const uint4 *>(p)) : __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// Piece assignment of the strided CRC: NT threads take the 16-byte pieces of
+// a range round-robin, aligned to the END of the range (only the first round
+// can be short). Thread t's piece in round r is NT r + t - v0.
+struct Strided {
+    uint64_t pieces, rounds, v0;
+    __device__ Strided(uint64_t len16, int NT) {
+        pieces = len16 / 16;
+        rounds = (pieces + NT - 1) / NT;
+        v0 = rounds * NT - pieces;
+    }
+};
+
+// Fold the per-thread registers of a strided CRC into the range's register.
+// Each thread holds the register of its own pieces with all other bytes
+// taken as zero, ending at its last piece; CRC-32 is linear, so the range's
+// register is the XOR of those registers, each shifted by the bytes after
+// its thread's last piece: a tree over threads with shifts of piece, 2
+// pieces, ... (piece = 2^log2_piece bytes). NW > 1 uses s_reg[NW] and
+// __syncthreads (every thread of the CTA must call it). Returns the result
+// in every thread.
+template <int NW>
+__device__ inline uint32_t crc_fold(uint32_t R, int log2_piece, uint32_t *s_reg) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < 5; k++) {
+        const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
+        R = shift_by(R, kShPow + log2_piece + k) ^ right;
+    }
+    if constexpr (NW > 1) {
+        const int warp = threadIdx.x >> 5;
+        if (lane == 0) s_reg[warp] = R;
+        __syncthreads();
+        if (warp == 0) {
+            R = lane < NW ? s_reg[lane] : 0u;
+#pragma unroll
+            for (int k = 0; (1 << k) < NW; k++) {
+                const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
+                R = shift_by(R, kShPow + log2_piece + 5 + k) ^ right;
+            }
+            if (lane == 0) s_reg[0] = R;
+        }
+        __syncthreads();
+        R = s_reg[0];
+        __syncthreads();
+        return R;
+    } else {
+        return __shfl_sync(kFull, R, 0);
+    }
+}
+
 // Raw CRC register (no final complement) over [p, p + len) from register
-// `init`, computed by NT = 32 * NW threads with coalesced loads: the
-// 16-byte pieces are dealt round-robin, aligned to the end of the range so
-// that only the first round can be short. Each thread keeps the register of
-// its own pieces with everything between them taken as zero bytes (after
-// each round it shifts by the NT*16-16 bytes of the other threads' pieces);
-// CRC-32 is linear, so the range's register is the XOR of the threads'
-// registers, each shifted by the bytes that follow its last piece: a tree
-// over threads with shifts of 16, 32, ... bytes. The last len % 16 bytes
-// are added by one thread. p must be 16-byte aligned; G is the shared-memory
-// copy of the gap table gap_table<32 * NW>(). Every thread of the group must
-// call it (NW > 1: the whole CTA, with s_reg[NW] shared memory); the result
-// is returned in every thread.
+// `init`, by NT = 32 NW threads with coalesced 16-byte loads (see Strided and
+// crc_fold); each thread shifts its register over the other threads' pieces
+// with the gap table G = gap_table<NT>() in shared memory, T is the
+// replicated byte table. The last len % 16 bytes are added by every thread.
+// p must be 16-byte aligned. Every thread of the group calls it.
 template <int NW, bool kLdcg>
-__device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
+__device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
                                        const uint32_t (*G)[256], uint32_t *s_reg) {
     constexpr int NT = 32 * NW;
     static_assert(NT == 32 || NT == 128 || NT == 256, "strided CRC runs on 1, 4 or 8 warps");
     const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
-    const int lane = threadIdx.x & 31, warp = tid >> 5;
+    const uint32_t *row = T + (threadIdx.x & 31);
     const uint64_t main = len & ~uint64_t(15);
-    const uint64_t pieces = main / 16;
+    const Strided sp(main, NT);
     uint32_t reg = init;
-    if (pieces) {
-        const uint64_t rounds = (pieces + NT - 1) / NT;
-        const uint64_t v0 = rounds * NT - pieces;  // empty slots before the first piece
+    if (sp.pieces) {
         uint32_t R = 0;
-        int64_t pidx = int64_t(tid) - int64_t(v0);
+        int64_t pidx = int64_t(tid) - int64_t(sp.v0);
         uint4 cur = pidx >= 0 ? load16<kLdcg>(p + 16 * pidx) : make_uint4(0, 0, 0, 0);
-        for (uint64_t r = 0; r < rounds; r++) {
+        for (uint64_t r = 0; r < sp.rounds; r++) {
             uint4 nxt = make_uint4(0, 0, 0, 0);
-            if (r + 1 < rounds) nxt = load16<kLdcg>(p + 16 * (pidx + NT));
+            if (r + 1 < sp.rounds) nxt = load16<kLdcg>(p + 16 * (pidx + NT));
             uint32_t c = r == 0 ? (pidx == 0 ? init : 0u) : shift_smem(R, G);
-            if (pidx >= 0) c = crc_step16(c, cur, T);
+            if (pidx >= 0) c = crc_rep16(c, cur, row);
             R = c;
             cur = nxt;
             pidx += NT;
         }
-#pragma unroll
-        for (int k = 0; k < 5; k++) {
-            const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
-            R = shift_by(R, kShPow + 4 + k) ^ right;
-        }
-        if constexpr (NW > 1) {
-            if (lane == 0) s_reg[warp] = R;
-            __syncthreads();
-            if (warp == 0) {
-                R = lane < NW ? s_reg[lane] : 0u;
-#pragma unroll
-                for (int k = 0; (1 << k) < NW; k++) {
-                    const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
-                    R = shift_by(R, kShPow + 9 + k) ^ right;
-                }
-                if (lane == 0) s_reg[0] = R;
-            }
-            __syncthreads();
-            reg = s_reg[0];
-            __syncthreads();
-        } else {
-            reg = __shfl_sync(kFull, R, 0);
-        }
+        reg = crc_fold<NW>(R, 4, s_reg);
     }
-    for (uint64_t i = main; i < len; i++) reg = crc_step1(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), T);
+    for (uint64_t i = main; i < len; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
     return reg;
 }
 
-template <bool kLdcg>
-__device__ inline uint32_t warp_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
-                                        const uint32_t (*G)[256]) {
-    return crc_strided<1, kLdcg>(p, len, init, T, G, nullptr);
-}
-
-template <int NW>
-__device__ inline uint32_t block_crc_raw(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t (*T)[256],
-                                         const uint32_t (*G)[256], uint32_t *s_reg) {
-    return crc_strided<NW, true>(p, len, init, T, G, s_reg);
+// As crc_strided, for a range that need not be 16-byte aligned: the bytes up
+// to the first 16-byte boundary are taken one at a time first.
+template <int NW, bool kLdcg>
+__device__ inline uint32_t crc_any(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
+                                   const uint32_t (*G)[256], uint32_t *s_reg) {
+    uint64_t head = (16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15;
+    if (head > len) head = len;
+    const uint32_t *row = T + (threadIdx.x & 31);
+    uint32_t reg = init;
+    for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
+    return crc_strided<NW, kLdcg>(p + head, len - head, reg, T, G, s_reg);
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() { uint32_t m; asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m)); return m; }
