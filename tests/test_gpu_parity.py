@@ -249,7 +249,7 @@ def test_workload_llama8b_sampled(zco):
             payload, raw_flag = zco.encode_chunk(chunk, 4, 0.95)
             stored = sm & 0x7FFFFFFF
             assert host[off:off + stored] == payload and (sm >> 31) == raw_flag
-            assert crc == zlib.crc32(payload)
+            assert crc == zlib.crc32(chunk.tobytes())   # the chunk's original bytes
         back = zc.decompress(blob)
         assert torch.equal(back.view(torch.int16), t.view(torch.int16))
         del t, blob, back, raw_dev
