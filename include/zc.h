@@ -30,7 +30,7 @@
  *     dtype, ndim, chunk_bytes, lanes = 32, prob_bits = 12, nbytes,
  *     n_chunks, header CRC-32 over header + chunk table, shape[8]); a chunk
  *     table of 16-byte entries {u64 offset, u32 stored | raw << 31, u32
- *     CRC-32 of the stored bytes}; then the chunk payloads, each zero-padded
+ *     CRC-32 of the chunk's original bytes}; then the chunk payloads, each zero-padded
  *     to 16 bytes. All integers little-endian.
  */
 #ifndef ZC_H
@@ -128,10 +128,13 @@ ZC_API int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, 
  *   d_blob       the blob (info->blob_bytes bytes)
  *   d_dst        output, dst_capacity >= info->nbytes, aligned to the
  *                element size
- *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check)
+ *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check, which is
+ *                taken over the bytes the chunk decoded to)
  *   d_status     device int32, OR-ed with ZC_ECRC / ZC_ECORRUPT / ZC_EFORMAT
- * Chunks that fail a check are not written (their output bytes are
- * unspecified). Every device read is bounds-checked against the blob. */
+ * The output bytes of a chunk that fails a check are unspecified; any
+ * nonzero status means the tensor must not be used. Every device read is
+ * bounds-checked against the blob; writes stay within the first
+ * info->nbytes bytes of d_dst. */
 ZC_API int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
                   uint32_t flags, int32_t *d_status, void *stream);
 
