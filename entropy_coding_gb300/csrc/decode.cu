@@ -35,13 +35,6 @@ constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
 // replicated CRC byte table + the gap table of the output pieces + the 496-byte gap table
 constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 struct Rans {
     uint32_t x;          // this lane's state
@@ -149,7 +142,7 @@ __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt)
         cp_async_commit();
         r.next_block--;
         if (r.next_block < 0) cp_async_wait_all();
-        else cp_async_wait1();
+        else cp_async_wait<1>();
         __syncwarp();
     }
     return s;

@@ -1,33 +1,42 @@
-// encode.cu — single-pass compression kernel.
+// encode.cu — compression: a statistics kernel and a coding kernel per wave
+// of chunks (ZipNN note, Method 5: fixed-size chunks coded independently).
 //
-// One CTA compresses one chunk at a time (ZipNN note, Method 5: fixed-size
-// chunks coded independently); CTAs are persistent and take chunk indices
-// from a global ticket counter, so every chunk below a CTA's chunk is already
-// owned by a running CTA. Per chunk:
-//   1. all warps build one 256-bin histogram per byte stream (order-0
-//      statistics, ZipNN note Key insight) of the exponent-extracted words;
-//   2. warp j takes stream j: a constant stream needs no record; otherwise it
-//      quantises the histogram to a 12-bit table, skips the stream if it
-//      provably cannot shrink below the threshold, and else rANS-codes it
-//      (32 interleaved lanes) into the CTA's workspace slot;
-//   3. warp 0 applies the passthrough rule per stream and per chunk (cuZipNN
-//      API, passthrough_threshold), publishes the chunk's padded size and
-//      finds its blob offset with a decoupled look-back over the chunks
-//      before it (an exclusive prefix scan of the metadata map, ZipNN note
-//      Method 5);
-//   4. all warps write the payload: the directory, the raw streams (one pass
-//      over the input for all of them), the coded records; then compute its
-//      CRC-32 together and write the chunk table entry.
-// The last CTA to finish writes the header and its CRC.
+// stats_kernel, one CTA per chunk (persistent CTAs, grid-stride over the
+// wave): one pass over the chunk's bytes builds the 256-bin histogram of
+// every byte stream of the exponent-extracted words (order-0 statistics,
+// ZipNN note Key insight) and the CRC-32 of the chunk's original bytes. Then
+// warp j takes stream j: a stream with one symbol is CONST; otherwise its
+// histogram is quantised to the 12-bit table, and the stream is RAW if its
+// coded size provably cannot come below the threshold, else a candidate
+// whose table goes to the workspace.
+//
+// code_kernel, one warp per chunk (persistent warps taking chunk tickets in
+// order): rANS-codes the candidate streams (32 interleaved lanes) into the
+// warp's workspace slot, applies the passthrough rule per stream and per
+// chunk (cuZipNN API, passthrough_threshold), finds the chunk's blob offset
+// with a decoupled look-back over the chunks before it (an exclusive prefix
+// scan of the metadata map, ZipNN note Method 5), and writes the payload and
+// the chunk table entry. The last warp to finish writes the header and its
+// CRC.
+//
+// The serial part of rANS coding (each lane's state runs through the whole
+// stream) stays on single warps that never wait at a CTA barrier, so an SM
+// keeps many such chains in flight, while the histogram pass, which is bound
+// by shared-memory traffic, runs on whole CTAs with per-lane counter copies.
 #include "zc_kernels.cuh"
 
 namespace zc {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSM = 3;
+constexpr int kStatWarps = 16;
+constexpr int kStatThreads = 32 * kStatWarps;
+constexpr uint32_t kPiece = 128;  // bytes per thread per round of the statistics pass
+constexpr int kCodeWarps = 16;    // coding warps per CTA, one CTA per SM
+constexpr int kCodeThreads = 32 * kCodeWarps;
+constexpr uint32_t kModeCand = 3;  // statistics -> coder only: a stream to rANS-code
+constexpr uint32_t kAborted = 0xFFFFFFFFu;
+constexpr uint32_t kCodeWarpSmem = 4096 + 4096 + 2048;  // per coding warp: rANS table, symbol ring, word stage
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
@@ -116,74 +125,6 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
         if (lane >= o) inc += t;
     }
     return inc - v;
-}
-
-// Histogram of the W byte streams of one chunk into h[W][256], by the CTA,
-// and the raw CRC register of the chunk's bytes (the chunk table's check of
-// the original data) from the same loads: the 16-byte pieces are dealt to
-// the threads as in crc_strided, so each thread's register only needs the
-// gap shift between its pieces. Returns the raw register in every thread.
-template <int DT>
-__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, uint32_t (*h)[256], const uint32_t *crc_rep,
-                                const uint32_t (*gap)[256], uint32_t *s_reg) {
-    constexpr int W = WordOf<DT>::W;
-    const int tid = threadIdx.x;
-    const uint32_t *row = crc_rep + (tid & 31);
-    for (int i = tid; i < W * 256; i += kThreads) h[i >> 8][i & 255] = 0;
-    __syncthreads();
-    auto count = [&](uint32_t w) {
-        const uint32_t p = Perm<DT>::fwd(w);
-#pragma unroll
-        for (int j = 0; j < W; j++) atomicAdd(&h[j][stream_byte<W>(p, j)], 1u);
-    };
-    uint32_t reg;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-        const uint32_t main = len & ~15u;
-        const Strided sp(main, kThreads);
-        uint32_t R = 0;
-        int64_t pidx = int64_t(tid) - int64_t(sp.v0);
-        constexpr int U = 4;  // pieces in flight per thread
-        for (uint64_t r0 = 0; r0 < sp.rounds; r0 += U) {
-            uint4 q[U];
-#pragma unroll
-            for (int u = 0; u < U; u++) {
-                const int64_t pi = pidx + int64_t(u) * kThreads;
-                q[u] = (r0 + u < sp.rounds && pi >= 0) ? __ldg(reinterpret_cast<const uint4 *>(src) + pi)
-                                                      : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; u++) {
-                if (r0 + u >= sp.rounds) break;
-                const int64_t pi = pidx + int64_t(u) * kThreads;
-                uint32_t c = (r0 + u == 0) ? (pi == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, gap);
-                if (pi >= 0) {
-                    c = crc_rep16(c, q[u], row);
-                    const uint32_t uu[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-                    for (int k = 0; k < 4; k++)
-#pragma unroll
-                        for (int e = 0; e < 4 / W; e++)
-                            count(W == 4 ? uu[k] : (uu[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u));
-                }
-                R = c;
-            }
-            pidx += int64_t(U) * kThreads;
-        }
-        reg = sp.pieces ? crc_fold<kWarps>(R, 4, s_reg) : 0xFFFFFFFFu;
-        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, __ldg(src + i), row);
-        for (uint32_t i = main / W + tid; i < len / W; i += kThreads) count(load_word<W>(src + uint64_t(i) * W));
-    } else {
-        // unaligned input: words one at a time; the CRC takes the bytes up to
-        // the first 16-byte boundary one by one, then the aligned rest
-        for (uint32_t i = tid; i < len / W; i += kThreads) count(load_word<W>(src + uint64_t(i) * W));
-        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15);
-        if (head > len) head = len;
-        uint32_t c = 0xFFFFFFFFu;
-        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, __ldg(src + i), row);
-        reg = crc_strided<kWarps, false>(src + head, len - head, c, crc_rep, gap, s_reg);
-    }
-    __syncthreads();
-    return reg;
 }
 
 // 12-bit table from counts held as 8 bins per lane (symbol 8*lane + k).
@@ -278,125 +219,119 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
     return excl;
 }
 
-// Code stream J of the chunk into rec (the workspace record area), one warp.
-// Returns the record's unpadded size. f holds the lane's 8 table entries.
-// Per symbol the table keeps {m, a, 2^20 f, (4096 - f) | cum << 13 | (k-32) << 25}
-// so that a step is: renormalise if x >= 2^20 f, q = (x m + a) >> k,
-// x += q (4096 - f) + cum.
-template <int DT, int J>
-__device__ uint32_t rans_encode_stream(const uint8_t *src, uint32_t n, const uint32_t f[8], uint4 *etab, uint8_t *rec) {
-    constexpr int W = WordOf<DT>::W;
-    const int lane = threadIdx.x & 31;
-    uint32_t present = 0, fsum = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        present += f[k] ? 1u : 0u;
-        fsum += f[k];
-    }
-    uint32_t rank = warp_excl_scan(present);
-    uint32_t cum = warp_excl_scan(fsum);
-    const uint32_t k_total = __shfl_sync(kFull, rank + present, 31);
-    uint32_t bits = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const uint32_t s = 8 * lane + k, fs = f[k];
-        if (fs) {
-            bits |= 1u << k;
-            reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
-            const uint32_t ka = kRecip.ka[fs], m = kRecip.m[fs];
-            etab[s] = make_uint4(m, (ka >> 8) ? m : 0u, fs << 20, (kM - fs) | (cum << 13) | (((ka & 0xFFu) - 32) << 25));
-        }
-        cum += fs;
-    }
-    rec[128 + lane] = uint8_t(bits);
-    const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
-    for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
-    __syncwarp();
+// ---------------------------------------------------------------- statistics
 
-    uint16_t *wout = reinterpret_cast<uint16_t *>(rec + words_at);
-    const uint32_t gt = lanemask_gt();
-    uint32_t x = kRansL;
-    uint32_t wc = 0;
-    const int T = int((n + 31) / 32);
-
-    auto sym_of = [&](uint32_t word) { return stream_byte<W>(Perm<DT>::fwd(word), J); };
-    auto step = [&](const uint4 &e, bool active) {
-        const bool emit = active && x >= e.z;
-        const uint32_t bal = __ballot_sync(kFull, emit);
-        // the store reads its own copy of x, so updating x need not wait for it
-        uint32_t wv;
-        asm volatile("mov.b32 %0, %1;" : "=r"(wv) : "r"(x));
-        const uint32_t pos = wc + __popc(bal & gt);
-        if (emit) wout[pos] = uint16_t(wv);
-        x = emit ? x >> 16 : x;
-        wc += __popc(bal);
-        const uint32_t q = uint32_t((uint64_t(x) * e.x + e.y) >> 32) >> ((e.w >> 25) & 0xFu);
-        const uint32_t xn = x + q * (e.w & 0x1FFFu) + ((e.w >> 13) & 0xFFFu);
-        if (active) x = xn;
-    };
-
-    // the last step first (the only one that may be partial)
-    {
-        const uint32_t i = uint32_t(T - 1) * 32 + lane;
-        const bool active = i < n;
-        step(etab[sym_of(active ? load_word<W>(src + uint64_t(i) * W) : 0u)], active);
-    }
-    // then the full steps T-2 .. 0, 16 at a time with the next 16 words in
-    // flight; each step's table entry is read one step ahead
-    constexpr int B = 16;
-    uint32_t buf[B];
-#pragma unroll
-    for (int k = 0; k < B; k++) {
-        const int t = T - 2 - k;
-        buf[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
-    }
-    uint4 e_next = etab[sym_of(buf[0])];
-    for (int t0 = T - 2; t0 >= 0; t0 -= B) {
-        uint32_t nxt[B];
-#pragma unroll
-        for (int k = 0; k < B; k++) {
-            const int t = t0 - B - k;
-            nxt[k] = t >= 0 ? load_word<W>(src + (uint64_t(t) * 32 + lane) * W) : 0u;
-        }
-        const bool full = t0 >= B - 1;
-#pragma unroll
-        for (int k = 0; k < B; k++) {
-            const uint4 e = e_next;
-            e_next = etab[sym_of(k + 1 < B ? buf[k + 1] : nxt[0])];
-            if (full || t0 - k >= 0) step(e, true);
-        }
-#pragma unroll
-        for (int k = 0; k < B; k++) buf[k] = nxt[k];
-    }
-    reinterpret_cast<uint32_t *>(rec)[lane] = x;
-    const uint32_t rec_bytes = words_at + 2 * wc;
-    for (uint32_t b = rec_bytes + lane; b < pad16(rec_bytes); b += 32) rec[b] = 0;
-    __syncwarp();
-    return rec_bytes;
-}
-
-struct Plan {
-    uint32_t mode[4];
-    uint32_t val[4];   // RAW: n, RANS: record bytes, CONST: symbol
-    uint32_t roff[4];  // record offset within the payload
-    uint64_t off;      // payload offset in the blob
-    uint64_t stored;
-    uint32_t raw_chunk;
-    uint32_t write;    // 0 when the chunk is not placed (capacity or timeout)
-    uint32_t c;
-    uint32_t crc;      // CRC-32 of the chunk's original bytes
-    uint32_t crc_reg[kWarps];
+// Shared memory of a statistics CTA. The histogram of stream j keeps one copy
+// per lane index: word (b >> 1) * 32 + lane holds the 16-bit counts of bins
+// b & ~1 (low half) and b | 1 (high half), so the 32 lanes of a warp always
+// add into 32 different banks. A copy sees at most about n / 32 counts of one
+// stream (each thread's pieces hold at most 1/512 of the chunk plus one
+// piece, 16 threads share a copy), far below 2^16.
+template <int W>
+struct StatsSmem {
+    uint32_t crc_rep[kCrcRepWords];  // replicated CRC byte table (32 KB)
+    uint32_t gap[4][256];            // register shift over the other threads' pieces
+    uint32_t hist[W][128 * 32];
+    uint32_t s_reg[kStatWarps];
+    uint32_t sv[4];
 };
 
-// Per-stream decision, by warp j for stream j.
-template <int DT, int J>
-__device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n, const uint32_t (*h)[256],
-                            uint4 *etab, uint8_t *rec, Plan &pl) {
-    constexpr int j = J;
-    const int lane = threadIdx.x & 31;
-    uint32_t cnt[8];
+template <int DT>
+__device__ __forceinline__ void count_elem(uint32_t w, uint32_t (*h)[128 * 32], int lane) {
+    constexpr int W = WordOf<DT>::W;
+    const uint32_t p = Perm<DT>::fwd(w);
 #pragma unroll
-    for (int k = 0; k < 8; k++) cnt[k] = h[j][8 * lane + k];
+    for (int j = 0; j < W; j++) {
+        const uint32_t b = stream_byte<W>(p, j);
+        atomicAdd(&h[j][(b >> 1) * 32 + lane], 1u << ((b & 1u) << 4));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void count_vec(const uint4 &q, uint32_t (*h)[128 * 32], int lane) {
+    constexpr int W = WordOf<DT>::W;
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+#pragma unroll
+        for (int e = 0; e < 4 / W; e++)
+            count_elem<DT>(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u), h, lane);
+}
+
+// Histograms of the chunk's W byte streams and the raw CRC register of its
+// bytes, by the CTA from one pass. Aligned input: the threads take 128-byte
+// pieces round-robin, aligned to the end of the chunk (see Strided; only the
+// first round can be short), so each thread's register needs one gap shift
+// per round. Returns the raw register in every thread.
+template <int DT>
+__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm) {
+    constexpr int W = WordOf<DT>::W;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t *row = sm.crc_rep + lane;
+    uint32_t reg;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint32_t main = len & ~(kPiece - 1);
+        const uint32_t pieces = main / kPiece;
+        const uint32_t rounds = (pieces + kStatThreads - 1) / kStatThreads;
+        int32_t pidx = tid - int32_t(rounds * kStatThreads - pieces);
+        uint32_t R = 0;
+        for (uint32_t r = 0; r < rounds; r++, pidx += kStatThreads) {
+            uint32_t c = r == 0 ? (pidx == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, sm.gap);
+            if (pidx >= 0) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx) * kPiece);
+                uint4 q[kPiece / 16];
+#pragma unroll
+                for (int u = 0; u < int(kPiece / 16); u++) q[u] = __ldg(p + u);
+#pragma unroll
+                for (int u = 0; u < int(kPiece / 16); u++) {
+                    c = crc_rep16(c, q[u], row);
+                    count_vec<DT>(q[u], sm.hist, lane);
+                }
+            }
+            R = c;
+        }
+        reg = pieces ? crc_fold<kStatWarps>(R, 7, sm.s_reg) : 0xFFFFFFFFu;
+        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, __ldg(src + i), row);
+        for (uint32_t i = main / W + tid; i < len / W; i += kStatThreads)
+            count_elem<DT>(load_word<W>(src + uint64_t(i) * W), sm.hist, lane);
+    } else {
+        // input aligned to its element size only: words one at a time; the
+        // CRC takes the bytes up to the first 16-byte boundary one by one,
+        // then the aligned rest with 16-byte pieces (gap table for 4080)
+        for (uint32_t i = tid; i < len / W; i += kStatThreads)
+            count_elem<DT>(load_word<W>(src + uint64_t(i) * W), sm.hist, lane);
+        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15);
+        if (head > len) head = len;
+        uint32_t c = 0xFFFFFFFFu;
+        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, __ldg(src + i), row);
+        reg = crc_strided<kStatWarps, false>(src + head, len - head, c, sm.crc_rep, sm.gap, sm.s_reg);
+    }
+    return reg;
+}
+
+// Stream j's decision after the histogram pass, by one warp: the 32 counter
+// copies are summed (and zeroed for the next chunk) into 8 bins per lane
+// (symbol 8 lane + k), then CONST / RAW / candidate. A candidate's 12-bit
+// table goes to ftab (256 u16).
+template <int W>
+__device__ void plan_stats(const EncodeArgs &a, uint32_t n, uint32_t *h, uint32_t *sv, uint32_t *sv_smem,
+                           uint8_t *ftab) {
+    const int lane = threadIdx.x & 31;
+    uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int L = 0; L < 32; L++) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t *cell = h + (4 * L + q) * 32 + lane;
+            const uint32_t v = *cell;
+            *cell = 0;
+            const uint32_t lo = __reduce_add_sync(kFull, v & 0xFFFFu);
+            const uint32_t hi = __reduce_add_sync(kFull, v >> 16);
+            if (lane == L) {
+                cnt[2 * q] = lo;
+                cnt[2 * q + 1] = hi;
+            }
+        }
+    }
     uint32_t pres = 0, only = 0;
 #pragma unroll
     for (int k = 0; k < 8; k++)
@@ -428,180 +363,429 @@ __device__ void plan_stream(const EncodeArgs &a, const uint8_t *src, uint32_t n,
         mode = kModeRaw;
         val = n;
         if (double(rec_lb) < a.threshold * double(n)) {
-            const uint32_t rb = rans_encode_stream<DT, J>(src, n, f, etab, rec);
-            if (double(rb) < a.threshold * double(n)) {
-                mode = kModeRans;
-                val = rb;
-            }
+            mode = kModeCand;
+            val = 0;
+            uint4 v;
+            v.x = f[0] | f[1] << 16;
+            v.y = f[2] | f[3] << 16;
+            v.z = f[4] | f[5] << 16;
+            v.w = f[6] | f[7] << 16;
+            reinterpret_cast<uint4 *>(ftab)[lane] = v;
         }
     }
     if (lane == 0) {
-        pl.mode[j] = mode;
-        pl.val[j] = val;
+        *sv = (mode << 30) | val;
+        *sv_smem = (mode << 30) | val;
     }
 }
 
-// All raw streams of a grouped chunk in one pass over the input: each thread
-// takes 16 consecutive elements and writes 16 bytes to every raw stream.
+// The bytes of every candidate stream of the chunk, in element order, into
+// cand + j * n_pad (a second pass over the chunk, which is in L2 by now).
 template <int DT>
-__device__ void write_raw_streams(const uint8_t *src, uint32_t n, const Plan &pl, uint8_t *out) {
+__device__ void write_cand(const uint8_t *src, uint32_t len, uint32_t candmask, uint8_t *cand, uint64_t n_pad) {
     constexpr int W = WordOf<DT>::W;
+    constexpr int E = 16 / W;  // elements per 16-byte vector
+    const int tid = threadIdx.x;
+    const uint32_t n = len / W;
+    uint32_t done = 0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint32_t nvec = len / 16;
+        for (uint32_t v = tid; v < nvec; v += kStatThreads) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+            uint32_t p[E];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+#pragma unroll
+                for (int e = 0; e < 4 / W; e++)
+                    p[k * (4 / W) + e] = Perm<DT>::fwd(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u));
+#pragma unroll
+            for (int j = 0; j < W; j++) {
+                if (!((candmask >> j) & 1u)) continue;
+                uint32_t o[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int e = 0; e < E; e++) o[e >> 2] |= stream_byte<W>(p[e], j) << (8 * (e & 3));
+                uint8_t *d = cand + uint64_t(j) * n_pad + uint64_t(v) * E;
+                if (E == 4) *reinterpret_cast<uint32_t *>(d) = o[0];
+                else if (E == 8) *reinterpret_cast<uint2 *>(d) = make_uint2(o[0], o[1]);
+                else *reinterpret_cast<uint4 *>(d) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        done = nvec * E;
+    }
+    for (uint32_t i = done + tid; i < n; i += kStatThreads) {
+        const uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
+#pragma unroll
+        for (int j = 0; j < W; j++)
+            if ((candmask >> j) & 1u) cand[uint64_t(j) * n_pad + i] = uint8_t(stream_byte<W>(p, j));
+    }
+}
+
+// One CTA per chunk of the wave (grid-stride). Writes per chunk 32 bytes of
+// info {CRC-32 of the original bytes, W stream words mode << 30 | value} and
+// the tables of the candidate streams.
+template <int DT>
+__global__ void __launch_bounds__(kStatThreads) stats_kernel(EncodeArgs a) {
+    constexpr int W = WordOf<DT>::W;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    StatsSmem<W> &sm = *reinterpret_cast<StatsSmem<W> *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    load_crc_rep(sm.crc_rep);
+    load_shift_smem(sm.gap, (reinterpret_cast<uintptr_t>(a.src) & 15) == 0 ? kSh65408 : gap_table<kStatThreads>());
+    for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
+    __syncthreads();
+    for (uint32_t cl = blockIdx.x; cl < a.wave_n; cl += gridDim.x) {
+        const uint64_t c = uint64_t(a.wave_start) + cl;
+        const uint8_t *src = a.src + c * a.chunk_bytes;
+        const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - c * a.chunk_bytes));
+        const uint32_t reg = chunk_stats<DT>(src, len, sm);
+        __syncthreads();
+        uint32_t *info = reinterpret_cast<uint32_t *>(a.ws_info + 32ull * cl);
+        if (warp < W)
+            plan_stats<W>(a, len / W, sm.hist[warp], info + 1 + warp, &sm.sv[warp],
+                          a.ws_ftab + (uint64_t(cl) * W + warp) * 512);
+        if (tid == 0) info[0] = reg ^ 0xFFFFFFFFu;
+        __syncthreads();
+        uint32_t candmask = 0;
+#pragma unroll
+        for (int j = 0; j < W; j++)
+            if ((sm.sv[j] >> 30) == kModeCand) candmask |= 1u << j;
+        if (candmask) write_cand<DT>(src, len, candmask, a.ws_cand + uint64_t(cl) * W * a.n_pad, a.n_pad);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- coding
+
+// Code one stream of the chunk into rec (the warp's slot), one warp, with the
+// 12-bit table f (8 entries per lane) and the stream's bytes in cand (element
+// order, padded to whole steps). Per symbol the table keeps
+// {m, a, 2^20 f, (4096 - f) | cum << 13 | (k-32) << 25} (bits 29-31 zero) so
+// that a step is:
+// renormalise if x >= 2^20 f, q = (x m + a) >> k, x += q (4096 - f) + cum.
+// The steps run in blocks of 32 (the last steps of the stream first); the
+// symbols of the next three blocks are in flight into a shared-memory ring
+// (row s of a block = the 32 symbols of its step s). A step stages the low
+// 16 bits of its state in shared memory and keeps one flag bit; after the block the
+// words of the emitting lanes are written out step by step (lanes 31..0
+// within a step), which keeps the word stores off the state's dependency
+// chain. Returns the record's unpadded size, or kAborted once the record has
+// reached lim bytes (it can then no longer be kept: the stream is stored raw).
+__device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint4 *etab,
+                                       uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim) {
+    const int lane = threadIdx.x & 31;
+    uint16_t *stage = stage_base + lane;  // step s of a block: stage[32 s]
+    const int T = int((n + 31) / 32);
+    const int nb = (T + 31) / 32;
+    // block b holds steps t = T-1-32b-s (s = 0..31); lane l fetches row l
+    auto issue = [&](int b) {
+        if (b < nb) {
+            const int t = T - 1 - 32 * b - lane;
+            if (t >= 0) {
+                uint8_t *d = ring + (b & 3) * 1024 + lane * 32;
+                cp_async16(d, cand + uint64_t(t) * 32);
+                cp_async16(d + 16, cand + uint64_t(t) * 32 + 16);
+            }
+        }
+        cp_async_commit();
+    };
+    issue(0);
+    issue(1);
+    issue(2);
+
+    uint32_t present = 0, fsum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        present += f[k] ? 1u : 0u;
+        fsum += f[k];
+    }
+    uint32_t rank = warp_excl_scan(present);
+    uint32_t cum = warp_excl_scan(fsum);
+    const uint32_t k_total = __shfl_sync(kFull, rank + present, 31);
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const uint32_t s = 8 * lane + k, fs = f[k];
+        if (fs) {
+            bits |= 1u << k;
+            reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
+            const uint32_t ka = kRecip.ka[fs], m = kRecip.m[fs];
+            etab[s] = make_uint4(m, (ka >> 8) ? m : 0u, fs << 20, (kM - fs) | (cum << 13) | (((ka & 0xFFu) - 32) << 25));
+        }
+        cum += fs;
+    }
+    rec[128 + lane] = uint8_t(bits);
+    const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
+    for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
+
+    uint16_t *wout = reinterpret_cast<uint16_t *>(rec + words_at);
+    const uint32_t gt = lanemask_gt();
+    uint32_t x = kRansL;
+    uint32_t wc = 0;
+    const bool first_active = uint32_t(T - 1) * 32 + lane < n;
+    bool aborted = false;
+    for (int b = 0; b < nb; b++) {
+        issue(b + 3);
+        cp_async_wait<3>();
+        __syncwarp();
+        const uint8_t *blk = ring + (b & 3) * 1024 + lane;
+        const int cnt = min(32, T - 32 * b);
+        uint32_t flags = 0;
+        int s = 0;
+        if (b == 0) {
+            // step T-1, the only one that may be partial; no lane emits a word
+            // there (x = 2^16 is below every 2^20 f)
+            const uint4 ec = etab[blk[0]];
+            const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+            if (first_active) x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+            s = 1;
+        }
+        // rows past the block read the next ring slot (or the stage after the
+        // last slot): harmless values that are never used
+        uint32_t sym_n = blk[(s + 1) * 32];
+        uint4 e = etab[blk[s * 32]];
+#pragma unroll 4
+        for (; s < cnt; s++) {
+            const uint4 ec = e;
+            e = etab[sym_n];
+            sym_n = blk[(s + 2) * 32];
+            const bool emit = x >= ec.z;
+            stage[s * 32] = uint16_t(x);
+            if (emit) flags |= 1u << s;
+            x = emit ? x >> 16 : x;
+            const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+            x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+        }
+#pragma unroll 4
+        for (int s = 0; s < cnt; s++) {
+            const bool em = (flags >> s) & 1u;
+            const uint32_t B = __ballot_sync(kFull, em);
+            if (em) wout[wc + __popc(B & gt)] = stage[s * 32];
+            wc += __popc(B);
+        }
+        __syncwarp();
+        if (words_at + 2ull * wc >= lim) {
+            aborted = true;
+            break;
+        }
+    }
+    cp_async_wait_all();  // the ring is reused by the next stream
+    __syncwarp();
+    if (aborted) return kAborted;
+    reinterpret_cast<uint32_t *>(rec)[lane] = x;
+    const uint32_t rec_bytes = words_at + 2 * wc;
+    for (uint32_t b = rec_bytes + lane; b < pad16(rec_bytes); b += 32) rec[b] = 0;
+    __syncwarp();
+    return rec_bytes;
+}
+
+// All raw streams of a grouped chunk in one pass over the input, by the
+// warp: a lane takes 16 consecutive elements at a time (G groups, 8 vectors
+// in flight) and writes 16 bytes to every raw stream, gathering byte j (from
+// the top) of four elements into a word with two byte permutes and a merge.
+template <int DT>
+__device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t mode[4], const uint32_t roff[4],
+                                 uint8_t *out) {
+    constexpr int W = WordOf<DT>::W;
+    constexpr int G = 8 / W;
+    const int lane = threadIdx.x & 31;
     bool any = false;
 #pragma unroll
-    for (int j = 0; j < W; j++) any |= pl.mode[j] == kModeRaw;
+    for (int j = 0; j < W; j++) any |= mode[j] == kModeRaw;
     if (!any) return;
     const uint32_t groups = (n + 15) / 16;
     const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-    for (uint32_t g = threadIdx.x; g < groups; g += kThreads) {
-        uint32_t wd[16];
-        if (vec && 16 * (g + 1) <= n) {
+    for (uint32_t g0 = lane; g0 < groups; g0 += 32 * G) {
+        uint4 qv[G][W];
 #pragma unroll
-            for (int v = 0; v < W; v++) {
-                uint4 q = __ldcs(reinterpret_cast<const uint4 *>(src + uint64_t(g) * 16 * W) + v);
-                uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        for (int gi = 0; gi < G; gi++) {
+            const uint32_t g = g0 + 32 * gi;
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-#pragma unroll
-                    for (int e = 0; e < 4 / W; e++)
-                        wd[(v * 4 + k) * (4 / W) + e] =
-                            (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; k++) {
-                uint32_t i = g * 16 + k;
-                wd[k] = i < n ? load_word<W>(src + uint64_t(i) * W) : 0u;
-            }
+            for (int v = 0; v < W; v++)
+                qv[gi][v] = (vec && 16 * (g + 1) <= n)
+                                ? __ldcs(reinterpret_cast<const uint4 *>(src + uint64_t(g) * 16 * W) + v)
+                                : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int k = 0; k < 16; k++) wd[k] = Perm<DT>::fwd(wd[k]);
+        for (int gi = 0; gi < G; gi++) {
+            const uint32_t g = g0 + 32 * gi;
+            if (g >= groups) break;
+            uint32_t wd[16];
+            if (vec && 16 * (g + 1) <= n) {
 #pragma unroll
-        for (int j = 0; j < W; j++) {
-            if (pl.mode[j] != kModeRaw) continue;
-            uint32_t b[16];
+                for (int v = 0; v < W; v++) {
+                    const uint32_t u[4] = {qv[gi][v].x, qv[gi][v].y, qv[gi][v].z, qv[gi][v].w};
 #pragma unroll
-            for (int k = 0; k < 16; k++) b[k] = (g * 16 + k < n) ? stream_byte<W>(wd[k], j) : 0u;
-            uint4 v;
-            v.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-            v.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-            v.z = b[8] | (b[9] << 8) | (b[10] << 16) | (b[11] << 24);
-            v.w = b[12] | (b[13] << 8) | (b[14] << 16) | (b[15] << 24);
-            reinterpret_cast<uint4 *>(out + pl.roff[j])[g] = v;
+                    for (int k = 0; k < 4; k++)
+#pragma unroll
+                        for (int e = 0; e < 4 / W; e++)
+                            wd[(v * 4 + k) * (4 / W) + e] =
+                                (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; k++) {
+                    const uint32_t i = g * 16 + k;
+                    wd[k] = i < n ? load_word<W>(src + uint64_t(i) * W) : 0u;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 16; k++) wd[k] = Perm<DT>::fwd(wd[k]);
+#pragma unroll
+            for (int j = 0; j < W; j++) {
+                if (mode[j] != kModeRaw) continue;
+                const uint32_t bj = uint32_t(W - 1 - j);        // byte of stream j in a permuted element
+                const uint32_t sel = bj | (4 + bj) << 4;         // [x.bj, y.bj, -, -]
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint32_t lo = __byte_perm(wd[4 * q], wd[4 * q + 1], sel);
+                    const uint32_t hi = __byte_perm(wd[4 * q + 2], wd[4 * q + 3], sel);
+                    o[q] = __byte_perm(lo, hi, 0x5410);
+                }
+                // elements past n contribute zero bytes
+                if (16 * (g + 1) > n) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+#pragma unroll
+                        for (int r = 0; r < 4; r++)
+                            if (g * 16 + 4 * q + r >= n) o[q] &= ~(0xFFu << (8 * r));
+                }
+                reinterpret_cast<uint4 *>(out + roff[j])[g] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
     }
 }
 
-// Copy len bytes (zero-padded to 16) by the CTA; dst is 16-aligned.
-__device__ void block_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
+// Copy len bytes (zero-padded to 16) by the warp, 8 vectors in flight per
+// lane; dst is 16-aligned.
+__device__ void warp_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
+    const int lane = threadIdx.x & 31;
     const uint64_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    for (uint64_t v = threadIdx.x; v < nvec; v += kThreads)
-        reinterpret_cast<uint4 *>(dst)[v] = __ldcs(reinterpret_cast<const uint4 *>(src) + v);
-    for (uint64_t i = nvec * 16 + threadIdx.x; i < pad16(len); i += kThreads) dst[i] = i < len ? src[i] : 0;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    constexpr int U = 8;
+    for (uint64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            if (v0 + 32 * u < nvec) t[u] = __ldcs(s4 + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            if (v0 + 32 * u < nvec) d4[v0 + 32 * u] = t[u];
+    }
+    for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? src[i] : 0;
 }
 
-// Dynamic shared memory of the compression CTA.
-template <int W>
-struct EncodeSmem {
-    uint32_t crc_rep[kCrcRepWords];  // replicated CRC byte table (32 KB)
-    uint32_t gap[4][256];            // register shift over the other threads' pieces
-    uint32_t hist[W][256];
-    uint4 etab[W][256];
-    Plan pl;
-};
+template <int DT, int J>
+__device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, uint32_t n, uint64_t lim, uint4 *etab,
+                                            uint8_t *ring, uint8_t *slot, uint32_t mode[4], uint32_t val[4]) {
+    constexpr int W = WordOf<DT>::W;
+    if (mode[J] != kModeCand) return;
+    const int lane = threadIdx.x & 31;
+    const uint4 fv = reinterpret_cast<const uint4 *>(a.ws_ftab + (uint64_t(cl) * W + J) * 512)[lane];
+    const uint32_t f[8] = {fv.x & 0xFFFFu, fv.x >> 16, fv.y & 0xFFFFu, fv.y >> 16,
+                           fv.z & 0xFFFFu, fv.z >> 16, fv.w & 0xFFFFu, fv.w >> 16};
+    const uint8_t *cand = a.ws_cand + (uint64_t(cl) * W + J) * a.n_pad;
+    const uint32_t rb = rans_encode_stream(cand, n, f, etab, ring, reinterpret_cast<uint16_t *>(ring + 4096),
+                                           slot + uint64_t(J) * a.rec_stride, lim);
+    if (rb != kAborted && rb < lim) {
+        mode[J] = kModeRans;
+        val[J] = rb;
+    } else {
+        mode[J] = kModeRaw;
+        val[J] = n;
+    }
+}
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    EncodeSmem<W> &sm = *reinterpret_cast<EncodeSmem<W> *>(smem_raw);
-    Plan &pl = sm.pl;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    load_crc_rep(sm.crc_rep);
-    load_shift_smem(sm.gap, gap_table<kThreads>());
-    const uint32_t *row = sm.crc_rep + lane;
-
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t gw = blockIdx.x * kCodeWarps + warp;
+    if (gw >= a.workers) return;
+    uint4 *etab = reinterpret_cast<uint4 *>(smem_raw + kCodeWarpSmem * warp);
+    uint8_t *ring = smem_raw + kCodeWarpSmem * warp + 4096;
+    uint8_t *slot = a.ws_slots + uint64_t(gw) * a.slot_bytes;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
-    uint8_t *slot = a.ws_slots + uint64_t(blockIdx.x) * a.slot_bytes;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
-    const uint64_t rec_stride = pad16(kRecHead + kMaxTable + 2ull * (a.chunk_bytes / W));
 
     for (;;) {
-        if (tid == 0) pl.c = atomicAdd(&ctrl[0], 1u);
-        __syncthreads();
-        const uint32_t c = pl.c;
-        if (c >= a.n_chunks) break;
+        uint32_t cl = 0;
+        if (lane == 0) cl = atomicAdd(&ctrl[0], 1u);
+        cl = __shfl_sync(kFull, cl, 0);
+        if (cl >= a.wave_n) break;
+        const uint32_t c = a.wave_start + cl;
         const uint8_t *src = a.src + uint64_t(c) * a.chunk_bytes;
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
-
-        const uint32_t crc = chunk_stats<DT>(src, len, sm.hist, sm.crc_rep, sm.gap, pl.crc_reg) ^ 0xFFFFFFFFu;
-
-        if (warp == 0) plan_stream<DT, 0>(a, src, n, sm.hist, sm.etab[0], slot, pl);
-        if constexpr (W > 1) {
-            if (warp == 1) plan_stream<DT, 1>(a, src, n, sm.hist, sm.etab[1], slot + rec_stride, pl);
+        const uint32_t *info = reinterpret_cast<const uint32_t *>(a.ws_info + 32ull * cl);
+        const uint32_t crc = info[0];
+        uint32_t mode[4] = {0, 0, 0, 0}, val[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            const uint32_t sv = info[1 + j];
+            mode[j] = sv >> 30;
+            val[j] = sv & 0x3FFFFFFFu;
         }
+        // a record is kept iff its size is below threshold x n, i.e. below lim
+        const uint64_t lim = uint64_t(ceil(a.threshold * double(n)));
+        code_stream<DT, 0>(a, cl, n, lim, etab, ring, slot, mode, val);
+        if constexpr (W > 1) code_stream<DT, 1>(a, cl, n, lim, etab, ring, slot, mode, val);
         if constexpr (W > 2) {
-            if (warp == 2) plan_stream<DT, 2>(a, src, n, sm.hist, sm.etab[2], slot + 2 * rec_stride, pl);
-            if (warp == 3) plan_stream<DT, 3>(a, src, n, sm.hist, sm.etab[3], slot + 3 * rec_stride, pl);
+            code_stream<DT, 2>(a, cl, n, lim, etab, ring, slot, mode, val);
+            code_stream<DT, 3>(a, cl, n, lim, etab, ring, slot, mode, val);
         }
-        __syncthreads();
 
-        if (warp == 0) {
-            uint64_t grouped = 16;  // pad16(4W) for W <= 4
-            uint32_t roff[4] = {0, 0, 0, 0};
+        uint64_t grouped = 16;  // pad16(4W) for W <= 4
+        uint32_t roff[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int j = 0; j < W; j++) {
-                roff[j] = uint32_t(grouped);
-                if (pl.mode[j] != kModeConst) grouped += pad16(pl.val[j]);
-            }
-            const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
-            const uint64_t stored = raw_chunk ? len : grouped;
-            bool timed;
-            const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status, &timed);
-            const bool fits = off + pad16(stored) <= a.cap;
-            if (lane == 0) {
-#pragma unroll
-                for (int j = 0; j < W; j++) pl.roff[j] = roff[j];
-                pl.off = off;
-                pl.stored = stored;
-                pl.raw_chunk = raw_chunk;
-                pl.write = fits && !timed;
-                if (!fits) status_or(a.d_status, ZC_ECAPACITY);
-            }
+        for (int j = 0; j < W; j++) {
+            roff[j] = uint32_t(grouped);
+            if (mode[j] != kModeConst) grouped += pad16(val[j]);
         }
-        __syncthreads();
+        const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
+        const uint64_t stored = raw_chunk ? len : grouped;
+        bool timed;
+        const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status, &timed);
+        const bool fits = off + pad16(stored) <= a.cap;
+        if (!fits && lane == 0) status_or(a.d_status, ZC_ECAPACITY);
 
-        if (pl.write) {
-            uint8_t *out = a.blob + pl.off;
-            if (pl.raw_chunk) {
-                block_copy(src, len, out);
+        if (fits && !timed) {
+            uint8_t *out = a.blob + off;
+            if (raw_chunk) {
+                warp_copy(src, len, out);
             } else {
-                if (tid < 4) {
+                if (lane < 4) {  // W words, zero-padded to 16 bytes
                     uint32_t e = 0;
 #pragma unroll
                     for (int j = 0; j < W; j++)
-                        if (tid == j) e = (pl.mode[j] << 30) | pl.val[j];
-                    reinterpret_cast<uint32_t *>(out)[tid] = e;
+                        if (lane == j) e = (mode[j] << 30) | val[j];
+                    reinterpret_cast<uint32_t *>(out)[lane] = e;
                 }
-                write_raw_streams<DT>(src, n, pl, out);
+                warp_raw_streams<DT>(src, n, mode, roff, out);
 #pragma unroll
                 for (int j = 0; j < W; j++)
-                    if (pl.mode[j] == kModeRans)
-                        block_copy(slot + uint64_t(j) * rec_stride, pad16(pl.val[j]), out + pl.roff[j]);
+                    if (mode[j] == kModeRans) warp_copy(slot + uint64_t(j) * a.rec_stride, pad16(val[j]), out + roff[j]);
             }
-            if (tid == 0) {
+            if (lane == 0) {
                 uint4 ent;
-                ent.x = uint32_t(pl.off);
-                ent.y = uint32_t(pl.off >> 32);
-                ent.z = uint32_t(pl.stored) | (pl.raw_chunk ? 0x80000000u : 0u);
+                ent.x = uint32_t(off);
+                ent.y = uint32_t(off >> 32);
+                ent.z = uint32_t(stored) | (raw_chunk ? 0x80000000u : 0u);
                 ent.w = crc;
                 reinterpret_cast<uint4 *>(a.blob + ZC_HEADER_BYTES)[c] = ent;
                 // header CRC = shift(crc(header), 16 n) ^ XOR_c shift(crc(entry_c), 16 (n-1-c))
-                const uint32_t ec = crc_rep16(0xFFFFFFFFu, ent, row) ^ 0xFFFFFFFFu;
+                uint32_t ec = 0xFFFFFFFFu;
+                ec = crc_word_global(ec, ent.x);
+                ec = crc_word_global(ec, ent.y);
+                ec = crc_word_global(ec, ent.z);
+                ec = crc_word_global(ec, ent.w) ^ 0xFFFFFFFFu;
                 atomicXor(&ctrl[2], shift_bytes(ec, 16ull * (a.n_chunks - 1 - c)));
             }
         }
-        if (tid == 0) {
+        if (lane == 0) {
             __threadfence();
             const uint32_t done = atomicAdd(&ctrl[1], 1u);
             if (done == a.n_chunks - 1) {
@@ -610,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 const unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
                 const uint64_t total = table_end + (last & kValMask);
                 uint32_t hc = 0xFFFFFFFFu;
-                for (int q = 0; q < 24; q++) hc = crc_rep_word(hc, a.header[q], row);
+                for (int q = 0; q < 24; q++) hc = crc_word_global(hc, a.header[q]);
                 hc ^= 0xFFFFFFFFu;
                 const uint32_t hcrc = shift_bytes(hc, 16ull * a.n_chunks) ^ acc;
                 uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
@@ -618,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) encode_kernel(EncodeArgs
                 *a.d_blob_bytes = total;
             }
         }
-        __syncthreads();
+        __syncwarp();
     }
 }
 
@@ -628,33 +812,53 @@ __global__ void empty_blob_kernel(EncodeArgs a) {
     if (threadIdx.x == 0) *a.d_blob_bytes = ZC_HEADER_BYTES;
 }
 
+int sms_of_device() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
 template <int DT>
-int launch_encode_t(const EncodeArgs &a, int grid, cudaStream_t s) {
-    const size_t smem = sizeof(EncodeSmem<WordOf<DT>::W>);
-    if (cudaFuncSetAttribute(encode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
+    constexpr int W = WordOf<DT>::W;
+    const size_t ssm = sizeof(StatsSmem<W>);
+    const size_t csm = size_t(kCodeWarps) * kCodeWarpSmem;
+    if (cudaFuncSetAttribute(stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssm)) != cudaSuccess)
         return ZC_ECUDA;
-    encode_kernel<DT><<<grid, kThreads, smem, s>>>(a);
+    if (cudaFuncSetAttribute(code_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(csm)) != cudaSuccess)
+        return ZC_ECUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT>, kStatThreads, ssm) != cudaSuccess)
+        return ZC_ECUDA;
+    const uint64_t most = uint64_t(per_sm < 1 ? 1 : per_sm) * uint64_t(sms_of_device() < 1 ? 1 : sms_of_device());
+    const int sgrid = int(a.wave_n < most ? a.wave_n : most);
+    stats_kernel<DT><<<sgrid, kStatThreads, ssm, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return ZC_ECUDA;
+    if (cudaMemsetAsync(a.ws_ctrl, 0, 4, s) != cudaSuccess) return ZC_ECUDA;  // coder ticket
+    const int cgrid = int((a.workers + kCodeWarps - 1) / kCodeWarps);
+    code_kernel<DT><<<cgrid, kCodeThreads, csm, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
 } // namespace
 
-int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s) {
+int launch_encode_wave(int dtype, const EncodeArgs &a, cudaStream_t s) {
     if (a.n_chunks == 0) {
         empty_blob_kernel<<<1, 32, 0, s>>>(a);
         return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
     }
     switch (dtype) {
-    case ZC_U8: return launch_encode_t<ZC_U8>(a, grid, s);
-    case ZC_U16: return launch_encode_t<ZC_U16>(a, grid, s);
-    case ZC_U32: return launch_encode_t<ZC_U32>(a, grid, s);
-    case ZC_BF16: return launch_encode_t<ZC_BF16>(a, grid, s);
-    case ZC_FP16: return launch_encode_t<ZC_FP16>(a, grid, s);
-    case ZC_FP32: return launch_encode_t<ZC_FP32>(a, grid, s);
+    case ZC_U8: return launch_wave_t<ZC_U8>(a, s);
+    case ZC_U16: return launch_wave_t<ZC_U16>(a, s);
+    case ZC_U32: return launch_wave_t<ZC_U32>(a, s);
+    case ZC_BF16: return launch_wave_t<ZC_BF16>(a, s);
+    case ZC_FP16: return launch_wave_t<ZC_FP16>(a, s);
+    case ZC_FP32: return launch_wave_t<ZC_FP32>(a, s);
     default: return ZC_EINVAL;
     }
 }
 
-int encode_ctas_per_sm() { return kCtasPerSM; }
+int encode_warps_per_sm() { return kCodeWarps; }
 
 } // namespace zc

@@ -26,9 +26,50 @@ bool valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double thres
 
 uint64_t chunks_of(uint64_t nbytes, uint32_t chunk_bytes) { return (nbytes + chunk_bytes - 1) / chunk_bytes; }
 
-// Staging for one CTA: room for a coded record of every stream of a chunk.
-uint64_t slot_bytes(uint32_t chunk_bytes, int W) {
-    return pad256(uint64_t(W) * pad16(kRecHead + kMaxTable + 2ull * (chunk_bytes / W)));
+constexpr uint64_t kInfoBytes = 32;          // per chunk of a wave: CRC + W stream words
+constexpr uint64_t kTableBytes = 512;        // per chunk of a wave and stream: 256 u16 table
+constexpr uint64_t kWaveBytes = 512ull << 20;  // workspace of one statistics + coding wave, at most
+
+// Room for one coded record of a stream in a coding warp's slot. A record is
+// kept only while it is below lim = ceil(threshold x n) bytes, and the coder
+// gives a stream up once its record has reached lim, after at most one more
+// batch of 32 steps x 32 words (2048 bytes); a record can never exceed the
+// header, the table and one word per symbol.
+uint64_t rec_stride(uint32_t chunk_bytes, int W, double threshold) {
+    const uint64_t n = chunk_bytes / W;
+    const uint64_t full = kRecHead + kMaxTable + 2 * n;
+    const double lim = std::ceil(threshold * double(n));
+    uint64_t cap = full;
+    if (lim + double(kRecHead + kMaxTable + 2048) < double(full)) cap = uint64_t(lim) + kRecHead + kMaxTable + 2048;
+    return pad16(cap) + 16;
+}
+
+uint64_t slot_bytes(uint32_t chunk_bytes, int W, double threshold) {
+    return pad256(uint64_t(W) * rec_stride(chunk_bytes, W, threshold));
+}
+
+// Workspace after the control block and the chunk status words: the wave's
+// info and tables, then the coding warps' slots.
+uint64_t n_pad(uint32_t chunk_bytes, int W) { return (uint64_t(chunk_bytes / W) + 31) / 32 * 32; }
+
+// Chunks per wave: all of them, unless their statistics and candidate bytes
+// would take more than kWaveBytes.
+uint64_t wave_chunks(uint64_t nc, uint32_t chunk_bytes, int W) {
+    const uint64_t per_chunk = kInfoBytes + (kTableBytes + n_pad(chunk_bytes, W)) * uint64_t(W);
+    const uint64_t most = kWaveBytes / per_chunk;
+    return nc < most ? nc : most;
+}
+
+struct WaveLayout {
+    uint64_t info, ftab, cand, slots;  // offsets from the start of the wave area
+};
+WaveLayout wave_layout(uint64_t wave, int W, uint32_t chunk_bytes) {
+    WaveLayout l;
+    l.info = 0;
+    l.ftab = pad256(kInfoBytes * wave);
+    l.cand = l.ftab + pad256(kTableBytes * uint64_t(W) * wave);
+    l.slots = l.cand + pad256(n_pad(chunk_bytes, W) * uint64_t(W) * wave);
+    return l;
 }
 
 uint32_t host_crc_table[256];
@@ -54,9 +95,9 @@ int sm_count() {
     return sms;
 }
 
-// Persistent compression CTAs: a few per SM (each holds one chunk in flight).
-uint64_t worker_count(uint64_t n_chunks) {
-    uint64_t most = uint64_t(sm_count()) * uint64_t(encode_ctas_per_sm());
+// Coding warps that can run at once (one chunk in flight each).
+uint64_t max_workers(uint64_t n_chunks) {
+    uint64_t most = uint64_t(sm_count()) * uint64_t(encode_warps_per_sm());
     if (most < 1) most = 1;
     return n_chunks < most ? n_chunks : most;
 }
@@ -89,7 +130,14 @@ extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk
     if (!valid_params(nbytes, dtype, chunk_bytes, 0.95)) return 0;
     const uint64_t nc = chunks_of(nbytes, chunk_bytes);
     if (nc == 0) return kCtrlBytes;
-    return kCtrlBytes + pad256(8 * nc) + worker_count(nc) * slot_bytes(chunk_bytes, word_bytes(dtype));
+    const int W = word_bytes(dtype);
+    const uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+    // every coding warp for thresholds up to 1; at least one warp for any
+    // threshold (larger thresholds then run fewer warps)
+    uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0);
+    const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9);
+    if (slots < one_any) slots = one_any;
+    return kCtrlBytes + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
 }
 
 extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out) {
@@ -189,22 +237,45 @@ extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int nd
     std::memcpy(a.header, head, ZC_HEADER_BYTES);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int grid = 1;
-    if (nc) {
-        const uint64_t fixed = kCtrlBytes + pad256(8 * nc);
-        const uint64_t slot = slot_bytes(chunk_bytes, W);
-        if (ws_bytes < fixed + slot) return ZC_ECAPACITY;
-        uint64_t workers = worker_count(nc);
-        const uint64_t fit = (ws_bytes - fixed) / slot;
-        if (workers > fit) workers = fit;
-        a.ws_ctrl = static_cast<uint8_t *>(d_ws);
-        a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + kCtrlBytes);
-        a.ws_slots = a.ws_ctrl + fixed;
-        a.slot_bytes = slot;
-        grid = int(workers);
-        if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
+    if (nc == 0) return launch_encode_wave(dtype, a, s);
+
+    const uint64_t fixed = kCtrlBytes + pad256(8 * nc);
+    const uint64_t slot = slot_bytes(chunk_bytes, W, threshold);
+    uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+    uint64_t workers = max_workers(nc);
+    if (ws_bytes < fixed) return ZC_ECAPACITY;
+    const uint64_t avail = ws_bytes - fixed;
+    if (wave_layout(wave, W, chunk_bytes).slots + workers * slot > avail) {
+        // a full wave with fewer coding warps, else smaller waves
+        const uint64_t area = wave_layout(wave, W, chunk_bytes).slots;
+        if (area + slot <= avail) {
+            workers = (avail - area) / slot;
+        } else {
+            workers = 1;
+            const uint64_t per_chunk = kInfoBytes + (kTableBytes + n_pad(chunk_bytes, W)) * uint64_t(W);
+            wave = avail > slot + 768 ? (avail - slot - 768) / per_chunk : 0;
+            if (wave == 0) return ZC_ECAPACITY;
+        }
     }
-    return launch_encode(dtype, a, grid, s);
+    const WaveLayout lay = wave_layout(wave, W, chunk_bytes);
+    a.ws_ctrl = static_cast<uint8_t *>(d_ws);
+    a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + kCtrlBytes);
+    a.ws_info = a.ws_ctrl + fixed + lay.info;
+    a.ws_ftab = a.ws_ctrl + fixed + lay.ftab;
+    a.ws_cand = a.ws_ctrl + fixed + lay.cand;
+    a.n_pad = n_pad(chunk_bytes, W);
+    a.ws_slots = a.ws_ctrl + fixed + lay.slots;
+    a.slot_bytes = slot;
+    a.rec_stride = rec_stride(chunk_bytes, W, threshold);
+    a.workers = uint32_t(workers < wave ? workers : wave);
+    if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
+    for (uint64_t w0 = 0; w0 < nc; w0 += wave) {
+        a.wave_start = uint32_t(w0);
+        a.wave_n = uint32_t(nc - w0 < wave ? nc - w0 : wave);
+        const int st = launch_encode_wave(dtype, a, s);
+        if (st != ZC_OK) return st;
+    }
+    return ZC_OK;
 }
 
 extern "C" int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,

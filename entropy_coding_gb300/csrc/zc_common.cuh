@@ -105,12 +105,22 @@ constexpr CrcTables make_crc_tables() {
 
 __device__ constexpr CrcTables kCrc = make_crc_tables();
 
+// Register update over a little-endian 32-bit word from the global tables
+// (slicing by four: byte i of the word is followed by 3 - i more bytes).
+__device__ __forceinline__ uint32_t crc_word_global(uint32_t c, uint32_t w) {
+    const uint32_t u = c ^ w;
+    return __ldg(&kCrc.t[3][u & 0xFFu]) ^ __ldg(&kCrc.t[2][(u >> 8) & 0xFFu]) ^ __ldg(&kCrc.t[1][(u >> 16) & 0xFFu]) ^
+           __ldg(&kCrc.t[0][u >> 24]);
+}
+
 // Multiplying a CRC register by a fixed x^(8n) mod P ("appending n zero
 // bytes") is linear in the register, so it is four table lookups, one per
 // register byte. Tables: kShPow + j shifts by 2^j bytes (j = 0..39), then the
-// stride gaps 248, 496, 992, 2032 and 4080 bytes used by the strided CRCs.
+// stride gaps 248, 496, 992, 2032, 4080, 8176 and 65408 bytes used by the
+// strided CRCs (a round of NT threads x P-byte pieces leaves a gap of
+// (NT - 1) P).
 constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh992 = 42, kSh2032 = 43, kSh4080 = 44,
-              kShCount = 45;
+              kSh8176 = 45, kSh65408 = 46, kShCount = 47;
 
 struct ShiftTables {
     uint32_t t[kShCount][4][256];
@@ -136,6 +146,8 @@ constexpr ShiftTables make_shift_tables() {
     K[kSh992] = xpow8(992);
     K[kSh2032] = xpow8(2032);
     K[kSh4080] = xpow8(4080);
+    K[kSh8176] = xpow8(8176);
+    K[kSh65408] = xpow8(65408);
     for (int c = 0; c < kShCount; c++) {
         // register bit m is the coefficient of x^(31-m); its image is K x^(31-m)
         uint32_t basis[32] = {};
@@ -174,7 +186,7 @@ __device__ inline void load_shift_smem(uint32_t (*dst)[256], int table) {
 }
 
 template <int NT>
-constexpr int gap_table() { return NT == 32 ? kSh496 : NT == 128 ? kSh2032 : kSh4080; }
+constexpr int gap_table() { return NT == 32 ? kSh496 : NT == 128 ? kSh2032 : NT == 256 ? kSh4080 : kSh8176; }
 
 // Register shifted by n bytes (n < 2^40): one table multiply per set bit.
 __device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
@@ -278,7 +290,7 @@ template <int NW, bool kLdcg>
 __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
                                        const uint32_t (*G)[256], uint32_t *s_reg) {
     constexpr int NT = 32 * NW;
-    static_assert(NT == 32 || NT == 128 || NT == 256, "strided CRC runs on 1, 4 or 8 warps");
+    static_assert(NT == 32 || NT == 128 || NT == 256 || NT == 512, "strided CRC runs on 1, 4, 8 or 16 warps");
     const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
     const uint32_t *row = T + (threadIdx.x & 31);
     const uint64_t main = len & ~uint64_t(15);
@@ -315,6 +327,16 @@ __device__ inline uint32_t crc_any(const uint8_t *p, uint64_t len, uint32_t init
     for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
     return crc_strided<NW, kLdcg>(p + head, len - head, reg, T, G, s_reg);
 }
+
+// 16-byte asynchronous global -> shared copies (both addresses 16-aligned).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t lanemask_lt() { uint32_t m; asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m)); return m; }
 __device__ __forceinline__ uint32_t lanemask_gt() { uint32_t m; asm("mov.u32 %0, %%lanemask_gt;" : "=r"(m)); return m; }

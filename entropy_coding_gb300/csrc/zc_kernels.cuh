@@ -17,10 +17,18 @@ struct EncodeArgs {
     uint64_t cap;
     uint64_t *d_blob_bytes;
     int32_t *d_status;
-    uint8_t *ws_ctrl;               // u32 ticket, u32 done, u32 header-CRC accumulator
+    uint8_t *ws_ctrl;               // u32 coder ticket, u32 done, u32 header-CRC accumulator
     unsigned long long *ws_status;  // per chunk: flag << 62 | padded size or prefix
-    uint8_t *ws_slots;              // per-CTA staging for coded records
+    uint8_t *ws_info;               // per chunk of the wave: 32 B {CRC, W stream words}
+    uint8_t *ws_ftab;               // per chunk of the wave and stream: 256 u16 table
+    uint8_t *ws_cand;               // per chunk of the wave and stream: n_pad symbol bytes
+    uint64_t n_pad;                 // chunk_bytes / W rounded up to whole steps of 32
+    uint8_t *ws_slots;              // per coding warp: W records of rec_stride bytes
     uint64_t slot_bytes;
+    uint64_t rec_stride;
+    uint32_t wave_start;            // first chunk of this wave
+    uint32_t wave_n;                // chunks in this wave
+    uint32_t workers;               // coding warps
     uint32_t header[24];            // the 96-byte header, CRC field zero (final CRC if empty)
 };
 
@@ -45,8 +53,10 @@ struct CrcArgs {
     uint32_t *out;
 };
 
-int launch_encode(int dtype, const EncodeArgs &a, int grid, cudaStream_t s);
-int encode_ctas_per_sm();
+// Statistics and coding kernels for chunks [wave_start, wave_start + wave_n);
+// the empty-tensor blob when n_chunks == 0.
+int launch_encode_wave(int dtype, const EncodeArgs &a, cudaStream_t s);
+int encode_warps_per_sm();
 int launch_decode(int dtype, const DecodeArgs &a, cudaStream_t s);
 int launch_crc(const CrcArgs &a, cudaStream_t s);
 

@@ -93,9 +93,12 @@ typedef struct {
 ZC_API uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold);
 
 /* Device workspace zc_compress needs for these parameters on the current
- * device (chunk status words for the offset scan plus per-worker staging
- * for coded words). Returns 0 for invalid parameters. Queries the device's
- * SM count; no allocation, no synchronisation. */
+ * device: chunk status words for the offset scan; per chunk of a wave (at
+ * most 512 MiB of it) the statistics pass's results and the bytes of the
+ * streams it chose to code; per coding warp room for a chunk's coded
+ * records. With at least this much, any threshold works; thresholds above 1
+ * may run fewer coding warps. Returns 0 for invalid parameters. Queries the
+ * device's SM count; no allocation, no synchronisation. */
 ZC_API uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes);
 
 /* Parse and check a blob's header and chunk table from a host copy of its
