@@ -1,58 +1,122 @@
 // decode.cu — decompression kernel.
 //
-// One warp restores one chunk (chunks are independent: ZipNN note, Method 5,
-// the metadata map lets chunks decode in parallel). Per chunk a warp:
-//   1. reads and bounds-checks the chunk table entry;
-//   2. checks the CRC-32 of the stored bytes (cuZipNN: verify a blob before
-//      decoding it), unless the caller asked not to;
-//   3. copies a RAW chunk, or parses a grouped chunk's directory and the
-//      frequency table of its first rANS stream into a slot -> symbol lookup
-//      table in shared memory;
-//   4. runs the 32 interleaved rANS lanes forward eight steps at a time,
-//      staging the decoded symbols of the 256 elements of those steps in
-//      shared memory, then lets each lane gather the bytes of 8 consecutive
-//      elements from every stream (coded, raw or constant), transpose them
-//      into words, undo the exponent extraction and store them with vector
-//      stores.
+// Chunks are independent (ZipNN note, Method 5: the metadata map lets chunks
+// decode in parallel); each one is restored by a pair of warps:
+//   - both warps read and bounds-check the chunk table entry and the grouped
+//     chunk's directory;
+//   - the producer warp parses the frequency table of the chunk's first rANS
+//     stream into a slot -> symbol lookup table in shared memory and runs the
+//     32 interleaved rANS lanes, eight steps (256 elements) at a time, into a
+//     queue of four 256-byte stage buffers;
+//   - the consumer warp takes each group of symbols, gathers the bytes of 8
+//     consecutive elements per lane from every stream (coded, raw or
+//     constant), transposes them into words, undoes the exponent extraction,
+//     stores them with vector stores and accumulates the CRC-32 of the bytes
+//     it wrote, which it checks against the chunk table at the end (unless
+//     the caller asked not to); a RAW chunk is a copy done by the consumer.
+// So the serial chain of rANS states is the only work on the producer's
+// critical path. The queue is guarded by shared-memory mbarriers; every wait
+// gives up after about a second (ZC_ETIMEOUT) so that a fault in one warp
+// cannot hang its partner.
 // Renormalisation words are consumed from the end of each record backwards
-// and staged in a two-block shared-memory ring filled by cp.async. Chunks
-// with more than one coded stream first decode the other ones into the
+// and staged in a four-block shared-memory ring filled by cp.async, topped up
+// once per group so that a decoding step has no branch. Chunks with more than
+// one coded stream first have the producer decode the other ones into the
 // tail of their own output range (one byte per element and stream,
-// interleaved); the main pass reads them from there before any store can
-// reach them (the write front advances W bytes per element, the read front
-// q < W bytes per element from (W - q) n onward, and they meet only at the
-// end).
+// interleaved); the consumer reads them from there, group by group, before
+// any of its stores can reach them (the write front advances W bytes per
+// element, the read front q < W bytes per element from (W - q) n onward, and
+// they meet only at the end).
 #include "zc_kernels.cuh"
 
 namespace zc {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 512, kRingBytes = 2 * kRingWords,
-                   kStageBytes = 256;
-constexpr uint32_t kSlotSmem = kLutBytes + kSymBytes + kRingBytes + kStageBytes;
-// replicated CRC byte table + the gap table of the output pieces + the 496-byte gap table
-constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
+constexpr int kPairs = 8;                 // chunks per CTA at most, one warp pair each
+constexpr int kThreads = 64 * kPairs;
+constexpr int kCtasPerSM = 2;
+constexpr int kStages = 4;                // symbol groups in flight within a pair
+constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
+// replicated CRC byte table + shift tables: one group's output (256 W
+// bytes), half a lane's piece (4 W bytes) and the 496-byte gap
+constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 3 * 4 * 256 * 4;
+constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
 
+// Shared memory of one warp pair.
+struct PairSmem {
+    uint8_t lut[kLutBytes];          // slot -> symbol
+    uint32_t sym[256];               // symbol -> f | cum << 12
+    uint16_t ring[kRingWords];       // renormalisation words
+    uint8_t stage[kStages][256];     // decoded symbols, row k = step k of a group
+    unsigned long long full[kStages], empty[kStages], start;
+    uint32_t flag;                   // producer -> consumer: 1 when the main stream is ready
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return uint32_t(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void mbar_init(unsigned long long *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(unsigned long long *b, uint32_t parity) {
+    uint32_t done;
+    // the thread may be suspended until the phase completes (at most 0.1 ms
+    // per call), so a waiting warp takes no issue slots
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\tselp.b32 %0, 1, 0, P;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(b)), "r"(parity), "r"(100000u)
+        : "memory");
+    return done != 0;
+}
+// Wait (the whole warp) until the phase of the given parity has completed;
+// false after about a second.
+__device__ bool mbar_wait(unsigned long long *b, uint32_t parity) {
+    const long long t0 = clock64();
+    for (;;) {
+        if (__all_sync(kFull, mbar_test(b, parity))) return true;
+        if (uint64_t(clock64() - t0) > kWaitCycles) return false;
+    }
+}
 
 struct Rans {
     uint32_t x;          // this lane's state
     int32_t ptr;         // words left to consume (warp-uniform)
-    int32_t next_block;  // next 256-word block to fetch, < 0 when all fetched
+    int32_t lo;          // lowest 256-word block fetched so far (warp-uniform)
     const uint8_t *wbase;
     uint32_t padded;     // pad16(2 * nwords)
     const uint8_t *lut;
     const uint32_t *sym;
     uint16_t *ring;
-    uint8_t *stage;
 };
 
 // Fetch 256-word block b of a record's word area into its ring slot.
 __device__ __forceinline__ void fetch_block(const Rans &r, int b) {
     const int lane = threadIdx.x & 31;
     uint32_t byte = uint32_t(b) * 512u + 16u * lane;
-    if (byte < r.padded) cp_async16(reinterpret_cast<uint8_t *>(r.ring) + (b & 1) * 512 + 16 * lane, r.wbase + byte);
+    if (byte < r.padded) cp_async16(reinterpret_cast<uint8_t *>(r.ring) + (b & 3) * 512 + 16 * lane, r.wbase + byte);
+}
+
+// Keep the ring ahead of the words still to be consumed: blocks down to
+// b - 3 requested and blocks b - 1 .. b complete, b being the block of the
+// next word. Block k goes to ring slot k & 3, whose previous block (k + 4)
+// lies wholly above the next word. One commit group per block, empty past the
+// record's first block, so the two newest groups are always the two lowest
+// blocks. Between two calls at most 256 words may be consumed.
+__device__ __forceinline__ void ring_refill(Rans &r) {
+    const int b = (r.ptr - 1) >> 8;
+    const int target = max(b - 3, -4);
+    if (r.lo > target) {
+        do {
+            r.lo--;
+            if (r.lo >= 0) fetch_block(r, r.lo);
+            cp_async_commit();
+        } while (r.lo > target);
+        cp_async_wait<2>();
+        __syncwarp();
+    }
 }
 
 // Parse a rANS record (val bytes) into lookup tables in `slot` and load the
@@ -113,12 +177,9 @@ __device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, Rans
     r.lut = lut;
     r.sym = sym;
     r.ring = reinterpret_cast<uint16_t *>(slot + kLutBytes + kSymBytes);
-    r.stage = slot + kLutBytes + kSymBytes + kRingBytes;
-    int top = nwords ? int((nwords - 1) >> 8) : -1;
-    if (top >= 0) fetch_block(r, top);
-    if (top >= 1) fetch_block(r, top - 1);
-    r.next_block = top - 2;
-    cp_async_commit();
+    r.lo = nwords ? int((nwords - 1) >> 8) + 1 : 0;
+    __syncwarp();
+    ring_refill(r);
     return true;
 }
 
@@ -136,15 +197,6 @@ __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt)
     xn = need ? ((xn << 16) | w) : xn;
     if (active) r.x = xn;
     r.ptr -= int32_t(__popc(bal));
-    if (r.next_block >= 0 && r.ptr <= 256 * (r.next_block + 2)) {
-        __syncwarp();
-        fetch_block(r, r.next_block);
-        cp_async_commit();
-        r.next_block--;
-        if (r.next_block < 0) cp_async_wait_all();
-        else cp_async_wait<1>();
-        __syncwarp();
-    }
     return s;
 }
 
@@ -152,8 +204,6 @@ __device__ __forceinline__ bool rans_final_ok(const Rans &r) {
     return !__any_sync(kFull, r.x != kRansL || r.ptr != 0);
 }
 
-// Stream kinds in the main pass.
-constexpr uint32_t kKConst = 0, kKRaw = 1, kKMain = 2, kKStaged = 3;
 
 // 8 consecutive elements' bytes of stream j packed in two words (element e
 // of the eight in byte e of the pair), from each kind of stream.
@@ -161,9 +211,293 @@ struct Col8 {
     uint32_t lo, hi;
 };
 
+// Stream kinds.
+constexpr uint32_t kKConst = 0, kKRaw = 1, kKMain = 2, kKStaged = 3;
+
+// What both warps of a pair know about a grouped chunk.
+struct ChunkCtx {
+    const uint8_t *p;      // payload
+    uint8_t *out;          // output range
+    uint8_t *tail;         // staged bytes of the coded streams after the first
+    uint32_t n, len, q, groups, T;
+    bool have_main;
+    uint32_t kind[4], val[4], roff[4], sub[4];
+};
+
+// Parse a grouped chunk's directory. Returns false if malformed.
+template <int W>
+__device__ bool parse_directory(const uint8_t *p, uint32_t stored, uint32_t n, ChunkCtx &cx) {
+    const int lane = threadIdx.x & 31;
+    // W entries of mode << 30 | value, zero-padded to 16 bytes
+    const uint32_t dir = lane < 4 ? reinterpret_cast<const uint32_t *>(p)[lane] : 0u;
+    bool bad = __any_sync(kFull, lane >= W && lane < 4 && dir != 0);
+    uint32_t pos = 16, coded = 0;
+    cx.have_main = false;
+#pragma unroll
+    for (int j = 0; j < W; j++) {
+        const uint32_t e = __shfl_sync(kFull, dir, j);
+        const uint32_t mode = e >> 30;
+        cx.val[j] = e & 0x3FFFFFFFu;
+        cx.roff[j] = pos;
+        cx.sub[j] = 0;
+        if (mode == kModeConst) {
+            cx.kind[j] = kKConst;
+            bad |= cx.val[j] > 255;
+        } else if (mode == kModeRaw) {
+            cx.kind[j] = kKRaw;
+            bad |= cx.val[j] != n;
+            pos += uint32_t(pad16(n));
+        } else if (mode == kModeRans) {
+            cx.kind[j] = coded == 0 ? kKMain : kKStaged;
+            cx.sub[j] = coded == 0 ? 0 : coded - 1;
+            cx.have_main = true;
+            coded++;
+            bad |= cx.val[j] < kRecHead || cx.val[j] > stored;
+            pos += uint32_t(pad16(cx.val[j]));
+        } else {
+            cx.kind[j] = kKConst;
+            bad = true;
+        }
+        if (pos > stored) bad = true;
+    }
+    cx.q = coded > 1 ? coded - 1 : 0;
+    return !bad && pos == stored;
+}
+
+// Producer warp: staged streams into the output tail, then the main stream's
+// symbols group by group into the stage queue (the last group may be
+// partial: steps past the stream leave the states alone).
 template <int DT>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, const uint32_t *crc_rep,
-                             const uint32_t (*gap_out)[256], const uint32_t (*gap496)[256]) {
+__device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
+    constexpr int W = WordOf<DT>::W;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = lanemask_lt();
+    uint8_t *slot = ps.lut;
+    bool bad = false;
+    if (cx.q) {
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            if (cx.kind[j] != kKStaged) continue;
+            Rans r;
+            if (!rans_setup(cx.p + cx.roff[j], cx.val[j], slot, r)) bad = true;
+            if (!bad) {
+                for (uint32_t t = 0; t < cx.T; t++) {
+                    const uint32_t i = t * 32 + lane;
+                    const bool active = i < cx.n;
+                    ring_refill(r);
+                    const uint32_t s = rans_step(r, active, lt);
+                    if (active) cx.tail[uint64_t(i) * cx.q + cx.sub[j]] = uint8_t(s);
+                }
+                bad |= !rans_final_ok(r);
+            }
+            cp_async_wait_all();  // the ring is reused by the next stream
+            __syncwarp();
+            if (bad) break;
+        }
+    }
+    Rans rs;
+#pragma unroll
+    for (int j = 0; j < W; j++)
+        if (!bad && cx.kind[j] == kKMain && !rans_setup(cx.p + cx.roff[j], cx.val[j], slot, rs)) bad = true;
+    if (lane == 0) ps.flag = bad ? 0u : 1u;
+    __syncwarp();
+    mbar_arrive(&ps.start);
+    if (bad) {
+        cp_async_wait_all();
+        if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+        return;
+    }
+    const uint32_t ng = (cx.T + 7) / 8;  // groups including a partial last one
+    for (uint32_t g = 0; g < ng; g++) {
+        const uint32_t k = g % kStages, r = g / kStages;
+        if (r > 0 && !mbar_wait(&ps.empty[k], (r - 1) & 1u)) {
+            if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+            cp_async_wait_all();
+            return;
+        }
+        ring_refill(rs);
+        uint8_t *st = ps.stage[k];
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+            const uint32_t t = 8 * g + s;
+            const bool active = t < cx.T && t * 32 + lane < cx.n;
+            st[32 * s + lane] = uint8_t(rans_step(rs, active, lt));
+        }
+        mbar_arrive(&ps.full[k]);
+    }
+    if (!rans_final_ok(rs) && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+    cp_async_wait_all();
+}
+
+// Consumer warp: the chunk's output and its CRC. The lane register follows
+// the lane's pieces: lane l's 8 elements of a group form one 8W-byte piece
+// and the pieces of a group are consecutive, so after group g it is
+// shift(register after g - 1, 256 W bytes) XOR the CRC register of the new
+// piece taken from zero (linearity); the lanes are folded at the end
+// (crc_fold) and the elements after the last whole group are added from the
+// output.
+template <int DT, bool kVerify>
+__device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, uint32_t expect_crc,
+                        const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*hshift)[256],
+                        const uint32_t (*gap496)[256]) {
+    constexpr int W = WordOf<DT>::W;
+    const int lane = threadIdx.x & 31;
+    const uint32_t *row = crc_rep + lane;
+    const uint32_t groups = cx.groups;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(cx.out) & 15) == 0;
+    if (cx.have_main) {
+        if (!mbar_wait(&ps.start, 0)) {
+            if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+            return;
+        }
+        if (ps.flag == 0) return;  // the producer has reported the chunk
+    }
+    uint32_t Rl = 0;
+    uint2 rn1[W], rn2[W];  // raw columns of the next two groups
+#pragma unroll
+    for (int j = 0; j < W; j++) {
+        const uint2 *src = reinterpret_cast<const uint2 *>(cx.p + cx.roff[j]) + lane;
+        rn1[j] = (cx.kind[j] == kKRaw && groups > 0) ? __ldg(src) : make_uint2(0, 0);
+        rn2[j] = (cx.kind[j] == kKRaw && groups > 1) ? __ldg(src + 32) : make_uint2(0, 0);
+    }
+    for (uint32_t g = 0; g < groups; g++) {
+        const uint32_t k = g % kStages, r = g / kStages;
+        Col8 col[W];
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            col[j].lo = rn1[j].x;
+            col[j].hi = rn1[j].y;
+            rn1[j] = rn2[j];
+            if (cx.kind[j] == kKRaw && g + 2 < groups)
+                rn2[j] = __ldg(reinterpret_cast<const uint2 *>(cx.p + cx.roff[j] + 256 * (g + 2)) + lane);
+        }
+        uint2 mv = make_uint2(0, 0);
+        if (cx.have_main) {
+            if (!mbar_wait(&ps.full[k], r & 1u)) {
+                if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+                return;
+            }
+            mv = *reinterpret_cast<const uint2 *>(ps.stage[k] + 8 * lane);
+            mbar_arrive(&ps.empty[k]);
+        }
+        const uint32_t e0 = 256 * g + 8 * lane;
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            const uint32_t cv = cx.val[j] * 0x01010101u;
+            col[j].lo = cx.kind[j] == kKConst ? cv : cx.kind[j] == kKMain ? mv.x : col[j].lo;
+            col[j].hi = cx.kind[j] == kKConst ? cv : cx.kind[j] == kKMain ? mv.y : col[j].hi;
+            if (cx.kind[j] == kKStaged) {
+                uint32_t v[2] = {0, 0};
+                for (int e = 0; e < 8; e++)
+                    v[e >> 2] |= uint32_t(__ldcg(cx.tail + uint64_t(e0 + e) * cx.q + cx.sub[j])) << (8 * (e & 3));
+                col[j].lo = v[0];
+                col[j].hi = v[1];
+            }
+        }
+        const uint32_t cin = (g == 0 && lane == 0) ? 0xFFFFFFFFu : 0u;
+        if constexpr (W == 4) {
+            uint4 v[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint32_t c0 = h ? col[0].hi : col[0].lo, c1 = h ? col[1].hi : col[1].lo;
+                const uint32_t c2 = h ? col[2].hi : col[2].lo, c3 = h ? col[3].hi : col[3].lo;
+                const uint32_t lo32 = __byte_perm(c3, c2, 0x5140), hi32 = __byte_perm(c3, c2, 0x7362);
+                const uint32_t lo10 = __byte_perm(c1, c0, 0x5140), hi10 = __byte_perm(c1, c0, 0x7362);
+                v[h].x = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x5410));
+                v[h].y = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x7632));
+                v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
+                v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
+            }
+            if constexpr (kVerify) {
+                // two independent 16-byte halves, joined by a 16-byte shift
+                const uint32_t p0 = crc_rep16(cin, v[0], row), p1 = crc_rep16(0u, v[1], row);
+                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ shift_smem(p0, hshift) ^ p1;
+            }
+            if (vec_ok) {
+                uint4 *o = reinterpret_cast<uint4 *>(cx.out + 4ull * e0);
+                o[0] = v[0];
+                o[1] = v[1];
+            } else {
+                uint32_t *o = reinterpret_cast<uint32_t *>(cx.out) + e0;
+                o[0] = v[0].x; o[1] = v[0].y; o[2] = v[0].z; o[3] = v[0].w;
+                o[4] = v[1].x; o[5] = v[1].y; o[6] = v[1].z; o[7] = v[1].w;
+            }
+        } else if constexpr (W == 2) {
+            uint4 v;
+            v.x = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x5140));
+            v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
+            v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
+            v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
+            if constexpr (kVerify) {
+                // two independent 8-byte halves, joined by an 8-byte shift
+                const uint32_t p0 = crc_rep_word(crc_rep_word(cin, v.x, row), v.y, row);
+                const uint32_t p1 = crc_rep_word(crc_rep_word(0u, v.z, row), v.w, row);
+                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ shift_smem(p0, hshift) ^ p1;
+            }
+            if (vec_ok) {
+                *reinterpret_cast<uint4 *>(cx.out + 2ull * e0) = v;
+            } else {
+                uint16_t *o = reinterpret_cast<uint16_t *>(cx.out) + e0;
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int e = 0; e < 4; e++) {
+                    o[2 * e] = uint16_t(w4[e]);
+                    o[2 * e + 1] = uint16_t(w4[e] >> 16);
+                }
+            }
+        } else {
+            if constexpr (kVerify) {
+                const uint32_t piece = crc_rep_word(crc_rep_word(cin, col[0].lo, row), col[0].hi, row);
+                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ piece;
+            }
+            if ((reinterpret_cast<uintptr_t>(cx.out) & 7) == 0) {
+                *reinterpret_cast<uint2 *>(cx.out + e0) = make_uint2(col[0].lo, col[0].hi);
+            } else {
+                for (int e = 0; e < 8; e++)
+                    cx.out[e0 + e] = uint8_t((e < 4 ? col[0].lo : col[0].hi) >> (8 * (e & 3)));
+            }
+        }
+    }
+    // the last < 256 elements: the producer's partial group, step by step
+    if (cx.T > 8 * groups) {
+        const uint32_t k = groups % kStages, r = groups / kStages;
+        if (cx.have_main && !mbar_wait(&ps.full[k], r & 1u)) {
+            if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+            return;
+        }
+        for (uint32_t t = groups * 8; t < cx.T; t++) {
+            const uint32_t i = t * 32 + lane;
+            if (i >= cx.n) continue;
+            const uint32_t sm = cx.have_main ? ps.stage[k][32 * (t - groups * 8) + lane] : 0u;
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < W; j++) {
+                uint32_t b;
+                if (cx.kind[j] == kKConst) b = cx.val[j];
+                else if (cx.kind[j] == kKRaw) b = __ldg(cx.p + cx.roff[j] + i);
+                else if (cx.kind[j] == kKMain) b = sm;
+                else b = __ldcg(cx.tail + uint64_t(i) * cx.q + cx.sub[j]);
+                word = (word << 8) | b;
+            }
+            const uint32_t w = Perm<DT>::inv(word);
+            if (W == 4) reinterpret_cast<uint32_t *>(cx.out)[i] = w;
+            else if (W == 2) reinterpret_cast<uint16_t *>(cx.out)[i] = uint16_t(w);
+            else cx.out[i] = uint8_t(w);
+        }
+        __syncwarp();
+    }
+    if constexpr (kVerify) {
+        constexpr int kLogPiece = W == 4 ? 5 : W == 2 ? 4 : 3;
+        uint32_t reg = groups ? crc_fold<1>(Rl, kLogPiece, nullptr) : 0xFFFFFFFFu;
+        const uint32_t done = groups * 256 * W;
+        reg = crc_any<1, true>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
+        if ((reg ^ 0xFFFFFFFFu) != expect_crc && lane == 0) status_or(a.d_status, ZC_ECRC);
+    }
+}
+
+template <int DT>
+__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, PairSmem &ps, const uint32_t *crc_rep,
+                             const uint32_t (*gshift)[256], const uint32_t (*hshift)[256],
+                             const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
@@ -183,14 +517,14 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
     bool ok = (off & 15) == 0 && off >= table_end && off <= a.blob_bytes && stored <= a.blob_bytes - off;
     ok = ok && (raw ? stored == len : (stored % 16 == 0 && stored >= 16 && stored <= max_grouped(len, W)));
     if (!ok) {
-        if (lane == 0) status_or(a.d_status, ZC_EFORMAT);
+        if (!producer && lane == 0) status_or(a.d_status, ZC_EFORMAT);
         return;
     }
     const uint8_t *p = a.blob + off;
     const bool verify = !(a.flags & ZC_NO_VERIFY);
-    const uint32_t *row = crc_rep + lane;
     uint8_t *out = a.dst + uint64_t(c) * a.chunk_bytes;
     if (raw) {
+        if (producer) return;
         uint32_t nvec = (reinterpret_cast<uintptr_t>(out) & 15) ? 0 : len / 16;
         for (uint32_t v = lane; v < nvec; v += 32)
             reinterpret_cast<uint4 *>(out)[v] = __ldg(reinterpret_cast<const uint4 *>(p) + v);
@@ -202,250 +536,73 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, uint8_t *wsm, cons
         return;
     }
 
-    // directory: W entries of mode << 30 | value, zero-padded to 16 bytes
-    uint32_t dir = lane < 4 ? reinterpret_cast<const uint32_t *>(p)[lane] : 0u;
-    bool bad = __any_sync(kFull, lane >= W && lane < 4 && dir != 0);
-    uint32_t kind[W], val[W], roff[W], sub[W];
-    uint32_t pos = 16, coded = 0;
-#pragma unroll
-    for (int j = 0; j < W; j++) {
-        uint32_t e = __shfl_sync(kFull, dir, j);
-        uint32_t mode = e >> 30;
-        val[j] = e & 0x3FFFFFFFu;
-        roff[j] = pos;
-        sub[j] = 0;
-        if (mode == kModeConst) {
-            kind[j] = kKConst;
-            bad |= val[j] > 255;
-        } else if (mode == kModeRaw) {
-            kind[j] = kKRaw;
-            bad |= val[j] != n;
-            pos += uint32_t(pad16(n));
-        } else if (mode == kModeRans) {
-            kind[j] = coded == 0 ? kKMain : kKStaged;
-            sub[j] = coded == 0 ? 0 : coded - 1;
-            coded++;
-            bad |= val[j] < kRecHead || val[j] > stored;
-            pos += uint32_t(pad16(val[j]));
-        } else {
-            kind[j] = kKConst;
-            bad = true;
-        }
-        if (pos > stored) bad = true;
-    }
-    if (bad || pos != stored) {
-        if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+    ChunkCtx cx;
+    if (!parse_directory<W>(p, stored, n, cx)) {
+        if (!producer && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
         return;
     }
-    const uint32_t lt = lanemask_lt();
-    const uint32_t T = (n + 31) / 32;
-
-    // coded streams after the first: decode into the output tail first, q
-    // bytes per element
-    const uint32_t q = coded > 1 ? coded - 1 : 0;
-    uint8_t *tail = out + (len - q * n);
-    if (q) {
-#pragma unroll
-        for (int j = 0; j < W; j++) {
-            if (kind[j] != kKStaged) continue;
-            Rans r;
-            if (!rans_setup(p + roff[j], val[j], wsm, r)) bad = true;
-            cp_async_wait_all();
-            __syncwarp();
-            if (bad) break;
-            for (uint32_t t = 0; t < T; t++) {
-                uint32_t i = t * 32 + lane;
-                bool active = i < n;
-                uint32_t s = rans_step(r, active, lt);
-                if (active) tail[uint64_t(i) * q + sub[j]] = uint8_t(s);
-            }
-            bad |= !rans_final_ok(r);
-            __syncwarp();
-        }
-        __syncwarp();
-        if (bad) {
-            if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
-            return;
-        }
+    cx.p = p;
+    cx.out = out;
+    cx.n = n;
+    cx.len = len;
+    cx.T = (n + 31) / 32;
+    cx.groups = n / 256;
+    cx.tail = out + (len - cx.q * n);
+    if (producer) {
+        if (cx.have_main) produce<DT>(a, cx, ps);
+    } else if (verify) {
+        consume<DT, true>(a, cx, ps, ent.w, crc_rep, gshift, hshift, gap496);
+    } else {
+        consume<DT, false>(a, cx, ps, ent.w, crc_rep, gshift, hshift, gap496);
     }
-
-    Rans rs;
-    bool have_main = false;
-#pragma unroll
-    for (int j = 0; j < W; j++) {
-        if (kind[j] != kKMain) continue;
-        have_main = true;
-        if (!rans_setup(p + roff[j], val[j], wsm, rs)) bad = true;
-    }
-    cp_async_wait_all();
-    __syncwarp();
-    if (bad) {
-        if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
-        return;
-    }
-
-    // groups of 8 steps = 256 elements; each lane then owns 8 consecutive
-    // elements 256 g + 8 lane .. + 7
-    const uint32_t groups = n / 256;
-    const bool vec_ok = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-    // CRC of the decoded bytes: lane l's 8 elements of each group form one
-    // 8W-byte piece; pieces of a group are consecutive, so each lane keeps the
-    // register of its own pieces and shifts it over the others' (256 W - 8 W
-    // bytes) between groups, then the lanes are folded (crc_fold).
-    uint32_t Rl = 0;
-    uint2 rn1[W], rn2[W];  // raw columns of the next two groups
-#pragma unroll
-    for (int j = 0; j < W; j++) {
-        const uint2 *src = reinterpret_cast<const uint2 *>(p + roff[j]) + lane;
-        rn1[j] = (kind[j] == kKRaw && groups > 0) ? __ldg(src) : make_uint2(0, 0);
-        rn2[j] = (kind[j] == kKRaw && groups > 1) ? __ldg(src + 32) : make_uint2(0, 0);
-    }
-    for (uint32_t g = 0; g < groups; g++) {
-        Col8 col[W];
-#pragma unroll
-        for (int j = 0; j < W; j++) {
-            col[j].lo = rn1[j].x;
-            col[j].hi = rn1[j].y;
-            rn1[j] = rn2[j];
-            if (kind[j] == kKRaw && g + 2 < groups)
-                rn2[j] = __ldg(reinterpret_cast<const uint2 *>(p + roff[j] + 256 * (g + 2)) + lane);
-        }
-        if (have_main) {
-#pragma unroll
-            for (int k = 0; k < 8; k++) rs.stage[32 * k + lane] = uint8_t(rans_step(rs, true, lt));
-            __syncwarp();
-        }
-        const uint32_t e0 = 256 * g + 8 * lane;
-#pragma unroll
-        for (int j = 0; j < W; j++) {
-            if (kind[j] == kKConst) {
-                col[j].lo = col[j].hi = val[j] * 0x01010101u;
-            } else if (kind[j] == kKMain) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(rs.stage + 8 * lane);
-                col[j].lo = v.x;
-                col[j].hi = v.y;
-            } else if (kind[j] == kKStaged) {
-                uint32_t v[2] = {0, 0};
-                for (int e = 0; e < 8; e++)
-                    v[e >> 2] |= uint32_t(__ldcg(tail + uint64_t(e0 + e) * q + sub[j])) << (8 * (e & 3));
-                col[j].lo = v[0];
-                col[j].hi = v[1];
-            }
-        }
-        __syncwarp();
-        const uint32_t cin = g == 0 ? (lane == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(Rl, gap_out);
-        if constexpr (W == 4) {
-            uint4 v[2];
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const uint32_t c0 = h ? col[0].hi : col[0].lo, c1 = h ? col[1].hi : col[1].lo;
-                const uint32_t c2 = h ? col[2].hi : col[2].lo, c3 = h ? col[3].hi : col[3].lo;
-                const uint32_t lo32 = __byte_perm(c3, c2, 0x5140), hi32 = __byte_perm(c3, c2, 0x7362);
-                const uint32_t lo10 = __byte_perm(c1, c0, 0x5140), hi10 = __byte_perm(c1, c0, 0x7362);
-                v[h].x = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x5410));
-                v[h].y = Perm<DT>::inv(__byte_perm(lo32, lo10, 0x7632));
-                v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
-                v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
-            }
-            if (verify) Rl = crc_rep16(crc_rep16(cin, v[0], row), v[1], row);
-            if (vec_ok) {
-                uint4 *o = reinterpret_cast<uint4 *>(out + 4ull * e0);
-                o[0] = v[0];
-                o[1] = v[1];
-            } else {
-                uint32_t *o = reinterpret_cast<uint32_t *>(out) + e0;
-                o[0] = v[0].x; o[1] = v[0].y; o[2] = v[0].z; o[3] = v[0].w;
-                o[4] = v[1].x; o[5] = v[1].y; o[6] = v[1].z; o[7] = v[1].w;
-            }
-        } else if constexpr (W == 2) {
-            uint4 v;
-            v.x = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x5140));
-            v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
-            v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
-            v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
-            if (verify) Rl = crc_rep16(cin, v, row);
-            if (vec_ok) {
-                *reinterpret_cast<uint4 *>(out + 2ull * e0) = v;
-            } else {
-                uint16_t *o = reinterpret_cast<uint16_t *>(out) + e0;
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                for (int e = 0; e < 4; e++) {
-                    o[2 * e] = uint16_t(w4[e]);
-                    o[2 * e + 1] = uint16_t(w4[e] >> 16);
-                }
-            }
-        } else {
-            if (verify) Rl = crc_rep_word(crc_rep_word(cin, col[0].lo, row), col[0].hi, row);
-            if ((reinterpret_cast<uintptr_t>(out) & 7) == 0) {
-                *reinterpret_cast<uint2 *>(out + e0) = make_uint2(col[0].lo, col[0].hi);
-            } else {
-                for (int e = 0; e < 8; e++) out[e0 + e] = uint8_t((e < 4 ? col[0].lo : col[0].hi) >> (8 * (e & 3)));
-            }
-        }
-    }
-    // the last < 256 elements, one step at a time
-    for (uint32_t t = groups * 8; t < T; t++) {
-        const uint32_t i = t * 32 + lane;
-        const bool active = i < n;
-        const uint32_t sm = have_main ? rans_step(rs, active, lt) : 0u;
-        uint32_t word = 0;
-#pragma unroll
-        for (int j = 0; j < W; j++) {
-            uint32_t b = 0;
-            if (active) {
-                if (kind[j] == kKConst) b = val[j];
-                else if (kind[j] == kKRaw) b = __ldg(p + roff[j] + i);
-                else if (kind[j] == kKMain) b = sm;
-                else b = __ldcg(tail + uint64_t(i) * q + sub[j]);
-            }
-            word = (word << 8) | b;
-        }
-        __syncwarp();
-        if (active) {
-            uint32_t w = Perm<DT>::inv(word);
-            if (W == 4) reinterpret_cast<uint32_t *>(out)[i] = w;
-            else if (W == 2) reinterpret_cast<uint16_t *>(out)[i] = uint16_t(w);
-            else out[i] = uint8_t(w);
-        }
-    }
-    bool bad_end = have_main && !rans_final_ok(rs);
-    if (verify) {
-        constexpr int kLogPiece = W == 4 ? 5 : W == 2 ? 4 : 3;
-        uint32_t reg = groups ? crc_fold<1>(Rl, kLogPiece, nullptr) : 0xFFFFFFFFu;
-        __syncwarp();
-        const uint32_t done = groups * 256 * W;
-        reg = crc_any<1, true>(out + done, len - done, reg, crc_rep, gap496, nullptr);
-        if ((reg ^ 0xFFFFFFFFu) != ent.w && lane == 0) status_or(a.d_status, ZC_ECRC);
-    }
-    if (bad_end && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kWarps * 32, 3) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int W = WordOf<DT>::W;
     uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
-    uint32_t(*gap_out)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
-    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
+    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
+    uint32_t(*hshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 8 * 256 * 4);
+    PairSmem *pairs = reinterpret_cast<PairSmem *>(smem + kCrcSmem);
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep(crc_rep);
-        load_shift_smem(gap_out, W == 4 ? kSh992 : W == 2 ? kSh496 : kSh248);
+        load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
+        load_shift_smem(hshift, kShPow + (W == 4 ? 4 : W == 2 ? 3 : 2));  // 4 W bytes
         load_shift_smem(gap496, kSh496);
     }
+    const uint32_t pairs_per_cta = blockDim.x >> 6;
+    if (threadIdx.x < pairs_per_cta) {
+        PairSmem &ps = pairs[threadIdx.x];
+        for (int k = 0; k < kStages; k++) {
+            mbar_init(&ps.full[k], 32);
+            mbar_init(&ps.empty[k], 32);
+        }
+        mbar_init(&ps.start, 32);
+    }
     __syncthreads();
-    uint32_t c = blockIdx.x * kWarps + warp;
+    const uint32_t c = blockIdx.x * pairs_per_cta + (warp >> 1);
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, smem + kCrcSmem + warp * kSlotSmem, crc_rep, gap_out, gap496);
+    decode_chunk<DT>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, hshift, gap496);
 }
 
 template <int DT>
 int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
-    const size_t smem = kCrcSmem + size_t(kWarps) * kSlotSmem;
-    if (cudaFuncSetAttribute(decode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    const size_t smem_max = kCrcSmem + size_t(kPairs) * sizeof(PairSmem);
+    if (cudaFuncSetAttribute(decode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max)) !=
+        cudaSuccess)
         return ZC_ECUDA;
-    const int grid = int((a.n_chunks + kWarps - 1) / kWarps);
-    decode_kernel<DT><<<grid, kWarps * 32, smem, s>>>(a);
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ECUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ZC_ECUDA;
+    // pairs per CTA: just enough for kCtasPerSM CTAs per SM to hold every
+    // chunk, so that the chunks spread evenly over the SMs
+    const uint64_t slots = uint64_t(sms) * kCtasPerSM;
+    const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.n_chunks + slots - 1) / slots));
+    const int grid = int((a.n_chunks + pc - 1) / pc);
+    decode_kernel<DT><<<grid, 64 * pc, kCrcSmem + size_t(pc) * sizeof(PairSmem), s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 

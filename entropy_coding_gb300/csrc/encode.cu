@@ -31,12 +31,12 @@ namespace {
 
 constexpr int kStatWarps = 16;
 constexpr int kStatThreads = 32 * kStatWarps;
-constexpr uint32_t kPiece = 128;  // bytes per thread per round of the statistics pass
-constexpr int kCodeWarps = 16;    // coding warps per CTA, one CTA per SM
+constexpr uint32_t kPiece = 32;  // bytes per thread per round of the statistics pass
+constexpr int kCodeWarps = 16;    // coding warps per SM (and at most per CTA)
 constexpr int kCodeThreads = 32 * kCodeWarps;
 constexpr uint32_t kModeCand = 3;  // statistics -> coder only: a stream to rANS-code
 constexpr uint32_t kAborted = 0xFFFFFFFFu;
-constexpr uint32_t kCodeWarpSmem = 4096 + 4096 + 2048;  // per coding warp: rANS table, symbol ring, word stage
+constexpr uint32_t kCodeWarpSmem = 4096 + 4096 + 4096;  // per coding warp: rANS table, symbol ring, 2 word stages
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
@@ -232,42 +232,71 @@ struct StatsSmem {
     uint32_t crc_rep[kCrcRepWords];  // replicated CRC byte table (32 KB)
     uint32_t gap[4][256];            // register shift over the other threads' pieces
     uint32_t hist[W][128 * 32];
+    uint32_t cnt[W][256];            // merged counts
     uint32_t s_reg[kStatWarps];
-    uint32_t sv[4];
 };
 
+// Count one element into the histograms; hrow = &h[0][lane]. For the byte b
+// of stream j at bit sh of the permuted word, the counter word is
+// (b >> 1) * 32 + lane of stream j and the half is b & 1.
 template <int DT>
-__device__ __forceinline__ void count_elem(uint32_t w, uint32_t (*h)[128 * 32], int lane) {
+__device__ __forceinline__ void count_elem(uint32_t w, uint32_t *hrow) {
     constexpr int W = WordOf<DT>::W;
     const uint32_t p = Perm<DT>::fwd(w);
 #pragma unroll
     for (int j = 0; j < W; j++) {
-        const uint32_t b = stream_byte<W>(p, j);
-        atomicAdd(&h[j][(b >> 1) * 32 + lane], 1u << ((b & 1u) << 4));
+        const int sh = 8 * (W - 1 - j);
+        const uint32_t half = (p >> (sh + 1)) & 0x7Fu;
+        const uint32_t inc = (p & (1u << sh)) ? 0x10000u : 1u;
+        atomicAdd(hrow + j * (128 * 32) + half * 32, inc);
     }
 }
 
 template <int DT>
-__device__ __forceinline__ void count_vec(const uint4 &q, uint32_t (*h)[128 * 32], int lane) {
+__device__ __forceinline__ void count_vec(const uint4 &q, uint32_t *hrow) {
     constexpr int W = WordOf<DT>::W;
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int k = 0; k < 4; k++)
 #pragma unroll
         for (int e = 0; e < 4 / W; e++)
-            count_elem<DT>(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u), h, lane);
+            count_elem<DT>(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u), hrow);
+}
+
+// Bytes of stream 0 (the top byte of each permuted element) of a 16-byte
+// vector: 16 / W of them, in element order, in the low bytes of o.
+template <int DT>
+__device__ __forceinline__ void stream0_bytes(const uint4 &q, uint32_t o[4]) {
+    constexpr int W = WordOf<DT>::W;
+    if constexpr (W == 1) {
+        o[0] = q.x; o[1] = q.y; o[2] = q.z; o[3] = q.w;
+    } else if constexpr (W == 2) {
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        uint32_t t[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            t[k] = __byte_perm(Perm<DT>::fwd(u[k] & 0xFFFFu), Perm<DT>::fwd(u[k] >> 16), 0x0051);  // [e0, e1]
+        o[0] = __byte_perm(t[0], t[1], 0x5410);
+        o[1] = __byte_perm(t[2], t[3], 0x5410);
+    } else {
+        const uint32_t a = __byte_perm(Perm<DT>::fwd(q.x), Perm<DT>::fwd(q.y), 0x0073);
+        const uint32_t b = __byte_perm(Perm<DT>::fwd(q.z), Perm<DT>::fwd(q.w), 0x0073);
+        o[0] = __byte_perm(a, b, 0x5410);
+    }
 }
 
 // Histograms of the chunk's W byte streams and the raw CRC register of its
-// bytes, by the CTA from one pass. Aligned input: the threads take 128-byte
-// pieces round-robin, aligned to the end of the chunk (see Strided; only the
-// first round can be short), so each thread's register needs one gap shift
-// per round. Returns the raw register in every thread.
+// bytes, by the CTA from one pass, and stream 0's bytes for the coder.
+// Aligned input: the threads take 32-byte pieces round-robin, aligned to the
+// end of the chunk (see Strided; only the first round can be short), so each
+// thread's register needs one gap shift per round. Returns the raw register
+// in every thread.
 template <int DT>
-__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm) {
+__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
     constexpr int W = WordOf<DT>::W;
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t *row = sm.crc_rep + lane;
+    uint32_t *hrow = &sm.hist[0][lane];
     uint32_t reg;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
         const uint32_t main = len & ~(kPiece - 1);
@@ -275,31 +304,59 @@ __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<Word
         const uint32_t rounds = (pieces + kStatThreads - 1) / kStatThreads;
         int32_t pidx = tid - int32_t(rounds * kStatThreads - pieces);
         uint32_t R = 0;
+        // the next round's two vectors are in flight while this round's are
+        // counted and checksummed
+        uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
+        if (rounds && pidx >= 0) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx) * kPiece);
+            n0 = __ldg(p);
+            n1 = __ldg(p + 1);
+        }
         for (uint32_t r = 0; r < rounds; r++, pidx += kStatThreads) {
+            const uint4 q0 = n0, q1 = n1;
+            if (r + 1 < rounds) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx + kStatThreads) * kPiece);
+                n0 = __ldg(p);
+                n1 = __ldg(p + 1);
+            }
             uint32_t c = r == 0 ? (pidx == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, sm.gap);
             if (pidx >= 0) {
-                const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx) * kPiece);
-                uint4 q[kPiece / 16];
-#pragma unroll
-                for (int u = 0; u < int(kPiece / 16); u++) q[u] = __ldg(p + u);
-#pragma unroll
-                for (int u = 0; u < int(kPiece / 16); u++) {
-                    c = crc_rep16(c, q[u], row);
-                    count_vec<DT>(q[u], sm.hist, lane);
+                c = crc_rep16(crc_rep16(c, q0, row), q1, row);
+                count_vec<DT>(q0, hrow);
+                count_vec<DT>(q1, hrow);
+                // stream 0's bytes of the piece, for the coder in case the
+                // stream is a candidate
+                uint8_t *d = cand0 + uint64_t(pidx) * (kPiece / W);
+                uint32_t o0[4], o1[4];
+                stream0_bytes<DT>(q0, o0);
+                stream0_bytes<DT>(q1, o1);
+                if constexpr (W == 4) {
+                    *reinterpret_cast<uint2 *>(d) = make_uint2(o0[0], o1[0]);
+                } else if constexpr (W == 2) {
+                    *reinterpret_cast<uint4 *>(d) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+                } else {
+                    reinterpret_cast<uint4 *>(d)[0] = q0;
+                    reinterpret_cast<uint4 *>(d)[1] = q1;
                 }
             }
             R = c;
         }
-        reg = pieces ? crc_fold<kStatWarps>(R, 7, sm.s_reg) : 0xFFFFFFFFu;
+        reg = pieces ? crc_fold<kStatWarps>(R, 5, sm.s_reg) : 0xFFFFFFFFu;
         for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, __ldg(src + i), row);
-        for (uint32_t i = main / W + tid; i < len / W; i += kStatThreads)
-            count_elem<DT>(load_word<W>(src + uint64_t(i) * W), sm.hist, lane);
+        for (uint32_t i = main / W + tid; i < len / W; i += kStatThreads) {
+            const uint32_t w = load_word<W>(src + uint64_t(i) * W);
+            count_elem<DT>(w, hrow);
+            cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
+        }
     } else {
         // input aligned to its element size only: words one at a time; the
         // CRC takes the bytes up to the first 16-byte boundary one by one,
         // then the aligned rest with 16-byte pieces (gap table for 4080)
-        for (uint32_t i = tid; i < len / W; i += kStatThreads)
-            count_elem<DT>(load_word<W>(src + uint64_t(i) * W), sm.hist, lane);
+        for (uint32_t i = tid; i < len / W; i += kStatThreads) {
+            const uint32_t w = load_word<W>(src + uint64_t(i) * W);
+            count_elem<DT>(w, hrow);
+            cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
+        }
         uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15);
         if (head > len) head = len;
         uint32_t c = 0xFFFFFFFFu;
@@ -309,29 +366,36 @@ __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<Word
     return reg;
 }
 
-// Stream j's decision after the histogram pass, by one warp: the 32 counter
-// copies are summed (and zeroed for the next chunk) into 8 bins per lane
-// (symbol 8 lane + k), then CONST / RAW / candidate. A candidate's 12-bit
-// table goes to ftab (256 u16).
+// Sum the 32 counter copies of every stream into cnt[j][b] (and zero them
+// for the next chunk), by all warps of the CTA.
 template <int W>
-__device__ void plan_stats(const EncodeArgs &a, uint32_t n, uint32_t *h, uint32_t *sv, uint32_t *sv_smem,
-                           uint8_t *ftab) {
-    const int lane = threadIdx.x & 31;
-    uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int L = 0; L < 32; L++) {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            uint32_t *cell = h + (4 * L + q) * 32 + lane;
-            const uint32_t v = *cell;
-            *cell = 0;
-            const uint32_t lo = __reduce_add_sync(kFull, v & 0xFFFFu);
-            const uint32_t hi = __reduce_add_sync(kFull, v >> 16);
-            if (lane == L) {
-                cnt[2 * q] = lo;
-                cnt[2 * q + 1] = hi;
-            }
+__device__ void merge_counts(StatsSmem<W> &sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll 4
+    for (int w = warp; w < W * 128; w += kStatWarps) {
+        uint32_t *cell = &sm.hist[w >> 7][(w & 127) * 32 + lane];
+        const uint32_t v = *cell;
+        *cell = 0;
+        const uint32_t lo = __reduce_add_sync(kFull, v & 0xFFFFu);
+        const uint32_t hi = __reduce_add_sync(kFull, v >> 16);
+        if (lane == 0) {
+            sm.cnt[w >> 7][2 * (w & 127)] = lo;
+            sm.cnt[w >> 7][2 * (w & 127) + 1] = hi;
         }
     }
+}
+
+// Stream j's decision after the histogram pass, by one warp, from its merged
+// counts (8 bins per lane: symbol 8 lane + k): CONST / RAW / candidate. A
+// candidate's 12-bit table goes to ftab (256 u16).
+template <int W>
+__device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *counts, uint32_t *sv, uint8_t *ftab) {
+    const int lane = threadIdx.x & 31;
+    uint32_t cnt[8];
+    const uint4 c0 = reinterpret_cast<const uint4 *>(counts)[2 * lane];
+    const uint4 c1 = reinterpret_cast<const uint4 *>(counts)[2 * lane + 1];
+    cnt[0] = c0.x; cnt[1] = c0.y; cnt[2] = c0.z; cnt[3] = c0.w;
+    cnt[4] = c1.x; cnt[5] = c1.y; cnt[6] = c1.z; cnt[7] = c1.w;
     uint32_t pres = 0, only = 0;
 #pragma unroll
     for (int k = 0; k < 8; k++)
@@ -373,85 +437,61 @@ __device__ void plan_stats(const EncodeArgs &a, uint32_t n, uint32_t *h, uint32_
             reinterpret_cast<uint4 *>(ftab)[lane] = v;
         }
     }
-    if (lane == 0) {
-        *sv = (mode << 30) | val;
-        *sv_smem = (mode << 30) | val;
-    }
+    if (lane == 0) *sv = (mode << 30) | val;
+    return mode == kModeCand;
 }
 
-// The bytes of every candidate stream of the chunk, in element order, into
-// cand + j * n_pad (a second pass over the chunk, which is in L2 by now).
+// The bytes of stream j of the chunk, in element order, into out (a second
+// pass over the chunk by one warp; streams after the first are candidates
+// only in unusual data).
 template <int DT>
-__device__ void write_cand(const uint8_t *src, uint32_t len, uint32_t candmask, uint8_t *cand, uint64_t n_pad) {
+__device__ void warp_write_cand(const uint8_t *src, uint32_t len, int j, uint8_t *out) {
     constexpr int W = WordOf<DT>::W;
-    constexpr int E = 16 / W;  // elements per 16-byte vector
-    const int tid = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const uint32_t n = len / W;
-    uint32_t done = 0;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-        const uint32_t nvec = len / 16;
-        for (uint32_t v = tid; v < nvec; v += kStatThreads) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-            uint32_t p[E];
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-#pragma unroll
-                for (int e = 0; e < 4 / W; e++)
-                    p[k * (4 / W) + e] = Perm<DT>::fwd(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u));
-#pragma unroll
-            for (int j = 0; j < W; j++) {
-                if (!((candmask >> j) & 1u)) continue;
-                uint32_t o[4] = {0, 0, 0, 0};
-#pragma unroll
-                for (int e = 0; e < E; e++) o[e >> 2] |= stream_byte<W>(p[e], j) << (8 * (e & 3));
-                uint8_t *d = cand + uint64_t(j) * n_pad + uint64_t(v) * E;
-                if (E == 4) *reinterpret_cast<uint32_t *>(d) = o[0];
-                else if (E == 8) *reinterpret_cast<uint2 *>(d) = make_uint2(o[0], o[1]);
-                else *reinterpret_cast<uint4 *>(d) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        }
-        done = nvec * E;
-    }
-    for (uint32_t i = done + tid; i < n; i += kStatThreads) {
+    for (uint32_t i = lane; i < n; i += 32) {
         const uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
+        uint32_t b = 0;
 #pragma unroll
-        for (int j = 0; j < W; j++)
-            if ((candmask >> j) & 1u) cand[uint64_t(j) * n_pad + i] = uint8_t(stream_byte<W>(p, j));
+        for (int k = 0; k < W; k++)
+            if (k == j) b = stream_byte<W>(p, k);
+        out[i] = uint8_t(b);
     }
 }
 
 // One CTA per chunk of the wave (grid-stride). Writes per chunk 32 bytes of
-// info {CRC-32 of the original bytes, W stream words mode << 30 | value} and
-// the tables of the candidate streams.
+// info {CRC-32 of the original bytes, W stream words mode << 30 | value}, the
+// tables of the candidate streams and their bytes.
 template <int DT>
-__global__ void __launch_bounds__(kStatThreads) stats_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     StatsSmem<W> &sm = *reinterpret_cast<StatsSmem<W> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     load_crc_rep(sm.crc_rep);
-    load_shift_smem(sm.gap, (reinterpret_cast<uintptr_t>(a.src) & 15) == 0 ? kSh65408 : gap_table<kStatThreads>());
+    load_shift_smem(sm.gap, (reinterpret_cast<uintptr_t>(a.src) & 15) == 0 ? kSh16352 : gap_table<kStatThreads>());
     for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
     __syncthreads();
     for (uint32_t cl = blockIdx.x; cl < a.wave_n; cl += gridDim.x) {
         const uint64_t c = uint64_t(a.wave_start) + cl;
         const uint8_t *src = a.src + c * a.chunk_bytes;
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - c * a.chunk_bytes));
-        const uint32_t reg = chunk_stats<DT>(src, len, sm);
+        uint8_t *cand = a.ws_cand + uint64_t(cl) * W * a.n_pad;
+        const uint32_t reg = chunk_stats<DT>(src, len, sm, cand);
+        __syncthreads();
+        merge_counts<W>(sm);
         __syncthreads();
         uint32_t *info = reinterpret_cast<uint32_t *>(a.ws_info + 32ull * cl);
-        if (warp < W)
-            plan_stats<W>(a, len / W, sm.hist[warp], info + 1 + warp, &sm.sv[warp],
-                          a.ws_ftab + (uint64_t(cl) * W + warp) * 512);
         if (tid == 0) info[0] = reg ^ 0xFFFFFFFFu;
-        __syncthreads();
-        uint32_t candmask = 0;
-#pragma unroll
-        for (int j = 0; j < W; j++)
-            if ((sm.sv[j] >> 30) == kModeCand) candmask |= 1u << j;
-        if (candmask) write_cand<DT>(src, len, candmask, a.ws_cand + uint64_t(cl) * W * a.n_pad, a.n_pad);
-        __syncthreads();
+        // warp j decides stream j (and, when stream j >= 1 is a candidate,
+        // writes its bytes for the coder; stream 0's are already there) while
+        // the other warps go on to the next chunk: the counters were zeroed by
+        // the merge, and the next merge comes after the next barrier
+        if (warp < W) {
+            const bool cand_j =
+                plan_stats<W>(a, len / W, sm.cnt[warp], info + 1 + warp, a.ws_ftab + (uint64_t(cl) * W + warp) * 512);
+            if (warp > 0 && cand_j) warp_write_cand<DT>(src, len, warp, cand + uint64_t(warp) * a.n_pad);
+        }
     }
 }
 
@@ -466,11 +506,12 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(EncodeArgs a) {
 // The steps run in blocks of 32 (the last steps of the stream first); the
 // symbols of the next three blocks are in flight into a shared-memory ring
 // (row s of a block = the 32 symbols of its step s). A step stages the low
-// 16 bits of its state in shared memory and keeps one flag bit; after the block the
-// words of the emitting lanes are written out step by step (lanes 31..0
-// within a step), which keeps the word stores off the state's dependency
-// chain. Returns the record's unpadded size, or kAborted once the record has
-// reached lim bytes (it can then no longer be kept: the stream is stored raw).
+// 16 bits of its state in shared memory and keeps one flag bit; the words of
+// the emitting lanes of a block are written out step by step (lanes 31..0
+// within a step) while the next block is coded, which keeps the word stores
+// off the state's dependency chain. Returns the record's unpadded size, or
+// kAborted once the record has reached lim bytes (it can then no longer be
+// kept: the stream is stored raw).
 __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint4 *etab,
                                        uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim) {
     const int lane = threadIdx.x & 31;
@@ -523,51 +564,92 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     uint32_t x = kRansL;
     uint32_t wc = 0;
     const bool first_active = uint32_t(T - 1) * 32 + lane < n;
+    // write out the words of one staged block (steps 0..cnt-1, emitting lanes
+    // 31..0 within a step)
+    auto flush = [&](const uint16_t *st, uint32_t flags, int cnt) {
+#pragma unroll 4
+        for (int s = 0; s < cnt; s++) {
+            const bool em = (flags >> s) & 1u;
+            const uint32_t B = __ballot_sync(kFull, em);
+            if (em) wout[wc + __popc(B & gt)] = st[s * 32];
+            wc += __popc(B);
+        }
+    };
+    uint32_t flags_prev = 0;
     bool aborted = false;
     for (int b = 0; b < nb; b++) {
         issue(b + 3);
         cp_async_wait<3>();
         __syncwarp();
         const uint8_t *blk = ring + (b & 3) * 1024 + lane;
+        uint16_t *st_cur = stage + (b & 1) * 1024;
+        const uint16_t *st_prev = stage + ((b + 1) & 1) * 1024;
         const int cnt = min(32, T - 32 * b);
         uint32_t flags = 0;
-        int s = 0;
-        if (b == 0) {
-            // step T-1, the only one that may be partial; no lane emits a word
-            // there (x = 2^16 is below every 2^20 f)
-            const uint4 ec = etab[blk[0]];
-            const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
-            if (first_active) x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
-            s = 1;
-        }
-        // rows past the block read the next ring slot (or the stage after the
-        // last slot): harmless values that are never used
-        uint32_t sym_n = blk[(s + 1) * 32];
-        uint4 e = etab[blk[s * 32]];
+        if (b > 0 && cnt == 32) {
+            // a full block, interleaved with the write-out of the previous one
+            // (always full): one straight-line body, so the two chains overlap
+            uint32_t sym_n = blk[32];
+            uint4 e = etab[blk[0]];
+            uint32_t fp = flags_prev;
+#pragma unroll 8
+            for (int s = 0; s < 32; s++) {
+                const uint4 ec = e;
+                e = etab[sym_n];
+                sym_n = blk[(s + 2) * 32];
+                const bool emit = x >= ec.z;
+                st_cur[s * 32] = uint16_t(x);
+                flags |= emit ? (1u << s) : 0u;
+                x = emit ? x >> 16 : x;
+                const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+                x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+
+                const bool em = fp & 1u;
+                fp >>= 1;
+                const uint32_t B = __ballot_sync(kFull, em);
+                if (em) wout[wc + __popc(B & gt)] = st_prev[s * 32];
+                wc += __popc(B);
+            }
+        } else {
+            if (b > 0) flush(st_prev, flags_prev, 32);
+            int s = 0;
+            if (b == 0) {
+                // step T-1, the only one that may be partial; no lane emits a
+                // word there (x = 2^16 is below every 2^20 f)
+                const uint4 ec = etab[blk[0]];
+                const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+                if (first_active) x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+                s = 1;
+            }
+            // rows past the block read the next ring slot (or the stage after
+            // the last slot): harmless values that are never used
+            uint32_t sym_n = blk[(s + 1) * 32];
+            uint4 e = etab[blk[s * 32]];
 #pragma unroll 4
-        for (; s < cnt; s++) {
-            const uint4 ec = e;
-            e = etab[sym_n];
-            sym_n = blk[(s + 2) * 32];
-            const bool emit = x >= ec.z;
-            stage[s * 32] = uint16_t(x);
-            if (emit) flags |= 1u << s;
-            x = emit ? x >> 16 : x;
-            const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
-            x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+            for (; s < cnt; s++) {
+                const uint4 ec = e;
+                e = etab[sym_n];
+                sym_n = blk[(s + 2) * 32];
+                const bool emit = x >= ec.z;
+                st_cur[s * 32] = uint16_t(x);
+                if (emit) flags |= 1u << s;
+                x = emit ? x >> 16 : x;
+                const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+                x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
+            }
         }
-#pragma unroll 4
-        for (int s = 0; s < cnt; s++) {
-            const bool em = (flags >> s) & 1u;
-            const uint32_t B = __ballot_sync(kFull, em);
-            if (em) wout[wc + __popc(B & gt)] = stage[s * 32];
-            wc += __popc(B);
-        }
+        flags_prev = flags;
         __syncwarp();
+        // the words written so far belong to the blocks before this one
         if (words_at + 2ull * wc >= lim) {
             aborted = true;
             break;
         }
+    }
+    if (!aborted) {
+        flush(stage + ((nb - 1) & 1) * 1024, flags_prev, T - 32 * (nb - 1));
+        __syncwarp();
+        aborted = words_at + 2ull * wc >= lim;
     }
     cp_async_wait_all();  // the ring is reused by the next stream
     __syncwarp();
@@ -703,7 +785,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t gw = blockIdx.x * kCodeWarps + warp;
+    const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
     if (gw >= a.workers) return;
     uint4 *etab = reinterpret_cast<uint4 *>(smem_raw + kCodeWarpSmem * warp);
     uint8_t *ring = smem_raw + kCodeWarpSmem * warp + 4096;
@@ -836,8 +918,12 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     stats_kernel<DT><<<sgrid, kStatThreads, ssm, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return ZC_ECUDA;
     if (cudaMemsetAsync(a.ws_ctrl, 0, 4, s) != cudaSuccess) return ZC_ECUDA;  // coder ticket
-    const int cgrid = int((a.workers + kCodeWarps - 1) / kCodeWarps);
-    code_kernel<DT><<<cgrid, kCodeThreads, csm, s>>>(a);
+    // the warps spread evenly over the SMs: CTAs of just enough warps for one
+    // CTA per SM (the block scheduler then gives every SM the same share)
+    const int sms = sms_of_device() < 1 ? 1 : sms_of_device();
+    const uint32_t wpc = std::min<uint32_t>(kCodeWarps, (a.workers + sms - 1) / sms);
+    const int cgrid = int((a.workers + wpc - 1) / wpc);
+    code_kernel<DT><<<cgrid, 32 * wpc, size_t(wpc) * kCodeWarpSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 

@@ -3,6 +3,7 @@
 // arithmetic that combines CRCs of adjacent byte ranges.
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -116,11 +117,11 @@ __device__ __forceinline__ uint32_t crc_word_global(uint32_t c, uint32_t w) {
 // Multiplying a CRC register by a fixed x^(8n) mod P ("appending n zero
 // bytes") is linear in the register, so it is four table lookups, one per
 // register byte. Tables: kShPow + j shifts by 2^j bytes (j = 0..39), then the
-// stride gaps 248, 496, 992, 2032, 4080, 8176 and 65408 bytes used by the
+// stride gaps 248, 496, 992, 2032, 4080, 8176 and 16352 bytes used by the
 // strided CRCs (a round of NT threads x P-byte pieces leaves a gap of
 // (NT - 1) P).
 constexpr int kShPow = 0, kShPowCount = 40, kSh248 = 40, kSh496 = 41, kSh992 = 42, kSh2032 = 43, kSh4080 = 44,
-              kSh8176 = 45, kSh65408 = 46, kShCount = 47;
+              kSh8176 = 45, kSh16352 = 46, kShCount = 47;
 
 struct ShiftTables {
     uint32_t t[kShCount][4][256];
@@ -147,7 +148,7 @@ constexpr ShiftTables make_shift_tables() {
     K[kSh2032] = xpow8(2032);
     K[kSh4080] = xpow8(4080);
     K[kSh8176] = xpow8(8176);
-    K[kSh65408] = xpow8(65408);
+    K[kSh16352] = xpow8(16352);
     for (int c = 0; c < kShCount; c++) {
         // register bit m is the coefficient of x^(31-m); its image is K x^(31-m)
         uint32_t basis[32] = {};
