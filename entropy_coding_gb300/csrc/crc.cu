@@ -23,7 +23,7 @@ __device__ uint32_t warp_crc_raw_any(const uint8_t *p, uint64_t len, uint32_t in
     uint64_t head = (16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15;
     if (head > len) head = len;
     uint32_t reg = init;
-    const uint32_t *row = T + (threadIdx.x & 31);
+    const uint32_t *row = crc_row(T);
     for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, __ldg(p + i), row);
     return crc_strided<1, false>(p + head, len - head, reg, T, G, nullptr);
 }

@@ -38,7 +38,7 @@ constexpr int kThreads = 64 * kPairs;
 constexpr int kCtasPerSM = 2;
 constexpr int kStages = 4;                // symbol groups in flight within a pair
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
-// replicated CRC byte table + shift tables: one group's output (256 W
+// CRC slicing tables + shift tables: one group's output (256 W
 // bytes), half a lane's piece (4 W bytes) and the 496-byte gap
 constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 3 * 4 * 256 * 4;
 constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
@@ -342,7 +342,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, u
                         const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
-    const uint32_t *row = crc_rep + lane;
+    const uint32_t *row = crc_row(crc_rep);
     const uint32_t groups = cx.groups;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(cx.out) & 15) == 0;
     if (cx.have_main) {

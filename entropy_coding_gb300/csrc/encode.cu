@@ -229,7 +229,7 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
 // piece, 16 threads share a copy), far below 2^16.
 template <int W>
 struct StatsSmem {
-    uint32_t crc_rep[kCrcRepWords];  // replicated CRC byte table (32 KB)
+    uint32_t crc_rep[kCrcRepWords];  // CRC slicing tables, 8 copies (32 KB)
     uint32_t gap[4][256];            // register shift over the other threads' pieces
     uint32_t hist[W][128 * 32];
     uint32_t cnt[W][256];            // merged counts
@@ -295,7 +295,7 @@ template <int DT>
 __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
     constexpr int W = WordOf<DT>::W;
     const int tid = threadIdx.x, lane = tid & 31;
-    const uint32_t *row = sm.crc_rep + lane;
+    const uint32_t *row = crc_row(sm.crc_rep);
     uint32_t *hrow = &sm.hist[0][lane];
     uint32_t reg;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {

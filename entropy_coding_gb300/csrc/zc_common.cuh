@@ -196,27 +196,32 @@ __device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
     return c;
 }
 
-// The byte table of the CRC (Sarwate's method: one lookup per byte) held in
-// shared memory once per lane: entry b of lane l is word b * 32 + l, so the
-// 32 lanes of a warp always read 32 different banks. 32 KB per CTA.
-constexpr uint32_t kCrcRepWords = 256 * 32;
+// The CRC tables in shared memory for slicing by four (Kounavis and Berry,
+// 2005): table k holds the register contribution of byte b followed by k zero
+// bytes (kCrc.t[k]), so a 32-bit word is four independent lookups instead of a
+// chain of four. Eight copies interleaved word by word: entry (k, b) of copy r
+// is word (256 k + b) * 8 + r and lane l reads copy l & 7, so a lookup
+// instruction meets at most four lanes per bank. 32 KB per CTA.
+constexpr uint32_t kCrcRepWords = 4 * 256 * 8;
 
 __device__ inline void load_crc_rep(uint32_t *t) {
-    for (uint32_t i = threadIdx.x; i < kCrcRepWords; i += blockDim.x) t[i] = kCrc.t[0][i >> 5];
+    for (uint32_t i = threadIdx.x; i < kCrcRepWords; i += blockDim.x) t[i] = kCrc.t[i >> 11][(i >> 3) & 0xFFu];
 }
 
-// row = table + lane
+// This lane's copy of the tables.
+__device__ __forceinline__ const uint32_t *crc_row(const uint32_t *t) { return t + (threadIdx.x & 7); }
+
+// Sarwate's byte step (table 0); row = crc_row(table)
 __device__ __forceinline__ uint32_t crc_rep_byte(uint32_t c, uint32_t byte, const uint32_t *row) {
-    return row[((c ^ byte) & 0xFFu) << 5] ^ (c >> 8);
+    return row[((c ^ byte) & 0xFFu) << 3] ^ (c >> 8);
 }
 
-// Register update over a little-endian 32-bit word: with u = c ^ w the
-// remaining data bytes ride down in u, so each step is u = T[u & 255] ^ u >> 8.
+// Register update over a little-endian 32-bit word: with u = c ^ w, byte i of
+// u is followed by 3 - i more bytes of the word.
 __device__ __forceinline__ uint32_t crc_rep_word(uint32_t c, uint32_t w, const uint32_t *row) {
-    uint32_t u = c ^ w;
-#pragma unroll
-    for (int k = 0; k < 4; k++) u = row[(u & 0xFFu) << 5] ^ (u >> 8);
-    return u;
+    const uint32_t u = c ^ w;
+    return row[3 * 2048 + ((u & 0xFFu) << 3)] ^ row[2 * 2048 + (((u >> 8) & 0xFFu) << 3)] ^
+           row[1 * 2048 + (((u >> 16) & 0xFFu) << 3)] ^ row[(u >> 24) << 3];
 }
 
 __device__ __forceinline__ uint32_t crc_rep16(uint32_t c, uint4 v, const uint32_t *row) {
@@ -293,7 +298,7 @@ __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t 
     constexpr int NT = 32 * NW;
     static_assert(NT == 32 || NT == 128 || NT == 256 || NT == 512, "strided CRC runs on 1, 4, 8 or 16 warps");
     const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
-    const uint32_t *row = T + (threadIdx.x & 31);
+    const uint32_t *row = crc_row(T);
     const uint64_t main = len & ~uint64_t(15);
     const Strided sp(main, NT);
     uint32_t reg = init;
@@ -323,7 +328,7 @@ __device__ inline uint32_t crc_any(const uint8_t *p, uint64_t len, uint32_t init
                                    const uint32_t (*G)[256], uint32_t *s_reg) {
     uint64_t head = (16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15;
     if (head > len) head = len;
-    const uint32_t *row = T + (threadIdx.x & 31);
+    const uint32_t *row = crc_row(T);
     uint32_t reg = init;
     for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
     return crc_strided<NW, kLdcg>(p + head, len - head, reg, T, G, s_reg);
