@@ -36,19 +36,25 @@ namespace {
 constexpr int kPairs = 8;                 // chunks per CTA at most, one warp pair each
 constexpr int kThreads = 64 * kPairs;
 constexpr int kCtasPerSM = 2;
+constexpr uint64_t kBigPairs = 7;        // pairs per CTA at most with one-level tables (one CTA per SM)
 constexpr int kStages = 4;                // symbol groups in flight within a pair
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
-// CRC slicing tables + shift tables: one group's output (256 W
-// bytes), half a lane's piece (4 W bytes) and the 496-byte gap
-constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 3 * 4 * 256 * 4;
+// CRC slicing tables + shift tables: one group's output (256 W bytes) and
+// the 496-byte gap
+constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
 constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
 
-// Shared memory of one warp pair.
+// Shared memory of one warp pair. With kBig (few pairs per SM) the decoding
+// step reads a one-level table slot -> symbol | f << 8 | (slot - cum) << 20
+// instead of the two-level slot -> symbol -> (f, cum), one dependent load
+// fewer per step.
+template <bool kBig>
 struct PairSmem {
     uint8_t lut[kLutBytes];          // slot -> symbol
     uint32_t sym[256];               // symbol -> f | cum << 12
     uint16_t ring[kRingWords];       // renormalisation words
-    uint8_t stage[kStages][256];     // decoded symbols, row k = step k of a group
+    uint32_t big[kBig ? kM : 1];     // one-level table (kBig)
+    alignas(16) uint8_t stage[kStages][256];  // decoded symbols, row k = step k of a group (read as uint2)
     unsigned long long full[kStages], empty[kStages], start;
     uint32_t flag;                   // producer -> consumer: 1 when the main stream is ready
 };
@@ -89,6 +95,7 @@ struct Rans {
     uint32_t padded;     // pad16(2 * nwords)
     const uint8_t *lut;
     const uint32_t *sym;
+    const uint32_t *big;
     uint16_t *ring;
 };
 
@@ -119,9 +126,11 @@ __device__ __forceinline__ void ring_refill(Rans &r) {
     }
 }
 
-// Parse a rANS record (val bytes) into lookup tables in `slot` and load the
-// lane states and the last two word blocks. Returns false if malformed.
-__device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, Rans &r) {
+// Parse a rANS record (val bytes) into lookup tables in `slot` (and the
+// one-level table `big` when kBig) and load the lane states and the first
+// word blocks. Returns false if malformed.
+template <bool kBig>
+__device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, uint32_t *big, Rans &r) {
     const int lane = threadIdx.x & 31;
     uint8_t *lut = slot;
     uint32_t *sym = reinterpret_cast<uint32_t *>(slot + kLutBytes);
@@ -176,7 +185,15 @@ __device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, Rans
     r.padded = uint32_t(pad16(2 * nwords));
     r.lut = lut;
     r.sym = sym;
+    r.big = big;
     r.ring = reinterpret_cast<uint16_t *>(slot + kLutBytes + kSymBytes);
+    if constexpr (kBig) {
+        __syncwarp();
+        for (uint32_t sl = lane; sl < kM; sl += 32) {
+            const uint32_t sy = lut[sl], e = sym[sy];
+            big[sl] = sy | (e & 0xFFFu) << 8 | (sl - (e >> 12)) << 20;
+        }
+    }
     r.lo = nwords ? int((nwords - 1) >> 8) + 1 : 0;
     __syncwarp();
     ring_refill(r);
@@ -184,11 +201,19 @@ __device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, Rans
 }
 
 // One rANS decode step of the warp: returns this lane's symbol.
+template <bool kBig>
 __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt) {
-    uint32_t slot = r.x & (kM - 1);
-    uint32_t s = r.lut[slot];
-    uint32_t e = r.sym[s];
-    uint32_t xn = (e & 0xFFFu) * (r.x >> kProbBits) + slot - (e >> 12);
+    const uint32_t slot = r.x & (kM - 1);
+    uint32_t s, xn;
+    if constexpr (kBig) {
+        const uint32_t e = r.big[slot];
+        s = e & 0xFFu;
+        xn = ((e >> 8) & 0xFFFu) * (r.x >> kProbBits) + (e >> 20);
+    } else {
+        s = r.lut[slot];
+        const uint32_t e = r.sym[s];
+        xn = (e & 0xFFFu) * (r.x >> kProbBits) + slot - (e >> 12);
+    }
     const bool need = active && xn < kRansL;
     const uint32_t bal = __ballot_sync(kFull, need);
     // every lane reads its candidate word (in bounds of the ring), so no branch
@@ -267,8 +292,8 @@ __device__ bool parse_directory(const uint8_t *p, uint32_t stored, uint32_t n, C
 // Producer warp: staged streams into the output tail, then the main stream's
 // symbols group by group into the stage queue (the last group may be
 // partial: steps past the stream leave the states alone).
-template <int DT>
-__device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
+template <int DT, bool kBig>
+__device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem<kBig> &ps) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint32_t lt = lanemask_lt();
@@ -279,13 +304,13 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
         for (int j = 0; j < W; j++) {
             if (cx.kind[j] != kKStaged) continue;
             Rans r;
-            if (!rans_setup(cx.p + cx.roff[j], cx.val[j], slot, r)) bad = true;
+            if (!rans_setup<kBig>(cx.p + cx.roff[j], cx.val[j], slot, ps.big, r)) bad = true;
             if (!bad) {
                 for (uint32_t t = 0; t < cx.T; t++) {
                     const uint32_t i = t * 32 + lane;
                     const bool active = i < cx.n;
                     ring_refill(r);
-                    const uint32_t s = rans_step(r, active, lt);
+                    const uint32_t s = rans_step<kBig>(r, active, lt);
                     if (active) cx.tail[uint64_t(i) * cx.q + cx.sub[j]] = uint8_t(s);
                 }
                 bad |= !rans_final_ok(r);
@@ -298,7 +323,8 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
     Rans rs;
 #pragma unroll
     for (int j = 0; j < W; j++)
-        if (!bad && cx.kind[j] == kKMain && !rans_setup(cx.p + cx.roff[j], cx.val[j], slot, rs)) bad = true;
+        if (!bad && cx.kind[j] == kKMain && !rans_setup<kBig>(cx.p + cx.roff[j], cx.val[j], slot, ps.big, rs))
+            bad = true;
     if (lane == 0) ps.flag = bad ? 0u : 1u;
     __syncwarp();
     mbar_arrive(&ps.start);
@@ -321,7 +347,7 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
         for (int s = 0; s < 8; s++) {
             const uint32_t t = 8 * g + s;
             const bool active = t < cx.T && t * 32 + lane < cx.n;
-            st[32 * s + lane] = uint8_t(rans_step(rs, active, lt));
+            st[32 * s + lane] = uint8_t(rans_step<kBig>(rs, active, lt));
         }
         mbar_arrive(&ps.full[k]);
     }
@@ -336,10 +362,9 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps) {
 // piece taken from zero (linearity); the lanes are folded at the end
 // (crc_fold) and the elements after the last whole group are added from the
 // output.
-template <int DT, bool kVerify>
-__device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, uint32_t expect_crc,
-                        const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*hshift)[256],
-                        const uint32_t (*gap496)[256]) {
+template <int DT, bool kVerify, class PS>
+__device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
+                        const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint32_t *row = crc_row(crc_rep);
@@ -408,11 +433,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, u
                 v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
                 v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
             }
-            if constexpr (kVerify) {
-                // two independent 16-byte halves, joined by a 16-byte shift
-                const uint32_t p0 = crc_rep16(cin, v[0], row), p1 = crc_rep16(0u, v[1], row);
-                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ shift_smem(p0, hshift) ^ p1;
-            }
+            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(crc_rep16(cin, v[0], row), v[1], row);
             if (vec_ok) {
                 uint4 *o = reinterpret_cast<uint4 *>(cx.out + 4ull * e0);
                 o[0] = v[0];
@@ -428,12 +449,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, u
             v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
             v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
             v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
-            if constexpr (kVerify) {
-                // two independent 8-byte halves, joined by an 8-byte shift
-                const uint32_t p0 = crc_rep_word(crc_rep_word(cin, v.x, row), v.y, row);
-                const uint32_t p1 = crc_rep_word(crc_rep_word(0u, v.z, row), v.w, row);
-                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ shift_smem(p0, hshift) ^ p1;
-            }
+            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(cin, v, row);
             if (vec_ok) {
                 *reinterpret_cast<uint4 *>(cx.out + 2ull * e0) = v;
             } else {
@@ -494,10 +510,9 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PairSmem &ps, u
     }
 }
 
-template <int DT>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, PairSmem &ps, const uint32_t *crc_rep,
-                             const uint32_t (*gshift)[256], const uint32_t (*hshift)[256],
-                             const uint32_t (*gap496)[256]) {
+template <int DT, bool kBig>
+__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, PairSmem<kBig> &ps, const uint32_t *crc_rep,
+                             const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
@@ -549,33 +564,31 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, Pai
     cx.groups = n / 256;
     cx.tail = out + (len - cx.q * n);
     if (producer) {
-        if (cx.have_main) produce<DT>(a, cx, ps);
+        if (cx.have_main) produce<DT, kBig>(a, cx, ps);
     } else if (verify) {
-        consume<DT, true>(a, cx, ps, ent.w, crc_rep, gshift, hshift, gap496);
+        consume<DT, true>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     } else {
-        consume<DT, false>(a, cx, ps, ent.w, crc_rep, gshift, hshift, gap496);
+        consume<DT, false>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     }
 }
 
-template <int DT>
+template <int DT, bool kBig>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int W = WordOf<DT>::W;
     uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
     uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
-    uint32_t(*hshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
-    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 8 * 256 * 4);
-    PairSmem *pairs = reinterpret_cast<PairSmem *>(smem + kCrcSmem);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
+    PairSmem<kBig> *pairs = reinterpret_cast<PairSmem<kBig> *>(smem + kCrcSmem);
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep(crc_rep);
         load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
-        load_shift_smem(hshift, kShPow + (W == 4 ? 4 : W == 2 ? 3 : 2));  // 4 W bytes
         load_shift_smem(gap496, kSh496);
     }
     const uint32_t pairs_per_cta = blockDim.x >> 6;
     if (threadIdx.x < pairs_per_cta) {
-        PairSmem &ps = pairs[threadIdx.x];
+        PairSmem<kBig> &ps = pairs[threadIdx.x];
         for (int k = 0; k < kStages; k++) {
             mbar_init(&ps.full[k], 32);
             mbar_init(&ps.empty[k], 32);
@@ -585,25 +598,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs
     __syncthreads();
     const uint32_t c = blockIdx.x * pairs_per_cta + (warp >> 1);
     if (c >= a.n_chunks) return;
-    decode_chunk<DT>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, hshift, gap496);
+    decode_chunk<DT, kBig>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
+}
+
+template <int DT, bool kBig>
+int launch_decode_mode(const DecodeArgs &a, uint32_t pc, cudaStream_t s) {
+    const size_t smem = kCrcSmem + size_t(pc) * sizeof(PairSmem<kBig>);
+    const size_t smem_max = kCrcSmem + size_t(kPairs) * sizeof(PairSmem<kBig>);
+    if (cudaFuncSetAttribute(decode_kernel<DT, kBig>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(std::min<size_t>(smem_max, 227 * 1024))) != cudaSuccess)
+        return ZC_ECUDA;
+    const int grid = int((a.n_chunks + pc - 1) / pc);
+    decode_kernel<DT, kBig><<<grid, 64 * pc, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
 template <int DT>
 int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
-    const size_t smem_max = kCrcSmem + size_t(kPairs) * sizeof(PairSmem);
-    if (cudaFuncSetAttribute(decode_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max)) !=
-        cudaSuccess)
-        return ZC_ECUDA;
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ECUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ZC_ECUDA;
-    // pairs per CTA: just enough for kCtasPerSM CTAs per SM to hold every
-    // chunk, so that the chunks spread evenly over the SMs
+    // Few chunks per SM (the rANS chains are then the critical path): one CTA
+    // per SM holding all its chunks, with one-level tables. Many: pairs per
+    // CTA just enough for kCtasPerSM CTAs per SM to hold every chunk, with
+    // the smaller two-level tables. Either way the chunks spread evenly over
+    // the SMs.
+    const uint64_t per_sm = (a.n_chunks + sms - 1) / uint64_t(sms);
+    if (per_sm <= kBigPairs) return launch_decode_mode<DT, true>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
     const uint64_t slots = uint64_t(sms) * kCtasPerSM;
     const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.n_chunks + slots - 1) / slots));
-    const int grid = int((a.n_chunks + pc - 1) / pc);
-    decode_kernel<DT><<<grid, 64 * pc, kCrcSmem + size_t(pc) * sizeof(PairSmem), s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+    return launch_decode_mode<DT, false>(a, pc, s);
 }
 
 } // namespace

@@ -183,6 +183,43 @@ def test_many_chunks_lookback(zco):
     check_parity(zco, raw, 4, (raw.size // 2,), 64, 0.95)
 
 
+def _compress_with_workspace(raw: np.ndarray, dtype: int, chunk: int, thr: float, ws_bytes: int) -> bytes:
+    nbytes = raw.size
+    src = torch.from_numpy(raw).to(DEV)
+    cap = zc.blob_size(nbytes, dtype, chunk, thr)
+    blob = torch.full((cap,), 0xAB, dtype=torch.uint8, device=DEV)
+    ws = torch.full((ws_bytes,), 0x5A, dtype=torch.uint8, device=DEV)
+    nb = torch.zeros(1, dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    zc.compress_into(src, blob, nb, ws, st, chunk, thr, dtype=dtype, shape=(nbytes // W_OF[dtype],))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return blob[: int(nb.item())].cpu().numpy().tobytes()
+
+
+@pytest.mark.parametrize("dtype,thr", [(6, 0.95), (4, 0.95), (1, 2.0)])
+def test_small_workspace_many_waves(zco, dtype, thr):
+    """A workspace far below zc_workspace_size: one coding warp and waves of a
+    few chunks each, the offset scan running across the waves."""
+    rng = np.random.default_rng(5 + dtype)
+    raw = _rand_tensor(rng, dtype, 75_000)
+    chunk = 4096
+    ref = zco.compress(raw, dtype, (raw.size // W_OF[dtype],), chunk, thr)
+    nc = (raw.size + chunk - 1) // chunk
+    W = W_OF[dtype]
+    n_pad = (chunk // W + 31) // 32 * 32
+    per_chunk = 32 + W * (512 + n_pad)
+    full = zc.workspace_size(raw.size, dtype, chunk)
+    # control + status words, room for about 5 chunks of a wave, and slots for
+    # one coding warp (bounded by a generous record size)
+    small = 256 + (8 * nc + 255) // 256 * 256 + 5 * per_chunk + 1024 + 2 * W * (2 * chunk // W + 4096)
+    assert small < full
+    got = _compress_with_workspace(raw, dtype, chunk, thr, small)
+    assert got == ref, "blob differs from the oracle's with a small workspace"
+    st, back = gpu_decompress_bytes(got)
+    assert st == 0 and back.tobytes() == raw.tobytes()
+
+
 def test_constant_and_special_tensors(zco):
     for dtype, word in ((4, 0x3F80), (6, 0x3F800000), (5, 0x3C00), (4, 0x0000), (6, 0x7FC00001)):
         W = W_OF[dtype]
