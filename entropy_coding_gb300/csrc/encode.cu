@@ -306,19 +306,23 @@ __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<Word
         uint32_t R = 0;
         // the next round's two vectors are in flight while this round's are
         // counted and checksummed
+        // a piece is one 32-byte load when the chunk is 32-byte aligned (a warp
+        // then reads 1 KiB contiguously), else two 16-byte loads
+        const bool wide = (reinterpret_cast<uintptr_t>(src) & 31) == 0;
+        auto load_piece = [&](int32_t pi, uint4 &lo, uint4 &hi) {
+            const uint8_t *p = src + uint64_t(pi) * kPiece;
+            if (wide) {
+                ldg32(p, lo, hi);
+            } else {
+                lo = __ldg(reinterpret_cast<const uint4 *>(p));
+                hi = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+            }
+        };
         uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
-        if (rounds && pidx >= 0) {
-            const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx) * kPiece);
-            n0 = __ldg(p);
-            n1 = __ldg(p + 1);
-        }
+        if (rounds && pidx >= 0) load_piece(pidx, n0, n1);
         for (uint32_t r = 0; r < rounds; r++, pidx += kStatThreads) {
             const uint4 q0 = n0, q1 = n1;
-            if (r + 1 < rounds) {
-                const uint4 *p = reinterpret_cast<const uint4 *>(src + uint64_t(pidx + kStatThreads) * kPiece);
-                n0 = __ldg(p);
-                n1 = __ldg(p + 1);
-            }
+            if (r + 1 < rounds) load_piece(pidx + kStatThreads, n0, n1);
             uint32_t c = r == 0 ? (pidx == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, sm.gap);
             if (pidx >= 0) {
                 c = crc_rep16(crc_rep16(c, q0, row), q1, row);

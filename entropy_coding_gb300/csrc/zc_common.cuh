@@ -334,6 +334,13 @@ __device__ inline uint32_t crc_any(const uint8_t *p, uint64_t len, uint32_t init
     return crc_strided<NW, kLdcg>(p + head, len - head, reg, T, G, s_reg);
 }
 
+// One 32-byte read-only global load (p 32-byte aligned) as two 16-byte halves.
+__device__ __forceinline__ void ldg32(const void *p, uint4 &lo, uint4 &hi) {
+    asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+}
+
 // 16-byte asynchronous global -> shared copies (both addresses 16-aligned).
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
