@@ -41,7 +41,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="fp32_64m",
-                   choices=["fp32_64m", "bf16_1m", "fp32clean_64m", "fp16_16m", "bf16_delta", "bf16_llama_gate"])
+                   choices=["fp32_64m", "bf16_1m", "fp32clean_64m", "fp16_16m", "bf16_delta", "bf16_delta_fused",
+                            "bf16_llama_gate"])
     p.add_argument("--chunk-bytes", type=int, default=131072)
     p.add_argument("--threshold", type=float, default=0.95)
     p.add_argument("--e2e-steps", type=int, default=5)
@@ -61,6 +62,11 @@ def make_workload(name: str, device):
         return wl.fp16_16m(device), "FP16 4096x4096 N(0,0.05) seed 3"
     if name == "bf16_delta":
         return wl.bf16_delta(device)[1], "U16 XOR of two BF16 4096x14336 checkpoints, seed 4"
+    if name == "bf16_delta_fused":
+        # the coded bytes are the XOR difference (what the oracle codes); the
+        # GPU arm forms it inside the kernels from the two checkpoints
+        return (wl.bf16_delta(device)[1], "two BF16 4096x14336 checkpoints, seed 4, XOR difference formed in "
+                                          "the kernels (compress_delta / decompress_delta)")
     if name == "bf16_llama_gate":
         specs = wl.llama8b_specs()
         nm, shape = specs[5]
@@ -245,6 +251,10 @@ def main():
     t, desc = make_workload(a.workload, dev)
     code = wl.dtype_code(t)
     src = wl.as_bytes(t)
+    base = None
+    if a.workload == "bf16_delta_fused":
+        ta, tb = wl.bf16_delta_pair(dev)
+        base, src = wl.as_bytes(ta), wl.as_bytes(tb)
     N = src.numel()
     C, thr = a.chunk_bytes, a.threshold
     cap = zc.blob_size(N, code, C, thr)
@@ -255,22 +265,34 @@ def main():
     out = torch.empty(N, dtype=torch.uint8, device=dev)
     shape = tuple(t.shape)
 
+    def comp(inp):
+        if base is None:
+            zc.compress_into(inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+        else:
+            zc.compress_delta_into(base, inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+
+    def decomp(info):
+        if base is None:
+            zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+        else:
+            zc.decompress_delta_into(blob, info, base, out, st, not a.no_verify, stream)
+
     # first pass outside timing: blob length, header, correctness
     with torch.cuda.stream(stream):
-        zc.compress_into(src, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+        comp(src)
     stream.synchronize()
     S = int(nb.item())
     assert int(st.item()) == 0
     info = zc.blob_info(blob[: 96 + 16 * ((N + C - 1) // C)].cpu())
     with torch.cuda.stream(stream):
-        zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+        decomp(info)
     stream.synchronize()
     assert int(st.item()) == 0 and torch.equal(out, src), "round trip failed"
 
     def one_step(ev):
-        zc.compress_into(src, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+        comp(src)
         ev[1].record(stream)
-        zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+        decomp(info)
         ev[2].record(stream)
 
     with torch.cuda.stream(stream):
@@ -307,17 +329,22 @@ def main():
     h2d = d2h = 0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    if base is not None:  # the base checkpoint travels with each step too
+        h_base = torch.empty(N, dtype=torch.uint8, pin_memory=True)
+        h_base.copy_(base.cpu())
     for _ in range(a.e2e_steps):
         with torch.cuda.stream(stream):
+            if base is not None:
+                base.copy_(h_base, non_blocking=True)
             d_in.copy_(h_src, non_blocking=True)
-            zc.compress_into(d_in, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+            comp(d_in)
             s_bytes = int(nb.item())
             h_blob[:s_bytes].copy_(blob[:s_bytes], non_blocking=True)
             blob[:s_bytes].copy_(h_blob[:s_bytes], non_blocking=True)
-            zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+            decomp(info)
             h_out.copy_(out, non_blocking=True)
         stream.synchronize()
-        h2d += N + s_bytes
+        h2d += N + s_bytes + (N if base is not None else 0)
         d2h += s_bytes + 8 + N
     t_e2e = time.perf_counter() - t0
     assert torch.equal(h_out, h_src)
@@ -329,8 +356,11 @@ def main():
     hbm, peak_kind = peaks()
     enc_gbs = N * a.steps / t_enc / 1e9
     dec_gbs = N * a.steps / t_dec / 1e9
-    enc_ach = (N + S) * a.steps / t_enc / 1e9
-    dec_ach = (N + S) * a.steps / t_dec / 1e9
+    # algorithmic bytes per call: the input and the blob (a delta also reads
+    # the base checkpoint, in both directions)
+    alg = N + S + (N if base is not None else 0)
+    enc_ach = alg * a.steps / t_enc / 1e9
+    dec_ach = alg * a.steps / t_dec / 1e9
     # the decompression call is one kernel (decode_kernel), the largest single
     # kernel of the step; compression is two (statistics, coding), each
     # shorter (profiles/launches_*.md), so the live roofline is decode's
@@ -353,7 +383,7 @@ def main():
         "size_pct": round(100.0 * S / N, 3),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": N + S},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": alg},
         "clocks": clk.summary(),
         "e2e": {"value": round(N * a.e2e_steps / t_e2e / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d // a.e2e_steps, "d2h_bytes_per_step": d2h // a.e2e_steps},

@@ -21,7 +21,8 @@ from . import build as _build
 from .workloads import BF16, FP16, FP32, U8, U16, U32
 
 __all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspace_size",
-           "compress_into", "decompress_into", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
+           "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
+           "decompress_delta_into", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
            "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
 
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
@@ -78,6 +79,11 @@ def lib() -> ctypes.CDLL:
                                       vp, u64, vp, vp, u64, vp, vp]
             L.zc_decompress.restype = i32
             L.zc_decompress.argtypes = [vp, ctypes.POINTER(_Info), vp, u64, u32, vp, vp]
+            L.zc_compress_delta.restype = i32
+            L.zc_compress_delta.argtypes = [vp, vp, u64, i32, i32, ctypes.POINTER(ctypes.c_int64), u32, dbl,
+                                            vp, u64, vp, vp, u64, vp, vp]
+            L.zc_decompress_delta.restype = i32
+            L.zc_decompress_delta.argtypes = [vp, ctypes.POINTER(_Info), vp, vp, u64, u32, vp, vp]
             L.zc_crc32.restype = i32
             L.zc_crc32.argtypes = [vp, u64, u64, vp, vp]
             _lib = L
@@ -205,6 +211,79 @@ def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True
     status = torch.zeros(1, dtype=torch.int32, device=blob.device)
     decompress_into(blob, info, out, status, verify, stream)
     _check(int(status.item()), "zc_decompress (device)")
+    return out
+
+
+_WORD_CODE = {1: U8, 2: U16, 4: U32}
+
+
+def compress_delta_into(base: torch.Tensor, new: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tensor,
+                        workspace: torch.Tensor, status: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK,
+                        threshold: float = DEFAULT_THRESHOLD, stream=None, dtype: int | None = None,
+                        shape=None) -> None:
+    """Launch fused delta compression of (base XOR new) into caller buffers;
+    no allocation, no sync. dtype: U8/U16/U32 (default: by element size)."""
+    if base.numel() * base.element_size() != new.numel() * new.element_size():
+        raise ZcError(EINVAL, "base and new differ in size")
+    code = _WORD_CODE[new.element_size()] if dtype is None else dtype
+    shape = tuple(new.shape) if shape is None else tuple(shape)
+    shp = (ctypes.c_int64 * max(1, len(shape)))(*shape)
+    nbytes = new.numel() * new.element_size()
+    st = lib().zc_compress_delta(base.data_ptr() if nbytes else None, new.data_ptr() if nbytes else None, nbytes,
+                                 code, len(shape), shp, chunk_bytes, threshold, blob.data_ptr(), blob.numel(),
+                                 blob_bytes.data_ptr(), workspace.data_ptr(), workspace.numel(), status.data_ptr(),
+                                 _stream(stream))
+    _check(st, "zc_compress_delta")
+
+
+def compress_delta(base: torch.Tensor, new: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK,
+                   threshold: float = DEFAULT_THRESHOLD, stream=None) -> torch.Tensor:
+    """Blob of the XOR difference of two same-shape CUDA tensors (a checkpoint
+    against its base), formed on the fly; synchronises once for the length."""
+    if not (base.is_cuda and new.is_cuda) or base.shape != new.shape or base.dtype != new.dtype:
+        raise ZcError(EINVAL, "compress_delta expects two CUDA tensors of one shape and dtype")
+    b, n = base.contiguous(), new.contiguous()
+    code = _WORD_CODE.get(n.element_size())
+    if code is None:
+        raise ZcError(EINVAL, f"unsupported element size {n.element_size()}")
+    nbytes = n.numel() * n.element_size()
+    cap = blob_size(nbytes, code, chunk_bytes, threshold)
+    if cap == 0:
+        raise ZcError(EINVAL, "invalid compression parameters")
+    dev = n.device
+    blob = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, workspace_size(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    compress_delta_into(b.view(-1).view(torch.uint8), n.view(-1).view(torch.uint8), blob, nb, ws, status,
+                        chunk_bytes, threshold, stream, dtype=code, shape=tuple(n.shape))
+    _check(int(status.item()), "zc_compress_delta (device)")
+    return blob[: int(nb.item())]
+
+
+def decompress_delta_into(blob: torch.Tensor, info: dict, base: torch.Tensor, out: torch.Tensor,
+                          status: torch.Tensor, verify: bool = True, stream=None) -> None:
+    """Launch decompression of a difference blob XOR-ed with base into out."""
+    st = lib().zc_decompress_delta(blob.data_ptr(), ctypes.byref(_info_struct(info)), base.data_ptr(),
+                                   out.data_ptr(), out.numel() * out.element_size(), 0 if verify else NO_VERIFY,
+                                   status.data_ptr(), _stream(stream))
+    _check(st, "zc_decompress_delta")
+
+
+def decompress_delta(blob: torch.Tensor, base: torch.Tensor, info: dict | None = None, verify: bool = True,
+                     stream=None) -> torch.Tensor:
+    """The checkpoint `new` from its difference blob and the base tensor."""
+    if not (blob.is_cuda and base.is_cuda):
+        raise ZcError(EINVAL, "decompress_delta expects a CUDA blob and base")
+    info = read_info(blob) if info is None else info
+    b = base.contiguous()
+    if b.numel() * b.element_size() != info["nbytes"]:
+        raise ZcError(EINVAL, "base size does not match the blob")
+    out = torch.empty_like(b)
+    status = torch.zeros(1, dtype=torch.int32, device=blob.device)
+    decompress_delta_into(blob, info, b.view(-1).view(torch.uint8), out.view(-1).view(torch.uint8), status,
+                          verify, stream)
+    _check(int(status.item()), "zc_decompress_delta (device)")
     return out
 
 

@@ -87,6 +87,13 @@ __device__ bool mbar_wait(unsigned long long *b, uint32_t parity) {
     }
 }
 
+template <int W>
+__device__ __forceinline__ uint32_t load_word_any(const uint8_t *p) {
+    if (W == 4) return *reinterpret_cast<const uint32_t *>(p);
+    if (W == 2) return *reinterpret_cast<const uint16_t *>(p);
+    return *p;
+}
+
 struct Rans {
     uint32_t x;          // this lane's state
     int32_t ptr;         // words left to consume (warp-uniform)
@@ -244,6 +251,7 @@ struct ChunkCtx {
     const uint8_t *p;      // payload
     uint8_t *out;          // output range
     uint8_t *tail;         // staged bytes of the coded streams after the first
+    const uint8_t *base;   // delta: the base tensor's bytes of this chunk (the output is decoded XOR base)
     uint32_t n, len, q, groups, T;
     bool have_main;
     uint32_t kind[4], val[4], roff[4], sub[4];
@@ -362,7 +370,7 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem<kBig> 
 // piece taken from zero (linearity); the lanes are folded at the end
 // (crc_fold) and the elements after the last whole group are added from the
 // output.
-template <int DT, bool kVerify, class PS>
+template <int DT, bool kVerify, bool kDelta, class PS>
 __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
                         const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
@@ -387,6 +395,22 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
     }
     for (uint32_t g = 0; g < groups; g++) {
         const uint32_t k = g % kStages, r = g / kStages;
+        // delta: the base bytes this group's output is XOR-ed with, loaded
+        // before they are needed (delta buffers are 16-byte aligned)
+        uint4 bv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if constexpr (kDelta) {
+            const uint64_t b0 = uint64_t(W) * (256 * g + 8 * lane);
+            if constexpr (W == 4) {
+                bv[0] = __ldcs(reinterpret_cast<const uint4 *>(cx.base + b0));
+                bv[1] = __ldcs(reinterpret_cast<const uint4 *>(cx.base + b0) + 1);
+            } else if constexpr (W == 2) {
+                bv[0] = __ldcs(reinterpret_cast<const uint4 *>(cx.base + b0));
+            } else {
+                const uint2 t = __ldcs(reinterpret_cast<const uint2 *>(cx.base + b0));
+                bv[0] = make_uint4(t.x, t.y, 0, 0);
+            }
+        }
+        auto xb = [](uint4 v, const uint4 &b) { return make_uint4(v.x ^ b.x, v.y ^ b.y, v.z ^ b.z, v.w ^ b.w); };
         Col8 col[W];
 #pragma unroll
         for (int j = 0; j < W; j++) {
@@ -434,6 +458,10 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
             }
             if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(crc_rep16(cin, v[0], row), v[1], row);
+            if constexpr (kDelta) {
+                v[0] = xb(v[0], bv[0]);
+                v[1] = xb(v[1], bv[1]);
+            }
             if (vec_ok) {
                 uint4 *o = reinterpret_cast<uint4 *>(cx.out + 4ull * e0);
                 o[0] = v[0];
@@ -450,6 +478,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
             v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
             if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(cin, v, row);
+            if constexpr (kDelta) v = xb(v, bv[0]);
             if (vec_ok) {
                 *reinterpret_cast<uint4 *>(cx.out + 2ull * e0) = v;
             } else {
@@ -464,6 +493,10 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             if constexpr (kVerify) {
                 const uint32_t piece = crc_rep_word(crc_rep_word(cin, col[0].lo, row), col[0].hi, row);
                 Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ piece;
+            }
+            if constexpr (kDelta) {
+                col[0].lo ^= bv[0].x;
+                col[0].hi ^= bv[0].y;
             }
             if ((reinterpret_cast<uintptr_t>(cx.out) & 7) == 0) {
                 *reinterpret_cast<uint2 *>(cx.out + e0) = make_uint2(col[0].lo, col[0].hi);
@@ -494,7 +527,8 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 else b = __ldcg(cx.tail + uint64_t(i) * cx.q + cx.sub[j]);
                 word = (word << 8) | b;
             }
-            const uint32_t w = Perm<DT>::inv(word);
+            uint32_t w = Perm<DT>::inv(word);
+            if constexpr (kDelta) w ^= load_word_any<W>(cx.base + uint64_t(i) * W);
             if (W == 4) reinterpret_cast<uint32_t *>(cx.out)[i] = w;
             else if (W == 2) reinterpret_cast<uint16_t *>(cx.out)[i] = uint16_t(w);
             else cx.out[i] = uint8_t(w);
@@ -505,12 +539,18 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
         constexpr int kLogPiece = W == 4 ? 5 : W == 2 ? 4 : 3;
         uint32_t reg = groups ? crc_fold<1>(Rl, kLogPiece, nullptr) : 0xFFFFFFFFu;
         const uint32_t done = groups * 256 * W;
-        reg = crc_any<1, true>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
+        if constexpr (kDelta) {
+            // the check is of the decoded bytes, before the XOR (only the last,
+            // partial chunk has elements after its whole groups)
+            for (uint32_t i = done; i < cx.len; i++) reg = crc_rep_byte(reg, __ldcg(cx.out + i) ^ cx.base[i], row);
+        } else {
+            reg = crc_any<1, true>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
+        }
         if ((reg ^ 0xFFFFFFFFu) != expect_crc && lane == 0) status_or(a.d_status, ZC_ECRC);
     }
 }
 
-template <int DT, bool kBig>
+template <int DT, bool kBig, bool kDelta>
 __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, PairSmem<kBig> &ps, const uint32_t *crc_rep,
                              const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
@@ -538,12 +578,19 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, Pai
     const uint8_t *p = a.blob + off;
     const bool verify = !(a.flags & ZC_NO_VERIFY);
     uint8_t *out = a.dst + uint64_t(c) * a.chunk_bytes;
+    const uint8_t *basec = kDelta ? a.base + uint64_t(c) * a.chunk_bytes : nullptr;
     if (raw) {
         if (producer) return;
         uint32_t nvec = (reinterpret_cast<uintptr_t>(out) & 15) ? 0 : len / 16;
-        for (uint32_t v = lane; v < nvec; v += 32)
-            reinterpret_cast<uint4 *>(out)[v] = __ldg(reinterpret_cast<const uint4 *>(p) + v);
-        for (uint32_t i = nvec * 16 + lane; i < len; i += 32) out[i] = p[i];
+        for (uint32_t v = lane; v < nvec; v += 32) {
+            uint4 t = __ldg(reinterpret_cast<const uint4 *>(p) + v);
+            if constexpr (kDelta) {
+                const uint4 b = __ldcs(reinterpret_cast<const uint4 *>(basec) + v);
+                t.x ^= b.x; t.y ^= b.y; t.z ^= b.z; t.w ^= b.w;
+            }
+            reinterpret_cast<uint4 *>(out)[v] = t;
+        }
+        for (uint32_t i = nvec * 16 + lane; i < len; i += 32) out[i] = kDelta ? uint8_t(p[i] ^ basec[i]) : p[i];
         // a RAW chunk stores the original bytes, so its CRC is the payload's
         if (verify && (crc_strided<1, false>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
             lane == 0)
@@ -563,16 +610,17 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, Pai
     cx.T = (n + 31) / 32;
     cx.groups = n / 256;
     cx.tail = out + (len - cx.q * n);
+    cx.base = basec;
     if (producer) {
         if (cx.have_main) produce<DT, kBig>(a, cx, ps);
     } else if (verify) {
-        consume<DT, true>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
+        consume<DT, true, kDelta>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     } else {
-        consume<DT, false>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
+        consume<DT, false, kDelta>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     }
 }
 
-template <int DT, bool kBig>
+template <int DT, bool kBig, bool kDelta>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int W = WordOf<DT>::W;
@@ -598,22 +646,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs
     __syncthreads();
     const uint32_t c = blockIdx.x * pairs_per_cta + (warp >> 1);
     if (c >= a.n_chunks) return;
-    decode_chunk<DT, kBig>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
+    decode_chunk<DT, kBig, kDelta>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
 }
 
-template <int DT, bool kBig>
+template <int DT, bool kBig, bool kDelta>
 int launch_decode_mode(const DecodeArgs &a, uint32_t pc, cudaStream_t s) {
     const size_t smem = kCrcSmem + size_t(pc) * sizeof(PairSmem<kBig>);
     const size_t smem_max = kCrcSmem + size_t(kPairs) * sizeof(PairSmem<kBig>);
-    if (cudaFuncSetAttribute(decode_kernel<DT, kBig>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_kernel<DT, kBig, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(std::min<size_t>(smem_max, 227 * 1024))) != cudaSuccess)
         return ZC_ECUDA;
     const int grid = int((a.n_chunks + pc - 1) / pc);
-    decode_kernel<DT, kBig><<<grid, 64 * pc, smem, s>>>(a);
+    decode_kernel<DT, kBig, kDelta><<<grid, 64 * pc, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
-template <int DT>
+template <int DT, bool kDelta>
 int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ECUDA;
@@ -624,10 +672,11 @@ int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     // the smaller two-level tables. Either way the chunks spread evenly over
     // the SMs.
     const uint64_t per_sm = (a.n_chunks + sms - 1) / uint64_t(sms);
-    if (per_sm <= kBigPairs) return launch_decode_mode<DT, true>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
+    if (per_sm <= kBigPairs)
+        return launch_decode_mode<DT, true, kDelta>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
     const uint64_t slots = uint64_t(sms) * kCtasPerSM;
     const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.n_chunks + slots - 1) / slots));
-    return launch_decode_mode<DT, false>(a, pc, s);
+    return launch_decode_mode<DT, false, kDelta>(a, pc, s);
 }
 
 } // namespace
@@ -635,12 +684,13 @@ int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
 int launch_decode(int dtype, const DecodeArgs &a, cudaStream_t s) {
     if (a.n_chunks == 0) return ZC_OK;
     switch (dtype) {
-    case ZC_U8: return launch_decode_t<ZC_U8>(a, s);
-    case ZC_U16: return launch_decode_t<ZC_U16>(a, s);
-    case ZC_U32: return launch_decode_t<ZC_U32>(a, s);
-    case ZC_BF16: return launch_decode_t<ZC_BF16>(a, s);
-    case ZC_FP16: return launch_decode_t<ZC_FP16>(a, s);
-    case ZC_FP32: return launch_decode_t<ZC_FP32>(a, s);
+    case ZC_U8: return a.base ? launch_decode_t<ZC_U8, true>(a, s) : launch_decode_t<ZC_U8, false>(a, s);
+    case ZC_U16: return a.base ? launch_decode_t<ZC_U16, true>(a, s) : launch_decode_t<ZC_U16, false>(a, s);
+    case ZC_U32: return a.base ? launch_decode_t<ZC_U32, true>(a, s) : launch_decode_t<ZC_U32, false>(a, s);
+    // deltas are coded as unsigned words only
+    case ZC_BF16: return a.base ? ZC_EINVAL : launch_decode_t<ZC_BF16, false>(a, s);
+    case ZC_FP16: return a.base ? ZC_EINVAL : launch_decode_t<ZC_FP16, false>(a, s);
+    case ZC_FP32: return a.base ? ZC_EINVAL : launch_decode_t<ZC_FP32, false>(a, s);
     default: return ZC_EINVAL;
     }
 }

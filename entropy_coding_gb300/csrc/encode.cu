@@ -101,6 +101,54 @@ __device__ __forceinline__ uint32_t stream_byte(uint32_t perm, int j) {
     return (perm >> (8 * (W - 1 - j))) & 0xFFu;
 }
 
+// The bytes a compression kernel reads: a tensor, or for a checkpoint delta
+// (ZipNN note, Method 6: XOR against a base) the XOR of two tensors of the
+// same layout, formed as it is read (kDelta), so that the difference never
+// goes through memory.
+template <bool kDelta>
+struct Source {
+    const uint8_t *p;  // the tensor (for a delta, the new one)
+    const uint8_t *x;  // the base tensor (kDelta only)
+    __device__ __forceinline__ Source at(uint64_t o) const { return Source{p + o, kDelta ? x + o : nullptr}; }
+    // bits that must be clear for an access of that alignment
+    __device__ __forceinline__ uintptr_t addr_bits() const {
+        return reinterpret_cast<uintptr_t>(p) | (kDelta ? reinterpret_cast<uintptr_t>(x) : 0);
+    }
+    __device__ __forceinline__ uint4 vec(uint64_t o) const {
+        uint4 v = __ldg(reinterpret_cast<const uint4 *>(p + o));
+        if constexpr (kDelta) {
+            const uint4 b = __ldg(reinterpret_cast<const uint4 *>(x + o));
+            v.x ^= b.x; v.y ^= b.y; v.z ^= b.z; v.w ^= b.w;
+        }
+        return v;
+    }
+    __device__ __forceinline__ uint4 vec_last(uint64_t o) const {  // last use: evict first
+        uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p + o));
+        if constexpr (kDelta) {
+            const uint4 b = __ldcs(reinterpret_cast<const uint4 *>(x + o));
+            v.x ^= b.x; v.y ^= b.y; v.z ^= b.z; v.w ^= b.w;
+        }
+        return v;
+    }
+    __device__ __forceinline__ void vec32(uint64_t o, uint4 &lo, uint4 &hi) const {
+        ldg32(p + o, lo, hi);
+        if constexpr (kDelta) {
+            uint4 a, b;
+            ldg32(x + o, a, b);
+            lo.x ^= a.x; lo.y ^= a.y; lo.z ^= a.z; lo.w ^= a.w;
+            hi.x ^= b.x; hi.y ^= b.y; hi.z ^= b.z; hi.w ^= b.w;
+        }
+    }
+    __device__ __forceinline__ uint32_t byte(uint64_t i) const {
+        return kDelta ? uint32_t(__ldg(p + i) ^ __ldg(x + i)) : uint32_t(__ldg(p + i));
+    }
+    template <int W>
+    __device__ __forceinline__ uint32_t word(uint64_t i) const {  // element i
+        const uint32_t w = load_word<W>(p + i * W);
+        return kDelta ? w ^ load_word<W>(x + i * W) : w;
+    }
+};
+
 __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
     for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
     return __shfl_sync(kFull, v, 0);
@@ -291,14 +339,14 @@ __device__ __forceinline__ void stream0_bytes(const uint4 &q, uint32_t o[4]) {
 // end of the chunk (see Strided; only the first round can be short), so each
 // thread's register needs one gap shift per round. Returns the raw register
 // in every thread.
-template <int DT>
-__device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
+template <int DT, bool kDelta>
+__device__ uint32_t chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
     constexpr int W = WordOf<DT>::W;
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t *row = crc_row(sm.crc_rep);
     uint32_t *hrow = &sm.hist[0][lane];
     uint32_t reg;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    if (kDelta || (src.addr_bits() & 15) == 0) {  // delta inputs are 16-byte aligned
         const uint32_t main = len & ~(kPiece - 1);
         const uint32_t pieces = main / kPiece;
         const uint32_t rounds = (pieces + kStatThreads - 1) / kStatThreads;
@@ -308,14 +356,14 @@ __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<Word
         // counted and checksummed
         // a piece is one 32-byte load when the chunk is 32-byte aligned (a warp
         // then reads 1 KiB contiguously), else two 16-byte loads
-        const bool wide = (reinterpret_cast<uintptr_t>(src) & 31) == 0;
+        const bool wide = (src.addr_bits() & 31) == 0;
         auto load_piece = [&](int32_t pi, uint4 &lo, uint4 &hi) {
-            const uint8_t *p = src + uint64_t(pi) * kPiece;
+            const uint64_t o = uint64_t(pi) * kPiece;
             if (wide) {
-                ldg32(p, lo, hi);
+                src.vec32(o, lo, hi);
             } else {
-                lo = __ldg(reinterpret_cast<const uint4 *>(p));
-                hi = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+                lo = src.vec(o);
+                hi = src.vec(o + 16);
             }
         };
         uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
@@ -346,26 +394,28 @@ __device__ uint32_t chunk_stats(const uint8_t *src, uint32_t len, StatsSmem<Word
             R = c;
         }
         reg = pieces ? crc_fold<kStatWarps>(R, 5, sm.s_reg) : 0xFFFFFFFFu;
-        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, __ldg(src + i), row);
+        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, src.byte(i), row);
         for (uint32_t i = main / W + tid; i < len / W; i += kStatThreads) {
-            const uint32_t w = load_word<W>(src + uint64_t(i) * W);
+            const uint32_t w = src.template word<W>(i);
             count_elem<DT>(w, hrow);
             cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
         }
-    } else {
+    } else if constexpr (!kDelta) {
         // input aligned to its element size only: words one at a time; the
         // CRC takes the bytes up to the first 16-byte boundary one by one,
         // then the aligned rest with 16-byte pieces (gap table for 4080)
         for (uint32_t i = tid; i < len / W; i += kStatThreads) {
-            const uint32_t w = load_word<W>(src + uint64_t(i) * W);
+            const uint32_t w = src.template word<W>(i);
             count_elem<DT>(w, hrow);
             cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
         }
-        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15);
+        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src.p) & 15)) & 15);
         if (head > len) head = len;
         uint32_t c = 0xFFFFFFFFu;
-        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, __ldg(src + i), row);
-        reg = crc_strided<kStatWarps, false>(src + head, len - head, c, sm.crc_rep, sm.gap, sm.s_reg);
+        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, src.byte(i), row);
+        reg = crc_strided<kStatWarps, false>(src.p + head, len - head, c, sm.crc_rep, sm.gap, sm.s_reg);
+    } else {
+        reg = 0;
     }
     return reg;
 }
@@ -445,16 +495,52 @@ __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *coun
     return mode == kModeCand;
 }
 
-// The bytes of stream j of the chunk, in element order, into out (a second
-// pass over the chunk by one warp; streams after the first are candidates
-// only in unusual data).
-template <int DT>
-__device__ void warp_write_cand(const uint8_t *src, uint32_t len, int j, uint8_t *out) {
+// The bytes of stream j of the chunk, in element order, into out: a second
+// pass over the chunk (now in L2) by one warp, 16-byte vectors with eight in
+// flight per lane; byte j (from the top) of four elements is gathered into a
+// word with two byte permutes and a merge.
+template <int DT, bool kDelta>
+__device__ void warp_write_cand(Source<kDelta> src, uint32_t len, int j, uint8_t *out) {
     constexpr int W = WordOf<DT>::W;
+    constexpr int E = 16 / W;  // elements per vector
+    constexpr int U = 8;
     const int lane = threadIdx.x & 31;
     const uint32_t n = len / W;
-    for (uint32_t i = lane; i < n; i += 32) {
-        const uint32_t p = Perm<DT>::fwd(load_word<W>(src + uint64_t(i) * W));
+    const uint32_t bj = uint32_t(W - 1 - j);
+    const uint32_t sel = bj | (4 + bj) << 4;
+    uint32_t done = 0;
+    if ((src.addr_bits() & 15) == 0) {
+        const uint32_t nvec = len / 16;
+        for (uint32_t v0 = lane; v0 < nvec; v0 += 32 * U) {
+            uint4 q[U];
+#pragma unroll
+            for (int u = 0; u < U; u++)
+                q[u] = v0 + 32 * u < nvec ? src.vec(16ull * (v0 + 32 * u)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const uint32_t v = v0 + 32 * u;
+                if (v >= nvec) break;
+                const uint32_t w4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+                uint32_t p[E];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+#pragma unroll
+                    for (int e = 0; e < 4 / W; e++)
+                        p[k * (4 / W) + e] = Perm<DT>::fwd(W == 4 ? w4[k] : (w4[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u));
+                uint32_t o[E / 4];
+#pragma unroll
+                for (int h = 0; h < E / 4; h++)
+                    o[h] = __byte_perm(__byte_perm(p[4 * h], p[4 * h + 1], sel), __byte_perm(p[4 * h + 2], p[4 * h + 3], sel),
+                                       0x5410);
+                if constexpr (E == 4) *reinterpret_cast<uint32_t *>(out + 4ull * v) = o[0];
+                else if constexpr (E == 8) *reinterpret_cast<uint2 *>(out + 8ull * v) = make_uint2(o[0], o[1]);
+                else *reinterpret_cast<uint4 *>(out + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        done = nvec * E;
+    }
+    for (uint32_t i = done + lane; i < n; i += 32) {
+        const uint32_t p = Perm<DT>::fwd(src.template word<W>(i));
         uint32_t b = 0;
 #pragma unroll
         for (int k = 0; k < W; k++)
@@ -466,7 +552,7 @@ __device__ void warp_write_cand(const uint8_t *src, uint32_t len, int j, uint8_t
 // One CTA per chunk of the wave (grid-stride). Writes per chunk 32 bytes of
 // info {CRC-32 of the original bytes, W stream words mode << 30 | value}, the
 // tables of the candidate streams and their bytes.
-template <int DT>
+template <int DT, bool kDelta>
 __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -474,14 +560,15 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5;
     load_crc_rep(sm.crc_rep);
     load_shift_smem(sm.gap, (reinterpret_cast<uintptr_t>(a.src) & 15) == 0 ? kSh16352 : gap_table<kStatThreads>());
+    const Source<kDelta> whole{a.src, a.base};
     for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
     __syncthreads();
     for (uint32_t cl = blockIdx.x; cl < a.wave_n; cl += gridDim.x) {
         const uint64_t c = uint64_t(a.wave_start) + cl;
-        const uint8_t *src = a.src + c * a.chunk_bytes;
+        const Source<kDelta> src = whole.at(c * a.chunk_bytes);
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - c * a.chunk_bytes));
         uint8_t *cand = a.ws_cand + uint64_t(cl) * W * a.n_pad;
-        const uint32_t reg = chunk_stats<DT>(src, len, sm, cand);
+        const uint32_t reg = chunk_stats<DT, kDelta>(src, len, sm, cand);
         __syncthreads();
         merge_counts<W>(sm);
         __syncthreads();
@@ -494,7 +581,7 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
         if (warp < W) {
             const bool cand_j =
                 plan_stats<W>(a, len / W, sm.cnt[warp], info + 1 + warp, a.ws_ftab + (uint64_t(cl) * W + warp) * 512);
-            if (warp > 0 && cand_j) warp_write_cand<DT>(src, len, warp, cand + uint64_t(warp) * a.n_pad);
+            if (warp > 0 && cand_j) warp_write_cand<DT, kDelta>(src, len, warp, cand + uint64_t(warp) * a.n_pad);
         }
     }
 }
@@ -669,8 +756,8 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
 // warp: a lane takes 16 consecutive elements at a time (G groups, 8 vectors
 // in flight) and writes 16 bytes to every raw stream, gathering byte j (from
 // the top) of four elements into a word with two byte permutes and a merge.
-template <int DT>
-__device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t mode[4], const uint32_t roff[4],
+template <int DT, bool kDelta>
+__device__ void warp_raw_streams(Source<kDelta> src, uint32_t n, const uint32_t mode[4], const uint32_t roff[4],
                                  uint8_t *out) {
     constexpr int W = WordOf<DT>::W;
     constexpr int G = 8 / W;
@@ -680,7 +767,7 @@ __device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t 
     for (int j = 0; j < W; j++) any |= mode[j] == kModeRaw;
     if (!any) return;
     const uint32_t groups = (n + 15) / 16;
-    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    const bool vec = (src.addr_bits() & 15) == 0;
     for (uint32_t g0 = lane; g0 < groups; g0 += 32 * G) {
         uint4 qv[G][W];
 #pragma unroll
@@ -689,7 +776,7 @@ __device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t 
 #pragma unroll
             for (int v = 0; v < W; v++)
                 qv[gi][v] = (vec && 16 * (g + 1) <= n)
-                                ? __ldcs(reinterpret_cast<const uint4 *>(src + uint64_t(g) * 16 * W) + v)
+                                ? src.vec_last(uint64_t(g) * 16 * W + 16 * v)
                                 : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -712,7 +799,7 @@ __device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t 
 #pragma unroll
                 for (int k = 0; k < 16; k++) {
                     const uint32_t i = g * 16 + k;
-                    wd[k] = i < n ? load_word<W>(src + uint64_t(i) * W) : 0u;
+                    wd[k] = i < n ? src.template word<W>(i) : 0u;
                 }
             }
 #pragma unroll
@@ -741,6 +828,26 @@ __device__ void warp_raw_streams(const uint8_t *src, uint32_t n, const uint32_t 
             }
         }
     }
+}
+
+// Copy the len bytes of a source (zero-padded to 16) by the warp, 8 vectors
+// in flight per lane; dst is 16-aligned.
+template <bool kDelta>
+__device__ void warp_copy_src(Source<kDelta> src, uint64_t len, uint8_t *dst) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t nvec = (src.addr_bits() & 15) ? 0 : len / 16;
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    constexpr int U = 8;
+    for (uint64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            if (v0 + 32 * u < nvec) t[u] = src.vec_last(16 * (v0 + 32 * u));
+#pragma unroll
+        for (int u = 0; u < U; u++)
+            if (v0 + 32 * u < nvec) d4[v0 + 32 * u] = t[u];
+    }
+    for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? uint8_t(src.byte(i)) : 0;
 }
 
 // Copy len bytes (zero-padded to 16) by the warp, 8 vectors in flight per
@@ -784,7 +891,7 @@ __device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, ui
     }
 }
 
-template <int DT>
+template <int DT, bool kDelta>
 __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -803,7 +910,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         cl = __shfl_sync(kFull, cl, 0);
         if (cl >= a.wave_n) break;
         const uint32_t c = a.wave_start + cl;
-        const uint8_t *src = a.src + uint64_t(c) * a.chunk_bytes;
+        const Source<kDelta> src = Source<kDelta>{a.src, a.base}.at(uint64_t(c) * a.chunk_bytes);
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
         const uint32_t *info = reinterpret_cast<const uint32_t *>(a.ws_info + 32ull * cl);
@@ -841,7 +948,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         if (fits && !timed) {
             uint8_t *out = a.blob + off;
             if (raw_chunk) {
-                warp_copy(src, len, out);
+                warp_copy_src(src, len, out);
             } else {
                 if (lane < 4) {  // W words, zero-padded to 16 bytes
                     uint32_t e = 0;
@@ -850,7 +957,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
                         if (lane == j) e = (mode[j] << 30) | val[j];
                     reinterpret_cast<uint32_t *>(out)[lane] = e;
                 }
-                warp_raw_streams<DT>(src, n, mode, roff, out);
+                warp_raw_streams<DT, kDelta>(src, n, mode, roff, out);
 #pragma unroll
                 for (int j = 0; j < W; j++)
                     if (mode[j] == kModeRans) warp_copy(slot + uint64_t(j) * a.rec_stride, pad16(val[j]), out + roff[j]);
@@ -905,21 +1012,21 @@ int sms_of_device() {
     return sms;
 }
 
-template <int DT>
+template <int DT, bool kDelta>
 int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     constexpr int W = WordOf<DT>::W;
     const size_t ssm = sizeof(StatsSmem<W>);
     const size_t csm = size_t(kCodeWarps) * kCodeWarpSmem;
-    if (cudaFuncSetAttribute(stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssm)) != cudaSuccess)
+    if (cudaFuncSetAttribute(stats_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssm)) != cudaSuccess)
         return ZC_ECUDA;
-    if (cudaFuncSetAttribute(code_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(csm)) != cudaSuccess)
+    if (cudaFuncSetAttribute(code_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(csm)) != cudaSuccess)
         return ZC_ECUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT>, kStatThreads, ssm) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT, kDelta>, kStatThreads, ssm) != cudaSuccess)
         return ZC_ECUDA;
     const uint64_t most = uint64_t(per_sm < 1 ? 1 : per_sm) * uint64_t(sms_of_device() < 1 ? 1 : sms_of_device());
     const int sgrid = int(a.wave_n < most ? a.wave_n : most);
-    stats_kernel<DT><<<sgrid, kStatThreads, ssm, s>>>(a);
+    stats_kernel<DT, kDelta><<<sgrid, kStatThreads, ssm, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return ZC_ECUDA;
     if (cudaMemsetAsync(a.ws_ctrl, 0, 4, s) != cudaSuccess) return ZC_ECUDA;  // coder ticket
     // the warps spread evenly over the SMs: CTAs of just enough warps for one
@@ -927,7 +1034,7 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     const int sms = sms_of_device() < 1 ? 1 : sms_of_device();
     const uint32_t wpc = std::min<uint32_t>(kCodeWarps, (a.workers + sms - 1) / sms);
     const int cgrid = int((a.workers + wpc - 1) / wpc);
-    code_kernel<DT><<<cgrid, 32 * wpc, size_t(wpc) * kCodeWarpSmem, s>>>(a);
+    code_kernel<DT, kDelta><<<cgrid, 32 * wpc, size_t(wpc) * kCodeWarpSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 
@@ -939,12 +1046,13 @@ int launch_encode_wave(int dtype, const EncodeArgs &a, cudaStream_t s) {
         return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
     }
     switch (dtype) {
-    case ZC_U8: return launch_wave_t<ZC_U8>(a, s);
-    case ZC_U16: return launch_wave_t<ZC_U16>(a, s);
-    case ZC_U32: return launch_wave_t<ZC_U32>(a, s);
-    case ZC_BF16: return launch_wave_t<ZC_BF16>(a, s);
-    case ZC_FP16: return launch_wave_t<ZC_FP16>(a, s);
-    case ZC_FP32: return launch_wave_t<ZC_FP32>(a, s);
+    case ZC_U8: return a.base ? launch_wave_t<ZC_U8, true>(a, s) : launch_wave_t<ZC_U8, false>(a, s);
+    case ZC_U16: return a.base ? launch_wave_t<ZC_U16, true>(a, s) : launch_wave_t<ZC_U16, false>(a, s);
+    case ZC_U32: return a.base ? launch_wave_t<ZC_U32, true>(a, s) : launch_wave_t<ZC_U32, false>(a, s);
+    // deltas are compressed as unsigned words only
+    case ZC_BF16: return a.base ? ZC_EINVAL : launch_wave_t<ZC_BF16, false>(a, s);
+    case ZC_FP16: return a.base ? ZC_EINVAL : launch_wave_t<ZC_FP16, false>(a, s);
+    case ZC_FP32: return a.base ? ZC_EINVAL : launch_wave_t<ZC_FP32, false>(a, s);
     default: return ZC_EINVAL;
     }
 }

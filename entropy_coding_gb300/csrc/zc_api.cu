@@ -190,10 +190,11 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
     return ZC_OK;
 }
 
-extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
-                           uint32_t chunk_bytes, double threshold,
-                           void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
-                           void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+namespace {
+
+int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                  uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity,
+                  uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZC_EINVAL;
     if (ndim < 0 || ndim > 8 || (ndim > 0 && !h_shape)) return ZC_EINVAL;
     const int W = word_bytes(dtype);
@@ -213,6 +214,7 @@ extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int nd
 
     EncodeArgs a{};
     a.src = static_cast<const uint8_t *>(d_src);
+    a.base = static_cast<const uint8_t *>(d_base);
     a.nbytes = nbytes;
     a.chunk_bytes = chunk_bytes;
     a.n_chunks = uint32_t(nc);
@@ -278,8 +280,8 @@ extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int nd
     return ZC_OK;
 }
 
-extern "C" int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
-                             uint32_t flags, int32_t *d_status, void *stream) {
+int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst, uint64_t dst_capacity,
+                    uint32_t flags, int32_t *d_status, void *stream) {
     if (!info || !d_status || !d_blob) return ZC_EINVAL;
     const int W = word_bytes(info->dtype);
     if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
@@ -295,9 +297,45 @@ extern "C" int zc_decompress(const void *d_blob, const zc_info *info, void *d_ds
     a.chunk_bytes = info->chunk_bytes;
     a.n_chunks = info->n_chunks;
     a.dst = static_cast<uint8_t *>(d_dst);
+    a.base = static_cast<const uint8_t *>(d_base);
     a.flags = flags;
     a.d_status = d_status;
     return launch_decode(info->dtype, a, static_cast<cudaStream_t>(stream));
+}
+
+bool delta_dtype(int dtype) { return dtype == ZC_U8 || dtype == ZC_U16 || dtype == ZC_U32; }
+
+} // namespace
+
+extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                           uint32_t chunk_bytes, double threshold,
+                           void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                           void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    return compress_impl(d_src, nullptr, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob, blob_capacity,
+                         d_blob_bytes, d_ws, ws_bytes, d_status, stream);
+}
+
+extern "C" int zc_compress_delta(const void *d_base, const void *d_new, uint64_t nbytes, int dtype, int ndim,
+                                 const int64_t *h_shape, uint32_t chunk_bytes, double threshold,
+                                 void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                                 void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!delta_dtype(dtype)) return ZC_EINVAL;
+    if (nbytes && (!d_base || !d_new || !aligned(d_base, 16) || !aligned(d_new, 16))) return ZC_EINVAL;
+    return compress_impl(d_new, nbytes ? d_base : nullptr, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold,
+                         d_blob, blob_capacity, d_blob_bytes, d_ws, ws_bytes, d_status, stream);
+}
+
+extern "C" int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
+                             uint32_t flags, int32_t *d_status, void *stream) {
+    return decompress_impl(d_blob, info, nullptr, d_dst, dst_capacity, flags, d_status, stream);
+}
+
+extern "C" int zc_decompress_delta(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst,
+                                   uint64_t dst_capacity, uint32_t flags, int32_t *d_status, void *stream) {
+    if (!info || !delta_dtype(info->dtype)) return ZC_EINVAL;
+    if (info->nbytes && (!d_base || !d_dst || !aligned(d_base, 16) || !aligned(d_dst, 16))) return ZC_EINVAL;
+    return decompress_impl(d_blob, info, info->nbytes ? d_base : nullptr, d_dst, dst_capacity, flags, d_status,
+                           stream);
 }
 
 extern "C" int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream) {

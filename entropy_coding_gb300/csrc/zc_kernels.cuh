@@ -9,6 +9,7 @@ namespace zc {
 
 struct EncodeArgs {
     const uint8_t *src;
+    const uint8_t *base;            // delta: the base tensor (src XOR base is coded), else null
     uint64_t nbytes;
     uint32_t chunk_bytes;
     uint32_t n_chunks;
@@ -34,6 +35,7 @@ struct EncodeArgs {
 
 struct DecodeArgs {
     const uint8_t *blob;
+    const uint8_t *base;            // delta: the output is the decoded bytes XOR base, else null
     uint64_t blob_bytes;
     uint64_t nbytes;
     uint32_t chunk_bytes;

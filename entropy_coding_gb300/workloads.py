@@ -57,6 +57,16 @@ def bf16_delta(device="cpu", rows: int = 4096) -> tuple[torch.Tensor, torch.Tens
     return a, x
 
 
+def bf16_delta_pair(device="cpu", rows: int = 4096) -> tuple[torch.Tensor, torch.Tensor]:
+    """(a, b): a base BF16 checkpoint tensor and its update (same draws as
+    bf16_delta, which returns their XOR instead of b)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(4)
+    a = (torch.randn(rows, 14336, generator=g, device=device) * 0.02).bfloat16()
+    b = (a.float() + torch.randn(rows, 14336, generator=g, device=device) * 1e-4).bfloat16()
+    return a, b
+
+
 LLAMA_LAYERS = 32
 LLAMA_LAYER_SHAPES = [("q", (4096, 4096)), ("k", (1024, 4096)), ("v", (1024, 4096)),
                       ("o", (4096, 4096)), ("gate", (14336, 4096)), ("up", (14336, 4096)),

@@ -141,6 +141,36 @@ ZC_API int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, 
 ZC_API int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
                   uint32_t flags, int32_t *d_status, void *stream);
 
+/* Compress the XOR of two same-layout tensors (ZipNN note, Method 6 and
+ * Deltas: XOR a checkpoint against a base, then code the byte groups), fused:
+ * the difference is formed as the input is read and never stored. The blob
+ * is exactly the blob zc_compress makes of (base XOR new) with the same
+ * parameters, so zc_decompress of it gives that difference back and
+ * zc_decompress_delta gives `new`.
+ *   d_base, d_new  device tensors of nbytes bytes each, 16-byte aligned
+ *   dtype          ZC_U8, ZC_U16 or ZC_U32: the word size the difference is
+ *                  grouped by (ZC_U16 for BF16/FP16 checkpoints, ZC_U32 for
+ *                  FP32); float dtypes are rejected (ZC_EINVAL)
+ *   everything else as zc_compress (same workspace size).
+ * Returns ZC_EINVAL for a non-integer dtype or misaligned inputs, else what
+ * zc_compress returns. */
+ZC_API int zc_compress_delta(const void *d_base, const void *d_new, uint64_t nbytes, int dtype, int ndim,
+                      const int64_t *h_shape, uint32_t chunk_bytes, double threshold,
+                      void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                      void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream);
+
+/* Decompress a blob made by zc_compress_delta (or by zc_compress of a
+ * difference) and XOR it with the base in the same pass: d_dst receives
+ * base XOR decoded. The per-chunk CRC is checked over the decoded difference
+ * (the bytes the blob holds), unless flags has ZC_NO_VERIFY.
+ *   info           from zc_blob_info; its dtype must be ZC_U8/U16/U32
+ *   d_base, d_dst  device buffers of info->nbytes bytes, 16-byte aligned;
+ *                  d_dst may not overlap d_base or the blob
+ * Errors as zc_decompress, plus ZC_EINVAL for a float dtype or misaligned
+ * buffers. */
+ZC_API int zc_decompress_delta(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst,
+                        uint64_t dst_capacity, uint32_t flags, int32_t *d_status, void *stream);
+
 /* zlib-compatible CRC-32 of each piece_bytes-byte piece of a device buffer,
  * the last piece possibly shorter (cuZipNN API hash_tensor_with_crc32,
  * checksum_chunk_bytes). piece_bytes = 0 means one CRC of the whole buffer.
