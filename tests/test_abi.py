@@ -72,3 +72,34 @@ def test_blob_info_rejects_moved_offsets(zco):
     with pytest.raises(zc.ZcError) as e:
         zc.blob_info(bytes(blob))
     assert e.value.status == zc.EFORMAT
+
+
+def test_delta_entry_points_reject_bad_arguments_on_the_host():
+    """The delta entry points check dtype and alignment before any launch
+    (the pointers below are never dereferenced)."""
+    import ctypes
+    import entropy_coding_gb300 as zc
+    L = zc.lib()
+    shape = (ctypes.c_int64 * 1)(1024)
+    aligned, odd = 0x10000, 0x10008
+    args = dict(nbytes=2048, ndim=1, shape=shape, chunk=4096, thr=0.95, blob=aligned, cap=1 << 16, nb=aligned,
+                ws=aligned, wsb=1 << 20, st=aligned, stream=None)
+
+    def comp(base, new, dtype):
+        return L.zc_compress_delta(base, new, args["nbytes"], dtype, args["ndim"], args["shape"], args["chunk"],
+                                   args["thr"], args["blob"], args["cap"], args["nb"], args["ws"], args["wsb"],
+                                   args["st"], args["stream"])
+    for dt in (zc.BF16, zc.FP16, zc.FP32, 0, 9):
+        assert comp(aligned, aligned, dt) == zc.EINVAL
+    assert comp(odd, aligned, zc.U16) == zc.EINVAL
+    assert comp(aligned, odd, zc.U16) == zc.EINVAL
+    assert comp(None, aligned, zc.U16) == zc.EINVAL
+
+    info = zc._Info()
+    info.dtype, info.ndim, info.nbytes, info.n_chunks, info.chunk_bytes = zc.BF16, 1, 2048, 1, 4096
+    info.shape[0] = 1024
+    info.blob_bytes = 1 << 12
+    assert L.zc_decompress_delta(aligned, ctypes.byref(info), aligned, aligned, 2048, 0, aligned, None) == zc.EINVAL
+    info.dtype = zc.U16
+    assert L.zc_decompress_delta(aligned, ctypes.byref(info), odd, aligned, 2048, 0, aligned, None) == zc.EINVAL
+    assert L.zc_decompress_delta(aligned, ctypes.byref(info), aligned, odd, 2048, 0, aligned, None) == zc.EINVAL
