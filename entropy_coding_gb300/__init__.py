@@ -22,7 +22,8 @@ from .workloads import BF16, FP16, FP32, U8, U16, U32
 
 __all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspace_size",
            "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
-           "decompress_delta_into", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
+           "decompress_delta_into", "compress_batch", "compress_batch_into", "decompress_batch",
+           "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
            "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
 
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
@@ -86,6 +87,16 @@ def lib() -> ctypes.CDLL:
             L.zc_decompress_delta.argtypes = [vp, ctypes.POINTER(_Info), vp, vp, u64, u32, vp, vp]
             L.zc_crc32.restype = i32
             L.zc_crc32.argtypes = [vp, u64, u64, vp, vp]
+            pu64, pi64, pi32 = ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+            L.zc_workspace_size_batch.restype = u64
+            L.zc_workspace_size_batch.argtypes = [pu64, u32, i32, u32]
+            L.zc_decompress_workspace_size_batch.restype = u64
+            L.zc_decompress_workspace_size_batch.argtypes = [u32]
+            L.zc_compress_batch.restype = i32
+            L.zc_compress_batch.argtypes = [u32, vp, vp, pu64, i32, pi32, pi64, u32, dbl, vp, pu64, vp, vp, u64,
+                                            vp, vp]
+            L.zc_decompress_batch.restype = i32
+            L.zc_decompress_batch.argtypes = [u32, vp, ctypes.POINTER(_Info), vp, vp, pu64, u32, vp, u64, vp, vp]
             _lib = L
     return _lib
 
@@ -299,3 +310,129 @@ def crc32(t: torch.Tensor, piece_bytes: int = 16384, stream=None) -> torch.Tenso
     _check(lib().zc_crc32(src.data_ptr() if nbytes else None, nbytes, piece_bytes, out.data_ptr(),
                           _stream(stream)), "zc_crc32")
     return out[:pieces].to(torch.int64) & 0xFFFFFFFF
+
+
+def _ptrs(ts) -> ctypes.Array:
+    return (ctypes.c_void_p * max(1, len(ts)))(*[t.data_ptr() if t.numel() else None for t in ts])
+
+
+def _u64s(vals) -> ctypes.Array:
+    return (ctypes.c_uint64 * max(1, len(vals)))(*vals)
+
+
+def workspace_size_batch(nbytes, dtype: int, chunk_bytes: int = DEFAULT_CHUNK) -> int:
+    """Workspace bytes for compress_batch_into over tensors of these sizes."""
+    return int(lib().zc_workspace_size_batch(_u64s(nbytes), len(nbytes), dtype, chunk_bytes))
+
+
+def decompress_workspace_size_batch(n: int) -> int:
+    return int(lib().zc_decompress_workspace_size_batch(n))
+
+
+def compress_batch_into(srcs, blobs, blob_bytes: torch.Tensor, workspace: torch.Tensor, status: torch.Tensor,
+                        dtype: int, shapes, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
+                        stream=None, bases=None) -> None:
+    """Launch compression of n tensors (flat byte views ``srcs``) into the
+    blobs ``blobs`` in one grid; ``blob_bytes`` is an n-element int64 CUDA
+    tensor receiving the blob lengths. With ``bases``, tensor t is coded as
+    srcs[t] XOR bases[t]. No allocation, no sync."""
+    n = len(srcs)
+    if len(blobs) != n or len(shapes) != n or (bases is not None and len(bases) != n) or blob_bytes.numel() < n:
+        raise ZcError(EINVAL, "compress_batch_into: argument lists differ in length")
+    nbytes = [t.numel() * t.element_size() for t in srcs]
+    ndims = (ctypes.c_int32 * max(1, n))(*[len(sh) for sh in shapes])
+    flat = []
+    for sh in shapes:
+        if len(sh) > 8:
+            raise ZcError(EINVAL, "at most 8 dimensions")
+        flat += list(sh) + [0] * (8 - len(sh))
+    shp = (ctypes.c_int64 * max(8, len(flat)))(*flat)
+    st = lib().zc_compress_batch(n, _ptrs(srcs), _ptrs(bases) if bases is not None else None, _u64s(nbytes), dtype,
+                                 ndims, shp, chunk_bytes, threshold, _ptrs(blobs), _u64s([b.numel() for b in blobs]),
+                                 blob_bytes.data_ptr(), workspace.data_ptr(), workspace.numel(), status.data_ptr(),
+                                 _stream(stream))
+    _check(st, "zc_compress_batch")
+
+
+def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD, stream=None,
+                   bases=None) -> list:
+    """Compress a list of CUDA tensors of one dtype in one call; returns one
+    blob per tensor, each equal to compress() of that tensor (with ``bases``:
+    to compress_delta(bases[t], tensors[t])). Synchronises once."""
+    n = len(tensors)
+    if n == 0:
+        return []
+    if not all(t.is_cuda for t in tensors) or len({t.dtype for t in tensors}) != 1:
+        raise ZcError(EINVAL, "compress_batch expects CUDA tensors of one dtype")
+    ts = [t.contiguous() for t in tensors]
+    if bases is not None:
+        bs = [b.contiguous() for b in bases]
+        if len(bs) != n or any(b.shape != t.shape or b.dtype != t.dtype or not b.is_cuda for b, t in zip(bs, ts)):
+            raise ZcError(EINVAL, "compress_batch: bases must match the tensors")
+        code = _WORD_CODE.get(ts[0].element_size())
+        if code is None:
+            raise ZcError(EINVAL, f"unsupported element size {ts[0].element_size()}")
+    else:
+        code = dtype_code(ts[0])
+    nbytes = [t.numel() * t.element_size() for t in ts]
+    caps = [blob_size(nb, code, chunk_bytes, threshold) for nb in nbytes]
+    if 0 in caps:
+        raise ZcError(EINVAL, "invalid compression parameters")
+    offs, o = [], 0
+    for c in caps:
+        offs.append(o)
+        o += (c + 255) // 256 * 256
+    dev = ts[0].device
+    buf = torch.empty(o, dtype=torch.uint8, device=dev)
+    blobs = [buf[a: a + c] for a, c in zip(offs, caps)]
+    ws = torch.empty(max(16, workspace_size_batch(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
+    nb = torch.zeros(n, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flat = [t.view(-1).view(torch.uint8) for t in ts]
+    compress_batch_into(flat, blobs, nb, ws, status, code, [tuple(t.shape) for t in tensors], chunk_bytes,
+                        threshold, stream, bases=[b.view(-1).view(torch.uint8) for b in bs] if bases is not None
+                        else None)
+    _check(int(status.item()), "zc_compress_batch (device)")
+    return [b[: int(k)] for b, k in zip(blobs, nb.tolist())]
+
+
+def decompress_batch_into(blobs, infos, outs, status: torch.Tensor, workspace: torch.Tensor | None = None,
+                          verify: bool = True, stream=None, bases=None) -> None:
+    """Launch decompression of n blobs (one dtype and chunk size) into
+    ``outs`` in one grid; with ``bases``, output t is the decoded bytes XOR
+    bases[t]. ``workspace`` holds decompress_workspace_size_batch(n) bytes
+    (None when n <= 1). No allocation, no sync."""
+    n = len(blobs)
+    if len(infos) != n or len(outs) != n or (bases is not None and len(bases) != n):
+        raise ZcError(EINVAL, "decompress_batch_into: argument lists differ in length")
+    arr = (_Info * max(1, n))(*[_info_struct(d) for d in infos])
+    caps = _u64s([t.numel() * t.element_size() for t in outs])
+    st = lib().zc_decompress_batch(n, _ptrs(blobs), arr, _ptrs(bases) if bases is not None else None, _ptrs(outs),
+                                   caps, 0 if verify else NO_VERIFY,
+                                   workspace.data_ptr() if workspace is not None else None,
+                                   workspace.numel() if workspace is not None else 0, status.data_ptr(),
+                                   _stream(stream))
+    _check(st, "zc_decompress_batch")
+
+
+def decompress_batch(blobs, infos=None, verify: bool = True, stream=None, bases=None) -> list:
+    """Restore a list of tensors from their blobs in one call (each equal to
+    decompress(), or with ``bases`` to decompress_delta(), of its blob)."""
+    n = len(blobs)
+    if n == 0:
+        return []
+    infos = [read_info(b) for b in blobs] if infos is None else list(infos)
+    dev = blobs[0].device
+    if bases is not None:
+        outs = [torch.empty_like(b.contiguous()) for b in bases]
+        bflat = [b.contiguous().view(-1).view(torch.uint8) for b in bases]
+    else:
+        outs = [torch.empty(d["shape"], dtype=_CODE_TO_TORCH[d["dtype"]], device=dev) for d in infos]
+        bflat = None
+    ws_n = decompress_workspace_size_batch(n)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev) if ws_n else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    decompress_batch_into(blobs, infos, [o.view(-1).view(torch.uint8) for o in outs], status, ws, verify, stream,
+                          bases=bflat)
+    _check(int(status.item()), "zc_decompress_batch (device)")
+    return outs

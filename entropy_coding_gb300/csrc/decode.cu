@@ -551,14 +551,21 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
 }
 
 template <int DT, bool kBig, bool kDelta>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, PairSmem<kBig> &ps, const uint32_t *crc_rep,
+__device__ void decode_chunk(const DecodeArgs &a, uint32_t g, bool producer, PairSmem<kBig> &ps, const uint32_t *crc_rep,
                              const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
-    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
+    // the blob of this call-wide chunk index
+    const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
+    const uint8_t *const blob = bd.blob;
+    const uint64_t blob_bytes = bd.blob_bytes, nbytes = bd.nbytes;
+    const uint32_t n_chunks = bd.n_chunks, c = g - bd.chunk_base;
+    uint8_t *const dst = bd.dst;
+    const uint8_t *const base = bd.base;
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * n_chunks;
 
     uint4 ent = make_uint4(0, 0, 0, 0);
-    if (lane == 0) ent = reinterpret_cast<const uint4 *>(a.blob + ZC_HEADER_BYTES)[c];
+    if (lane == 0) ent = reinterpret_cast<const uint4 *>(blob + ZC_HEADER_BYTES)[c];
     ent.x = __shfl_sync(kFull, ent.x, 0);
     ent.y = __shfl_sync(kFull, ent.y, 0);
     ent.z = __shfl_sync(kFull, ent.z, 0);
@@ -566,19 +573,19 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t c, bool producer, Pai
     const uint64_t off = uint64_t(ent.x) | (uint64_t(ent.y) << 32);
     const uint32_t stored = ent.z & 0x7FFFFFFFu;
     const bool raw = ent.z >> 31;
-    const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
+    const uint32_t len = uint32_t(umin64(a.chunk_bytes, nbytes - uint64_t(c) * a.chunk_bytes));
     const uint32_t n = len / W;
 
-    bool ok = (off & 15) == 0 && off >= table_end && off <= a.blob_bytes && stored <= a.blob_bytes - off;
+    bool ok = (off & 15) == 0 && off >= table_end && off <= blob_bytes && stored <= blob_bytes - off;
     ok = ok && (raw ? stored == len : (stored % 16 == 0 && stored >= 16 && stored <= max_grouped(len, W)));
     if (!ok) {
         if (!producer && lane == 0) status_or(a.d_status, ZC_EFORMAT);
         return;
     }
-    const uint8_t *p = a.blob + off;
+    const uint8_t *p = blob + off;
     const bool verify = !(a.flags & ZC_NO_VERIFY);
-    uint8_t *out = a.dst + uint64_t(c) * a.chunk_bytes;
-    const uint8_t *basec = kDelta ? a.base + uint64_t(c) * a.chunk_bytes : nullptr;
+    uint8_t *out = dst + uint64_t(c) * a.chunk_bytes;
+    const uint8_t *basec = kDelta ? base + uint64_t(c) * a.chunk_bytes : nullptr;
     if (raw) {
         if (producer) return;
         uint32_t nvec = (reinterpret_cast<uintptr_t>(out) & 15) ? 0 : len / 16;
@@ -644,9 +651,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs
         mbar_init(&ps.start, 32);
     }
     __syncthreads();
-    const uint32_t c = blockIdx.x * pairs_per_cta + (warp >> 1);
-    if (c >= a.n_chunks) return;
-    decode_chunk<DT, kBig, kDelta>(a, c, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
+    const uint32_t g = blockIdx.x * pairs_per_cta + (warp >> 1);
+    if (g >= a.total_chunks) return;
+    decode_chunk<DT, kBig, kDelta>(a, g, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
 }
 
 template <int DT, bool kBig, bool kDelta>
@@ -656,7 +663,7 @@ int launch_decode_mode(const DecodeArgs &a, uint32_t pc, cudaStream_t s) {
     if (cudaFuncSetAttribute(decode_kernel<DT, kBig, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(std::min<size_t>(smem_max, 227 * 1024))) != cudaSuccess)
         return ZC_ECUDA;
-    const int grid = int((a.n_chunks + pc - 1) / pc);
+    const int grid = int((a.total_chunks + pc - 1) / pc);
     decode_kernel<DT, kBig, kDelta><<<grid, 64 * pc, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
@@ -671,26 +678,26 @@ int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     // CTA just enough for kCtasPerSM CTAs per SM to hold every chunk, with
     // the smaller two-level tables. Either way the chunks spread evenly over
     // the SMs.
-    const uint64_t per_sm = (a.n_chunks + sms - 1) / uint64_t(sms);
+    const uint64_t per_sm = (a.total_chunks + sms - 1) / uint64_t(sms);
     if (per_sm <= kBigPairs)
         return launch_decode_mode<DT, true, kDelta>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
     const uint64_t slots = uint64_t(sms) * kCtasPerSM;
-    const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.n_chunks + slots - 1) / slots));
+    const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.total_chunks + slots - 1) / slots));
     return launch_decode_mode<DT, false, kDelta>(a, pc, s);
 }
 
 } // namespace
 
-int launch_decode(int dtype, const DecodeArgs &a, cudaStream_t s) {
-    if (a.n_chunks == 0) return ZC_OK;
+int launch_decode(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s) {
+    if (a.total_chunks == 0) return ZC_OK;
     switch (dtype) {
-    case ZC_U8: return a.base ? launch_decode_t<ZC_U8, true>(a, s) : launch_decode_t<ZC_U8, false>(a, s);
-    case ZC_U16: return a.base ? launch_decode_t<ZC_U16, true>(a, s) : launch_decode_t<ZC_U16, false>(a, s);
-    case ZC_U32: return a.base ? launch_decode_t<ZC_U32, true>(a, s) : launch_decode_t<ZC_U32, false>(a, s);
+    case ZC_U8: return delta ? launch_decode_t<ZC_U8, true>(a, s) : launch_decode_t<ZC_U8, false>(a, s);
+    case ZC_U16: return delta ? launch_decode_t<ZC_U16, true>(a, s) : launch_decode_t<ZC_U16, false>(a, s);
+    case ZC_U32: return delta ? launch_decode_t<ZC_U32, true>(a, s) : launch_decode_t<ZC_U32, false>(a, s);
     // deltas are coded as unsigned words only
-    case ZC_BF16: return a.base ? ZC_EINVAL : launch_decode_t<ZC_BF16, false>(a, s);
-    case ZC_FP16: return a.base ? ZC_EINVAL : launch_decode_t<ZC_FP16, false>(a, s);
-    case ZC_FP32: return a.base ? ZC_EINVAL : launch_decode_t<ZC_FP32, false>(a, s);
+    case ZC_BF16: return delta ? ZC_EINVAL : launch_decode_t<ZC_BF16, false>(a, s);
+    case ZC_FP16: return delta ? ZC_EINVAL : launch_decode_t<ZC_FP16, false>(a, s);
+    case ZC_FP32: return delta ? ZC_EINVAL : launch_decode_t<ZC_FP32, false>(a, s);
     default: return ZC_EINVAL;
     }
 }

@@ -149,6 +149,39 @@ struct Source {
     }
 };
 
+// The tensor a call-wide chunk index belongs to (fields read once per chunk).
+struct TView {
+    const uint8_t *src, *base;
+    uint8_t *blob;
+    uint64_t nbytes, cap;
+    uint32_t n_chunks, chunk_base, t;
+};
+
+__device__ __forceinline__ TView tensor_view(const EncodeArgs &a, uint32_t g) {
+    TView v;
+    if (a.n_tensors == 1) {
+        v.src = a.one.src;
+        v.base = a.one.base;
+        v.blob = a.one.blob;
+        v.nbytes = a.one.nbytes;
+        v.cap = a.one.cap;
+        v.n_chunks = a.one.n_chunks;
+        v.chunk_base = 0;
+        v.t = 0;
+    } else {
+        v.t = owner_of(a.tensors, a.n_tensors, g);
+        const TensorDesc &d = a.tensors[v.t];
+        v.src = d.src;
+        v.base = d.base;
+        v.blob = d.blob;
+        v.nbytes = d.nbytes;
+        v.cap = d.cap;
+        v.n_chunks = d.n_chunks;
+        v.chunk_base = d.chunk_base;
+    }
+    return v;
+}
+
 __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
     for (int o = 16; o; o >>= 1) v += __shfl_down_sync(kFull, v, o);
     return __shfl_sync(kFull, v, 0);
@@ -278,7 +311,8 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
 template <int W>
 struct StatsSmem {
     uint32_t crc_rep[kCrcRepWords];  // CRC slicing tables, 8 copies (32 KB)
-    uint32_t gap[4][256];            // register shift over the other threads' pieces
+    uint32_t gap[4][256];            // register shift over the other threads' 32-byte pieces
+    uint32_t gapu[4][256];           // the same for 16-byte pieces (unaligned inputs)
     uint32_t hist[W][128 * 32];
     uint32_t cnt[W][256];            // merged counts
     uint32_t s_reg[kStatWarps];
@@ -413,7 +447,7 @@ __device__ uint32_t chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<Word
         if (head > len) head = len;
         uint32_t c = 0xFFFFFFFFu;
         for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, src.byte(i), row);
-        reg = crc_strided<kStatWarps, false>(src.p + head, len - head, c, sm.crc_rep, sm.gap, sm.s_reg);
+        reg = crc_strided<kStatWarps, false>(src.p + head, len - head, c, sm.crc_rep, sm.gapu, sm.s_reg);
     } else {
         reg = 0;
     }
@@ -559,14 +593,16 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     StatsSmem<W> &sm = *reinterpret_cast<StatsSmem<W> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     load_crc_rep(sm.crc_rep);
-    load_shift_smem(sm.gap, (reinterpret_cast<uintptr_t>(a.src) & 15) == 0 ? kSh16352 : gap_table<kStatThreads>());
-    const Source<kDelta> whole{a.src, a.base};
+    load_shift_smem(sm.gap, kSh16352);
+    load_shift_smem(sm.gapu, gap_table<kStatThreads>());
     for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
     __syncthreads();
     for (uint32_t cl = blockIdx.x; cl < a.wave_n; cl += gridDim.x) {
-        const uint64_t c = uint64_t(a.wave_start) + cl;
-        const Source<kDelta> src = whole.at(c * a.chunk_bytes);
-        const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - c * a.chunk_bytes));
+        const uint32_t g = a.wave_start + cl;
+        const TView tv = tensor_view(a, g);
+        const uint64_t c = g - tv.chunk_base;
+        const Source<kDelta> src = Source<kDelta>{tv.src, tv.base}.at(c * a.chunk_bytes);
+        const uint32_t len = uint32_t(umin64(a.chunk_bytes, tv.nbytes - c * a.chunk_bytes));
         uint8_t *cand = a.ws_cand + uint64_t(cl) * W * a.n_pad;
         const uint32_t reg = chunk_stats<DT, kDelta>(src, len, sm, cand);
         __syncthreads();
@@ -902,16 +938,19 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     uint8_t *ring = smem_raw + kCodeWarpSmem * warp + 4096;
     uint8_t *slot = a.ws_slots + uint64_t(gw) * a.slot_bytes;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
-    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * a.n_chunks;
 
     for (;;) {
         uint32_t cl = 0;
         if (lane == 0) cl = atomicAdd(&ctrl[0], 1u);
         cl = __shfl_sync(kFull, cl, 0);
         if (cl >= a.wave_n) break;
-        const uint32_t c = a.wave_start + cl;
-        const Source<kDelta> src = Source<kDelta>{a.src, a.base}.at(uint64_t(c) * a.chunk_bytes);
-        const uint32_t len = uint32_t(umin64(a.chunk_bytes, a.nbytes - uint64_t(c) * a.chunk_bytes));
+        const uint32_t g = a.wave_start + cl;
+        const TView tv = tensor_view(a, g);
+        const uint32_t c = g - tv.chunk_base;  // chunk of its tensor
+        uint32_t *tctrl = ctrl + 64 + 4 * tv.t;  // the tensor's done counter and header-CRC accumulator
+        const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * tv.n_chunks;
+        const Source<kDelta> src = Source<kDelta>{tv.src, tv.base}.at(uint64_t(c) * a.chunk_bytes);
+        const uint32_t len = uint32_t(umin64(a.chunk_bytes, tv.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
         const uint32_t *info = reinterpret_cast<const uint32_t *>(a.ws_info + 32ull * cl);
         const uint32_t crc = info[0];
@@ -941,12 +980,12 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
         const uint64_t stored = raw_chunk ? len : grouped;
         bool timed;
-        const uint64_t off = table_end + lookback(a.ws_status, c, pad16(stored), a.d_status, &timed);
-        const bool fits = off + pad16(stored) <= a.cap;
+        const uint64_t off = table_end + lookback(a.ws_status + tv.chunk_base, c, pad16(stored), a.d_status, &timed);
+        const bool fits = off + pad16(stored) <= tv.cap;
         if (!fits && lane == 0) status_or(a.d_status, ZC_ECAPACITY);
 
         if (fits && !timed) {
-            uint8_t *out = a.blob + off;
+            uint8_t *out = tv.blob + off;
             if (raw_chunk) {
                 warp_copy_src(src, len, out);
             } else {
@@ -968,31 +1007,34 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
                 ent.y = uint32_t(off >> 32);
                 ent.z = uint32_t(stored) | (raw_chunk ? 0x80000000u : 0u);
                 ent.w = crc;
-                reinterpret_cast<uint4 *>(a.blob + ZC_HEADER_BYTES)[c] = ent;
+                reinterpret_cast<uint4 *>(tv.blob + ZC_HEADER_BYTES)[c] = ent;
                 // header CRC = shift(crc(header), 16 n) ^ XOR_c shift(crc(entry_c), 16 (n-1-c))
                 uint32_t ec = 0xFFFFFFFFu;
                 ec = crc_word_global(ec, ent.x);
                 ec = crc_word_global(ec, ent.y);
                 ec = crc_word_global(ec, ent.z);
                 ec = crc_word_global(ec, ent.w) ^ 0xFFFFFFFFu;
-                atomicXor(&ctrl[2], shift_bytes(ec, 16ull * (a.n_chunks - 1 - c)));
+                atomicXor(&tctrl[1], shift_bytes(ec, 16ull * (tv.n_chunks - 1 - c)));
             }
         }
         if (lane == 0) {
             __threadfence();
-            const uint32_t done = atomicAdd(&ctrl[1], 1u);
-            if (done == a.n_chunks - 1) {
+            const uint32_t done = atomicAdd(&tctrl[0], 1u);
+            if (done == tv.n_chunks - 1) {
+                // the tensor's last chunk: its header and blob length
                 __threadfence();
-                const uint32_t acc = atomicXor(&ctrl[2], 0u);
-                const unsigned long long last = ld_acquire(&a.ws_status[a.n_chunks - 1]);
+                const uint32_t acc = atomicXor(&tctrl[1], 0u);
+                const unsigned long long last = ld_acquire(&a.ws_status[tv.chunk_base + tv.n_chunks - 1]);
                 const uint64_t total = table_end + (last & kValMask);
+                const uint32_t *header = a.n_tensors == 1 ? a.one.header : a.tensors[tv.t].header;
+                uint64_t *d_blob_bytes = a.n_tensors == 1 ? a.one.d_blob_bytes : a.tensors[tv.t].d_blob_bytes;
                 uint32_t hc = 0xFFFFFFFFu;
-                for (int q = 0; q < 24; q++) hc = crc_word_global(hc, a.header[q]);
+                for (int q = 0; q < 24; q++) hc = crc_word_global(hc, header[q]);
                 hc ^= 0xFFFFFFFFu;
-                const uint32_t hcrc = shift_bytes(hc, 16ull * a.n_chunks) ^ acc;
-                uint32_t *hdr = reinterpret_cast<uint32_t *>(a.blob);
-                for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : a.header[q];
-                *a.d_blob_bytes = total;
+                const uint32_t hcrc = shift_bytes(hc, 16ull * tv.n_chunks) ^ acc;
+                uint32_t *hdr = reinterpret_cast<uint32_t *>(tv.blob);
+                for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : header[q];
+                *d_blob_bytes = total;
             }
         }
         __syncwarp();
@@ -1001,8 +1043,12 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
 
 // A blob of an empty tensor is its header alone (its CRC made on the host).
 __global__ void empty_blob_kernel(EncodeArgs a) {
-    if (threadIdx.x < 24) reinterpret_cast<uint32_t *>(a.blob)[threadIdx.x] = a.header[threadIdx.x];
-    if (threadIdx.x == 0) *a.d_blob_bytes = ZC_HEADER_BYTES;
+    for (uint32_t t = blockIdx.x; t < a.n_tensors; t += gridDim.x) {
+        const TensorDesc &d = a.n_tensors == 1 ? a.one : a.tensors[t];
+        if (d.n_chunks != 0) continue;
+        if (threadIdx.x < 24) reinterpret_cast<uint32_t *>(d.blob)[threadIdx.x] = d.header[threadIdx.x];
+        if (threadIdx.x == 0) *d.d_blob_bytes = ZC_HEADER_BYTES;
+    }
 }
 
 int sms_of_device() {
@@ -1040,19 +1086,21 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
 
 } // namespace
 
-int launch_encode_wave(int dtype, const EncodeArgs &a, cudaStream_t s) {
-    if (a.n_chunks == 0) {
-        empty_blob_kernel<<<1, 32, 0, s>>>(a);
-        return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
-    }
+int launch_empty_blobs(const EncodeArgs &a, cudaStream_t s) {
+    empty_blob_kernel<<<std::min<uint32_t>(a.n_tensors, 1024), 32, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
+
+int launch_encode_wave(int dtype, bool delta, const EncodeArgs &a, cudaStream_t s) {
+    if (a.total_chunks == 0) return ZC_EINVAL;
     switch (dtype) {
-    case ZC_U8: return a.base ? launch_wave_t<ZC_U8, true>(a, s) : launch_wave_t<ZC_U8, false>(a, s);
-    case ZC_U16: return a.base ? launch_wave_t<ZC_U16, true>(a, s) : launch_wave_t<ZC_U16, false>(a, s);
-    case ZC_U32: return a.base ? launch_wave_t<ZC_U32, true>(a, s) : launch_wave_t<ZC_U32, false>(a, s);
+    case ZC_U8: return delta ? launch_wave_t<ZC_U8, true>(a, s) : launch_wave_t<ZC_U8, false>(a, s);
+    case ZC_U16: return delta ? launch_wave_t<ZC_U16, true>(a, s) : launch_wave_t<ZC_U16, false>(a, s);
+    case ZC_U32: return delta ? launch_wave_t<ZC_U32, true>(a, s) : launch_wave_t<ZC_U32, false>(a, s);
     // deltas are compressed as unsigned words only
-    case ZC_BF16: return a.base ? ZC_EINVAL : launch_wave_t<ZC_BF16, false>(a, s);
-    case ZC_FP16: return a.base ? ZC_EINVAL : launch_wave_t<ZC_FP16, false>(a, s);
-    case ZC_FP32: return a.base ? ZC_EINVAL : launch_wave_t<ZC_FP32, false>(a, s);
+    case ZC_BF16: return delta ? ZC_EINVAL : launch_wave_t<ZC_BF16, false>(a, s);
+    case ZC_FP16: return delta ? ZC_EINVAL : launch_wave_t<ZC_FP16, false>(a, s);
+    case ZC_FP32: return delta ? ZC_EINVAL : launch_wave_t<ZC_FP32, false>(a, s);
     default: return ZC_EINVAL;
     }
 }

@@ -1,8 +1,9 @@
 // zc_api.cu — the C ABI (include/zc.h): argument checks, workspace layout,
-// header construction and kernel launches. No entry point allocates memory or
-// synchronises; device-side errors are reported through *d_status.
+// header construction and kernel launches. No entry point allocates device
+// memory or synchronises; device-side errors are reported through *d_status.
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "zc_kernels.cuh"
 
@@ -10,7 +11,7 @@ namespace {
 
 using namespace zc;
 
-constexpr uint64_t kCtrlBytes = 256;    // ticket, done counter, header CRC accumulator
+constexpr uint64_t kCtrlBytes = 256;    // coder ticket; then per tensor: done counter, header CRC accumulator
 constexpr uint64_t kCrcUnit = 32768;    // bytes per warp in zc_crc32
 
 uint64_t pad256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
@@ -126,20 +127,6 @@ extern "C" uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_byte
     return total + full * worst(chunk_bytes) + worst(last);
 }
 
-extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes) {
-    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95)) return 0;
-    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
-    if (nc == 0) return kCtrlBytes;
-    const int W = word_bytes(dtype);
-    const uint64_t wave = wave_chunks(nc, chunk_bytes, W);
-    // every coding warp for thresholds up to 1; at least one warp for any
-    // threshold (larger thresholds then run fewer warps)
-    uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0);
-    const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9);
-    if (slots < one_any) slots = one_any;
-    return kCtrlBytes + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
-}
-
 extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out) {
     const uint8_t *b = static_cast<const uint8_t *>(h_blob_prefix);
     if (!b || !out || avail < ZC_HEADER_BYTES) return ZC_EFORMAT;
@@ -192,38 +179,33 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
 
 namespace {
 
-int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
-                  uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity,
-                  uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+// Check one tensor of a compression call and describe it for the kernels
+// (chunk_base is set by the caller).
+int make_tensor(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                TensorDesc &d) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZC_EINVAL;
     if (ndim < 0 || ndim > 8 || (ndim > 0 && !h_shape)) return ZC_EINVAL;
     const int W = word_bytes(dtype);
     uint64_t elems = 1;
-    for (int d = 0; d < ndim; d++) {
-        if (h_shape[d] < 0) return ZC_EINVAL;
-        if (h_shape[d] && elems > UINT64_MAX / uint64_t(h_shape[d])) return ZC_EINVAL;
-        elems *= uint64_t(h_shape[d]);
+    for (int dd = 0; dd < ndim; dd++) {
+        if (h_shape[dd] < 0) return ZC_EINVAL;
+        if (h_shape[dd] && elems > UINT64_MAX / uint64_t(h_shape[dd])) return ZC_EINVAL;
+        elems *= uint64_t(h_shape[dd]);
     }
     if (elems * uint64_t(W) != nbytes) return ZC_EINVAL;
-    if (!d_blob || !d_blob_bytes || !d_status || !d_ws || (nbytes && !d_src)) return ZC_EINVAL;
-    if (!aligned(d_src, W) || !aligned(d_blob, 16) || !aligned(d_ws, 16) || !aligned(d_blob_bytes, 8))
-        return ZC_EINVAL;
+    if (!d_blob || !d_blob_bytes || (nbytes && !d_src)) return ZC_EINVAL;
+    if (!aligned(d_src, W) || !aligned(d_blob, 16) || !aligned(d_blob_bytes, 8)) return ZC_EINVAL;
     const uint64_t nc = chunks_of(nbytes, chunk_bytes);
-    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc;
-    if (blob_capacity < table_end) return ZC_ECAPACITY;
-
-    EncodeArgs a{};
-    a.src = static_cast<const uint8_t *>(d_src);
-    a.base = static_cast<const uint8_t *>(d_base);
-    a.nbytes = nbytes;
-    a.chunk_bytes = chunk_bytes;
-    a.n_chunks = uint32_t(nc);
-    a.threshold = threshold;
-    a.blob = static_cast<uint8_t *>(d_blob);
-    a.cap = blob_capacity;
-    a.d_blob_bytes = d_blob_bytes;
-    a.d_status = d_status;
-
+    if (blob_capacity < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc) return ZC_ECAPACITY;
+    d = TensorDesc{};
+    d.src = static_cast<const uint8_t *>(d_src);
+    d.base = static_cast<const uint8_t *>(d_base);
+    d.blob = static_cast<uint8_t *>(d_blob);
+    d.d_blob_bytes = d_blob_bytes;
+    d.nbytes = nbytes;
+    d.cap = blob_capacity;
+    d.n_chunks = uint32_t(nc);
     uint8_t head[ZC_HEADER_BYTES] = {};
     std::memcpy(head, "ZCNN", 4);
     head[4] = 1;
@@ -234,18 +216,90 @@ int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dt
     head[13] = uint8_t(kProbBits);
     put64(head + 16, nbytes);
     put32(head + 24, uint32_t(nc));
-    for (int d = 0; d < ndim; d++) put64(head + 32 + 8 * d, uint64_t(h_shape[d]));
+    for (int dd = 0; dd < ndim; dd++) put64(head + 32 + 8 * dd, uint64_t(h_shape[dd]));
     if (nc == 0) put32(head + 28, host_crc32(head, ZC_HEADER_BYTES) ^ 0xFFFFFFFFu);
-    std::memcpy(a.header, head, ZC_HEADER_BYTES);
+    std::memcpy(d.header, head, ZC_HEADER_BYTES);
+    return ZC_OK;
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (nc == 0) return launch_encode_wave(dtype, a, s);
+// A batch's descriptor table reaches the device through kernel parameters
+// (copied when the launch is issued): no pageable copy, no host wait.
+constexpr uint32_t kParamWords = 7680;
+struct TableBlock {
+    uint32_t words;
+    uint32_t w[kParamWords];
+};
+static_assert(sizeof(TableBlock) <= 32764, "kernel parameters are at most 32764 bytes");
 
-    const uint64_t fixed = kCtrlBytes + pad256(8 * nc);
+__global__ void table_kernel(const TableBlock b, uint32_t *dst) {
+    for (uint32_t i = threadIdx.x; i < b.words; i += blockDim.x) dst[i] = b.w[i];
+}
+
+int upload_table(const void *h, uint64_t bytes, void *d, cudaStream_t s) {
+    static_assert(sizeof(TensorDesc) % 4 == 0 && sizeof(BlobDesc) % 4 == 0, "descriptors are whole words");
+    const uint32_t *src = static_cast<const uint32_t *>(h);
+    uint32_t *dst = static_cast<uint32_t *>(d);
+    const uint64_t words = bytes / 4;
+    static thread_local TableBlock blk;  // 30 KB: off the stack
+    for (uint64_t w0 = 0; w0 < words; w0 += kParamWords) {
+        blk.words = uint32_t(words - w0 < kParamWords ? words - w0 : kParamWords);
+        std::memcpy(blk.w, src + w0, 4ull * blk.words);
+        table_kernel<<<1, 256, 0, s>>>(blk, dst + w0);
+        if (cudaGetLastError() != cudaSuccess) return ZC_ECUDA;
+    }
+    return ZC_OK;
+}
+
+// Workspace of a compression call over n tensors and nc chunks: control
+// (coder ticket; per tensor a done counter and a header-CRC accumulator),
+// the tensor table (batches), the chunk status words, then a wave's
+// statistics and the coding warps' slots.
+uint64_t ctrl_bytes(uint64_t n) { return kCtrlBytes + pad256(16 * n); }
+uint64_t table_bytes(uint64_t n) { return n > 1 ? pad256(sizeof(TensorDesc) * n) : 0; }
+
+uint64_t ws_size(uint64_t n, uint64_t nc, int W, uint32_t chunk_bytes) {
+    if (nc == 0) return ctrl_bytes(n) + table_bytes(n);
+    const uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+    // every coding warp for thresholds up to 1; at least one warp for any
+    // threshold (larger thresholds then run fewer warps)
+    uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0);
+    const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9);
+    if (slots < one_any) slots = one_any;
+    return ctrl_bytes(n) + table_bytes(n) + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
+}
+
+// Lay out the workspace and launch the statistics + coding waves over the
+// call's chunks. `table` holds the n > 1 tensors (copied to the workspace).
+int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta, int dtype, uint32_t chunk_bytes,
+                 double threshold, void *d_ws, uint64_t ws_bytes, cudaStream_t s) {
+    const int W = word_bytes(dtype);
+    const uint64_t nc = a.total_chunks;
+    a.n_tensors = n;
+    a.chunk_bytes = chunk_bytes;
+    a.threshold = threshold;
+    if (!d_ws || !aligned(d_ws, 16)) return ZC_EINVAL;
+    const uint64_t head = ctrl_bytes(n) + table_bytes(n);
+    const uint64_t fixed = head + pad256(8 * nc);
+    if (ws_bytes < fixed) return ZC_ECAPACITY;
+    a.ws_ctrl = static_cast<uint8_t *>(d_ws);
+    a.tensors = n > 1 ? reinterpret_cast<const TensorDesc *>(a.ws_ctrl + ctrl_bytes(n)) : nullptr;
+    a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + head);
+    if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
+    if (n > 1) {
+        const int st = upload_table(table, sizeof(TensorDesc) * n, const_cast<TensorDesc *>(a.tensors), s);
+        if (st != ZC_OK) return st;
+    }
+    bool any_empty = false;
+    for (uint32_t t = 0; t < n; t++) any_empty |= (n == 1 ? a.one : table[t]).n_chunks == 0;
+    if (any_empty) {
+        const int st = launch_empty_blobs(a, s);
+        if (st != ZC_OK) return st;
+    }
+    if (nc == 0) return ZC_OK;
+
     const uint64_t slot = slot_bytes(chunk_bytes, W, threshold);
     uint64_t wave = wave_chunks(nc, chunk_bytes, W);
     uint64_t workers = max_workers(nc);
-    if (ws_bytes < fixed) return ZC_ECAPACITY;
     const uint64_t avail = ws_bytes - fixed;
     if (wave_layout(wave, W, chunk_bytes).slots + workers * slot > avail) {
         // a full wave with fewer coding warps, else smaller waves
@@ -260,8 +314,6 @@ int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dt
         }
     }
     const WaveLayout lay = wave_layout(wave, W, chunk_bytes);
-    a.ws_ctrl = static_cast<uint8_t *>(d_ws);
-    a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + kCtrlBytes);
     a.ws_info = a.ws_ctrl + fixed + lay.info;
     a.ws_ftab = a.ws_ctrl + fixed + lay.ftab;
     a.ws_cand = a.ws_ctrl + fixed + lay.cand;
@@ -270,42 +322,85 @@ int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dt
     a.slot_bytes = slot;
     a.rec_stride = rec_stride(chunk_bytes, W, threshold);
     a.workers = uint32_t(workers < wave ? workers : wave);
-    if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
     for (uint64_t w0 = 0; w0 < nc; w0 += wave) {
         a.wave_start = uint32_t(w0);
         a.wave_n = uint32_t(nc - w0 < wave ? nc - w0 : wave);
-        const int st = launch_encode_wave(dtype, a, s);
+        const int st = launch_encode_wave(dtype, delta, a, s);
         if (st != ZC_OK) return st;
     }
     return ZC_OK;
 }
 
-int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst, uint64_t dst_capacity,
-                    uint32_t flags, int32_t *d_status, void *stream) {
-    if (!info || !d_status || !d_blob) return ZC_EINVAL;
+int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                  uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity,
+                  uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!d_status) return ZC_EINVAL;
+    EncodeArgs a{};
+    const int st = make_tensor(d_src, d_base, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob,
+                               blob_capacity, d_blob_bytes, a.one);
+    if (st != ZC_OK) return st;
+    a.total_chunks = a.one.n_chunks;
+    a.d_status = d_status;
+    return run_compress(a, nullptr, 1, d_base != nullptr, dtype, chunk_bytes, threshold, d_ws, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+// Check one blob of a decompression call and describe it for the kernel
+// (chunk_base is set by the caller).
+int make_blob(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst, uint64_t dst_capacity,
+              BlobDesc &d) {
+    if (!info || !d_blob) return ZC_EINVAL;
     const int W = word_bytes(info->dtype);
     if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
     if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
     if (info->blob_bytes < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks) return ZC_EINVAL;
     if (dst_capacity < info->nbytes || (info->nbytes && !d_dst)) return ZC_ECAPACITY;
     if (!aligned(d_blob, 16) || !aligned(d_dst, W)) return ZC_EINVAL;
+    d = BlobDesc{};
+    d.blob = static_cast<const uint8_t *>(d_blob);
+    d.base = static_cast<const uint8_t *>(d_base);
+    d.dst = static_cast<uint8_t *>(d_dst);
+    d.blob_bytes = info->blob_bytes;
+    d.nbytes = info->nbytes;
+    d.n_chunks = info->n_chunks;
+    return ZC_OK;
+}
+
+int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst, uint64_t dst_capacity,
+                    uint32_t flags, int32_t *d_status, void *stream) {
+    if (!d_status) return ZC_EINVAL;
     if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
     DecodeArgs a{};
-    a.blob = static_cast<const uint8_t *>(d_blob);
-    a.blob_bytes = info->blob_bytes;
-    a.nbytes = info->nbytes;
+    const int st = make_blob(d_blob, info, d_base, d_dst, dst_capacity, a.one);
+    if (st != ZC_OK) return st;
+    a.n_blobs = 1;
+    a.total_chunks = info->n_chunks;
     a.chunk_bytes = info->chunk_bytes;
-    a.n_chunks = info->n_chunks;
-    a.dst = static_cast<uint8_t *>(d_dst);
-    a.base = static_cast<const uint8_t *>(d_base);
     a.flags = flags;
     a.d_status = d_status;
-    return launch_decode(info->dtype, a, static_cast<cudaStream_t>(stream));
+    return launch_decode(info->dtype, d_base != nullptr, a, static_cast<cudaStream_t>(stream));
 }
 
 bool delta_dtype(int dtype) { return dtype == ZC_U8 || dtype == ZC_U16 || dtype == ZC_U32; }
 
 } // namespace
+
+extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes) {
+    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95)) return 0;
+    return ws_size(1, chunks_of(nbytes, chunk_bytes), word_bytes(dtype), chunk_bytes);
+}
+
+extern "C" uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes) {
+    if (n == 0) return kCtrlBytes;
+    if (!nbytes) return 0;
+    uint64_t nc = 0;
+    for (uint32_t t = 0; t < n; t++) {
+        if (!valid_params(nbytes[t], dtype, chunk_bytes, 0.95)) return 0;
+        nc += chunks_of(nbytes[t], chunk_bytes);
+    }
+    if (nc > 0xFFFFFFFFull) return 0;
+    return ws_size(n, nc, word_bytes(dtype), chunk_bytes);
+}
 
 extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
                            uint32_t chunk_bytes, double threshold,
@@ -336,6 +431,84 @@ extern "C" int zc_decompress_delta(const void *d_blob, const zc_info *info, cons
     if (info->nbytes && (!d_base || !d_dst || !aligned(d_base, 16) || !aligned(d_dst, 16))) return ZC_EINVAL;
     return decompress_impl(d_blob, info, info->nbytes ? d_base : nullptr, d_dst, dst_capacity, flags, d_status,
                            stream);
+}
+
+extern "C" uint64_t zc_decompress_workspace_size_batch(uint32_t n) {
+    return n > 1 ? pad256(sizeof(BlobDesc) * uint64_t(n)) : 0;
+}
+
+extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const void *const *d_bases,
+                                 const uint64_t *nbytes, int dtype, const int32_t *ndims, const int64_t *shapes,
+                                 uint32_t chunk_bytes, double threshold, void *const *d_blobs,
+                                 const uint64_t *blob_capacities, uint64_t *d_blob_bytes, void *d_ws,
+                                 uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (n == 0) return ZC_OK;
+    if (!d_srcs || !nbytes || !ndims || !shapes || !d_blobs || !blob_capacities || !d_blob_bytes || !d_status)
+        return ZC_EINVAL;
+    if (d_bases && !delta_dtype(dtype)) return ZC_EINVAL;
+    std::vector<TensorDesc> table(n);
+    uint64_t nc = 0;
+    for (uint32_t t = 0; t < n; t++) {
+        const void *base = nullptr;
+        if (d_bases && nbytes[t]) {
+            base = d_bases[t];
+            if (!base || !d_srcs[t] || !aligned(base, 16) || !aligned(d_srcs[t], 16)) return ZC_EINVAL;
+        }
+        const int st = make_tensor(d_srcs[t], base, nbytes[t], dtype, ndims[t], shapes + 8 * uint64_t(t),
+                                   chunk_bytes, threshold, d_blobs[t], blob_capacities[t], d_blob_bytes + t,
+                                   table[t]);
+        if (st != ZC_OK) return st;
+        table[t].chunk_base = uint32_t(nc);
+        nc += table[t].n_chunks;
+        if (nc > 0xFFFFFFFFull) return ZC_EINVAL;
+    }
+    EncodeArgs a{};
+    if (n == 1) a.one = table[0];
+    a.total_chunks = uint32_t(nc);
+    a.d_status = d_status;
+    return run_compress(a, table.data(), n, d_bases != nullptr, dtype, chunk_bytes, threshold, d_ws, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const zc_info *infos,
+                                   const void *const *d_bases, void *const *d_dsts, const uint64_t *dst_capacities,
+                                   uint32_t flags, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (n == 0) return ZC_OK;
+    if (!d_blobs || !infos || !d_dsts || !dst_capacities || !d_status) return ZC_EINVAL;
+    if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
+    const int dtype = infos[0].dtype;
+    const uint32_t chunk_bytes = infos[0].chunk_bytes;
+    if (d_bases && !delta_dtype(dtype)) return ZC_EINVAL;
+    if (n > 1 && (!d_ws || !aligned(d_ws, 16) || ws_bytes < zc_decompress_workspace_size_batch(n))) return ZC_EINVAL;
+    std::vector<BlobDesc> table(n);
+    uint64_t nc = 0;
+    for (uint32_t t = 0; t < n; t++) {
+        if (infos[t].dtype != dtype || infos[t].chunk_bytes != chunk_bytes) return ZC_EINVAL;
+        const void *base = nullptr;
+        if (d_bases && infos[t].nbytes) {
+            base = d_bases[t];
+            if (!base || !d_dsts[t] || !aligned(base, 16) || !aligned(d_dsts[t], 16)) return ZC_EINVAL;
+        }
+        const int st = make_blob(d_blobs[t], &infos[t], base, d_dsts[t], dst_capacities[t], table[t]);
+        if (st != ZC_OK) return st;
+        table[t].chunk_base = uint32_t(nc);
+        nc += table[t].n_chunks;
+        if (nc > 0xFFFFFFFFull) return ZC_EINVAL;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DecodeArgs a{};
+    if (n == 1) a.one = table[0];
+    else {
+        const int st = upload_table(table.data(), sizeof(BlobDesc) * n, d_ws, s);
+        if (st != ZC_OK) return st;
+        a.blobs = static_cast<const BlobDesc *>(d_ws);
+    }
+    a.n_blobs = n;
+    a.total_chunks = uint32_t(nc);
+    a.chunk_bytes = chunk_bytes;
+    a.flags = flags;
+    a.d_status = d_status;
+    return launch_decode(dtype, d_bases != nullptr, a, s);
 }
 
 extern "C" int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream) {

@@ -7,19 +7,29 @@
 
 namespace zc {
 
-struct EncodeArgs {
+// One tensor of a compression call.
+struct TensorDesc {
     const uint8_t *src;
     const uint8_t *base;            // delta: the base tensor (src XOR base is coded), else null
-    uint64_t nbytes;
-    uint32_t chunk_bytes;
-    uint32_t n_chunks;
-    double threshold;
     uint8_t *blob;
-    uint64_t cap;
     uint64_t *d_blob_bytes;
+    uint64_t nbytes;
+    uint64_t cap;                   // blob capacity
+    uint32_t n_chunks;
+    uint32_t chunk_base;            // call-wide index of its first chunk
+    uint32_t header[24];            // the 96-byte header, CRC field zero (final CRC if empty)
+};
+
+struct EncodeArgs {
+    TensorDesc one;                 // the tensor, when the call has one
+    const TensorDesc *tensors;      // device table of the tensors, when it has more
+    uint32_t n_tensors;
+    uint32_t total_chunks;          // over all tensors
+    uint32_t chunk_bytes;
+    double threshold;
     int32_t *d_status;
-    uint8_t *ws_ctrl;               // u32 coder ticket, u32 done, u32 header-CRC accumulator
-    unsigned long long *ws_status;  // per chunk: flag << 62 | padded size or prefix
+    uint8_t *ws_ctrl;               // u32 coder ticket; per tensor t at 256 + 16 t: u32 done, u32 header-CRC acc.
+    unsigned long long *ws_status;  // per chunk (call-wide index): flag << 62 | padded size or prefix
     uint8_t *ws_info;               // per chunk of the wave: 32 B {CRC, W stream words}
     uint8_t *ws_ftab;               // per chunk of the wave and stream: 256 u16 table
     uint8_t *ws_cand;               // per chunk of the wave and stream: n_pad symbol bytes
@@ -27,20 +37,28 @@ struct EncodeArgs {
     uint8_t *ws_slots;              // per coding warp: W records of rec_stride bytes
     uint64_t slot_bytes;
     uint64_t rec_stride;
-    uint32_t wave_start;            // first chunk of this wave
+    uint32_t wave_start;            // first chunk of this wave (call-wide index)
     uint32_t wave_n;                // chunks in this wave
     uint32_t workers;               // coding warps
-    uint32_t header[24];            // the 96-byte header, CRC field zero (final CRC if empty)
+};
+
+// One blob of a decompression call.
+struct BlobDesc {
+    const uint8_t *blob;
+    const uint8_t *base;            // delta: the output is the decoded bytes XOR base, else null
+    uint8_t *dst;
+    uint64_t blob_bytes;
+    uint64_t nbytes;
+    uint32_t n_chunks;
+    uint32_t chunk_base;            // call-wide index of its first chunk
 };
 
 struct DecodeArgs {
-    const uint8_t *blob;
-    const uint8_t *base;            // delta: the output is the decoded bytes XOR base, else null
-    uint64_t blob_bytes;
-    uint64_t nbytes;
+    BlobDesc one;                   // the blob, when the call has one
+    const BlobDesc *blobs;          // device table of the blobs, when it has more
+    uint32_t n_blobs;
+    uint32_t total_chunks;
     uint32_t chunk_bytes;
-    uint32_t n_chunks;
-    uint8_t *dst;
     uint32_t flags;
     int32_t *d_status;
 };
@@ -55,11 +73,27 @@ struct CrcArgs {
     uint32_t *out;
 };
 
-// Statistics and coding kernels for chunks [wave_start, wave_start + wave_n);
-// the empty-tensor blob when n_chunks == 0.
-int launch_encode_wave(int dtype, const EncodeArgs &a, cudaStream_t s);
+// Statistics and coding kernels for chunks [wave_start, wave_start + wave_n)
+// (total_chunks > 0).
+int launch_encode_wave(int dtype, bool delta, const EncodeArgs &a, cudaStream_t s);
+// The blobs (header alone) of the call's tensors that have no chunks.
+int launch_empty_blobs(const EncodeArgs &a, cudaStream_t s);
+
+// The tensor (blob) of a call-wide chunk index: the last one whose first
+// chunk is at or before it (binary search over the table).
+template <class D>
+__device__ __forceinline__ uint32_t owner_of(const D *table, uint32_t n, uint32_t g) {
+    uint32_t lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (table[mid].chunk_base <= g) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
 int encode_warps_per_sm();
-int launch_decode(int dtype, const DecodeArgs &a, cudaStream_t s);
+// delta: whether the blobs carry base tensors (all or none of them)
+int launch_decode(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s);
 int launch_crc(const CrcArgs &a, cudaStream_t s);
 
 } // namespace zc

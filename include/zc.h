@@ -171,6 +171,59 @@ ZC_API int zc_compress_delta(const void *d_base, const void *d_new, uint64_t nby
 ZC_API int zc_decompress_delta(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst,
                         uint64_t dst_capacity, uint32_t flags, int32_t *d_status, void *stream);
 
+/* Batched compression: n tensors of one dtype and chunk size in one call,
+ * each to its own blob, byte-identical to zc_compress (or, with d_bases,
+ * zc_compress_delta) of that tensor alone. The chunks of all the tensors
+ * form one grid, so a model's many small tensors (ZipNN note, Table II
+ * models; lmzip README, safetensors shards compressed tensor by tensor) keep
+ * every SM busy where a call per tensor would leave most of them idle.
+ *   n                  number of tensors; 0 is a no-op
+ *   d_srcs[t]          device tensor t (host array of n device pointers)
+ *   d_bases            NULL, or n device base tensors: tensor t is then coded
+ *                      as d_srcs[t] XOR d_bases[t] as in zc_compress_delta
+ *                      (dtype ZC_U8/U16/U32, both 16-byte aligned)
+ *   nbytes[t]          host array: bytes of tensor t (0 allowed)
+ *   ndims[t], shapes   host arrays: rank of tensor t and its shape in
+ *                      shapes[8 t .. 8 t + ndims[t])
+ *   d_blobs[t], blob_capacities[t]
+ *                      blob t (16-byte aligned) and its capacity, as in
+ *                      zc_compress
+ *   d_blob_bytes       DEVICE array of n uint64: entry t receives blob t's size
+ *   d_ws, ws_bytes     ws_bytes >= zc_workspace_size_batch(nbytes, n, ...)
+ *   d_status           one device int32 for the whole call
+ * The descriptor table travels with the launches: the host arrays may be
+ * reused or freed when the call returns. Blobs must not overlap one another
+ * or any input. Returns ZC_EINVAL (with nothing launched) when any tensor's
+ * arguments are invalid, and zc_compress's other codes. */
+ZC_API int zc_compress_batch(uint32_t n, const void *const *d_srcs, const void *const *d_bases,
+                             const uint64_t *nbytes, int dtype, const int32_t *ndims, const int64_t *shapes,
+                             uint32_t chunk_bytes, double threshold, void *const *d_blobs,
+                             const uint64_t *blob_capacities, uint64_t *d_blob_bytes, void *d_ws,
+                             uint64_t ws_bytes, int32_t *d_status, void *stream);
+
+/* Workspace bytes for zc_compress_batch of n tensors of the given sizes
+ * (0 if a size or the parameters are invalid). Host only. */
+ZC_API uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes);
+
+/* Batched decompression of n blobs of one dtype and chunk size in one grid,
+ * each output byte-identical to zc_decompress (or, with d_bases,
+ * zc_decompress_delta) of that blob alone.
+ *   d_blobs[t], infos[t]   blob t (device, 16-byte aligned) and its
+ *                          zc_blob_info; every info has the same dtype and
+ *                          chunk_bytes (else ZC_EINVAL)
+ *   d_bases                NULL, or n device base tensors (delta blobs)
+ *   d_dsts[t], dst_capacities[t]  output t, as in zc_decompress
+ *   d_ws, ws_bytes         ws_bytes >= zc_decompress_workspace_size_batch(n)
+ *                          (0 for n <= 1, when d_ws may be NULL)
+ *   d_status               one device int32 for the whole call
+ * Host arrays may be reused or freed when the call returns. */
+ZC_API int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const zc_info *infos,
+                               const void *const *d_bases, void *const *d_dsts, const uint64_t *dst_capacities,
+                               uint32_t flags, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream);
+
+/* Workspace bytes for zc_decompress_batch of n blobs (the descriptor table). */
+ZC_API uint64_t zc_decompress_workspace_size_batch(uint32_t n);
+
 /* zlib-compatible CRC-32 of each piece_bytes-byte piece of a device buffer,
  * the last piece possibly shorter (cuZipNN API hash_tensor_with_crc32,
  * checksum_chunk_bytes). piece_bytes = 0 means one CRC of the whole buffer.

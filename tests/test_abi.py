@@ -103,3 +103,51 @@ def test_delta_entry_points_reject_bad_arguments_on_the_host():
     info.dtype = zc.U16
     assert L.zc_decompress_delta(aligned, ctypes.byref(info), odd, aligned, 2048, 0, aligned, None) == zc.EINVAL
     assert L.zc_decompress_delta(aligned, ctypes.byref(info), aligned, odd, 2048, 0, aligned, None) == zc.EINVAL
+
+
+def test_batch_entry_points_reject_bad_arguments_on_the_host():
+    """The batched entry points check every tensor (blob) before any launch
+    (the device pointers below are never dereferenced)."""
+    import ctypes
+    import entropy_coding_gb300 as zc
+    L = zc.lib()
+    aligned = 0x10000
+    vp2 = ctypes.c_void_p * 2
+    u64_2 = ctypes.c_uint64 * 2
+    ndims = (ctypes.c_int32 * 2)(1, 1)
+    shapes = (ctypes.c_int64 * 16)(*([1024] + [0] * 7 + [1024] + [0] * 7))
+
+    def comp(n, srcs, bases, nbytes, dtype, nd=ndims):
+        return L.zc_compress_batch(n, srcs, bases, nbytes, dtype, nd, shapes, 4096, 0.95, vp2(aligned, aligned),
+                                   u64_2(1 << 16, 1 << 16), aligned, aligned, 1 << 24, aligned, None)
+    assert comp(0, None, None, None, zc.BF16) == zc.OK
+    assert comp(2, None, None, u64_2(2048, 2048), zc.BF16) == zc.EINVAL
+    # deltas only for unsigned word dtypes
+    assert comp(2, vp2(aligned, aligned), vp2(aligned, aligned), u64_2(2048, 2048), zc.BF16) == zc.EINVAL
+    # the second tensor's shape does not match its size
+    assert comp(2, vp2(aligned, aligned), None, u64_2(2048, 4096), zc.BF16) == zc.EINVAL
+    # a misaligned second source
+    assert comp(2, vp2(aligned, aligned + 1), None, u64_2(2048, 2048), zc.BF16) == zc.EINVAL
+
+    infos = (zc._Info * 2)()
+    for i, dt in enumerate((zc.BF16, zc.FP32)):
+        infos[i].dtype, infos[i].ndim, infos[i].n_chunks, infos[i].chunk_bytes = dt, 1, 1, 4096
+        infos[i].nbytes = 2048 if dt == zc.BF16 else 4096
+        infos[i].shape[0] = 1024
+        infos[i].blob_bytes = 1 << 12
+    caps = u64_2(1 << 16, 1 << 16)
+    ws = zc.decompress_workspace_size_batch(2)
+    assert ws >= 2 * 48 and zc.decompress_workspace_size_batch(1) == 0
+    # mixed dtypes in one batch
+    assert L.zc_decompress_batch(2, vp2(aligned, aligned), infos, None, vp2(aligned, aligned), caps, 0, aligned,
+                                 ws, aligned, None) == zc.EINVAL
+    infos[1].dtype, infos[1].nbytes = zc.BF16, 2048
+    # no workspace for the descriptor table
+    assert L.zc_decompress_batch(2, vp2(aligned, aligned), infos, None, vp2(aligned, aligned), caps, 0, None, 0,
+                                 aligned, None) == zc.EINVAL
+    # an output too small for the second blob
+    assert L.zc_decompress_batch(2, vp2(aligned, aligned), infos, None, vp2(aligned, aligned), u64_2(1 << 16, 16),
+                                 0, aligned, ws, aligned, None) == zc.ECAPACITY
+    assert L.zc_decompress_batch(0, None, None, None, None, None, 0, None, 0, None, None) == zc.OK
+    assert zc.workspace_size_batch([2048, 3], zc.BF16, 4096) == 0
+    assert zc.workspace_size_batch([2048, 0], zc.BF16, 4096) > 0
