@@ -42,7 +42,7 @@ def _args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="fp32_64m",
                    choices=["fp32_64m", "bf16_1m", "fp32clean_64m", "fp16_16m", "bf16_delta", "bf16_delta_fused",
-                            "bf16_llama_gate"])
+                            "bf16_llama_gate", "llama8b", "llama8b_batch"])
     p.add_argument("--chunk-bytes", type=int, default=131072)
     p.add_argument("--threshold", type=float, default=0.95)
     p.add_argument("--e2e-steps", type=int, default=5)
@@ -67,11 +67,35 @@ def make_workload(name: str, device):
         # GPU arm forms it inside the kernels from the two checkpoints
         return (wl.bf16_delta(device)[1], "two BF16 4096x14336 checkpoints, seed 4, XOR difference formed in "
                                           "the kernels (compress_delta / decompress_delta)")
+    if name in MODEL_WORKLOADS:
+        # the reference arm samples the model from its start (the embedding)
+        nm, shape = wl.llama8b_specs()[0]
+        return wl.llama8b_tensor(0, nm, shape, device), MODEL_WORKLOADS[name]
     if name == "bf16_llama_gate":
         specs = wl.llama8b_specs()
         nm, shape = specs[5]
         return wl.llama8b_tensor(5, nm, shape, device), "Llama-3.1-8B layer-0 gate_proj BF16 14336x4096"
     raise ValueError(name)
+
+
+MODEL_WORKLOADS = {
+    "llama8b": "Llama-3.1-8B-shaped BF16 model (290 tensors, 16.06 GB), N(0,0.02) per tensor, RMSNorm vectors of "
+               "ones; one compression and one decompression call per tensor",
+    "llama8b_batch": "Llama-3.1-8B-shaped BF16 model (290 tensors, 16.06 GB), N(0,0.02) per tensor, RMSNorm "
+                     "vectors of ones; all tensors in one batched compression and one batched decompression call",
+}
+
+
+def encode_launches(n_chunks: int, word: int, chunk_bytes: int) -> int:
+    """Kernels one compression call of n_chunks launches: a statistics and a
+    coding kernel per wave, a wave holding at most 512 MiB of per-chunk
+    statistics (32 + W (512 + n_pad) bytes a chunk), as the library plans it
+    with a full-size workspace."""
+    if n_chunks == 0:
+        return 1  # the empty-blob kernel
+    n_pad = (chunk_bytes // word + 31) // 32 * 32
+    wave = min(n_chunks, (512 << 20) // (32 + word * (512 + n_pad)))
+    return 2 * ((n_chunks + wave - 1) // wave)
 
 
 def peaks():
@@ -229,6 +253,180 @@ def cpu_baseline(t, code, a):
                       f"decompressed once, single-threaded C oracle, {t_total:.1f} s"}
 
 
+def run_model(a, world, rank, local, dev, stream):
+    """The Llama-shaped model: every tensor compressed and decompressed, by one
+    call per tensor (llama8b) or one batched call each way (llama8b_batch)."""
+    import torch
+    import torch.distributed as dist
+    import entropy_coding_gb300 as zc
+    from entropy_coding_gb300 import workloads as wl
+
+    batched = a.workload == "llama8b_batch"
+    specs = wl.llama8b_specs()
+    C, thr, code, Wd = a.chunk_bytes, a.threshold, wl.BF16, 2
+    sizes = [2 * int(torch.Size(sh).numel()) for _, sh in specs]
+    n = len(specs)
+
+    def layout(lens):
+        offs, o = [], 0
+        for x in lens:
+            offs.append(o)
+            o += (x + 255) // 256 * 256
+        return offs, o
+
+    s_offs, s_total = layout(sizes)
+    src_all = torch.empty(s_total, dtype=torch.uint8, device=dev)
+    srcs = [src_all[o: o + x] for o, x in zip(s_offs, sizes)]
+    for i, ((nm, sh), d) in enumerate(zip(specs, srcs)):
+        d.copy_(wl.as_bytes(wl.llama8b_tensor(i, nm, sh, dev)))
+    out_all = torch.empty(s_total, dtype=torch.uint8, device=dev)
+    outs = [out_all[o: o + x] for o, x in zip(s_offs, sizes)]
+    caps = [zc.blob_size(x, code, C, thr) for x in sizes]
+    b_offs, b_total = layout(caps)
+    blob_all = torch.empty(b_total, dtype=torch.uint8, device=dev)
+    blobs = [blob_all[o: o + x] for o, x in zip(b_offs, caps)]
+    shapes = [tuple(sh) for _, sh in specs]
+    nb = torch.zeros(n, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if batched:
+        ws = torch.empty(zc.workspace_size_batch(sizes, code, C), dtype=torch.uint8, device=dev)
+        n_dws = zc.decompress_workspace_size_batch(n)
+        dws = torch.empty(max(16, n_dws), dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(max(zc.workspace_size(x, code, C) for x in sizes), dtype=torch.uint8, device=dev)
+    N = sum(sizes)
+    verify = not a.no_verify
+
+    def comp(inputs):
+        if batched:
+            zc.compress_batch_into(inputs, blobs, nb, ws, st, code, shapes, C, thr, stream)
+        else:
+            for t in range(n):
+                zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws, st, C, thr, stream, dtype=code,
+                                 shape=shapes[t])
+
+    def decomp(infos):
+        if batched:
+            zc.decompress_batch_into(blobs, infos, outs, st, dws, verify, stream)
+        else:
+            for t in range(n):
+                zc.decompress_into(blobs[t], infos[t], outs[t], st, verify, stream)
+
+    with torch.cuda.stream(stream):
+        comp(srcs)
+    stream.synchronize()
+    assert int(st.item()) == 0
+    lens = nb.tolist()
+    S = sum(lens)
+    infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C)].cpu()) for b, x in zip(blobs, sizes)]
+    with torch.cuda.stream(stream):
+        decomp(infos)
+    stream.synchronize()
+    assert int(st.item()) == 0 and torch.equal(out_all, src_all), "round trip failed"
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            comp(srcs)
+            decomp(infos)
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for ev in evs:
+                ev[0].record(stream)
+                comp(srcs)
+                ev[1].record(stream)
+                decomp(infos)
+                ev[2].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    t_enc = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    assert int(st.item()) == 0 and nb.tolist() == lens
+    total = t_enc + t_dec
+    if world > 1:
+        tt = torch.tensor([total, t_enc, t_dec], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total, t_enc, t_dec = tt.tolist()
+        dist.barrier()
+
+    # end to end through the public calls: the model from pinned host memory,
+    # the blobs back to the host and up again, the restored model to the host
+    e2e_steps = max(1, min(a.e2e_steps, 2))
+    h_src = torch.empty(s_total, dtype=torch.uint8, pin_memory=True)
+    h_src.copy_(src_all)
+    h_blob = torch.empty(b_total, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(s_total, dtype=torch.uint8, pin_memory=True)
+    h2d = d2h = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            src_all.copy_(h_src, non_blocking=True)
+            comp(srcs)
+            got = nb.tolist()
+            for o, k in zip(b_offs, got):
+                h_blob[o: o + k].copy_(blob_all[o: o + k], non_blocking=True)
+            for o, k in zip(b_offs, got):
+                blob_all[o: o + k].copy_(h_blob[o: o + k], non_blocking=True)
+            decomp(infos)
+            h_out.copy_(out_all, non_blocking=True)
+        stream.synchronize()
+        h2d += s_total + sum(got)
+        d2h += sum(got) + 8 * n + s_total
+    t_e2e = time.perf_counter() - t0
+    assert int(st.item()) == 0 and torch.equal(h_out, h_src)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    hbm, peak_kind = peaks()
+    alg = N + S
+    enc_ach = alg * a.steps / t_enc / 1e9
+    dec_ach = alg * a.steps / t_dec / 1e9
+    chunks = [(x + C - 1) // C for x in sizes]
+    if batched:
+        table_launches = lambda words: (words + 7679) // 7680
+        per_step = (encode_launches(sum(chunks), Wd, C) + table_launches(38 * n) + (1 if 0 in sizes else 0)
+                    + 1 + table_launches(12 * n))
+    else:
+        per_step = sum(encode_launches(c, Wd, C) + (1 if c else 0) for c in chunks)
+    line = {
+        "metric": "round-trip GB/s (original bytes; encode + decode)",
+        "value": round(world * N * a.steps / total / 1e9, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": a.workload, "desc": MODEL_WORKLOADS[a.workload], "nbytes": N, "tensors": n,
+                   "chunk_bytes": C, "threshold": thr, "verify_crc_on_decode": verify,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "encode": {"gbs": round(N * a.steps / t_enc / 1e9, 2), "roofline_frac": round(enc_ach / hbm, 4),
+                   "ms": round(1e3 * t_enc / a.steps, 4)},
+        "decode": {"gbs": round(N * a.steps / t_dec / 1e9, 2), "roofline_frac": round(dec_ach / hbm, 4),
+                   "ms": round(1e3 * t_dec / a.steps, 4)},
+        "size_pct": round(100.0 * S / N, 3),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(dec_ach, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
+                     "traffic": profiled_traffic("decode_kernel", a.workload),
+                     "algorithmic_bytes_per_launch": alg if batched else None,
+                     "note": "decompression time of the whole model (one decode_kernel launch when batched)"},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(N * e2e_steps / t_e2e / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d // e2e_steps, "d2h_bytes_per_step": d2h // e2e_steps},
+        "gpu_launches": per_step * a.steps,
+    }
+    del src_all, out_all, blob_all
+    first = wl.llama8b_tensor(0, *specs[0])
+    line["cpu_baseline"] = cpu_baseline(first, code, a)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     a = _args()
     if a.impl == "reference":
@@ -247,6 +445,9 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
+    if a.workload in MODEL_WORKLOADS:
+        run_model(a, world, rank, local, dev, stream)
+        return
 
     t, desc = make_workload(a.workload, dev)
     code = wl.dtype_code(t)
