@@ -88,13 +88,13 @@ MODEL_WORKLOADS = {
 
 def encode_launches(n_chunks: int, word: int, chunk_bytes: int) -> int:
     """Kernels one compression call of n_chunks launches: a statistics and a
-    coding kernel per wave, a wave holding at most 512 MiB of per-chunk
+    coding kernel per wave, a wave holding at most 2 GiB of per-chunk
     statistics (32 + W (512 + n_pad) bytes a chunk), as the library plans it
     with a full-size workspace."""
     if n_chunks == 0:
         return 1  # the empty-blob kernel
     n_pad = (chunk_bytes // word + 31) // 32 * 32
-    wave = min(n_chunks, (512 << 20) // (32 + word * (512 + n_pad)))
+    wave = min(n_chunks, (2048 << 20) // (32 + word * (512 + n_pad)))
     return 2 * ((n_chunks + wave - 1) // wave)
 
 

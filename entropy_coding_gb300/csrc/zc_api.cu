@@ -29,7 +29,7 @@ uint64_t chunks_of(uint64_t nbytes, uint32_t chunk_bytes) { return (nbytes + chu
 
 constexpr uint64_t kInfoBytes = 32;          // per chunk of a wave: CRC + W stream words
 constexpr uint64_t kTableBytes = 512;        // per chunk of a wave and stream: 256 u16 table
-constexpr uint64_t kWaveBytes = 512ull << 20;  // workspace of one statistics + coding wave, at most
+constexpr uint64_t kWaveBytes = 2048ull << 20;  // workspace of one statistics + coding wave, at most
 
 // Room for one coded record of a stream in a coding warp's slot. A record is
 // kept only while it is below lim = ceil(threshold x n) bytes, and the coder
