@@ -297,7 +297,7 @@ def run_model(a, world, rank, local, dev, stream):
     N = sum(sizes)
     verify = not a.no_verify
 
-    def comp(inputs):
+    def comp(inputs, blobs=blobs, nb=nb):
         if batched:
             zc.compress_batch_into(inputs, blobs, nb, ws, st, code, shapes, C, thr, stream)
         else:
@@ -305,7 +305,7 @@ def run_model(a, world, rank, local, dev, stream):
                 zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws, st, C, thr, stream, dtype=code,
                                  shape=shapes[t])
 
-    def decomp(infos):
+    def decomp(infos, blobs=blobs):
         if batched:
             zc.decompress_batch_into(blobs, infos, outs, st, dws, verify, stream)
         else:
@@ -380,6 +380,32 @@ def run_model(a, world, rank, local, dev, stream):
     t_e2e = time.perf_counter() - t0
     assert int(st.item()) == 0 and torch.equal(h_out, h_src)
 
+    # end to end with the blobs in page-locked host memory, written and read
+    # by the kernels; the host parses every header and table between the calls
+    del h_blob
+    hb_all = torch.empty(b_total, dtype=torch.uint8, pin_memory=True)
+    hb_blobs = [hb_all[o: o + x] for o, x in zip(b_offs, caps)]
+    hb_nb = torch.zeros(n, dtype=torch.int64, pin_memory=True)
+    h_out.zero_()
+    hb_h2d = hb_d2h = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            src_all.copy_(h_src, non_blocking=True)
+            comp(srcs, hb_blobs, hb_nb)
+        stream.synchronize()
+        got = hb_nb.tolist()
+        hb_infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C)]) for b, x in zip(hb_blobs, sizes)]
+        with torch.cuda.stream(stream):
+            decomp(hb_infos, [b[:k] for b, k in zip(hb_blobs, got)])
+            h_out.copy_(out_all, non_blocking=True)
+        stream.synchronize()
+        hb_h2d += s_total + sum(got)
+        hb_d2h += sum(got) + 8 * n + s_total
+    t_hb = time.perf_counter() - t0
+    assert int(st.item()) == 0 and torch.equal(h_out, h_src)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -416,7 +442,11 @@ def run_model(a, world, rank, local, dev, stream):
                      "note": "decompression time of the whole model (one decode_kernel launch when batched)"},
         "clocks": clk.summary(),
         "e2e": {"value": round(N * e2e_steps / t_e2e / 1e9, 3), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d // e2e_steps, "d2h_bytes_per_step": d2h // e2e_steps},
+                "h2d_bytes_per_step": h2d // e2e_steps, "d2h_bytes_per_step": d2h // e2e_steps,
+                "mode": "device blobs, copied to pinned host memory and back"},
+        "e2e_host_blob": {"value": round(N * e2e_steps / t_hb / 1e9, 3), "unit": "GB/s",
+                          "h2d_bytes_per_step": hb_h2d // e2e_steps, "d2h_bytes_per_step": hb_d2h // e2e_steps,
+                          "mode": "blobs written to and decoded from pinned host memory by the kernels"},
         "gpu_launches": per_step * a.steps,
     }
     del src_all, out_all, blob_all
@@ -466,13 +496,13 @@ def main():
     out = torch.empty(N, dtype=torch.uint8, device=dev)
     shape = tuple(t.shape)
 
-    def comp(inp):
+    def comp(inp, blob=blob, nb=nb):
         if base is None:
             zc.compress_into(inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
         else:
             zc.compress_delta_into(base, inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
 
-    def decomp(info):
+    def decomp(info, blob=blob, out=out):
         if base is None:
             zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
         else:
@@ -550,6 +580,56 @@ def main():
     t_e2e = time.perf_counter() - t0
     assert torch.equal(h_out, h_src)
 
+    # end to end with the blob in page-locked host memory: the coding kernel
+    # writes it over the host link and the decoder reads it from there (no
+    # blob copies); the host parses the header and table between the calls
+    hb_blob = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+    hb_nb = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    h_out.zero_()
+    hb_h2d = hb_d2h = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(a.e2e_steps):
+        with torch.cuda.stream(stream):
+            if base is not None:
+                base.copy_(h_base, non_blocking=True)
+            d_in.copy_(h_src, non_blocking=True)
+            comp(d_in, hb_blob, hb_nb)
+        stream.synchronize()
+        s_bytes = int(hb_nb.item())
+        hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C)])
+        with torch.cuda.stream(stream):
+            decomp(hb_info, hb_blob[:s_bytes])
+            h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        hb_h2d += N + s_bytes + (N if base is not None else 0)
+        hb_d2h += s_bytes + 8 + N
+    t_hb = time.perf_counter() - t0
+    assert torch.equal(h_out, h_src)
+
+    # zero copy: the tensor, the blob and the restored tensor all stay in
+    # page-locked host memory; the kernels read and write them over the link
+    zc_line = None
+    if base is None:
+        h_out.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(a.e2e_steps):
+            with torch.cuda.stream(stream):
+                comp(h_src, hb_blob, hb_nb)
+            stream.synchronize()
+            s_bytes = int(hb_nb.item())
+            hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C)])
+            with torch.cuda.stream(stream):
+                decomp(hb_info, hb_blob[:s_bytes], h_out)
+            stream.synchronize()
+        t_zc = time.perf_counter() - t0
+        assert int(st.item()) == 0 and torch.equal(h_out, h_src)
+        zc_line = {"value": round(N * a.e2e_steps / t_zc / 1e9, 3), "unit": "GB/s",
+                   "h2d_bytes_per_step": hb_h2d // a.e2e_steps, "d2h_bytes_per_step": hb_d2h // a.e2e_steps,
+                   "mode": "tensor, blob and restored tensor in pinned host memory, read and written by the "
+                           "kernels (no copies)"}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -587,7 +667,12 @@ def main():
                      "traffic": traffic, "algorithmic_bytes_per_launch": alg},
         "clocks": clk.summary(),
         "e2e": {"value": round(N * a.e2e_steps / t_e2e / 1e9, 3), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d // a.e2e_steps, "d2h_bytes_per_step": d2h // a.e2e_steps},
+                "h2d_bytes_per_step": h2d // a.e2e_steps, "d2h_bytes_per_step": d2h // a.e2e_steps,
+                "mode": "device blob, copied to pinned host memory and back"},
+        "e2e_host_blob": {"value": round(N * a.e2e_steps / t_hb / 1e9, 3), "unit": "GB/s",
+                          "h2d_bytes_per_step": hb_h2d // a.e2e_steps, "d2h_bytes_per_step": hb_d2h // a.e2e_steps,
+                          "mode": "blob written to and decoded from pinned host memory by the kernels"},
+        "e2e_zero_copy": zc_line,
         "gpu_launches": 3 * a.steps,  # stats_kernel + code_kernel + decode_kernel per step
     }
     line["cpu_baseline"] = cpu_baseline(t, code, a)

@@ -146,9 +146,11 @@ def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tenso
 
 
 def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
-             stream=None) -> torch.Tensor:
-    """Compress a CUDA tensor into a self-describing blob (1-D uint8 CUDA tensor).
+             stream=None, host_blob: bool = False) -> torch.Tensor:
+    """Compress a CUDA tensor into a self-describing blob (1-D uint8 tensor).
 
+    The blob is a CUDA tensor, or with ``host_blob`` a page-locked CPU tensor
+    that the kernels write directly over the host link (no separate copy).
     Synchronises once, to read the blob length."""
     if not t.is_cuda:
         raise ZcError(EINVAL, "compress expects a CUDA tensor")
@@ -159,15 +161,20 @@ def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float
     if cap == 0:
         raise ZcError(EINVAL, "invalid compression parameters")
     dev = src.device
-    blob = torch.empty(cap, dtype=torch.uint8, device=dev)
+    if host_blob:
+        blob = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+        nb = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    else:
+        blob = torch.empty(cap, dtype=torch.uint8, device=dev)
+        nb = torch.zeros(1, dtype=torch.int64, device=dev)
     ws = torch.empty(max(16, workspace_size(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
-    nb = torch.zeros(1, dtype=torch.int64, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flat = src.view(-1).view(torch.uint8) if src.dtype != torch.bool else src.view(-1).view(torch.uint8)
+    flat = src.view(-1).view(torch.uint8)
     compress_into(flat, blob, nb, ws, status, chunk_bytes, threshold, stream, dtype=code, shape=tuple(t.shape))
-    st, n = int(status.item()), int(nb.item())
-    _check(st, "zc_compress (device)")
-    return blob[:n]
+    if host_blob:
+        torch.cuda.synchronize(dev)  # the length is written to host memory by the kernel
+    _check(int(status.item()), "zc_compress (device)")
+    return blob[: int(nb.item())]
 
 
 def blob_info(prefix) -> dict:
@@ -197,7 +204,7 @@ def _info_struct(d: dict) -> _Info:
 
 
 def read_info(blob: torch.Tensor) -> dict:
-    """blob_info of a device blob (copies the header and table to the host)."""
+    """blob_info of a device or host blob (the header and table on the host)."""
     head = blob[:96].cpu()
     n_chunks = int.from_bytes(bytes(head[24:28].numpy()), "little")
     return blob_info(blob[: 96 + 16 * n_chunks].cpu())
@@ -212,14 +219,24 @@ def decompress_into(blob: torch.Tensor, info: dict, out: torch.Tensor, status: t
     _check(st, "zc_decompress")
 
 
-def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True, stream=None) -> torch.Tensor:
-    """Restore the exact tensor (dtype and shape from the blob header)."""
-    if not blob.is_cuda:
-        raise ZcError(EINVAL, "decompress expects a CUDA blob")
+def _readable(blob: torch.Tensor) -> bool:
+    return blob.is_cuda or (blob.device.type == "cpu" and blob.is_pinned())
+
+
+def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True, stream=None,
+               device=None) -> torch.Tensor:
+    """Restore the exact tensor (dtype and shape from the blob header). The
+    blob is a CUDA tensor or a page-locked CPU tensor, which the kernel reads
+    directly; the tensor is made on the blob's device (CUDA blob) or on
+    ``device`` (default: the current CUDA device)."""
+    if not _readable(blob):
+        raise ZcError(EINVAL, "decompress expects a CUDA or page-locked CPU blob")
     info = read_info(blob) if info is None else info
+    dev = blob.device if blob.is_cuda else torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
     dt = _CODE_TO_TORCH[info["dtype"]]
-    out = torch.empty(info["shape"], dtype=dt, device=blob.device)
-    status = torch.zeros(1, dtype=torch.int32, device=blob.device)
+    out = torch.empty(info["shape"], dtype=dt, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     decompress_into(blob, info, out, status, verify, stream)
     _check(int(status.item()), "zc_decompress (device)")
     return out
@@ -355,10 +372,12 @@ def compress_batch_into(srcs, blobs, blob_bytes: torch.Tensor, workspace: torch.
 
 
 def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD, stream=None,
-                   bases=None) -> list:
+                   bases=None, host_blob: bool = False) -> list:
     """Compress a list of CUDA tensors of one dtype in one call; returns one
     blob per tensor, each equal to compress() of that tensor (with ``bases``:
-    to compress_delta(bases[t], tensors[t])). Synchronises once."""
+    to compress_delta(bases[t], tensors[t])); with ``host_blob`` the blobs are
+    views of one page-locked CPU buffer written by the kernels. Synchronises
+    once."""
     n = len(tensors)
     if n == 0:
         return []
@@ -383,7 +402,8 @@ def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float =
         offs.append(o)
         o += (c + 255) // 256 * 256
     dev = ts[0].device
-    buf = torch.empty(o, dtype=torch.uint8, device=dev)
+    buf = torch.empty(o, dtype=torch.uint8, pin_memory=True) if host_blob else \
+        torch.empty(o, dtype=torch.uint8, device=dev)
     blobs = [buf[a: a + c] for a, c in zip(offs, caps)]
     ws = torch.empty(max(16, workspace_size_batch(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
     nb = torch.zeros(n, dtype=torch.int64, device=dev)
@@ -392,6 +412,8 @@ def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float =
     compress_batch_into(flat, blobs, nb, ws, status, code, [tuple(t.shape) for t in tensors], chunk_bytes,
                         threshold, stream, bases=[b.view(-1).view(torch.uint8) for b in bs] if bases is not None
                         else None)
+    if host_blob:
+        torch.cuda.synchronize(dev)
     _check(int(status.item()), "zc_compress_batch (device)")
     return [b[: int(k)] for b, k in zip(blobs, nb.tolist())]
 
@@ -421,8 +443,10 @@ def decompress_batch(blobs, infos=None, verify: bool = True, stream=None, bases=
     n = len(blobs)
     if n == 0:
         return []
+    if not all(_readable(b) for b in blobs):
+        raise ZcError(EINVAL, "decompress_batch expects CUDA or page-locked CPU blobs")
     infos = [read_info(b) for b in blobs] if infos is None else list(infos)
-    dev = blobs[0].device
+    dev = blobs[0].device if blobs[0].is_cuda else torch.device("cuda", torch.cuda.current_device())
     if bases is not None:
         outs = [torch.empty_like(b.contiguous()) for b in bases]
         bflat = [b.contiguous().view(-1).view(torch.uint8) for b in bases]

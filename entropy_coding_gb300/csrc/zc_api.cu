@@ -250,6 +250,55 @@ int upload_table(const void *h, uint64_t bytes, void *d, cudaStream_t s) {
     return ZC_OK;
 }
 
+// The address the kernels use for a data buffer: device or managed memory of
+// the current device as given, page-locked host memory (cudaHostAlloc,
+// cudaHostRegister) through its device mapping, so that the kernels read or
+// write host memory directly over the host link. Unregistered host memory
+// and other devices' memory are refused: the kernels never touch an address
+// that the current device cannot reach.
+int kernel_address(const void *p, const void **out) {
+    *out = nullptr;
+    if (!p) return ZC_OK;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not left behind for the launch checks
+        return ZC_EINVAL;
+    }
+    if (!at.devicePointer) return ZC_EINVAL;
+    if (at.type == cudaMemoryTypeDevice) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || at.device != dev) return ZC_EINVAL;
+    } else if (at.type != cudaMemoryTypeHost && at.type != cudaMemoryTypeManaged) {
+        return ZC_EINVAL;
+    }
+    *out = at.devicePointer;
+    return ZC_OK;
+}
+
+template <class T>
+int resolve(T *&p) {
+    const void *q = nullptr;
+    const int st = kernel_address(p, &q);
+    p = const_cast<T *>(static_cast<const T *>(q));
+    return st;
+}
+
+// Kernel addresses of a tensor's (a blob's) buffers; after all checks.
+int resolve_tensor(TensorDesc &d) {
+    int st = resolve(d.src);
+    if (st == ZC_OK) st = resolve(d.base);
+    if (st == ZC_OK) st = resolve(d.blob);
+    if (st == ZC_OK) st = resolve(d.d_blob_bytes);
+    return st;
+}
+
+int resolve_blob(BlobDesc &d) {
+    int st = resolve(d.blob);
+    if (st == ZC_OK) st = resolve(d.base);
+    if (st == ZC_OK) st = resolve(d.dst);
+    return st;
+}
+
 // Workspace of a compression call over n tensors and nc chunks: control
 // (coder ticket; per tensor a done counter and a header-CRC accumulator),
 // the tensor table (batches), the chunk status words, then a wave's
@@ -339,6 +388,7 @@ int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dt
     const int st = make_tensor(d_src, d_base, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob,
                                blob_capacity, d_blob_bytes, a.one);
     if (st != ZC_OK) return st;
+    if (resolve_tensor(a.one) != ZC_OK) return ZC_EINVAL;
     a.total_chunks = a.one.n_chunks;
     a.d_status = d_status;
     return run_compress(a, nullptr, 1, d_base != nullptr, dtype, chunk_bytes, threshold, d_ws, ws_bytes,
@@ -373,6 +423,7 @@ int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base,
     DecodeArgs a{};
     const int st = make_blob(d_blob, info, d_base, d_dst, dst_capacity, a.one);
     if (st != ZC_OK) return st;
+    if (resolve_blob(a.one) != ZC_OK) return ZC_EINVAL;
     a.n_blobs = 1;
     a.total_chunks = info->n_chunks;
     a.chunk_bytes = info->chunk_bytes;
@@ -462,6 +513,8 @@ extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const vo
         nc += table[t].n_chunks;
         if (nc > 0xFFFFFFFFull) return ZC_EINVAL;
     }
+    for (auto &d : table)
+        if (resolve_tensor(d) != ZC_OK) return ZC_EINVAL;
     EncodeArgs a{};
     if (n == 1) a.one = table[0];
     a.total_chunks = uint32_t(nc);
@@ -495,6 +548,8 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
         nc += table[t].n_chunks;
         if (nc > 0xFFFFFFFFull) return ZC_EINVAL;
     }
+    for (auto &d : table)
+        if (resolve_blob(d) != ZC_OK) return ZC_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DecodeArgs a{};
     if (n == 1) a.one = table[0];
