@@ -19,8 +19,18 @@
  * Conventions for every entry point:
  *   - "d_" pointers are device pointers on the current CUDA device; "h_"
  *     pointers are host pointers. The caller owns every buffer, the stream and
- *     the context. No entry point allocates memory, creates streams, or
+ *     the context. No entry point allocates device memory, creates streams, or
  *     synchronises.
+ *   - Host-blob mode (cuZipNN Usage: GPU tensor to CPU blob and back). The
+ *     data buffers of the compression and decompression calls (sources,
+ *     bases, blobs, outputs and d_blob_bytes) may also be page-locked host
+ *     memory (cudaHostAlloc, cudaHostRegister) or managed memory: the kernels
+ *     then read and write host memory directly over the host link, as they
+ *     code, with no separate copy. Pointers are checked with
+ *     cudaPointerGetAttributes after the other argument checks; unregistered
+ *     (pageable) host memory and another device's memory are refused with
+ *     ZC_EINVAL before any launch. Workspaces and d_status must be device
+ *     memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *   - The return value reports argument errors found on the host before any
  *     launch, and launch errors (ZC_ECUDA). Errors only the device can see
