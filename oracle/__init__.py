@@ -80,6 +80,21 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint64)]
             L.zco_decompress.restype = ctypes.c_int
             L.zco_decompress.argtypes = [c_u8p, ctypes.c_uint64, c_u8p, ctypes.c_uint64, ctypes.c_uint32]
+            L.zco_normalize64.restype = ctypes.c_int
+            L.zco_normalize64.argtypes = [c_u8p, ctypes.c_uint64, c_u8p]
+            L.zco_plane_tables.restype = ctypes.c_int
+            L.zco_plane_tables.argtypes = [c_u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint32, c_u8p]
+            L.zco_rans_record_shared.restype = ctypes.c_uint64
+            L.zco_rans_record_shared.argtypes = [c_u8p, ctypes.c_uint32, c_u8p, c_u8p, ctypes.c_uint64]
+            L.zco_rans_decode_shared.restype = ctypes.c_int
+            L.zco_rans_decode_shared.argtypes = [c_u8p, ctypes.c_uint64, ctypes.c_uint32, c_u8p, c_u8p]
+            L.zco_blob_size_v.restype = ctypes.c_uint64
+            L.zco_blob_size_v.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_uint32, ctypes.c_double,
+                                          ctypes.c_int]
+            L.zco_compress_v.restype = ctypes.c_int
+            L.zco_compress_v.argtypes = [c_u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, c_u8p,
+                                         ctypes.c_uint32, ctypes.c_double, ctypes.c_int, c_u8p, ctypes.c_uint64,
+                                         ctypes.POINTER(ctypes.c_uint64)]
             _lib = L
     return _lib
 
@@ -164,27 +179,73 @@ def encode_chunk(chunk, dtype: int, threshold: float = 0.95) -> tuple[bytes, boo
     return out[:r].tobytes(), bool(raw.value)
 
 
-def blob_size(nbytes: int, dtype: int, chunk_bytes: int = 131072, threshold: float = 0.95) -> int:
-    return int(lib().zco_blob_size(nbytes, dtype, chunk_bytes, threshold))
+def blob_size(nbytes: int, dtype: int, chunk_bytes: int = 131072, threshold: float = 0.95,
+              version: int = 1) -> int:
+    return int(lib().zco_blob_size_v(nbytes, dtype, chunk_bytes, threshold, version))
 
 
-def compress(data, dtype: int, shape=None, chunk_bytes: int = 131072, threshold: float = 0.95) -> bytes:
+def compress(data, dtype: int, shape=None, chunk_bytes: int = 131072, threshold: float = 0.95,
+             version: int = 1) -> bytes:
+    """Blob of a tensor in format v1 (a table per coded stream) or v2 (shared
+    plane tables)."""
     d = _u8(data)
     W = WORD_BYTES[dtype]
     if shape is None:
         shape = (d.size // W,)
     shp = np.zeros(8, np.int64)
     shp[: len(shape)] = shape
-    cap = blob_size(d.size, dtype, chunk_bytes, threshold)
+    cap = blob_size(d.size, dtype, chunk_bytes, threshold, version)
     if cap == 0:
         raise OracleError(EINVAL, "blob_size")
     blob = np.zeros(cap, np.uint8)
     nb = ctypes.c_uint64(0)
-    st = lib().zco_compress(_ptr(d), d.size, dtype, len(shape), _ptr(shp), chunk_bytes, threshold,
-                            _ptr(blob), cap, ctypes.byref(nb))
+    st = lib().zco_compress_v(_ptr(d), d.size, dtype, len(shape), _ptr(shp), chunk_bytes, threshold, version,
+                              _ptr(blob), cap, ctypes.byref(nb))
     if st:
         raise OracleError(st, "compress")
     return blob[: nb.value].tobytes()
+
+
+def normalize64(counts, n: int) -> np.ndarray:
+    c = np.ascontiguousarray(counts, dtype=np.uint64)
+    assert c.size == 256
+    f = np.zeros(256, np.uint32)
+    st = lib().zco_normalize64(_ptr(c), n, _ptr(f))
+    if st:
+        raise OracleError(st, "normalize64")
+    return f
+
+
+def plane_tables(data, dtype: int, chunk_bytes: int = 131072) -> np.ndarray:
+    """Format v2's W plane tables of a tensor, shape (W, 256)."""
+    d = _u8(data)
+    W = WORD_BYTES[dtype]
+    out = np.zeros(W * 256, np.uint32)
+    st = lib().zco_plane_tables(_ptr(d), d.size, dtype, chunk_bytes, _ptr(out))
+    if st:
+        raise OracleError(st, "plane_tables")
+    return out.reshape(W, 256)
+
+
+def rans_record_shared(symbols, f) -> bytes:
+    s = _u8(symbols)
+    t = np.ascontiguousarray(f, dtype=np.uint32)
+    cap = 128 + 2 * s.size + 16
+    rec = np.zeros(cap, np.uint8)
+    r = lib().zco_rans_record_shared(_ptr(s), s.size, _ptr(t), _ptr(rec), cap)
+    if r == 0:
+        raise OracleError(EINVAL, "rans_record_shared")
+    return rec[:r].tobytes()
+
+
+def rans_decode_shared(record: bytes, n: int, f) -> np.ndarray:
+    r = np.frombuffer(record, np.uint8).copy()
+    t = np.ascontiguousarray(f, dtype=np.uint32)
+    out = np.zeros(max(n, 1), np.uint8)
+    st = lib().zco_rans_decode_shared(_ptr(r), r.size, n, _ptr(t), _ptr(out))
+    if st:
+        raise OracleError(st, "rans_decode_shared")
+    return out[:n]
 
 
 def blob_info(blob: bytes) -> dict:
@@ -198,7 +259,8 @@ def blob_info(blob: bytes) -> dict:
     if st:
         raise OracleError(st, "blob_info")
     return dict(dtype=dt.value, ndim=nd.value, shape=tuple(int(x) for x in shp[: nd.value]),
-                nbytes=nbytes.value, n_chunks=nc.value, chunk_bytes=cb.value, blob_bytes=nbb.value)
+                nbytes=nbytes.value, n_chunks=nc.value, chunk_bytes=cb.value, blob_bytes=nbb.value,
+                version=int(b[4]) | int(b[5]) << 8)
 
 
 def decompress_status(blob: bytes, flags: int = 0) -> tuple[int, np.ndarray]:

@@ -39,6 +39,16 @@
  *   present symbols in ascending order; zero pad to 16; then the 16-bit
  *   renormalisation words in the order the encoder emitted them (a decoder
  *   consumes them from the last one backwards).
+ *
+ * Blob format v2 (shared tables; lmz "Building on lmz": one table per plane
+ * kind for many chunks) differs from v1 in three places only:
+ *   - version = 2;
+ *   - after the chunk table come W plane tables of 256 x u16 (512 bytes
+ *     each): plane j's 12-bit table, or all zeros when stream j has fewer
+ *     than two distinct symbols over the whole tensor; the header CRC covers
+ *     bytes [0, 96 + 16*n_chunks + 512*W) and offset_0 = 96 + 16n + 512W;
+ *   - a RANS record is the 32 final states followed by the words (no bitmap,
+ *     no frequencies): the stream is coded with its plane's table.
  */
 #include "zco.h"
 
@@ -398,6 +408,217 @@ done:
     return result;
 }
 
+/* ------------------------------------------ format v2: shared plane tables */
+
+/* lmz "Building on lmz": a table per plane kind shared by many chunks (the
+ * chunk records then carry none). Reading: plane j's table is the 12-bit
+ * table of the histogram of stream j over every element of the tensor,
+ * quantised by the same rule as zco_normalize (written out again here for
+ * 64-bit counts, since a tensor may hold more than 2^32 elements). */
+int zco_normalize64(const uint64_t counts[256], uint64_t n, uint32_t f[256]) {
+    uint64_t total = 0;
+    int present = 0;
+    for (int s = 0; s < 256; s++) {
+        total += counts[s];
+        if (counts[s]) present++;
+    }
+    if (total != n || present < 2 || n > (1ull << 50)) return ZCO_EINVAL;
+
+    int64_t sum = 0;
+    for (int s = 0; s < 256; s++) {
+        if (counts[s] == 0) {
+            f[s] = 0;
+        } else {
+            uint64_t q = counts[s] * ZCO_M / n;
+            f[s] = q < 1 ? 1u : (uint32_t)q;
+        }
+        sum += f[s];
+    }
+    if (sum < (int64_t)ZCO_M) {
+        int best = 0;
+        for (int s = 1; s < 256; s++)
+            if (counts[s] > counts[best]) best = s;
+        f[best] += (uint32_t)((int64_t)ZCO_M - sum);
+        sum = ZCO_M;
+    }
+    while (sum > (int64_t)ZCO_M) {
+        int best = -1;
+        for (int s = 0; s < 256; s++)
+            if (f[s] > 1 && (best < 0 || f[s] > f[best])) best = s;
+        f[best] -= 1;
+        sum -= 1;
+    }
+    return ZCO_OK;
+}
+
+/* The W plane tables of a tensor (planes[j*256 + s]), from the streams of
+ * every chunk; all zeros for a plane with fewer than two distinct symbols. */
+int zco_plane_tables(const uint8_t *src, uint64_t nbytes, int dtype, uint32_t chunk_bytes, uint32_t *planes) {
+    int W = zco_word_bytes(dtype);
+    if (W == 0 || chunk_bytes == 0 || nbytes % (uint64_t)W) return ZCO_EINVAL;
+    uint64_t *counts = (uint64_t *)calloc(256u * (size_t)W, sizeof(uint64_t));
+    uint8_t *streams = (uint8_t *)malloc(chunk_bytes);
+    if (!counts || !streams) {
+        free(counts);
+        free(streams);
+        return ZCO_EINVAL;
+    }
+    for (uint64_t off = 0; off < nbytes; off += chunk_bytes) {
+        uint32_t len = (uint32_t)(nbytes - off < chunk_bytes ? nbytes - off : chunk_bytes);
+        uint32_t n = len / (uint32_t)W;
+        zco_group_split(src + off, n, dtype, streams);
+        for (int j = 0; j < W; j++)
+            for (uint32_t i = 0; i < n; i++) counts[256u * j + streams[(uint64_t)j * n + i]]++;
+    }
+    int st = ZCO_OK;
+    for (int j = 0; j < W; j++) {
+        uint32_t *f = planes + 256u * j;
+        if (zco_normalize64(counts + 256u * j, nbytes / (uint64_t)W, f) != ZCO_OK)
+            memset(f, 0, 256 * sizeof(uint32_t));  /* fewer than two symbols (or an empty tensor) */
+    }
+    free(counts);
+    free(streams);
+    return st;
+}
+
+/* v2 record: the same rANS steps as zco_rans_record with the plane's table
+ * f; the record is the 32 final states and the words. Returns the record's
+ * byte count, or 0 if rec_cap is too small or a symbol has no frequency. */
+uint64_t zco_rans_record_shared(const uint8_t *sym, uint32_t n, const uint32_t f[256], uint8_t *rec,
+                                uint64_t rec_cap) {
+    uint32_t cum[257];
+    cum[0] = 0;
+    for (int s = 0; s < 256; s++) cum[s + 1] = cum[s] + f[s];
+    if (cum[256] != ZCO_M) return 0;
+    const uint64_t words_at = 4u * ZCO_LANES;
+    if (rec_cap < words_at) return 0;
+
+    uint32_t x[ZCO_LANES];
+    for (uint32_t l = 0; l < ZCO_LANES; l++) x[l] = ZCO_L;
+    uint64_t nwords = 0;
+    uint32_t T = (n + ZCO_LANES - 1) / ZCO_LANES;
+    for (uint32_t t = T; t-- > 0;) {
+        for (uint32_t l = ZCO_LANES; l-- > 0;) {
+            uint64_t i = (uint64_t)t * ZCO_LANES + l;
+            if (i >= n) continue;
+            uint32_t s = sym[i];
+            if (f[s] == 0) return 0;
+            if (x[l] >= (f[s] << 20)) {
+                if (words_at + 2 * (nwords + 1) > rec_cap) return 0;
+                put16(rec + words_at + 2 * nwords, x[l] & 0xFFFFu);
+                nwords++;
+                x[l] >>= 16;
+            }
+            x[l] = ((x[l] / f[s]) << ZCO_PROB_BITS) + (x[l] % f[s]) + cum[s];
+        }
+    }
+    for (uint32_t l = 0; l < ZCO_LANES; l++) put32(rec + 4 * l, x[l]);
+    return words_at + 2 * nwords;
+}
+
+/* Inverse of zco_rans_record_shared (the steps of zco_rans_decode). */
+int zco_rans_decode_shared(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, const uint32_t f[256],
+                           uint8_t *sym) {
+    const uint64_t words_at = 4u * ZCO_LANES;
+    uint32_t cum[257];
+    cum[0] = 0;
+    for (int s = 0; s < 256; s++) cum[s + 1] = cum[s] + f[s];
+    if (cum[256] != ZCO_M) return ZCO_ECORRUPT;
+    if (rec_bytes < words_at || ((rec_bytes - words_at) & 1u)) return ZCO_ECORRUPT;
+    uint32_t x[ZCO_LANES];
+    for (uint32_t l = 0; l < ZCO_LANES; l++) {
+        x[l] = get32(rec + 4 * l);
+        if (x[l] < ZCO_L) return ZCO_ECORRUPT;
+    }
+    const uint8_t *words = rec + words_at;
+    uint64_t ptr = (rec_bytes - words_at) / 2;
+    uint32_t T = (n + ZCO_LANES - 1) / ZCO_LANES;
+    for (uint32_t t = 0; t < T; t++) {
+        for (uint32_t l = 0; l < ZCO_LANES; l++) {
+            uint64_t i = (uint64_t)t * ZCO_LANES + l;
+            if (i >= n) continue;
+            uint32_t slot = x[l] & (ZCO_M - 1);
+            uint32_t s = 0;
+            while (!(cum[s] <= slot && slot < cum[s + 1])) s++;
+            x[l] = f[s] * (x[l] >> ZCO_PROB_BITS) + slot - cum[s];
+            if (x[l] < ZCO_L) {
+                if (ptr == 0) return ZCO_ECORRUPT;
+                ptr--;
+                x[l] = (x[l] << 16) | get16(words + 2 * ptr);
+            }
+            sym[i] = (uint8_t)s;
+        }
+    }
+    for (uint32_t l = 0; l < ZCO_LANES; l++)
+        if (x[l] != ZCO_L) return ZCO_ECORRUPT;
+    if (ptr != 0) return ZCO_ECORRUPT;
+    return ZCO_OK;
+}
+
+/* One chunk in format v2: the per-stream and per-chunk rules of
+ * zco_encode_chunk, with coded streams using their plane's table. */
+uint64_t zco_encode_chunk_shared(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                                 const uint32_t *planes, uint8_t *out, uint64_t cap, int *mode_raw) {
+    int W = zco_word_bytes(dtype);
+    uint32_t n = len / (uint32_t)W;
+    uint8_t *streams = (uint8_t *)malloc(len ? len : 1);
+    uint64_t rec_cap = 4u * ZCO_LANES + 2u * (uint64_t)n;
+    uint8_t *rec = (uint8_t *)malloc((size_t)rec_cap);
+    uint8_t *grouped = (uint8_t *)malloc((size_t)(16 + (uint64_t)W * pad16(rec_cap)));
+    uint64_t result = 0;
+    if (!streams || !rec || !grouped) goto done;
+
+    zco_group_split(src, n, dtype, streams);
+
+    uint64_t g = pad16(4u * (uint64_t)W);
+    memset(grouped, 0, (size_t)g);
+    for (int j = 0; j < W; j++) {
+        const uint8_t *sj = streams + (uint64_t)j * n;
+        uint32_t counts[256] = {0};
+        for (uint32_t i = 0; i < n; i++) counts[sj[i]]++;
+        int present = 0, only = 0;
+        for (int s = 0; s < 256; s++)
+            if (counts[s]) { present++; only = s; }
+
+        uint32_t entry;
+        if (present == 1) {
+            entry = ((uint32_t)ZCO_MODE_CONST << 30) | (uint32_t)only;
+        } else {
+            uint64_t r = zco_rans_record_shared(sj, n, planes + 256u * j, rec, rec_cap);
+            if (r == 0) goto done;
+            if ((double)r < threshold * (double)n) {
+                entry = ((uint32_t)ZCO_MODE_RANS << 30) | (uint32_t)r;
+                memcpy(grouped + g, rec, (size_t)r);
+                memset(grouped + g + r, 0, (size_t)(pad16(r) - r));
+                g += pad16(r);
+            } else {
+                entry = ((uint32_t)ZCO_MODE_RAW << 30) | n;
+                memcpy(grouped + g, sj, n);
+                memset(grouped + g + n, 0, (size_t)(pad16(n) - n));
+                g += pad16(n);
+            }
+        }
+        put32(grouped + 4 * j, entry);
+    }
+
+    if ((double)g < threshold * (double)len) {
+        if (g > cap) goto done;
+        memcpy(out, grouped, (size_t)g);
+        *mode_raw = 0;
+        result = g;
+    } else {
+        if (len > cap) goto done;
+        memcpy(out, src, len);
+        *mode_raw = 1;
+        result = len;
+    }
+done:
+    free(streams);
+    free(rec);
+    free(grouped);
+    return result;
+}
+
 /* --------------------------------------------------------------- blobs */
 
 static int valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
@@ -428,6 +649,77 @@ uint64_t zco_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double 
         total += worst;
     }
     return total;
+}
+
+/* Worst case of either format: v2 adds the W plane tables. */
+uint64_t zco_blob_size_v(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, int version) {
+    uint64_t b = zco_blob_size(nbytes, dtype, chunk_bytes, threshold);
+    if (b == 0 || (version != 1 && version != 2)) return 0;
+    return version == 2 ? b + 512u * (uint64_t)zco_word_bytes(dtype) : b;
+}
+
+/* Format v2 compression (see the top of this file). */
+static int compress_shared(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
+                           uint32_t chunk_bytes, double threshold, uint8_t *blob, uint64_t cap,
+                           uint64_t *blob_bytes) {
+    int W = zco_word_bytes(dtype);
+    uint64_t nc = (nbytes + chunk_bytes - 1) / chunk_bytes;
+    uint64_t table_end = ZCO_HEADER + ZCO_ENTRY * nc;
+    uint64_t planes_end = table_end + 512u * (uint64_t)W;
+    if (cap < planes_end) return ZCO_ECAPACITY;
+    uint32_t planes[4 * 256];
+    if (zco_plane_tables(src, nbytes, dtype, chunk_bytes, planes) != ZCO_OK) return ZCO_EINVAL;
+    memset(blob, 0, (size_t)planes_end);
+
+    memcpy(blob, "ZCNN", 4);
+    put16(blob + 4, 2);
+    blob[6] = (uint8_t)dtype;
+    blob[7] = (uint8_t)ndim;
+    put32(blob + 8, chunk_bytes);
+    blob[12] = (uint8_t)ZCO_LANES;
+    blob[13] = (uint8_t)ZCO_PROB_BITS;
+    put64(blob + 16, nbytes);
+    put32(blob + 24, (uint32_t)nc);
+    for (int d = 0; d < ndim; d++) put64(blob + 32 + 8 * d, (uint64_t)shape[d]);
+    for (int j = 0; j < W; j++)
+        for (int v = 0; v < 256; v++) put16(blob + table_end + 512u * j + 2u * v, planes[256 * j + v]);
+
+    uint64_t off = planes_end;
+    for (uint64_t c = 0; c < nc; c++) {
+        uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - c * chunk_bytes);
+        int raw = 0;
+        uint64_t room = cap > off ? cap - off : 0;
+        uint64_t stored = zco_encode_chunk_shared(src + c * (uint64_t)chunk_bytes, len, dtype, threshold, planes,
+                                                  blob + off, room, &raw);
+        if (stored == 0 || pad16(stored) > room) return ZCO_ECAPACITY;
+        memset(blob + off + stored, 0, (size_t)(pad16(stored) - stored));
+        uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * c;
+        put64(e, off);
+        put32(e + 8, (uint32_t)stored | ((uint32_t)raw << 31));
+        put32(e + 12, zco_crc32(src + c * (uint64_t)chunk_bytes, len));
+        off += pad16(stored);
+    }
+    put32(blob + 28, zco_crc32(blob, planes_end));
+    *blob_bytes = off;
+    return ZCO_OK;
+}
+
+int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
+                   uint32_t chunk_bytes, double threshold, int version,
+                   uint8_t *blob, uint64_t cap, uint64_t *blob_bytes) {
+    if (version == 1) return zco_compress(src, nbytes, dtype, ndim, shape, chunk_bytes, threshold, blob, cap,
+                                          blob_bytes);
+    if (version != 2) return ZCO_EINVAL;
+    if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZCO_EINVAL;
+    if (ndim < 0 || ndim > 8) return ZCO_EINVAL;
+    int W = zco_word_bytes(dtype);
+    uint64_t elems = 1;
+    for (int d = 0; d < ndim; d++) {
+        if (shape[d] < 0) return ZCO_EINVAL;
+        elems *= (uint64_t)shape[d];
+    }
+    if (elems * (uint64_t)W != nbytes) return ZCO_EINVAL;
+    return compress_shared(src, nbytes, dtype, ndim, shape, chunk_bytes, threshold, blob, cap, blob_bytes);
 }
 
 int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
@@ -490,7 +782,8 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
                   int64_t shape_out[8], uint64_t *nbytes_out, uint32_t *n_chunks_out,
                   uint32_t *chunk_bytes_out, uint64_t *blob_bytes_out) {
     if (avail < ZCO_HEADER) return ZCO_EFORMAT;
-    if (memcmp(blob, "ZCNN", 4) != 0 || get16(blob + 4) != 1) return ZCO_EFORMAT;
+    int version = (int)get16(blob + 4);
+    if (memcmp(blob, "ZCNN", 4) != 0 || (version != 1 && version != 2)) return ZCO_EFORMAT;
     int dtype = blob[6], ndim = blob[7];
     uint32_t chunk_bytes = get32(blob + 8);
     uint64_t nbytes = get64(blob + 16);
@@ -513,7 +806,21 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
     }
     if (elems * (uint64_t)W != nbytes) return ZCO_EFORMAT;
     uint64_t table_end = ZCO_HEADER + ZCO_ENTRY * (uint64_t)nc;
+    if (version == 2) table_end += 512u * (uint64_t)W; /* the plane tables */
     if (avail < table_end) return ZCO_EFORMAT;
+    if (version == 2) {
+        /* each plane table is all zeros or a 12-bit table of at least two symbols */
+        for (int j = 0; j < W; j++) {
+            const uint8_t *t = blob + table_end - 512u * (uint64_t)(W - j);
+            uint32_t sum = 0, nz = 0;
+            for (int v = 0; v < 256; v++) {
+                uint32_t f = get16(t + 2 * v);
+                sum += f;
+                nz += f ? 1u : 0u;
+            }
+            if (!(sum == 0 || (sum == ZCO_M && nz >= 2))) return ZCO_EFORMAT;
+        }
+    }
 
     /* header CRC with its own field read as zero */
     uint8_t *copy = (uint8_t *)malloc((size_t)table_end);
@@ -548,8 +855,10 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
     return ZCO_OK;
 }
 
-/* Inverse of one grouped chunk payload. */
-static int decode_grouped(const uint8_t *p, uint32_t stored, uint32_t len, int dtype, uint8_t *dst) {
+/* Inverse of one grouped chunk payload; planes is NULL for v1, else the
+ * v2 plane tables (a RANS stream then uses its plane's table). */
+static int decode_grouped(const uint8_t *p, uint32_t stored, uint32_t len, int dtype, const uint32_t *planes,
+                          uint8_t *dst) {
     int W = zco_word_bytes(dtype);
     uint32_t n = len / (uint32_t)W;
     uint64_t g = pad16(4u * (uint64_t)W);
@@ -573,6 +882,7 @@ static int decode_grouped(const uint8_t *p, uint32_t stored, uint32_t len, int d
                 if (p[b]) st = ZCO_ECORRUPT;
             if (st != ZCO_OK) break;
             if (mode == ZCO_MODE_RAW) memcpy(sj, p + g, n);
+            else if (planes) st = zco_rans_decode_shared(p + g, v, n, planes + 256u * j, sj);
             else st = zco_rans_decode(p + g, v, n, sj);
             g += pad16(v);
         } else {
@@ -593,6 +903,14 @@ int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_
     if (st != ZCO_OK) return st;
     if (total > blob_len) return ZCO_EFORMAT;
     if (cap < nbytes) return ZCO_ECAPACITY;
+    uint32_t planes[4 * 256];
+    const int shared = get16(blob + 4) == 2;
+    if (shared) {
+        int W = zco_word_bytes(dtype);
+        const uint8_t *t = blob + ZCO_HEADER + ZCO_ENTRY * (uint64_t)nc;
+        for (int j = 0; j < W; j++)
+            for (int v = 0; v < 256; v++) planes[256 * j + v] = get16(t + 512u * j + 2u * v);
+    }
     int status = ZCO_OK;
     for (uint32_t c = 0; c < nc; c++) {
         const uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * (uint64_t)c;
@@ -603,7 +921,7 @@ int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_
         uint8_t *out = dst + (uint64_t)c * chunk_bytes;
         int cst = ZCO_OK;
         if (sm >> 31) memcpy(out, blob + off, len);
-        else cst = decode_grouped(blob + off, stored, len, dtype, out);
+        else cst = decode_grouped(blob + off, stored, len, dtype, shared ? planes : NULL, out);
         status |= cst;
         /* the chunk CRC covers the original bytes: check what was decoded */
         if (cst == ZCO_OK && !(flags & ZCO_NO_VERIFY) && zco_crc32(out, len) != get32(e + 12))

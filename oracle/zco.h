@@ -83,11 +83,32 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
                  uint32_t chunk_bytes, double threshold,
                  uint8_t *blob, uint64_t cap, uint64_t *blob_bytes);
 
-/* Parse and check a blob header and chunk table. Fills the optional out
- * fields. Returns status. */
+/* Parse and check a blob header and chunk table (format v1 or v2; for v2
+ * also the plane tables). Fills the optional out fields. Returns status. */
 int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype, int *ndim, int64_t shape[8],
                   uint64_t *nbytes, uint32_t *n_chunks, uint32_t *chunk_bytes, uint64_t *blob_bytes);
 
+/* Format v2 (shared plane tables). 12-bit table from 64-bit counts, by the
+ * zco_normalize rule. */
+int zco_normalize64(const uint64_t counts[256], uint64_t n, uint32_t f[256]);
+/* The W plane tables of a tensor (planes[256 j + s]); zeros for a plane
+ * with fewer than two distinct symbols. */
+int zco_plane_tables(const uint8_t *src, uint64_t nbytes, int dtype, uint32_t chunk_bytes, uint32_t *planes);
+/* v2 record (32 states + words) of n symbols with table f; 0 on error. */
+uint64_t zco_rans_record_shared(const uint8_t *sym, uint32_t n, const uint32_t f[256], uint8_t *rec,
+                                uint64_t rec_cap);
+/* Inverse of zco_rans_record_shared. Returns status. */
+int zco_rans_decode_shared(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, const uint32_t f[256],
+                           uint8_t *sym);
+/* One chunk in format v2 (coded streams use the plane tables). */
+uint64_t zco_encode_chunk_shared(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                                 const uint32_t *planes, uint8_t *out, uint64_t cap, int *mode_raw);
+/* Worst-case blob size of format version 1 or 2. */
+uint64_t zco_blob_size_v(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, int version);
+/* Compress a tensor in format version 1 or 2. */
+int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
+                   uint32_t chunk_bytes, double threshold, int version,
+                   uint8_t *blob, uint64_t cap, uint64_t *blob_bytes);
 /* Decompress a blob into dst (capacity cap). Returns status. */
 int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_t cap, uint32_t flags);
 

@@ -2,7 +2,9 @@
 
 Written from the format description (header, chunk table, grouped-chunk
 directory, rANS record), not from the oracle's code, and sharing nothing with
-either implementation. It decodes small blobs (tens of KiB) only. A blob that
+either implementation. It decodes small blobs (tens of KiB) only, in
+format v1 (a table in every record) or v2 (one table per plane after the
+chunk table, records of states and words). A blob that
 this reader and the oracle both turn back into the input is a valid encoding
 of the documented format, which pins the oracle's layout choices from the
 outside.
@@ -35,13 +37,20 @@ def _unpermute(p: int, dtype: int) -> int:
     return (s << (B - 1)) | (e << (B - 1 - E)) | m
 
 
-def _rans(rec: bytes, n: int) -> list[int]:
+def _rans(rec: bytes, n: int, plane=None) -> list[int]:
+    """Decode a record: v1 carries its table (bitmap + frequencies); a v2
+    record is states + words and uses its plane's table (256 frequencies)."""
     states = list(struct.unpack_from("<32I", rec, 0))
-    bitmap = rec[128:160]
-    present = [s for s in range(256) if bitmap[s // 8] >> (s % 8) & 1]
-    k = len(present)
-    freqs = struct.unpack_from(f"<{k}H", rec, 160)
-    words_at = 160 + (2 * k + 15) // 16 * 16
+    if plane is None:
+        bitmap = rec[128:160]
+        present = [s for s in range(256) if bitmap[s // 8] >> (s % 8) & 1]
+        k = len(present)
+        freqs = struct.unpack_from(f"<{k}H", rec, 160)
+        words_at = 160 + (2 * k + 15) // 16 * 16
+    else:
+        present = [s for s in range(256) if plane[s]]
+        freqs = [plane[s] for s in present]
+        words_at = 128
     words = struct.unpack_from(f"<{(len(rec) - words_at) // 2}H", rec, words_at)
     # slot -> symbol map, built by laying the symbols' slot ranges end to end
     slot_sym, start = [], {}
@@ -72,13 +81,19 @@ def _rans(rec: bytes, n: int) -> list[int]:
 
 
 def decode(blob: bytes) -> bytes:
-    if blob[:4] != b"ZCNN" or struct.unpack_from("<H", blob, 4)[0] != 1:
+    version, = struct.unpack_from("<H", blob, 4)
+    if blob[:4] != b"ZCNN" or version not in (1, 2):
         raise SpecError("magic/version")
     dtype, ndim = blob[6], blob[7]
     chunk_bytes, = struct.unpack_from("<I", blob, 8)
     nbytes, = struct.unpack_from("<Q", blob, 16)
     n_chunks, hcrc = struct.unpack_from("<II", blob, 24)
     table_end = 96 + 16 * n_chunks
+    planes = None
+    if version == 2:  # W plane tables of 256 u16 follow the chunk table
+        W = WORD[dtype]
+        planes = [struct.unpack_from("<256H", blob, table_end + 512 * j) for j in range(W)]
+        table_end += 512 * W
     head = bytearray(blob[:table_end])
     head[28:32] = b"\0\0\0\0"
     if zlib.crc32(bytes(head)) != hcrc:
@@ -93,13 +108,13 @@ def decode(blob: bytes) -> bytes:
         if raw:
             out += payload
         else:
-            out += _grouped(payload, length, dtype)
+            out += _grouped(payload, length, dtype, planes)
         if zlib.crc32(bytes(out[start:])) != crc:   # CRC of the original bytes
             raise SpecError(f"chunk {c} crc")
     return bytes(out)
 
 
-def _grouped(payload: bytes, length: int, dtype: int) -> bytes:
+def _grouped(payload: bytes, length: int, dtype: int, planes=None) -> bytes:
     W = WORD[dtype]
     n = length // W
     pos = (4 * W + 15) // 16 * 16
@@ -111,7 +126,7 @@ def _grouped(payload: bytes, length: int, dtype: int) -> bytes:
             streams.append([v] * n)
             continue
         rec = payload[pos:pos + v]
-        streams.append(list(rec) if mode == 0 else _rans(rec, n))
+        streams.append(list(rec) if mode == 0 else _rans(rec, n, None if planes is None else planes[j]))
         pos += (v + 15) // 16 * 16
     out = bytearray()
     for i in range(n):

@@ -424,3 +424,158 @@ def test_param_validation(zco):
     assert zco.blob_size(64, 1, 64, 0.0) == 0
     assert zco.blob_size(64, 9, 64, 0.95) == 0
     assert zco.blob_size(0, 1, 64, 0.95) == 96
+
+
+# ------------------------------------------------- format v2 (shared tables)
+# lmz "Building on lmz": one table per plane kind shared by many chunks. The
+# v2 pins tie it to the pinned v1 coder (a one-chunk tensor's plane table is
+# the table v1 stores in that chunk's record, and the v2 record is the v1
+# record without its table), to the independent reader, to the entropy, and
+# to the rule's invariants with 64-bit counts.
+
+def _v1_records(blob, W):
+    """{stream j: record bytes} of the single grouped chunk of a v1 blob."""
+    off, sm, _ = struct.unpack_from("<QII", blob, 96)
+    assert not sm >> 31
+    pos, recs = 16, {}
+    for j in range(W):
+        entry, = struct.unpack_from("<I", blob, off + 4 * j)
+        mode, v = entry >> 30, entry & 0x3FFFFFFF
+        if mode == 1:
+            recs[j] = blob[off + pos: off + pos + v]
+        if mode != 2:
+            pos += (v + 15) // 16 * 16
+    return recs
+
+
+def test_v2_single_chunk_equals_v1_records(zco):
+    rng = np.random.default_rng(31)
+    cases = [(workloads.as_bytes(workloads.bf16_1m()[:32]).numpy(), 4),
+             (workloads.as_bytes(workloads.fp32_64m(rows=1)[:, :4000]).numpy(), 6),
+             (rng.integers(0, 9, 20000, dtype=np.uint8), 1),
+             ((rng.integers(0, 4, 6000, dtype=np.uint16) * 257).view(np.uint8), 2)]
+    for raw, dt in cases:
+        W = {1: 1, 2: 2, 4: 2, 6: 4}[dt]
+        b1 = zco.compress(raw, dt, None, 131072, 2.0)   # threshold 2: every non-constant stream coded
+        b2 = zco.compress(raw, dt, None, 131072, 2.0, version=2)
+        planes = zco.plane_tables(raw, dt)
+        nc, = struct.unpack_from("<I", b2, 24)
+        stored = np.frombuffer(b2[96 + 16 * nc: 96 + 16 * nc + 512 * W], "<u2").reshape(W, 256)
+        assert (stored == planes).all()
+        recs1 = _v1_records(b1, W)
+        off2, _, _ = struct.unpack_from("<QII", b2, 96)
+        pos = 16
+        for j in range(W):
+            entry, = struct.unpack_from("<I", b2, off2 + 4 * j)
+            mode, v = entry >> 30, entry & 0x3FFFFFFF
+            if j in recs1:
+                r1 = recs1[j]
+                bitmap = r1[128:160]
+                present = [s for s in range(256) if bitmap[s // 8] >> (s % 8) & 1]
+                k = len(present)
+                f1 = dict(zip(present, struct.unpack_from(f"<{k}H", r1, 160)))
+                assert {s: int(planes[j][s]) for s in range(256) if planes[j][s]} == f1
+                words1 = r1[160 + (2 * k + 15) // 16 * 16:]
+                assert mode == 1 and b2[off2 + pos: off2 + pos + v] == r1[:128] + words1
+            if mode != 2:
+                pos += (v + 15) // 16 * 16
+        assert zco.decompress(b2).tobytes() == raw.tobytes()
+        assert spec_decoder.decode(b2) == raw.tobytes()
+
+
+def test_v2_roundtrip_random_tensors(zco):
+    rng = np.random.default_rng(4096)
+    for trial in range(160):
+        dtype = int(rng.integers(1, 7))
+        n = int(rng.choice([0, 1, 31, 33, 4097, int(rng.integers(0, 6001))]))
+        data = _rand_tensor(rng, dtype, n)
+        chunk = int(rng.choice([64, 1024, 4096, 131072]))
+        thr = float(rng.choice([0.5, 0.95, 1.0, 2.0]))
+        blob = zco.compress(data, dtype, (n,), chunk, thr, version=2)
+        assert len(blob) <= zco.blob_size(data.size, dtype, chunk, thr, version=2)
+        info = zco.blob_info(blob)
+        assert info["version"] == 2 and info["dtype"] == dtype
+        assert zco.decompress(blob).tobytes() == data.tobytes(), (trial, dtype, n, chunk, thr)
+        if data.size <= 20000:
+            assert spec_decoder.decode(blob) == data.tobytes()
+
+
+def test_v2_exhaustive_bf16_patterns(zco):
+    """All 65,536 BF16 patterns shuffled over 4 KiB chunks, every stream coded
+    (threshold 2) with the two plane tables of the whole tensor (each plane is
+    uniform over the tensor: f = 16 for all 256 symbols)."""
+    perm = np.random.default_rng(9).permutation(65536).astype(np.uint16).view(np.uint8)
+    planes = zco.plane_tables(perm, 4, 4096)
+    assert (planes == 16).all()
+    blob = zco.compress(perm, 4, (65536,), 4096, 2.0, version=2)
+    nc, = struct.unpack_from("<I", blob, 24)
+    assert nc == 32
+    assert zco.decompress(blob).tobytes() == perm.tobytes()
+    assert spec_decoder.decode(blob) == perm.tobytes()
+
+
+def test_v2_plane_tables_invariants(zco):
+    rng = np.random.default_rng(77)
+    t = workloads.fp32_64m(rows=64)
+    raw = workloads.as_bytes(t).numpy()
+    planes = zco.plane_tables(raw, 6, 131072)
+    streams = zco.group_split(raw, 6)
+    for j in range(4):
+        counts = np.bincount(streams[j], minlength=256)
+        f = planes[j]
+        assert f.sum() == 4096 and ((f > 0) == (counts > 0)).all()
+        nz = counts > 0
+        H = float(-(counts[nz] * np.log2(counts[nz] / counts.sum())).sum())
+        cost = float((counts[nz] * np.log2(4096.0 / f[nz])).sum())
+        assert H - 1e-6 <= cost <= 1.01 * H + 64
+    # a plane with one symbol over the tensor has an all-zero table
+    clean = workloads.as_bytes(workloads.fp32clean_64m(rows=4)).numpy()
+    p2 = zco.plane_tables(clean, 6, 131072)
+    assert (p2[2] == 0).all() and (p2[3] == 0).all() and p2[0].sum() == 4096
+    # the 64-bit rule reduces to the 32-bit one, and depends on ratios only
+    for _ in range(20):
+        counts = rng.integers(0, 5000, 256) * (rng.random(256) < 0.3)
+        counts[int(rng.integers(0, 256))] += 1
+        counts[int(rng.integers(0, 256))] += 1
+        n = int(counts.sum())
+        f32 = zco.normalize(counts.astype(np.uint32), n)
+        assert (zco.normalize64(counts.astype(np.uint64), n) == f32).all()
+        big = counts.astype(np.uint64) << np.uint64(20)
+        assert (zco.normalize64(big, n << 20) == f32).all()
+
+
+def test_v2_entropy_bound_and_size(zco):
+    """Coded exponent records are within the cross-entropy under the plane
+    table (H_x - 8 <= record <= 1.01 H_x + 8, in bytes), and the shared
+    tables cost little against per-chunk tables on a stationary tensor."""
+    for t, dt in [(workloads.bf16_1m(), 4), (workloads.fp32_64m(rows=256), 6)]:
+        raw = workloads.as_bytes(t).numpy()
+        planes = zco.plane_tables(raw, dt)
+        f = planes[0].astype(np.float64)
+        C = 131072
+        for c in range(0, raw.size, C):
+            e = zco.group_split(raw[c:c + C], dt)[0]
+            counts = np.bincount(e, minlength=256)
+            nz = counts > 0
+            Hx = float((counts[nz] * np.log2(4096.0 / f[nz])).sum()) / 8
+            rec = zco.rans_record_shared(e, planes[0])
+            assert Hx - 8 <= len(rec) <= 1.01 * Hx + 8, (dt, c)
+            assert (zco.rans_decode_shared(rec, e.size, planes[0]) == e).all()
+        b1 = zco.compress(raw, dt, None, C, 0.95)
+        b2 = zco.compress(raw, dt, None, C, 0.95, version=2)
+        assert len(b2) <= 1.003 * len(b1) + 2048
+
+
+def test_v2_rejections(zco):
+    raw = workloads.as_bytes(workloads.bf16_1m()[:64]).numpy()
+    blob = bytearray(zco.compress(raw, 4, None, 131072, 0.95, version=2))
+    nc, = struct.unpack_from("<I", blob, 24)
+    t0 = 96 + 16 * nc
+    bad = bytearray(blob)
+    bad[t0 + 2 * 120] ^= 1                      # a plane table no longer sums to 4096
+    st, _ = zco.decompress_status(bytes(bad))
+    assert st & (zco.EFORMAT | zco.ECRC)
+    bad = bytearray(blob)
+    bad[4] = 3                                   # unknown version
+    st, _ = zco.decompress_status(bytes(bad))
+    assert st & zco.EFORMAT
