@@ -418,7 +418,7 @@ def run_model(a, world, rank, local, dev, stream):
     if batched:
         table_launches = lambda words: (words + 7679) // 7680
         per_step = (encode_launches(sum(chunks), Wd, C) + table_launches(38 * n) + (1 if 0 in sizes else 0)
-                    + 1 + table_launches(12 * n))
+                    + 1 + table_launches(14 * n))
     else:
         per_step = sum(encode_launches(c, Wd, C) + (1 if c else 0) for c in chunks)
     line = {

@@ -23,11 +23,12 @@ from .workloads import BF16, FP16, FP32, U8, U16, U32
 __all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspace_size",
            "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
            "decompress_delta_into", "compress_batch", "compress_batch_into", "decompress_batch",
-           "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "OK", "EINVAL", "EFORMAT",
+           "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "SHARED_TABLES", "OK", "EINVAL", "EFORMAT",
            "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
 
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
 NO_VERIFY = 1
+SHARED_TABLES = 2  # compression flag: blob format v2 (shared plane tables)
 DEFAULT_CHUNK = 131072
 DEFAULT_THRESHOLD = 0.95
 
@@ -54,7 +55,8 @@ class ZcError(RuntimeError):
 class _Info(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * 8),
                 ("nbytes", ctypes.c_uint64), ("blob_bytes", ctypes.c_uint64),
-                ("n_chunks", ctypes.c_uint32), ("chunk_bytes", ctypes.c_uint32)]
+                ("n_chunks", ctypes.c_uint32), ("chunk_bytes", ctypes.c_uint32),
+                ("version", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 _lock = threading.Lock()
@@ -78,6 +80,13 @@ def lib() -> ctypes.CDLL:
             L.zc_compress.restype = i32
             L.zc_compress.argtypes = [vp, u64, i32, i32, ctypes.POINTER(ctypes.c_int64), u32, dbl,
                                       vp, u64, vp, vp, u64, vp, vp]
+            L.zc_compress_ex.restype = i32
+            L.zc_compress_ex.argtypes = [vp, u64, i32, i32, ctypes.POINTER(ctypes.c_int64), u32, dbl, u32,
+                                         vp, u64, vp, vp, u64, vp, vp]
+            L.zc_workspace_size_ex.restype = u64
+            L.zc_workspace_size_ex.argtypes = [u64, i32, u32, u32]
+            L.zc_blob_size_ex.restype = u64
+            L.zc_blob_size_ex.argtypes = [u64, i32, u32, dbl, u32]
             L.zc_decompress.restype = i32
             L.zc_decompress.argtypes = [vp, ctypes.POINTER(_Info), vp, u64, u32, vp, vp]
             L.zc_compress_delta.restype = i32
@@ -89,12 +98,12 @@ def lib() -> ctypes.CDLL:
             L.zc_crc32.argtypes = [vp, u64, u64, vp, vp]
             pu64, pi64, pi32 = ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
             L.zc_workspace_size_batch.restype = u64
-            L.zc_workspace_size_batch.argtypes = [pu64, u32, i32, u32]
+            L.zc_workspace_size_batch.argtypes = [pu64, u32, i32, u32, u32]
             L.zc_decompress_workspace_size_batch.restype = u64
             L.zc_decompress_workspace_size_batch.argtypes = [u32]
             L.zc_compress_batch.restype = i32
-            L.zc_compress_batch.argtypes = [u32, vp, vp, pu64, i32, pi32, pi64, u32, dbl, vp, pu64, vp, vp, u64,
-                                            vp, vp]
+            L.zc_compress_batch.argtypes = [u32, vp, vp, pu64, i32, pi32, pi64, u32, dbl, u32, vp, pu64, vp, vp,
+                                            u64, vp, vp]
             L.zc_decompress_batch.restype = i32
             L.zc_decompress_batch.argtypes = [u32, vp, ctypes.POINTER(_Info), vp, vp, pu64, u32, vp, u64, vp, vp]
             _lib = L
@@ -114,12 +123,13 @@ def dtype_code(t: torch.Tensor) -> int:
         raise ZcError(EINVAL, f"unsupported dtype {t.dtype}") from None
 
 
-def blob_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD) -> int:
-    return int(lib().zc_blob_size(nbytes, dtype, chunk_bytes, threshold))
+def blob_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
+              flags: int = 0) -> int:
+    return int(lib().zc_blob_size_ex(nbytes, dtype, chunk_bytes, threshold, flags))
 
 
-def workspace_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK) -> int:
-    return int(lib().zc_workspace_size(nbytes, dtype, chunk_bytes))
+def workspace_size(nbytes: int, dtype: int, chunk_bytes: int = DEFAULT_CHUNK, flags: int = 0) -> int:
+    return int(lib().zc_workspace_size_ex(nbytes, dtype, chunk_bytes, flags))
 
 
 def _check(st: int, what: str):
@@ -130,7 +140,7 @@ def _check(st: int, what: str):
 def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tensor, workspace: torch.Tensor,
                   status: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK,
                   threshold: float = DEFAULT_THRESHOLD, stream=None, dtype: int | None = None,
-                  shape=None) -> None:
+                  shape=None, flags: int = 0) -> None:
     """Launch compression into caller buffers; no allocation, no sync.
 
     ``blob_bytes`` is a 1-element int64 CUDA tensor that receives the blob
@@ -139,25 +149,27 @@ def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tenso
     shape = tuple(src.shape) if shape is None else tuple(shape)
     shp = (ctypes.c_int64 * max(1, len(shape)))(*shape)
     nbytes = src.numel() * src.element_size()
-    st = lib().zc_compress(src.data_ptr() if nbytes else None, nbytes, code, len(shape), shp, chunk_bytes,
-                           threshold, blob.data_ptr(), blob.numel(), blob_bytes.data_ptr(),
-                           workspace.data_ptr(), workspace.numel(), status.data_ptr(), _stream(stream))
+    st = lib().zc_compress_ex(src.data_ptr() if nbytes else None, nbytes, code, len(shape), shp, chunk_bytes,
+                              threshold, flags, blob.data_ptr(), blob.numel(), blob_bytes.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), status.data_ptr(), _stream(stream))
     _check(st, "zc_compress")
 
 
 def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
-             stream=None, host_blob: bool = False) -> torch.Tensor:
+             stream=None, host_blob: bool = False, shared_tables: bool = False) -> torch.Tensor:
     """Compress a CUDA tensor into a self-describing blob (1-D uint8 tensor).
 
     The blob is a CUDA tensor, or with ``host_blob`` a page-locked CPU tensor
     that the kernels write directly over the host link (no separate copy).
-    Synchronises once, to read the blob length."""
+    ``shared_tables`` writes format v2 (one table per byte plane of the
+    tensor). Synchronises once, to read the blob length."""
+    flags = SHARED_TABLES if shared_tables else 0
     if not t.is_cuda:
         raise ZcError(EINVAL, "compress expects a CUDA tensor")
     src = t.contiguous()
     code = dtype_code(src)
     nbytes = src.numel() * src.element_size()
-    cap = blob_size(nbytes, code, chunk_bytes, threshold)
+    cap = blob_size(nbytes, code, chunk_bytes, threshold, flags)
     if cap == 0:
         raise ZcError(EINVAL, "invalid compression parameters")
     dev = src.device
@@ -167,10 +179,11 @@ def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float
     else:
         blob = torch.empty(cap, dtype=torch.uint8, device=dev)
         nb = torch.zeros(1, dtype=torch.int64, device=dev)
-    ws = torch.empty(max(16, workspace_size(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, workspace_size(nbytes, code, chunk_bytes, flags)), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flat = src.view(-1).view(torch.uint8)
-    compress_into(flat, blob, nb, ws, status, chunk_bytes, threshold, stream, dtype=code, shape=tuple(t.shape))
+    compress_into(flat, blob, nb, ws, status, chunk_bytes, threshold, stream, dtype=code, shape=tuple(t.shape),
+                  flags=flags)
     if host_blob:
         torch.cuda.synchronize(dev)  # the length is written to host memory by the kernel
     _check(int(status.item()), "zc_compress (device)")
@@ -190,7 +203,7 @@ def blob_info(prefix) -> dict:
 def _info_dict(info: _Info) -> dict:
     return dict(dtype=info.dtype, ndim=info.ndim, shape=tuple(info.shape[: info.ndim]),
                 nbytes=info.nbytes, blob_bytes=info.blob_bytes, n_chunks=info.n_chunks,
-                chunk_bytes=info.chunk_bytes)
+                chunk_bytes=info.chunk_bytes, version=info.version)
 
 
 def _info_struct(d: dict) -> _Info:
@@ -200,14 +213,17 @@ def _info_struct(d: dict) -> _Info:
         info.shape[i] = v
     info.nbytes, info.blob_bytes = d["nbytes"], d["blob_bytes"]
     info.n_chunks, info.chunk_bytes = d["n_chunks"], d["chunk_bytes"]
+    info.version = d.get("version", 1)
     return info
 
 
 def read_info(blob: torch.Tensor) -> dict:
     """blob_info of a device or host blob (the header and table on the host)."""
-    head = blob[:96].cpu()
-    n_chunks = int.from_bytes(bytes(head[24:28].numpy()), "little")
-    return blob_info(blob[: 96 + 16 * n_chunks].cpu())
+    head = bytes(blob[:96].cpu().numpy())
+    n_chunks = int.from_bytes(head[24:28], "little")
+    version = head[4] | head[5] << 8
+    planes = 512 * _WORD.get(head[6], 0) if version == 2 else 0  # v2: the plane tables follow the chunk table
+    return blob_info(blob[: 96 + 16 * n_chunks + planes].cpu())
 
 
 def decompress_into(blob: torch.Tensor, info: dict, out: torch.Tensor, status: torch.Tensor,
@@ -337,9 +353,9 @@ def _u64s(vals) -> ctypes.Array:
     return (ctypes.c_uint64 * max(1, len(vals)))(*vals)
 
 
-def workspace_size_batch(nbytes, dtype: int, chunk_bytes: int = DEFAULT_CHUNK) -> int:
+def workspace_size_batch(nbytes, dtype: int, chunk_bytes: int = DEFAULT_CHUNK, flags: int = 0) -> int:
     """Workspace bytes for compress_batch_into over tensors of these sizes."""
-    return int(lib().zc_workspace_size_batch(_u64s(nbytes), len(nbytes), dtype, chunk_bytes))
+    return int(lib().zc_workspace_size_batch(_u64s(nbytes), len(nbytes), dtype, chunk_bytes, flags))
 
 
 def decompress_workspace_size_batch(n: int) -> int:
@@ -348,7 +364,7 @@ def decompress_workspace_size_batch(n: int) -> int:
 
 def compress_batch_into(srcs, blobs, blob_bytes: torch.Tensor, workspace: torch.Tensor, status: torch.Tensor,
                         dtype: int, shapes, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
-                        stream=None, bases=None) -> None:
+                        stream=None, bases=None, flags: int = 0) -> None:
     """Launch compression of n tensors (flat byte views ``srcs``) into the
     blobs ``blobs`` in one grid; ``blob_bytes`` is an n-element int64 CUDA
     tensor receiving the blob lengths. With ``bases``, tensor t is coded as
@@ -365,14 +381,15 @@ def compress_batch_into(srcs, blobs, blob_bytes: torch.Tensor, workspace: torch.
         flat += list(sh) + [0] * (8 - len(sh))
     shp = (ctypes.c_int64 * max(8, len(flat)))(*flat)
     st = lib().zc_compress_batch(n, _ptrs(srcs), _ptrs(bases) if bases is not None else None, _u64s(nbytes), dtype,
-                                 ndims, shp, chunk_bytes, threshold, _ptrs(blobs), _u64s([b.numel() for b in blobs]),
+                                 ndims, shp, chunk_bytes, threshold, flags, _ptrs(blobs),
+                                 _u64s([b.numel() for b in blobs]),
                                  blob_bytes.data_ptr(), workspace.data_ptr(), workspace.numel(), status.data_ptr(),
                                  _stream(stream))
     _check(st, "zc_compress_batch")
 
 
 def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD, stream=None,
-                   bases=None, host_blob: bool = False) -> list:
+                   bases=None, host_blob: bool = False, shared_tables: bool = False) -> list:
     """Compress a list of CUDA tensors of one dtype in one call; returns one
     blob per tensor, each equal to compress() of that tensor (with ``bases``:
     to compress_delta(bases[t], tensors[t])); with ``host_blob`` the blobs are
@@ -393,8 +410,9 @@ def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float =
             raise ZcError(EINVAL, f"unsupported element size {ts[0].element_size()}")
     else:
         code = dtype_code(ts[0])
+    flags = SHARED_TABLES if shared_tables else 0
     nbytes = [t.numel() * t.element_size() for t in ts]
-    caps = [blob_size(nb, code, chunk_bytes, threshold) for nb in nbytes]
+    caps = [blob_size(nb, code, chunk_bytes, threshold, flags) for nb in nbytes]
     if 0 in caps:
         raise ZcError(EINVAL, "invalid compression parameters")
     offs, o = [], 0
@@ -405,13 +423,13 @@ def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float =
     buf = torch.empty(o, dtype=torch.uint8, pin_memory=True) if host_blob else \
         torch.empty(o, dtype=torch.uint8, device=dev)
     blobs = [buf[a: a + c] for a, c in zip(offs, caps)]
-    ws = torch.empty(max(16, workspace_size_batch(nbytes, code, chunk_bytes)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, workspace_size_batch(nbytes, code, chunk_bytes, flags)), dtype=torch.uint8, device=dev)
     nb = torch.zeros(n, dtype=torch.int64, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flat = [t.view(-1).view(torch.uint8) for t in ts]
     compress_batch_into(flat, blobs, nb, ws, status, code, [tuple(t.shape) for t in tensors], chunk_bytes,
                         threshold, stream, bases=[b.view(-1).view(torch.uint8) for b in bs] if bases is not None
-                        else None)
+                        else None, flags=flags)
     if host_blob:
         torch.cuda.synchronize(dev)
     _check(int(status.item()), "zc_compress_batch (device)")

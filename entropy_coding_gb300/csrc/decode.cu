@@ -43,6 +43,8 @@ constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
 // the 496-byte gap
 constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
 constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
+constexpr uint32_t kV2Pairs = 16;             // v2: chunks per CTA at most (one CTA per SM)
+constexpr int kV2Threads = 64 * kV2Pairs;
 
 // Shared memory of one warp pair. With kBig (few pairs per SM) the decoding
 // step reads a one-level table slot -> symbol | f << 8 | (slot - cum) << 20
@@ -57,6 +59,16 @@ struct PairSmem {
     alignas(16) uint8_t stage[kStages][256];  // decoded symbols, row k = step k of a group (read as uint2)
     unsigned long long full[kStages], empty[kStages], start;
     uint32_t flag;                   // producer -> consumer: 1 when the main stream is ready
+};
+
+// Shared memory of one warp pair in format v2: the decoding tables are the
+// CTA's (one per plane, shared by all its pairs), so a pair keeps only its
+// word ring, its stage queue and their barriers.
+struct PairSmemV2 {
+    uint16_t ring[kRingWords];
+    alignas(16) uint8_t stage[kStages][256];
+    unsigned long long full[kStages], empty[kStages], start;
+    uint32_t flag;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return uint32_t(__cvta_generic_to_shared(p)); }
@@ -207,6 +219,29 @@ __device__ bool rans_setup(const uint8_t *rec, uint32_t val, uint8_t *slot, uint
     return true;
 }
 
+// Format v2 record: the 32 lane states, then the words; the table is the
+// plane's one-level table `big` built by the CTA (null when the blob's plane
+// table is not a valid 12-bit table). Returns false if malformed.
+__device__ bool rans_setup_shared(const uint8_t *rec, uint32_t val, const uint32_t *big, uint16_t *ring, Rans &r) {
+    const int lane = threadIdx.x & 31;
+    bool bad = big == nullptr || val < 128 || ((val - 128) & 1u);
+    r.x = bad ? kRansL : reinterpret_cast<const uint32_t *>(rec)[lane];
+    bad |= r.x < kRansL;
+    if (__any_sync(kFull, bad)) return false;
+    const uint32_t nwords = (val - 128) / 2;
+    r.ptr = int32_t(nwords);
+    r.wbase = rec + 128;
+    r.padded = uint32_t(pad16(2 * nwords));
+    r.lut = nullptr;
+    r.sym = nullptr;
+    r.big = big;
+    r.ring = ring;
+    r.lo = nwords ? int((nwords - 1) >> 8) + 1 : 0;
+    __syncwarp();
+    ring_refill(r);
+    return true;
+}
+
 // One rANS decode step of the warp: returns this lane's symbol.
 template <bool kBig>
 __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt) {
@@ -258,7 +293,7 @@ struct ChunkCtx {
 };
 
 // Parse a grouped chunk's directory. Returns false if malformed.
-template <int W>
+template <int W, bool kV2>
 __device__ bool parse_directory(const uint8_t *p, uint32_t stored, uint32_t n, ChunkCtx &cx) {
     const int lane = threadIdx.x & 31;
     // W entries of mode << 30 | value, zero-padded to 16 bytes
@@ -285,7 +320,7 @@ __device__ bool parse_directory(const uint8_t *p, uint32_t stored, uint32_t n, C
             cx.sub[j] = coded == 0 ? 0 : coded - 1;
             cx.have_main = true;
             coded++;
-            bad |= cx.val[j] < kRecHead || cx.val[j] > stored;
+            bad |= cx.val[j] < (kV2 ? 128u : kRecHead) || cx.val[j] > stored;
             pos += uint32_t(pad16(cx.val[j]));
         } else {
             cx.kind[j] = kKConst;
@@ -300,19 +335,27 @@ __device__ bool parse_directory(const uint8_t *p, uint32_t stored, uint32_t n, C
 // Producer warp: staged streams into the output tail, then the main stream's
 // symbols group by group into the stage queue (the last group may be
 // partial: steps past the stream leave the states alone).
-template <int DT, bool kBig>
-__device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem<kBig> &ps) {
+template <int DT, bool kBig, bool kV2, class PS>
+__device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const uint32_t *const *pbig) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
     const uint32_t lt = lanemask_lt();
-    uint8_t *slot = ps.lut;
+    // v1: the record's own table, built into the pair's tables; v2: the
+    // CTA's table of the stream's plane
+    auto setup = [&](int j, Rans &r) -> bool {
+        if constexpr (kV2) {
+            return rans_setup_shared(cx.p + cx.roff[j], cx.val[j], pbig[j], ps.ring, r);
+        } else {
+            return rans_setup<kBig>(cx.p + cx.roff[j], cx.val[j], ps.lut, ps.big, r);
+        }
+    };
     bool bad = false;
     if (cx.q) {
 #pragma unroll
         for (int j = 0; j < W; j++) {
             if (cx.kind[j] != kKStaged) continue;
             Rans r;
-            if (!rans_setup<kBig>(cx.p + cx.roff[j], cx.val[j], slot, ps.big, r)) bad = true;
+            if (!setup(j, r)) bad = true;
             if (!bad) {
                 for (uint32_t t = 0; t < cx.T; t++) {
                     const uint32_t i = t * 32 + lane;
@@ -331,8 +374,7 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PairSmem<kBig> 
     Rans rs;
 #pragma unroll
     for (int j = 0; j < W; j++)
-        if (!bad && cx.kind[j] == kKMain && !rans_setup<kBig>(cx.p + cx.roff[j], cx.val[j], slot, ps.big, rs))
-            bad = true;
+        if (!bad && cx.kind[j] == kKMain && !setup(j, rs)) bad = true;
     if (lane == 0) ps.flag = bad ? 0u : 1u;
     __syncwarp();
     mbar_arrive(&ps.start);
@@ -550,19 +592,22 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
     }
 }
 
-template <int DT, bool kBig, bool kDelta>
-__device__ void decode_chunk(const DecodeArgs &a, uint32_t g, bool producer, PairSmem<kBig> &ps, const uint32_t *crc_rep,
-                             const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
+// Chunk c of blob bd, by one warp pair (kV2: format v2, with the CTA's
+// plane tables pbig).
+template <int DT, bool kBig, bool kDelta, bool kV2, class PS>
+__device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c, bool producer, PS &ps,
+                             const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256],
+                             const uint32_t *const *pbig) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
-    // the blob of this call-wide chunk index
-    const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
     const uint8_t *const blob = bd.blob;
     const uint64_t blob_bytes = bd.blob_bytes, nbytes = bd.nbytes;
-    const uint32_t n_chunks = bd.n_chunks, c = g - bd.chunk_base;
+    const uint32_t n_chunks = bd.n_chunks;
     uint8_t *const dst = bd.dst;
     const uint8_t *const base = bd.base;
-    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * n_chunks;
+    // payloads follow the chunk table (v2: and the W plane tables)
+    const uint64_t table_end =
+        ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * n_chunks + (kV2 ? 512ull * W : 0ull);
 
     uint4 ent = make_uint4(0, 0, 0, 0);
     if (lane == 0) ent = reinterpret_cast<const uint4 *>(blob + ZC_HEADER_BYTES)[c];
@@ -606,7 +651,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t g, bool producer, Pai
     }
 
     ChunkCtx cx;
-    if (!parse_directory<W>(p, stored, n, cx)) {
+    if (!parse_directory<W, kV2>(p, stored, n, cx)) {
         if (!producer && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
         return;
     }
@@ -619,7 +664,7 @@ __device__ void decode_chunk(const DecodeArgs &a, uint32_t g, bool producer, Pai
     cx.tail = out + (len - cx.q * n);
     cx.base = basec;
     if (producer) {
-        if (cx.have_main) produce<DT, kBig>(a, cx, ps);
+        if (cx.have_main) produce<DT, kBig, kV2>(a, cx, ps, pbig);
     } else if (verify) {
         consume<DT, true, kDelta>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     } else {
@@ -653,7 +698,114 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs
     __syncthreads();
     const uint32_t g = blockIdx.x * pairs_per_cta + (warp >> 1);
     if (g >= a.total_chunks) return;
-    decode_chunk<DT, kBig, kDelta>(a, g, (warp & 1) == 0, pairs[warp >> 1], crc_rep, gshift, gap496);
+    // the blob of this call-wide chunk index
+    const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
+    decode_chunk<DT, kBig, kDelta, false>(a, bd, g - bd.chunk_base, (warp & 1) == 0, pairs[warp >> 1], crc_rep,
+                                          gshift, gap496, nullptr);
+}
+
+// Format v2 (shared plane tables): a CTA decodes up to a.pairs consecutive
+// chunks of one blob (CTAs never span blobs). It first checks the blob's W
+// plane tables and builds the one-level table of each valid one
+// (slot -> symbol | f << 8 | (slot - cum) << 20, as the v1 big tables),
+// which all its warp pairs then share: every decoding step is a single
+// table read, whatever the number of chunks per SM, and no chunk builds a
+// table of its own.
+template <int DT, bool kDelta>
+__global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int W = WordOf<DT>::W;
+    uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
+    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
+    uint32_t *big = reinterpret_cast<uint32_t *>(smem + kCrcSmem);  // W x 4096
+    uint32_t *symcum = big + W * kM;                                  // W x 256: f | cum << 12
+    uint32_t *pvalid = symcum + W * 256;                              // W flags (padded to 16 bytes)
+    PairSmemV2 *pairs = reinterpret_cast<PairSmemV2 *>(pvalid + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the blob: the last one whose first CTA is at or before this one
+    uint32_t bi = 0;
+    if (a.n_blobs > 1) {
+        uint32_t lo = 0, hi = a.n_blobs;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (a.blobs[mid].cta_base <= blockIdx.x) lo = mid;
+            else hi = mid;
+        }
+        bi = lo;
+    }
+    const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[bi];
+    const uint32_t first = (blockIdx.x - bd.cta_base) * a.pairs;
+
+    if (!(a.flags & ZC_NO_VERIFY)) {
+        load_crc_rep(crc_rep);
+        load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
+        load_shift_smem(gap496, kSh496);
+    }
+    const uint32_t pairs_per_cta = blockDim.x >> 6;
+    if (threadIdx.x < pairs_per_cta) {
+        PairSmemV2 &ps = pairs[threadIdx.x];
+        for (int k = 0; k < kStages; k++) {
+            mbar_init(&ps.full[k], 32);
+            mbar_init(&ps.empty[k], 32);
+        }
+        mbar_init(&ps.start, 32);
+    }
+    // the warps check the plane tables in turn (256 u16 each after the chunk
+    // table; the host checked that the blob holds them) and lay out
+    // f | cum << 12 (a CTA may have fewer warps than planes)
+    for (int j = warp; j < W; j += int(blockDim.x >> 5)) {
+        const uint8_t *pt = bd.blob + ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * bd.n_chunks + 512ull * j;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(pt) + lane);
+        const uint32_t f[8] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16,
+                               v.z & 0xFFFFu, v.z >> 16, v.w & 0xFFFFu, v.w >> 16};
+        uint32_t fsum = 0, nz = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            fsum += f[k];
+            nz += f[k] ? 1u : 0u;
+        }
+        uint32_t cum = fsum;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, cum, o);
+            if (lane >= o) cum += t;
+        }
+        const bool ok = __shfl_sync(kFull, cum, 31) == kM && __reduce_add_sync(kFull, nz) >= 2;
+        cum -= fsum;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            symcum[j * 256 + 8 * lane + k] = f[k] | cum << 12;
+            cum += f[k];
+        }
+        if (lane == 0) pvalid[j] = ok ? 1u : 0u;
+    }
+    __syncthreads();
+    // slot -> symbol: the last symbol whose range starts at or before the slot
+    // (a symbol of frequency 0 shares its start with the next one, and the
+    // last range ends at 4096, so the search always lands on a symbol with
+    // f > 0 for a valid table)
+    for (uint32_t i = threadIdx.x; i < uint32_t(W) * kM; i += blockDim.x) {
+        const uint32_t j = i / kM, slot = i % kM;
+        if (!pvalid[j]) continue;
+        const uint32_t *sc = symcum + j * 256;
+        uint32_t lo = 0, hi = 256;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if ((sc[mid] >> 12) <= slot) lo = mid;
+            else hi = mid;
+        }
+        const uint32_t e = sc[lo];
+        big[i] = lo | (e & 0xFFFu) << 8 | (slot - (e >> 12)) << 20;
+    }
+    __syncthreads();
+    const uint32_t pair = uint32_t(warp >> 1);
+    if (first + pair >= bd.n_chunks) return;
+    const uint32_t *pbig[4] = {nullptr, nullptr, nullptr, nullptr};
+#pragma unroll
+    for (int j = 0; j < W; j++) pbig[j] = pvalid[j] ? big + j * kM : nullptr;
+    decode_chunk<DT, true, kDelta, true>(a, bd, first + pair, (warp & 1) == 0, pairs[pair], crc_rep, gshift, gap496,
+                                         pbig);
 }
 
 template <int DT, bool kBig, bool kDelta>
@@ -686,10 +838,47 @@ int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     return launch_decode_mode<DT, false, kDelta>(a, pc, s);
 }
 
+template <int DT, bool kDelta>
+int launch_decode_v2_t(const DecodeArgs &a, cudaStream_t s) {
+    constexpr int W = WordOf<DT>::W;
+    if (a.pairs == 0 || a.pairs > kV2Pairs || a.n_ctas == 0) return ZC_EINVAL;
+    const size_t fixed = kCrcSmem + size_t(W) * (kM * 4 + 256 * 4) + 16;
+    const size_t smem = fixed + size_t(a.pairs) * sizeof(PairSmemV2);
+    const size_t smem_max = fixed + size_t(kV2Pairs) * sizeof(PairSmemV2);
+    if (cudaFuncSetAttribute(decode_v2_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem_max)) != cudaSuccess)
+        return ZC_ECUDA;
+    decode_v2_kernel<DT, kDelta><<<a.n_ctas, 64 * a.pairs, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
+
+int launch_decode_v2(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s) {
+    switch (dtype) {
+    case ZC_U8: return delta ? launch_decode_v2_t<ZC_U8, true>(a, s) : launch_decode_v2_t<ZC_U8, false>(a, s);
+    case ZC_U16: return delta ? launch_decode_v2_t<ZC_U16, true>(a, s) : launch_decode_v2_t<ZC_U16, false>(a, s);
+    case ZC_U32: return delta ? launch_decode_v2_t<ZC_U32, true>(a, s) : launch_decode_v2_t<ZC_U32, false>(a, s);
+    case ZC_BF16: return delta ? ZC_EINVAL : launch_decode_v2_t<ZC_BF16, false>(a, s);
+    case ZC_FP16: return delta ? ZC_EINVAL : launch_decode_v2_t<ZC_FP16, false>(a, s);
+    case ZC_FP32: return delta ? ZC_EINVAL : launch_decode_v2_t<ZC_FP32, false>(a, s);
+    default: return ZC_EINVAL;
+    }
+}
+
 } // namespace
+
+uint32_t decode_v2_pairs(uint64_t total_chunks) {
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms < 1)
+        sms = 1;
+    // one CTA per SM holds its chunks when they fit; else CTAs of kV2Pairs
+    const uint64_t per_sm = (total_chunks + uint64_t(sms) - 1) / uint64_t(sms);
+    return uint32_t(std::max<uint64_t>(1, std::min<uint64_t>(kV2Pairs, per_sm)));
+}
 
 int launch_decode(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s) {
     if (a.total_chunks == 0) return ZC_OK;
+    if (a.version == 2) return launch_decode_v2(dtype, delta, a, s);
     switch (dtype) {
     case ZC_U8: return delta ? launch_decode_t<ZC_U8, true>(a, s) : launch_decode_t<ZC_U8, false>(a, s);
     case ZC_U16: return delta ? launch_decode_t<ZC_U16, true>(a, s) : launch_decode_t<ZC_U16, false>(a, s);

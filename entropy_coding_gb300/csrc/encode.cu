@@ -256,6 +256,66 @@ __device__ void normalize_warp(const uint32_t cnt[8], uint32_t n, uint32_t f[8])
     }
 }
 
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long t = __shfl_xor_sync(kFull, v, o);
+        v = t > v ? t : v;
+    }
+    return v;
+}
+
+// The same quantisation rule as normalize_warp for a plane's counts over a
+// whole tensor (shared tables; lmzip "Building on lmz": one table per plane
+// kind), which may exceed 32 bits: 64-bit counts and keys in the first two
+// steps; the third works on the frequencies alone.
+__device__ void normalize_plane_warp(const unsigned long long cnt[8], unsigned long long n, uint32_t f[8]) {
+    const int lane = threadIdx.x & 31;
+    uint32_t local = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const unsigned long long q = cnt[k] * kM / n;
+        f[k] = cnt[k] ? (q < 1 ? 1u : uint32_t(q)) : 0u;
+        local += f[k];
+    }
+    uint32_t sum = warp_sum_u32(local);
+    if (sum < kM) {
+        unsigned long long key = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const unsigned long long kk = (cnt[k] << 8) | (255u - (8 * lane + k));
+            key = kk > key ? kk : key;
+        }
+        key = warp_max_u64(key);
+        const uint32_t sb = 255u - uint32_t(key & 0xFFu);
+        if ((sb >> 3) == uint32_t(lane)) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (k == int(sb & 7)) f[k] += kM - sum;
+        }
+    }
+    while (sum > kM) {
+        uint32_t key = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (f[k] > 1) key = max(key, (f[k] << 8) | (255u - (8 * lane + k)));
+        key = warp_max_u32(key);
+        uint32_t f1 = key >> 8, s1 = 255u - (key & 0xFFu);
+        uint32_t key2 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (f[k] > 1 && 8 * lane + k != s1) key2 = max(key2, f[k]);
+        uint32_t m2 = max(warp_max_u32(key2), 1u);
+        uint32_t dec = (f1 > m2) ? min(sum - kM, f1 - m2) : 1u;
+        if ((s1 >> 3) == uint32_t(lane)) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (k == int(s1 & 7)) f[k] -= dec;
+        }
+        sum -= dec;
+    }
+}
+
 // Exclusive prefix of this chunk's padded size over the chunks before it
 // (decoupled look-back, one warp). Every wait is bounded; a timeout sets
 // ZC_ETIMEOUT and the chunk is not placed.
@@ -477,7 +537,8 @@ __device__ void merge_counts(StatsSmem<W> &sm) {
 // counts (8 bins per lane: symbol 8 lane + k): CONST / RAW / candidate. A
 // candidate's 12-bit table goes to ftab (256 u16).
 template <int W>
-__device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *counts, uint32_t *sv, uint8_t *ftab) {
+__device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *counts, uint32_t *sv, uint8_t *ftab,
+                           unsigned long long *hist) {
     const int lane = threadIdx.x & 31;
     uint32_t cnt[8];
     const uint4 c0 = reinterpret_cast<const uint4 *>(counts)[2 * lane];
@@ -490,6 +551,8 @@ __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *coun
         if (cnt[k]) {
             pres++;
             only = 8 * lane + k;
+            // v2: the chunk's counts join its tensor's plane histogram
+            if (hist) atomicAdd(hist + 8 * lane + k, (unsigned long long)cnt[k]);
         }
     const uint32_t k_total = warp_sum_u32(pres);
     uint32_t mode, val;
@@ -497,6 +560,22 @@ __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *coun
         const uint32_t who = __ballot_sync(kFull, pres != 0);
         mode = kModeConst;
         val = __shfl_sync(kFull, only, __ffs(who) - 1);
+    } else if (hist) {
+        // v2: the table is the tensor's, not known yet. Its cost is at least
+        // the chunk's own order-0 information n H (Gibbs' inequality: no
+        // table codes the chunk below its empirical entropy), so the bound
+        // below, with the v2 record head (32 states, no table), holds for
+        // whatever table the tensor gets.
+        const float lg_n = __log2f(float(n));
+        float info = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (cnt[k]) info += float(cnt[k]) * (lg_n - __log2f(float(cnt[k])));
+        info = warp_sum_f32(info);
+        const float words_lb = (info * (1.0f - 1.0f / 1024) - 0.0932f * float(n) - 512.0f - 64.0f) / 16.1f;
+        const uint64_t rec_lb = 128 + 2ull * uint64_t(words_lb > 0.f ? words_lb : 0.f);
+        mode = double(rec_lb) < a.threshold * double(n) ? kModeCand : kModeRaw;
+        val = mode == kModeRaw ? n : 0;
     } else {
         uint32_t f[8];
         normalize_warp(cnt, n, f);
@@ -615,8 +694,10 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
         // the other warps go on to the next chunk: the counters were zeroed by
         // the merge, and the next merge comes after the next barrier
         if (warp < W) {
-            const bool cand_j =
-                plan_stats<W>(a, len / W, sm.cnt[warp], info + 1 + warp, a.ws_ftab + (uint64_t(cl) * W + warp) * 512);
+            unsigned long long *hist =
+                a.version == 2 ? a.ws_hist + (uint64_t(tv.t) * W + warp) * 256 : nullptr;
+            const bool cand_j = plan_stats<W>(a, len / W, sm.cnt[warp], info + 1 + warp,
+                                              a.ws_ftab + (uint64_t(cl) * W + warp) * 512, hist);
             if (warp > 0 && cand_j) warp_write_cand<DT, kDelta>(src, len, warp, cand + uint64_t(warp) * a.n_pad);
         }
     }
@@ -640,7 +721,8 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
 // kAborted once the record has reached lim bytes (it can then no longer be
 // kept: the stream is stored raw).
 __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint4 *etab,
-                                       uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim) {
+                                       uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim,
+                                       bool shared) {
     const int lane = threadIdx.x & 31;
     uint16_t *stage = stage_base + lane;  // step s of a block: stage[32 s]
     const int T = int((n + 31) / 32);
@@ -676,15 +758,21 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         const uint32_t s = 8 * lane + k, fs = f[k];
         if (fs) {
             bits |= 1u << k;
-            reinterpret_cast<uint16_t *>(rec + kRecHead)[rank++] = uint16_t(fs);
+            if (!shared) reinterpret_cast<uint16_t *>(rec + kRecHead)[rank] = uint16_t(fs);
+            rank++;
             const uint32_t ka = kRecip.ka[fs], m = kRecip.m[fs];
             etab[s] = make_uint4(m, (ka >> 8) ? m : 0u, fs << 20, (kM - fs) | (cum << 13) | (((ka & 0xFFu) - 32) << 25));
         }
         cum += fs;
     }
-    rec[128 + lane] = uint8_t(bits);
-    const uint32_t words_at = kRecHead + uint32_t(pad16(2 * k_total));
-    for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
+    // v1 record: states | presence bitmap | frequencies | pad | words; v2
+    // (shared plane tables): states | words
+    uint32_t words_at = 128;
+    if (!shared) {
+        rec[128 + lane] = uint8_t(bits);
+        words_at = kRecHead + uint32_t(pad16(2 * k_total));
+        for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
+    }
 
     uint16_t *wout = reinterpret_cast<uint16_t *>(rec + words_at);
     const uint32_t gt = lanemask_gt();
@@ -907,17 +995,21 @@ __device__ void warp_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
 }
 
 template <int DT, int J>
-__device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, uint32_t n, uint64_t lim, uint4 *etab,
-                                            uint8_t *ring, uint8_t *slot, uint32_t mode[4], uint32_t val[4]) {
+__device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, uint32_t t, uint32_t n, uint64_t lim,
+                                            uint4 *etab, uint8_t *ring, uint8_t *slot, uint32_t mode[4],
+                                            uint32_t val[4]) {
     constexpr int W = WordOf<DT>::W;
     if (mode[J] != kModeCand) return;
     const int lane = threadIdx.x & 31;
-    const uint4 fv = reinterpret_cast<const uint4 *>(a.ws_ftab + (uint64_t(cl) * W + J) * 512)[lane];
+    // v1: the chunk's own table; v2: its tensor's plane table
+    const uint8_t *ftab = a.version == 2 ? a.ws_ptab + (uint64_t(t) * W + J) * 512
+                                         : a.ws_ftab + (uint64_t(cl) * W + J) * 512;
+    const uint4 fv = reinterpret_cast<const uint4 *>(ftab)[lane];
     const uint32_t f[8] = {fv.x & 0xFFFFu, fv.x >> 16, fv.y & 0xFFFFu, fv.y >> 16,
                            fv.z & 0xFFFFu, fv.z >> 16, fv.w & 0xFFFFu, fv.w >> 16};
     const uint8_t *cand = a.ws_cand + (uint64_t(cl) * W + J) * a.n_pad;
     const uint32_t rb = rans_encode_stream(cand, n, f, etab, ring, reinterpret_cast<uint16_t *>(ring + 4096),
-                                           slot + uint64_t(J) * a.rec_stride, lim);
+                                           slot + uint64_t(J) * a.rec_stride, lim, a.version == 2);
     if (rb != kAborted && rb < lim) {
         mode[J] = kModeRans;
         val[J] = rb;
@@ -947,8 +1039,11 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         const uint32_t g = a.wave_start + cl;
         const TView tv = tensor_view(a, g);
         const uint32_t c = g - tv.chunk_base;  // chunk of its tensor
-        uint32_t *tctrl = ctrl + 64 + 4 * tv.t;  // the tensor's done counter and header-CRC accumulator
-        const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * tv.n_chunks;
+        // the tensor's done counter, header-CRC accumulator and (v2) plane-table CRC
+        uint32_t *tctrl = ctrl + 64 + 4 * tv.t;
+        // payloads start after the chunk table (v2: and the W plane tables)
+        const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * tv.n_chunks +
+                                   (a.version == 2 ? 512ull * W : 0ull);
         const Source<kDelta> src = Source<kDelta>{tv.src, tv.base}.at(uint64_t(c) * a.chunk_bytes);
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, tv.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
@@ -963,11 +1058,11 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         }
         // a record is kept iff its size is below threshold x n, i.e. below lim
         const uint64_t lim = uint64_t(ceil(a.threshold * double(n)));
-        code_stream<DT, 0>(a, cl, n, lim, etab, ring, slot, mode, val);
-        if constexpr (W > 1) code_stream<DT, 1>(a, cl, n, lim, etab, ring, slot, mode, val);
+        code_stream<DT, 0>(a, cl, tv.t, n, lim, etab, ring, slot, mode, val);
+        if constexpr (W > 1) code_stream<DT, 1>(a, cl, tv.t, n, lim, etab, ring, slot, mode, val);
         if constexpr (W > 2) {
-            code_stream<DT, 2>(a, cl, n, lim, etab, ring, slot, mode, val);
-            code_stream<DT, 3>(a, cl, n, lim, etab, ring, slot, mode, val);
+            code_stream<DT, 2>(a, cl, tv.t, n, lim, etab, ring, slot, mode, val);
+            code_stream<DT, 3>(a, cl, tv.t, n, lim, etab, ring, slot, mode, val);
         }
 
         uint64_t grouped = 16;  // pad16(4W) for W <= 4
@@ -1031,7 +1126,9 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
                 uint32_t hc = 0xFFFFFFFFu;
                 for (int q = 0; q < 24; q++) hc = crc_word_global(hc, header[q]);
                 hc ^= 0xFFFFFFFFu;
-                const uint32_t hcrc = shift_bytes(hc, 16ull * tv.n_chunks) ^ acc;
+                uint32_t hcrc = shift_bytes(hc, 16ull * tv.n_chunks) ^ acc;
+                // v2: the CRC runs on over the plane tables that follow
+                if (a.version == 2) hcrc = shift_bytes(hcrc, 512ull * W) ^ atomicXor(&tctrl[2], 0u);
                 uint32_t *hdr = reinterpret_cast<uint32_t *>(tv.blob);
                 for (int q = 0; q < 24; q++) hdr[q] = (q == 7) ? hcrc : header[q];
                 *d_blob_bytes = total;
@@ -1041,14 +1138,63 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     }
 }
 
-// A blob of an empty tensor is its header alone (its CRC made on the host).
+// A blob of an empty tensor is its header alone (v2: and W zero plane
+// tables); its CRC is made on the host.
 __global__ void empty_blob_kernel(EncodeArgs a) {
     for (uint32_t t = blockIdx.x; t < a.n_tensors; t += gridDim.x) {
         const TensorDesc &d = a.n_tensors == 1 ? a.one : a.tensors[t];
         if (d.n_chunks != 0) continue;
-        if (threadIdx.x < 24) reinterpret_cast<uint32_t *>(d.blob)[threadIdx.x] = d.header[threadIdx.x];
-        if (threadIdx.x == 0) *d.d_blob_bytes = ZC_HEADER_BYTES;
+        uint32_t *b = reinterpret_cast<uint32_t *>(d.blob);
+        if (threadIdx.x < 24) b[threadIdx.x] = d.header[threadIdx.x];
+        const int W = word_bytes(int(d.header[1] >> 16) & 0xFF);
+        const uint32_t plane_words = a.version == 2 ? 128u * W : 0u;
+        for (uint32_t i = threadIdx.x; i < plane_words; i += blockDim.x) b[24 + i] = 0;
+        if (threadIdx.x == 0) *d.d_blob_bytes = ZC_HEADER_BYTES + 4ull * plane_words;
     }
+}
+
+// v2: the plane tables of the wave's tensors, one warp per tensor and plane.
+// The plane's counts over the whole tensor (every chunk's statistics have
+// been added) give its 12-bit table, or zeros for fewer than two symbols.
+// The table goes to the blob (after the chunk table) and to the workspace
+// for the coder; the CRC of the W tables (512 bytes each, in plane order)
+// is accumulated into the tensor's control word for the header CRC.
+template <int W>
+__global__ void plane_kernel(EncodeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const uint32_t t = a.wave_t0 + gw / W, j = gw % W;
+    if (t >= a.wave_t1) return;
+    const TensorDesc &d = a.n_tensors == 1 ? a.one : a.tensors[t];
+    if (d.n_chunks == 0) return;  // written whole by empty_blob_kernel
+    const unsigned long long *h = a.ws_hist + (uint64_t(t) * W + j) * 256;
+    unsigned long long cnt[8];
+    uint32_t pres = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        cnt[k] = h[8 * lane + k];
+        pres += cnt[k] ? 1u : 0u;
+    }
+    uint32_t f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (warp_sum_u32(pres) >= 2) normalize_plane_warp(cnt, d.nbytes / W, f);
+    uint4 v;
+    v.x = f[0] | f[1] << 16;
+    v.y = f[2] | f[3] << 16;
+    v.z = f[4] | f[5] << 16;
+    v.w = f[6] | f[7] << 16;
+    const uint64_t at = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * d.n_chunks + 512ull * j;
+    reinterpret_cast<uint4 *>(d.blob + at)[lane] = v;
+    reinterpret_cast<uint4 *>(a.ws_ptab + (uint64_t(t) * W + j) * 512)[lane] = v;
+    // CRC(P_0 .. P_{W-1}) = XOR over the 16-byte pieces of shift(CRC(piece),
+    // bytes after it), by linearity
+    uint32_t c = 0xFFFFFFFFu;
+    c = crc_word_global(c, v.x);
+    c = crc_word_global(c, v.y);
+    c = crc_word_global(c, v.z);
+    c = crc_word_global(c, v.w) ^ 0xFFFFFFFFu;
+    c = shift_bytes(c, 16ull * (31 - lane) + 512ull * (W - 1 - j));
+    c = __reduce_xor_sync(kFull, c);
+    if (lane == 0) atomicXor(reinterpret_cast<uint32_t *>(a.ws_ctrl) + 64 + 4 * t + 2, c);
 }
 
 int sms_of_device() {
@@ -1074,6 +1220,10 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     const int sgrid = int(a.wave_n < most ? a.wave_n : most);
     stats_kernel<DT, kDelta><<<sgrid, kStatThreads, ssm, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return ZC_ECUDA;
+    if (a.version == 2) {  // the wave holds whole tensors: their plane tables are complete now
+        const int st = launch_plane_tables(DT, a, s);
+        if (st != ZC_OK) return st;
+    }
     if (cudaMemsetAsync(a.ws_ctrl, 0, 4, s) != cudaSuccess) return ZC_ECUDA;  // coder ticket
     // the warps spread evenly over the SMs: CTAs of just enough warps for one
     // CTA per SM (the block scheduler then gives every SM the same share)
@@ -1088,6 +1238,20 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
 
 int launch_empty_blobs(const EncodeArgs &a, cudaStream_t s) {
     empty_blob_kernel<<<std::min<uint32_t>(a.n_tensors, 1024), 32, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
+
+int launch_plane_tables(int dtype, const EncodeArgs &a, cudaStream_t s) {
+    const int W = word_bytes(dtype);
+    const uint32_t warps = (a.wave_t1 - a.wave_t0) * uint32_t(W);
+    if (warps == 0) return ZC_OK;
+    const uint32_t grid = (warps + 3) / 4;
+    switch (W) {
+    case 1: plane_kernel<1><<<grid, 128, 0, s>>>(a); break;
+    case 2: plane_kernel<2><<<grid, 128, 0, s>>>(a); break;
+    case 4: plane_kernel<4><<<grid, 128, 0, s>>>(a); break;
+    default: return ZC_EINVAL;
+    }
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 

@@ -130,7 +130,8 @@ extern "C" uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_byte
 extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out) {
     const uint8_t *b = static_cast<const uint8_t *>(h_blob_prefix);
     if (!b || !out || avail < ZC_HEADER_BYTES) return ZC_EFORMAT;
-    if (std::memcmp(b, "ZCNN", 4) != 0 || (b[4] | b[5] << 8) != 1) return ZC_EFORMAT;
+    const uint32_t version = uint32_t(b[4] | b[5] << 8);
+    if (std::memcmp(b, "ZCNN", 4) != 0 || (version != 1 && version != 2)) return ZC_EFORMAT;
     const int dtype = b[6], ndim = b[7];
     const uint32_t chunk_bytes = get32(b + 8);
     const uint64_t nbytes = get64(b + 16);
@@ -150,8 +151,22 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
         elems *= uint64_t(v);
     }
     if (elems * uint64_t(W) != nbytes) return ZC_EFORMAT;
-    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc;
+    // v2: W plane tables of 256 u16 follow the chunk table, each all zeros or
+    // a 12-bit table of at least two symbols
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc + (version == 2 ? 512ull * W : 0);
     if (avail < table_end) return ZC_EFORMAT;
+    if (version == 2) {
+        for (int j = 0; j < W; j++) {
+            const uint8_t *t = b + table_end - 512ull * (W - j);
+            uint32_t sum = 0, nz = 0;
+            for (int v = 0; v < 256; v++) {
+                const uint32_t f = uint32_t(t[2 * v]) | uint32_t(t[2 * v + 1]) << 8;
+                sum += f;
+                nz += f ? 1u : 0u;
+            }
+            if (!(sum == 0 || (sum == kM && nz >= 2))) return ZC_EFORMAT;
+        }
+    }
     uint8_t head[ZC_HEADER_BYTES];
     std::memcpy(head, b, ZC_HEADER_BYTES);
     put32(head + 28, 0);
@@ -174,6 +189,8 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
     out->blob_bytes = off;
     out->n_chunks = nc;
     out->chunk_bytes = chunk_bytes;
+    out->version = version;
+    out->reserved = 0;
     return ZC_OK;
 }
 
@@ -183,7 +200,7 @@ namespace {
 // (chunk_base is set by the caller).
 int make_tensor(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
                 uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
-                TensorDesc &d) {
+                uint32_t version, TensorDesc &d) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZC_EINVAL;
     if (ndim < 0 || ndim > 8 || (ndim > 0 && !h_shape)) return ZC_EINVAL;
     const int W = word_bytes(dtype);
@@ -197,7 +214,8 @@ int make_tensor(const void *d_src, const void *d_base, uint64_t nbytes, int dtyp
     if (!d_blob || !d_blob_bytes || (nbytes && !d_src)) return ZC_EINVAL;
     if (!aligned(d_src, W) || !aligned(d_blob, 16) || !aligned(d_blob_bytes, 8)) return ZC_EINVAL;
     const uint64_t nc = chunks_of(nbytes, chunk_bytes);
-    if (blob_capacity < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc) return ZC_ECAPACITY;
+    const uint64_t planes = version == 2 ? 512ull * W : 0;  // v2: the plane tables
+    if (blob_capacity < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc + planes) return ZC_ECAPACITY;
     d = TensorDesc{};
     d.src = static_cast<const uint8_t *>(d_src);
     d.base = static_cast<const uint8_t *>(d_base);
@@ -208,7 +226,7 @@ int make_tensor(const void *d_src, const void *d_base, uint64_t nbytes, int dtyp
     d.n_chunks = uint32_t(nc);
     uint8_t head[ZC_HEADER_BYTES] = {};
     std::memcpy(head, "ZCNN", 4);
-    head[4] = 1;
+    head[4] = uint8_t(version);
     head[6] = uint8_t(dtype);
     head[7] = uint8_t(ndim);
     put32(head + 8, chunk_bytes);
@@ -217,7 +235,12 @@ int make_tensor(const void *d_src, const void *d_base, uint64_t nbytes, int dtyp
     put64(head + 16, nbytes);
     put32(head + 24, uint32_t(nc));
     for (int dd = 0; dd < ndim; dd++) put64(head + 32 + 8 * dd, uint64_t(h_shape[dd]));
-    if (nc == 0) put32(head + 28, host_crc32(head, ZC_HEADER_BYTES) ^ 0xFFFFFFFFu);
+    if (nc == 0) {  // the whole blob is the header (v2: and zero plane tables)
+        uint32_t reg = host_crc32(head, ZC_HEADER_BYTES);
+        static const uint8_t zeros[512] = {};
+        for (uint64_t z = 0; z < planes; z += 512) reg = host_crc32(zeros, 512, reg);
+        put32(head + 28, reg ^ 0xFFFFFFFFu);
+    }
     std::memcpy(d.header, head, ZC_HEADER_BYTES);
     return ZC_OK;
 }
@@ -305,41 +328,56 @@ int resolve_blob(BlobDesc &d) {
 // statistics and the coding warps' slots.
 uint64_t ctrl_bytes(uint64_t n) { return kCtrlBytes + pad256(16 * n); }
 uint64_t table_bytes(uint64_t n) { return n > 1 ? pad256(sizeof(TensorDesc) * n) : 0; }
+// v2: per tensor and plane, 256 u64 counts, then the 512-byte tables
+uint64_t hist_bytes(uint64_t n, int W, uint32_t version) { return version == 2 ? pad256(2048ull * W * n) : 0; }
+uint64_t ptab_bytes(uint64_t n, int W, uint32_t version) { return version == 2 ? pad256(512ull * W * n) : 0; }
 
-uint64_t ws_size(uint64_t n, uint64_t nc, int W, uint32_t chunk_bytes) {
-    if (nc == 0) return ctrl_bytes(n) + table_bytes(n);
-    const uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+// max_tc: the most chunks of one tensor (v2 waves hold whole tensors)
+uint64_t ws_size(uint64_t n, uint64_t nc, int W, uint32_t chunk_bytes, uint32_t version, uint64_t max_tc) {
+    const uint64_t head = ctrl_bytes(n) + table_bytes(n) + hist_bytes(n, W, version) + ptab_bytes(n, W, version);
+    if (nc == 0) return head;
+    uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+    if (version == 2 && wave < max_tc) wave = max_tc;
     // every coding warp for thresholds up to 1; at least one warp for any
     // threshold (larger thresholds then run fewer warps)
     uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0);
     const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9);
     if (slots < one_any) slots = one_any;
-    return ctrl_bytes(n) + table_bytes(n) + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
+    return head + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
 }
 
 // Lay out the workspace and launch the statistics + coding waves over the
 // call's chunks. `table` holds the n > 1 tensors (copied to the workspace).
 int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta, int dtype, uint32_t chunk_bytes,
-                 double threshold, void *d_ws, uint64_t ws_bytes, cudaStream_t s) {
+                 double threshold, uint32_t version, void *d_ws, uint64_t ws_bytes, cudaStream_t s) {
     const int W = word_bytes(dtype);
     const uint64_t nc = a.total_chunks;
     a.n_tensors = n;
     a.chunk_bytes = chunk_bytes;
     a.threshold = threshold;
+    a.version = version;
     if (!d_ws || !aligned(d_ws, 16)) return ZC_EINVAL;
     const uint64_t head = ctrl_bytes(n) + table_bytes(n);
-    const uint64_t fixed = head + pad256(8 * nc);
+    const uint64_t planes = hist_bytes(n, W, version) + ptab_bytes(n, W, version);
+    const uint64_t fixed = head + planes + pad256(8 * nc);
     if (ws_bytes < fixed) return ZC_ECAPACITY;
     a.ws_ctrl = static_cast<uint8_t *>(d_ws);
     a.tensors = n > 1 ? reinterpret_cast<const TensorDesc *>(a.ws_ctrl + ctrl_bytes(n)) : nullptr;
-    a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + head);
+    a.ws_hist = version == 2 ? reinterpret_cast<unsigned long long *>(a.ws_ctrl + head) : nullptr;
+    a.ws_ptab = version == 2 ? a.ws_ctrl + head + hist_bytes(n, W, version) : nullptr;
+    a.ws_status = reinterpret_cast<unsigned long long *>(a.ws_ctrl + head + planes);
     if (cudaMemsetAsync(d_ws, 0, fixed, s) != cudaSuccess) return ZC_ECUDA;
     if (n > 1) {
         const int st = upload_table(table, sizeof(TensorDesc) * n, const_cast<TensorDesc *>(a.tensors), s);
         if (st != ZC_OK) return st;
     }
     bool any_empty = false;
-    for (uint32_t t = 0; t < n; t++) any_empty |= (n == 1 ? a.one : table[t]).n_chunks == 0;
+    uint64_t max_tc = 0;
+    for (uint32_t t = 0; t < n; t++) {
+        const uint32_t tc = (n == 1 ? a.one : table[t]).n_chunks;
+        any_empty |= tc == 0;
+        max_tc = tc > max_tc ? tc : max_tc;
+    }
     if (any_empty) {
         const int st = launch_empty_blobs(a, s);
         if (st != ZC_OK) return st;
@@ -348,6 +386,7 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
 
     const uint64_t slot = slot_bytes(chunk_bytes, W, threshold);
     uint64_t wave = wave_chunks(nc, chunk_bytes, W);
+    if (version == 2 && wave < max_tc) wave = max_tc;
     uint64_t workers = max_workers(nc);
     const uint64_t avail = ws_bytes - fixed;
     if (wave_layout(wave, W, chunk_bytes).slots + workers * slot > avail) {
@@ -359,39 +398,68 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
             workers = 1;
             const uint64_t per_chunk = kInfoBytes + (kTableBytes + n_pad(chunk_bytes, W)) * uint64_t(W);
             wave = avail > slot + 768 ? (avail - slot - 768) / per_chunk : 0;
-            if (wave == 0) return ZC_ECAPACITY;
+            if (wave == 0 || (version == 2 && wave < max_tc)) return ZC_ECAPACITY;
         }
     }
     const WaveLayout lay = wave_layout(wave, W, chunk_bytes);
-    a.ws_info = a.ws_ctrl + fixed + lay.info;
-    a.ws_ftab = a.ws_ctrl + fixed + lay.ftab;
-    a.ws_cand = a.ws_ctrl + fixed + lay.cand;
+    const uint64_t area0 = fixed;
+    a.ws_info = a.ws_ctrl + area0 + lay.info;
+    a.ws_ftab = a.ws_ctrl + area0 + lay.ftab;
+    a.ws_cand = a.ws_ctrl + area0 + lay.cand;
     a.n_pad = n_pad(chunk_bytes, W);
-    a.ws_slots = a.ws_ctrl + fixed + lay.slots;
+    a.ws_slots = a.ws_ctrl + area0 + lay.slots;
     a.slot_bytes = slot;
     a.rec_stride = rec_stride(chunk_bytes, W, threshold);
     a.workers = uint32_t(workers < wave ? workers : wave);
-    for (uint64_t w0 = 0; w0 < nc; w0 += wave) {
-        a.wave_start = uint32_t(w0);
-        a.wave_n = uint32_t(nc - w0 < wave ? nc - w0 : wave);
+    if (version == 1) {
+        for (uint64_t w0 = 0; w0 < nc; w0 += wave) {
+            a.wave_start = uint32_t(w0);
+            a.wave_n = uint32_t(nc - w0 < wave ? nc - w0 : wave);
+            const int st = launch_encode_wave(dtype, delta, a, s);
+            if (st != ZC_OK) return st;
+        }
+        return ZC_OK;
+    }
+    // v2: a wave is a run of whole tensors, so that every tensor's plane
+    // counts are complete before any of its chunks is coded
+    uint32_t t = 0;
+    while (t < n) {
+        const uint32_t t0 = t;
+        uint64_t chunks = 0;
+        while (t < n) {
+            const uint64_t tc = (n == 1 ? a.one : table[t]).n_chunks;
+            if (t > t0 && chunks + tc > wave) break;
+            chunks += tc;
+            t++;
+        }
+        if (chunks == 0) continue;  // empty tensors only
+        a.wave_start = (n == 1 ? a.one : table[t0]).chunk_base;
+        a.wave_n = uint32_t(chunks);
+        a.wave_t0 = t0;
+        a.wave_t1 = t;
+        a.workers = uint32_t(workers < chunks ? workers : chunks);
         const int st = launch_encode_wave(dtype, delta, a, s);
         if (st != ZC_OK) return st;
     }
     return ZC_OK;
 }
 
+uint32_t version_of(uint32_t flags) { return (flags & ZC_SHARED_TABLES) ? 2u : 1u; }
+
 int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
                   uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity,
-                  uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
-    if (!d_status) return ZC_EINVAL;
+                  uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream,
+                  uint32_t flags = 0) {
+    if (!d_status || (flags & ~ZC_SHARED_TABLES)) return ZC_EINVAL;
+    const uint32_t version = version_of(flags);
     EncodeArgs a{};
     const int st = make_tensor(d_src, d_base, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob,
-                               blob_capacity, d_blob_bytes, a.one);
+                               blob_capacity, d_blob_bytes, version, a.one);
     if (st != ZC_OK) return st;
     if (resolve_tensor(a.one) != ZC_OK) return ZC_EINVAL;
     a.total_chunks = a.one.n_chunks;
     a.d_status = d_status;
-    return run_compress(a, nullptr, 1, d_base != nullptr, dtype, chunk_bytes, threshold, d_ws, ws_bytes,
+    return run_compress(a, nullptr, 1, d_base != nullptr, dtype, chunk_bytes, threshold, version, d_ws, ws_bytes,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -403,7 +471,9 @@ int make_blob(const void *d_blob, const zc_info *info, const void *d_base, void 
     const int W = word_bytes(info->dtype);
     if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
     if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
-    if (info->blob_bytes < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks) return ZC_EINVAL;
+    if (info->version != 1 && info->version != 2) return ZC_EINVAL;
+    const uint64_t planes = info->version == 2 ? 512ull * W : 0;  // v2: the plane tables
+    if (info->blob_bytes < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks + planes) return ZC_EINVAL;
     if (dst_capacity < info->nbytes || (info->nbytes && !d_dst)) return ZC_ECAPACITY;
     if (!aligned(d_blob, 16) || !aligned(d_dst, W)) return ZC_EINVAL;
     d = BlobDesc{};
@@ -429,6 +499,11 @@ int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base,
     a.chunk_bytes = info->chunk_bytes;
     a.flags = flags;
     a.d_status = d_status;
+    a.version = info->version;
+    if (a.version == 2) {  // CTAs of a.pairs chunks
+        a.pairs = decode_v2_pairs(a.total_chunks);
+        a.n_ctas = (a.total_chunks + a.pairs - 1) / a.pairs;
+    }
     return launch_decode(info->dtype, d_base != nullptr, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -436,21 +511,45 @@ bool delta_dtype(int dtype) { return dtype == ZC_U8 || dtype == ZC_U16 || dtype 
 
 } // namespace
 
-extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes) {
-    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95)) return 0;
-    return ws_size(1, chunks_of(nbytes, chunk_bytes), word_bytes(dtype), chunk_bytes);
+extern "C" uint64_t zc_workspace_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, uint32_t flags) {
+    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95) || (flags & ~ZC_SHARED_TABLES)) return 0;
+    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
+    return ws_size(1, nc, word_bytes(dtype), chunk_bytes, version_of(flags), nc);
 }
 
-extern "C" uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes) {
+extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes) {
+    return zc_workspace_size_ex(nbytes, dtype, chunk_bytes, 0);
+}
+
+extern "C" uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes,
+                                            uint32_t flags) {
+    if (flags & ~ZC_SHARED_TABLES) return 0;
     if (n == 0) return kCtrlBytes;
     if (!nbytes) return 0;
-    uint64_t nc = 0;
+    uint64_t nc = 0, max_tc = 0;
     for (uint32_t t = 0; t < n; t++) {
         if (!valid_params(nbytes[t], dtype, chunk_bytes, 0.95)) return 0;
-        nc += chunks_of(nbytes[t], chunk_bytes);
+        const uint64_t tc = chunks_of(nbytes[t], chunk_bytes);
+        nc += tc;
+        max_tc = tc > max_tc ? tc : max_tc;
     }
     if (nc > 0xFFFFFFFFull) return 0;
-    return ws_size(n, nc, word_bytes(dtype), chunk_bytes);
+    return ws_size(n, nc, word_bytes(dtype), chunk_bytes, version_of(flags), max_tc);
+}
+
+extern "C" uint64_t zc_blob_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold,
+                                    uint32_t flags) {
+    if (flags & ~ZC_SHARED_TABLES) return 0;
+    const uint64_t b = zc_blob_size(nbytes, dtype, chunk_bytes, threshold);
+    return b && version_of(flags) == 2 ? b + 512ull * word_bytes(dtype) : b;
+}
+
+extern "C" int zc_compress_ex(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                              uint32_t chunk_bytes, double threshold, uint32_t flags,
+                              void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                              void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    return compress_impl(d_src, nullptr, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob, blob_capacity,
+                         d_blob_bytes, d_ws, ws_bytes, d_status, stream, flags);
 }
 
 extern "C" int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
@@ -490,9 +589,11 @@ extern "C" uint64_t zc_decompress_workspace_size_batch(uint32_t n) {
 
 extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const void *const *d_bases,
                                  const uint64_t *nbytes, int dtype, const int32_t *ndims, const int64_t *shapes,
-                                 uint32_t chunk_bytes, double threshold, void *const *d_blobs,
+                                 uint32_t chunk_bytes, double threshold, uint32_t flags, void *const *d_blobs,
                                  const uint64_t *blob_capacities, uint64_t *d_blob_bytes, void *d_ws,
                                  uint64_t ws_bytes, int32_t *d_status, void *stream) {
+    if (flags & ~ZC_SHARED_TABLES) return ZC_EINVAL;
+    const uint32_t version = version_of(flags);
     if (n == 0) return ZC_OK;
     if (!d_srcs || !nbytes || !ndims || !shapes || !d_blobs || !blob_capacities || !d_blob_bytes || !d_status)
         return ZC_EINVAL;
@@ -507,7 +608,7 @@ extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const vo
         }
         const int st = make_tensor(d_srcs[t], base, nbytes[t], dtype, ndims[t], shapes + 8 * uint64_t(t),
                                    chunk_bytes, threshold, d_blobs[t], blob_capacities[t], d_blob_bytes + t,
-                                   table[t]);
+                                   version, table[t]);
         if (st != ZC_OK) return st;
         table[t].chunk_base = uint32_t(nc);
         nc += table[t].n_chunks;
@@ -519,8 +620,8 @@ extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const vo
     if (n == 1) a.one = table[0];
     a.total_chunks = uint32_t(nc);
     a.d_status = d_status;
-    return run_compress(a, table.data(), n, d_bases != nullptr, dtype, chunk_bytes, threshold, d_ws, ws_bytes,
-                        static_cast<cudaStream_t>(stream));
+    return run_compress(a, table.data(), n, d_bases != nullptr, dtype, chunk_bytes, threshold, version, d_ws,
+                        ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const zc_info *infos,
@@ -530,13 +631,14 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
     if (!d_blobs || !infos || !d_dsts || !dst_capacities || !d_status) return ZC_EINVAL;
     if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
     const int dtype = infos[0].dtype;
-    const uint32_t chunk_bytes = infos[0].chunk_bytes;
+    const uint32_t chunk_bytes = infos[0].chunk_bytes, version = infos[0].version;
     if (d_bases && !delta_dtype(dtype)) return ZC_EINVAL;
     if (n > 1 && (!d_ws || !aligned(d_ws, 16) || ws_bytes < zc_decompress_workspace_size_batch(n))) return ZC_EINVAL;
     std::vector<BlobDesc> table(n);
     uint64_t nc = 0;
     for (uint32_t t = 0; t < n; t++) {
-        if (infos[t].dtype != dtype || infos[t].chunk_bytes != chunk_bytes) return ZC_EINVAL;
+        if (infos[t].dtype != dtype || infos[t].chunk_bytes != chunk_bytes || infos[t].version != version)
+            return ZC_EINVAL;
         const void *base = nullptr;
         if (d_bases && infos[t].nbytes) {
             base = d_bases[t];
@@ -552,6 +654,17 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
         if (resolve_blob(d) != ZC_OK) return ZC_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DecodeArgs a{};
+    a.version = version;
+    if (version == 2) {  // CTAs of a.pairs chunks of one blob each
+        a.pairs = decode_v2_pairs(nc);
+        uint64_t ctas = 0;
+        for (auto &d : table) {
+            d.cta_base = uint32_t(ctas);
+            ctas += (d.n_chunks + a.pairs - 1) / a.pairs;
+        }
+        if (ctas > 0x7FFFFFFFull) return ZC_EINVAL;
+        a.n_ctas = uint32_t(ctas);
+    }
     if (n == 1) a.one = table[0];
     else {
         const int st = upload_table(table.data(), sizeof(BlobDesc) * n, d_ws, s);

@@ -40,6 +40,11 @@ struct EncodeArgs {
     uint32_t wave_start;            // first chunk of this wave (call-wide index)
     uint32_t wave_n;                // chunks in this wave
     uint32_t workers;               // coding warps
+    // format v2 (shared plane tables): a wave holds whole tensors [wave_t0, wave_t1)
+    uint32_t version;               // 1 or 2
+    uint32_t wave_t0, wave_t1;
+    unsigned long long *ws_hist;    // v2: per tensor and plane, 256 u64 counts over the tensor
+    uint8_t *ws_ptab;               // v2: per tensor and plane, the 12-bit table (256 u16)
 };
 
 // One blob of a decompression call.
@@ -51,6 +56,8 @@ struct BlobDesc {
     uint64_t nbytes;
     uint32_t n_chunks;
     uint32_t chunk_base;            // call-wide index of its first chunk
+    uint32_t cta_base;              // v2: index of the blob's first CTA (CTAs never span blobs)
+    uint32_t pad_;
 };
 
 struct DecodeArgs {
@@ -61,6 +68,9 @@ struct DecodeArgs {
     uint32_t chunk_bytes;
     uint32_t flags;
     int32_t *d_status;
+    uint32_t version;               // 1 or 2 (every blob of the call)
+    uint32_t pairs;                 // v2: chunks (warp pairs) per CTA
+    uint32_t n_ctas;                // v2: CTAs of the call
 };
 
 struct CrcArgs {
@@ -76,8 +86,13 @@ struct CrcArgs {
 // Statistics and coding kernels for chunks [wave_start, wave_start + wave_n)
 // (total_chunks > 0).
 int launch_encode_wave(int dtype, bool delta, const EncodeArgs &a, cudaStream_t s);
-// The blobs (header alone) of the call's tensors that have no chunks.
+// The blobs (header alone; v2: and zero plane tables) of the call's tensors
+// that have no chunks.
 int launch_empty_blobs(const EncodeArgs &a, cudaStream_t s);
+// v2: the plane tables of the wave's tensors (after its statistics kernel).
+int launch_plane_tables(int dtype, const EncodeArgs &a, cudaStream_t s);
+// v2 decoding: CTAs of `pairs` chunks each, never spanning two blobs.
+uint32_t decode_v2_pairs(uint64_t total_chunks);
 
 // The tensor (blob) of a call-wide chunk index: the last one whose first
 // chunk is at or before it (binary search over the table).

@@ -77,6 +77,9 @@ enum zc_status {
 
 /* zc_decompress flag: skip the per-chunk CRC-32 check. */
 #define ZC_NO_VERIFY 1u
+/* compression flag: blob format v2 (one 12-bit table per byte plane of the
+ * tensor, shared by all its chunks; lmzip "Building on lmz") */
+#define ZC_SHARED_TABLES 2u
 
 /* Parameter limits of format v1. */
 #define ZC_MIN_CHUNK 64u
@@ -93,6 +96,8 @@ typedef struct {
     uint64_t blob_bytes;  /* total blob length */
     uint32_t n_chunks;
     uint32_t chunk_bytes;
+    uint32_t version;     /* blob format: 1 (a table per coded stream) or 2 (shared plane tables) */
+    uint32_t reserved;
 } zc_info;
 
 /* Worst-case blob length for compressing nbytes of dtype with these
@@ -198,6 +203,7 @@ ZC_API int zc_decompress_delta(const void *d_blob, const zc_info *info, const vo
  *   d_blobs[t], blob_capacities[t]
  *                      blob t (16-byte aligned) and its capacity, as in
  *                      zc_compress
+ *   flags              0 (format v1) or ZC_SHARED_TABLES (format v2, below)
  *   d_blob_bytes       DEVICE array of n uint64: entry t receives blob t's size
  *   d_ws, ws_bytes     ws_bytes >= zc_workspace_size_batch(nbytes, n, ...)
  *   d_status           one device int32 for the whole call
@@ -207,13 +213,14 @@ ZC_API int zc_decompress_delta(const void *d_blob, const zc_info *info, const vo
  * arguments are invalid, and zc_compress's other codes. */
 ZC_API int zc_compress_batch(uint32_t n, const void *const *d_srcs, const void *const *d_bases,
                              const uint64_t *nbytes, int dtype, const int32_t *ndims, const int64_t *shapes,
-                             uint32_t chunk_bytes, double threshold, void *const *d_blobs,
+                             uint32_t chunk_bytes, double threshold, uint32_t flags, void *const *d_blobs,
                              const uint64_t *blob_capacities, uint64_t *d_blob_bytes, void *d_ws,
                              uint64_t ws_bytes, int32_t *d_status, void *stream);
 
-/* Workspace bytes for zc_compress_batch of n tensors of the given sizes
- * (0 if a size or the parameters are invalid). Host only. */
-ZC_API uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes);
+/* Workspace bytes for zc_compress_batch of n tensors of the given sizes and
+ * flags (0 if a size or the parameters are invalid). Host only. */
+ZC_API uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes,
+                                        uint32_t flags);
 
 /* Batched decompression of n blobs of one dtype and chunk size in one grid,
  * each output byte-identical to zc_decompress (or, with d_bases,
@@ -233,6 +240,28 @@ ZC_API int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const zc_
 
 /* Workspace bytes for zc_decompress_batch of n blobs (the descriptor table). */
 ZC_API uint64_t zc_decompress_workspace_size_batch(uint32_t n);
+
+/* Format v2: shared plane tables (lmzip "Building on lmz": one frequency
+ * table per plane kind for many chunks). With flags = ZC_SHARED_TABLES the
+ * compressor writes blob version 2: the W plane tables (256 u16 each: the
+ * 12-bit table of stream j over the whole tensor, zeros for a plane with
+ * fewer than two symbols) follow the chunk table and are covered by the
+ * header CRC, and rANS records hold only the lane states and the words.
+ * Every other rule (grouping, CONST/RAW/RANS choice per stream, the chunk
+ * threshold, CRCs) is that of v1. zc_decompress, zc_decompress_delta and
+ * zc_decompress_batch read both versions (zc_info.version); a batch must
+ * not mix them. The decoder builds each plane's one-level table once per
+ * CTA and shares it among the CTA's chunks.
+ *   zc_compress_ex        zc_compress with flags (0 or ZC_SHARED_TABLES)
+ *   zc_workspace_size_ex  its workspace (v2 holds a whole tensor's
+ *                         statistics in one wave)
+ *   zc_blob_size_ex       worst-case blob bytes (v2 adds 512 W) */
+ZC_API int zc_compress_ex(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
+                          uint32_t chunk_bytes, double threshold, uint32_t flags,
+                          void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
+                          void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream);
+ZC_API uint64_t zc_workspace_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, uint32_t flags);
+ZC_API uint64_t zc_blob_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, uint32_t flags);
 
 /* zlib-compatible CRC-32 of each piece_bytes-byte piece of a device buffer,
  * the last piece possibly shorter (cuZipNN API hash_tensor_with_crc32,

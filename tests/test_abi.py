@@ -99,6 +99,7 @@ def test_delta_entry_points_reject_bad_arguments_on_the_host():
     info.dtype, info.ndim, info.nbytes, info.n_chunks, info.chunk_bytes = zc.BF16, 1, 2048, 1, 4096
     info.shape[0] = 1024
     info.blob_bytes = 1 << 12
+    info.version = 1
     assert L.zc_decompress_delta(aligned, ctypes.byref(info), aligned, aligned, 2048, 0, aligned, None) == zc.EINVAL
     info.dtype = zc.U16
     assert L.zc_decompress_delta(aligned, ctypes.byref(info), odd, aligned, 2048, 0, aligned, None) == zc.EINVAL
@@ -117,10 +118,12 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
     ndims = (ctypes.c_int32 * 2)(1, 1)
     shapes = (ctypes.c_int64 * 16)(*([1024] + [0] * 7 + [1024] + [0] * 7))
 
-    def comp(n, srcs, bases, nbytes, dtype, nd=ndims):
-        return L.zc_compress_batch(n, srcs, bases, nbytes, dtype, nd, shapes, 4096, 0.95, vp2(aligned, aligned),
-                                   u64_2(1 << 16, 1 << 16), aligned, aligned, 1 << 24, aligned, None)
+    def comp(n, srcs, bases, nbytes, dtype, nd=ndims, flags=0):
+        return L.zc_compress_batch(n, srcs, bases, nbytes, dtype, nd, shapes, 4096, 0.95, flags,
+                                   vp2(aligned, aligned), u64_2(1 << 16, 1 << 16), aligned, aligned, 1 << 24,
+                                   aligned, None)
     assert comp(0, None, None, None, zc.BF16) == zc.OK
+    assert comp(0, None, None, None, zc.BF16, flags=4) == zc.EINVAL   # unknown flag
     assert comp(2, None, None, u64_2(2048, 2048), zc.BF16) == zc.EINVAL
     # deltas only for unsigned word dtypes
     assert comp(2, vp2(aligned, aligned), vp2(aligned, aligned), u64_2(2048, 2048), zc.BF16) == zc.EINVAL
@@ -135,6 +138,7 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
         infos[i].nbytes = 2048 if dt == zc.BF16 else 4096
         infos[i].shape[0] = 1024
         infos[i].blob_bytes = 1 << 12
+        infos[i].version = 1
     caps = u64_2(1 << 16, 1 << 16)
     ws = zc.decompress_workspace_size_batch(2)
     assert ws >= 2 * 48 and zc.decompress_workspace_size_batch(1) == 0
@@ -150,4 +154,6 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
                                  0, aligned, ws, aligned, None) == zc.ECAPACITY
     assert L.zc_decompress_batch(0, None, None, None, None, None, 0, None, 0, None, None) == zc.OK
     assert zc.workspace_size_batch([2048, 3], zc.BF16, 4096) == 0
+    assert zc.workspace_size_batch([2048, 0], zc.BF16, 4096, zc.SHARED_TABLES) > 0
+    assert zc.blob_size(2048, zc.BF16, 4096, 0.95, zc.SHARED_TABLES) == zc.blob_size(2048, zc.BF16, 4096) + 1024
     assert zc.workspace_size_batch([2048, 0], zc.BF16, 4096) > 0
