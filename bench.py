@@ -47,6 +47,8 @@ def _args():
     p.add_argument("--threshold", type=float, default=0.95)
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-verify", action="store_true", help="decode without the CRC check")
+    p.add_argument("--shared-tables", action="store_true",
+                   help="blob format v2: one table per byte plane of each tensor (ZC_SHARED_TABLES)")
     return p.parse_args()
 
 
@@ -86,16 +88,30 @@ MODEL_WORKLOADS = {
 }
 
 
-def encode_launches(n_chunks: int, word: int, chunk_bytes: int) -> int:
-    """Kernels one compression call of n_chunks launches: a statistics and a
-    coding kernel per wave, a wave holding at most 2 GiB of per-chunk
-    statistics (32 + W (512 + n_pad) bytes a chunk), as the library plans it
-    with a full-size workspace."""
-    if n_chunks == 0:
-        return 1  # the empty-blob kernel
+def encode_launches(tensor_chunks, word: int, chunk_bytes: int, v2: bool = False) -> int:
+    """Kernels one compression call over tensors of these chunk counts
+    launches, as the library plans it with a full-size workspace: a wave
+    holds at most 2 GiB of per-chunk statistics (32 + W (512 + n_pad) bytes a
+    chunk; v2: at least the largest tensor, and only whole tensors); each wave
+    is a statistics and a coding kernel (v2: and a plane-table kernel); the
+    empty tensors' blobs take one more kernel."""
+    nc = sum(tensor_chunks)
+    empty = 1 if 0 in tensor_chunks else 0
+    if nc == 0:
+        return empty
     n_pad = (chunk_bytes // word + 31) // 32 * 32
-    wave = min(n_chunks, (2048 << 20) // (32 + word * (512 + n_pad)))
-    return 2 * ((n_chunks + wave - 1) // wave)
+    wave = min(nc, (2048 << 20) // (32 + word * (512 + n_pad)))
+    if not v2:
+        return empty + 2 * ((nc + wave - 1) // wave)
+    wave = max(wave, max(tensor_chunks))
+    waves, t, n = 0, 0, len(tensor_chunks)
+    while t < n:
+        t0, chunks = t, 0
+        while t < n and (t == t0 or chunks + tensor_chunks[t] <= wave):
+            chunks += tensor_chunks[t]
+            t += 1
+        waves += 1 if chunks else 0
+    return empty + 3 * waves
 
 
 def peaks():
@@ -262,6 +278,7 @@ def run_model(a, world, rank, local, dev, stream):
     from entropy_coding_gb300 import workloads as wl
 
     batched = a.workload == "llama8b_batch"
+    flags = zc.SHARED_TABLES if a.shared_tables else 0
     specs = wl.llama8b_specs()
     C, thr, code, Wd = a.chunk_bytes, a.threshold, wl.BF16, 2
     sizes = [2 * int(torch.Size(sh).numel()) for _, sh in specs]
@@ -281,7 +298,7 @@ def run_model(a, world, rank, local, dev, stream):
         d.copy_(wl.as_bytes(wl.llama8b_tensor(i, nm, sh, dev)))
     out_all = torch.empty(s_total, dtype=torch.uint8, device=dev)
     outs = [out_all[o: o + x] for o, x in zip(s_offs, sizes)]
-    caps = [zc.blob_size(x, code, C, thr) for x in sizes]
+    caps = [zc.blob_size(x, code, C, thr, flags) for x in sizes]
     b_offs, b_total = layout(caps)
     blob_all = torch.empty(b_total, dtype=torch.uint8, device=dev)
     blobs = [blob_all[o: o + x] for o, x in zip(b_offs, caps)]
@@ -289,21 +306,21 @@ def run_model(a, world, rank, local, dev, stream):
     nb = torch.zeros(n, dtype=torch.int64, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     if batched:
-        ws = torch.empty(zc.workspace_size_batch(sizes, code, C), dtype=torch.uint8, device=dev)
+        ws = torch.empty(zc.workspace_size_batch(sizes, code, C, flags), dtype=torch.uint8, device=dev)
         n_dws = zc.decompress_workspace_size_batch(n)
         dws = torch.empty(max(16, n_dws), dtype=torch.uint8, device=dev)
     else:
-        ws = torch.empty(max(zc.workspace_size(x, code, C) for x in sizes), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(zc.workspace_size(x, code, C, flags) for x in sizes), dtype=torch.uint8, device=dev)
     N = sum(sizes)
     verify = not a.no_verify
 
     def comp(inputs, blobs=blobs, nb=nb):
         if batched:
-            zc.compress_batch_into(inputs, blobs, nb, ws, st, code, shapes, C, thr, stream)
+            zc.compress_batch_into(inputs, blobs, nb, ws, st, code, shapes, C, thr, stream, flags=flags)
         else:
             for t in range(n):
                 zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws, st, C, thr, stream, dtype=code,
-                                 shape=shapes[t])
+                                 shape=shapes[t], flags=flags)
 
     def decomp(infos, blobs=blobs):
         if batched:
@@ -318,7 +335,8 @@ def run_model(a, world, rank, local, dev, stream):
     assert int(st.item()) == 0
     lens = nb.tolist()
     S = sum(lens)
-    infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C)].cpu()) for b, x in zip(blobs, sizes)]
+    planes = 512 * Wd if flags else 0  # v2: the plane tables follow the chunk table
+    infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C) + planes].cpu()) for b, x in zip(blobs, sizes)]
     with torch.cuda.stream(stream):
         decomp(infos)
     stream.synchronize()
@@ -396,7 +414,7 @@ def run_model(a, world, rank, local, dev, stream):
             comp(srcs, hb_blobs, hb_nb)
         stream.synchronize()
         got = hb_nb.tolist()
-        hb_infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C)]) for b, x in zip(hb_blobs, sizes)]
+        hb_infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C) + planes]) for b, x in zip(hb_blobs, sizes)]
         with torch.cuda.stream(stream):
             decomp(hb_infos, [b[:k] for b, k in zip(hb_blobs, got)])
             h_out.copy_(out_all, non_blocking=True)
@@ -417,10 +435,10 @@ def run_model(a, world, rank, local, dev, stream):
     chunks = [(x + C - 1) // C for x in sizes]
     if batched:
         table_launches = lambda words: (words + 7679) // 7680
-        per_step = (encode_launches(sum(chunks), Wd, C) + table_launches(38 * n) + (1 if 0 in sizes else 0)
+        per_step = (encode_launches(chunks, Wd, C, bool(flags)) + table_launches(38 * n)
                     + 1 + table_launches(14 * n))
     else:
-        per_step = sum(encode_launches(c, Wd, C) + (1 if c else 0) for c in chunks)
+        per_step = sum(encode_launches([c], Wd, C, bool(flags)) + (1 if c else 0) for c in chunks)
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
         "value": round(world * N * a.steps / total / 1e9, 3), "unit": "GB/s",
@@ -429,6 +447,7 @@ def run_model(a, world, rank, local, dev, stream):
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": a.workload, "desc": MODEL_WORKLOADS[a.workload], "nbytes": N, "tensors": n,
                    "chunk_bytes": C, "threshold": thr, "verify_crc_on_decode": verify,
+                   "format": "v2 (shared plane tables)" if flags else "v1 (a table per coded stream)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "encode": {"gbs": round(N * a.steps / t_enc / 1e9, 2), "roofline_frac": round(enc_ach / hbm, 4),
                    "ms": round(1e3 * t_enc / a.steps, 4)},
@@ -488,9 +507,11 @@ def main():
         base, src = wl.as_bytes(ta), wl.as_bytes(tb)
     N = src.numel()
     C, thr = a.chunk_bytes, a.threshold
-    cap = zc.blob_size(N, code, C, thr)
+    flags = zc.SHARED_TABLES if a.shared_tables else 0
+    planes = 512 * (N // max(1, t.numel())) if flags else 0  # v2: the plane tables follow the chunk table
+    cap = zc.blob_size(N, code, C, thr, flags)
     blob = torch.empty(cap, dtype=torch.uint8, device=dev)
-    ws = torch.empty(zc.workspace_size(N, code, C), dtype=torch.uint8, device=dev)
+    ws = torch.empty(zc.workspace_size(N, code, C, flags), dtype=torch.uint8, device=dev)
     nb = torch.zeros(1, dtype=torch.int64, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty(N, dtype=torch.uint8, device=dev)
@@ -498,7 +519,9 @@ def main():
 
     def comp(inp, blob=blob, nb=nb):
         if base is None:
-            zc.compress_into(inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
+            zc.compress_into(inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape, flags=flags)
+        elif flags:  # a v2 delta goes through the batched entry point (a batch of one)
+            zc.compress_batch_into([inp], [blob], nb, ws, st, code, [shape], C, thr, stream, bases=[base], flags=flags)
         else:
             zc.compress_delta_into(base, inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
 
@@ -514,7 +537,7 @@ def main():
     stream.synchronize()
     S = int(nb.item())
     assert int(st.item()) == 0
-    info = zc.blob_info(blob[: 96 + 16 * ((N + C - 1) // C)].cpu())
+    info = zc.blob_info(blob[: 96 + 16 * ((N + C - 1) // C) + planes].cpu())
     with torch.cuda.stream(stream):
         decomp(info)
     stream.synchronize()
@@ -597,7 +620,7 @@ def main():
             comp(d_in, hb_blob, hb_nb)
         stream.synchronize()
         s_bytes = int(hb_nb.item())
-        hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C)])
+        hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C) + planes])
         with torch.cuda.stream(stream):
             decomp(hb_info, hb_blob[:s_bytes])
             h_out.copy_(out, non_blocking=True)
@@ -619,7 +642,7 @@ def main():
                 comp(h_src, hb_blob, hb_nb)
             stream.synchronize()
             s_bytes = int(hb_nb.item())
-            hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C)])
+            hb_info = zc.blob_info(hb_blob[: 96 + 16 * ((N + C - 1) // C) + planes])
             with torch.cuda.stream(stream):
                 decomp(hb_info, hb_blob[:s_bytes], h_out)
             stream.synchronize()
@@ -656,6 +679,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": a.workload, "desc": desc, "nbytes": N, "chunk_bytes": C, "threshold": thr,
                    "verify_crc_on_decode": not a.no_verify, "l2": "inputs larger than L2 (no flush)",
+                   "format": "v2 (shared plane tables)" if flags else "v1 (a table per coded stream)",
                    "parallelism": f"replicas x{world}"},
         "encode": {"gbs": round(enc_gbs, 2), "roofline_frac": round(enc_ach / hbm, 4),
                    "ms": round(1e3 * t_enc / a.steps, 4)},
@@ -673,7 +697,8 @@ def main():
                           "h2d_bytes_per_step": hb_h2d // a.e2e_steps, "d2h_bytes_per_step": hb_d2h // a.e2e_steps,
                           "mode": "blob written to and decoded from pinned host memory by the kernels"},
         "e2e_zero_copy": zc_line,
-        "gpu_launches": 3 * a.steps,  # stats_kernel + code_kernel + decode_kernel per step
+        # stats_kernel + code_kernel (v2: + plane_kernel) + decode_kernel per step
+        "gpu_launches": (encode_launches([(N + C - 1) // C], N // max(1, t.numel()), C, bool(flags)) + 1) * a.steps,
     }
     line["cpu_baseline"] = cpu_baseline(t, code, a)
     print(json.dumps(line), flush=True)

@@ -375,6 +375,7 @@ struct StatsSmem {
     uint32_t gapu[4][256];           // the same for 16-byte pieces (unaligned inputs)
     uint32_t hist[W][128 * 32];
     uint32_t cnt[W][256];            // merged counts
+    uint32_t plane[W][256];          // v2: counts of this CTA's recent chunks of one tensor, per plane
     uint32_t s_reg[kStatWarps];
 };
 
@@ -538,7 +539,7 @@ __device__ void merge_counts(StatsSmem<W> &sm) {
 // candidate's 12-bit table goes to ftab (256 u16).
 template <int W>
 __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *counts, uint32_t *sv, uint8_t *ftab,
-                           unsigned long long *hist) {
+                           uint32_t *plane) {
     const int lane = threadIdx.x & 31;
     uint32_t cnt[8];
     const uint4 c0 = reinterpret_cast<const uint4 *>(counts)[2 * lane];
@@ -551,8 +552,8 @@ __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *coun
         if (cnt[k]) {
             pres++;
             only = 8 * lane + k;
-            // v2: the chunk's counts join its tensor's plane histogram
-            if (hist) atomicAdd(hist + 8 * lane + k, (unsigned long long)cnt[k]);
+            // v2: the chunk's counts join the CTA's count of the plane
+            if (plane) plane[8 * lane + k] += cnt[k];
         }
     const uint32_t k_total = warp_sum_u32(pres);
     uint32_t mode, val;
@@ -560,7 +561,7 @@ __device__ bool plan_stats(const EncodeArgs &a, uint32_t n, const uint32_t *coun
         const uint32_t who = __ballot_sync(kFull, pres != 0);
         mode = kModeConst;
         val = __shfl_sync(kFull, only, __ffs(who) - 1);
-    } else if (hist) {
+    } else if (plane) {
         // v2: the table is the tensor's, not known yet. Its cost is at least
         // the chunk's own order-0 information n H (Gibbs' inequality: no
         // table codes the chunk below its empirical entropy), so the bound
@@ -675,6 +676,21 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     load_shift_smem(sm.gap, kSh16352);
     load_shift_smem(sm.gapu, gap_table<kStatThreads>());
     for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
+    for (int i = tid; i < W * 256; i += kStatThreads) (&sm.plane[0][0])[i] = 0;
+    // v2: warp j < W adds stream j's counts into sm.plane[j] for tensor cur_t
+    // and moves them to the tensor's plane histogram in global memory when
+    // the tensor changes, every 4096 chunks (32-bit counters) and at the end
+    uint32_t cur_t = 0xFFFFFFFFu, since = 0;
+    auto flush = [&](uint32_t t) {
+        unsigned long long *h = a.ws_hist + (uint64_t(t) * W + warp) * 256;
+        uint32_t *row = sm.plane[warp];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const uint32_t v = row[8 * (tid & 31) + k];
+            if (v) atomicAdd(h + 8 * (tid & 31) + k, (unsigned long long)v);
+            row[8 * (tid & 31) + k] = 0;
+        }
+    };
     __syncthreads();
     for (uint32_t cl = blockIdx.x; cl < a.wave_n; cl += gridDim.x) {
         const uint32_t g = a.wave_start + cl;
@@ -694,13 +710,19 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
         // the other warps go on to the next chunk: the counters were zeroed by
         // the merge, and the next merge comes after the next barrier
         if (warp < W) {
-            unsigned long long *hist =
-                a.version == 2 ? a.ws_hist + (uint64_t(tv.t) * W + warp) * 256 : nullptr;
+            if (a.version == 2 && (tv.t != cur_t || since == 4096)) {
+                if (cur_t != 0xFFFFFFFFu) flush(cur_t);
+                cur_t = tv.t;
+                since = 0;
+            }
+            since++;
             const bool cand_j = plan_stats<W>(a, len / W, sm.cnt[warp], info + 1 + warp,
-                                              a.ws_ftab + (uint64_t(cl) * W + warp) * 512, hist);
+                                              a.ws_ftab + (uint64_t(cl) * W + warp) * 512,
+                                              a.version == 2 ? sm.plane[warp] : nullptr);
             if (warp > 0 && cand_j) warp_write_cand<DT, kDelta>(src, len, warp, cand + uint64_t(warp) * a.n_pad);
         }
     }
+    if (warp < W && cur_t != 0xFFFFFFFFu) flush(cur_t);  // v2 only: cur_t is set only there
 }
 
 // ---------------------------------------------------------------- coding
