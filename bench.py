@@ -114,6 +114,26 @@ def encode_launches(tensor_chunks, word: int, chunk_bytes: int, v2: bool = False
     return empty + 3 * waves
 
 
+def max_over_ranks(vals, device) -> list:
+    """Per-rank timings reduced to their maximum over all ranks (replicas:
+    the job takes as long as its slowest rank), followed by a barrier; the
+    values unchanged with one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(vals)
+    t = torch.tensor(list(vals), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return t.tolist()
+
+
+def replica_value(units_per_rank: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput of independent replicas: the units every rank
+    processed over the slowest rank's time."""
+    return world * units_per_rank * steps / seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -365,11 +385,7 @@ def run_model(a, world, rank, local, dev, stream):
     t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     assert int(st.item()) == 0 and nb.tolist() == lens
     total = t_enc + t_dec
-    if world > 1:
-        tt = torch.tensor([total, t_enc, t_dec], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total, t_enc, t_dec = tt.tolist()
-        dist.barrier()
+    total, t_enc, t_dec = max_over_ranks([total, t_enc, t_dec], dev)
 
     # end to end through the public calls: the model from pinned host memory,
     # the blobs back to the host and up again, the restored model to the host
@@ -441,7 +457,7 @@ def run_model(a, world, rank, local, dev, stream):
         per_step = sum(encode_launches([c], Wd, C, bool(flags)) + (1 if c else 0) for c in chunks)
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
-        "value": round(world * N * a.steps / total / 1e9, 3), "unit": "GB/s",
+        "value": round(replica_value(N, a.steps, world, total) / 1e9, 3), "unit": "GB/s",
         "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
@@ -568,11 +584,7 @@ def main():
     t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     assert int(st.item()) == 0 and int(nb.item()) == S
     total = t_enc + t_dec
-    if world > 1:
-        tt = torch.tensor([total, t_enc, t_dec], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total, t_enc, t_dec = tt.tolist()
-        dist.barrier()
+    total, t_enc, t_dec = max_over_ranks([total, t_enc, t_dec], dev)
 
     # end to end through the public calls, host (pinned) buffers in and out
     h_src = torch.empty(N, dtype=torch.uint8, pin_memory=True)
@@ -673,7 +685,7 @@ def main():
     traffic = profiled_traffic(dominant, a.workload)
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
-        "value": round(world * N * a.steps / total / 1e9, 3), "unit": "GB/s",
+        "value": round(replica_value(N, a.steps, world, total) / 1e9, 3), "unit": "GB/s",
         "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
