@@ -449,6 +449,7 @@ def run_model(a, world, rank, local, dev, stream):
     enc_ach = alg * a.steps / t_enc / 1e9
     dec_ach = alg * a.steps / t_dec / 1e9
     chunks = [(x + C - 1) // C for x in sizes]
+    dec_kernel = "decode_v2_kernel" if flags else "decode_kernel"
     if batched:
         table_launches = lambda words: (words + 7679) // 7680
         per_step = (encode_launches(chunks, Wd, C, bool(flags)) + table_launches(38 * n)
@@ -470,9 +471,9 @@ def run_model(a, world, rank, local, dev, stream):
         "decode": {"gbs": round(N * a.steps / t_dec / 1e9, 2), "roofline_frac": round(dec_ach / hbm, 4),
                    "ms": round(1e3 * t_dec / a.steps, 4)},
         "size_pct": round(100.0 * S / N, 3),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(dec_ach, 1), "peak": hbm,
+        "roofline": {"bound": "hbm", "kernel": dec_kernel, "achieved": round(dec_ach, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
-                     "traffic": profiled_traffic("decode_kernel", a.workload),
+                     "traffic": profiled_traffic(dec_kernel, a.workload),
                      "algorithmic_bytes_per_launch": alg if batched else None,
                      "note": "decompression time of the whole model (one decode_kernel launch when batched)"},
         "clocks": clk.summary(),
@@ -680,7 +681,7 @@ def main():
     # the decompression call is one kernel (decode_kernel), the largest single
     # kernel of the step; compression is two (statistics, coding), each
     # shorter (profiles/launches_*.md), so the live roofline is decode's
-    dominant = "decode_kernel"
+    dominant = "decode_v2_kernel" if flags else "decode_kernel"
     ach = dec_ach
     traffic = profiled_traffic(dominant, a.workload)
     line = {
