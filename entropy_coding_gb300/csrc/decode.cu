@@ -33,15 +33,15 @@ namespace zc {
 
 namespace {
 
-constexpr int kPairs = 8;                 // chunks per CTA at most, one warp pair each
+constexpr int kPairs = 16;                // chunks per CTA at most, one warp pair each (one CTA per SM)
 constexpr int kThreads = 64 * kPairs;
-constexpr int kCtasPerSM = 2;
 constexpr uint64_t kBigPairs = 7;        // pairs per CTA at most with one-level tables (one CTA per SM)
 constexpr int kStages = 4;                // symbol groups in flight within a pair
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
-// CRC slicing tables + shift tables: one group's output (256 W bytes) and
-// the 496-byte gap
-constexpr uint32_t kCrcSmem = kCrcRepWords * 4 + 2 * 4 * 256 * 4;
+// CRC slicing tables (C copies) + shift tables: one group's output (256 W
+// bytes) and the 496-byte gap
+template <int C>
+constexpr uint32_t crc_smem() { return crc_rep_words<C>() * 4 + 2 * 4 * 256 * 4; }
 constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
 constexpr uint32_t kV2Pairs = 16;             // v2: chunks per CTA at most (one CTA per SM)
 constexpr int kV2Threads = 64 * kV2Pairs;
@@ -412,12 +412,12 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
 // piece taken from zero (linearity); the lanes are folded at the end
 // (crc_fold) and the elements after the last whole group are added from the
 // output.
-template <int DT, bool kVerify, bool kDelta, class PS>
+template <int DT, bool kVerify, bool kDelta, int C, class PS>
 __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
                         const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
-    const uint32_t *row = crc_row(crc_rep);
+    const uint32_t *row = crc_row<C>(crc_rep);
     const uint32_t groups = cx.groups;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(cx.out) & 15) == 0;
     if (cx.have_main) {
@@ -499,7 +499,8 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
                 v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
             }
-            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(crc_rep16(cin, v[0], row), v[1], row);
+            if constexpr (kVerify)
+                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16<C>(crc_rep16<C>(cin, v[0], row), v[1], row);
             if constexpr (kDelta) {
                 v[0] = xb(v[0], bv[0]);
                 v[1] = xb(v[1], bv[1]);
@@ -519,7 +520,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
             v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
             v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
-            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16(cin, v, row);
+            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16<C>(cin, v, row);
             if constexpr (kDelta) v = xb(v, bv[0]);
             if (vec_ok) {
                 *reinterpret_cast<uint4 *>(cx.out + 2ull * e0) = v;
@@ -533,7 +534,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             }
         } else {
             if constexpr (kVerify) {
-                const uint32_t piece = crc_rep_word(crc_rep_word(cin, col[0].lo, row), col[0].hi, row);
+                const uint32_t piece = crc_rep_word<C>(crc_rep_word<C>(cin, col[0].lo, row), col[0].hi, row);
                 Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ piece;
             }
             if constexpr (kDelta) {
@@ -584,9 +585,9 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
         if constexpr (kDelta) {
             // the check is of the decoded bytes, before the XOR (only the last,
             // partial chunk has elements after its whole groups)
-            for (uint32_t i = done; i < cx.len; i++) reg = crc_rep_byte(reg, __ldcg(cx.out + i) ^ cx.base[i], row);
+            for (uint32_t i = done; i < cx.len; i++) reg = crc_rep_byte<C>(reg, __ldcg(cx.out + i) ^ cx.base[i], row);
         } else {
-            reg = crc_any<1, true>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
+            reg = crc_any<1, true, C>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
         }
         if ((reg ^ 0xFFFFFFFFu) != expect_crc && lane == 0) status_or(a.d_status, ZC_ECRC);
     }
@@ -594,7 +595,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
 
 // Chunk c of blob bd, by one warp pair (kV2: format v2, with the CTA's
 // plane tables pbig).
-template <int DT, bool kBig, bool kDelta, bool kV2, class PS>
+template <int DT, bool kBig, bool kDelta, bool kV2, int C, class PS>
 __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c, bool producer, PS &ps,
                              const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256],
                              const uint32_t *const *pbig) {
@@ -644,7 +645,7 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
         }
         for (uint32_t i = nvec * 16 + lane; i < len; i += 32) out[i] = kDelta ? uint8_t(p[i] ^ basec[i]) : p[i];
         // a RAW chunk stores the original bytes, so its CRC is the payload's
-        if (verify && (crc_strided<1, false>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
+        if (verify && (crc_strided<1, false, C>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
             lane == 0)
             status_or(a.d_status, ZC_ECRC);
         return;
@@ -666,23 +667,27 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
     if (producer) {
         if (cx.have_main) produce<DT, kBig, kV2>(a, cx, ps, pbig);
     } else if (verify) {
-        consume<DT, true, kDelta>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
+        consume<DT, true, kDelta, C>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     } else {
-        consume<DT, false, kDelta>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
+        consume<DT, false, kDelta, C>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     }
 }
 
+// One CTA per SM. With one-level tables (kBig: few chunks per SM, 16 KB of
+// table per pair) the CRC tables have 8 copies; with two-level tables (up
+// to 16 pairs) they have 16, so fewer lanes meet on a bank.
 template <int DT, bool kBig, bool kDelta>
-__global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int W = WordOf<DT>::W;
+    constexpr int C = kBig ? 8 : 16;
     uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
-    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
-    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
-    PairSmem<kBig> *pairs = reinterpret_cast<PairSmem<kBig> *>(smem + kCrcSmem);
+    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + crc_rep_words<C>() * 4);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + crc_rep_words<C>() * 4 + 4 * 256 * 4);
+    PairSmem<kBig> *pairs = reinterpret_cast<PairSmem<kBig> *>(smem + crc_smem<C>());
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
-        load_crc_rep(crc_rep);
+        load_crc_rep<C>(crc_rep);
         load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
         load_shift_smem(gap496, kSh496);
     }
@@ -700,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM) decode_kernel(DecodeArgs
     if (g >= a.total_chunks) return;
     // the blob of this call-wide chunk index
     const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
-    decode_chunk<DT, kBig, kDelta, false>(a, bd, g - bd.chunk_base, (warp & 1) == 0, pairs[warp >> 1], crc_rep,
-                                          gshift, gap496, nullptr);
+    decode_chunk<DT, kBig, kDelta, false, C>(a, bd, g - bd.chunk_base, (warp & 1) == 0, pairs[warp >> 1], crc_rep,
+                                             gshift, gap496, nullptr);
 }
 
 // Format v2 (shared plane tables): a CTA decodes up to a.pairs consecutive
@@ -715,10 +720,11 @@ template <int DT, bool kDelta>
 __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int W = WordOf<DT>::W;
+    constexpr int C = 16;  // CRC table copies
     uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
-    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4);
-    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + kCrcRepWords * 4 + 4 * 256 * 4);
-    uint32_t *big = reinterpret_cast<uint32_t *>(smem + kCrcSmem);  // W x 4096
+    uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + crc_rep_words<C>() * 4);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + crc_rep_words<C>() * 4 + 4 * 256 * 4);
+    uint32_t *big = reinterpret_cast<uint32_t *>(smem + crc_smem<C>());  // W x 4096
     uint32_t *symcum = big + W * kM;                                  // W x 256: f | cum << 12
     uint32_t *pvalid = symcum + W * 256;                              // W flags (padded to 16 bytes)
     PairSmemV2 *pairs = reinterpret_cast<PairSmemV2 *>(pvalid + 4);
@@ -739,7 +745,7 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
     const uint32_t first = (blockIdx.x - bd.cta_base) * a.pairs;
 
     if (!(a.flags & ZC_NO_VERIFY)) {
-        load_crc_rep(crc_rep);
+        load_crc_rep<C>(crc_rep);
         load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
         load_shift_smem(gap496, kSh496);
     }
@@ -804,14 +810,16 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
     const uint32_t *pbig[4] = {nullptr, nullptr, nullptr, nullptr};
 #pragma unroll
     for (int j = 0; j < W; j++) pbig[j] = pvalid[j] ? big + j * kM : nullptr;
-    decode_chunk<DT, true, kDelta, true>(a, bd, first + pair, (warp & 1) == 0, pairs[pair], crc_rep, gshift, gap496,
-                                         pbig);
+    decode_chunk<DT, true, kDelta, true, C>(a, bd, first + pair, (warp & 1) == 0, pairs[pair], crc_rep, gshift,
+                                            gap496, pbig);
 }
 
 template <int DT, bool kBig, bool kDelta>
 int launch_decode_mode(const DecodeArgs &a, uint32_t pc, cudaStream_t s) {
-    const size_t smem = kCrcSmem + size_t(pc) * sizeof(PairSmem<kBig>);
-    const size_t smem_max = kCrcSmem + size_t(kPairs) * sizeof(PairSmem<kBig>);
+    constexpr int C = kBig ? 8 : 16;
+    constexpr size_t most = kBig ? kBigPairs : kPairs;
+    const size_t smem = crc_smem<C>() + size_t(pc) * sizeof(PairSmem<kBig>);
+    const size_t smem_max = crc_smem<C>() + most * sizeof(PairSmem<kBig>);
     if (cudaFuncSetAttribute(decode_kernel<DT, kBig, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(std::min<size_t>(smem_max, 227 * 1024))) != cudaSuccess)
         return ZC_ECUDA;
@@ -825,24 +833,21 @@ int launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ECUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ZC_ECUDA;
-    // Few chunks per SM (the rANS chains are then the critical path): one CTA
-    // per SM holding all its chunks, with one-level tables. Many: pairs per
-    // CTA just enough for kCtasPerSM CTAs per SM to hold every chunk, with
-    // the smaller two-level tables. Either way the chunks spread evenly over
-    // the SMs.
+    // One CTA per SM holding the SM's share of the chunks. Few chunks per SM
+    // (the rANS chains are then the critical path): one-level tables. Many:
+    // the smaller two-level tables, up to kPairs chunks per CTA. Either way
+    // the chunks spread evenly over the SMs.
     const uint64_t per_sm = (a.total_chunks + sms - 1) / uint64_t(sms);
     if (per_sm <= kBigPairs)
         return launch_decode_mode<DT, true, kDelta>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
-    const uint64_t slots = uint64_t(sms) * kCtasPerSM;
-    const uint32_t pc = uint32_t(std::min<uint64_t>(kPairs, (a.total_chunks + slots - 1) / slots));
-    return launch_decode_mode<DT, false, kDelta>(a, pc, s);
+    return launch_decode_mode<DT, false, kDelta>(a, uint32_t(std::min<uint64_t>(kPairs, per_sm)), s);
 }
 
 template <int DT, bool kDelta>
 int launch_decode_v2_t(const DecodeArgs &a, cudaStream_t s) {
     constexpr int W = WordOf<DT>::W;
     if (a.pairs == 0 || a.pairs > kV2Pairs || a.n_ctas == 0) return ZC_EINVAL;
-    const size_t fixed = kCrcSmem + size_t(W) * (kM * 4 + 256 * 4) + 16;
+    const size_t fixed = crc_smem<16>() + size_t(W) * (kM * 4 + 256 * 4) + 16;
     const size_t smem = fixed + size_t(a.pairs) * sizeof(PairSmemV2);
     const size_t smem_max = fixed + size_t(kV2Pairs) * sizeof(PairSmemV2);
     if (cudaFuncSetAttribute(decode_v2_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,

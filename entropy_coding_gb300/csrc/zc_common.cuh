@@ -199,36 +199,49 @@ __device__ inline uint32_t shift_bytes(uint32_t c, uint64_t n) {
 // The CRC tables in shared memory for slicing by four (Kounavis and Berry,
 // 2005): table k holds the register contribution of byte b followed by k zero
 // bytes (kCrc.t[k]), so a 32-bit word is four independent lookups instead of a
-// chain of four. Eight copies interleaved word by word: entry (k, b) of copy r
-// is word (256 k + b) * 8 + r and lane l reads copy l & 7, so a lookup
-// instruction meets at most four lanes per bank. 32 KB per CTA.
-constexpr uint32_t kCrcRepWords = 4 * 256 * 8;
+// chain of four. C copies interleaved word by word: entry (k, b) of copy r is
+// word (256 k + b) * C + r and lane l reads copy l % C, so a lookup
+// instruction meets at most 32 / C lanes per bank. 4 C KB per CTA (C = 8:
+// 32 KB; the decoders that run one CTA per SM take 16 copies, 64 KB, which
+// halves the lanes that can collide on a bank).
+template <int C = 8>
+constexpr uint32_t crc_rep_words() { return 4u * 256u * C; }
+constexpr uint32_t kCrcRepWords = crc_rep_words<8>();
 
+template <int C = 8>
 __device__ inline void load_crc_rep(uint32_t *t) {
-    for (uint32_t i = threadIdx.x; i < kCrcRepWords; i += blockDim.x) t[i] = kCrc.t[i >> 11][(i >> 3) & 0xFFu];
+    static_assert(C == 8 || C == 16, "8 or 16 table copies");
+    constexpr int LC = C == 8 ? 3 : 4;
+    for (uint32_t i = threadIdx.x; i < crc_rep_words<C>(); i += blockDim.x)
+        t[i] = kCrc.t[i >> (8 + LC)][(i >> LC) & 0xFFu];
 }
 
 // This lane's copy of the tables.
-__device__ __forceinline__ const uint32_t *crc_row(const uint32_t *t) { return t + (threadIdx.x & 7); }
+template <int C = 8>
+__device__ __forceinline__ const uint32_t *crc_row(const uint32_t *t) { return t + (threadIdx.x & (C - 1)); }
 
 // Sarwate's byte step (table 0); row = crc_row(table)
+template <int C = 8>
 __device__ __forceinline__ uint32_t crc_rep_byte(uint32_t c, uint32_t byte, const uint32_t *row) {
-    return row[((c ^ byte) & 0xFFu) << 3] ^ (c >> 8);
+    return row[((c ^ byte) & 0xFFu) * C] ^ (c >> 8);
 }
 
 // Register update over a little-endian 32-bit word: with u = c ^ w, byte i of
 // u is followed by 3 - i more bytes of the word.
+template <int C = 8>
 __device__ __forceinline__ uint32_t crc_rep_word(uint32_t c, uint32_t w, const uint32_t *row) {
     const uint32_t u = c ^ w;
-    return row[3 * 2048 + ((u & 0xFFu) << 3)] ^ row[2 * 2048 + (((u >> 8) & 0xFFu) << 3)] ^
-           row[1 * 2048 + (((u >> 16) & 0xFFu) << 3)] ^ row[(u >> 24) << 3];
+    constexpr uint32_t S = 256u * C;  // one slice table
+    return row[3 * S + (u & 0xFFu) * C] ^ row[2 * S + ((u >> 8) & 0xFFu) * C] ^
+           row[1 * S + ((u >> 16) & 0xFFu) * C] ^ row[(u >> 24) * C];
 }
 
+template <int C = 8>
 __device__ __forceinline__ uint32_t crc_rep16(uint32_t c, uint4 v, const uint32_t *row) {
-    c = crc_rep_word(c, v.x, row);
-    c = crc_rep_word(c, v.y, row);
-    c = crc_rep_word(c, v.z, row);
-    return crc_rep_word(c, v.w, row);
+    c = crc_rep_word<C>(c, v.x, row);
+    c = crc_rep_word<C>(c, v.y, row);
+    c = crc_rep_word<C>(c, v.z, row);
+    return crc_rep_word<C>(c, v.w, row);
 }
 
 template <bool kLdcg>
@@ -292,13 +305,13 @@ __device__ inline uint32_t crc_fold(uint32_t R, int log2_piece, uint32_t *s_reg)
 // with the gap table G = gap_table<NT>() in shared memory, T is the
 // replicated byte table. The last len % 16 bytes are added by every thread.
 // p must be 16-byte aligned. Every thread of the group calls it.
-template <int NW, bool kLdcg>
+template <int NW, bool kLdcg, int C = 8>
 __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
                                        const uint32_t (*G)[256], uint32_t *s_reg) {
     constexpr int NT = 32 * NW;
     static_assert(NT == 32 || NT == 128 || NT == 256 || NT == 512, "strided CRC runs on 1, 4, 8 or 16 warps");
     const int tid = NW == 1 ? int(threadIdx.x & 31) : int(threadIdx.x);
-    const uint32_t *row = crc_row(T);
+    const uint32_t *row = crc_row<C>(T);
     const uint64_t main = len & ~uint64_t(15);
     const Strided sp(main, NT);
     uint32_t reg = init;
@@ -310,28 +323,28 @@ __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t 
             uint4 nxt = make_uint4(0, 0, 0, 0);
             if (r + 1 < sp.rounds) nxt = load16<kLdcg>(p + 16 * (pidx + NT));
             uint32_t c = r == 0 ? (pidx == 0 ? init : 0u) : shift_smem(R, G);
-            if (pidx >= 0) c = crc_rep16(c, cur, row);
+            if (pidx >= 0) c = crc_rep16<C>(c, cur, row);
             R = c;
             cur = nxt;
             pidx += NT;
         }
         reg = crc_fold<NW>(R, 4, s_reg);
     }
-    for (uint64_t i = main; i < len; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
+    for (uint64_t i = main; i < len; i++) reg = crc_rep_byte<C>(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
     return reg;
 }
 
 // As crc_strided, for a range that need not be 16-byte aligned: the bytes up
 // to the first 16-byte boundary are taken one at a time first.
-template <int NW, bool kLdcg>
+template <int NW, bool kLdcg, int C = 8>
 __device__ inline uint32_t crc_any(const uint8_t *p, uint64_t len, uint32_t init, const uint32_t *T,
                                    const uint32_t (*G)[256], uint32_t *s_reg) {
     uint64_t head = (16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15;
     if (head > len) head = len;
-    const uint32_t *row = crc_row(T);
+    const uint32_t *row = crc_row<C>(T);
     uint32_t reg = init;
-    for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
-    return crc_strided<NW, kLdcg>(p + head, len - head, reg, T, G, s_reg);
+    for (uint64_t i = 0; i < head; i++) reg = crc_rep_byte<C>(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
+    return crc_strided<NW, kLdcg, C>(p + head, len - head, reg, T, G, s_reg);
 }
 
 // One 32-byte read-only global load (p 32-byte aligned) as two 16-byte halves.
