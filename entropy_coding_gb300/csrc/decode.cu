@@ -245,6 +245,11 @@ __device__ bool rans_setup_shared(const uint8_t *rec, uint32_t val, const uint32
 // One rANS decode step of the warp: returns this lane's symbol.
 template <bool kBig>
 __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt) {
+    // lane l's candidate is the (l + 1)-th word from the top, read before the
+    // table so that the load is off the state's chain; the lane with p
+    // emitting lanes below it takes lane p's (the range read is the same
+    // ring range as a direct read of the word: blocks b - 1 .. b)
+    const uint32_t wl = r.ring[uint32_t(r.ptr - 1 - int32_t(threadIdx.x & 31)) & (kRingWords - 1)];
     const uint32_t slot = r.x & (kM - 1);
     uint32_t s, xn;
     if constexpr (kBig) {
@@ -258,9 +263,7 @@ __device__ __forceinline__ uint32_t rans_step(Rans &r, bool active, uint32_t lt)
     }
     const bool need = active && xn < kRansL;
     const uint32_t bal = __ballot_sync(kFull, need);
-    // every lane reads its candidate word (in bounds of the ring), so no branch
-    const int32_t idx = r.ptr - 1 - int32_t(__popc(bal & lt));
-    const uint32_t w = r.ring[uint32_t(idx) & (kRingWords - 1)];
+    const uint32_t w = __shfl_sync(kFull, wl, __popc(bal & lt));
     xn = need ? ((xn << 16) | w) : xn;
     if (active) r.x = xn;
     r.ptr -= int32_t(__popc(bal));
