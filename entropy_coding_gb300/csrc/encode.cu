@@ -672,6 +672,9 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     StatsSmem<W> &sm = *reinterpret_cast<StatsSmem<W> *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
+    // the coding kernel's chunk ticket starts from zero in every wave (the
+    // previous wave's coding kernel has finished: same stream)
+    if (blockIdx.x == 0 && tid == 0) reinterpret_cast<uint32_t *>(a.ws_ctrl)[0] = 0;
     load_crc_rep(sm.crc_rep);
     load_shift_smem(sm.gap, kSh16352);
     load_shift_smem(sm.gapu, gap_table<kStatThreads>());
@@ -1246,7 +1249,6 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
         const int st = launch_plane_tables(DT, a, s);
         if (st != ZC_OK) return st;
     }
-    if (cudaMemsetAsync(a.ws_ctrl, 0, 4, s) != cudaSuccess) return ZC_ECUDA;  // coder ticket
     // the warps spread evenly over the SMs: CTAs of just enough warps for one
     // CTA per SM (the block scheduler then gives every SM the same share)
     const int sms = sms_of_device() < 1 ? 1 : sms_of_device();
