@@ -186,3 +186,39 @@ def test_v2_corrupted_plane_table_is_reported(zco):
         zc.decompress_into(b, info, out, st)
         torch.cuda.synchronize()
         assert int(st.item()) & (zc.ECORRUPT | zc.ECRC), mutate
+
+
+def test_v2_small_workspace_waves_at_tensor_boundaries(zco):
+    """A batch whose workspace holds 40 chunks of statistics and one coding
+    warp: the v2 waves hold whole tensors ([9, 0, 2], [30, 1], [12] chunks),
+    so every tensor's plane tables are complete before it is coded."""
+    rng = np.random.default_rng(23)
+    dtype, chunk, W = 6, 4096, 4
+    sizes = [9000, 0, 1500, 30000, 100, 12000]
+    raws = [_bytes(rng, dtype, n, k % 3) for k, n in enumerate(sizes)]
+    n = len(raws)
+    nc = sum((r.size + chunk - 1) // chunk for r in raws)
+    pad = lambda x: (x + 255) // 256 * 256
+    n_pad = (chunk // W + 31) // 32 * 32
+    per_chunk = 32 + W * (512 + n_pad)
+    fixed = (256 + pad(16 * n)) + pad(152 * n) + pad(2048 * W * n) + pad(512 * W * n) + pad(8 * nc)
+    rec = min(160 + 512 + 2 * (chunk // W), int(np.ceil(0.95 * (chunk // W))) + 160 + 512 + 2048)
+    slot = pad(W * ((rec + 15) // 16 * 16 + 16))
+    small = fixed + 40 * per_chunk + slot + 768
+    full = zc.workspace_size_batch([r.size for r in raws], dtype, chunk, V2)
+    assert small < full
+    srcs = [torch.from_numpy(r).to(DEV) if r.size else torch.empty(0, dtype=torch.uint8, device=DEV) for r in raws]
+    blobs = [torch.full((zc.blob_size(r.size, dtype, chunk, 0.95, V2),), 0xAB, dtype=torch.uint8, device=DEV)
+             for r in raws]
+    ws = torch.full((small,), 0x5A, dtype=torch.uint8, device=DEV)
+    nb = torch.zeros(n, dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    zc.compress_batch_into(srcs, blobs, nb, ws, st, dtype, [(r.size // W,) for r in raws], chunk, 0.95, flags=V2)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for r, b, k in zip(raws, blobs, nb.tolist()):
+        got = b[:k].cpu().numpy().tobytes()
+        assert got == zco.compress(r, dtype, (r.size // W,), chunk, 0.95, version=2)
+        if r.size:
+            s2, back = gpu_decode(got)
+            assert s2 == 0 and back == r.tobytes()
