@@ -29,7 +29,7 @@ __device__ uint32_t warp_crc_raw_any(const uint8_t *p, uint64_t len, uint32_t in
 }
 
 __global__ void __launch_bounds__(kWarps * 32) crc_kernel(CrcArgs a) {
-    __shared__ uint32_t tab[kCrcRepWords];
+    __shared__ __align__(16) uint32_t tab[kCrcRepWords];
     __shared__ uint32_t gap[4][256];
     load_crc_rep(tab);
     load_shift_smem(gap, gap_table<32>());

@@ -730,7 +730,8 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
     uint32_t *big = reinterpret_cast<uint32_t *>(smem + crc_smem<C>());  // W x 4096
     uint32_t *symcum = big + W * kM;                                  // W x 256: f | cum << 12
     uint32_t *pvalid = symcum + W * 256;                              // W flags (padded to 16 bytes)
-    PairSmemV2 *pairs = reinterpret_cast<PairSmemV2 *>(pvalid + 4);
+    uint8_t *luts = reinterpret_cast<uint8_t *>(pvalid + 4);           // W x 4096: slot -> symbol, scratch
+    PairSmemV2 *pairs = reinterpret_cast<PairSmemV2 *>(luts + W * kM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // the blob: the last one whose first CTA is at or before this one
@@ -790,22 +791,28 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
         if (lane == 0) pvalid[j] = ok ? 1u : 0u;
     }
     __syncthreads();
-    // slot -> symbol: the last symbol whose range starts at or before the slot
-    // (a symbol of frequency 0 shares its start with the next one, and the
-    // last range ends at 4096, so the search always lands on a symbol with
-    // f > 0 for a valid table)
+    // slot -> symbol bytes, laid out by runs (a thread per plane and symbol,
+    // whole words where a run covers them), then each slot's entry from its
+    // symbol: two independent reads per slot. A valid table's runs tile
+    // [0, 4096) exactly.
+    for (uint32_t i = threadIdx.x; i < uint32_t(W) * 256; i += blockDim.x) {
+        const uint32_t j = i >> 8, sy = i & 255;
+        if (!pvalid[j]) continue;
+        const uint32_t e = symcum[i];
+        uint8_t *lut = luts + j * kM;
+        uint32_t s = e >> 12;
+        const uint32_t end = s + (e & 0xFFFu);
+        for (; s < end && (s & 3); s++) lut[s] = uint8_t(sy);
+        for (; s + 4 <= end; s += 4) *reinterpret_cast<uint32_t *>(lut + s) = sy * 0x01010101u;
+        for (; s < end; s++) lut[s] = uint8_t(sy);
+    }
+    __syncthreads();
     for (uint32_t i = threadIdx.x; i < uint32_t(W) * kM; i += blockDim.x) {
         const uint32_t j = i / kM, slot = i % kM;
         if (!pvalid[j]) continue;
-        const uint32_t *sc = symcum + j * 256;
-        uint32_t lo = 0, hi = 256;
-        while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if ((sc[mid] >> 12) <= slot) lo = mid;
-            else hi = mid;
-        }
-        const uint32_t e = sc[lo];
-        big[i] = lo | (e & 0xFFFu) << 8 | (slot - (e >> 12)) << 20;
+        const uint32_t sy = luts[i];
+        const uint32_t e = symcum[j * 256 + sy];
+        big[i] = sy | (e & 0xFFFu) << 8 | (slot - (e >> 12)) << 20;
     }
     __syncthreads();
     const uint32_t pair = uint32_t(warp >> 1);
@@ -850,7 +857,7 @@ template <int DT, bool kDelta>
 int launch_decode_v2_t(const DecodeArgs &a, cudaStream_t s) {
     constexpr int W = WordOf<DT>::W;
     if (a.pairs == 0 || a.pairs > kV2Pairs || a.n_ctas == 0) return ZC_EINVAL;
-    const size_t fixed = crc_smem<16>() + size_t(W) * (kM * 4 + 256 * 4) + 16;
+    const size_t fixed = crc_smem<16>() + size_t(W) * (kM * 4 + 256 * 4) + 16 + size_t(W) * kM;
     const size_t smem = fixed + size_t(a.pairs) * sizeof(PairSmemV2);
     const size_t smem_max = fixed + size_t(kV2Pairs) * sizeof(PairSmemV2);
     if (cudaFuncSetAttribute(decode_v2_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -208,12 +208,18 @@ template <int C = 8>
 constexpr uint32_t crc_rep_words() { return 4u * 256u * C; }
 constexpr uint32_t kCrcRepWords = crc_rep_words<8>();
 
+// Fill the copies: each of the 1024 table entries is read once and written
+// as C consecutive words (16-byte stores; t 16-byte aligned), so a CTA reads
+// 4 KB of tables whatever C is.
 template <int C = 8>
 __device__ inline void load_crc_rep(uint32_t *t) {
     static_assert(C == 8 || C == 16, "8 or 16 table copies");
-    constexpr int LC = C == 8 ? 3 : 4;
-    for (uint32_t i = threadIdx.x; i < crc_rep_words<C>(); i += blockDim.x)
-        t[i] = kCrc.t[i >> (8 + LC)][(i >> LC) & 0xFFu];
+    for (uint32_t e = threadIdx.x; e < 4 * 256; e += blockDim.x) {
+        const uint32_t v = kCrc.t[e >> 8][e & 0xFFu];
+        uint4 *d = reinterpret_cast<uint4 *>(t + e * C);
+#pragma unroll
+        for (int q = 0; q < C / 4; q++) d[q] = make_uint4(v, v, v, v);
+    }
 }
 
 // This lane's copy of the tables.
