@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint64)]
             L.zco_decompress.restype = ctypes.c_int
             L.zco_decompress.argtypes = [c_u8p, ctypes.c_uint64, c_u8p, ctypes.c_uint64, ctypes.c_uint32]
+            L.zco_verify.restype = ctypes.c_int
+            L.zco_verify.argtypes = [c_u8p, ctypes.c_uint64]
             L.zco_normalize64.restype = ctypes.c_int
             L.zco_normalize64.argtypes = [c_u8p, ctypes.c_uint64, c_u8p]
             L.zco_plane_tables.restype = ctypes.c_int
@@ -280,3 +282,12 @@ def decompress(blob: bytes, flags: int = 0) -> np.ndarray:
     if st:
         raise OracleError(st, "decompress")
     return out
+
+
+def verify(blob: bytes) -> int:
+    """Status of checking a blob's header, table and chunk CRCs without
+    decoding it (0 = intact)."""
+    b = np.frombuffer(blob, np.uint8)
+    if b.size == 0:
+        return EFORMAT
+    return int(lib().zco_verify(_ptr(b), b.size))

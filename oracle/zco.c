@@ -24,7 +24,8 @@
  *              field read as zero
  *   32   64    shape[8] as int64, unused dims zero
  *   96   16*n  chunk table: u64 offset, u32 stored | raw_flag << 31,
- *              u32 CRC-32 of the chunk's original (uncompressed) bytes
+ *              u32 CRC-32 of the chunk's stored payload bytes (the
+ *              `stored` bytes at `offset`, without the padding after them)
  *   then each chunk's payload in chunk order, zero-padded to 16 bytes;
  *   offset_0 = 96 + 16n, offset_{c+1} = offset_c + pad16(stored_c).
  *
@@ -696,7 +697,7 @@ static int compress_shared(const uint8_t *src, uint64_t nbytes, int dtype, int n
         uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * c;
         put64(e, off);
         put32(e + 8, (uint32_t)stored | ((uint32_t)raw << 31));
-        put32(e + 12, zco_crc32(src + c * (uint64_t)chunk_bytes, len));
+        put32(e + 12, zco_crc32(blob + off, stored));
         off += pad16(stored);
     }
     put32(blob + 28, zco_crc32(blob, planes_end));
@@ -755,9 +756,9 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
      * chunk's variable compressed size so chunks decode independently. The
      * map here holds offsets, which are the running sum of the padded sizes
      * of the chunks before. Each entry also carries the zlib CRC-32 of the
-     * chunk's original bytes (cuZipNN: checksums match zlib.crc32; reading:
-     * the chunk CRC checks the decoded result end to end, while whole-blob
-     * checks before decoding use the CRC of the blob's own bytes). */
+     * chunk's stored payload (cuZipNN API: checksums match zlib.crc32 and
+     * are taken over pieces of the blob, so that an untrusted blob can be
+     * checked before it is decoded). */
     uint64_t off = table_end;
     for (uint64_t c = 0; c < nc; c++) {
         uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - c * chunk_bytes);
@@ -770,7 +771,7 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
         uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * c;
         put64(e, off);
         put32(e + 8, (uint32_t)stored | ((uint32_t)raw << 31));
-        put32(e + 12, zco_crc32(src + c * (uint64_t)chunk_bytes, len));
+        put32(e + 12, zco_crc32(blob + off, stored));
         off += pad16(stored);
     }
     put32(blob + 28, zco_crc32(blob, table_end));
@@ -919,13 +920,32 @@ int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_
         uint32_t stored = sm & 0x7FFFFFFFu;
         uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - (uint64_t)c * chunk_bytes);
         uint8_t *out = dst + (uint64_t)c * chunk_bytes;
-        int cst = ZCO_OK;
-        if (sm >> 31) memcpy(out, blob + off, len);
-        else cst = decode_grouped(blob + off, stored, len, dtype, shared ? planes : NULL, out);
-        status |= cst;
-        /* the chunk CRC covers the original bytes: check what was decoded */
-        if (cst == ZCO_OK && !(flags & ZCO_NO_VERIFY) && zco_crc32(out, len) != get32(e + 12))
+        /* the chunk CRC covers the stored payload: a chunk that fails it is
+         * reported and not decoded (its output bytes are left as they were) */
+        if (!(flags & ZCO_NO_VERIFY) && zco_crc32(blob + off, stored) != get32(e + 12)) {
             status |= ZCO_ECRC;
+            continue;
+        }
+        if (sm >> 31) memcpy(out, blob + off, len);
+        else status |= decode_grouped(blob + off, stored, len, dtype, shared ? planes : NULL, out);
+    }
+    return status;
+}
+
+/* Check a blob without decoding it (cuZipNN API: verify an untrusted blob
+ * with the CRC-32 helpers before decompressing it): the header and chunk
+ * table as zco_blob_info checks them, that the payloads lie within blob_len,
+ * then every chunk's CRC over its stored bytes. Returns status. */
+int zco_verify(const uint8_t *blob, uint64_t blob_len) {
+    uint64_t total;
+    uint32_t nc;
+    int st = zco_blob_info(blob, blob_len, NULL, NULL, NULL, NULL, &nc, NULL, &total);
+    if (st != ZCO_OK) return st;
+    if (total > blob_len) return ZCO_EFORMAT;
+    int status = ZCO_OK;
+    for (uint32_t c = 0; c < nc; c++) {
+        const uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * (uint64_t)c;
+        if (zco_crc32(blob + get64(e), get32(e + 8) & 0x7FFFFFFFu) != get32(e + 12)) status |= ZCO_ECRC;
     }
     return status;
 }

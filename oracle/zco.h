@@ -109,8 +109,14 @@ uint64_t zco_blob_size_v(uint64_t nbytes, int dtype, uint32_t chunk_bytes, doubl
 int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
                    uint32_t chunk_bytes, double threshold, int version,
                    uint8_t *blob, uint64_t cap, uint64_t *blob_bytes);
-/* Decompress a blob into dst (capacity cap). Returns status. */
+/* Decompress a blob into dst (capacity cap). Unless flags has
+ * ZCO_NO_VERIFY, each chunk's CRC-32 over its stored bytes is checked before
+ * the chunk is decoded; a chunk that fails is reported (ZCO_ECRC) and not
+ * decoded. Returns status. */
 int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_t cap, uint32_t flags);
+/* Check a blob's header, table and every chunk CRC without decoding it.
+ * Returns status (ZCO_OK, ZCO_EFORMAT or ZCO_ECRC bits). */
+int zco_verify(const uint8_t *blob, uint64_t blob_len);
 
 #ifdef __cplusplus
 }

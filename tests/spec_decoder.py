@@ -103,14 +103,13 @@ def decode(blob: bytes) -> bytes:
         off, sm, crc = struct.unpack_from("<QII", blob, 96 + 16 * c)
         stored, raw = sm & 0x7FFFFFFF, sm >> 31
         payload = blob[off:off + stored]
+        if zlib.crc32(bytes(payload)) != crc:   # CRC of the stored bytes, checked first
+            raise SpecError(f"chunk {c} crc")
         length = min(chunk_bytes, nbytes - c * chunk_bytes)
-        start = len(out)
         if raw:
             out += payload
         else:
             out += _grouped(payload, length, dtype, planes)
-        if zlib.crc32(bytes(out[start:])) != crc:   # CRC of the original bytes
-            raise SpecError(f"chunk {c} crc")
     return bytes(out)
 
 

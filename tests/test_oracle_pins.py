@@ -227,7 +227,7 @@ def test_tiny_blob_golden(zco):
     assert len(payload) == int(g["chunk0_stored"])
     entry = struct.pack("<QII", int(g["chunk0_offset"]),
                         int(g["chunk0_stored"]) | (int(g["chunk0_raw"]) << 31),
-                        zlib.crc32(bytes.fromhex(g["chunk0_original"])))
+                        zlib.crc32(payload))  # the stored payload bytes
     table = bytes(head) + entry
     assert len(table) == table_end
     hcrc = zlib.crc32(table)
@@ -390,6 +390,42 @@ def test_corruption_detected(zco):
     for cut in (0, 50, 96, 100, len(blob) - 1):
         st, _ = zco.decompress_status(blob[:cut])
         assert st != 0
+
+
+def test_chunk_crc_is_checked_before_decoding(zco):
+    """cuZipNN API: the CRC-32s are taken over pieces of the blob so that an
+    untrusted blob can be rejected before it is decoded. A changed payload
+    byte fails its chunk's CRC; that chunk is reported and never decoded (so
+    no structural error is raised from inside it), the other chunks decode
+    exactly, and the check without decoding (verify) reports the same. Bytes
+    of the zero padding between payloads are outside every CRC."""
+    rng = np.random.default_rng(31)
+    t = workloads.bf16_1m()[:48]
+    raw = workloads.as_bytes(t).numpy()
+    C = 4096
+    blob = zco.compress(raw, 4, tuple(t.shape), C, 0.95)
+    assert zco.verify(blob) == 0
+    nc, = struct.unpack_from("<I", blob, 24)
+    entries = [struct.unpack_from("<QII", blob, 96 + 16 * c) for c in range(nc)]
+    for c, (off, sm, crc) in enumerate(entries):
+        stored = sm & 0x7FFFFFFF
+        assert crc == zlib.crc32(blob[off:off + stored]), c
+        for pos in (off, off + stored - 1, off + int(rng.integers(0, stored))):
+            bad = bytearray(blob)
+            bad[pos] ^= int(rng.integers(1, 256))
+            st, out = zco.decompress_status(bytes(bad))
+            assert st == zco.ECRC, (c, pos)
+            assert zco.verify(bytes(bad)) == zco.ECRC
+            keep = np.ones(raw.size, bool)
+            keep[c * C:(c + 1) * C] = False
+            assert (out[keep] == raw[keep]).all()
+    # a header or table byte: caught by the header CRC or the layout checks
+    for pos in list(range(0, 96, 7)) + [96 + 16 * c + 13 for c in range(nc)]:
+        bad = bytearray(blob)
+        bad[pos] ^= 0x40
+        assert zco.verify(bytes(bad)) & (zco.EFORMAT | zco.ECRC), pos
+    # truncated: a payload outside the blob
+    assert zco.verify(blob[:-16]) & zco.EFORMAT
 
 
 def test_no_verify_flag_still_checks_structure(zco):
