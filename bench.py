@@ -2,12 +2,15 @@
 """Benchmark: encode and decode throughput (GB/s of original bytes) of the
 compressor on one GB300, with the HBM roofline fraction and the size ratio.
 
-A step is one pass of the whole hot path over one tensor: compression (byte
-grouping, per-chunk tables, rANS with passthrough, offset scan, CRC-32) and
-decompression of the blob it made (CRC check, rANS decode, merge). Inputs are
-device-resident when the timed region starts; they are larger than the L2
-cache (no flush needed). `value` = original bytes of all ranks / (encode +
-decode time); encode and decode are also reported on their own.
+A step is one pass of the whole hot path over the workload: compression
+(byte grouping, per-chunk tables, rANS with passthrough, offset scan, CRC-32)
+and decompression of the blobs it made (rANS decode, merge, CRC check). The
+default workload is the Llama-3.1-8B-shaped BF16 model (290 tensors, 16.06
+GB), compressed and decompressed tensor by tensor from device memory; the
+same model in one batched call each way is reported beside it. Inputs are
+device-resident when the timed region starts; inputs smaller than 256 MiB get
+the L2 flushed before every timed call. `value` = original bytes of all ranks
+/ (encode + decode time); encode and decode are also reported on their own.
 
 `--impl reference` times the CPU oracle (plain C, one thread) on a bounded
 sample of the same workload, as the reference arm.
@@ -41,7 +44,7 @@ def _args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    p.add_argument("--workload", default="fp32_64m",
+    p.add_argument("--workload", default="llama8b",
                    choices=["fp32_64m", "bf16_1m", "fp32clean_64m", "fp16_16m", "bf16_delta", "bf16_delta_fused",
                             "bf16_llama_gate", "llama8b", "llama8b_batch"])
     p.add_argument("--chunk-bytes", type=int, default=131072)
@@ -354,6 +357,7 @@ def run_model(a, world, rank, local, dev, stream):
     from entropy_coding_gb300 import workloads as wl
 
     batched = a.workload == "llama8b_batch"
+    also_batched = not batched  # the per-tensor line also reports the batched calls
     flags = zc.SHARED_TABLES if a.shared_tables else 0
     specs = wl.llama8b_specs()
     C, thr, code, Wd = a.chunk_bytes, a.threshold, wl.BF16, 2
@@ -381,25 +385,27 @@ def run_model(a, world, rank, local, dev, stream):
     shapes = [tuple(sh) for _, sh in specs]
     nb = torch.zeros(n, dtype=torch.int64, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    if batched:
-        ws = torch.empty(zc.workspace_size_batch(sizes, code, C, flags), dtype=torch.uint8, device=dev)
+    ws_b = dws = ws_1 = None
+    if batched or also_batched:
+        ws_b = torch.empty(zc.workspace_size_batch(sizes, code, C, flags), dtype=torch.uint8, device=dev)
         n_dws = zc.decompress_workspace_size_batch(n)
         dws = torch.empty(max(16, n_dws), dtype=torch.uint8, device=dev)
-    else:
-        ws = torch.empty(max(zc.workspace_size(x, code, C, flags) for x in sizes), dtype=torch.uint8, device=dev)
+    if not batched:
+        ws_1 = torch.empty(max(zc.workspace_size(x, code, C, flags) for x in sizes), dtype=torch.uint8,
+                           device=dev)
     N = sum(sizes)
     verify = not a.no_verify
 
-    def comp(inputs, blobs=blobs, nb=nb):
-        if batched:
-            zc.compress_batch_into(inputs, blobs, nb, ws, st, code, shapes, C, thr, stream, flags=flags)
+    def comp(inputs, blobs=blobs, nb=nb, one_call=batched):
+        if one_call:
+            zc.compress_batch_into(inputs, blobs, nb, ws_b, st, code, shapes, C, thr, stream, flags=flags)
         else:
             for t in range(n):
-                zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws, st, C, thr, stream, dtype=code,
+                zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws_1, st, C, thr, stream, dtype=code,
                                  shape=shapes[t], flags=flags)
 
-    def decomp(infos, blobs=blobs):
-        if batched:
+    def decomp(infos, blobs=blobs, one_call=batched):
+        if one_call:
             zc.decompress_batch_into(blobs, infos, outs, st, dws, verify, stream)
         else:
             for t in range(n):
@@ -442,6 +448,30 @@ def run_model(a, world, rank, local, dev, stream):
     assert int(st.item()) == 0 and nb.tolist() == lens
     total = t_enc + t_dec
     total, t_enc, t_dec = max_over_ranks([total, t_enc, t_dec], dev)
+
+    # the same model in one batched call each way, beside the per-tensor line
+    batched_line = None
+    if also_batched:
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, a.warmup)):
+                comp(srcs, one_call=True)
+                decomp(infos, one_call=True)
+        stream.synchronize()
+        assert int(st.item()) == 0 and nb.tolist() == lens and torch.equal(out_all, src_all)
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+        with torch.cuda.stream(stream):
+            for ev in bev:
+                ev[0].record(stream)
+                comp(srcs, one_call=True)
+                ev[1].record(stream)
+                decomp(infos, one_call=True)
+                ev[2].record(stream)
+        stream.synchronize()
+        bt_enc = sum(e[0].elapsed_time(e[1]) for e in bev) / 1e3
+        bt_dec = sum(e[1].elapsed_time(e[2]) for e in bev) / 1e3
+        assert int(st.item()) == 0 and nb.tolist() == lens
+        bt_enc, bt_dec = max_over_ranks([bt_enc, bt_dec], dev)
+        batched_line = (bt_enc, bt_dec)
 
     # end to end through the public calls: the model from pinned host memory,
     # the blobs back to the host and up again, the restored model to the host
@@ -543,6 +573,15 @@ def run_model(a, world, rank, local, dev, stream):
                             "mode": "device blobs, copied to pinned host memory and back"},
         "gpu_launches": per_step * a.steps,
     }
+    if batched_line is not None:
+        bt_enc, bt_dec = batched_line
+        line["batched"] = {
+            "desc": "the same model, all tensors in one zc_compress_batch and one zc_decompress_batch call",
+            "value": round(replica_value(N, a.steps, world, bt_enc + bt_dec) / 1e9, 3), "unit": "GB/s",
+            "encode": {"gbs": round(N * a.steps / bt_enc / 1e9, 2), "ms": round(1e3 * bt_enc / a.steps, 4),
+                       "roofline_frac": round(alg * a.steps / bt_enc / 1e9 / hbm, 4)},
+            "decode": {"gbs": round(N * a.steps / bt_dec / 1e9, 2), "ms": round(1e3 * bt_dec / a.steps, 4),
+                       "roofline_frac": round(alg * a.steps / bt_dec / 1e9 / hbm, 4)}}
     del src_all, out_all, blob_all
     first = wl.llama8b_tensor(0, *specs[0])
     line["cpu_baseline"] = cpu_baseline(first, code, a)

@@ -20,7 +20,7 @@ import torch
 from . import build as _build
 from .workloads import BF16, FP16, FP32, U8, U16, U32
 
-__all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspace_size",
+__all__ = ["compress", "decompress", "crc32", "verify", "verify_into", "blob_info", "blob_size", "workspace_size",
            "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
            "decompress_delta_into", "compress_batch", "compress_batch_into", "decompress_batch",
            "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "SHARED_TABLES", "OK", "EINVAL", "EFORMAT",
@@ -29,6 +29,7 @@ __all__ = ["compress", "decompress", "crc32", "blob_info", "blob_size", "workspa
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
 NO_VERIFY = 1
 SHARED_TABLES = 2  # compression flag: blob format v2 (shared plane tables)
+HOOK_LOOKBACK_STALL, HOOK_PRODUCER_STALL = 1, 2  # test hooks (zc_set_test_hooks)
 DEFAULT_CHUNK = 131072
 DEFAULT_THRESHOLD = 0.95
 
@@ -96,6 +97,10 @@ def lib() -> ctypes.CDLL:
             L.zc_decompress_delta.argtypes = [vp, ctypes.POINTER(_Info), vp, vp, u64, u32, vp, vp]
             L.zc_crc32.restype = i32
             L.zc_crc32.argtypes = [vp, u64, u64, vp, vp]
+            L.zc_set_test_hooks.restype = None
+            L.zc_set_test_hooks.argtypes = [u32]
+            L.zc_verify.restype = i32
+            L.zc_verify.argtypes = [vp, ctypes.POINTER(_Info), vp, vp]
             pu64, pi64, pi32 = ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
             L.zc_workspace_size_batch.restype = u64
             L.zc_workspace_size_batch.argtypes = [pu64, u32, i32, u32, u32]
@@ -329,6 +334,32 @@ def decompress_delta(blob: torch.Tensor, base: torch.Tensor, info: dict | None =
                           verify, stream)
     _check(int(status.item()), "zc_decompress_delta (device)")
     return out
+
+
+def set_test_hooks(hooks: int) -> None:
+    """Test hooks that make a bounded device wait run out (tests only; 0 =
+    none): HOOK_LOOKBACK_STALL, HOOK_PRODUCER_STALL."""
+    lib().zc_set_test_hooks(hooks)
+
+
+def verify_into(blob: torch.Tensor, info: dict, status: torch.Tensor, stream=None) -> None:
+    """Launch the check of a blob's header CRC and chunk CRCs without
+    decoding it (OR-ed into the device int32 ``status``); no sync."""
+    _check(lib().zc_verify(blob.data_ptr(), ctypes.byref(_info_struct(info)), status.data_ptr(), _stream(stream)),
+           "zc_verify")
+
+
+def verify(blob: torch.Tensor, info: dict | None = None, stream=None) -> int:
+    """Status of checking a CUDA or page-locked CPU blob without decoding it
+    (cuZipNN API: verify an untrusted blob before decompressing it): 0 when
+    the header CRC and every chunk CRC match, else ECRC / EFORMAT bits."""
+    if not _readable(blob):
+        raise ZcError(EINVAL, "verify expects a CUDA or page-locked CPU blob")
+    info = read_info(blob) if info is None else info
+    dev = blob.device if blob.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    verify_into(blob, info, status, stream)
+    return int(status.item())
 
 
 def crc32(t: torch.Tensor, piece_bytes: int = 16384, stream=None) -> torch.Tensor:

@@ -1,6 +1,8 @@
 // crc.cu — piecewise CRC-32 of any device buffer (cuZipNN API,
 // hash_tensor_with_crc32: a zlib-compatible CRC of every checksum-chunk-sized
-// piece of a tensor's bytes, computed on the GPU).
+// piece of a tensor's bytes, computed on the GPU), and the check of a blob's
+// CRCs without decoding it (cuZipNN API: verify an untrusted blob with the
+// CRC-32 helpers before decompressing it).
 //
 // Each piece is cut into work units of at most `unit` bytes; one warp takes
 // one unit. CRC-32 is linear over GF(2), so the register after a whole piece
@@ -50,7 +52,54 @@ __global__ void __launch_bounds__(kWarps * 32) crc_kernel(CrcArgs a) {
     }
 }
 
+// One CTA per chunk (grid-stride), and one unit more for the header: the
+// header CRC runs over the header with its CRC field read as zero and over
+// the chunk table (v2: and the plane tables); a chunk's over its stored
+// bytes. A table entry that points outside the blob is reported as a format
+// error and its bytes are not read.
+constexpr int kVerifyWarps = 8;
+
+__global__ void __launch_bounds__(kVerifyWarps * 32) verify_kernel(VerifyArgs a) {
+    __shared__ __align__(16) uint32_t tab[kCrcRepWords];
+    __shared__ uint32_t gap[4][256];
+    __shared__ uint32_t s_reg[kVerifyWarps];
+    load_crc_rep(tab);
+    load_shift_smem(gap, gap_table<kVerifyWarps * 32>());
+    __syncthreads();
+    const uint32_t *row = crc_row(tab);
+    for (uint64_t u = blockIdx.x; u <= a.n_chunks; u += gridDim.x) {
+        if (u == a.n_chunks) {
+            uint32_t reg = 0xFFFFFFFFu;
+            for (int i = 0; i < 28; i++) reg = crc_rep_byte(reg, __ldg(a.blob + i), row);
+            reg = crc_rep_word(reg, 0u, row);
+            reg = crc_strided<kVerifyWarps, false>(a.blob + 32, a.table_end - 32, reg, tab, gap, s_reg);
+            const uint32_t want = __ldg(reinterpret_cast<const uint32_t *>(a.blob + 28));
+            if (threadIdx.x == 0 && (reg ^ 0xFFFFFFFFu) != want) status_or(a.d_status, ZC_ECRC);
+            continue;
+        }
+        const uint4 ent = __ldg(reinterpret_cast<const uint4 *>(a.blob + ZC_HEADER_BYTES) + u);
+        const uint64_t off = uint64_t(ent.x) | (uint64_t(ent.y) << 32);
+        const uint64_t stored = ent.z & 0x7FFFFFFFu;
+        if ((off & 15) || off < a.table_end || off > a.blob_bytes || stored > a.blob_bytes - off) {
+            if (threadIdx.x == 0) status_or(a.d_status, ZC_EFORMAT);
+            continue;
+        }
+        const uint32_t reg = crc_strided<kVerifyWarps, false>(a.blob + off, stored, 0xFFFFFFFFu, tab, gap, s_reg);
+        if (threadIdx.x == 0 && (reg ^ 0xFFFFFFFFu) != ent.w) status_or(a.d_status, ZC_ECRC);
+    }
+}
+
 } // namespace
+
+int launch_verify(const VerifyArgs &a, cudaStream_t s) {
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ECUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ZC_ECUDA;
+    const uint64_t units = uint64_t(a.n_chunks) + 1;
+    const uint64_t cap = uint64_t(sms) * 4;
+    verify_kernel<<<int(units < cap ? units : cap), kVerifyWarps * 32, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
+}
 
 int launch_crc(const CrcArgs &a, cudaStream_t s) {
     if (a.n_units == 0) return ZC_OK;

@@ -10,10 +10,12 @@
 //     queue of four 256-byte stage buffers;
 //   - the consumer warp takes each group of symbols, gathers the bytes of 8
 //     consecutive elements per lane from every stream (coded, raw or
-//     constant), transposes them into words, undoes the exponent extraction,
-//     stores them with vector stores and accumulates the CRC-32 of the bytes
-//     it wrote, which it checks against the chunk table at the end (unless
-//     the caller asked not to); a RAW chunk is a copy done by the consumer.
+//     constant), transposes them into words, undoes the exponent extraction
+//     and stores them with vector stores. Unless the caller asked not to, it
+//     also takes the CRC-32 of the chunk's stored bytes (cuZipNN API: the
+//     CRCs are over pieces of the blob): the raw streams' bytes as it reads
+//     them, the directory and the coded records at the end, and checks it
+//     against the chunk table; a RAW chunk is a copy done by the consumer.
 // So the serial chain of rANS states is the only work on the producer's
 // critical path. The queue is guarded by shared-memory mbarriers; every wait
 // gives up after about a second (ZC_ETIMEOUT) so that a fault in one warp
@@ -38,11 +40,10 @@ constexpr int kThreads = 64 * kPairs;
 constexpr uint64_t kBigPairs = 7;        // pairs per CTA at most with one-level tables (one CTA per SM)
 constexpr int kStages = 4;                // symbol groups in flight within a pair
 constexpr uint32_t kLutBytes = 4096, kSymBytes = 1024, kRingWords = 1024;
-// CRC slicing tables (C copies) + shift tables: one group's output (256 W
-// bytes) and the 496-byte gap
+// CRC slicing tables (C copies) + shift tables: one group's bytes of a
+// stream (256) and the 496-byte gap
 template <int C>
 constexpr uint32_t crc_smem() { return crc_rep_words<C>() * 4 + 2 * 4 * 256 * 4; }
-constexpr uint64_t kWaitCycles = 1ull << 31;  // about a second at GB300 clocks
 constexpr uint32_t kV2Pairs = 16;             // v2: chunks per CTA at most (one CTA per SM)
 constexpr int kV2Threads = 64 * kV2Pairs;
 
@@ -90,12 +91,12 @@ __device__ __forceinline__ bool mbar_test(unsigned long long *b, uint32_t parity
     return done != 0;
 }
 // Wait (the whole warp) until the phase of the given parity has completed;
-// false after about a second.
-__device__ bool mbar_wait(unsigned long long *b, uint32_t parity) {
+// false after `limit` clock cycles (about a second in normal calls).
+__device__ bool mbar_wait(unsigned long long *b, uint32_t parity, unsigned long long limit) {
     const long long t0 = clock64();
     for (;;) {
         if (__all_sync(kFull, mbar_test(b, parity))) return true;
-        if (uint64_t(clock64() - t0) > kWaitCycles) return false;
+        if ((unsigned long long)(clock64() - t0) > limit) return false;
     }
 }
 
@@ -290,7 +291,7 @@ struct ChunkCtx {
     uint8_t *out;          // output range
     uint8_t *tail;         // staged bytes of the coded streams after the first
     const uint8_t *base;   // delta: the base tensor's bytes of this chunk (the output is decoded XOR base)
-    uint32_t n, len, q, groups, T;
+    uint32_t n, len, q, groups, T, stored;
     bool have_main;
     uint32_t kind[4], val[4], roff[4], sub[4];
 };
@@ -342,6 +343,9 @@ template <int DT, bool kBig, bool kV2, class PS>
 __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const uint32_t *const *pbig) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
+    // test hook: the producer stops before its first signal (nothing in
+    // flight), so the consumer's wait runs out
+    if (a.hooks & ZC_HOOK_PRODUCER_STALL) return;
     const uint32_t lt = lanemask_lt();
     // v1: the record's own table, built into the pair's tables; v2: the
     // CTA's table of the stream's plane
@@ -389,7 +393,7 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
     const uint32_t ng = (cx.T + 7) / 8;  // groups including a partial last one
     for (uint32_t g = 0; g < ng; g++) {
         const uint32_t k = g % kStages, r = g / kStages;
-        if (r > 0 && !mbar_wait(&ps.empty[k], (r - 1) & 1u)) {
+        if (r > 0 && !mbar_wait(&ps.empty[k], (r - 1) & 1u, a.wait_cycles)) {
             if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
             cp_async_wait_all();
             return;
@@ -408,13 +412,15 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
     cp_async_wait_all();
 }
 
-// Consumer warp: the chunk's output and its CRC. The lane register follows
-// the lane's pieces: lane l's 8 elements of a group form one 8W-byte piece
-// and the pieces of a group are consecutive, so after group g it is
-// shift(register after g - 1, 256 W bytes) XOR the CRC register of the new
-// piece taken from zero (linearity); the lanes are folded at the end
-// (crc_fold) and the elements after the last whole group are added from the
-// output.
+// Consumer warp: the chunk's output and the CRC of its stored bytes. For a
+// raw stream the lane register follows the lane's 8-byte pieces: group g of
+// the stream is its bytes [256 g, 256 g + 256) and lane l reads bytes 8 l ..
+// 8 l + 7 of it, so after group g the register is shift(register after
+// g - 1, 256 bytes) XOR the register of the new piece taken from zero
+// (linearity); the lanes are folded at the end (crc_fold) and the stream's
+// bytes after its last whole group (and its padding) are added from the
+// blob. The directory and the coded records are taken from the blob at the
+// end, and the parts are appended in payload order.
 template <int DT, bool kVerify, bool kDelta, int C, class PS>
 __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
                         const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
@@ -424,13 +430,21 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
     const uint32_t groups = cx.groups;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(cx.out) & 15) == 0;
     if (cx.have_main) {
-        if (!mbar_wait(&ps.start, 0)) {
+        if (!mbar_wait(&ps.start, 0, a.wait_cycles)) {
             if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
             return;
         }
-        if (ps.flag == 0) return;  // the producer has reported the chunk
+        if (ps.flag == 0) {  // the producer has reported the chunk: is the payload the stored one?
+            if constexpr (kVerify) {
+                const uint32_t reg = crc_strided<1, false, C>(cx.p, cx.stored, 0xFFFFFFFFu, crc_rep, gap496, nullptr);
+                if ((reg ^ 0xFFFFFFFFu) != expect_crc && lane == 0) status_or(a.d_status, ZC_ECRC);
+            }
+            return;
+        }
     }
-    uint32_t Rl = 0;
+    uint32_t Rraw[W];  // CRC registers of the raw streams (kVerify)
+#pragma unroll
+    for (int j = 0; j < W; j++) Rraw[j] = 0;
     uint2 rn1[W], rn2[W];  // raw columns of the next two groups
 #pragma unroll
     for (int j = 0; j < W; j++) {
@@ -464,10 +478,15 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             rn1[j] = rn2[j];
             if (cx.kind[j] == kKRaw && g + 2 < groups)
                 rn2[j] = __ldg(reinterpret_cast<const uint2 *>(cx.p + cx.roff[j] + 256 * (g + 2)) + lane);
+            if constexpr (kVerify) {
+                if (cx.kind[j] == kKRaw)
+                    Rraw[j] = (g ? shift_smem(Rraw[j], gshift) : 0u) ^
+                              crc_rep_word<C>(crc_rep_word<C>(0u, col[j].lo, row), col[j].hi, row);
+            }
         }
         uint2 mv = make_uint2(0, 0);
         if (cx.have_main) {
-            if (!mbar_wait(&ps.full[k], r & 1u)) {
+            if (!mbar_wait(&ps.full[k], r & 1u, a.wait_cycles)) {
                 if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
                 return;
             }
@@ -488,7 +507,6 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 col[j].hi = v[1];
             }
         }
-        const uint32_t cin = (g == 0 && lane == 0) ? 0xFFFFFFFFu : 0u;
         if constexpr (W == 4) {
             uint4 v[2];
 #pragma unroll
@@ -502,8 +520,6 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 v[h].z = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x5410));
                 v[h].w = Perm<DT>::inv(__byte_perm(hi32, hi10, 0x7632));
             }
-            if constexpr (kVerify)
-                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16<C>(crc_rep16<C>(cin, v[0], row), v[1], row);
             if constexpr (kDelta) {
                 v[0] = xb(v[0], bv[0]);
                 v[1] = xb(v[1], bv[1]);
@@ -523,7 +539,6 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             v.y = Perm<DT>::inv2(__byte_perm(col[1].lo, col[0].lo, 0x7362));
             v.z = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x5140));
             v.w = Perm<DT>::inv2(__byte_perm(col[1].hi, col[0].hi, 0x7362));
-            if constexpr (kVerify) Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ crc_rep16<C>(cin, v, row);
             if constexpr (kDelta) v = xb(v, bv[0]);
             if (vec_ok) {
                 *reinterpret_cast<uint4 *>(cx.out + 2ull * e0) = v;
@@ -536,10 +551,6 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
                 }
             }
         } else {
-            if constexpr (kVerify) {
-                const uint32_t piece = crc_rep_word<C>(crc_rep_word<C>(cin, col[0].lo, row), col[0].hi, row);
-                Rl = (g ? shift_smem(Rl, gshift) : 0u) ^ piece;
-            }
             if constexpr (kDelta) {
                 col[0].lo ^= bv[0].x;
                 col[0].hi ^= bv[0].y;
@@ -555,7 +566,7 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
     // the last < 256 elements: the producer's partial group, step by step
     if (cx.T > 8 * groups) {
         const uint32_t k = groups % kStages, r = groups / kStages;
-        if (cx.have_main && !mbar_wait(&ps.full[k], r & 1u)) {
+        if (cx.have_main && !mbar_wait(&ps.full[k], r & 1u, a.wait_cycles)) {
             if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
             return;
         }
@@ -582,15 +593,24 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
         __syncwarp();
     }
     if constexpr (kVerify) {
-        constexpr int kLogPiece = W == 4 ? 5 : W == 2 ? 4 : 3;
-        uint32_t reg = groups ? crc_fold<1>(Rl, kLogPiece, nullptr) : 0xFFFFFFFFu;
-        const uint32_t done = groups * 256 * W;
-        if constexpr (kDelta) {
-            // the check is of the decoded bytes, before the XOR (only the last,
-            // partial chunk has elements after its whole groups)
-            for (uint32_t i = done; i < cx.len; i++) reg = crc_rep_byte<C>(reg, __ldcg(cx.out + i) ^ cx.base[i], row);
-        } else {
-            reg = crc_any<1, true, C>(cx.out + done, cx.len - done, reg, crc_rep, gap496, nullptr);
+        // the directory (16 bytes) from the preset register
+        uint32_t reg = crc_rep16<C>(0xFFFFFFFFu, __ldg(reinterpret_cast<const uint4 *>(cx.p)), row);
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            if (cx.kind[j] == kKConst) continue;
+            const uint8_t *seg = cx.p + cx.roff[j];
+            uint64_t seg_len;
+            uint32_t part;
+            if (cx.kind[j] == kKRaw) {
+                seg_len = pad16(cx.n);
+                part = groups ? crc_fold<1, 3>(Rraw[j], nullptr) : 0u;
+                const uint32_t done = 256 * groups;
+                part = crc_strided<1, false, C>(seg + done, seg_len - done, part, crc_rep, gap496, nullptr);
+            } else {
+                seg_len = pad16(cx.val[j]);
+                part = warp_crc16<C, true, 4>(seg, uint32_t(seg_len), crc_rep, gap496);
+            }
+            reg = crc_append_small(reg, part, uint32_t(seg_len));
         }
         if ((reg ^ 0xFFFFFFFFu) != expect_crc && lane == 0) status_or(a.d_status, ZC_ECRC);
     }
@@ -656,10 +676,17 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
 
     ChunkCtx cx;
     if (!parse_directory<W, kV2>(p, stored, n, cx)) {
-        if (!producer && lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+        if (!producer) {
+            if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
+            // a changed payload is reported as such (the check the caller asked for)
+            if (verify && (crc_strided<1, false, C>(p, stored, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) !=
+                              ent.w && lane == 0)
+                status_or(a.d_status, ZC_ECRC);
+        }
         return;
     }
     cx.p = p;
+    cx.stored = stored;
     cx.out = out;
     cx.n = n;
     cx.len = len;
@@ -691,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep<C>(crc_rep);
-        load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
+        load_shift_smem(gshift, kShPow + 8);  // 256 bytes
         load_shift_smem(gap496, kSh496);
     }
     const uint32_t pairs_per_cta = blockDim.x >> 6;
@@ -750,7 +777,7 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
 
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep<C>(crc_rep);
-        load_shift_smem(gshift, kShPow + (W == 4 ? 10 : W == 2 ? 9 : 8));  // 256 W bytes
+        load_shift_smem(gshift, kShPow + 8);  // 256 bytes
         load_shift_smem(gap496, kSh496);
     }
     const uint32_t pairs_per_cta = blockDim.x >> 6;

@@ -4,7 +4,7 @@
 // stats_kernel, one CTA per chunk (persistent CTAs, grid-stride over the
 // wave): one pass over the chunk's bytes builds the 256-bin histogram of
 // every byte stream of the exponent-extracted words (order-0 statistics,
-// ZipNN note Key insight) and the CRC-32 of the chunk's original bytes. Then
+// ZipNN note Key insight). Then
 // warp j takes stream j: a stream with one symbol is CONST; otherwise its
 // histogram is quantised to the 12-bit table, and the stream is RAW if its
 // coded size provably cannot come below the threshold, else a candidate
@@ -15,9 +15,10 @@
 // warp's workspace slot, applies the passthrough rule per stream and per
 // chunk (cuZipNN API, passthrough_threshold), finds the chunk's blob offset
 // with a decoupled look-back over the chunks before it (an exclusive prefix
-// scan of the metadata map, ZipNN note Method 5), and writes the payload and
-// the chunk table entry. The last warp to finish writes the header and its
-// CRC.
+// scan of the metadata map, ZipNN note Method 5), and writes the payload,
+// taking the CRC-32 of the stored bytes as it writes them (cuZipNN API: the
+// CRCs are over pieces of the blob), and the chunk table entry. The last
+// warp to finish writes the header and its CRC.
 //
 // The serial part of rANS coding (each lane's state runs through the whole
 // stream) stays on single warps that never wait at a CTA barrier, so an SM
@@ -38,7 +39,6 @@ constexpr uint32_t kModeCand = 3;  // statistics -> coder only: a stream to rANS
 constexpr uint32_t kAborted = 0xFFFFFFFFu;
 constexpr uint32_t kCodeWarpSmem = 4096 + 4096 + 4096;  // per coding warp: rANS table, symbol ring, 2 word stages
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
-constexpr uint32_t kSpinLimit = 1u << 22;
 
 // Exact division by a table frequency f in [1, 4095] for every dividend the
 // encoder can see (x < 2^20 f, since larger states are renormalised first):
@@ -317,13 +317,16 @@ __device__ void normalize_plane_warp(const unsigned long long cnt[8], unsigned l
 }
 
 // Exclusive prefix of this chunk's padded size over the chunks before it
-// (decoupled look-back, one warp). Every wait is bounded; a timeout sets
-// ZC_ETIMEOUT and the chunk is not placed.
-__device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, int32_t *d_status, bool *timed) {
+// (decoupled look-back, one warp). Every wait is bounded (spin_limit polls);
+// a timeout sets ZC_ETIMEOUT and the chunk is not placed. With the test hook
+// ZC_HOOK_LOOKBACK_STALL the first chunk never publishes its prefix, so the
+// waits of the others run out.
+__device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, int32_t *d_status, bool *timed,
+                             uint32_t spin_limit, uint32_t hooks) {
     const int lane = threadIdx.x & 31;
     *timed = false;
     if (c == 0) {
-        if (lane == 0) st_release(&st[0], kFlagPre | agg);
+        if (lane == 0 && !(hooks & ZC_HOOK_LOOKBACK_STALL)) st_release(&st[0], kFlagPre | agg);
         return 0;
     }
     if (lane == 0) st_release(&st[c], kFlagAgg | agg);
@@ -337,7 +340,7 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
             uint32_t spins = 0;
             v = ld_acquire(&st[idx]);
             while ((v >> 62) == 0) {
-                if (++spins > kSpinLimit) {
+                if (++spins > spin_limit) {
                     timed_out = true;
                     break;
                 }
@@ -370,13 +373,9 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
 // piece, 16 threads share a copy), far below 2^16.
 template <int W>
 struct StatsSmem {
-    uint32_t crc_rep[kCrcRepWords];  // CRC slicing tables, 8 copies (32 KB)
-    uint32_t gap[4][256];            // register shift over the other threads' 32-byte pieces
-    uint32_t gapu[4][256];           // the same for 16-byte pieces (unaligned inputs)
     uint32_t hist[W][128 * 32];
     uint32_t cnt[W][256];            // merged counts
     uint32_t plane[W][256];          // v2: counts of this CTA's recent chunks of one tensor, per plane
-    uint32_t s_reg[kStatWarps];
 };
 
 // Count one element into the histograms; hrow = &h[0][lane]. For the byte b
@@ -428,31 +427,21 @@ __device__ __forceinline__ void stream0_bytes(const uint4 &q, uint32_t o[4]) {
     }
 }
 
-// Histograms of the chunk's W byte streams and the raw CRC register of its
-// bytes, by the CTA from one pass, and stream 0's bytes for the coder.
-// Aligned input: the threads take 32-byte pieces round-robin, aligned to the
-// end of the chunk (see Strided; only the first round can be short), so each
-// thread's register needs one gap shift per round. Returns the raw register
-// in every thread.
+// Histograms of the chunk's W byte streams by the CTA from one pass, and
+// stream 0's bytes for the coder. Aligned input: the threads take 32-byte
+// pieces round-robin (the next round's piece is loaded while this round's is
+// counted); a piece is one 32-byte load when the chunk is 32-byte aligned (a
+// warp then reads 1 KiB contiguously), else two 16-byte loads.
 template <int DT, bool kDelta>
-__device__ uint32_t chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
+__device__ void chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<WordOf<DT>::W> &sm, uint8_t *cand0) {
     constexpr int W = WordOf<DT>::W;
     const int tid = threadIdx.x, lane = tid & 31;
-    const uint32_t *row = crc_row(sm.crc_rep);
     uint32_t *hrow = &sm.hist[0][lane];
-    uint32_t reg;
+    uint32_t done = 0;  // elements counted by the vector pass
     if (kDelta || (src.addr_bits() & 15) == 0) {  // delta inputs are 16-byte aligned
-        const uint32_t main = len & ~(kPiece - 1);
-        const uint32_t pieces = main / kPiece;
-        const uint32_t rounds = (pieces + kStatThreads - 1) / kStatThreads;
-        int32_t pidx = tid - int32_t(rounds * kStatThreads - pieces);
-        uint32_t R = 0;
-        // the next round's two vectors are in flight while this round's are
-        // counted and checksummed
-        // a piece is one 32-byte load when the chunk is 32-byte aligned (a warp
-        // then reads 1 KiB contiguously), else two 16-byte loads
+        const uint32_t pieces = len / kPiece;
         const bool wide = (src.addr_bits() & 31) == 0;
-        auto load_piece = [&](int32_t pi, uint4 &lo, uint4 &hi) {
+        auto load_piece = [&](uint32_t pi, uint4 &lo, uint4 &hi) {
             const uint64_t o = uint64_t(pi) * kPiece;
             if (wide) {
                 src.vec32(o, lo, hi);
@@ -461,58 +450,38 @@ __device__ uint32_t chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<Word
                 hi = src.vec(o + 16);
             }
         };
+        uint32_t pidx = tid;
         uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
-        if (rounds && pidx >= 0) load_piece(pidx, n0, n1);
-        for (uint32_t r = 0; r < rounds; r++, pidx += kStatThreads) {
+        if (pidx < pieces) load_piece(pidx, n0, n1);
+        for (; pidx < pieces; pidx += kStatThreads) {
             const uint4 q0 = n0, q1 = n1;
-            if (r + 1 < rounds) load_piece(pidx + kStatThreads, n0, n1);
-            uint32_t c = r == 0 ? (pidx == 0 ? 0xFFFFFFFFu : 0u) : shift_smem(R, sm.gap);
-            if (pidx >= 0) {
-                c = crc_rep16(crc_rep16(c, q0, row), q1, row);
-                count_vec<DT>(q0, hrow);
-                count_vec<DT>(q1, hrow);
-                // stream 0's bytes of the piece, for the coder in case the
-                // stream is a candidate
-                uint8_t *d = cand0 + uint64_t(pidx) * (kPiece / W);
-                uint32_t o0[4], o1[4];
-                stream0_bytes<DT>(q0, o0);
-                stream0_bytes<DT>(q1, o1);
-                if constexpr (W == 4) {
-                    *reinterpret_cast<uint2 *>(d) = make_uint2(o0[0], o1[0]);
-                } else if constexpr (W == 2) {
-                    *reinterpret_cast<uint4 *>(d) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
-                } else {
-                    reinterpret_cast<uint4 *>(d)[0] = q0;
-                    reinterpret_cast<uint4 *>(d)[1] = q1;
-                }
+            if (pidx + kStatThreads < pieces) load_piece(pidx + kStatThreads, n0, n1);
+            count_vec<DT>(q0, hrow);
+            count_vec<DT>(q1, hrow);
+            // stream 0's bytes of the piece, for the coder in case the
+            // stream is a candidate
+            uint8_t *d = cand0 + uint64_t(pidx) * (kPiece / W);
+            uint32_t o0[4], o1[4];
+            stream0_bytes<DT>(q0, o0);
+            stream0_bytes<DT>(q1, o1);
+            if constexpr (W == 4) {
+                *reinterpret_cast<uint2 *>(d) = make_uint2(o0[0], o1[0]);
+            } else if constexpr (W == 2) {
+                *reinterpret_cast<uint4 *>(d) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+            } else {
+                reinterpret_cast<uint4 *>(d)[0] = q0;
+                reinterpret_cast<uint4 *>(d)[1] = q1;
             }
-            R = c;
         }
-        reg = pieces ? crc_fold<kStatWarps>(R, 5, sm.s_reg) : 0xFFFFFFFFu;
-        for (uint32_t i = main; i < len; i++) reg = crc_rep_byte(reg, src.byte(i), row);
-        for (uint32_t i = main / W + tid; i < len / W; i += kStatThreads) {
-            const uint32_t w = src.template word<W>(i);
-            count_elem<DT>(w, hrow);
-            cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
-        }
-    } else if constexpr (!kDelta) {
-        // input aligned to its element size only: words one at a time; the
-        // CRC takes the bytes up to the first 16-byte boundary one by one,
-        // then the aligned rest with 16-byte pieces (gap table for 4080)
-        for (uint32_t i = tid; i < len / W; i += kStatThreads) {
-            const uint32_t w = src.template word<W>(i);
-            count_elem<DT>(w, hrow);
-            cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
-        }
-        uint32_t head = uint32_t((16 - (reinterpret_cast<uintptr_t>(src.p) & 15)) & 15);
-        if (head > len) head = len;
-        uint32_t c = 0xFFFFFFFFu;
-        for (uint32_t i = 0; i < head; i++) c = crc_rep_byte(c, src.byte(i), row);
-        reg = crc_strided<kStatWarps, false>(src.p + head, len - head, c, sm.crc_rep, sm.gapu, sm.s_reg);
-    } else {
-        reg = 0;
+        done = pieces * (kPiece / W);
     }
-    return reg;
+    // the rest (or, for input aligned to its element size only, all of it):
+    // one word at a time
+    for (uint32_t i = done + tid; i < len / W; i += kStatThreads) {
+        const uint32_t w = src.template word<W>(i);
+        count_elem<DT>(w, hrow);
+        cand0[i] = uint8_t(stream_byte<W>(Perm<DT>::fwd(w), 0));
+    }
 }
 
 // Sum the 32 counter copies of every stream into cnt[j][b] (and zero them
@@ -664,8 +633,8 @@ __device__ void warp_write_cand(Source<kDelta> src, uint32_t len, int j, uint8_t
 }
 
 // One CTA per chunk of the wave (grid-stride). Writes per chunk 32 bytes of
-// info {CRC-32 of the original bytes, W stream words mode << 30 | value}, the
-// tables of the candidate streams and their bytes.
+// info {unused word, W stream words mode << 30 | value}, the tables of the
+// candidate streams and their bytes.
 template <int DT, bool kDelta>
 __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     constexpr int W = WordOf<DT>::W;
@@ -675,9 +644,6 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     // the coding kernel's chunk ticket starts from zero in every wave (the
     // previous wave's coding kernel has finished: same stream)
     if (blockIdx.x == 0 && tid == 0) reinterpret_cast<uint32_t *>(a.ws_ctrl)[0] = 0;
-    load_crc_rep(sm.crc_rep);
-    load_shift_smem(sm.gap, kSh16352);
-    load_shift_smem(sm.gapu, gap_table<kStatThreads>());
     for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
     for (int i = tid; i < W * 256; i += kStatThreads) (&sm.plane[0][0])[i] = 0;
     // v2: warp j < W adds stream j's counts into sm.plane[j] for tensor cur_t
@@ -702,12 +668,11 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
         const Source<kDelta> src = Source<kDelta>{tv.src, tv.base}.at(c * a.chunk_bytes);
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, tv.nbytes - c * a.chunk_bytes));
         uint8_t *cand = a.ws_cand + uint64_t(cl) * W * a.n_pad;
-        const uint32_t reg = chunk_stats<DT, kDelta>(src, len, sm, cand);
+        chunk_stats<DT, kDelta>(src, len, sm, cand);
         __syncthreads();
         merge_counts<W>(sm);
         __syncthreads();
         uint32_t *info = reinterpret_cast<uint32_t *>(a.ws_info + 32ull * cl);
-        if (tid == 0) info[0] = reg ^ 0xFFFFFFFFu;
         // warp j decides stream j (and, when stream j >= 1 is a candidate,
         // writes its bytes for the coder; stream 0's are already there) while
         // the other warps go on to the next chunk: the counters were zeroed by
@@ -901,37 +866,77 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     return rec_bytes;
 }
 
+// The coder's CRC tables in shared memory: 4 copies of the slicing tables
+// (16 KB) and the register shift over the 31 other lanes' 16-byte pieces
+// (496 bytes) of the strided CRCs below.
+constexpr int kCodeCrcCopies = 4;
+constexpr uint32_t kCodeCrcBytes = crc_rep_words<kCodeCrcCopies>() * 4 + 4 * 256 * 4;
+
+struct CrcSmem {
+    const uint32_t *rep;              // crc_rep_words<kCodeCrcCopies>() words
+    const uint32_t (*gap496)[256];
+};
+
+// Pieces of a region of `pieces` 16-byte pieces taken by the warp's lanes
+// round-robin, aligned to the END of the region (only the first round can be
+// short): lane l's piece in round r is 32 r + l - v0. Each lane's CRC
+// register then ends 16 (31 - l) bytes before the region's end, which
+// crc_fold undoes.
+struct EndAligned {
+    uint32_t rounds, v0;
+    __device__ explicit EndAligned(uint32_t pieces) {
+        rounds = (pieces + 31) / 32;
+        v0 = rounds * 32 - pieces;
+    }
+};
+
 // All raw streams of a grouped chunk in one pass over the input, by the
 // warp: a lane takes 16 consecutive elements at a time (G groups, 8 vectors
 // in flight) and writes 16 bytes to every raw stream, gathering byte j (from
 // the top) of four elements into a word with two byte permutes and a merge.
+// Returns in reg[j] the CRC register, taken from zero, of raw stream j's
+// stored bytes (its n bytes and the zero padding to 16), which are exactly
+// the vectors written.
 template <int DT, bool kDelta>
 __device__ void warp_raw_streams(Source<kDelta> src, uint32_t n, const uint32_t mode[4], const uint32_t roff[4],
-                                 uint8_t *out) {
+                                 uint8_t *out, const CrcSmem &cs, uint32_t reg[4]) {
     constexpr int W = WordOf<DT>::W;
     constexpr int G = 8 / W;
     const int lane = threadIdx.x & 31;
+    const uint32_t *row = crc_row<kCodeCrcCopies>(cs.rep);
+#pragma unroll
+    for (int j = 0; j < W; j++) reg[j] = 0;
     bool any = false;
 #pragma unroll
     for (int j = 0; j < W; j++) any |= mode[j] == kModeRaw;
     if (!any) return;
     const uint32_t groups = (n + 15) / 16;
+    const EndAligned ea(groups);
     const bool vec = (src.addr_bits() & 15) == 0;
-    for (uint32_t g0 = lane; g0 < groups; g0 += 32 * G) {
+    for (uint32_t r0 = 0; r0 < ea.rounds; r0 += G) {
         uint4 qv[G][W];
 #pragma unroll
         for (int gi = 0; gi < G; gi++) {
-            const uint32_t g = g0 + 32 * gi;
+            const int64_t g = int64_t(32) * (r0 + gi) + lane - ea.v0;
 #pragma unroll
             for (int v = 0; v < W; v++)
-                qv[gi][v] = (vec && 16 * (g + 1) <= n)
+                qv[gi][v] = (vec && r0 + gi < ea.rounds && g >= 0 && 16 * (g + 1) <= n)
                                 ? src.vec_last(uint64_t(g) * 16 * W + 16 * v)
                                 : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int gi = 0; gi < G; gi++) {
-            const uint32_t g = g0 + 32 * gi;
-            if (g >= groups) break;
+            const uint32_t r = r0 + gi;
+            if (r >= ea.rounds) break;
+            const int64_t gs = int64_t(32) * r + lane - ea.v0;
+            // the register moves over the other lanes' pieces of this round
+            if (r > 0) {
+#pragma unroll
+                for (int j = 0; j < W; j++)
+                    if (mode[j] == kModeRaw) reg[j] = shift_smem(reg[j], cs.gap496);
+            }
+            if (gs < 0) continue;  // first round only
+            const uint32_t g = uint32_t(gs);
             uint32_t wd[16];
             if (vec && 16 * (g + 1) <= n) {
 #pragma unroll
@@ -970,13 +975,51 @@ __device__ void warp_raw_streams(Source<kDelta> src, uint32_t n, const uint32_t 
 #pragma unroll
                     for (int q = 0; q < 4; q++)
 #pragma unroll
-                        for (int r = 0; r < 4; r++)
-                            if (g * 16 + 4 * q + r >= n) o[q] &= ~(0xFFu << (8 * r));
+                        for (int b = 0; b < 4; b++)
+                            if (g * 16 + 4 * q + b >= n) o[q] &= ~(0xFFu << (8 * b));
                 }
-                reinterpret_cast<uint4 *>(out + roff[j])[g] = make_uint4(o[0], o[1], o[2], o[3]);
+                const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4 *>(out + roff[j])[g] = ov;
+                reg[j] = crc_rep16<kCodeCrcCopies>(reg[j], ov, row);
             }
         }
     }
+#pragma unroll
+    for (int j = 0; j < W; j++)
+        if (mode[j] == kModeRaw) reg[j] = crc_fold<1, 4>(reg[j], nullptr);
+}
+
+// Copy len bytes (a multiple of 16) from a 16-byte aligned source by the
+// warp, 8 vectors in flight per lane, and return the CRC register of the
+// copied bytes taken from zero; dst is 16-aligned.
+__device__ uint32_t warp_copy_crc(const uint8_t *src, uint64_t len, uint8_t *dst, const CrcSmem &cs) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t *row = crc_row<kCodeCrcCopies>(cs.rep);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    const EndAligned ea(uint32_t(len / 16));
+    constexpr int U = 8;
+    uint32_t R = 0;
+    for (uint32_t r0 = 0; r0 < ea.rounds; r0 += U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t v = int64_t(32) * (r0 + u) + lane - ea.v0;
+            t[u] = (r0 + u < ea.rounds && v >= 0) ? __ldcs(s4 + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const uint32_t r = r0 + u;
+            if (r >= ea.rounds) break;
+            const int64_t v = int64_t(32) * r + lane - ea.v0;
+            if (r > 0) R = shift_smem(R, cs.gap496);
+            if (v >= 0) {
+                d4[v] = t[u];
+                R = crc_rep16<kCodeCrcCopies>(R, t[u], row);
+            }
+        }
+    }
+    return ea.rounds ? crc_fold<1, 4>(R, nullptr) : 0u;
 }
 
 // Copy the len bytes of a source (zero-padded to 16) by the warp, 8 vectors
@@ -997,26 +1040,6 @@ __device__ void warp_copy_src(Source<kDelta> src, uint64_t len, uint8_t *dst) {
             if (v0 + 32 * u < nvec) d4[v0 + 32 * u] = t[u];
     }
     for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? uint8_t(src.byte(i)) : 0;
-}
-
-// Copy len bytes (zero-padded to 16) by the warp, 8 vectors in flight per
-// lane; dst is 16-aligned.
-__device__ void warp_copy(const uint8_t *src, uint64_t len, uint8_t *dst) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t nvec = (reinterpret_cast<uintptr_t>(src) & 15) ? 0 : len / 16;
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    constexpr int U = 8;
-    for (uint64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
-        uint4 t[U];
-#pragma unroll
-        for (int u = 0; u < U; u++)
-            if (v0 + 32 * u < nvec) t[u] = __ldcs(s4 + v0 + 32 * u);
-#pragma unroll
-        for (int u = 0; u < U; u++)
-            if (v0 + 32 * u < nvec) d4[v0 + 32 * u] = t[u];
-    }
-    for (uint64_t i = nvec * 16 + lane; i < pad16(len); i += 32) dst[i] = i < len ? src[i] : 0;
 }
 
 template <int DT, int J>
@@ -1050,9 +1073,17 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + warp;
+    // the CTA's CRC tables, then 12 KB per warp
+    uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem_raw);
+    uint32_t(*gap496)[256] = reinterpret_cast<uint32_t(*)[256]>(smem_raw + crc_rep_words<kCodeCrcCopies>() * 4);
+    load_crc_rep<kCodeCrcCopies>(crc_rep);
+    load_shift_smem(gap496, kSh496);
+    __syncthreads();
     if (gw >= a.workers) return;
-    uint4 *etab = reinterpret_cast<uint4 *>(smem_raw + kCodeWarpSmem * warp);
-    uint8_t *ring = smem_raw + kCodeWarpSmem * warp + 4096;
+    const CrcSmem cs{crc_rep, gap496};
+    uint8_t *warp_smem = smem_raw + kCodeCrcBytes + kCodeWarpSmem * warp;
+    uint4 *etab = reinterpret_cast<uint4 *>(warp_smem);
+    uint8_t *ring = warp_smem + 4096;
     uint8_t *slot = a.ws_slots + uint64_t(gw) * a.slot_bytes;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
 
@@ -1073,7 +1104,6 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         const uint32_t len = uint32_t(umin64(a.chunk_bytes, tv.nbytes - uint64_t(c) * a.chunk_bytes));
         const uint32_t n = len / W;
         const uint32_t *info = reinterpret_cast<const uint32_t *>(a.ws_info + 32ull * cl);
-        const uint32_t crc = info[0];
         uint32_t mode[4] = {0, 0, 0, 0}, val[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int j = 0; j < W; j++) {
@@ -1100,27 +1130,42 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
         const bool raw_chunk = !(double(grouped) < a.threshold * double(len));
         const uint64_t stored = raw_chunk ? len : grouped;
         bool timed;
-        const uint64_t off = table_end + lookback(a.ws_status + tv.chunk_base, c, pad16(stored), a.d_status, &timed);
+        const uint64_t off = table_end + lookback(a.ws_status + tv.chunk_base, c, pad16(stored), a.d_status, &timed,
+                                                 a.spin_limit, a.hooks);
         const bool fits = off + pad16(stored) <= tv.cap;
         if (!fits && lane == 0) status_or(a.d_status, ZC_ECAPACITY);
 
         if (fits && !timed) {
             uint8_t *out = tv.blob + off;
+            // CRC-32 of the stored bytes, taken as they are written: the
+            // register of each part taken from zero, appended in payload order
+            uint32_t reg;
             if (raw_chunk) {
+                // a copy of the chunk; its CRC from the written bytes (L2)
                 warp_copy_src(src, len, out);
+                __syncwarp();
+                reg = crc_strided<1, true, kCodeCrcCopies>(out, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr);
             } else {
-                if (lane < 4) {  // W words, zero-padded to 16 bytes
-                    uint32_t e = 0;
+                // directory: W words mode << 30 | value, zero-padded to 16 bytes
+                uint32_t e[4] = {0, 0, 0, 0};
 #pragma unroll
-                    for (int j = 0; j < W; j++)
-                        if (lane == j) e = (mode[j] << 30) | val[j];
-                    reinterpret_cast<uint32_t *>(out)[lane] = e;
-                }
-                warp_raw_streams<DT, kDelta>(src, n, mode, roff, out);
+                for (int j = 0; j < W; j++) e[j] = (mode[j] << 30) | val[j];
+                if (lane == 0) reinterpret_cast<uint4 *>(out)[0] = make_uint4(e[0], e[1], e[2], e[3]);
+                reg = crc_rep16<kCodeCrcCopies>(0xFFFFFFFFu, make_uint4(e[0], e[1], e[2], e[3]),
+                                                crc_row<kCodeCrcCopies>(crc_rep));
+                uint32_t part[4];
+                warp_raw_streams<DT, kDelta>(src, n, mode, roff, out, cs, part);
 #pragma unroll
                 for (int j = 0; j < W; j++)
-                    if (mode[j] == kModeRans) warp_copy(slot + uint64_t(j) * a.rec_stride, pad16(val[j]), out + roff[j]);
+                    if (mode[j] == kModeRans)
+                        part[j] = warp_copy_crc(slot + uint64_t(j) * a.rec_stride, pad16(val[j]), out + roff[j], cs);
+#pragma unroll
+                for (int j = 0; j < W; j++) {
+                    if (mode[j] == kModeConst) continue;
+                    reg = crc_append_small(reg, part[j], uint32_t(mode[j] == kModeRaw ? pad16(n) : pad16(val[j])));
+                }
             }
+            const uint32_t crc = reg ^ 0xFFFFFFFFu;
             if (lane == 0) {
                 uint4 ent;
                 ent.x = uint32_t(off);
@@ -1233,7 +1278,7 @@ template <int DT, bool kDelta>
 int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     constexpr int W = WordOf<DT>::W;
     const size_t ssm = sizeof(StatsSmem<W>);
-    const size_t csm = size_t(kCodeWarps) * kCodeWarpSmem;
+    const size_t csm = kCodeCrcBytes + size_t(kCodeWarps) * kCodeWarpSmem;
     if (cudaFuncSetAttribute(stats_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssm)) != cudaSuccess)
         return ZC_ECUDA;
     if (cudaFuncSetAttribute(code_kernel<DT, kDelta>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(csm)) != cudaSuccess)
@@ -1254,7 +1299,7 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
     const int sms = sms_of_device() < 1 ? 1 : sms_of_device();
     const uint32_t wpc = std::min<uint32_t>(kCodeWarps, (a.workers + sms - 1) / sms);
     const int cgrid = int((a.workers + wpc - 1) / wpc);
-    code_kernel<DT, kDelta><<<cgrid, 32 * wpc, size_t(wpc) * kCodeWarpSmem, s>>>(a);
+    code_kernel<DT, kDelta><<<cgrid, 32 * wpc, kCodeCrcBytes + size_t(wpc) * kCodeWarpSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 

@@ -1,6 +1,7 @@
 // zc_api.cu — the C ABI (include/zc.h): argument checks, workspace layout,
 // header construction and kernel launches. No entry point allocates device
 // memory or synchronises; device-side errors are reported through *d_status.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -110,7 +111,23 @@ void put64(uint8_t *p, uint64_t v) { for (int i = 0; i < 8; i++) p[i] = uint8_t(
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+std::atomic<uint32_t> g_hooks{0};
+
+// The wait limits of a call: short ones when a test hook makes a wait run out.
+void set_waits(EncodeArgs &a) {
+    a.hooks = g_hooks.load(std::memory_order_relaxed);
+    a.spin_limit = (a.hooks & ZC_HOOK_LOOKBACK_STALL) ? kSpinLimitTest : kSpinLimit;
+}
+void set_waits(DecodeArgs &a) {
+    a.hooks = g_hooks.load(std::memory_order_relaxed);
+    a.wait_cycles = (a.hooks & ZC_HOOK_PRODUCER_STALL) ? kWaitCyclesTest : kWaitCycles;
+}
+
 } // namespace
+
+extern "C" void zc_set_test_hooks(uint32_t hooks) {
+    g_hooks.store(hooks & (ZC_HOOK_LOOKBACK_STALL | ZC_HOOK_PRODUCER_STALL), std::memory_order_relaxed);
+}
 
 extern "C" uint64_t zc_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return 0;
@@ -356,6 +373,7 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
     a.chunk_bytes = chunk_bytes;
     a.threshold = threshold;
     a.version = version;
+    set_waits(a);
     if (!d_ws || !aligned(d_ws, 16)) return ZC_EINVAL;
     const uint64_t head = ctrl_bytes(n) + table_bytes(n);
     const uint64_t planes = hist_bytes(n, W, version) + ptab_bytes(n, W, version);
@@ -387,18 +405,35 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
     const uint64_t slot = slot_bytes(chunk_bytes, W, threshold);
     uint64_t wave = wave_chunks(nc, chunk_bytes, W);
     if (version == 2 && wave < max_tc) wave = max_tc;
-    uint64_t workers = max_workers(nc);
+    const uint64_t most_workers = max_workers(nc);
+    uint64_t workers = most_workers;
     const uint64_t avail = ws_bytes - fixed;
-    if (wave_layout(wave, W, chunk_bytes).slots + workers * slot > avail) {
-        // a full wave with fewer coding warps, else smaller waves
-        const uint64_t area = wave_layout(wave, W, chunk_bytes).slots;
-        if (area + slot <= avail) {
-            workers = (avail - area) / slot;
+    // room for a wave of w chunks with one coding warp per chunk (up to the
+    // warps that can run at once)
+    auto need = [&](uint64_t w) {
+        return wave_layout(w, W, chunk_bytes).slots + std::min<uint64_t>(w, most_workers) * slot;
+    };
+    if (need(wave) > avail) {
+        // A smaller workspace: the largest wave whose chunks all get a coding
+        // warp (more waves, each as parallel as the full one), since every
+        // chunk's rANS chain is a serial path that only more warps shorten.
+        uint64_t lo = 0, hi = wave;  // need(lo) fits (0: nothing), need(hi) does not
+        while (hi - lo > 1) {
+            const uint64_t mid = lo + (hi - lo) / 2;
+            if (need(mid) <= avail) lo = mid;
+            else hi = mid;
+        }
+        if (version == 2 && lo < max_tc) {
+            // v2 waves hold whole tensors: the largest tensor's statistics in
+            // one wave, with the coding warps that still fit
+            wave = max_tc;
+            const uint64_t area = wave_layout(wave, W, chunk_bytes).slots;
+            if (area + slot > avail) return ZC_ECAPACITY;
+            workers = std::min<uint64_t>((avail - area) / slot, most_workers);
         } else {
-            workers = 1;
-            const uint64_t per_chunk = kInfoBytes + (kTableBytes + n_pad(chunk_bytes, W)) * uint64_t(W);
-            wave = avail > slot + 768 ? (avail - slot - 768) / per_chunk : 0;
-            if (wave == 0 || (version == 2 && wave < max_tc)) return ZC_ECAPACITY;
+            if (lo == 0) return ZC_ECAPACITY;
+            wave = lo;
+            workers = std::min<uint64_t>(lo, most_workers);
         }
     }
     const WaveLayout lay = wave_layout(wave, W, chunk_bytes);
@@ -500,6 +535,7 @@ int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base,
     a.flags = flags;
     a.d_status = d_status;
     a.version = info->version;
+    set_waits(a);
     if (a.version == 2) {  // CTAs of a.pairs chunks
         a.pairs = decode_v2_pairs(a.total_chunks);
         a.n_ctas = (a.total_chunks + a.pairs - 1) / a.pairs;
@@ -676,7 +712,28 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
     a.chunk_bytes = chunk_bytes;
     a.flags = flags;
     a.d_status = d_status;
+    set_waits(a);
     return launch_decode(dtype, d_bases != nullptr, a, s);
+}
+
+extern "C" int zc_verify(const void *d_blob, const zc_info *info, int32_t *d_status, void *stream) {
+    if (!d_status || !info || !d_blob) return ZC_EINVAL;
+    const int W = word_bytes(info->dtype);
+    if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
+    if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
+    if (info->version != 1 && info->version != 2) return ZC_EINVAL;
+    const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks +
+                               (info->version == 2 ? 512ull * W : 0ull);
+    if (info->blob_bytes < table_end || !aligned(d_blob, 16)) return ZC_EINVAL;
+    const void *kb = nullptr;
+    if (kernel_address(d_blob, &kb) != ZC_OK) return ZC_EINVAL;
+    VerifyArgs a{};
+    a.blob = static_cast<const uint8_t *>(kb);
+    a.blob_bytes = info->blob_bytes;
+    a.table_end = table_end;
+    a.n_chunks = info->n_chunks;
+    a.d_status = d_status;
+    return launch_verify(a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream) {

@@ -213,7 +213,7 @@ constexpr uint32_t kCrcRepWords = crc_rep_words<8>();
 // 4 KB of tables whatever C is.
 template <int C = 8>
 __device__ inline void load_crc_rep(uint32_t *t) {
-    static_assert(C == 8 || C == 16, "8 or 16 table copies");
+    static_assert(C == 4 || C == 8 || C == 16, "4, 8 or 16 table copies");
     for (uint32_t e = threadIdx.x; e < 4 * 256; e += blockDim.x) {
         const uint32_t v = kCrc.t[e >> 8][e & 0xFFu];
         uint4 *d = reinterpret_cast<uint4 *>(t + e * C);
@@ -267,33 +267,95 @@ struct Strided {
     }
 };
 
+// Multiplying a register by a FIXED x^(8 2^J) mod P with no table: the
+// product is linear in the register, so it is the XOR of the images of the
+// register's set bits, 32 constants worked out at compile time (register
+// bit m is the coefficient of x^(31-m); its image is K x^(31-m)). About 64
+// integer instructions and no memory access, where a table lookup that
+// misses L1 costs an L2 round trip on the dependency chain.
+__host__ __device__ constexpr uint32_t x8pow2(int J) {  // x^(8 * 2^J) mod P
+    uint32_t k = 0x80000000u;                            // x^0
+    for (int i = 0; i < 8; i++) k = gf2_mul_x(k);
+    for (int i = 0; i < J; i++) k = gf2_mulmod(k, k);
+    return k;
+}
+
+// Column m: the image of register bit m under multiplication by K, i.e.
+// K x^(31-m) mod P.
+__host__ __device__ constexpr uint32_t mul_column(uint32_t K, int m) {
+    uint32_t v = K;
+    for (int i = 0; i < 31 - m; i++) v = gf2_mul_x(v);
+    return v;
+}
+
+template <int J, int M>
+__device__ __forceinline__ uint32_t mul_bits(uint32_t r) {
+    if constexpr (M == 32) {
+        return 0u;
+    } else {
+        constexpr uint32_t c = mul_column(x8pow2(J), M);
+        return ((0u - ((r >> M) & 1u)) & c) ^ mul_bits<J, M + 1>(r);
+    }
+}
+
+// Register shifted by 2^J bytes, in registers.
+template <int J>
+__device__ __forceinline__ uint32_t shift_pow2(uint32_t r) { return mul_bits<J, 0>(r); }
+
+template <int J, int END>
+__device__ __forceinline__ uint32_t shift_bits(uint32_t c, uint32_t n) {
+    if constexpr (J == END) {
+        return c;
+    } else {
+        if ((n >> J) & 1u) c = shift_pow2<J>(c);
+        return shift_bits<J + 1, END>(c, n);
+    }
+}
+
+// Register shifted by n < 2^20 bytes (a chunk's parts), in registers: one
+// constant multiply per set bit of n.
+static __device__ __noinline__ uint32_t shift_bytes_small(uint32_t c, uint32_t n) { return shift_bits<0, 20>(c, n); }
+
+// Register over A followed by B, from the register over A (any preset) and
+// the register over B taken from zero, B being len < 2^20 bytes (linearity).
+__device__ __forceinline__ uint32_t crc_append_small(uint32_t reg_a, uint32_t reg_b0, uint32_t len) {
+    return shift_bytes_small(reg_a, len) ^ reg_b0;
+}
+
+// Levels K .. KEND-1 of a fold tree over lanes: at level k a lane's register
+// moves over 2^(L2 + k) bytes and takes in the register of the lane 2^k
+// above it.
+template <int L2, int K, int KEND>
+__device__ __forceinline__ uint32_t fold_levels(uint32_t R) {
+    if constexpr (K == KEND) {
+        return R;
+    } else {
+        const uint32_t right = __shfl_down_sync(kFull, R, 1 << K);
+        return fold_levels<L2, K + 1, KEND>(shift_pow2<L2 + K>(R) ^ right);
+    }
+}
+
 // Fold the per-thread registers of a strided CRC into the range's register.
 // Each thread holds the register of its own pieces with all other bytes
 // taken as zero, ending at its last piece; CRC-32 is linear, so the range's
 // register is the XOR of those registers, each shifted by the bytes after
 // its thread's last piece: a tree over threads with shifts of piece, 2
-// pieces, ... (piece = 2^log2_piece bytes). NW > 1 uses s_reg[NW] and
+// pieces, ... (piece = 2^L2 bytes). NW > 1 uses s_reg[NW] and
 // __syncthreads (every thread of the CTA must call it). Returns the result
 // in every thread.
-template <int NW>
-__device__ inline uint32_t crc_fold(uint32_t R, int log2_piece, uint32_t *s_reg) {
+template <int NW, int L2>
+__device__ inline uint32_t crc_fold(uint32_t R, uint32_t *s_reg) {
     const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 0; k < 5; k++) {
-        const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
-        R = shift_by(R, kShPow + log2_piece + k) ^ right;
-    }
+    R = fold_levels<L2, 0, 5>(R);
     if constexpr (NW > 1) {
+        constexpr int kLevels = NW >= 16 ? 4 : NW >= 8 ? 3 : NW >= 4 ? 2 : 1;
+        static_assert((1 << kLevels) == NW, "NW is a power of two up to 16");
         const int warp = threadIdx.x >> 5;
         if (lane == 0) s_reg[warp] = R;
         __syncthreads();
         if (warp == 0) {
             R = lane < NW ? s_reg[lane] : 0u;
-#pragma unroll
-            for (int k = 0; (1 << k) < NW; k++) {
-                const uint32_t right = __shfl_down_sync(kFull, R, 1 << k);
-                R = shift_by(R, kShPow + log2_piece + 5 + k) ^ right;
-            }
+            R = fold_levels<L2 + 5, 0, kLevels>(R);
             if (lane == 0) s_reg[0] = R;
         }
         __syncthreads();
@@ -334,10 +396,40 @@ __device__ inline uint32_t crc_strided(const uint8_t *p, uint64_t len, uint32_t 
             cur = nxt;
             pidx += NT;
         }
-        reg = crc_fold<NW>(R, 4, s_reg);
+        reg = crc_fold<NW, 4>(R, s_reg);
     }
     for (uint64_t i = main; i < len; i++) reg = crc_rep_byte<C>(reg, kLdcg ? __ldcg(p + i) : __ldg(p + i), row);
     return reg;
+}
+
+// CRC register, taken from zero, of len bytes (a multiple of 16) at p
+// (16-byte aligned), by one warp: 16-byte pieces taken round-robin, aligned
+// to the end of the range (only the first round can be short), with U
+// loads in flight per lane, so that a short range costs about one memory
+// latency per U rounds instead of one per round.
+template <int C, bool kLdcg, int U = 8>
+__device__ inline uint32_t warp_crc16(const uint8_t *p, uint32_t len, const uint32_t *T, const uint32_t (*G)[256]) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t *row = crc_row<C>(T);
+    const uint32_t pieces = len / 16;
+    const uint32_t rounds = (pieces + 31) / 32, v0 = rounds * 32 - pieces;
+    uint32_t R = 0;
+    for (uint32_t r0 = 0; r0 < rounds; r0 += U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t v = int64_t(32) * (r0 + u) + lane - v0;
+            t[u] = (r0 + u < rounds && v >= 0) ? load16<kLdcg>(p + 16 * v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const uint32_t r = r0 + u;
+            if (r >= rounds) break;
+            if (r > 0) R = shift_smem(R, G);
+            if (int64_t(32) * r + lane >= v0) R = crc_rep16<C>(R, t[u], row);
+        }
+    }
+    return rounds ? crc_fold<1, 4>(R, nullptr) : 0u;
 }
 
 // As crc_strided, for a range that need not be 16-byte aligned: the bytes up

@@ -45,6 +45,8 @@ struct EncodeArgs {
     uint32_t wave_t0, wave_t1;
     unsigned long long *ws_hist;    // v2: per tensor and plane, 256 u64 counts over the tensor
     uint8_t *ws_ptab;               // v2: per tensor and plane, the 12-bit table (256 u16)
+    uint32_t hooks;                 // test hooks (zc_set_test_hooks)
+    uint32_t spin_limit;            // polls of one look-back wait before it gives up
 };
 
 // One blob of a decompression call.
@@ -71,6 +73,22 @@ struct DecodeArgs {
     uint32_t version;               // 1 or 2 (every blob of the call)
     uint32_t pairs;                 // v2: chunks (warp pairs) per CTA
     uint32_t n_ctas;                // v2: CTAs of the call
+    uint32_t hooks;                 // test hooks (zc_set_test_hooks)
+    unsigned long long wait_cycles; // clock cycles of one barrier wait before it gives up
+};
+
+// Wait limits: about a second of polling in normal calls, a short one under
+// the test hooks that make a wait run out.
+constexpr uint32_t kSpinLimit = 1u << 22, kSpinLimitTest = 1u << 10;
+constexpr unsigned long long kWaitCycles = 1ull << 31, kWaitCyclesTest = 1ull << 20;
+
+// zc_verify: a blob's header CRC and every chunk's CRC, without decoding.
+struct VerifyArgs {
+    const uint8_t *blob;
+    uint64_t blob_bytes;
+    uint64_t table_end;      // header + chunk table (v2: + plane tables)
+    uint32_t n_chunks;
+    int32_t *d_status;
 };
 
 struct CrcArgs {
@@ -110,5 +128,6 @@ int encode_warps_per_sm();
 // delta: whether the blobs carry base tensors (all or none of them)
 int launch_decode(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s);
 int launch_crc(const CrcArgs &a, cudaStream_t s);
+int launch_verify(const VerifyArgs &a, cudaStream_t s);
 
 } // namespace zc

@@ -11,12 +11,21 @@
 //
 // The array is kStaticScratchBytes (64 MiB) in every device's memory once the
 // library's code for this file is loaded on that device, and stays there
-// until the process exits. All calls share it: calls that overlap on the GPU
-// (on different streams, or from different host threads without ordering)
-// race on it and corrupt each other's results; callers must order them. The
-// first call on each device looks up the array's device address (once per
-// device, with that device current); that first call should therefore be
-// made before any stream capture begins.
+// until the process exits. Under CUDA's lazy module loading (the default) the
+// code is loaded, and the 64 MiB committed, by the first call on a device:
+// a caller whose memory pool reserves all free memory at start-up should make
+// that first call before the pool does. All calls share the array: calls
+// that overlap on the GPU (on different streams, or from different host
+// threads without ordering) race on it and corrupt each other's results;
+// callers must order them. The first call on each device looks up the
+// array's device address (once per device, with that device current); that
+// first call should therefore be made before any stream capture begins. The
+// address is kept for the life of the process: after cudaDeviceReset the
+// caller must not use this entry point on that device again.
+//
+// With 64 MiB the workspace planner runs waves of about 250 chunks (FP32,
+// 128 KiB chunks), each with a coding warp per chunk, so a tensor larger than
+// a wave is compressed in several waves on the same stream.
 #include <mutex>
 
 #include "zc_kernels.cuh"
@@ -55,7 +64,9 @@ extern "C" int zc_compress_noalloc(const void *d_src, uint64_t nbytes, int dtype
                                    uint32_t chunk_bytes, double threshold,
                                    void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,
                                    int32_t *d_status, void *stream) {
-    if (chunk_bytes == 0) return ZC_EINVAL;
+    // the parameters are checked first, so that an invalid call is reported
+    // as such whatever its size
+    if (zc_workspace_size(nbytes, dtype, chunk_bytes) == 0) return ZC_EINVAL;
     const uint64_t n_chunks = (nbytes + chunk_bytes - 1) / chunk_bytes;
     if (n_chunks > kStaticMaxChunks) return ZC_ECAPACITY;  // tensor too large for the fixed scratch
     void *scratch = nullptr;

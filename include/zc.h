@@ -40,8 +40,12 @@
  *     dtype, ndim, chunk_bytes, lanes = 32, prob_bits = 12, nbytes,
  *     n_chunks, header CRC-32 over header + chunk table, shape[8]); a chunk
  *     table of 16-byte entries {u64 offset, u32 stored | raw << 31, u32
- *     CRC-32 of the chunk's original bytes}; then the chunk payloads, each zero-padded
- *     to 16 bytes. All integers little-endian.
+ *     CRC-32 of the chunk's `stored` payload bytes at `offset`}; then the
+ *     chunk payloads, each zero-padded to 16 bytes. All integers
+ *     little-endian. The chunk CRCs are over pieces of the blob (cuZipNN API:
+ *     CRC-32 helpers over checksum-sized pieces, used to check an untrusted
+ *     blob before decompressing it), so zc_verify can check a blob without
+ *     decoding it.
  */
 #ifndef ZC_H
 #define ZC_H
@@ -122,6 +126,21 @@ ZC_API uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk_byt
  * layout exactly. Returns ZC_OK, ZC_EFORMAT or ZC_ECRC. Host only. */
 ZC_API int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *out);
 
+/* Check a blob without decoding it (cuZipNN API: verify an untrusted blob
+ * with the CRC-32 helpers before decompress_tensor). On the device, over the
+ * blob as it is in memory: the header CRC-32 (header with its CRC field read
+ * as zero, chunk table, and for format v2 the plane tables) and each chunk's
+ * CRC-32 over its stored bytes; a table entry that points outside
+ * info->blob_bytes is reported as ZC_EFORMAT and not read.
+ *   d_blob     the blob (device or page-locked host memory, 16-byte aligned)
+ *   info       from zc_blob_info on a host copy of the blob's prefix
+ *   d_status   device int32, OR-ed with ZC_ECRC / ZC_EFORMAT
+ * Returns ZC_EINVAL for inconsistent info or unusable pointers (nothing
+ * launched), ZC_ECUDA for a launch error, else ZC_OK. One launch, no
+ * allocation, no synchronisation. A blob that passes decodes with
+ * zc_decompress without a CRC error. */
+ZC_API int zc_verify(const void *d_blob, const zc_info *info, int32_t *d_status, void *stream);
+
 /* Compress a contiguous row-major tensor (cuZipNN Usage: tensor in,
  * self-describing blob out).
  *   d_src        nbytes of input, aligned to the element size
@@ -146,13 +165,16 @@ ZC_API int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, 
  *   d_blob       the blob (info->blob_bytes bytes)
  *   d_dst        output, dst_capacity >= info->nbytes, aligned to the
  *                element size
- *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check, which is
- *                taken over the bytes the chunk decoded to)
+ *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check)
  *   d_status     device int32, OR-ed with ZC_ECRC / ZC_ECORRUPT / ZC_EFORMAT
- * The output bytes of a chunk that fails a check are unspecified; any
+ * With the check, each chunk's CRC-32 is taken over its stored bytes in the
+ * same pass that reads them for decoding, and compared at the end of the
+ * chunk. The output bytes of a chunk that fails a check are unspecified; any
  * nonzero status means the tensor must not be used. Every device read is
- * bounds-checked against the blob; writes stay within the first
- * info->nbytes bytes of d_dst. */
+ * bounds-checked against the blob, so a damaged blob is never read or
+ * written out of bounds; writes stay within the first info->nbytes bytes of
+ * d_dst. To reject an untrusted blob before any output is written, call
+ * zc_verify first. */
 ZC_API int zc_decompress(const void *d_blob, const zc_info *info, void *d_dst, uint64_t dst_capacity,
                   uint32_t flags, int32_t *d_status, void *stream);
 
@@ -176,8 +198,8 @@ ZC_API int zc_compress_delta(const void *d_base, const void *d_new, uint64_t nby
 
 /* Decompress a blob made by zc_compress_delta (or by zc_compress of a
  * difference) and XOR it with the base in the same pass: d_dst receives
- * base XOR decoded. The per-chunk CRC is checked over the decoded difference
- * (the bytes the blob holds), unless flags has ZC_NO_VERIFY.
+ * base XOR decoded. The per-chunk CRC is checked over the stored bytes, as
+ * in zc_decompress, unless flags has ZC_NO_VERIFY.
  *   info           from zc_blob_info; its dtype must be ZC_U8/U16/U32
  *   d_base, d_dst  device buffers of info->nbytes bytes, 16-byte aligned;
  *                  d_dst may not overlap d_base or the blob
@@ -271,6 +293,24 @@ ZC_API uint64_t zc_blob_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes
  * stream by this call before the kernel runs. */
 ZC_API int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, uint32_t *d_out, void *stream);
 
+/* Test hooks, for the library's own tests of its bounded waits (not for
+ * use in production). Every device wait of the library gives up after a
+ * limit and reports ZC_ETIMEOUT instead of hanging; these hooks make a wait
+ * run out on purpose, with a short limit (about a millisecond), so that a
+ * test can check that the kernel then returns and reports it.
+ *   ZC_HOOK_LOOKBACK_STALL  compression: the first chunk of each tensor
+ *                           never publishes its offset, so the other chunks'
+ *                           offset-scan (look-back) waits run out; those
+ *                           chunks are not written
+ *   ZC_HOOK_PRODUCER_STALL  decompression: the warp that runs a chunk's rANS
+ *                           lanes stops before it signals anything, so the
+ *                           partner warp's barrier wait runs out
+ * zc_set_test_hooks sets the hooks (0 = none, the default) for the calls
+ * that the process makes afterwards, from any thread. */
+#define ZC_HOOK_LOOKBACK_STALL 1u
+#define ZC_HOOK_PRODUCER_STALL 2u
+ZC_API void zc_set_test_hooks(uint32_t hooks);
+
 /* Compression without any device allocation: the same work and the same
  * output as zc_compress, but the workspace comes from a fixed 64 MiB scratch
  * array that the library keeps in device memory (none of the source pages
@@ -287,7 +327,17 @@ ZC_API int zc_crc32(const void *d_data, uint64_t nbytes, uint64_t piece_bytes, u
  *   streams, or unordered host threads) race and must be ordered by the
  *   caller.
  *   The first call on a device looks up the array's address on that device;
- *   make that first call before starting any stream capture. */
+ *   make that first call before starting any stream capture. Under CUDA's
+ *   lazy module loading (the default) that first call also loads this part
+ *   of the library and so commits the 64 MiB: a caller whose memory pool
+ *   reserves all free device memory at start-up should make it before the
+ *   pool does. The address is kept for the rest of the process; after
+ *   cudaDeviceReset this entry point must not be used on that device again.
+ *   Arguments are checked as in zc_compress first (ZC_EINVAL), then the
+ *   chunk limit (ZC_ECAPACITY). The 64 MiB holds the offset-scan words and
+ *   a wave of per-chunk statistics with a coding warp per chunk (about 250
+ *   chunks of 128 KiB FP32); a larger tensor is compressed in several waves
+ *   on the stream. */
 ZC_API int zc_compress_noalloc(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
                                uint32_t chunk_bytes, double threshold,
                                void *d_blob, uint64_t blob_capacity, uint64_t *d_blob_bytes,

@@ -21,6 +21,6 @@ def test_reference_arm_prints_one_valid_line():
               "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
-    assert d["config"]["workload"] == "fp32_64m"
+    assert d["config"]["workload"] == "llama8b"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

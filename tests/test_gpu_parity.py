@@ -3,9 +3,9 @@
 Integer/byte work, so the bar is bit-exactness everywhere: GPU blobs equal
 oracle blobs byte for byte, GPU decoding restores the input exactly (from
 both GPU and oracle blobs), and the oracle decodes GPU blobs. Inputs are the
-seeded synthetic workloads (tests use every configuration at full size; the
-16 GB Llama-shaped set is checked on whole small tensors and sampled chunks
-of the large ones) plus edge cases: empty, ragged, tiny, constant, NaN-laden,
+seeded synthetic workloads (every configuration at full size; the 16 GB
+Llama-shaped model, every tensor, is in test_gpu_llama8b_full.py) plus edge
+cases: empty, ragged, tiny, constant, NaN-laden,
 near the passthrough threshold, many chunks, unaligned pointers, corrupted
 blobs.
 """
@@ -259,41 +259,6 @@ def test_workload_bf16_delta(zco):
     assert len(blob) < 0.4 * x.numel() * 2
 
 
-def test_workload_llama8b_sampled(zco):
-    """Whole small tensors of the Llama-3.1-8B-shaped set and sampled chunks
-    of the big ones; table properties checked on every chunk."""
-    specs = wl.llama8b_specs()
-    for idx in (1, 2, 3, 8, 9, 10):          # layer 0: q, k, v, input_norm, post_norm, layer 1 q
-        name, shape = specs[idx]
-        _check_tensor(zco, wl.llama8b_tensor(idx, name, shape, DEV))
-    rng = np.random.default_rng(0)
-    for idx in (0, 5, len(specs) - 1):      # embedding, gate, lm_head
-        name, shape = specs[idx]
-        t = wl.llama8b_tensor(idx, name, shape, DEV)
-        blob = zc.compress(t)
-        host = blob.cpu().numpy().tobytes()
-        info = zc.blob_info(host)
-        nc = info["n_chunks"]
-        raw_dev = wl.as_bytes(t)
-        off_prev = 96 + 16 * nc
-        entries = [struct.unpack_from("<QII", host, 96 + 16 * c) for c in range(nc)]
-        for c, (off, sm, _) in enumerate(entries):          # the prefix scan, every chunk
-            assert off == off_prev
-            off_prev += (sm & 0x7FFFFFFF) + 15 & ~15
-        assert off_prev == len(host)
-        for c in sorted(set(rng.integers(0, nc, 24).tolist()) | {0, nc - 1}):
-            off, sm, crc = entries[c]
-            chunk = raw_dev[c * 131072:(c + 1) * 131072].cpu().numpy()
-            payload, raw_flag = zco.encode_chunk(chunk, 4, 0.95)
-            stored = sm & 0x7FFFFFFF
-            assert host[off:off + stored] == payload and (sm >> 31) == raw_flag
-            assert crc == zlib.crc32(chunk.tobytes())   # the chunk's original bytes
-        back = zc.decompress(blob)
-        assert torch.equal(back.view(torch.int16), t.view(torch.int16))
-        del t, blob, back, raw_dev
-        torch.cuda.empty_cache()
-
-
 # ------------------------------------------------------------ corruption
 
 def test_corrupted_blobs_are_rejected(zco):
@@ -314,6 +279,69 @@ def test_corrupted_blobs_are_rejected(zco):
         st2, _ = gpu_decompress_bytes(bytes(bad), verify=False)
         assert st2 in (0, zc.ECORRUPT, zc.EFORMAT)
     assert hits > 150
+
+
+def test_verify_matches_oracle(zco):
+    """zc_verify checks a blob without decoding it (cuZipNN API: verify an
+    untrusted blob first). It passes every intact blob, and for a blob with
+    one changed byte it reports exactly what the oracle's check reports for
+    a payload or padding byte, and an error whenever the oracle does for a
+    header or table byte (the device check sees the header CRC fail where the
+    oracle may first see a malformed field)."""
+    rng = np.random.default_rng(41)
+    cases = [(wl.as_bytes(wl.bf16_1m("cpu")[:96]).numpy(), 4, 4096, 1),
+             (wl.as_bytes(wl.fp32_64m("cpu", rows=8)).numpy(), 6, 65536, 1),
+             (rng.integers(0, 256, 70001, dtype=np.uint8), 1, 4096, 1),   # RAW chunks, ragged tail
+             (wl.as_bytes(wl.bf16_1m("cpu")[:64]).numpy(), 4, 8192, 2)]
+    for raw, dt, C, ver in cases:
+        blob = zco.compress(raw, dt, None, C, 0.95, version=ver)
+        info = zc.blob_info(blob)
+        table_end = 96 + 16 * info["n_chunks"] + (512 * W_OF[dt] if ver == 2 else 0)
+        good = torch.from_numpy(np.frombuffer(blob, np.uint8).copy()).to(DEV)
+        assert zc.verify(good, info) == 0 and zco.verify(blob) == 0
+        # a GPU blob of the same tensor passes too
+        if ver == 1:
+            gb = gpu_compress_bytes(raw, dt, (raw.size // W_OF[dt],), C, 0.95)
+            assert zc.verify(torch.from_numpy(np.frombuffer(gb, np.uint8).copy()).to(DEV)) == 0
+        positions = list(rng.integers(0, len(blob), 120)) + list(range(0, 96, 5)) + [table_end - 1, len(blob) - 1]
+        for pos in positions:
+            bad = bytearray(blob)
+            bad[int(pos)] ^= int(rng.integers(1, 256))
+            dev = torch.from_numpy(np.frombuffer(bytes(bad), np.uint8).copy()).to(DEV)
+            st = zc.verify(dev, info)
+            want = zco.verify(bytes(bad))
+            if pos >= table_end:
+                assert st == want, (dt, ver, int(pos), st, want)
+            else:
+                assert (st != 0) == (want != 0) and st & (zc.ECRC | zc.EFORMAT), (dt, ver, int(pos), st, want)
+    # a table entry pointing past the blob: a format error, no read
+    raw, dt, C, _ = cases[0]
+    blob = bytearray(zco.compress(raw, dt, None, C, 0.95))
+    info = zc.blob_info(bytes(blob))
+    struct.pack_into("<Q", blob, 96 + 16 * 2, 1 << 40)
+    dev = torch.from_numpy(np.frombuffer(bytes(blob), np.uint8).copy()).to(DEV)
+    assert zc.verify(dev, info) & zc.EFORMAT
+
+
+def test_decode_reports_changed_payload_as_crc(zco):
+    """A changed payload byte fails its chunk's CRC over the stored bytes in
+    decoding too; the other chunks decode exactly."""
+    rng = np.random.default_rng(43)
+    raw = wl.as_bytes(wl.bf16_1m("cpu")[:64]).numpy()
+    C = 8192
+    blob = zco.compress(raw, 4, None, C, 0.95)
+    nc = struct.unpack_from("<I", blob, 24)[0]
+    for c in range(0, nc, 3):
+        off, sm, _ = struct.unpack_from("<QII", blob, 96 + 16 * c)
+        stored = sm & 0x7FFFFFFF
+        for pos in (off, off + stored - 1, off + int(rng.integers(0, stored))):
+            bad = bytearray(blob)
+            bad[pos] ^= 0x10
+            st, out = gpu_decompress_bytes(bytes(bad))
+            assert st & zc.ECRC, (c, pos)
+            keep = np.ones(raw.size, bool)
+            keep[c * C:(c + 1) * C] = False
+            assert (out[keep] == raw[keep]).all()
 
 
 def test_corrupted_table_entry_device_checks():

@@ -66,6 +66,16 @@ def test_noalloc_matches_compress_on_consecutive_calls():
     cases = [(wl.fp32_64m(dev, rows=2048), 131072, 0.95),     # 64 MiB FP32, 512 chunks
              (wl.bf16_1m(dev), 131072, 0.95),
              (wl.bf16_1m(dev)[:200], 4096, 2.0)]
+    # near the chunk limit: 2^20 - 1 chunks of 64 bytes, the last one ragged;
+    # constant and random chunks, so both grouped and raw chunks appear. The
+    # 8-byte status word per chunk then takes 8 MiB of the array, and the
+    # statistics run in many waves
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    n = ((1 << 20) - 1) * 64 - 17
+    many = torch.randint(0, 256, (n,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    many.view(-1)[: (n // 128) * 128].view(-1, 128)[:, :64] = 7
+    cases.append((many, 64, 0.95))
     for t, chunk, thr in cases:
         ref = _compress(t, chunk, thr)
         first = _compress_noalloc(t, chunk, thr)
@@ -74,6 +84,21 @@ def test_noalloc_matches_compress_on_consecutive_calls():
         assert second == ref
         back = zc.decompress(torch.frombuffer(bytearray(second), dtype=torch.uint8).to(dev))
         assert torch.equal(back.view(torch.uint8), t.view(torch.uint8))
+
+
+def test_noalloc_checks_arguments_before_its_limit():
+    """An invalid call is reported as invalid (ZC_EINVAL) whatever its size,
+    and only a valid one beyond the chunk limit as ZC_ECAPACITY."""
+    dev = torch.device("cuda:0")
+    t = torch.zeros(16, dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    big = (1 << 20) * 64 + 64
+    for nbytes, dtype, chunk in ((big, 1, 1), (big, 9, 64), (big + 1, 2, 64)):
+        shape = (ctypes.c_int64 * 1)(nbytes)
+        rc = _noalloc_fn()(t.data_ptr(), nbytes, dtype, 1, shape, chunk, 0.95, t.data_ptr(), 16,
+                           nb.data_ptr(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == zc.EINVAL, (nbytes, dtype, chunk, rc)
 
 
 def test_noalloc_rejects_tensors_beyond_its_scratch():
