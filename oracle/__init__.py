@@ -80,6 +80,13 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint64)]
             L.zco_decompress.restype = ctypes.c_int
             L.zco_decompress.argtypes = [c_u8p, ctypes.c_uint64, c_u8p, ctypes.c_uint64, ctypes.c_uint32]
+            L.zco_rans_record_lanes.restype = ctypes.c_uint64
+            L.zco_rans_record_lanes.argtypes = [c_u8p, ctypes.c_uint32, c_u8p, ctypes.c_uint64]
+            L.zco_rans_decode_lanes.restype = ctypes.c_int
+            L.zco_rans_decode_lanes.argtypes = [c_u8p, ctypes.c_uint64, ctypes.c_uint32, c_u8p]
+            L.zco_encode_chunk_lanes.restype = ctypes.c_uint64
+            L.zco_encode_chunk_lanes.argtypes = [c_u8p, ctypes.c_uint32, ctypes.c_int, ctypes.c_double,
+                                                 c_u8p, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int)]
             L.zco_verify.restype = ctypes.c_int
             L.zco_verify.argtypes = [c_u8p, ctypes.c_uint64]
             L.zco_normalize64.restype = ctypes.c_int
@@ -168,14 +175,36 @@ def rans_decode(record: bytes, n: int) -> np.ndarray:
     return out[:n]
 
 
-def encode_chunk(chunk, dtype: int, threshold: float = 0.95) -> tuple[bytes, bool]:
-    """One chunk's stored payload (unpadded) and whether it is a RAW chunk."""
+def rans_record_lanes(symbols) -> bytes:
+    """Format v3 record: a word list per lane."""
+    s = _u8(symbols)
+    cap = 160 + 512 + 64 + 2 * s.size + 8 * 32 + 16
+    rec = np.zeros(cap, np.uint8)
+    r = lib().zco_rans_record_lanes(_ptr(s), s.size, _ptr(rec), cap)
+    if r == 0:
+        raise OracleError(EINVAL, "rans_record_lanes")
+    return rec[:r].tobytes()
+
+
+def rans_decode_lanes(record: bytes, n: int) -> np.ndarray:
+    r = np.frombuffer(record, np.uint8).copy()
+    out = np.zeros(max(n, 1), np.uint8)
+    st = lib().zco_rans_decode_lanes(_ptr(r), r.size, n, _ptr(out))
+    if st:
+        raise OracleError(st, "rans_decode_lanes")
+    return out[:n]
+
+
+def encode_chunk(chunk, dtype: int, threshold: float = 0.95, version: int = 1) -> tuple[bytes, bool]:
+    """One chunk's stored payload (unpadded) and whether it is a RAW chunk
+    (format v1, or v3 with a word list per lane)."""
     d = _u8(chunk)
     W = WORD_BYTES[dtype]
-    cap = 16 + W * (160 + 512 + 2 * (d.size // W) + 16) + d.size
+    cap = 16 + W * (160 + 512 + 64 + 8 * 32 + 2 * (d.size // W) + 16) + d.size
     out = np.zeros(cap, np.uint8)
     raw = ctypes.c_int(0)
-    r = lib().zco_encode_chunk(_ptr(d), d.size, dtype, threshold, _ptr(out), cap, ctypes.byref(raw))
+    fn = lib().zco_encode_chunk_lanes if version == 3 else lib().zco_encode_chunk
+    r = fn(_ptr(d), d.size, dtype, threshold, _ptr(out), cap, ctypes.byref(raw))
     if r == 0:
         raise OracleError(ECAPACITY, "encode_chunk")
     return out[:r].tobytes(), bool(raw.value)
@@ -188,8 +217,8 @@ def blob_size(nbytes: int, dtype: int, chunk_bytes: int = 131072, threshold: flo
 
 def compress(data, dtype: int, shape=None, chunk_bytes: int = 131072, threshold: float = 0.95,
              version: int = 1) -> bytes:
-    """Blob of a tensor in format v1 (a table per coded stream) or v2 (shared
-    plane tables)."""
+    """Blob of a tensor in format v1 (a table per coded stream), v2 (shared
+    plane tables) or v3 (v1 with a word list per lane in each record)."""
     d = _u8(data)
     W = WORD_BYTES[dtype]
     if shape is None:

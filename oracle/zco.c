@@ -41,6 +41,13 @@
  *   renormalisation words in the order the encoder emitted them (a decoder
  *   consumes them from the last one backwards).
  *
+ * Blob format v3 (a word list per lane) differs from v1 in the RANS record
+ * only: after v1's head (32 final states, presence bitmap, frequencies, zero
+ * pad to 16) come 32 x u16 word counts c_0 .. c_31, then for lane 0 .. 31
+ * the c_l words that lane emitted, in the order it emitted them (a decoder
+ * consumes each list from its end backwards), each list zero-padded to a
+ * multiple of 4 words. Record bytes = head + 64 + 2 * sum pad4(c_l).
+ *
  * Blob format v2 (shared tables; lmz "Building on lmz": one table per plane
  * kind for many chunks) differs from v1 in three places only:
  *   - version = 2;
@@ -338,6 +345,145 @@ int zco_rans_decode(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t 
     return ZCO_OK;
 }
 
+/* ------------------------------------------ format v3: a word list per lane */
+
+/* lmz "On a GPU": a GPU rANS decoder is bound by the dependent chain of each
+ * lane's steps. With one word list for all lanes (v1), where a lane's next
+ * word lies depends on how many words the lanes before it took in the same
+ * step, so every step of every lane also waits on the other lanes. A v3
+ * record gives each lane its own list (see the top of this file); the coding
+ * steps are exactly zco_rans_record's, only the place a word is written
+ * differs. */
+static uint64_t pad4w(uint64_t words) { return (words + 3u) & ~(uint64_t)3u; }
+
+uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uint64_t rec_cap) {
+    uint32_t counts[256] = {0}, f[256], cum[257];
+    for (uint32_t i = 0; i < n; i++) counts[sym[i]]++;
+    if (zco_normalize(counts, n, f) != ZCO_OK) return 0;
+    cum[0] = 0;
+    for (int s = 0; s < 256; s++) cum[s + 1] = cum[s] + f[s];
+
+    uint32_t k = 0;
+    for (int s = 0; s < 256; s++) k += f[s] ? 1u : 0u;
+    const uint64_t head = ZCO_REC_HEAD + pad16(2u * (uint64_t)k);
+    const uint64_t lists_at = head + 2u * ZCO_LANES;
+    uint32_t T = (n + ZCO_LANES - 1) / ZCO_LANES;
+
+    /* each lane's words in the order it emits them */
+    uint16_t *lw = (uint16_t *)malloc(((size_t)ZCO_LANES * T + 1) * sizeof(uint16_t));
+    if (!lw) return 0;
+    uint32_t c[ZCO_LANES] = {0};
+    uint32_t x[ZCO_LANES];
+    for (uint32_t l = 0; l < ZCO_LANES; l++) x[l] = ZCO_L;
+    for (uint32_t t = T; t-- > 0;) {
+        for (uint32_t l = ZCO_LANES; l-- > 0;) {
+            uint64_t i = (uint64_t)t * ZCO_LANES + l;
+            if (i >= n) continue;
+            uint32_t s = sym[i];
+            if (x[l] >= (f[s] << 20)) {
+                lw[(uint64_t)l * T + c[l]] = (uint16_t)(x[l] & 0xFFFFu);
+                c[l]++;
+                x[l] >>= 16;
+            }
+            x[l] = ((x[l] / f[s]) << ZCO_PROB_BITS) + (x[l] % f[s]) + cum[s];
+        }
+    }
+
+    uint64_t size = lists_at;
+    for (uint32_t l = 0; l < ZCO_LANES; l++) size += 2u * pad4w(c[l]);
+    if (size > rec_cap) {
+        free(lw);
+        return 0;
+    }
+    memset(rec, 0, (size_t)size);
+    for (uint32_t l = 0; l < ZCO_LANES; l++) put32(rec + 4 * l, x[l]);
+    uint8_t *bitmap = rec + 4 * ZCO_LANES;
+    uint8_t *freqs = bitmap + 32;
+    uint32_t j = 0;
+    for (int s = 0; s < 256; s++) {
+        if (!f[s]) continue;
+        bitmap[s >> 3] |= (uint8_t)(1u << (s & 7));
+        put16(freqs + 2 * j, f[s]);
+        j++;
+    }
+    uint64_t off = lists_at;
+    for (uint32_t l = 0; l < ZCO_LANES; l++) {
+        put16(rec + head + 2 * l, c[l]);
+        for (uint32_t q = 0; q < c[l]; q++) put16(rec + off + 2u * q, lw[(uint64_t)l * T + q]);
+        off += 2u * pad4w(c[l]);
+    }
+    free(lw);
+    return size;
+}
+
+/* Inverse of zco_rans_record_lanes: zco_rans_decode's steps, with lane l
+ * taking its words from the end of its own list backwards. The counts must
+ * describe the record exactly and the padding must be zero. */
+int zco_rans_decode_lanes(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t *sym) {
+    if (rec_bytes < ZCO_REC_HEAD) return ZCO_ECORRUPT;
+    const uint8_t *bitmap = rec + 4 * ZCO_LANES;
+    const uint8_t *freqs = bitmap + 32;
+    uint32_t f[256], cum[257];
+    uint32_t k = 0;
+    for (int s = 0; s < 256; s++) k += (bitmap[s >> 3] >> (s & 7)) & 1u;
+    const uint64_t head = ZCO_REC_HEAD + pad16(2u * (uint64_t)k);
+    const uint64_t lists_at = head + 2u * ZCO_LANES;
+    if (k < 2 || rec_bytes < lists_at) return ZCO_ECORRUPT;
+    for (uint64_t b = ZCO_REC_HEAD + 2u * k; b < head; b++)
+        if (rec[b]) return ZCO_ECORRUPT;
+    uint32_t j = 0;
+    for (int s = 0; s < 256; s++) {
+        f[s] = 0;
+        if ((bitmap[s >> 3] >> (s & 7)) & 1u) {
+            f[s] = get16(freqs + 2 * j);
+            j++;
+            if (f[s] == 0 || f[s] >= ZCO_M) return ZCO_ECORRUPT;
+        }
+    }
+    cum[0] = 0;
+    for (int s = 0; s < 256; s++) cum[s + 1] = cum[s] + f[s];
+    if (cum[256] != ZCO_M) return ZCO_ECORRUPT;
+
+    uint64_t base[ZCO_LANES], left[ZCO_LANES];
+    uint64_t off = lists_at;
+    for (uint32_t l = 0; l < ZCO_LANES; l++) {
+        uint32_t c = get16(rec + head + 2 * l);
+        base[l] = off;
+        left[l] = c;
+        off += 2u * pad4w(c);
+        if (off > rec_bytes) return ZCO_ECORRUPT;
+        for (uint64_t q = c; q < pad4w(c); q++)
+            if (get16(rec + base[l] + 2u * q)) return ZCO_ECORRUPT;
+    }
+    if (off != rec_bytes) return ZCO_ECORRUPT;
+
+    uint32_t x[ZCO_LANES];
+    for (uint32_t l = 0; l < ZCO_LANES; l++) {
+        x[l] = get32(rec + 4 * l);
+        if (x[l] < ZCO_L) return ZCO_ECORRUPT;
+    }
+    uint32_t T = (n + ZCO_LANES - 1) / ZCO_LANES;
+    for (uint32_t t = 0; t < T; t++) {
+        for (uint32_t l = 0; l < ZCO_LANES; l++) {
+            uint64_t i = (uint64_t)t * ZCO_LANES + l;
+            if (i >= n) continue;
+            uint32_t slot = x[l] & (ZCO_M - 1);
+            uint32_t s = 0;
+            while (!(cum[s] <= slot && slot < cum[s + 1])) s++;
+            x[l] = f[s] * (x[l] >> ZCO_PROB_BITS) + slot - cum[s];
+            if (x[l] < ZCO_L) {
+                if (left[l] == 0) return ZCO_ECORRUPT;
+                left[l]--;
+                x[l] = (x[l] << 16) | get16(rec + base[l] + 2u * left[l]);
+            }
+            sym[i] = (uint8_t)s;
+        }
+    }
+    for (uint32_t l = 0; l < ZCO_LANES; l++)
+        if (x[l] != ZCO_L || left[l] != 0) return ZCO_ECORRUPT;
+    return ZCO_OK;
+}
+
 /* ---------------------------------------------------------------- chunks */
 
 /* ZipNN Method 3: all-zero streams are truncated to a header (generalised
@@ -347,12 +493,28 @@ int zco_rans_decode(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t 
  * incompressible groups at 100% beside a coded exponent) and again per chunk
  * (an incompressible chunk then decodes as a copy); "below" is strict and the
  * comparison is in IEEE double. */
+static uint64_t encode_chunk_v(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                               uint8_t *out, uint64_t cap, int *mode_raw, int lanes);
+
 uint64_t zco_encode_chunk(const uint8_t *src, uint32_t len, int dtype, double threshold,
                           uint8_t *out, uint64_t cap, int *mode_raw) {
+    return encode_chunk_v(src, len, dtype, threshold, out, cap, mode_raw, 0);
+}
+
+/* One chunk in format v3 (a word list per lane in every RANS record). */
+uint64_t zco_encode_chunk_lanes(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                                uint8_t *out, uint64_t cap, int *mode_raw) {
+    return encode_chunk_v(src, len, dtype, threshold, out, cap, mode_raw, 1);
+}
+
+static uint64_t encode_chunk_v(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                               uint8_t *out, uint64_t cap, int *mode_raw, int lanes) {
     int W = zco_word_bytes(dtype);
     uint32_t n = len / (uint32_t)W;
     uint8_t *streams = (uint8_t *)malloc(len ? len : 1);
-    uint64_t rec_cap = ZCO_REC_HEAD + 512u + 2u * (uint64_t)n;
+    /* v1: head + table + one word per symbol at most; v3 adds the counts and
+     * the padding of each list to 4 words */
+    uint64_t rec_cap = ZCO_REC_HEAD + 512u + 2u * (uint64_t)n + (lanes ? 64u + 8u * ZCO_LANES : 0u);
     uint8_t *rec = (uint8_t *)malloc((size_t)rec_cap);
     uint8_t *grouped = (uint8_t *)malloc((size_t)(16 + (uint64_t)W * pad16(rec_cap)));
     uint64_t result = 0;
@@ -374,7 +536,7 @@ uint64_t zco_encode_chunk(const uint8_t *src, uint32_t len, int dtype, double th
         if (present == 1) {
             entry = ((uint32_t)ZCO_MODE_CONST << 30) | (uint32_t)only;
         } else {
-            uint64_t r = zco_rans_record(sj, n, rec, rec_cap);
+            uint64_t r = lanes ? zco_rans_record_lanes(sj, n, rec, rec_cap) : zco_rans_record(sj, n, rec, rec_cap);
             if (r == 0) goto done;
             if ((double)r < threshold * (double)n) {
                 entry = ((uint32_t)ZCO_MODE_RANS << 30) | (uint32_t)r;
@@ -632,13 +794,15 @@ static int valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double
     return 1;
 }
 
-/* Largest possible grouped payload for a chunk of len bytes. */
-static uint64_t max_grouped(uint64_t len, int W) {
+/* Largest possible grouped payload for a chunk of len bytes; v3 records
+ * also hold the word counts and up to 3 padding words per lane. */
+static uint64_t max_grouped_v(uint64_t len, int W, int version) {
     uint64_t n = len / (uint64_t)W;
-    return pad16(4u * (uint64_t)W) + (uint64_t)W * pad16(ZCO_REC_HEAD + 512u + 2u * n);
+    uint64_t extra = version == 3 ? 64u + 6u * ZCO_LANES : 0u;
+    return pad16(4u * (uint64_t)W) + (uint64_t)W * pad16(ZCO_REC_HEAD + 512u + 2u * n + extra);
 }
 
-uint64_t zco_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
+static uint64_t blob_size_of(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, int version) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return 0;
     int W = zco_word_bytes(dtype);
     uint64_t nc = (nbytes + chunk_bytes - 1) / chunk_bytes;
@@ -646,16 +810,23 @@ uint64_t zco_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double 
     for (uint64_t c = 0; c < nc; c++) {
         uint64_t len = (c + 1 < nc) ? chunk_bytes : nbytes - c * chunk_bytes;
         uint64_t worst = pad16(len);
-        if (threshold > 1.0 && max_grouped(len, W) > worst) worst = max_grouped(len, W);
+        uint64_t g = max_grouped_v(len, W, version);
+        if (threshold > 1.0 && g > worst) worst = g;
         total += worst;
     }
     return total;
 }
 
-/* Worst case of either format: v2 adds the W plane tables. */
+uint64_t zco_blob_size(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold) {
+    return blob_size_of(nbytes, dtype, chunk_bytes, threshold, 1);
+}
+
+/* Worst case of any format: v2 adds the W plane tables; v3 records may be
+ * longer (only reachable with threshold > 1). */
 uint64_t zco_blob_size_v(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, int version) {
-    uint64_t b = zco_blob_size(nbytes, dtype, chunk_bytes, threshold);
-    if (b == 0 || (version != 1 && version != 2)) return 0;
+    if (version < 1 || version > 3) return 0;
+    uint64_t b = blob_size_of(nbytes, dtype, chunk_bytes, threshold, version);
+    if (b == 0) return 0;
     return version == 2 ? b + 512u * (uint64_t)zco_word_bytes(dtype) : b;
 }
 
@@ -705,11 +876,15 @@ static int compress_shared(const uint8_t *src, uint64_t nbytes, int dtype, int n
     return ZCO_OK;
 }
 
+static int compress_v13(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
+                        uint32_t chunk_bytes, double threshold, int version,
+                        uint8_t *blob, uint64_t cap, uint64_t *blob_bytes);
+
 int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
                    uint32_t chunk_bytes, double threshold, int version,
                    uint8_t *blob, uint64_t cap, uint64_t *blob_bytes) {
-    if (version == 1) return zco_compress(src, nbytes, dtype, ndim, shape, chunk_bytes, threshold, blob, cap,
-                                          blob_bytes);
+    if (version == 1 || version == 3)
+        return compress_v13(src, nbytes, dtype, ndim, shape, chunk_bytes, threshold, version, blob, cap, blob_bytes);
     if (version != 2) return ZCO_EINVAL;
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZCO_EINVAL;
     if (ndim < 0 || ndim > 8) return ZCO_EINVAL;
@@ -726,6 +901,13 @@ int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, con
 int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
                  uint32_t chunk_bytes, double threshold,
                  uint8_t *blob, uint64_t cap, uint64_t *blob_bytes) {
+    return compress_v13(src, nbytes, dtype, ndim, shape, chunk_bytes, threshold, 1, blob, cap, blob_bytes);
+}
+
+/* Formats v1 and v3 (they differ in the RANS records only). */
+static int compress_v13(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
+                        uint32_t chunk_bytes, double threshold, int version,
+                        uint8_t *blob, uint64_t cap, uint64_t *blob_bytes) {
     if (!valid_params(nbytes, dtype, chunk_bytes, threshold)) return ZCO_EINVAL;
     if (ndim < 0 || ndim > 8) return ZCO_EINVAL;
     int W = zco_word_bytes(dtype);
@@ -742,7 +924,7 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
     memset(blob, 0, (size_t)table_end);
 
     memcpy(blob, "ZCNN", 4);
-    put16(blob + 4, 1);
+    put16(blob + 4, (uint32_t)version);
     blob[6] = (uint8_t)dtype;
     blob[7] = (uint8_t)ndim;
     put32(blob + 8, chunk_bytes);
@@ -764,8 +946,10 @@ int zco_compress(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const
         uint32_t len = (uint32_t)((c + 1 < nc) ? chunk_bytes : nbytes - c * chunk_bytes);
         int raw = 0;
         uint64_t room = cap > off ? cap - off : 0;
-        uint64_t stored = zco_encode_chunk(src + c * (uint64_t)chunk_bytes, len, dtype, threshold,
-                                           blob + off, room, &raw);
+        uint64_t stored = version == 3 ? zco_encode_chunk_lanes(src + c * (uint64_t)chunk_bytes, len, dtype,
+                                                                threshold, blob + off, room, &raw)
+                                       : zco_encode_chunk(src + c * (uint64_t)chunk_bytes, len, dtype, threshold,
+                                                          blob + off, room, &raw);
         if (stored == 0 || pad16(stored) > room) return ZCO_ECAPACITY;
         memset(blob + off + stored, 0, (size_t)(pad16(stored) - stored));
         uint8_t *e = blob + ZCO_HEADER + ZCO_ENTRY * c;
@@ -784,7 +968,7 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
                   uint32_t *chunk_bytes_out, uint64_t *blob_bytes_out) {
     if (avail < ZCO_HEADER) return ZCO_EFORMAT;
     int version = (int)get16(blob + 4);
-    if (memcmp(blob, "ZCNN", 4) != 0 || (version != 1 && version != 2)) return ZCO_EFORMAT;
+    if (memcmp(blob, "ZCNN", 4) != 0 || version < 1 || version > 3) return ZCO_EFORMAT;
     int dtype = blob[6], ndim = blob[7];
     uint32_t chunk_bytes = get32(blob + 8);
     uint64_t nbytes = get64(blob + 16);
@@ -842,7 +1026,7 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
         int raw = (int)(sm >> 31);
         if (get64(e) != off) return ZCO_EFORMAT;
         if (raw && stored != len) return ZCO_EFORMAT;
-        if (!raw && (stored % 16 || stored > max_grouped(len, W))) return ZCO_EFORMAT;
+        if (!raw && (stored % 16 || stored > max_grouped_v(len, W, version))) return ZCO_EFORMAT;
         off += pad16(stored);
     }
     if (dtype_out) *dtype_out = dtype;
@@ -859,7 +1043,7 @@ int zco_blob_info(const uint8_t *blob, uint64_t avail, int *dtype_out, int *ndim
 /* Inverse of one grouped chunk payload; planes is NULL for v1, else the
  * v2 plane tables (a RANS stream then uses its plane's table). */
 static int decode_grouped(const uint8_t *p, uint32_t stored, uint32_t len, int dtype, const uint32_t *planes,
-                          uint8_t *dst) {
+                          int lanes, uint8_t *dst) {
     int W = zco_word_bytes(dtype);
     uint32_t n = len / (uint32_t)W;
     uint64_t g = pad16(4u * (uint64_t)W);
@@ -884,6 +1068,7 @@ static int decode_grouped(const uint8_t *p, uint32_t stored, uint32_t len, int d
             if (st != ZCO_OK) break;
             if (mode == ZCO_MODE_RAW) memcpy(sj, p + g, n);
             else if (planes) st = zco_rans_decode_shared(p + g, v, n, planes + 256u * j, sj);
+            else if (lanes) st = zco_rans_decode_lanes(p + g, v, n, sj);
             else st = zco_rans_decode(p + g, v, n, sj);
             g += pad16(v);
         } else {
@@ -927,7 +1112,8 @@ int zco_decompress(const uint8_t *blob, uint64_t blob_len, uint8_t *dst, uint64_
             continue;
         }
         if (sm >> 31) memcpy(out, blob + off, len);
-        else status |= decode_grouped(blob + off, stored, len, dtype, shared ? planes : NULL, out);
+        else status |= decode_grouped(blob + off, stored, len, dtype, shared ? planes : NULL, get16(blob + 4) == 3,
+                                      out);
     }
     return status;
 }

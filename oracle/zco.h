@@ -103,9 +103,16 @@ int zco_rans_decode_shared(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, c
 /* One chunk in format v2 (coded streams use the plane tables). */
 uint64_t zco_encode_chunk_shared(const uint8_t *src, uint32_t len, int dtype, double threshold,
                                  const uint32_t *planes, uint8_t *out, uint64_t cap, int *mode_raw);
-/* Worst-case blob size of format version 1 or 2. */
+/* Format v3 (a word list per lane): the record of zco_rans_record's steps
+ * with each lane's words in a list of its own (counts, then the lists, each
+ * padded to 4 words), and its inverse. */
+uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uint64_t rec_cap);
+int zco_rans_decode_lanes(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t *sym);
+uint64_t zco_encode_chunk_lanes(const uint8_t *src, uint32_t len, int dtype, double threshold,
+                                uint8_t *out, uint64_t cap, int *mode_raw);
+/* Worst-case blob size of format version 1, 2 or 3. */
 uint64_t zco_blob_size_v(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold, int version);
-/* Compress a tensor in format version 1 or 2. */
+/* Compress a tensor in format version 1, 2 or 3. */
 int zco_compress_v(const uint8_t *src, uint64_t nbytes, int dtype, int ndim, const int64_t *shape,
                    uint32_t chunk_bytes, double threshold, int version,
                    uint8_t *blob, uint64_t cap, uint64_t *blob_bytes);

@@ -3,8 +3,9 @@
 Written from the format description (header, chunk table, grouped-chunk
 directory, rANS record), not from the oracle's code, and sharing nothing with
 either implementation. It decodes small blobs (tens of KiB) only, in
-format v1 (a table in every record) or v2 (one table per plane after the
-chunk table, records of states and words). A blob that
+format v1 (a table in every record), v2 (one table per plane after the
+chunk table, records of states and words) or v3 (v1 with a word list per
+lane in every record). A blob that
 this reader and the oracle both turn back into the input is a valid encoding
 of the documented format, which pins the oracle's layout choices from the
 outside.
@@ -37,9 +38,26 @@ def _unpermute(p: int, dtype: int) -> int:
     return (s << (B - 1)) | (e << (B - 1 - E)) | m
 
 
-def _rans(rec: bytes, n: int, plane=None) -> list[int]:
-    """Decode a record: v1 carries its table (bitmap + frequencies); a v2
-    record is states + words and uses its plane's table (256 frequencies)."""
+def _lane_lists(rec: bytes, at: int) -> list[list[int]]:
+    """v3: 32 u16 counts at `at`, then each lane's words (padded to 4)."""
+    counts = struct.unpack_from("<32H", rec, at)
+    lists, pos = [], at + 64
+    for c in counts:
+        lists.append(list(struct.unpack_from(f"<{c}H", rec, pos)))
+        if any(struct.unpack_from(f"<{-c % 4}H", rec, pos + 2 * c)):
+            raise SpecError("nonzero list padding")
+        pos += 2 * (c + -c % 4)
+    if pos != len(rec):
+        raise SpecError("lane lists do not fill the record")
+    return lists
+
+
+def _rans(rec: bytes, n: int, plane=None, lanes: bool = False, owners: list | None = None) -> list[int]:
+    """Decode a record: v1 carries its table (bitmap + frequencies) and one
+    word list; a v2 record is states + words and uses its plane's table (256
+    frequencies); a v3 record (lanes) is v1's head, then a word list per lane.
+    With `owners` (v1), the lane that takes each word is appended to it in
+    the order the words are taken."""
     states = list(struct.unpack_from("<32I", rec, 0))
     if plane is None:
         bitmap = rec[128:160]
@@ -51,7 +69,8 @@ def _rans(rec: bytes, n: int, plane=None) -> list[int]:
         present = [s for s in range(256) if plane[s]]
         freqs = [plane[s] for s in present]
         words_at = 128
-    words = struct.unpack_from(f"<{(len(rec) - words_at) // 2}H", rec, words_at)
+    lists = _lane_lists(rec, words_at) if lanes else None
+    words = [] if lanes else struct.unpack_from(f"<{(len(rec) - words_at) // 2}H", rec, words_at)
     # slot -> symbol map, built by laying the symbols' slot ranges end to end
     slot_sym, start = [], {}
     for s, f in zip(present, freqs):
@@ -69,20 +88,27 @@ def _rans(rec: bytes, n: int, plane=None) -> list[int]:
         s = slot_sym[slot]
         x = freq[s] * (x // 4096) + slot - start[s]
         if x < 65536:
-            nxt -= 1
-            if nxt < 0:
-                raise SpecError("ran out of words")
-            x = x * 65536 + words[nxt]
+            if lanes:  # the lane's own list, from its end backwards
+                if not lists[lane]:
+                    raise SpecError("ran out of words")
+                x = x * 65536 + lists[lane].pop()
+            else:
+                nxt -= 1
+                if nxt < 0:
+                    raise SpecError("ran out of words")
+                x = x * 65536 + words[nxt]
+                if owners is not None:
+                    owners.append(lane)
         states[lane] = x
         out[i] = s
-    if nxt != 0 or any(x != 65536 for x in states):
+    if nxt != 0 or any(x != 65536 for x in states) or (lanes and any(lists)):
         raise SpecError("bad final state")
     return out
 
 
 def decode(blob: bytes) -> bytes:
     version, = struct.unpack_from("<H", blob, 4)
-    if blob[:4] != b"ZCNN" or version not in (1, 2):
+    if blob[:4] != b"ZCNN" or version not in (1, 2, 3):
         raise SpecError("magic/version")
     dtype, ndim = blob[6], blob[7]
     chunk_bytes, = struct.unpack_from("<I", blob, 8)
@@ -109,11 +135,11 @@ def decode(blob: bytes) -> bytes:
         if raw:
             out += payload
         else:
-            out += _grouped(payload, length, dtype, planes)
+            out += _grouped(payload, length, dtype, planes, lanes=version == 3)
     return bytes(out)
 
 
-def _grouped(payload: bytes, length: int, dtype: int, planes=None) -> bytes:
+def _grouped(payload: bytes, length: int, dtype: int, planes=None, lanes: bool = False) -> bytes:
     W = WORD[dtype]
     n = length // W
     pos = (4 * W + 15) // 16 * 16
@@ -125,7 +151,7 @@ def _grouped(payload: bytes, length: int, dtype: int, planes=None) -> bytes:
             streams.append([v] * n)
             continue
         rec = payload[pos:pos + v]
-        streams.append(list(rec) if mode == 0 else _rans(rec, n, None if planes is None else planes[j]))
+        streams.append(list(rec) if mode == 0 else _rans(rec, n, None if planes is None else planes[j], lanes))
         pos += (v + 15) // 16 * 16
     out = bytearray()
     for i in range(n):

@@ -612,6 +612,128 @@ def test_v2_rejections(zco):
     st, _ = zco.decompress_status(bytes(bad))
     assert st & (zco.EFORMAT | zco.ECRC)
     bad = bytearray(blob)
-    bad[4] = 3                                   # unknown version
+    bad[4] = 4                                   # unknown version
     st, _ = zco.decompress_status(bytes(bad))
     assert st & zco.EFORMAT
+
+
+# ------------------------------------------- format v3 (a word list per lane)
+# lmz "On a GPU": the decoder is bound by each lane's dependent chain; v3
+# gives every lane its own word list so that no step waits on the others.
+
+def _v3_head(rec: bytes) -> int:
+    k = sum(bin(b).count("1") for b in rec[128:160])
+    return 160 + (2 * k + 15) // 16 * 16
+
+
+def test_v3_lane_lists_are_the_v1_words_by_lane(zco):
+    """A v3 record holds exactly the v1 record's states, table and words,
+    with lane l's list the words lane l takes when the v1 record is decoded
+    by the independent reader, in reverse order of taking (the order the
+    lane emitted them). This ties v3 to the pinned v1 coder."""
+    rng = np.random.default_rng(303)
+    for n in (2, 31, 32, 33, 100, 1000, 4095, 4097, 32768, 65536):
+        for dist in ("skew", "uniform", "geom"):
+            if dist == "skew":
+                s = rng.choice(256, n, p=rng.dirichlet(np.full(256, 0.05)))
+            elif dist == "uniform":
+                s = rng.integers(0, 256, n)
+            else:
+                s = np.minimum(rng.geometric(0.3, n), 255)
+            s = s.astype(np.uint8)
+            if np.unique(s).size < 2:
+                s[0] ^= 1
+            r1, r3 = zco.rans_record(s), zco.rans_record_lanes(s)
+            head = _v3_head(r1)
+            assert r3[:head] == r1[:head]
+            owners: list[int] = []
+            assert spec_decoder._rans(r1, n, owners=owners) == s.tolist()
+            words = struct.unpack_from(f"<{(len(r1) - head) // 2}H", r1, head)
+            assert len(owners) == len(words)
+            want = [[] for _ in range(32)]
+            for i, lane in enumerate(owners):       # the i-th word taken is words[-1 - i]
+                want[lane].append(words[len(words) - 1 - i])
+            want = [w[::-1] for w in want]
+            assert spec_decoder._lane_lists(r3, head) == want
+            assert len(r3) == head + 64 + sum(2 * (len(w) + -len(w) % 4) for w in want)
+            assert (zco.rans_decode_lanes(r3, n) == s).all()
+            assert spec_decoder._rans(r3, n, lanes=True) == s.tolist()
+
+
+def test_v3_tiny_blob_golden(zco):
+    g = dict(line.split(None, 1) for line in _golden_lines("tiny_v3_blob.txt"))
+    blob = zco.compress(np.array([0, 1], np.uint8), 1, (2,), chunk_bytes=64, threshold=1e6, version=3)
+    assert len(blob) == int(g["blob_bytes"])
+    head = bytearray(96)
+    head[0:4] = b"ZCNN"
+    struct.pack_into("<HBBIBBHQI", head, 4, int(g["version"]), 1, 1, 64, 32, 12, 0, 2, 1)
+    struct.pack_into("<q", head, 32, 2)
+    states = [int(g["state0"]), int(g["state1"])] + [int(g["state_rest"])] * 30
+    rec = struct.pack("<32I", *states) + bytes([int(g["bitmap_byte0"], 16)]) + bytes(31)
+    rec += struct.pack("<2H", *map(int, g["freqs"].split())) + bytes(12)
+    rec += struct.pack("<32H", *([int(g["counts"])] * 32))
+    payload = struct.pack("<I", int(g["dir0"], 16)) + bytes(12) + rec
+    assert len(payload) == int(g["chunk0_stored"])
+    entry = struct.pack("<QII", int(g["table_end"]), int(g["chunk0_stored"]), zlib.crc32(payload))
+    table = bytes(head) + entry
+    assert len(table) == int(g["table_end"])
+    expect = table[:28] + struct.pack("<I", zlib.crc32(table)) + table[32:] + payload
+    assert blob == expect
+
+
+def test_v3_roundtrip_random_tensors(zco):
+    rng = np.random.default_rng(333)
+    for trial in range(160):
+        dtype = int(rng.integers(1, 7))
+        n = int(rng.choice([0, 1, 31, 33, 4097, int(rng.integers(0, 6001))]))
+        data = _rand_tensor(rng, dtype, n)
+        chunk = int(rng.choice([64, 1024, 4096, 131072]))
+        thr = float(rng.choice([0.5, 0.95, 1.0, 2.0]))
+        blob = zco.compress(data, dtype, (n,), chunk, thr, version=3)
+        assert len(blob) <= zco.blob_size(data.size, dtype, chunk, thr, version=3)
+        info = zco.blob_info(blob)
+        assert info["version"] == 3 and info["dtype"] == dtype
+        assert zco.decompress(blob).tobytes() == data.tobytes(), (trial, dtype, n, chunk, thr)
+        assert zco.verify(blob) == 0
+        if data.size <= 20000:
+            assert spec_decoder.decode(blob) == data.tobytes()
+
+
+def test_v3_exhaustive_bf16_patterns(zco):
+    """All 65,536 BF16 patterns: in order over 4 KiB chunks (exponent coded,
+    sign|mantissa RAW) and shuffled with every stream coded (threshold 2)."""
+    words = np.arange(65536, dtype=np.uint16).view(np.uint8)
+    blob = zco.compress(words, 4, (65536,), 4096, 0.95, version=3)
+    raws, modes = _chunk_modes(blob, 2)
+    assert raws == [0] * 32 and all(m == [1, 0] for m in modes)
+    assert (zco.decompress(blob) == words).all()
+    perm = np.random.default_rng(7).permutation(65536).astype(np.uint16).view(np.uint8)
+    blob = zco.compress(perm, 4, (256, 256), 131072, 2.0, version=3)
+    raws, modes = _chunk_modes(blob, 2)
+    assert raws == [0] and modes == [[1, 1]]
+    assert (zco.decompress(blob) == perm).all()
+    assert spec_decoder.decode(blob) == perm.tobytes()
+
+
+def test_v3_size_and_corruption(zco):
+    """v3 costs at most the counts and the list padding per coded record
+    over v1, and a changed byte anywhere is detected (CRC or structure)."""
+    raw = workloads.as_bytes(workloads.bf16_1m()).numpy()
+    b1 = zco.compress(raw, 4, None, 131072, 0.95)
+    b3 = zco.compress(raw, 4, None, 131072, 0.95, version=3)
+    nc = raw.size // 131072
+    assert len(b1) < len(b3) <= len(b1) + nc * pad16(64 + 6 * 32)
+    rng = np.random.default_rng(77)
+    small = zco.compress(raw[:8192], 4, None, 4096, 0.95, version=3)
+    for pos in list(rng.integers(0, len(small), 200)):
+        bad = bytearray(small)
+        bad[pos] ^= int(rng.integers(1, 256))
+        st, out = zco.decompress_status(bytes(bad))
+        assert st != 0 or out.tobytes() == raw[:8192].tobytes(), pos
+        # without the CRC check a changed raw byte decodes silently; the
+        # structure checks still keep every read within the blob
+        zco.decompress_status(bytes(bad), zco.NO_VERIFY)
+
+
+def pad16(x: int) -> int:
+    return (x + 15) // 16 * 16
