@@ -178,7 +178,7 @@ def rans_decode(record: bytes, n: int) -> np.ndarray:
 def rans_record_lanes(symbols) -> bytes:
     """Format v3 record: a word list per lane."""
     s = _u8(symbols)
-    cap = 160 + 512 + 64 + 2 * s.size + 8 * 32 + 16
+    cap = 160 + 512 + 64 + 2 * s.size + 16 * 32 + 16
     rec = np.zeros(cap, np.uint8)
     r = lib().zco_rans_record_lanes(_ptr(s), s.size, _ptr(rec), cap)
     if r == 0:
@@ -200,7 +200,7 @@ def encode_chunk(chunk, dtype: int, threshold: float = 0.95, version: int = 1) -
     (format v1, or v3 with a word list per lane)."""
     d = _u8(chunk)
     W = WORD_BYTES[dtype]
-    cap = 16 + W * (160 + 512 + 64 + 8 * 32 + 2 * (d.size // W) + 16) + d.size
+    cap = 16 + W * (160 + 512 + 64 + 16 * 32 + 2 * (d.size // W) + 16) + d.size
     out = np.zeros(cap, np.uint8)
     raw = ctypes.c_int(0)
     fn = lib().zco_encode_chunk_lanes if version == 3 else lib().zco_encode_chunk

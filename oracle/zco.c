@@ -46,7 +46,8 @@
  * pad to 16) come 32 x u16 word counts c_0 .. c_31, then for lane 0 .. 31
  * the c_l words that lane emitted, in the order it emitted them (a decoder
  * consumes each list from its end backwards), each list zero-padded to a
- * multiple of 4 words. Record bytes = head + 64 + 2 * sum pad4(c_l).
+ * multiple of 8 words (16 bytes, so that a lane reads its list in aligned
+ * 16-byte blocks). Record bytes = head + 64 + 2 * sum pad8(c_l).
  *
  * Blob format v2 (shared tables; lmz "Building on lmz": one table per plane
  * kind for many chunks) differs from v1 in three places only:
@@ -354,7 +355,7 @@ int zco_rans_decode(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t 
  * record gives each lane its own list (see the top of this file); the coding
  * steps are exactly zco_rans_record's, only the place a word is written
  * differs. */
-static uint64_t pad4w(uint64_t words) { return (words + 3u) & ~(uint64_t)3u; }
+static uint64_t pad8w(uint64_t words) { return (words + 7u) & ~(uint64_t)7u; }
 
 uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uint64_t rec_cap) {
     uint32_t counts[256] = {0}, f[256], cum[257];
@@ -390,7 +391,7 @@ uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uin
     }
 
     uint64_t size = lists_at;
-    for (uint32_t l = 0; l < ZCO_LANES; l++) size += 2u * pad4w(c[l]);
+    for (uint32_t l = 0; l < ZCO_LANES; l++) size += 2u * pad8w(c[l]);
     if (size > rec_cap) {
         free(lw);
         return 0;
@@ -410,7 +411,7 @@ uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uin
     for (uint32_t l = 0; l < ZCO_LANES; l++) {
         put16(rec + head + 2 * l, c[l]);
         for (uint32_t q = 0; q < c[l]; q++) put16(rec + off + 2u * q, lw[(uint64_t)l * T + q]);
-        off += 2u * pad4w(c[l]);
+        off += 2u * pad8w(c[l]);
     }
     free(lw);
     return size;
@@ -450,9 +451,9 @@ int zco_rans_decode_lanes(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, ui
         uint32_t c = get16(rec + head + 2 * l);
         base[l] = off;
         left[l] = c;
-        off += 2u * pad4w(c);
+        off += 2u * pad8w(c);
         if (off > rec_bytes) return ZCO_ECORRUPT;
-        for (uint64_t q = c; q < pad4w(c); q++)
+        for (uint64_t q = c; q < pad8w(c); q++)
             if (get16(rec + base[l] + 2u * q)) return ZCO_ECORRUPT;
     }
     if (off != rec_bytes) return ZCO_ECORRUPT;
@@ -513,8 +514,8 @@ static uint64_t encode_chunk_v(const uint8_t *src, uint32_t len, int dtype, doub
     uint32_t n = len / (uint32_t)W;
     uint8_t *streams = (uint8_t *)malloc(len ? len : 1);
     /* v1: head + table + one word per symbol at most; v3 adds the counts and
-     * the padding of each list to 4 words */
-    uint64_t rec_cap = ZCO_REC_HEAD + 512u + 2u * (uint64_t)n + (lanes ? 64u + 8u * ZCO_LANES : 0u);
+     * the padding of each list to 8 words */
+    uint64_t rec_cap = ZCO_REC_HEAD + 512u + 2u * (uint64_t)n + (lanes ? 64u + 16u * ZCO_LANES : 0u);
     uint8_t *rec = (uint8_t *)malloc((size_t)rec_cap);
     uint8_t *grouped = (uint8_t *)malloc((size_t)(16 + (uint64_t)W * pad16(rec_cap)));
     uint64_t result = 0;
@@ -798,7 +799,7 @@ static int valid_params(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double
  * also hold the word counts and up to 3 padding words per lane. */
 static uint64_t max_grouped_v(uint64_t len, int W, int version) {
     uint64_t n = len / (uint64_t)W;
-    uint64_t extra = version == 3 ? 64u + 6u * ZCO_LANES : 0u;
+    uint64_t extra = version == 3 ? 64u + 14u * ZCO_LANES : 0u;
     return pad16(4u * (uint64_t)W) + (uint64_t)W * pad16(ZCO_REC_HEAD + 512u + 2u * n + extra);
 }
 

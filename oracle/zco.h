@@ -105,7 +105,7 @@ uint64_t zco_encode_chunk_shared(const uint8_t *src, uint32_t len, int dtype, do
                                  const uint32_t *planes, uint8_t *out, uint64_t cap, int *mode_raw);
 /* Format v3 (a word list per lane): the record of zco_rans_record's steps
  * with each lane's words in a list of its own (counts, then the lists, each
- * padded to 4 words), and its inverse. */
+ * padded to 8 words), and its inverse. */
 uint64_t zco_rans_record_lanes(const uint8_t *sym, uint32_t n, uint8_t *rec, uint64_t rec_cap);
 int zco_rans_decode_lanes(const uint8_t *rec, uint64_t rec_bytes, uint32_t n, uint8_t *sym);
 uint64_t zco_encode_chunk_lanes(const uint8_t *src, uint32_t len, int dtype, double threshold,

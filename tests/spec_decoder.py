@@ -39,14 +39,14 @@ def _unpermute(p: int, dtype: int) -> int:
 
 
 def _lane_lists(rec: bytes, at: int) -> list[list[int]]:
-    """v3: 32 u16 counts at `at`, then each lane's words (padded to 4)."""
+    """v3: 32 u16 counts at `at`, then each lane's words (padded to 8)."""
     counts = struct.unpack_from("<32H", rec, at)
     lists, pos = [], at + 64
     for c in counts:
         lists.append(list(struct.unpack_from(f"<{c}H", rec, pos)))
-        if any(struct.unpack_from(f"<{-c % 4}H", rec, pos + 2 * c)):
+        if any(struct.unpack_from(f"<{-c % 8}H", rec, pos + 2 * c)):
             raise SpecError("nonzero list padding")
-        pos += 2 * (c + -c % 4)
+        pos += 2 * (c + -c % 8)
     if pos != len(rec):
         raise SpecError("lane lists do not fill the record")
     return lists

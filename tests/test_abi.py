@@ -123,7 +123,8 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
                                    vp2(aligned, aligned), u64_2(1 << 16, 1 << 16), aligned, aligned, 1 << 24,
                                    aligned, None)
     assert comp(0, None, None, None, zc.BF16) == zc.OK
-    assert comp(0, None, None, None, zc.BF16, flags=4) == zc.EINVAL   # unknown flag
+    assert comp(0, None, None, None, zc.BF16, flags=8) == zc.EINVAL   # unknown flag
+    assert comp(0, None, None, None, zc.BF16, flags=6) == zc.EINVAL   # two formats at once
     assert comp(2, None, None, u64_2(2048, 2048), zc.BF16) == zc.EINVAL
     # deltas only for unsigned word dtypes
     assert comp(2, vp2(aligned, aligned), vp2(aligned, aligned), u64_2(2048, 2048), zc.BF16) == zc.EINVAL
