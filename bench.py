@@ -53,7 +53,27 @@ def _args():
     p.add_argument("--no-verify", action="store_true", help="decode without the CRC check")
     p.add_argument("--shared-tables", action="store_true",
                    help="blob format v2: one table per byte plane of each tensor (ZC_SHARED_TABLES)")
+    p.add_argument("--streams", type=int, default=4,
+                   help="llama8b: the per-tensor calls are issued round-robin on this many CUDA streams, each "
+                        "with its own workspace (1: one stream, every call after the previous one)")
+    p.add_argument("--format", type=int, default=None, choices=[1, 2, 3],
+                   help="blob format: 1 (a table and one word list per coded stream), 2 (shared plane "
+                        "tables, as --shared-tables), 3 (a word list per rANS lane, ZC_LANE_WORDS)")
     return p.parse_args()
+
+
+FORMAT_NAMES = {1: "v1 (a table and one word list per coded stream)", 2: "v2 (shared plane tables)",
+                3: "v3 (v1 with a word list per rANS lane)"}
+
+
+def format_version(a) -> int:
+    if a.format is not None:
+        return a.format
+    return 2 if a.shared_tables else 1
+
+
+def format_flags(a, zc) -> int:
+    return {1: 0, 2: zc.SHARED_TABLES, 3: zc.LANE_WORDS}[format_version(a)]
 
 
 def make_workload(name: str, device):
@@ -86,7 +106,8 @@ def make_workload(name: str, device):
 
 MODEL_WORKLOADS = {
     "llama8b": "Llama-3.1-8B-shaped BF16 model (290 tensors, 16.06 GB), N(0,0.02) per tensor, RMSNorm vectors of "
-               "ones; one compression and one decompression call per tensor",
+               "ones; one compression and one decompression call per tensor (issued round-robin on the "
+               "configured number of CUDA streams)",
     "llama8b_batch": "Llama-3.1-8B-shaped BF16 model (290 tensors, 16.06 GB), N(0,0.02) per tensor, RMSNorm "
                      "vectors of ones; all tensors in one batched compression and one batched decompression call",
 }
@@ -358,7 +379,7 @@ def run_model(a, world, rank, local, dev, stream):
 
     batched = a.workload == "llama8b_batch"
     also_batched = not batched  # the per-tensor line also reports the batched calls
-    flags = zc.SHARED_TABLES if a.shared_tables else 0
+    flags = format_flags(a, zc)
     specs = wl.llama8b_specs()
     C, thr, code, Wd = a.chunk_bytes, a.threshold, wl.BF16, 2
     sizes = [2 * int(torch.Size(sh).numel()) for _, sh in specs]
@@ -390,26 +411,51 @@ def run_model(a, world, rank, local, dev, stream):
         ws_b = torch.empty(zc.workspace_size_batch(sizes, code, C, flags), dtype=torch.uint8, device=dev)
         n_dws = zc.decompress_workspace_size_batch(n)
         dws = torch.empty(max(16, n_dws), dtype=torch.uint8, device=dev)
+    # per-tensor calls: round-robin on n_streams streams, each with its own
+    # workspace; the calls of one step start after an event on `stream` and
+    # `stream` waits for all of them at the end of the step
+    n_streams = 1 if batched else max(1, a.streams)
+    workers = [stream] if n_streams == 1 else [torch.cuda.Stream(device=dev) for _ in range(n_streams)]
+    ws_1 = []
     if not batched:
-        ws_1 = torch.empty(max(zc.workspace_size(x, code, C, flags) for x in sizes), dtype=torch.uint8,
-                           device=dev)
+        ws_bytes_1 = max(zc.workspace_size(x, code, C, flags) for x in sizes)
+        ws_1 = [torch.empty(ws_bytes_1, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
     N = sum(sizes)
     verify = not a.no_verify
+
+    def fan_out():
+        if n_streams > 1:
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            for w in workers:
+                w.wait_event(ev)
+
+    def fan_in():
+        if n_streams > 1:
+            for w in workers:
+                ev = torch.cuda.Event()
+                ev.record(w)
+                stream.wait_event(ev)
 
     def comp(inputs, blobs=blobs, nb=nb, one_call=batched):
         if one_call:
             zc.compress_batch_into(inputs, blobs, nb, ws_b, st, code, shapes, C, thr, stream, flags=flags)
         else:
+            fan_out()
             for t in range(n):
-                zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws_1, st, C, thr, stream, dtype=code,
+                k = t % n_streams
+                zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws_1[k], st, C, thr, workers[k], dtype=code,
                                  shape=shapes[t], flags=flags)
+            fan_in()
 
     def decomp(infos, blobs=blobs, one_call=batched):
         if one_call:
             zc.decompress_batch_into(blobs, infos, outs, st, dws, verify, stream)
         else:
+            fan_out()
             for t in range(n):
-                zc.decompress_into(blobs[t], infos[t], outs[t], st, verify, stream)
+                zc.decompress_into(blobs[t], infos[t], outs[t], st, verify, workers[t % n_streams])
+            fan_in()
 
     with torch.cuda.stream(stream):
         comp(srcs)
@@ -417,7 +463,7 @@ def run_model(a, world, rank, local, dev, stream):
     assert int(st.item()) == 0
     lens = nb.tolist()
     S = sum(lens)
-    planes = 512 * Wd if flags else 0  # v2: the plane tables follow the chunk table
+    planes = 512 * Wd if flags & zc.SHARED_TABLES else 0  # v2: the plane tables follow the chunk table
     infos = [zc.blob_info(b[: 96 + 16 * ((x + C - 1) // C) + planes].cpu()) for b, x in zip(blobs, sizes)]
     with torch.cuda.stream(stream):
         decomp(infos)
@@ -535,13 +581,13 @@ def run_model(a, world, rank, local, dev, stream):
     enc_ach = alg * a.steps / t_enc / 1e9
     dec_ach = alg * a.steps / t_dec / 1e9
     chunks = [(x + C - 1) // C for x in sizes]
-    dec_kernel = "decode_v2_kernel" if flags else "decode_kernel"
+    dec_kernel = "decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel"
     if batched:
         table_launches = lambda words: (words + 7679) // 7680
-        per_step = (encode_launches(chunks, Wd, C, bool(flags)) + table_launches(38 * n)
+        per_step = (encode_launches(chunks, Wd, C, bool(flags & zc.SHARED_TABLES)) + table_launches(38 * n)
                     + 1 + table_launches(14 * n))
     else:
-        per_step = sum(encode_launches([c], Wd, C, bool(flags)) + (1 if c else 0) for c in chunks)
+        per_step = sum(encode_launches([c], Wd, C, bool(flags & zc.SHARED_TABLES)) + (1 if c else 0) for c in chunks)
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
         "value": round(replica_value(N, a.steps, world, total) / 1e9, 3), "unit": "GB/s",
@@ -549,8 +595,9 @@ def run_model(a, world, rank, local, dev, stream):
         "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": a.workload, "desc": MODEL_WORKLOADS[a.workload], "nbytes": N, "tensors": n,
+                   "streams": n_streams,
                    "chunk_bytes": C, "threshold": thr, "verify_crc_on_decode": verify,
-                   "format": "v2 (shared plane tables)" if flags else "v1 (a table per coded stream)",
+                   "format": FORMAT_NAMES[format_version(a)],
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "encode": {"gbs": round(N * a.steps / t_enc / 1e9, 2), "roofline_frac": round(enc_ach / hbm, 4),
                    "ms": round(1e3 * t_enc / a.steps, 4)},
@@ -621,8 +668,8 @@ def main():
         base, src = wl.as_bytes(ta), wl.as_bytes(tb)
     N = src.numel()
     C, thr = a.chunk_bytes, a.threshold
-    flags = zc.SHARED_TABLES if a.shared_tables else 0
-    planes = 512 * (N // max(1, t.numel())) if flags else 0  # v2: the plane tables follow the chunk table
+    flags = format_flags(a, zc)
+    planes = 512 * (N // max(1, t.numel())) if flags & zc.SHARED_TABLES else 0  # v2: the plane tables follow the chunk table
     cap = zc.blob_size(N, code, C, thr, flags)
     blob = torch.empty(cap, dtype=torch.uint8, device=dev)
     ws = torch.empty(zc.workspace_size(N, code, C, flags), dtype=torch.uint8, device=dev)
@@ -791,7 +838,7 @@ def main():
     # the decompression call is one kernel (decode_kernel), the largest single
     # kernel of the step; compression is two (statistics, coding), each
     # shorter (profiles/launches_*.md), so the live roofline is decode's
-    dominant = "decode_v2_kernel" if flags else "decode_kernel"
+    dominant = "decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel"
     ach = dec_ach
     traffic = profiled_traffic(dominant, a.workload)
     line = {
@@ -804,7 +851,7 @@ def main():
                    "verify_crc_on_decode": not a.no_verify,
                    "l2": "512 MiB written before each compression and decompression (not timed)" if flush_l2
                    else "inputs larger than L2 (no flush)",
-                   "format": "v2 (shared plane tables)" if flags else "v1 (a table per coded stream)",
+                   "format": FORMAT_NAMES[format_version(a)],
                    "parallelism": f"replicas x{world}"},
         "encode": {"gbs": round(enc_gbs, 2), "roofline_frac": round(enc_ach / hbm, 4),
                    "ms": round(1e3 * t_enc / a.steps, 4)},
@@ -829,7 +876,7 @@ def main():
                             "mode": "device blob, copied to pinned host memory and back"},
         "e2e_zero_copy": zc_line,
         # stats_kernel + code_kernel (v2: + plane_kernel) + decode_kernel per step
-        "gpu_launches": (encode_launches([(N + C - 1) // C], N // max(1, t.numel()), C, bool(flags)) + 1) * a.steps,
+        "gpu_launches": (encode_launches([(N + C - 1) // C], N // max(1, t.numel()), C, bool(flags & zc.SHARED_TABLES)) + 1) * a.steps,
     }
     line["cpu_baseline"] = cpu_baseline(t, code, a)
     print(json.dumps(line), flush=True)

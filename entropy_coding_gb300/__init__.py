@@ -23,12 +23,13 @@ from .workloads import BF16, FP16, FP32, U8, U16, U32
 __all__ = ["compress", "decompress", "crc32", "verify", "verify_into", "blob_info", "blob_size", "workspace_size",
            "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
            "decompress_delta_into", "compress_batch", "compress_batch_into", "decompress_batch",
-           "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "SHARED_TABLES", "OK", "EINVAL", "EFORMAT",
+           "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "SHARED_TABLES", "LANE_WORDS", "OK", "EINVAL", "EFORMAT",
            "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
 
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
 NO_VERIFY = 1
 SHARED_TABLES = 2  # compression flag: blob format v2 (shared plane tables)
+LANE_WORDS = 4     # compression flag: blob format v3 (a word list per rANS lane)
 HOOK_LOOKBACK_STALL, HOOK_PRODUCER_STALL = 1, 2  # test hooks (zc_set_test_hooks)
 DEFAULT_CHUNK = 131072
 DEFAULT_THRESHOLD = 0.95
@@ -161,14 +162,17 @@ def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tenso
 
 
 def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
-             stream=None, host_blob: bool = False, shared_tables: bool = False) -> torch.Tensor:
+             stream=None, host_blob: bool = False, shared_tables: bool = False,
+             lane_words: bool = False) -> torch.Tensor:
     """Compress a CUDA tensor into a self-describing blob (1-D uint8 tensor).
 
     The blob is a CUDA tensor, or with ``host_blob`` a page-locked CPU tensor
     that the kernels write directly over the host link (no separate copy).
     ``shared_tables`` writes format v2 (one table per byte plane of the
-    tensor). Synchronises once, to read the blob length."""
-    flags = SHARED_TABLES if shared_tables else 0
+    tensor), ``lane_words`` format v3 (a word list per rANS lane, which the
+    decoder steps through without waiting on the other lanes). Synchronises
+    once, to read the blob length."""
+    flags = (SHARED_TABLES if shared_tables else 0) | (LANE_WORDS if lane_words else 0)
     if not t.is_cuda:
         raise ZcError(EINVAL, "compress expects a CUDA tensor")
     src = t.contiguous()
@@ -420,7 +424,8 @@ def compress_batch_into(srcs, blobs, blob_bytes: torch.Tensor, workspace: torch.
 
 
 def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD, stream=None,
-                   bases=None, host_blob: bool = False, shared_tables: bool = False) -> list:
+                   bases=None, host_blob: bool = False, shared_tables: bool = False,
+                   lane_words: bool = False) -> list:
     """Compress a list of CUDA tensors of one dtype in one call; returns one
     blob per tensor, each equal to compress() of that tensor (with ``bases``:
     to compress_delta(bases[t], tensors[t])); with ``host_blob`` the blobs are
@@ -441,7 +446,7 @@ def compress_batch(tensors, chunk_bytes: int = DEFAULT_CHUNK, threshold: float =
             raise ZcError(EINVAL, f"unsupported element size {ts[0].element_size()}")
     else:
         code = dtype_code(ts[0])
-    flags = SHARED_TABLES if shared_tables else 0
+    flags = (SHARED_TABLES if shared_tables else 0) | (LANE_WORDS if lane_words else 0)
     nbytes = [t.numel() * t.element_size() for t in ts]
     caps = [blob_size(nb, code, chunk_bytes, threshold, flags) for nb in nbytes]
     if 0 in caps:

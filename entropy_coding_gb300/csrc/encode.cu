@@ -710,6 +710,13 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
 // off the state's dependency chain. Returns the record's unpadded size, or
 // kAborted once the record has reached lim bytes (it can then no longer be
 // kept: the stream is stored raw).
+//
+// kLanes (format v3, a word list per lane): a lane collects its words in
+// registers and writes each 8 of them (16 bytes) to its own list, no ballot
+// needed; lane l's list is staged at a stride of pad8(T) words after the 32
+// counts (the record's size counts each list padded to 8 words), and
+// warp_copy_crc_lanes gathers the lists into place in the blob.
+template <bool kLanes>
 __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint4 *etab,
                                        uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim,
                                        bool shared) {
@@ -764,10 +771,25 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         for (uint32_t b = kRecHead + 2 * k_total + lane; b < words_at; b += 32) rec[b] = 0;
     }
 
-    uint16_t *wout = reinterpret_cast<uint16_t *>(rec + words_at);
+    // v3: the lists follow the 32 counts; lane l stages its words at
+    // lists_at + 2 l Ts, Ts = pad8(T), in 16-byte blocks collected in acc
+    const uint32_t lists_at = words_at + 64;
+    const uint32_t Ts = (uint32_t(T) + 7) & ~7u;
+    uint16_t *wout = reinterpret_cast<uint16_t *>(rec + (kLanes ? lists_at : words_at));
+    uint4 *lw4 = reinterpret_cast<uint4 *>(wout + uint32_t(lane) * Ts);
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    // append a word to the lane's block (words in emission order, the first
+    // at the lowest address); a full block goes to the lane's list
+    auto push = [&](uint32_t w, uint32_t &count) {
+        acc.x = __funnelshift_r(acc.x, acc.y, 16);
+        acc.y = __funnelshift_r(acc.y, acc.z, 16);
+        acc.z = __funnelshift_r(acc.z, acc.w, 16);
+        acc.w = (acc.w >> 16) | (w << 16);
+        if ((++count & 7u) == 0) lw4[(count >> 3) - 1] = acc;
+    };
     const uint32_t gt = lanemask_gt();
     uint32_t x = kRansL;
-    uint32_t wc = 0;
+    uint32_t wc = 0;  // v1/v2: words of the warp; v3: words of this lane
     const bool first_active = uint32_t(T - 1) * 32 + lane < n;
     // write out the words of one staged block (steps 0..cnt-1, emitting lanes
     // 31..0 within a step)
@@ -775,10 +797,19 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
 #pragma unroll 4
         for (int s = 0; s < cnt; s++) {
             const bool em = (flags >> s) & 1u;
-            const uint32_t B = __ballot_sync(kFull, em);
-            if (em) wout[wc + __popc(B & gt)] = st[s * 32];
-            wc += __popc(B);
+            if constexpr (kLanes) {
+                if (em) push(st[s * 32], wc);
+            } else {
+                const uint32_t B = __ballot_sync(kFull, em);
+                if (em) wout[wc + __popc(B & gt)] = st[s * 32];
+                wc += __popc(B);
+            }
         }
+    };
+    // the record's size if it ended with the words written so far
+    auto size_now = [&]() -> uint64_t {
+        if constexpr (kLanes) return lists_at + 2ull * warp_sum_u32((wc + 7) & ~7u);
+        else return words_at + 2ull * wc;
     };
     uint32_t flags_prev = 0;
     bool aborted = false;
@@ -811,9 +842,13 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
 
                 const bool em = fp & 1u;
                 fp >>= 1;
-                const uint32_t B = __ballot_sync(kFull, em);
-                if (em) wout[wc + __popc(B & gt)] = st_prev[s * 32];
-                wc += __popc(B);
+                if constexpr (kLanes) {
+                    if (em) push(st_prev[s * 32], wc);
+                } else {
+                    const uint32_t B = __ballot_sync(kFull, em);
+                    if (em) wout[wc + __popc(B & gt)] = st_prev[s * 32];
+                    wc += __popc(B);
+                }
             }
         } else {
             if (b > 0) flush(st_prev, flags_prev, 32);
@@ -846,7 +881,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         flags_prev = flags;
         __syncwarp();
         // the words written so far belong to the blocks before this one
-        if (words_at + 2ull * wc >= lim) {
+        if (size_now() >= lim) {
             aborted = true;
             break;
         }
@@ -854,13 +889,28 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     if (!aborted) {
         flush(stage + ((nb - 1) & 1) * 1024, flags_prev, T - 32 * (nb - 1));
         __syncwarp();
-        aborted = words_at + 2ull * wc >= lim;
+        aborted = size_now() >= lim;
     }
     cp_async_wait_all();  // the ring is reused by the next stream
     __syncwarp();
     if (aborted) return kAborted;
     reinterpret_cast<uint32_t *>(rec)[lane] = x;
-    const uint32_t rec_bytes = words_at + 2 * wc;
+    uint32_t rec_bytes = words_at + 2 * wc;
+    if constexpr (kLanes) {
+        // the lane's last, partial block: zero words pushed in behind its
+        // words move them to the bottom
+        if (wc & 7u) {
+            uint32_t c = wc;
+            while (c & 7u) push(0u, c);
+        }
+        __syncwarp();
+        // the counts; the lists stay at their staging places, and the copy
+        // into the blob gathers them to lists_at + 2 off_l (off_l = the
+        // padded counts of the lanes below)
+        const uint32_t padded = (wc + 7) & ~7u;
+        reinterpret_cast<uint16_t *>(rec + words_at)[lane] = uint16_t(wc);
+        rec_bytes = lists_at + 2 * warp_sum_u32(padded);
+    }
     for (uint32_t b = rec_bytes + lane; b < pad16(rec_bytes); b += 32) rec[b] = 0;
     __syncwarp();
     return rec_bytes;
@@ -1022,6 +1072,62 @@ __device__ uint32_t warp_copy_crc(const uint8_t *src, uint64_t len, uint8_t *dst
     return ea.rounds ? crc_fold<1, 4>(R, nullptr) : 0u;
 }
 
+// Format v3: copy a record staged by rans_encode_stream<true> into the blob
+// (len bytes, a multiple of 16) and return its CRC register taken from
+// zero: the head and the counts (lists_at bytes) as they are, then output
+// block ob of the lists from lane l's staged list, l the lane with
+// boff_l <= ob < boff_l + the lane's padded count / 8 (boff_l = the blocks
+// of the lanes below). The pieces go round-robin as in warp_copy_crc.
+__device__ uint32_t warp_copy_crc_lanes(const uint8_t *rec, uint32_t len, uint32_t lists_at, uint32_t Ts,
+                                        uint8_t *dst, const CrcSmem &cs) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t *row = crc_row<kCodeCrcCopies>(cs.rep);
+    const uint32_t cnt = reinterpret_cast<const uint16_t *>(rec + lists_at - 64)[lane];
+    const uint32_t blocks = (cnt + 7) / 8;
+    const uint32_t boff = warp_excl_scan(blocks);
+    const uint32_t head = lists_at / 16;
+    // every lane runs the whole search (its shuffles need all 32 lanes),
+    // whichever part of the record its piece is in
+    auto src_of = [&](uint32_t v) -> const uint4 * {
+        const uint32_t ob = v < head ? 0u : v - head;
+        uint32_t lo = 0, hi = 32;  // the last lane whose first block is at or before ob
+#pragma unroll
+        for (int it = 0; it < 5; it++) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (__shfl_sync(kFull, boff, mid) <= ob) lo = mid;
+            else hi = mid;
+        }
+        const uint32_t base = __shfl_sync(kFull, boff, lo);
+        const uint4 *list = reinterpret_cast<const uint4 *>(rec + lists_at + 2ull * lo * Ts) + (ob - base);
+        return v < head ? reinterpret_cast<const uint4 *>(rec) + v : list;
+    };
+    const EndAligned ea(len / 16);
+    constexpr int U = 8;
+    uint32_t R = 0;
+    for (uint32_t r0 = 0; r0 < ea.rounds; r0 += U) {
+        uint4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t v = int64_t(32) * (r0 + u) + lane - ea.v0;
+            const uint32_t vv = v < 0 ? 0u : uint32_t(v);
+            const uint4 *sp = src_of(vv);  // every lane takes part in the search's shuffles
+            t[u] = (r0 + u < ea.rounds && v >= 0) ? __ldcs(sp) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const uint32_t r = r0 + u;
+            if (r >= ea.rounds) break;
+            const int64_t v = int64_t(32) * r + lane - ea.v0;
+            if (r > 0) R = shift_smem(R, cs.gap496);
+            if (v >= 0) {
+                reinterpret_cast<uint4 *>(dst)[v] = t[u];
+                R = crc_rep16<kCodeCrcCopies>(R, t[u], row);
+            }
+        }
+    }
+    return ea.rounds ? crc_fold<1, 4>(R, nullptr) : 0u;
+}
+
 // Copy the len bytes of a source (zero-padded to 16) by the warp, 8 vectors
 // in flight per lane; dst is 16-aligned.
 template <bool kDelta>
@@ -1056,8 +1162,11 @@ __device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, ui
     const uint32_t f[8] = {fv.x & 0xFFFFu, fv.x >> 16, fv.y & 0xFFFFu, fv.y >> 16,
                            fv.z & 0xFFFFu, fv.z >> 16, fv.w & 0xFFFFu, fv.w >> 16};
     const uint8_t *cand = a.ws_cand + (uint64_t(cl) * W + J) * a.n_pad;
-    const uint32_t rb = rans_encode_stream(cand, n, f, etab, ring, reinterpret_cast<uint16_t *>(ring + 4096),
-                                           slot + uint64_t(J) * a.rec_stride, lim, a.version == 2);
+    uint16_t *stage = reinterpret_cast<uint16_t *>(ring + 4096);
+    uint8_t *rec = slot + uint64_t(J) * a.rec_stride;
+    const uint32_t rb = a.version == 3 ? rans_encode_stream<true>(cand, n, f, etab, ring, stage, rec, lim, false)
+                                       : rans_encode_stream<false>(cand, n, f, etab, ring, stage, rec, lim,
+                                                                   a.version == 2);
     if (rb != kAborted && rb < lim) {
         mode[J] = kModeRans;
         val[J] = rb;
@@ -1156,9 +1265,19 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
                 uint32_t part[4];
                 warp_raw_streams<DT, kDelta>(src, n, mode, roff, out, cs, part);
 #pragma unroll
-                for (int j = 0; j < W; j++)
-                    if (mode[j] == kModeRans)
-                        part[j] = warp_copy_crc(slot + uint64_t(j) * a.rec_stride, pad16(val[j]), out + roff[j], cs);
+                for (int j = 0; j < W; j++) {
+                    if (mode[j] != kModeRans) continue;
+                    const uint8_t *rec = slot + uint64_t(j) * a.rec_stride;
+                    if (a.version == 3) {
+                        // v3: the lists follow the table and the counts
+                        const uint32_t k = warp_sum_u32(__popc(rec[128 + lane]));
+                        const uint32_t lists_at = kRecHead + uint32_t(pad16(2 * k)) + 64;
+                        const uint32_t Ts = ((n + 31) / 32 + 7) & ~7u;
+                        part[j] = warp_copy_crc_lanes(rec, val[j], lists_at, Ts, out + roff[j], cs);
+                    } else {
+                        part[j] = warp_copy_crc(rec, pad16(val[j]), out + roff[j], cs);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < W; j++) {
                     if (mode[j] == kModeConst) continue;

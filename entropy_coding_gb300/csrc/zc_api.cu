@@ -37,8 +37,14 @@ constexpr uint64_t kWaveBytes = 2048ull << 20;  // workspace of one statistics +
 // gives a stream up once its record has reached lim, after at most one more
 // batch of 32 steps x 32 words (2048 bytes); a record can never exceed the
 // header, the table and one word per symbol.
-uint64_t rec_stride(uint32_t chunk_bytes, int W, double threshold) {
+uint64_t rec_stride(uint32_t chunk_bytes, int W, double threshold, uint32_t version = 1) {
     const uint64_t n = chunk_bytes / W;
+    if (version == 3) {
+        // a word list per lane: each lane's words are staged at a stride of
+        // pad8(T) words (T = steps) after the counts, whatever the threshold
+        const uint64_t Ts = ((n + 31) / 32 + 7) & ~uint64_t(7);
+        return pad16(kRecHead + kMaxTable + 64 + 2 * 32 * Ts) + 16;
+    }
     const uint64_t full = kRecHead + kMaxTable + 2 * n;
     const double lim = std::ceil(threshold * double(n));
     uint64_t cap = full;
@@ -46,8 +52,8 @@ uint64_t rec_stride(uint32_t chunk_bytes, int W, double threshold) {
     return pad16(cap) + 16;
 }
 
-uint64_t slot_bytes(uint32_t chunk_bytes, int W, double threshold) {
-    return pad256(uint64_t(W) * rec_stride(chunk_bytes, W, threshold));
+uint64_t slot_bytes(uint32_t chunk_bytes, int W, double threshold, uint32_t version = 1) {
+    return pad256(uint64_t(W) * rec_stride(chunk_bytes, W, threshold, version));
 }
 
 // Workspace after the control block and the chunk status words: the wave's
@@ -148,7 +154,7 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
     const uint8_t *b = static_cast<const uint8_t *>(h_blob_prefix);
     if (!b || !out || avail < ZC_HEADER_BYTES) return ZC_EFORMAT;
     const uint32_t version = uint32_t(b[4] | b[5] << 8);
-    if (std::memcmp(b, "ZCNN", 4) != 0 || (version != 1 && version != 2)) return ZC_EFORMAT;
+    if (std::memcmp(b, "ZCNN", 4) != 0 || version < 1 || version > 3) return ZC_EFORMAT;
     const int dtype = b[6], ndim = b[7];
     const uint32_t chunk_bytes = get32(b + 8);
     const uint64_t nbytes = get64(b + 16);
@@ -196,7 +202,7 @@ extern "C" int zc_blob_info(const void *h_blob_prefix, uint64_t avail, zc_info *
         const uint64_t len = (c + 1 < nc) ? chunk_bytes : nbytes - uint64_t(c) * chunk_bytes;
         const uint32_t sm = get32(e + 8), stored = sm & 0x7FFFFFFFu;
         if (get64(e) != off) return ZC_EFORMAT;
-        if ((sm >> 31) ? stored != len : (stored % 16 || stored > max_grouped(len, W))) return ZC_EFORMAT;
+        if ((sm >> 31) ? stored != len : (stored % 16 || stored > max_grouped(len, W, version))) return ZC_EFORMAT;
         off += pad16(stored);
     }
     out->dtype = dtype;
@@ -357,8 +363,8 @@ uint64_t ws_size(uint64_t n, uint64_t nc, int W, uint32_t chunk_bytes, uint32_t 
     if (version == 2 && wave < max_tc) wave = max_tc;
     // every coding warp for thresholds up to 1; at least one warp for any
     // threshold (larger thresholds then run fewer warps)
-    uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0);
-    const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9);
+    uint64_t slots = max_workers(nc) * slot_bytes(chunk_bytes, W, 1.0, version);
+    const uint64_t one_any = slot_bytes(chunk_bytes, W, 1e9, version);
     if (slots < one_any) slots = one_any;
     return head + pad256(8 * nc) + wave_layout(wave, W, chunk_bytes).slots + slots;
 }
@@ -402,7 +408,7 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
     }
     if (nc == 0) return ZC_OK;
 
-    const uint64_t slot = slot_bytes(chunk_bytes, W, threshold);
+    const uint64_t slot = slot_bytes(chunk_bytes, W, threshold, version);
     uint64_t wave = wave_chunks(nc, chunk_bytes, W);
     if (version == 2 && wave < max_tc) wave = max_tc;
     const uint64_t most_workers = max_workers(nc);
@@ -444,9 +450,9 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
     a.n_pad = n_pad(chunk_bytes, W);
     a.ws_slots = a.ws_ctrl + area0 + lay.slots;
     a.slot_bytes = slot;
-    a.rec_stride = rec_stride(chunk_bytes, W, threshold);
+    a.rec_stride = rec_stride(chunk_bytes, W, threshold, version);
     a.workers = uint32_t(workers < wave ? workers : wave);
-    if (version == 1) {
+    if (version != 2) {
         for (uint64_t w0 = 0; w0 < nc; w0 += wave) {
             a.wave_start = uint32_t(w0);
             a.wave_n = uint32_t(nc - w0 < wave ? nc - w0 : wave);
@@ -479,14 +485,21 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
     return ZC_OK;
 }
 
-uint32_t version_of(uint32_t flags) { return (flags & ZC_SHARED_TABLES) ? 2u : 1u; }
+// Blob format of a compression call's flags: 1 by default, 2 with shared
+// plane tables, 3 with a word list per lane; 0 for flags that are invalid
+// (unknown bits, or both formats at once).
+uint32_t version_of(uint32_t flags) {
+    if (flags & ~(ZC_SHARED_TABLES | ZC_LANE_WORDS)) return 0;
+    if ((flags & ZC_SHARED_TABLES) && (flags & ZC_LANE_WORDS)) return 0;
+    return (flags & ZC_SHARED_TABLES) ? 2u : (flags & ZC_LANE_WORDS) ? 3u : 1u;
+}
 
 int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
                   uint32_t chunk_bytes, double threshold, void *d_blob, uint64_t blob_capacity,
                   uint64_t *d_blob_bytes, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream,
                   uint32_t flags = 0) {
-    if (!d_status || (flags & ~ZC_SHARED_TABLES)) return ZC_EINVAL;
     const uint32_t version = version_of(flags);
+    if (!d_status || version == 0) return ZC_EINVAL;
     EncodeArgs a{};
     const int st = make_tensor(d_src, d_base, nbytes, dtype, ndim, h_shape, chunk_bytes, threshold, d_blob,
                                blob_capacity, d_blob_bytes, version, a.one);
@@ -506,7 +519,7 @@ int make_blob(const void *d_blob, const zc_info *info, const void *d_base, void 
     const int W = word_bytes(info->dtype);
     if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
     if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
-    if (info->version != 1 && info->version != 2) return ZC_EINVAL;
+    if (info->version < 1 || info->version > 3) return ZC_EINVAL;
     const uint64_t planes = info->version == 2 ? 512ull * W : 0;  // v2: the plane tables
     if (info->blob_bytes < ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks + planes) return ZC_EINVAL;
     if (dst_capacity < info->nbytes || (info->nbytes && !d_dst)) return ZC_ECAPACITY;
@@ -548,7 +561,7 @@ bool delta_dtype(int dtype) { return dtype == ZC_U8 || dtype == ZC_U16 || dtype 
 } // namespace
 
 extern "C" uint64_t zc_workspace_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, uint32_t flags) {
-    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95) || (flags & ~ZC_SHARED_TABLES)) return 0;
+    if (!valid_params(nbytes, dtype, chunk_bytes, 0.95) || version_of(flags) == 0) return 0;
     const uint64_t nc = chunks_of(nbytes, chunk_bytes);
     return ws_size(1, nc, word_bytes(dtype), chunk_bytes, version_of(flags), nc);
 }
@@ -559,7 +572,7 @@ extern "C" uint64_t zc_workspace_size(uint64_t nbytes, int dtype, uint32_t chunk
 
 extern "C" uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int dtype, uint32_t chunk_bytes,
                                             uint32_t flags) {
-    if (flags & ~ZC_SHARED_TABLES) return 0;
+    if (version_of(flags) == 0) return 0;
     if (n == 0) return kCtrlBytes;
     if (!nbytes) return 0;
     uint64_t nc = 0, max_tc = 0;
@@ -575,9 +588,19 @@ extern "C" uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, 
 
 extern "C" uint64_t zc_blob_size_ex(uint64_t nbytes, int dtype, uint32_t chunk_bytes, double threshold,
                                     uint32_t flags) {
-    if (flags & ~ZC_SHARED_TABLES) return 0;
-    const uint64_t b = zc_blob_size(nbytes, dtype, chunk_bytes, threshold);
-    return b && version_of(flags) == 2 ? b + 512ull * word_bytes(dtype) : b;
+    const uint32_t version = version_of(flags);
+    if (version == 0 || !valid_params(nbytes, dtype, chunk_bytes, threshold)) return 0;
+    const int W = word_bytes(dtype);
+    const uint64_t nc = chunks_of(nbytes, chunk_bytes);
+    uint64_t total = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * nc + (version == 2 ? 512ull * W : 0ull);
+    if (nc == 0) return total;
+    const uint64_t full = nc - 1, last = nbytes - full * chunk_bytes;
+    auto worst = [&](uint64_t len) {
+        uint64_t w = pad16(len);
+        if (threshold > 1.0 && max_grouped(len, W, version) > w) w = max_grouped(len, W, version);
+        return w;
+    };
+    return total + full * worst(chunk_bytes) + worst(last);
 }
 
 extern "C" int zc_compress_ex(const void *d_src, uint64_t nbytes, int dtype, int ndim, const int64_t *h_shape,
@@ -628,8 +651,8 @@ extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const vo
                                  uint32_t chunk_bytes, double threshold, uint32_t flags, void *const *d_blobs,
                                  const uint64_t *blob_capacities, uint64_t *d_blob_bytes, void *d_ws,
                                  uint64_t ws_bytes, int32_t *d_status, void *stream) {
-    if (flags & ~ZC_SHARED_TABLES) return ZC_EINVAL;
     const uint32_t version = version_of(flags);
+    if (version == 0) return ZC_EINVAL;
     if (n == 0) return ZC_OK;
     if (!d_srcs || !nbytes || !ndims || !shapes || !d_blobs || !blob_capacities || !d_blob_bytes || !d_status)
         return ZC_EINVAL;
@@ -721,7 +744,7 @@ extern "C" int zc_verify(const void *d_blob, const zc_info *info, int32_t *d_sta
     const int W = word_bytes(info->dtype);
     if (!valid_params(info->nbytes, info->dtype, info->chunk_bytes, 0.95)) return ZC_EINVAL;
     if (chunks_of(info->nbytes, info->chunk_bytes) != info->n_chunks) return ZC_EINVAL;
-    if (info->version != 1 && info->version != 2) return ZC_EINVAL;
+    if (info->version < 1 || info->version > 3) return ZC_EINVAL;
     const uint64_t table_end = ZC_HEADER_BYTES + uint64_t(ZC_ENTRY_BYTES) * info->n_chunks +
                                (info->version == 2 ? 512ull * W : 0ull);
     if (info->blob_bytes < table_end || !aligned(d_blob, 16)) return ZC_EINVAL;

@@ -33,10 +33,12 @@ __host__ __device__ inline int word_bytes(int dtype) {
 }
 
 // Largest grouped payload of a chunk of n symbols per stream and W streams:
-// the directory plus W records of at most 160 + 512 + 2n bytes each.
-__host__ __device__ inline uint64_t max_grouped(uint64_t len, int W) {
+// the directory plus W records of at most 160 + 512 + 2n bytes each (format
+// v3: and 64 bytes of word counts and up to 7 padding words per lane).
+__host__ __device__ inline uint64_t max_grouped(uint64_t len, int W, uint32_t version = 1) {
     uint64_t n = len / uint64_t(W);
-    return pad16(4ull * W) + uint64_t(W) * pad16(kRecHead + kMaxTable + 2 * n);
+    const uint64_t extra = version == 3 ? 64 + 14 * kLanes : 0;
+    return pad16(4ull * W) + uint64_t(W) * pad16(kRecHead + kMaxTable + 2 * n + extra);
 }
 
 // ---------------------------------------------------------------------------

@@ -127,6 +127,13 @@ __device__ __forceinline__ uint32_t owner_of(const D *table, uint32_t n, uint32_
 int encode_warps_per_sm();
 // delta: whether the blobs carry base tensors (all or none of them)
 int launch_decode(int dtype, bool delta, const DecodeArgs &a, cudaStream_t s);
+// the kernels of one dtype (decode_<dtype>.cu)
+int launch_decode_u8(bool delta, const DecodeArgs &a, cudaStream_t s);
+int launch_decode_u16(bool delta, const DecodeArgs &a, cudaStream_t s);
+int launch_decode_u32(bool delta, const DecodeArgs &a, cudaStream_t s);
+int launch_decode_bf16(bool delta, const DecodeArgs &a, cudaStream_t s);
+int launch_decode_fp16(bool delta, const DecodeArgs &a, cudaStream_t s);
+int launch_decode_fp32(bool delta, const DecodeArgs &a, cudaStream_t s);
 int launch_crc(const CrcArgs &a, cudaStream_t s);
 int launch_verify(const VerifyArgs &a, cudaStream_t s);
 

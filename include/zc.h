@@ -84,6 +84,10 @@ enum zc_status {
 /* compression flag: blob format v2 (one 12-bit table per byte plane of the
  * tensor, shared by all its chunks; lmzip "Building on lmz") */
 #define ZC_SHARED_TABLES 2u
+/* compression flag: blob format v3 (v1 with a word list per rANS lane in
+ * every coded record; lmzip "On a GPU": the decoder is bound by the lanes'
+ * dependent chains). Not combinable with ZC_SHARED_TABLES. */
+#define ZC_LANE_WORDS 4u
 
 /* Parameter limits of format v1. */
 #define ZC_MIN_CHUNK 64u
