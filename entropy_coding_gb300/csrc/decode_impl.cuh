@@ -94,9 +94,20 @@ __device__ __forceinline__ bool mbar_test(unsigned long long *b, uint32_t parity
         : "memory");
     return done != 0;
 }
+__device__ __forceinline__ bool mbar_done(unsigned long long *b, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tmbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\tselp.b32 %0, 1, 0, P;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 // Wait (the whole warp) until the phase of the given parity has completed;
-// false after `limit` clock cycles (about a second in normal calls).
+// false after `limit` clock cycles (about a second in normal calls). A
+// phase that has already completed costs one test and no clock read.
 __device__ bool mbar_wait(unsigned long long *b, uint32_t parity, unsigned long long limit) {
+    if (__all_sync(kFull, mbar_done(b, parity))) return true;
     const long long t0 = clock64();
     for (;;) {
         if (__all_sync(kFull, mbar_test(b, parity))) return true;
@@ -156,17 +167,19 @@ __device__ __forceinline__ void lane_fill(Rans &r, int32_t lowest) {
 }
 
 // After every 8 steps: a lane keeps its current block and the three below
-// it in its ring (a lane takes at most 8 words in 8 steps, so it crosses at
-// most one block boundary between two calls); the copy for a block is
-// requested 3 blocks before it is entered and waited for 3 calls later
-// (wait_group 2: every lane commits one group per call).
+// it in its ring. A lane takes at most 8 words in 8 steps, so it crosses at
+// most one block boundary between two calls and at most one block is
+// requested per call; the copy for a block is requested 3 blocks before it
+// is entered and waited for 3 calls later (wait_group 2: every lane commits
+// one group per call).
 __device__ __forceinline__ void lane_refill(Rans &r) {
-    lane_fill(r, (r.ptr >> 3) - 3);
+    const int32_t want = (r.ptr >> 3) - 3;
+    if (r.filled > want && r.filled > 0) {
+        r.filled--;
+        cp_async16(lane_slot(r.ring, r.filled), r.wbase + 16 * r.filled);
+    }
+    cp_async_commit();
     cp_async_wait<2>();
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Fetch 256-word block b of a record's word area into its ring slot.
@@ -517,11 +530,16 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
     }
     const uint32_t ng = (cx.T + 7) / 8;  // groups including a partial last one
     for (uint32_t g = 0; g < ng; g++) {
-        const uint32_t k = g % kStages, r = g / kStages;
-        if (r > 0 && !mbar_wait(&ps.empty[k], (r - 1) & 1u, a.wait_cycles)) {
-            if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
-            cp_async_wait_all();
-            return;
+        const uint32_t k = g % kStages;
+        // the consumer frees the stages in order: at an even group, wait for
+        // the stage of the next group too (one wait for two groups)
+        if ((g & 1u) == 0) {
+            const uint32_t gw = g + 1 < ng ? g + 1 : g, kw = gw % kStages, rw = gw / kStages;
+            if (rw > 0 && !mbar_wait(&ps.empty[kw], (rw - 1) & 1u, a.wait_cycles)) {
+                if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+                cp_async_wait_all();
+                return;
+            }
         }
         if constexpr (!kLanes) ring_refill(rs);
         else lane_refill(rs);
@@ -784,12 +802,17 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
 
 // Chunk c of blob bd, by one warp pair (kV2: format v2, with the CTA's
 // plane tables pbig).
-template <int DT, bool kBig, bool kDelta, bool kV2, int C, bool kLanes, class PS>
-__device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c, bool producer, PS &ps,
+// role: 0 the producer (rANS lanes), 1 the consumer (output), 2 the CRC
+// warp (kCrcWarp: the chunk's CRC over its stored bytes is checked by a
+// warp of its own, in parallel with the decoding; else the consumer takes
+// it as it reads the payload).
+template <int DT, bool kBig, bool kDelta, bool kV2, int C, bool kLanes, bool kCrcWarp, class PS>
+__device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c, int role, PS &ps,
                              const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256],
                              const uint32_t *const *pbig) {
     constexpr int W = WordOf<DT>::W;
     const int lane = threadIdx.x & 31;
+    const bool producer = role == 0;
     const uint8_t *const blob = bd.blob;
     const uint64_t blob_bytes = bd.blob_bytes, nbytes = bd.nbytes;
     const uint32_t n_chunks = bd.n_chunks;
@@ -819,6 +842,17 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
     }
     const uint8_t *p = blob + off;
     const bool verify = !(a.flags & ZC_NO_VERIFY);
+    if (role == 2) {
+        // CRC warp: the stored bytes, 8 pieces of 16 bytes in flight per
+        // lane, then the last stored % 16 bytes one at a time
+        if (!verify) return;
+        const uint32_t main = stored & ~15u;
+        uint32_t reg = shift_bytes_small(0xFFFFFFFFu, main) ^ warp_crc16<C, false, 8>(p, main, crc_rep, gap496);
+        const uint32_t *row = crc_row<C>(crc_rep);
+        for (uint32_t i = main; i < stored; i++) reg = crc_rep_byte<C>(reg, __ldg(p + i), row);
+        if ((reg ^ 0xFFFFFFFFu) != ent.w && lane == 0) status_or(a.d_status, ZC_ECRC);
+        return;
+    }
     uint8_t *out = dst + uint64_t(c) * a.chunk_bytes;
     const uint8_t *basec = kDelta ? base + uint64_t(c) * a.chunk_bytes : nullptr;
     if (raw) {
@@ -834,7 +868,8 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
         }
         for (uint32_t i = nvec * 16 + lane; i < len; i += 32) out[i] = kDelta ? uint8_t(p[i] ^ basec[i]) : p[i];
         // a RAW chunk stores the original bytes, so its CRC is the payload's
-        if (verify && (crc_strided<1, false, C>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
+        if (!kCrcWarp && verify &&
+            (crc_strided<1, false, C>(p, len, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) != ent.w &&
             lane == 0)
             status_or(a.d_status, ZC_ECRC);
         return;
@@ -845,8 +880,9 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
         if (!producer) {
             if (lane == 0) status_or(a.d_status, ZC_ECORRUPT);
             // a changed payload is reported as such (the check the caller asked for)
-            if (verify && (crc_strided<1, false, C>(p, stored, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) !=
-                              ent.w && lane == 0)
+            if (!kCrcWarp && verify &&
+                (crc_strided<1, false, C>(p, stored, 0xFFFFFFFFu, crc_rep, gap496, nullptr) ^ 0xFFFFFFFFu) !=
+                    ent.w && lane == 0)
                 status_or(a.d_status, ZC_ECRC);
         }
         return;
@@ -862,7 +898,7 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
     cx.base = basec;
     if (producer) {
         if (cx.have_main) produce<DT, kBig, kV2, kLanes>(a, cx, ps, pbig);
-    } else if (verify) {
+    } else if (verify && !kCrcWarp) {
         consume<DT, true, kDelta, C>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
     } else {
         consume<DT, false, kDelta, C>(a, cx, ps, ent.w, crc_rep, gshift, gap496);
@@ -872,6 +908,12 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
 // One CTA per SM. With one-level tables (kBig: few chunks per SM, 16 KB of
 // table per pair) the CRC tables have 8 copies; with two-level tables (up
 // to 16 pairs) they have 16, so fewer lanes meet on a bank.
+// Warps per chunk: with one-level tables (few chunks per SM, so the pair's
+// chains are latency-bound) a third warp checks the chunk's CRC; with up to
+// 16 pairs per CTA there is no room for it and the consumer takes the CRC.
+template <bool kBig>
+constexpr int warps_per_chunk() { return kBig ? 3 : 2; }
+
 template <int DT, bool kBig, bool kDelta, bool kLanes>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -887,7 +929,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         load_shift_smem(gshift, kShPow + 8);  // 256 bytes
         load_shift_smem(gap496, kSh496);
     }
-    const uint32_t pairs_per_cta = blockDim.x >> 6;
+    constexpr int kWpc = warps_per_chunk<kBig>();
+    const uint32_t pairs_per_cta = blockDim.x / (32 * kWpc);
     if (threadIdx.x < pairs_per_cta) {
         PairSmem<kBig> &ps = pairs[threadIdx.x];
         for (int k = 0; k < kStages; k++) {
@@ -897,12 +940,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         mbar_init(&ps.start, 32);
     }
     __syncthreads();
-    const uint32_t g = blockIdx.x * pairs_per_cta + (warp >> 1);
+    const uint32_t slot = uint32_t(warp) / kWpc;
+    const uint32_t g = blockIdx.x * pairs_per_cta + slot;
     if (g >= a.total_chunks) return;
     // the blob of this call-wide chunk index
     const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
-    decode_chunk<DT, kBig, kDelta, false, C, kLanes>(a, bd, g - bd.chunk_base, (warp & 1) == 0, pairs[warp >> 1],
-                                                     crc_rep, gshift, gap496, nullptr);
+    decode_chunk<DT, kBig, kDelta, false, C, kLanes, kBig>(a, bd, g - bd.chunk_base, int(uint32_t(warp) % kWpc),
+                                                           pairs[slot], crc_rep, gshift, gap496, nullptr);
 }
 
 // Format v2 (shared plane tables): a CTA decodes up to a.pairs consecutive
@@ -1013,8 +1057,8 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
     const uint32_t *pbig[4] = {nullptr, nullptr, nullptr, nullptr};
 #pragma unroll
     for (int j = 0; j < W; j++) pbig[j] = pvalid[j] ? big + j * kM : nullptr;
-    decode_chunk<DT, true, kDelta, true, C, false>(a, bd, first + pair, (warp & 1) == 0, pairs[pair], crc_rep,
-                                                   gshift, gap496, pbig);
+    decode_chunk<DT, true, kDelta, true, C, false, false>(a, bd, first + pair, warp & 1, pairs[pair], crc_rep,
+                                                          gshift, gap496, pbig);
 }
 
 template <int DT, bool kBig, bool kDelta, bool kLanes>
@@ -1027,7 +1071,7 @@ int launch_decode_mode(const DecodeArgs &a, uint32_t pc, cudaStream_t s) {
                              int(std::min<size_t>(smem_max, 227 * 1024))) != cudaSuccess)
         return ZC_ECUDA;
     const int grid = int((a.total_chunks + pc - 1) / pc);
-    decode_kernel<DT, kBig, kDelta, kLanes><<<grid, 64 * pc, smem, s>>>(a);
+    decode_kernel<DT, kBig, kDelta, kLanes><<<grid, 32 * warps_per_chunk<kBig>() * pc, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;
 }
 

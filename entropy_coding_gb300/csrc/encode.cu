@@ -787,6 +787,18 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         acc.w = (acc.w >> 16) | (w << 16);
         if ((++count & 7u) == 0) lw4[(count >> 3) - 1] = acc;
     };
+    // the same for a lane that may or may not emit, without a branch on em
+    // (the shifted block is selected; only a full block's store branches)
+    auto push_if = [&](bool em, uint32_t w, uint32_t &count) {
+        const uint4 sh = make_uint4(__funnelshift_r(acc.x, acc.y, 16), __funnelshift_r(acc.y, acc.z, 16),
+                                    __funnelshift_r(acc.z, acc.w, 16), (acc.w >> 16) | (w << 16));
+        acc.x = em ? sh.x : acc.x;
+        acc.y = em ? sh.y : acc.y;
+        acc.z = em ? sh.z : acc.z;
+        acc.w = em ? sh.w : acc.w;
+        count += em ? 1u : 0u;
+        if (em && (count & 7u) == 0) lw4[(count >> 3) - 1] = acc;
+    };
     const uint32_t gt = lanemask_gt();
     uint32_t x = kRansL;
     uint32_t wc = 0;  // v1/v2: words of the warp; v3: words of this lane
@@ -798,7 +810,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         for (int s = 0; s < cnt; s++) {
             const bool em = (flags >> s) & 1u;
             if constexpr (kLanes) {
-                if (em) push(st[s * 32], wc);
+                push_if(em, st[s * 32], wc);
             } else {
                 const uint32_t B = __ballot_sync(kFull, em);
                 if (em) wout[wc + __popc(B & gt)] = st[s * 32];
@@ -843,7 +855,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
                 const bool em = fp & 1u;
                 fp >>= 1;
                 if constexpr (kLanes) {
-                    if (em) push(st_prev[s * 32], wc);
+                    push_if(em, st_prev[s * 32], wc);
                 } else {
                     const uint32_t B = __ballot_sync(kFull, em);
                     if (em) wout[wc + __popc(B & gt)] = st_prev[s * 32];
