@@ -53,12 +53,13 @@ def _args():
     p.add_argument("--no-verify", action="store_true", help="decode without the CRC check")
     p.add_argument("--shared-tables", action="store_true",
                    help="blob format v2: one table per byte plane of each tensor (ZC_SHARED_TABLES)")
-    p.add_argument("--streams", type=int, default=4,
+    p.add_argument("--streams", type=int, default=8,
                    help="llama8b: the per-tensor calls are issued round-robin on this many CUDA streams, each "
                         "with its own workspace (1: one stream, every call after the previous one)")
     p.add_argument("--format", type=int, default=None, choices=[1, 2, 3],
                    help="blob format: 1 (a table and one word list per coded stream), 2 (shared plane "
-                        "tables, as --shared-tables), 3 (a word list per rANS lane, ZC_LANE_WORDS)")
+                        "tables, as --shared-tables), 3 (a word list per rANS lane, ZC_LANE_WORDS; the "
+                        "default)")
     return p.parse_args()
 
 
@@ -69,7 +70,7 @@ FORMAT_NAMES = {1: "v1 (a table and one word list per coded stream)", 2: "v2 (sh
 def format_version(a) -> int:
     if a.format is not None:
         return a.format
-    return 2 if a.shared_tables else 1
+    return 2 if a.shared_tables else 3
 
 
 def format_flags(a, zc) -> int:
@@ -248,9 +249,9 @@ def _oracle_round_trip(job):
     """One pool worker's share of a reference step: the oracle, as it stands,
     compresses and decompresses its sample; returns the bytes and whether the
     round trip was exact."""
-    raw, code, chunk_bytes, threshold = job
+    raw, code, chunk_bytes, threshold, version = job
     import oracle
-    blob = oracle.compress(raw, code, None, chunk_bytes, threshold)
+    blob = oracle.compress(raw, code, None, chunk_bytes, threshold, version)
     return raw.size, oracle.decompress(blob).tobytes() == raw.tobytes()
 
 
@@ -269,7 +270,7 @@ def run_reference_model(a):
     for i in range(1, 1 + cores):  # layer 0, 1, ... tensors after the embedding
         nm, shape = specs[i]
         raw = wl.as_bytes(wl.llama8b_tensor(i, nm, shape)).numpy()
-        jobs.append((raw[: 16 * a.chunk_bytes].copy(), wl.BF16, a.chunk_bytes, a.threshold))
+        jobs.append((raw[: 16 * a.chunk_bytes].copy(), wl.BF16, a.chunk_bytes, a.threshold, format_version(a)))
     sample = sum(j[0].size for j in jobs)
     with mp.get_context("spawn").Pool(cores) as pool:
         for _ in range(max(1, a.warmup)):
@@ -315,13 +316,13 @@ def run_reference(a):
     W = raw.size // max(1, t.numel())
     sample = min(raw.size, 16 * a.chunk_bytes)     # 2 MiB per step: a few seconds of CPU work
     part = raw[:sample]
-    blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold)   # warm-up
+    blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold, format_version(a))  # warm-up
     oracle.decompress(blob)
     t_enc = t_dec = 0.0
     size = 0
     for _ in range(a.steps):
         t0 = time.perf_counter()
-        blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold)
+        blob = oracle.compress(part, code, (sample // W,), a.chunk_bytes, a.threshold, format_version(a))
         t1 = time.perf_counter()
         out = oracle.decompress(blob)
         t2 = time.perf_counter()
@@ -358,7 +359,7 @@ def cpu_baseline(t, code, a):
     while t_total < budget and done < raw.size:
         part = raw[done:done + step]
         t0 = time.perf_counter()
-        blob = oracle.compress(part, code, (part.size // W,), a.chunk_bytes, a.threshold)
+        blob = oracle.compress(part, code, (part.size // W,), a.chunk_bytes, a.threshold, format_version(a))
         out = oracle.decompress(blob)
         t_total += time.perf_counter() - t0
         assert out.tobytes() == part.tobytes()

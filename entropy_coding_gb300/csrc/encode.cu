@@ -837,14 +837,17 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
         if (b > 0 && cnt == 32) {
             // a full block, interleaved with the write-out of the previous one
             // (always full): one straight-line body, so the two chains overlap
-            uint32_t sym_n = blk[32];
-            uint4 e = etab[blk[0]];
+            // table entries two steps ahead, symbols three (rows past the
+            // block read the next ring slot or the stage: values never used)
+            uint32_t sym_n = blk[64];
+            uint4 e = etab[blk[0]], e2 = etab[blk[32]];
             uint32_t fp = flags_prev;
 #pragma unroll 8
             for (int s = 0; s < 32; s++) {
                 const uint4 ec = e;
-                e = etab[sym_n];
-                sym_n = blk[(s + 2) * 32];
+                e = e2;
+                e2 = etab[sym_n];
+                sym_n = blk[(s + 3) * 32];
                 const bool emit = x >= ec.z;
                 st_cur[s * 32] = uint16_t(x);
                 flags |= emit ? (1u << s) : 0u;

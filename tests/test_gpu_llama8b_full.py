@@ -30,12 +30,21 @@ from entropy_coding_gb300 import workloads as wl  # noqa: E402
 DEV = torch.device("cuda:0")
 
 
-def test_llama8b_every_tensor_matches_oracle(zco):
+@pytest.mark.parametrize("version,streams", [(1, 1), (3, 8)])
+def test_llama8b_every_tensor_matches_oracle(zco, version, streams):
+    """Format v1 one call after another, and format v3 (a word list per lane)
+    with the calls issued round-robin on 8 streams, each with its own
+    workspace: the launch configuration the benchmark times."""
     from oracle.parallel import blob_digest
 
+    flags = {1: 0, 3: zc.LANE_WORDS}[version]
+    C, thr = 131072, 0.95
     specs = wl.llama8b_specs()
     order = [0, len(specs) - 1] + list(range(1, len(specs) - 1))
     cores = max(1, len(os.sched_getaffinity(0)))
+    workers = [torch.cuda.Stream(device=DEV) for _ in range(streams)]
+    ws_bytes = max(zc.workspace_size(2 * torch.Size(sh).numel(), wl.BF16, C, flags) for _, sh in specs)
+    ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=DEV) for _ in range(streams)]
     pending: dict = {}
     checked = total_bytes = total_blob = 0
 
@@ -50,19 +59,35 @@ def test_llama8b_every_tensor_matches_oracle(zco):
             checked += 1
 
     with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
-        for idx in order:
-            name, shape = specs[idx]
-            t = wl.llama8b_tensor(idx, name, shape, DEV)
-            blob = zc.compress(t)
-            back = zc.decompress(blob)
-            assert torch.equal(back.view(torch.int16), t.view(torch.int16)), name
-            gpu = blob.cpu().numpy().tobytes()
-            raw = wl.as_bytes(t).cpu().numpy()
-            total_bytes += raw.size
-            total_blob += len(gpu)
-            want = (len(gpu), hashlib.sha256(gpu).hexdigest())
-            del t, blob, back, gpu
-            pending[ex.submit(blob_digest, raw, wl.BF16, shape, 131072, 0.95, 1)] = (name, want)
+        for i0 in range(0, len(order), streams):
+            group = []
+            for k, idx in enumerate(order[i0:i0 + streams]):
+                name, shape = specs[idx]
+                src = wl.as_bytes(wl.llama8b_tensor(idx, name, shape, DEV))
+                blob = torch.empty(zc.blob_size(src.numel(), wl.BF16, C, thr, flags), dtype=torch.uint8, device=DEV)
+                nb = torch.zeros(1, dtype=torch.int64, device=DEV)
+                st = torch.zeros(1, dtype=torch.int32, device=DEV)
+                zc.compress_into(src, blob, nb, ws[k], st, C, thr, workers[k], dtype=wl.BF16, shape=tuple(shape),
+                                 flags=flags)
+                group.append((k, name, shape, src, blob, nb, st))
+            torch.cuda.synchronize()
+            outs = []
+            for k, name, shape, src, blob, nb, st in group:
+                assert int(st.item()) == 0, name
+                b = blob[: int(nb.item())]
+                out = torch.empty_like(src)
+                zc.decompress_into(b, zc.read_info(b), out, st, True, workers[k])
+                outs.append((name, shape, src, b, out, st))
+            torch.cuda.synchronize()
+            for name, shape, src, b, out, st in outs:
+                assert int(st.item()) == 0 and torch.equal(out, src), name
+                gpu = b.cpu().numpy().tobytes()
+                raw = src.cpu().numpy()
+                total_bytes += raw.size
+                total_blob += len(gpu)
+                want = (len(gpu), hashlib.sha256(gpu).hexdigest())
+                pending[ex.submit(blob_digest, raw, wl.BF16, shape, C, thr, version)] = (name, want)
+            del group, outs
             while len(pending) > 2 * cores:
                 settle(block=True)
         while pending:

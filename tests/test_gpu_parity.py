@@ -344,6 +344,30 @@ def test_decode_reports_changed_payload_as_crc(zco):
             assert (out[keep] == raw[keep]).all()
 
 
+@pytest.mark.parametrize("version", [1, 3])
+def test_many_chunks_per_sm_report_every_chunk(zco, version):
+    """With many chunks per SM (two-level tables, 16 chunks per CTA here) the
+    consumer checks the CRC as it reads: a changed byte in any chunk, at
+    every position of a CTA's chunk list, is reported, and the blob decodes
+    exactly when nothing was changed."""
+    t = wl.fp32_64m("cpu", rows=128)  # 4 MiB: 4096 chunks of 1 KiB, 27 per SM
+    raw = wl.as_bytes(t).numpy()
+    C = 1024
+    blob = zco.compress(raw, wl.dtype_code(t), tuple(t.shape), C, 0.95, version)
+    st, out = gpu_decompress_bytes(blob)
+    assert st == 0 and (out == raw).all()
+    nc = struct.unpack_from("<I", blob, 24)[0]
+    rng = np.random.default_rng(44)
+    for c in list(range(0, 20)) + [nc // 2, nc // 2 + 7, nc - 2, nc - 1]:
+        off, sm, _ = struct.unpack_from("<QII", blob, 96 + 16 * c)
+        bad = bytearray(blob)
+        bad[off + int(rng.integers(0, sm & 0x7FFFFFFF))] ^= 0x04
+        st, out = gpu_decompress_bytes(bytes(bad))
+        assert st & zc.ECRC, (c, st)
+        st, _ = gpu_decompress_bytes(bytes(bad), verify=False)
+        assert not st & zc.ECRC, (c, st)
+
+
 def test_corrupted_table_entry_device_checks():
     """A table entry pointing outside the blob is caught on the device even
     when the host check is bypassed (info taken from the good blob)."""
