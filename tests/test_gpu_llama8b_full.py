@@ -67,6 +67,7 @@ def test_llama8b_every_tensor_matches_oracle(zco, version, streams):
                 blob = torch.empty(zc.blob_size(src.numel(), wl.BF16, C, thr, flags), dtype=torch.uint8, device=DEV)
                 nb = torch.zeros(1, dtype=torch.int64, device=DEV)
                 st = torch.zeros(1, dtype=torch.int32, device=DEV)
+                workers[k].wait_stream(torch.cuda.current_stream())  # the inputs were made there
                 zc.compress_into(src, blob, nb, ws[k], st, C, thr, workers[k], dtype=wl.BF16, shape=tuple(shape),
                                  flags=flags)
                 group.append((k, name, shape, src, blob, nb, st))
