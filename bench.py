@@ -183,13 +183,14 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    from the current kernel sources."""
+def profiled_traffic(kernel: str, workload: str, version: int):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    workload and blob format, if it was taken from the current kernel
+    sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             d = json.load(fh)
-        e = d[f"{kernel}:{workload}"]
+        e = d[f"{kernel}:{workload}:v{version}"]
         if e.get("source_hash") == kernel_source_hash():
             return int(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
@@ -583,6 +584,11 @@ def run_model(a, world, rank, local, dev, stream):
     dec_ach = alg * a.steps / t_dec / 1e9
     chunks = [(x + C - 1) // C for x in sizes]
     dec_kernel = "decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel"
+    # the roofline of the phase that takes longer: compression (stats_kernel
+    # then code_kernel per call; code_kernel is most of its kernel time) or
+    # decompression (decode_kernel)
+    enc_dom = t_enc >= t_dec
+    dom_kernel, dom_ach = ("code_kernel", enc_ach) if enc_dom else (dec_kernel, dec_ach)
     if batched:
         table_launches = lambda words: (words + 7679) // 7680
         per_step = (encode_launches(chunks, Wd, C, bool(flags & zc.SHARED_TABLES)) + table_launches(38 * n)
@@ -605,12 +611,13 @@ def run_model(a, world, rank, local, dev, stream):
         "decode": {"gbs": round(N * a.steps / t_dec / 1e9, 2), "roofline_frac": round(dec_ach / hbm, 4),
                    "ms": round(1e3 * t_dec / a.steps, 4)},
         "size_pct": round(100.0 * S / N, 3),
-        "roofline": {"bound": "hbm", "kernel": dec_kernel, "achieved": round(dec_ach, 1), "peak": hbm,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
-                     "frac_of_nominal": round(dec_ach / NOMINAL_HBM_GBS, 4),
-                     "traffic": profiled_traffic(dec_kernel, a.workload),
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(dom_ach, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_ach / hbm, 4),
+                     "frac_of_nominal": round(dom_ach / NOMINAL_HBM_GBS, 4),
+                     "traffic": profiled_traffic(dom_kernel, a.workload, format_version(a)),
                      "algorithmic_bytes_per_launch": alg if batched else None,
-                     "note": "decompression time of the whole model (one decode_kernel launch when batched)"},
+                     "note": ("compression" if enc_dom else "decompression") + " phase of the whole model: its "
+                             "algorithmic bytes (original + blob) over its time"},
         "clocks": clk.summary(),
         "e2e": {"value": round(N * e2e_steps / t_hb / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": hb_h2d // e2e_steps, "d2h_bytes_per_step": hb_d2h // e2e_steps,
@@ -836,12 +843,13 @@ def main():
     alg = N + S + (N if base is not None else 0)
     enc_ach = alg * a.steps / t_enc / 1e9
     dec_ach = alg * a.steps / t_dec / 1e9
-    # the decompression call is one kernel (decode_kernel), the largest single
-    # kernel of the step; compression is two (statistics, coding), each
-    # shorter (profiles/launches_*.md), so the live roofline is decode's
-    dominant = "decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel"
-    ach = dec_ach
-    traffic = profiled_traffic(dominant, a.workload)
+    # the roofline of the call that takes longer: compression (stats_kernel
+    # then code_kernel; code_kernel is most of its time) or decompression
+    # (one decode_kernel launch)
+    enc_dom = t_enc >= t_dec
+    dominant = "code_kernel" if enc_dom else ("decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel")
+    ach = enc_ach if enc_dom else dec_ach
+    traffic = profiled_traffic(dominant, a.workload, format_version(a))
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
         "value": round(replica_value(N, a.steps, world, total) / 1e9, 3), "unit": "GB/s",

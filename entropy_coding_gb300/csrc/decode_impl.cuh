@@ -136,13 +136,21 @@ struct Rans {
 };
 
 // Lane lists (format v3): each lane keeps the 4 blocks of 8 words of its
-// list that hold its next words in shared memory, in its own 32 ring words
-// (block b at ring word 32 lane + 8 (b & 3), so word p of the list is ring
-// word 32 lane + (p & 31)), filled by asynchronous copies, so that no
-// register waits on a global load. A step reads its word with one shared
-// load whose address is known before the step starts.
+// list that hold its next words in shared memory, in its own 32 ring words,
+// filled by asynchronous copies, so that no register waits on a global
+// load. A step reads its word with one shared load whose address is known
+// before the step starts. Lanes 2r and 2r + 1 share the 128-byte row r of
+// the ring, one half each (swapped for r & 4), and word p of a lane's list
+// is word (p & 31) ^ 8 ((r & 3)) of its half: lanes that read the same word
+// of their lists (they start together and drift apart slowly) then meet 4
+// to a bank instead of 16, and each 16-byte block stays whole and aligned.
+__device__ __forceinline__ uint32_t lane_ring_base() {  // in words
+    const uint32_t l = threadIdx.x & 31u;
+    return 64u * (l >> 1) + 32u * ((l ^ (l >> 3)) & 1u);
+}
+__device__ __forceinline__ uint32_t lane_ring_xor() { return ((threadIdx.x >> 1) & 3u) << 3; }
 __device__ __forceinline__ uint16_t *lane_slot(uint16_t *ring, int32_t b) {
-    return ring + (threadIdx.x & 31u) * 32u + (uint32_t(b) & 3u) * 8u;
+    return ring + lane_ring_base() + ((8u * (uint32_t(b) & 3u)) ^ lane_ring_xor());
 }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
@@ -356,7 +364,7 @@ template <bool kBig>
 __device__ __forceinline__ uint32_t rans_step_lanes(Rans &r, bool active) {
     // this lane's next word, from its ring (a lane that has no word left
     // reads a slot it will not use)
-    const uint32_t w = r.ring[(threadIdx.x & 31u) * 32u + (uint32_t(r.ptr) & 31u)];
+    const uint32_t w = r.ring[lane_ring_base() + ((uint32_t(r.ptr) & 31u) ^ lane_ring_xor())];
     const uint32_t slot = r.x & (kM - 1);
     uint32_t s, xn;
     if constexpr (kBig) {
@@ -549,12 +557,13 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
                 // a group of 8 steps in which every lane has a symbol: the
                 // step reduced to its dependent chain (32-bit shared
                 // addresses; renormalisation by one byte permute)
-                const uint32_t ring_lane = smem_u32(rs.ring) + 64u * lane, big_base = smem_u32(rs.big);
+                const uint32_t ring_lane = smem_u32(rs.ring) + 2u * lane_ring_base(), big_base = smem_u32(rs.big);
+                const uint32_t rx = lane_ring_xor();
                 uint32_t x = rs.x;
                 int32_t ptr = rs.ptr;
 #pragma unroll
                 for (int s = 0; s < 8; s++) {
-                    const uint32_t w = lds_u16(ring_lane + ((uint32_t(ptr) & 31u) << 1));
+                    const uint32_t w = lds_u16(ring_lane + (((uint32_t(ptr) & 31u) ^ rx) << 1));
                     const uint32_t e = lds_u32(big_base + ((x & (kM - 1)) << 2));
                     const uint32_t xn = ((e >> 8) & 0xFFFu) * (x >> kProbBits) + (e >> 20);
                     const bool need = xn < kRansL;
