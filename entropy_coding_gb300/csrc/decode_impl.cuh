@@ -926,7 +926,6 @@ constexpr int warps_per_chunk() { return kBig ? 3 : 2; }
 template <int DT, bool kBig, bool kDelta, bool kLanes>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int W = WordOf<DT>::W;
     constexpr int C = kBig ? 8 : 16;
     uint32_t *crc_rep = reinterpret_cast<uint32_t *>(smem);
     uint32_t(*gshift)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + crc_rep_words<C>() * 4);

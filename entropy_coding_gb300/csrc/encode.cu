@@ -366,21 +366,24 @@ __device__ uint64_t lookback(unsigned long long *st, uint32_t c, uint64_t agg, i
 // ---------------------------------------------------------------- statistics
 
 // Shared memory of a statistics CTA. The histogram of stream j keeps one copy
-// per lane index: word (b >> 1) * 32 + lane holds the 16-bit counts of bins
-// b & ~1 (low half) and b | 1 (high half), so the 32 lanes of a warp always
-// add into 32 different banks. A copy sees at most about n / 32 counts of one
+// per lane index, so the 32 lanes of a warp always add into 32 different
+// banks. For W <= 2 word b * 32 + lane holds the 32-bit count of bin b (32 KB
+// per stream); for W = 4, where that would not leave room for two CTAs per
+// SM, word (b >> 1) * 32 + lane holds the 16-bit counts of bins b & ~1 (low
+// half) and b | 1 (high half): a copy sees at most about n / 32 counts of one
 // stream (each thread's pieces hold at most 1/512 of the chunk plus one
 // piece, 16 threads share a copy), far below 2^16.
 template <int W>
 struct StatsSmem {
-    uint32_t hist[W][128 * 32];
+    static constexpr int kWords = W <= 2 ? 256 : 128;  // counter words per stream and lane
+    uint32_t hist[W][kWords * 32];
     uint32_t cnt[W][256];            // merged counts
     uint32_t plane[W][256];          // v2: counts of this CTA's recent chunks of one tensor, per plane
 };
 
 // Count one element into the histograms; hrow = &h[0][lane]. For the byte b
-// of stream j at bit sh of the permuted word, the counter word is
-// (b >> 1) * 32 + lane of stream j and the half is b & 1.
+// of stream j at bit sh of the permuted word, the counter word is b * 32 +
+// lane of stream j (W <= 2), or (b >> 1) * 32 + lane with the half b & 1.
 template <int DT>
 __device__ __forceinline__ void count_elem(uint32_t w, uint32_t *hrow) {
     constexpr int W = WordOf<DT>::W;
@@ -388,9 +391,13 @@ __device__ __forceinline__ void count_elem(uint32_t w, uint32_t *hrow) {
 #pragma unroll
     for (int j = 0; j < W; j++) {
         const int sh = 8 * (W - 1 - j);
-        const uint32_t half = (p >> (sh + 1)) & 0x7Fu;
-        const uint32_t inc = (p & (1u << sh)) ? 0x10000u : 1u;
-        atomicAdd(hrow + j * (128 * 32) + half * 32, inc);
+        if constexpr (W <= 2) {
+            atomicAdd(hrow + j * (256 * 32) + ((p >> sh) & 0xFFu) * 32, 1u);
+        } else {
+            const uint32_t half = (p >> (sh + 1)) & 0x7Fu;
+            const uint32_t inc = (p & (1u << sh)) ? 0x10000u : 1u;
+            atomicAdd(hrow + j * (128 * 32) + half * 32, inc);
+        }
     }
 }
 
@@ -489,16 +496,22 @@ __device__ void chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<WordOf<D
 template <int W>
 __device__ void merge_counts(StatsSmem<W> &sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int K = StatsSmem<W>::kWords;
 #pragma unroll 4
-    for (int w = warp; w < W * 128; w += kStatWarps) {
-        uint32_t *cell = &sm.hist[w >> 7][(w & 127) * 32 + lane];
+    for (int w = warp; w < W * K; w += kStatWarps) {
+        uint32_t *cell = &sm.hist[w / K][(w % K) * 32 + lane];
         const uint32_t v = *cell;
         *cell = 0;
-        const uint32_t lo = __reduce_add_sync(kFull, v & 0xFFFFu);
-        const uint32_t hi = __reduce_add_sync(kFull, v >> 16);
-        if (lane == 0) {
-            sm.cnt[w >> 7][2 * (w & 127)] = lo;
-            sm.cnt[w >> 7][2 * (w & 127) + 1] = hi;
+        if constexpr (K == 256) {
+            const uint32_t c = __reduce_add_sync(kFull, v);
+            if (lane == 0) sm.cnt[w / K][w % K] = c;
+        } else {
+            const uint32_t lo = __reduce_add_sync(kFull, v & 0xFFFFu);
+            const uint32_t hi = __reduce_add_sync(kFull, v >> 16);
+            if (lane == 0) {
+                sm.cnt[w / K][2 * (w % K)] = lo;
+                sm.cnt[w / K][2 * (w % K) + 1] = hi;
+            }
         }
     }
 }
@@ -644,7 +657,7 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
     // the coding kernel's chunk ticket starts from zero in every wave (the
     // previous wave's coding kernel has finished: same stream)
     if (blockIdx.x == 0 && tid == 0) reinterpret_cast<uint32_t *>(a.ws_ctrl)[0] = 0;
-    for (int i = tid; i < W * 128 * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
+    for (int i = tid; i < W * StatsSmem<W>::kWords * 32; i += kStatThreads) (&sm.hist[0][0])[i] = 0;
     for (int i = tid; i < W * 256; i += kStatThreads) (&sm.plane[0][0])[i] = 0;
     // v2: warp j < W adds stream j's counts into sm.plane[j] for tensor cur_t
     // and moves them to the tensor's plane histogram in global memory when
