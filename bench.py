@@ -55,7 +55,8 @@ def _args():
                    help="blob format v2: one table per byte plane of each tensor (ZC_SHARED_TABLES)")
     p.add_argument("--streams", type=int, default=8,
                    help="llama8b: the per-tensor calls are issued round-robin on this many CUDA streams, each "
-                        "with its own workspace (1: one stream, every call after the previous one)")
+                        "with its own workspace, and packed into few SMs (ZC_PACKED) when there are several "
+                        "(1: one stream, every call after the previous one)")
     p.add_argument("--format", type=int, default=None, choices=[1, 2, 3],
                    help="blob format: 1 (a table and one word list per coded stream), 2 (shared plane "
                         "tables, as --shared-tables), 3 (a word list per rANS lane, ZC_LANE_WORDS; the "
@@ -439,6 +440,10 @@ def run_model(a, world, rank, local, dev, stream):
                 ev.record(w)
                 stream.wait_event(ev)
 
+    # calls on several streams pack their chunks into few SMs (ZC_PACKED), so
+    # that the calls in flight share the GPU instead of each spreading over it
+    packed = n_streams > 1
+
     def comp(inputs, blobs=blobs, nb=nb, one_call=batched):
         if one_call:
             zc.compress_batch_into(inputs, blobs, nb, ws_b, st, code, shapes, C, thr, stream, flags=flags)
@@ -447,7 +452,7 @@ def run_model(a, world, rank, local, dev, stream):
             for t in range(n):
                 k = t % n_streams
                 zc.compress_into(inputs[t], blobs[t], nb[t:t + 1], ws_1[k], st, C, thr, workers[k], dtype=code,
-                                 shape=shapes[t], flags=flags)
+                                 shape=shapes[t], flags=flags | (zc.PACKED if packed else 0))
             fan_in()
 
     def decomp(infos, blobs=blobs, one_call=batched):
@@ -456,7 +461,7 @@ def run_model(a, world, rank, local, dev, stream):
         else:
             fan_out()
             for t in range(n):
-                zc.decompress_into(blobs[t], infos[t], outs[t], st, verify, workers[t % n_streams])
+                zc.decompress_into(blobs[t], infos[t], outs[t], st, verify, workers[t % n_streams], packed=packed)
             fan_in()
 
     with torch.cuda.stream(stream):
@@ -602,7 +607,7 @@ def run_model(a, world, rank, local, dev, stream):
         "ms_per_step": round(1e3 * total / a.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": a.workload, "desc": MODEL_WORKLOADS[a.workload], "nbytes": N, "tensors": n,
-                   "streams": n_streams,
+                   "streams": n_streams, "packed_launches": packed,
                    "chunk_bytes": C, "threshold": thr, "verify_crc_on_decode": verify,
                    "format": FORMAT_NAMES[format_version(a)],
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},

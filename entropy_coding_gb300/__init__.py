@@ -24,12 +24,13 @@ __all__ = ["compress", "decompress", "crc32", "verify", "verify_into", "blob_inf
            "compress_into", "decompress_into", "compress_delta", "decompress_delta", "compress_delta_into",
            "decompress_delta_into", "compress_batch", "compress_batch_into", "decompress_batch",
            "decompress_batch_into", "workspace_size_batch", "decompress_workspace_size_batch", "ZcError", "lib", "SHARED_TABLES", "LANE_WORDS", "OK", "EINVAL", "EFORMAT",
-           "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY"]
+           "ECRC", "ECORRUPT", "ETIMEOUT", "ECAPACITY", "ECUDA", "NO_VERIFY", "PACKED"]
 
 OK, EINVAL, EFORMAT, ECRC, ECORRUPT, ETIMEOUT, ECAPACITY, ECUDA = 0, 1, 2, 4, 8, 16, 32, 64
 NO_VERIFY = 1
 SHARED_TABLES = 2  # compression flag: blob format v2 (shared plane tables)
 LANE_WORDS = 4     # compression flag: blob format v3 (a word list per rANS lane)
+PACKED = 8         # compression and decompression flag: pack the call's chunks into few SMs (calls on several streams)
 HOOK_LOOKBACK_STALL, HOOK_PRODUCER_STALL = 1, 2  # test hooks (zc_set_test_hooks)
 DEFAULT_CHUNK = 131072
 DEFAULT_THRESHOLD = 0.95
@@ -236,11 +237,12 @@ def read_info(blob: torch.Tensor) -> dict:
 
 
 def decompress_into(blob: torch.Tensor, info: dict, out: torch.Tensor, status: torch.Tensor,
-                    verify: bool = True, stream=None) -> None:
-    """Launch decompression into a caller buffer; no allocation, no sync."""
+                    verify: bool = True, stream=None, packed: bool = False) -> None:
+    """Launch decompression into a caller buffer; no allocation, no sync.
+    ``packed`` (ZC_PACKED) fills few SMs, for calls on several streams."""
+    flags = (0 if verify else NO_VERIFY) | (PACKED if packed else 0)
     st = lib().zc_decompress(blob.data_ptr(), ctypes.byref(_info_struct(info)), out.data_ptr(),
-                             out.numel() * out.element_size(), 0 if verify else NO_VERIFY,
-                             status.data_ptr(), _stream(stream))
+                             out.numel() * out.element_size(), flags, status.data_ptr(), _stream(stream))
     _check(st, "zc_decompress")
 
 

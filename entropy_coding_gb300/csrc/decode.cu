@@ -4,13 +4,14 @@
 
 namespace zc {
 
-uint32_t decode_v2_pairs(uint64_t total_chunks) {
+uint32_t decode_v2_pairs(uint64_t total_chunks, bool packed) {
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess || sms < 1)
         sms = 1;
     // one CTA per SM holds its chunks when they fit; else CTAs of kV2Pairs
-    const uint64_t per_sm = (total_chunks + uint64_t(sms) - 1) / uint64_t(sms);
+    // (ZC_PACKED: CTAs of kV2Pairs whatever the number of chunks)
+    const uint64_t per_sm = packed ? total_chunks : (total_chunks + uint64_t(sms) - 1) / uint64_t(sms);
     return uint32_t(std::max<uint64_t>(1, std::min<uint64_t>(kV2Pairs, per_sm)));
 }
 

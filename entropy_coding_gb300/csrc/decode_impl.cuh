@@ -1093,6 +1093,10 @@ int launch_decode_lt(const DecodeArgs &a, cudaStream_t s) {
     // the smaller two-level tables, up to kPairs chunks per CTA. Either way
     // the chunks spread evenly over the SMs.
     const uint64_t per_sm = (a.total_chunks + sms - 1) / uint64_t(sms);
+    // ZC_PACKED: CTAs of up to kPairs chunks, on as few SMs as they fill
+    if (a.flags & ZC_PACKED)
+        return launch_decode_mode<DT, false, kDelta, kLanes>(
+            a, uint32_t(std::max<uint64_t>(1, std::min<uint64_t>(kPairs, a.total_chunks))), s);
     if (per_sm <= kBigPairs)
         return launch_decode_mode<DT, true, kDelta, kLanes>(a, uint32_t(std::max<uint64_t>(per_sm, 1)), s);
     return launch_decode_mode<DT, false, kDelta, kLanes>(a, uint32_t(std::min<uint64_t>(kPairs, per_sm)), s);

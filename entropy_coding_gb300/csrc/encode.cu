@@ -1475,9 +1475,11 @@ int launch_wave_t(const EncodeArgs &a, cudaStream_t s) {
         if (st != ZC_OK) return st;
     }
     // the warps spread evenly over the SMs: CTAs of just enough warps for one
-    // CTA per SM (the block scheduler then gives every SM the same share)
+    // CTA per SM (the block scheduler then gives every SM the same share);
+    // ZC_PACKED: CTAs of up to kCodeWarps warps, on as few SMs as they fill
     const int sms = sms_of_device() < 1 ? 1 : sms_of_device();
-    const uint32_t wpc = std::min<uint32_t>(kCodeWarps, (a.workers + sms - 1) / sms);
+    const uint32_t wpc = a.packed ? std::min<uint32_t>(kCodeWarps, a.workers)
+                                  : std::min<uint32_t>(kCodeWarps, (a.workers + sms - 1) / sms);
     const int cgrid = int((a.workers + wpc - 1) / wpc);
     code_kernel<DT, kDelta><<<cgrid, 32 * wpc, kCodeCrcBytes + size_t(wpc) * kCodeWarpSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? ZC_OK : ZC_ECUDA;

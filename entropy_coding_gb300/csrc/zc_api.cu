@@ -487,9 +487,9 @@ int run_compress(EncodeArgs &a, const TensorDesc *table, uint32_t n, bool delta,
 
 // Blob format of a compression call's flags: 1 by default, 2 with shared
 // plane tables, 3 with a word list per lane; 0 for flags that are invalid
-// (unknown bits, or both formats at once).
+// (unknown bits, or both formats at once). ZC_PACKED changes no format.
 uint32_t version_of(uint32_t flags) {
-    if (flags & ~(ZC_SHARED_TABLES | ZC_LANE_WORDS)) return 0;
+    if (flags & ~(ZC_SHARED_TABLES | ZC_LANE_WORDS | ZC_PACKED)) return 0;
     if ((flags & ZC_SHARED_TABLES) && (flags & ZC_LANE_WORDS)) return 0;
     return (flags & ZC_SHARED_TABLES) ? 2u : (flags & ZC_LANE_WORDS) ? 3u : 1u;
 }
@@ -507,6 +507,7 @@ int compress_impl(const void *d_src, const void *d_base, uint64_t nbytes, int dt
     if (resolve_tensor(a.one) != ZC_OK) return ZC_EINVAL;
     a.total_chunks = a.one.n_chunks;
     a.d_status = d_status;
+    a.packed = (flags & ZC_PACKED) ? 1u : 0u;
     return run_compress(a, nullptr, 1, d_base != nullptr, dtype, chunk_bytes, threshold, version, d_ws, ws_bytes,
                         static_cast<cudaStream_t>(stream));
 }
@@ -537,7 +538,7 @@ int make_blob(const void *d_blob, const zc_info *info, const void *d_base, void 
 int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base, void *d_dst, uint64_t dst_capacity,
                     uint32_t flags, int32_t *d_status, void *stream) {
     if (!d_status) return ZC_EINVAL;
-    if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
+    if (flags & ~(ZC_NO_VERIFY | ZC_PACKED)) return ZC_EINVAL;
     DecodeArgs a{};
     const int st = make_blob(d_blob, info, d_base, d_dst, dst_capacity, a.one);
     if (st != ZC_OK) return st;
@@ -550,7 +551,7 @@ int decompress_impl(const void *d_blob, const zc_info *info, const void *d_base,
     a.version = info->version;
     set_waits(a);
     if (a.version == 2) {  // CTAs of a.pairs chunks
-        a.pairs = decode_v2_pairs(a.total_chunks);
+        a.pairs = decode_v2_pairs(a.total_chunks, (flags & ZC_PACKED) != 0);
         a.n_ctas = (a.total_chunks + a.pairs - 1) / a.pairs;
     }
     return launch_decode(info->dtype, d_base != nullptr, a, static_cast<cudaStream_t>(stream));
@@ -679,6 +680,7 @@ extern "C" int zc_compress_batch(uint32_t n, const void *const *d_srcs, const vo
     if (n == 1) a.one = table[0];
     a.total_chunks = uint32_t(nc);
     a.d_status = d_status;
+    a.packed = (flags & ZC_PACKED) ? 1u : 0u;
     return run_compress(a, table.data(), n, d_bases != nullptr, dtype, chunk_bytes, threshold, version, d_ws,
                         ws_bytes, static_cast<cudaStream_t>(stream));
 }
@@ -688,7 +690,7 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
                                    uint32_t flags, void *d_ws, uint64_t ws_bytes, int32_t *d_status, void *stream) {
     if (n == 0) return ZC_OK;
     if (!d_blobs || !infos || !d_dsts || !dst_capacities || !d_status) return ZC_EINVAL;
-    if (flags & ~ZC_NO_VERIFY) return ZC_EINVAL;
+    if (flags & ~(ZC_NO_VERIFY | ZC_PACKED)) return ZC_EINVAL;
     const int dtype = infos[0].dtype;
     const uint32_t chunk_bytes = infos[0].chunk_bytes, version = infos[0].version;
     if (d_bases && !delta_dtype(dtype)) return ZC_EINVAL;
@@ -715,7 +717,7 @@ extern "C" int zc_decompress_batch(uint32_t n, const void *const *d_blobs, const
     DecodeArgs a{};
     a.version = version;
     if (version == 2) {  // CTAs of a.pairs chunks of one blob each
-        a.pairs = decode_v2_pairs(nc);
+        a.pairs = decode_v2_pairs(nc, (flags & ZC_PACKED) != 0);
         uint64_t ctas = 0;
         for (auto &d : table) {
             d.cta_base = uint32_t(ctas);

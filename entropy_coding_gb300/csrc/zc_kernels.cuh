@@ -47,6 +47,7 @@ struct EncodeArgs {
     uint8_t *ws_ptab;               // v2: per tensor and plane, the 12-bit table (256 u16)
     uint32_t hooks;                 // test hooks (zc_set_test_hooks)
     uint32_t spin_limit;            // polls of one look-back wait before it gives up
+    uint32_t packed;                // ZC_PACKED: coding CTAs of up to 16 warps, filling few SMs
 };
 
 // One blob of a decompression call.
@@ -110,7 +111,7 @@ int launch_empty_blobs(const EncodeArgs &a, cudaStream_t s);
 // v2: the plane tables of the wave's tensors (after its statistics kernel).
 int launch_plane_tables(int dtype, const EncodeArgs &a, cudaStream_t s);
 // v2 decoding: CTAs of `pairs` chunks each, never spanning two blobs.
-uint32_t decode_v2_pairs(uint64_t total_chunks);
+uint32_t decode_v2_pairs(uint64_t total_chunks, bool packed);
 
 // The tensor (blob) of a call-wide chunk index: the last one whose first
 // chunk is at or before it (binary search over the table).

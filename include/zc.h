@@ -88,6 +88,14 @@ enum zc_status {
  * every coded record; lmzip "On a GPU": the decoder is bound by the lanes'
  * dependent chains). Not combinable with ZC_SHARED_TABLES. */
 #define ZC_LANE_WORDS 4u
+/* flag of the compression and decompression calls (the pages have no
+ * counterpart; a launch-shape choice that changes no byte of any blob): pack
+ * the call's chunks into as few SMs as they fill, up to 16 coding warps or 16
+ * decoding warp pairs per SM, instead of spreading them over every SM. Meant
+ * for calls issued on several streams at once (one call per tensor of a
+ * model): the SMs a call leaves free run the other streams' calls, and every
+ * SM holds more rANS chains. A call alone on the GPU is faster without it. */
+#define ZC_PACKED 8u
 
 /* Parameter limits of format v1. */
 #define ZC_MIN_CHUNK 64u
@@ -169,7 +177,8 @@ ZC_API int zc_compress(const void *d_src, uint64_t nbytes, int dtype, int ndim, 
  *   d_blob       the blob (info->blob_bytes bytes)
  *   d_dst        output, dst_capacity >= info->nbytes, aligned to the
  *                element size
- *   flags        0 or ZC_NO_VERIFY (skip the per-chunk CRC check)
+ *   flags        0, or ZC_NO_VERIFY (skip the per-chunk CRC check) and/or
+ *                ZC_PACKED (the launch shape for calls on several streams)
  *   d_status     device int32, OR-ed with ZC_ECRC / ZC_ECORRUPT / ZC_EFORMAT
  * With the check, each chunk's CRC-32 is taken over its stored bytes in the
  * same pass that reads them for decoding, and compared at the end of the
@@ -229,7 +238,8 @@ ZC_API int zc_decompress_delta(const void *d_blob, const zc_info *info, const vo
  *   d_blobs[t], blob_capacities[t]
  *                      blob t (16-byte aligned) and its capacity, as in
  *                      zc_compress
- *   flags              0 (format v1) or ZC_SHARED_TABLES (format v2, below)
+ *   flags              0 (format v1), ZC_SHARED_TABLES (format v2, below) or
+ *                      ZC_LANE_WORDS (format v3), each with ZC_PACKED or not
  *   d_blob_bytes       DEVICE array of n uint64: entry t receives blob t's size
  *   d_ws, ws_bytes     ws_bytes >= zc_workspace_size_batch(nbytes, n, ...)
  *   d_status           one device int32 for the whole call
@@ -278,7 +288,9 @@ ZC_API uint64_t zc_decompress_workspace_size_batch(uint32_t n);
  * zc_decompress_batch read both versions (zc_info.version); a batch must
  * not mix them. The decoder builds each plane's one-level table once per
  * CTA and shares it among the CTA's chunks.
- *   zc_compress_ex        zc_compress with flags (0 or ZC_SHARED_TABLES)
+ *   zc_compress_ex        zc_compress with flags: 0, ZC_SHARED_TABLES or
+ *                         ZC_LANE_WORDS (the format), each with ZC_PACKED
+ *                         or not (the launch shape)
  *   zc_workspace_size_ex  its workspace (v2 holds a whole tensor's
  *                         statistics in one wave)
  *   zc_blob_size_ex       worst-case blob bytes (v2 adds 512 W) */

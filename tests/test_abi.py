@@ -123,8 +123,9 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
                                    vp2(aligned, aligned), u64_2(1 << 16, 1 << 16), aligned, aligned, 1 << 24,
                                    aligned, None)
     assert comp(0, None, None, None, zc.BF16) == zc.OK
-    assert comp(0, None, None, None, zc.BF16, flags=8) == zc.EINVAL   # unknown flag
+    assert comp(0, None, None, None, zc.BF16, flags=16) == zc.EINVAL  # unknown flag
     assert comp(0, None, None, None, zc.BF16, flags=6) == zc.EINVAL   # two formats at once
+    assert comp(0, None, None, None, zc.BF16, flags=zc.PACKED | zc.LANE_WORDS) == zc.OK
     assert comp(2, None, None, u64_2(2048, 2048), zc.BF16) == zc.EINVAL
     # deltas only for unsigned word dtypes
     assert comp(2, vp2(aligned, aligned), vp2(aligned, aligned), u64_2(2048, 2048), zc.BF16) == zc.EINVAL
@@ -158,3 +159,24 @@ def test_batch_entry_points_reject_bad_arguments_on_the_host():
     assert zc.workspace_size_batch([2048, 0], zc.BF16, 4096, zc.SHARED_TABLES) > 0
     assert zc.blob_size(2048, zc.BF16, 4096, 0.95, zc.SHARED_TABLES) == zc.blob_size(2048, zc.BF16, 4096) + 1024
     assert zc.workspace_size_batch([2048, 0], zc.BF16, 4096) > 0
+
+
+def test_packed_flag_is_a_launch_choice_on_the_host():
+    """ZC_PACKED combines with every format and with ZC_NO_VERIFY and sizes
+    nothing differently; unknown bits are refused before any launch (the
+    device pointers below are never dereferenced)."""
+    import ctypes
+    import entropy_coding_gb300 as zc
+    L = zc.lib()
+    for fmt in (0, zc.SHARED_TABLES, zc.LANE_WORDS):
+        for nb in (0, 1000, 1 << 20):
+            assert L.zc_blob_size_ex(nb, zc.BF16, 4096, 0.95, fmt | zc.PACKED) == L.zc_blob_size_ex(
+                nb, zc.BF16, 4096, 0.95, fmt)
+            assert L.zc_workspace_size_ex(nb, zc.BF16, 4096, fmt | zc.PACKED) == L.zc_workspace_size_ex(
+                nb, zc.BF16, 4096, fmt)
+    assert L.zc_blob_size_ex(1000, zc.BF16, 4096, 0.95, 16) == 0
+    aligned = 0x10000
+    info = zc._info_struct({"version": 1, "dtype": zc.BF16, "ndim": 1, "shape": [512], "nbytes": 1024,
+                            "chunk_bytes": 4096, "n_chunks": 1, "blob_bytes": 4096})
+    assert L.zc_decompress(aligned, ctypes.byref(info), aligned, 2048, 16, aligned, None) == zc.EINVAL
+    assert L.zc_decompress(aligned, ctypes.byref(info), aligned, 2048, 32 | zc.PACKED, aligned, None) == zc.EINVAL

@@ -34,10 +34,12 @@ DEV = torch.device("cuda:0")
 def test_llama8b_every_tensor_matches_oracle(zco, version, streams):
     """Format v1 one call after another, and format v3 (a word list per lane)
     with the calls issued round-robin on 8 streams, each with its own
-    workspace: the launch configuration the benchmark times."""
+    workspace and packed into few SMs (ZC_PACKED): the launch configuration
+    the benchmark times."""
     from oracle.parallel import blob_digest
 
     flags = {1: 0, 3: zc.LANE_WORDS}[version]
+    packed = streams > 1
     C, thr = 131072, 0.95
     specs = wl.llama8b_specs()
     order = [0, len(specs) - 1] + list(range(1, len(specs) - 1))
@@ -69,7 +71,7 @@ def test_llama8b_every_tensor_matches_oracle(zco, version, streams):
                 st = torch.zeros(1, dtype=torch.int32, device=DEV)
                 workers[k].wait_stream(torch.cuda.current_stream())  # the inputs were made there
                 zc.compress_into(src, blob, nb, ws[k], st, C, thr, workers[k], dtype=wl.BF16, shape=tuple(shape),
-                                 flags=flags)
+                                 flags=flags | (zc.PACKED if packed else 0))
                 group.append((k, name, shape, src, blob, nb, st))
             torch.cuda.synchronize()
             outs = []
@@ -77,7 +79,7 @@ def test_llama8b_every_tensor_matches_oracle(zco, version, streams):
                 assert int(st.item()) == 0, name
                 b = blob[: int(nb.item())]
                 out = torch.empty_like(src)
-                zc.decompress_into(b, zc.read_info(b), out, st, True, workers[k])
+                zc.decompress_into(b, zc.read_info(b), out, st, True, workers[k], packed=packed)
                 outs.append((name, shape, src, b, out, st))
             torch.cuda.synchronize()
             for name, shape, src, b, out, st in outs:
