@@ -57,6 +57,9 @@ def _args():
                    help="llama8b: the per-tensor calls are issued round-robin on this many CUDA streams, each "
                         "with its own workspace, and packed into few SMs (ZC_PACKED) when there are several "
                         "(1: one stream, every call after the previous one)")
+    p.add_argument("--packed", action="store_true",
+                   help="single-tensor workloads: pack each call into few SMs (ZC_PACKED), the launch shape the "
+                        "model's calls on several streams use")
     p.add_argument("--format", type=int, default=None, choices=[1, 2, 3],
                    help="blob format: 1 (a table and one word list per coded stream), 2 (shared plane "
                         "tables, as --shared-tables), 3 (a word list per rANS lane, ZC_LANE_WORDS; the "
@@ -681,7 +684,7 @@ def main():
         base, src = wl.as_bytes(ta), wl.as_bytes(tb)
     N = src.numel()
     C, thr = a.chunk_bytes, a.threshold
-    flags = format_flags(a, zc)
+    flags = format_flags(a, zc) | (zc.PACKED if a.packed else 0)
     planes = 512 * (N // max(1, t.numel())) if flags & zc.SHARED_TABLES else 0  # v2: the plane tables follow the chunk table
     cap = zc.blob_size(N, code, C, thr, flags)
     blob = torch.empty(cap, dtype=torch.uint8, device=dev)
@@ -694,14 +697,14 @@ def main():
     def comp(inp, blob=blob, nb=nb):
         if base is None:
             zc.compress_into(inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape, flags=flags)
-        elif flags:  # a v2 delta goes through the batched entry point (a batch of one)
+        elif flags & ~zc.PACKED:  # a v2 or v3 delta goes through the batched entry point (a batch of one)
             zc.compress_batch_into([inp], [blob], nb, ws, st, code, [shape], C, thr, stream, bases=[base], flags=flags)
         else:
             zc.compress_delta_into(base, inp, blob, nb, ws, st, C, thr, stream, dtype=code, shape=shape)
 
     def decomp(info, blob=blob, out=out):
         if base is None:
-            zc.decompress_into(blob, info, out, st, not a.no_verify, stream)
+            zc.decompress_into(blob, info, out, st, not a.no_verify, stream, packed=a.packed)
         else:
             zc.decompress_delta_into(blob, info, base, out, st, not a.no_verify, stream)
 
@@ -865,7 +868,7 @@ def main():
                    "verify_crc_on_decode": not a.no_verify,
                    "l2": "512 MiB written before each compression and decompression (not timed)" if flush_l2
                    else "inputs larger than L2 (no flush)",
-                   "format": FORMAT_NAMES[format_version(a)],
+                   "format": FORMAT_NAMES[format_version(a)], "packed_launches": a.packed,
                    "parallelism": f"replicas x{world}"},
         "encode": {"gbs": round(enc_gbs, 2), "roofline_frac": round(enc_ach / hbm, 4),
                    "ms": round(1e3 * t_enc / a.steps, 4)},

@@ -163,6 +163,11 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
 
 // Request this lane's blocks down to `lowest` (none below block 0) and
 // commit them as one group.
@@ -577,6 +582,33 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
                 continue;
             }
         }
+        if constexpr (kLanes && !kBig && !kV2) {
+            if (8 * g + 8 <= cx.n / 32) {
+                // the same with the two-level table: slot -> symbol, then
+                // symbol -> f | cum << 12
+                const uint32_t ring_lane = smem_u32(rs.ring) + 2u * lane_ring_base();
+                const uint32_t lut_base = smem_u32(rs.lut), sym_base = smem_u32(rs.sym);
+                const uint32_t rx = lane_ring_xor();
+                uint32_t x = rs.x;
+                int32_t ptr = rs.ptr;
+#pragma unroll
+                for (int s = 0; s < 8; s++) {
+                    const uint32_t w = lds_u16(ring_lane + (((uint32_t(ptr) & 31u) ^ rx) << 1));
+                    const uint32_t slot = x & (kM - 1);
+                    const uint32_t sy = lds_u8(lut_base + slot);
+                    const uint32_t e = lds_u32(sym_base + (sy << 2));
+                    const uint32_t xn = (e & 0xFFFu) * (x >> kProbBits) + slot - (e >> 12);
+                    const bool need = xn < kRansL;
+                    x = need ? __byte_perm(w, xn, 0x5410) : xn;
+                    ptr -= need ? 1 : 0;
+                    st[32 * s + lane] = uint8_t(sy);
+                }
+                rs.x = x;
+                rs.ptr = ptr;
+                mbar_arrive(&ps.full[k]);
+                continue;
+            }
+        }
 #pragma unroll
         for (int s = 0; s < 8; s++) {
             const uint32_t t = 8 * g + s;
@@ -597,7 +629,9 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
 // (linearity); the lanes are folded at the end (crc_fold) and the stream's
 // bytes after its last whole group (and its padding) are added from the
 // blob. The directory and the coded records are taken from the blob at the
-// end, and the parts are appended in payload order.
+// end, and the parts are appended in payload order. (Taking each lane's CRC
+// over a contiguous slice of the stream instead needs no shift, but its
+// loads, 32 lines per instruction, cost more than the shift saves.)
 template <int DT, bool kVerify, bool kDelta, int C, class PS>
 __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
                         const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
