@@ -728,8 +728,8 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
 // dependency chain.
 //
 // kLanes (format v3, a word list per lane): no lane depends on another, so
-// a step appends its word to the lane's 16-byte block in registers at once,
-// without a branch, and each full block (8 words) goes to the lane's own
+// a step appends its word to the lane's 8-byte block in registers at once,
+// without a branch, and each full block (4 words) goes to the lane's own
 // list; lane l's list is staged at a stride of pad8(T) words after the 32
 // counts (the record's size counts each list padded to 8 words), and
 // warp_copy_crc_lanes gathers the lists into place in the blob.
@@ -789,32 +789,27 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     }
 
     // v3: the lists follow the 32 counts; lane l stages its words at
-    // lists_at + 2 l Ts, Ts = pad8(T), in 16-byte blocks collected in acc
+    // lists_at + 2 l Ts, Ts = pad8(T), in 8-byte blocks collected in acc
     const uint32_t lists_at = words_at + 64;
     const uint32_t Ts = (uint32_t(T) + 7) & ~7u;
     uint16_t *wout = reinterpret_cast<uint16_t *>(rec + (kLanes ? lists_at : words_at));
-    uint4 *lw4 = reinterpret_cast<uint4 *>(wout + uint32_t(lane) * Ts);
-    uint4 acc = make_uint4(0, 0, 0, 0);
+    uint2 *lw2 = reinterpret_cast<uint2 *>(wout + uint32_t(lane) * Ts);
+    uint2 acc = make_uint2(0, 0);
     // append a word to the lane's block (words in emission order, the first
-    // at the lowest address); a full block goes to the lane's list
+    // at the lowest address); a full block (4 words) goes to the lane's list
     auto push = [&](uint32_t w, uint32_t &count) {
         acc.x = __funnelshift_r(acc.x, acc.y, 16);
-        acc.y = __funnelshift_r(acc.y, acc.z, 16);
-        acc.z = __funnelshift_r(acc.z, acc.w, 16);
-        acc.w = (acc.w >> 16) | (w << 16);
-        if ((++count & 7u) == 0) lw4[(count >> 3) - 1] = acc;
+        acc.y = (acc.y >> 16) | (w << 16);
+        if ((++count & 3u) == 0) lw2[(count >> 2) - 1] = acc;
     };
     // the same for a lane that may or may not emit, without a branch on em
     // (the shifted block is selected; only a full block's store branches)
     auto push_if = [&](bool em, uint32_t w, uint32_t &count) {
-        const uint4 sh = make_uint4(__funnelshift_r(acc.x, acc.y, 16), __funnelshift_r(acc.y, acc.z, 16),
-                                    __funnelshift_r(acc.z, acc.w, 16), (acc.w >> 16) | (w << 16));
+        const uint2 sh = make_uint2(__funnelshift_r(acc.x, acc.y, 16), (acc.y >> 16) | (w << 16));
         acc.x = em ? sh.x : acc.x;
         acc.y = em ? sh.y : acc.y;
-        acc.z = em ? sh.z : acc.z;
-        acc.w = em ? sh.w : acc.w;
         count += em ? 1u : 0u;
-        if (em && (count & 7u) == 0) lw4[(count >> 3) - 1] = acc;
+        if (em && (count & 3u) == 0) lw2[(count >> 2) - 1] = acc;
     };
     const uint32_t gt = lanemask_gt();
     uint32_t x = kRansL;
@@ -958,8 +953,8 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     reinterpret_cast<uint32_t *>(rec)[lane] = x;
     uint32_t rec_bytes = words_at + 2 * wc;
     if constexpr (kLanes) {
-        // the lane's last, partial block: zero words pushed in behind its
-        // words move them to the bottom
+        // the lane's last, partial blocks: zero words pushed in behind its
+        // words move them to the bottom, up to a whole 8 words
         if (wc & 7u) {
             uint32_t c = wc;
             while (c & 7u) push(0u, c);
