@@ -187,14 +187,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str, version: int):
-    """DRAM bytes per launch from the committed ncu summary of this kernel,
-    workload and blob format, if it was taken from the current kernel
-    sources."""
+def profiled_traffic(kernel: str, workload: str, version: int, packed: bool):
+    """DRAM bytes of the timed unit (one call; for the model, one phase) from
+    the committed ncu summaries of this kernel, workload, blob format and
+    launch shape, if they were taken from the current kernel sources. For
+    code_kernel the unit is the compression call (stats_kernel too)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             d = json.load(fh)
-        e = d[f"{kernel}:{workload}:v{version}"]
+        e = d[f"{kernel}:{workload}:v{version}" + (":packed" if packed else "")]
         if e.get("source_hash") == kernel_source_hash():
             return int(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
@@ -622,7 +623,7 @@ def run_model(a, world, rank, local, dev, stream):
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(dom_ach, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_ach / hbm, 4),
                      "frac_of_nominal": round(dom_ach / NOMINAL_HBM_GBS, 4),
-                     "traffic": profiled_traffic(dom_kernel, a.workload, format_version(a)),
+                     "traffic": profiled_traffic(dom_kernel, a.workload, format_version(a), packed),
                      "algorithmic_bytes_per_launch": alg if batched else None,
                      "note": ("compression" if enc_dom else "decompression") + " phase of the whole model: its "
                              "algorithmic bytes (original + blob) over its time"},
@@ -857,7 +858,7 @@ def main():
     enc_dom = t_enc >= t_dec
     dominant = "code_kernel" if enc_dom else ("decode_v2_kernel" if flags & zc.SHARED_TABLES else "decode_kernel")
     ach = enc_ach if enc_dom else dec_ach
-    traffic = profiled_traffic(dominant, a.workload, format_version(a))
+    traffic = profiled_traffic(dominant, a.workload, format_version(a), a.packed)
     line = {
         "metric": "round-trip GB/s (original bytes; encode + decode)",
         "value": round(replica_value(N, a.steps, world, total) / 1e9, 3), "unit": "GB/s",
