@@ -412,6 +412,26 @@ __device__ __forceinline__ void count_vec(const uint4 &q, uint32_t *hrow) {
             count_elem<DT>(W == 4 ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u), hrow);
 }
 
+// 2-byte words: count the 8 elements of a 16-byte vector and return the
+// bytes of stream 0 (the top byte of each permuted element) in o[0..1], in
+// element order; the permutation runs on two elements per register.
+template <int DT>
+__device__ __forceinline__ void count_vec2(const uint4 &q, uint32_t *hrow, uint32_t o[2]) {
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        p[k] = Perm<DT>::fwd2(u[k]);
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            atomicAdd(hrow + ((p[k] >> (16 * e + 8)) & 0xFFu) * 32, 1u);              // stream 0
+            atomicAdd(hrow + 256 * 32 + ((p[k] >> (16 * e)) & 0xFFu) * 32, 1u);        // stream 1
+        }
+    }
+    o[0] = __byte_perm(p[0], p[1], 0x7531);
+    o[1] = __byte_perm(p[2], p[3], 0x7531);
+}
+
 // Bytes of stream 0 (the top byte of each permuted element) of a 16-byte
 // vector: 16 / W of them, in element order, in the low bytes of o.
 template <int DT>
@@ -463,14 +483,19 @@ __device__ void chunk_stats(Source<kDelta> src, uint32_t len, StatsSmem<WordOf<D
         for (; pidx < pieces; pidx += kStatThreads) {
             const uint4 q0 = n0, q1 = n1;
             if (pidx + kStatThreads < pieces) load_piece(pidx + kStatThreads, n0, n1);
-            count_vec<DT>(q0, hrow);
-            count_vec<DT>(q1, hrow);
             // stream 0's bytes of the piece, for the coder in case the
             // stream is a candidate
             uint8_t *d = cand0 + uint64_t(pidx) * (kPiece / W);
             uint32_t o0[4], o1[4];
-            stream0_bytes<DT>(q0, o0);
-            stream0_bytes<DT>(q1, o1);
+            if constexpr (W == 2) {
+                count_vec2<DT>(q0, hrow, o0);
+                count_vec2<DT>(q1, hrow, o1);
+            } else {
+                count_vec<DT>(q0, hrow);
+                count_vec<DT>(q1, hrow);
+                stream0_bytes<DT>(q0, o0);
+                stream0_bytes<DT>(q1, o1);
+            }
             if constexpr (W == 4) {
                 *reinterpret_cast<uint2 *>(d) = make_uint2(o0[0], o1[0]);
             } else if constexpr (W == 2) {
@@ -1043,38 +1068,62 @@ __device__ void warp_raw_streams(Source<kDelta> src, uint32_t n, const uint32_t 
             }
             if (gs < 0) continue;  // first round only
             const uint32_t g = uint32_t(gs);
-            uint32_t wd[16];
+            // the 16 elements permuted: W = 2 two to a register (wd[k] holds
+            // elements 2k and 2k + 1), else one to a register
+            constexpr int NR = W == 2 ? 8 : 16;
+            uint32_t wd[NR];
             if (vec && 16 * (g + 1) <= n) {
 #pragma unroll
                 for (int v = 0; v < W; v++) {
                     const uint32_t u[4] = {qv[gi][v].x, qv[gi][v].y, qv[gi][v].z, qv[gi][v].w};
 #pragma unroll
-                    for (int k = 0; k < 4; k++)
+                    for (int k = 0; k < 4; k++) {
+                        if constexpr (W == 2) {
+                            wd[4 * v + k] = u[k];
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 4 / W; e++)
-                            wd[(v * 4 + k) * (4 / W) + e] =
-                                (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+                            for (int e = 0; e < 4 / W; e++)
+                                wd[(v * 4 + k) * (4 / W) + e] =
+                                    (W == 4) ? u[k] : (u[k] >> (8 * W * e)) & ((1u << (8 * W)) - 1u);
+                        }
+                    }
                 }
             } else {
 #pragma unroll
                 for (int k = 0; k < 16; k++) {
                     const uint32_t i = g * 16 + k;
-                    wd[k] = i < n ? src.template word<W>(i) : 0u;
+                    const uint32_t w = i < n ? src.template word<W>(i) : 0u;
+                    if constexpr (W == 2) {
+                        if (k & 1) wd[k >> 1] |= w << 16;
+                        else wd[k >> 1] = w;
+                    } else {
+                        wd[k] = w;
+                    }
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 16; k++) wd[k] = Perm<DT>::fwd(wd[k]);
+            for (int k = 0; k < NR; k++) {
+                if constexpr (W == 2) wd[k] = Perm<DT>::fwd2(wd[k]);
+                else wd[k] = Perm<DT>::fwd(wd[k]);
+            }
 #pragma unroll
             for (int j = 0; j < W; j++) {
                 if (mode[j] != kModeRaw) continue;
                 const uint32_t bj = uint32_t(W - 1 - j);        // byte of stream j in a permuted element
-                const uint32_t sel = bj | (4 + bj) << 4;         // [x.bj, y.bj, -, -]
                 uint32_t o[4];
+                if constexpr (W == 2) {
+                    // [e0.bj, e1.bj, e2.bj, e3.bj] from two registers of two elements
+                    const uint32_t sel = bj | (2 + bj) << 4 | (4 + bj) << 8 | (6 + bj) << 12;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const uint32_t lo = __byte_perm(wd[4 * q], wd[4 * q + 1], sel);
-                    const uint32_t hi = __byte_perm(wd[4 * q + 2], wd[4 * q + 3], sel);
-                    o[q] = __byte_perm(lo, hi, 0x5410);
+                    for (int q = 0; q < 4; q++) o[q] = __byte_perm(wd[2 * q], wd[2 * q + 1], sel);
+                } else {
+                    const uint32_t sel = bj | (4 + bj) << 4;         // [x.bj, y.bj, -, -]
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint32_t lo = __byte_perm(wd[4 * q], wd[4 * q + 1], sel);
+                        const uint32_t hi = __byte_perm(wd[4 * q + 2], wd[4 * q + 3], sel);
+                        o[q] = __byte_perm(lo, hi, 0x5410);
+                    }
                 }
                 // elements past n contribute zero bytes
                 if (16 * (g + 1) > n) {

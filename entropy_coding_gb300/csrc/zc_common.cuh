@@ -47,20 +47,23 @@ __host__ __device__ inline uint64_t max_grouped(uint64_t len, int W, uint32_t ve
 // grouping (Method 2) then takes byte j from the most significant end as
 // stream j. Integer dtypes are grouped without the permutation.
 template <int DT> struct Perm;
-// inv2 applies inv to two 16-bit words packed in one 32-bit register.
+// fwd2 and inv2 apply fwd and inv to two 16-bit words packed in one 32-bit
+// register.
 template <> struct Perm<ZC_U8>  { static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return w; } static __device__ __forceinline__ uint32_t inv(uint32_t p) { return p; } };
-template <> struct Perm<ZC_U16> { static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return w; } static __device__ __forceinline__ uint32_t inv(uint32_t p) { return p; } static __device__ __forceinline__ uint32_t inv2(uint32_t v) { return v; } };
+template <> struct Perm<ZC_U16> { static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return w; } static __device__ __forceinline__ uint32_t inv(uint32_t p) { return p; } static __device__ __forceinline__ uint32_t fwd2(uint32_t v) { return v; } static __device__ __forceinline__ uint32_t inv2(uint32_t v) { return v; } };
 template <> struct Perm<ZC_U32> { static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return w; } static __device__ __forceinline__ uint32_t inv(uint32_t p) { return p; } };
 // BF16: s e8 m7 -> e8 s m7
 template <> struct Perm<ZC_BF16> {
     static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return ((w << 1) & 0xFF00u) | ((w >> 8) & 0x80u) | (w & 0x7Fu); }
     static __device__ __forceinline__ uint32_t inv(uint32_t p) { return ((p & 0x80u) << 8) | ((p >> 1) & 0x7F80u) | (p & 0x7Fu); }
+    static __device__ __forceinline__ uint32_t fwd2(uint32_t v) { return ((v << 1) & 0xFF00FF00u) | ((v >> 8) & 0x00800080u) | (v & 0x007F007Fu); }
     static __device__ __forceinline__ uint32_t inv2(uint32_t v) { return ((v & 0x00800080u) << 8) | ((v >> 1) & 0x7F807F80u) | (v & 0x007F007Fu); }
 };
 // FP16: s e5 m10 -> e5 s m10
 template <> struct Perm<ZC_FP16> {
     static __device__ __forceinline__ uint32_t fwd(uint32_t w) { return ((w << 1) & 0xF800u) | ((w >> 5) & 0x400u) | (w & 0x3FFu); }
     static __device__ __forceinline__ uint32_t inv(uint32_t p) { return ((p & 0x400u) << 5) | ((p >> 1) & 0x7C00u) | (p & 0x3FFu); }
+    static __device__ __forceinline__ uint32_t fwd2(uint32_t v) { return ((v << 1) & 0xF800F800u) | ((v >> 5) & 0x04000400u) | (v & 0x03FF03FFu); }
     static __device__ __forceinline__ uint32_t inv2(uint32_t v) { return ((v & 0x04000400u) << 5) | ((v >> 1) & 0x7C007C00u) | (v & 0x03FF03FFu); }
 };
 // FP32: s e8 m23 -> e8 s m23
