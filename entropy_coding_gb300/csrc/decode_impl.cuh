@@ -622,20 +622,29 @@ __device__ void produce(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, const u
 }
 
 // Consumer warp: the chunk's output and the CRC of its stored bytes. For a
-// raw stream the lane register follows the lane's 8-byte pieces: group g of
-// the stream is its bytes [256 g, 256 g + 256) and lane l reads bytes 8 l ..
-// 8 l + 7 of it, so after group g the register is shift(register after
-// g - 1, 256 bytes) XOR the register of the new piece taken from zero
-// (linearity); the lanes are folded at the end (crc_fold) and the stream's
-// bytes after its last whole group (and its padding) are added from the
-// blob. The directory and the coded records are taken from the blob at the
+// raw stream the lane register follows the lane's pieces: with 4-byte words
+// group g of the stream is its bytes [256 g, 256 g + 256) and lane l takes
+// bytes 8 l .. 8 l + 7 of it (the bytes it reads for the output), so after
+// group g the register is shift(register after g - 1, 256 bytes) XOR the
+// register of the new piece taken from zero (linearity); with words of up to
+// 2 bytes the lane takes bytes 32 l .. 32 l + 31 of every 4 groups (1024
+// bytes), read again, coalesced, two groups before they are used: fewer
+// lookups per byte (one shift per 32 bytes instead of per 8). The lanes are
+// folded at the end (crc_fold) and the stream's bytes after its last whole
+// piece round (and its padding) are added from the blob. The directory and the coded records are taken from the blob at the
 // end, and the parts are appended in payload order. (Taking each lane's CRC
 // over a contiguous slice of the stream instead needs no shift, but its
 // loads, 32 lines per instruction, cost more than the shift saves.)
+// The consumer's shift table (gshift): the stride of a lane's raw-stream
+// pieces, 1024 bytes for words of up to 2 bytes, else 256.
+template <int W>
+constexpr int consume_shift_table() { return kShPow + (W <= 2 ? 10 : 8); }
+
 template <int DT, bool kVerify, bool kDelta, int C, class PS>
 __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_t expect_crc,
                         const uint32_t *crc_rep, const uint32_t (*gshift)[256], const uint32_t (*gap496)[256]) {
     constexpr int W = WordOf<DT>::W;
+    constexpr bool kBlk = W <= 2;  // 32-byte pieces every 4 groups
     const int lane = threadIdx.x & 31;
     const uint32_t *row = crc_row<C>(crc_rep);
     const uint32_t groups = cx.groups;
@@ -654,8 +663,13 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
         }
     }
     uint32_t Rraw[W];  // CRC registers of the raw streams (kVerify)
+    uint4 cb0[W], cb1[W];  // kBlk: the lane's next 32-byte piece of each raw stream
+    const uint32_t blocks = kBlk ? groups / 4 : 0;
 #pragma unroll
-    for (int j = 0; j < W; j++) Rraw[j] = 0;
+    for (int j = 0; j < W; j++) {
+        Rraw[j] = 0;
+        cb0[j] = cb1[j] = make_uint4(0, 0, 0, 0);
+    }
     // The raw streams are read 8 bytes per lane and group, two groups ahead,
     // too few bytes in flight to cover a DRAM access: their lines are
     // prefetched into L2 kAhead groups ahead (a group of a stream is 256
@@ -705,7 +719,19 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             rn1[j] = rn2[j];
             if (cx.kind[j] == kKRaw && g + 2 < groups)
                 rn2[j] = __ldg(reinterpret_cast<const uint2 *>(cx.p + cx.roff[j] + 256 * (g + 2)) + lane);
-            if constexpr (kVerify) {
+            if constexpr (kVerify && kBlk) {
+                const uint32_t k = g >> 2;
+                if (cx.kind[j] == kKRaw && k < blocks) {
+                    if ((g & 3u) == 1u) {
+                        const uint4 *q = reinterpret_cast<const uint4 *>(cx.p + cx.roff[j] + 1024ull * k) + 2 * lane;
+                        cb0[j] = __ldg(q);
+                        cb1[j] = __ldg(q + 1);
+                    } else if ((g & 3u) == 3u) {
+                        Rraw[j] = (k ? shift_smem(Rraw[j], gshift) : 0u) ^
+                                  crc_rep16<C>(crc_rep16<C>(0u, cb0[j], row), cb1[j], row);
+                    }
+                }
+            } else if constexpr (kVerify) {
                 if (cx.kind[j] == kKRaw)
                     Rraw[j] = (g ? shift_smem(Rraw[j], gshift) : 0u) ^
                               crc_rep_word<C>(crc_rep_word<C>(0u, col[j].lo, row), col[j].hi, row);
@@ -830,8 +856,14 @@ __device__ void consume(const DecodeArgs &a, const ChunkCtx &cx, PS &ps, uint32_
             uint32_t part;
             if (cx.kind[j] == kKRaw) {
                 seg_len = pad16(cx.n);
-                part = groups ? crc_fold<1, 3>(Rraw[j], nullptr) : 0u;
-                const uint32_t done = 256 * groups;
+                uint32_t done;
+                if constexpr (kBlk) {
+                    part = blocks ? crc_fold<1, 5>(Rraw[j], nullptr) : 0u;
+                    done = 1024 * blocks;
+                } else {
+                    part = groups ? crc_fold<1, 3>(Rraw[j], nullptr) : 0u;
+                    done = 256 * groups;
+                }
                 part = crc_strided<1, false, C>(seg + done, seg_len - done, part, crc_rep, gap496, nullptr);
             } else {
                 seg_len = pad16(cx.val[j]);
@@ -968,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int warp = threadIdx.x >> 5;
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep<C>(crc_rep);
-        load_shift_smem(gshift, kShPow + 8);  // 256 bytes
+        load_shift_smem(gshift, consume_shift_table<WordOf<DT>::W>());
         load_shift_smem(gap496, kSh496);
     }
     constexpr int kWpc = warps_per_chunk<kBig>();
@@ -1029,7 +1061,7 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
 
     if (!(a.flags & ZC_NO_VERIFY)) {
         load_crc_rep<C>(crc_rep);
-        load_shift_smem(gshift, kShPow + 8);  // 256 bytes
+        load_shift_smem(gshift, consume_shift_table<W>());
         load_shift_smem(gap496, kSh496);
     }
     const uint32_t pairs_per_cta = blockDim.x >> 6;
