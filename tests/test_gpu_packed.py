@@ -35,15 +35,18 @@ def _run(src: torch.Tensor, dtype: int, shape, chunk: int, version: int, stream,
 @pytest.mark.parametrize("version", [1, 2, 3])
 def test_packed_blobs_match_oracle(zco, version):
     rng = np.random.default_rng(91)
-    cases = [(wl.BF16, wl.as_bytes(wl.bf16_1m("cpu")).numpy(), 4096),     # 512 chunks: many CTAs of 16
+    cases = [(wl.BF16, np.zeros(0, np.uint8), 4096),                       # empty
+             (wl.BF16, wl.as_bytes(wl.bf16_1m("cpu")).numpy()[:2], 4096),  # one element
+             (wl.U16, rng.integers(0, 256, 2 * 4097, dtype=np.uint8), 64),   # 129 chunks of 64 bytes, ragged
+             (wl.BF16, wl.as_bytes(wl.bf16_1m("cpu")).numpy(), 4096),     # 512 chunks: many CTAs of 16
              (wl.FP32, wl.as_bytes(wl.fp32_64m("cpu", rows=32)).numpy(), 8192),
              (wl.FP16, wl.as_bytes(wl.fp16_16m("cpu", rows=64)).numpy(), 131072),
              (wl.U8, rng.integers(0, 16, 300_001, dtype=np.uint8), 65536)]
     stream = torch.cuda.Stream(device=DEV)
     for dtype, raw, chunk in cases:
-        W = {wl.BF16: 2, wl.FP32: 4, wl.FP16: 2, wl.U8: 1}[dtype]
+        W = {wl.BF16: 2, wl.FP32: 4, wl.FP16: 2, wl.U8: 1, wl.U16: 2}[dtype]
         shape = (raw.size // W,)
-        src = torch.from_numpy(raw.copy()).to(DEV)
+        src = torch.from_numpy(raw.copy()).to(DEV) if raw.size else torch.empty(16, dtype=torch.uint8, device=DEV)[:0]
         ws = torch.empty(max(16, zc.workspace_size(raw.size, dtype, chunk, FLAGS[version])), dtype=torch.uint8,
                          device=DEV)
         stream.wait_stream(torch.cuda.current_stream())

@@ -200,8 +200,9 @@ def _compress_with_workspace(raw: np.ndarray, dtype: int, chunk: int, thr: float
 
 @pytest.mark.parametrize("dtype,thr", [(6, 0.95), (4, 0.95), (1, 2.0)])
 def test_small_workspace_many_waves(zco, dtype, thr):
-    """A workspace far below zc_workspace_size: one coding warp and waves of a
-    few chunks each, the offset scan running across the waves."""
+    """A workspace far below zc_workspace_size: waves of a few chunks each
+    (every chunk of a wave with a coding warp of its own, as many as the
+    slots that fit), the offset scan running across the waves."""
     rng = np.random.default_rng(5 + dtype)
     raw = _rand_tensor(rng, dtype, 75_000)
     chunk = 4096
@@ -211,8 +212,8 @@ def test_small_workspace_many_waves(zco, dtype, thr):
     n_pad = (chunk // W + 31) // 32 * 32
     per_chunk = 32 + W * (512 + n_pad)
     full = zc.workspace_size(raw.size, dtype, chunk)
-    # control + status words, room for about 5 chunks of a wave, and slots for
-    # one coding warp (bounded by a generous record size)
+    # control + status words, room for about 5 chunks of a wave, and about
+    # one coding slot (bounded by a generous record size)
     small = 256 + (8 * nc + 255) // 256 * 256 + 5 * per_chunk + 1024 + 2 * W * (2 * chunk // W + 4096)
     assert small < full
     got = _compress_with_workspace(raw, dtype, chunk, thr, small)
