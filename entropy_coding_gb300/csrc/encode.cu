@@ -37,7 +37,7 @@ constexpr int kCodeWarps = 16;    // coding warps per SM (and at most per CTA)
 constexpr int kCodeThreads = 32 * kCodeWarps;
 constexpr uint32_t kModeCand = 3;  // statistics -> coder only: a stream to rANS-code
 constexpr uint32_t kAborted = 0xFFFFFFFFu;
-constexpr uint32_t kCodeWarpSmem = 2048 + 4096 + 4096;  // per coding warp: rANS table, symbol ring, 2 word stages
+constexpr uint32_t kCodeWarpSmem = 4096 + 4096 + 4096;  // per coding warp: rANS table, symbol ring, 2 word stages
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 
 // Exact division by a table frequency f in [1, 4095] for every dividend the
@@ -735,9 +735,9 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
 
 // Code one stream of the chunk into rec (the warp's slot), one warp, with the
 // 12-bit table f (8 entries per lane) and the stream's bytes in cand (element
-// order, padded to whole steps). Per symbol the table keeps 8 bytes,
-// {m, f | cum << 12 | (k-32) << 24 | (a != 0) << 31} with a = 0 or m, so
-// that a step is:
+// order, padded to whole steps). Per symbol the table keeps 16 bytes,
+// {m, a, 2^20 f, (4096 - f) | cum << 13 | (k-32) << 25} (bits 29-31 zero;
+// a = 0 or m), so that a step is:
 // renormalise if x >= 2^20 f, q = (x m + a) >> k, x += q (4096 - f) + cum.
 // The steps run in blocks of 32 (the last steps of the stream first); the
 // symbols of the next three blocks are in flight into a shared-memory ring
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(kStatThreads, 2) stats_kernel(EncodeArgs a) {
 // counts (the record's size counts each list padded to 8 words), and
 // warp_copy_crc_lanes gathers the lists into place in the blob.
 template <bool kLanes>
-__device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint2 *etab,
+__device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const uint32_t f[8], uint4 *etab,
                                        uint8_t *ring, uint16_t *stage_base, uint8_t *rec, uint64_t lim,
                                        bool shared) {
     const int lane = threadIdx.x & 31;
@@ -800,7 +800,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
             if (!shared) reinterpret_cast<uint16_t *>(rec + kRecHead)[rank] = uint16_t(fs);
             rank++;
             const uint32_t ka = kRecip.ka[fs], m = kRecip.m[fs];
-            etab[s] = make_uint2(m, fs | (cum << 12) | (((ka & 0xFFu) - 32) << 24) | ((ka >> 8) ? 0x80000000u : 0u));
+            etab[s] = make_uint4(m, (ka >> 8) ? m : 0u, fs << 20, (kM - fs) | (cum << 13) | (((ka & 0xFFu) - 32) << 25));
         }
         cum += fs;
     }
@@ -842,23 +842,19 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
     const bool first_active = uint32_t(T - 1) * 32 + lane < n;
     // one coding step with table entry ec; returns whether it renormalised
     // (emitting the low 16 bits of the state before it)
-    auto code_step = [&](const uint2 ec) -> bool {
-        const uint32_t fs = ec.y & 0xFFFu;
-        const bool emit = x >= (fs << 20);
+    auto code_step = [&](const uint4 ec) -> bool {
+        const bool emit = x >= ec.z;
         if constexpr (kLanes) push_if(emit, x & 0xFFFFu, wc);
         x = emit ? x >> 16 : x;
-        const uint32_t add = int32_t(ec.y) < 0 ? ec.x : 0u;
-        const uint32_t q = uint32_t((uint64_t(x) * ec.x + add) >> 32) >> ((ec.y >> 24) & 31u);
-        x = x + q * (kM - fs) + ((ec.y >> 12) & 0xFFFu);
+        const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+        x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
         return emit;
     };
     // step T-1, the only one that may be partial; no lane emits a word there
     // (x = 2^16 is below every 2^20 f)
-    auto first_step = [&](const uint2 ec) {
-        const uint32_t fs = ec.y & 0xFFFu;
-        const uint32_t add = int32_t(ec.y) < 0 ? ec.x : 0u;
-        const uint32_t q = uint32_t((uint64_t(x) * ec.x + add) >> 32) >> ((ec.y >> 24) & 31u);
-        if (first_active) x = x + q * (kM - fs) + ((ec.y >> 12) & 0xFFFu);
+    auto first_step = [&](const uint4 ec) {
+        const uint32_t q = uint32_t((uint64_t(x) * ec.x + ec.y) >> 32) >> (ec.w >> 25);
+        if (first_active) x = x + q * (ec.w & 0x1FFFu) + ((ec.w >> 13) & 0xFFFu);
     };
     // write out the words of one staged block (steps 0..cnt-1, emitting lanes
     // 31..0 within a step)
@@ -893,11 +889,11 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
                 s = 1;
             }
             uint32_t sym_n = blk[(s + 2) * 32];
-            uint2 e = etab[blk[s * 32]], e2 = etab[blk[(s + 1) * 32]];
+            uint4 e = etab[blk[s * 32]], e2 = etab[blk[(s + 1) * 32]];
             if (cnt == 32 && s == 0) {
 #pragma unroll 8
                 for (int k = 0; k < 32; k++) {
-                    const uint2 ec = e;
+                    const uint4 ec = e;
                     e = e2;
                     e2 = etab[sym_n];
                     sym_n = blk[(k + 3) * 32];
@@ -906,7 +902,7 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
             } else {
 #pragma unroll 4
                 for (; s < cnt; s++) {
-                    const uint2 ec = e;
+                    const uint4 ec = e;
                     e = e2;
                     e2 = etab[sym_n];
                     sym_n = blk[(s + 3) * 32];
@@ -922,11 +918,11 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
                 // one (always full): one straight-line body, so the two
                 // chains overlap
                 uint32_t sym_n = blk[64];
-                uint2 e = etab[blk[0]], e2 = etab[blk[32]];
+                uint4 e = etab[blk[0]], e2 = etab[blk[32]];
                 uint32_t fp = flags_prev;
 #pragma unroll 8
                 for (int s = 0; s < 32; s++) {
-                    const uint2 ec = e;
+                    const uint4 ec = e;
                     e = e2;
                     e2 = etab[sym_n];
                     sym_n = blk[(s + 3) * 32];
@@ -947,10 +943,10 @@ __device__ uint32_t rans_encode_stream(const uint8_t *cand, uint32_t n, const ui
                     s = 1;
                 }
                 uint32_t sym_n = blk[(s + 2) * 32];
-                uint2 e = etab[blk[s * 32]], e2 = etab[blk[(s + 1) * 32]];
+                uint4 e = etab[blk[s * 32]], e2 = etab[blk[(s + 1) * 32]];
 #pragma unroll 4
                 for (; s < cnt; s++) {
-                    const uint2 ec = e;
+                    const uint4 ec = e;
                     e = e2;
                     e2 = etab[sym_n];
                     sym_n = blk[(s + 3) * 32];
@@ -1255,7 +1251,7 @@ __device__ void warp_copy_src(Source<kDelta> src, uint64_t len, uint8_t *dst) {
 
 template <int DT, int J>
 __device__ __forceinline__ void code_stream(const EncodeArgs &a, uint32_t cl, uint32_t t, uint32_t n, uint64_t lim,
-                                            uint2 *etab, uint8_t *ring, uint8_t *slot, uint32_t mode[4],
+                                            uint4 *etab, uint8_t *ring, uint8_t *slot, uint32_t mode[4],
                                             uint32_t val[4]) {
     constexpr int W = WordOf<DT>::W;
     if (mode[J] != kModeCand) return;
@@ -1296,8 +1292,8 @@ __global__ void __launch_bounds__(kCodeThreads, 1) code_kernel(EncodeArgs a) {
     if (gw >= a.workers) return;
     const CrcSmem cs{crc_rep, gap496};
     uint8_t *warp_smem = smem_raw + kCodeCrcBytes + kCodeWarpSmem * warp;
-    uint2 *etab = reinterpret_cast<uint2 *>(warp_smem);
-    uint8_t *ring = warp_smem + 2048;
+    uint4 *etab = reinterpret_cast<uint4 *>(warp_smem);
+    uint8_t *ring = warp_smem + 4096;
     uint8_t *slot = a.ws_slots + uint64_t(gw) * a.slot_bytes;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws_ctrl);
 
