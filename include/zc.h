@@ -212,7 +212,7 @@ ZC_API int zc_compress_delta(const void *d_base, const void *d_new, uint64_t nby
 /* Decompress a blob made by zc_compress_delta (or by zc_compress of a
  * difference) and XOR it with the base in the same pass: d_dst receives
  * base XOR decoded. The per-chunk CRC is checked over the stored bytes, as
- * in zc_decompress, unless flags has ZC_NO_VERIFY.
+ * in zc_decompress, unless flags has ZC_NO_VERIFY; ZC_PACKED as there.
  *   info           from zc_blob_info; its dtype must be ZC_U8/U16/U32
  *   d_base, d_dst  device buffers of info->nbytes bytes, 16-byte aligned;
  *                  d_dst may not overlap d_base or the blob
@@ -266,6 +266,7 @@ ZC_API uint64_t zc_workspace_size_batch(const uint64_t *nbytes, uint32_t n, int 
  *                          chunk_bytes (else ZC_EINVAL)
  *   d_bases                NULL, or n device base tensors (delta blobs)
  *   d_dsts[t], dst_capacities[t]  output t, as in zc_decompress
+ *   flags                  as in zc_decompress (ZC_NO_VERIFY, ZC_PACKED)
  *   d_ws, ws_bytes         ws_bytes >= zc_decompress_workspace_size_batch(n)
  *                          (0 for n <= 1, when d_ws may be NULL)
  *   d_status               one device int32 for the whole call
