@@ -164,16 +164,18 @@ def compress_into(src: torch.Tensor, blob: torch.Tensor, blob_bytes: torch.Tenso
 
 def compress(t: torch.Tensor, chunk_bytes: int = DEFAULT_CHUNK, threshold: float = DEFAULT_THRESHOLD,
              stream=None, host_blob: bool = False, shared_tables: bool = False,
-             lane_words: bool = False) -> torch.Tensor:
+             lane_words: bool = False, packed: bool = False) -> torch.Tensor:
     """Compress a CUDA tensor into a self-describing blob (1-D uint8 tensor).
 
     The blob is a CUDA tensor, or with ``host_blob`` a page-locked CPU tensor
     that the kernels write directly over the host link (no separate copy).
     ``shared_tables`` writes format v2 (one table per byte plane of the
     tensor), ``lane_words`` format v3 (a word list per rANS lane, which the
-    decoder steps through without waiting on the other lanes). Synchronises
-    once, to read the blob length."""
-    flags = (SHARED_TABLES if shared_tables else 0) | (LANE_WORDS if lane_words else 0)
+    decoder steps through without waiting on the other lanes). ``packed``
+    (ZC_PACKED) fills few SMs, for calls on several streams at once; it
+    changes no byte of the blob. Synchronises once, to read the blob
+    length."""
+    flags = (SHARED_TABLES if shared_tables else 0) | (LANE_WORDS if lane_words else 0) | (PACKED if packed else 0)
     if not t.is_cuda:
         raise ZcError(EINVAL, "compress expects a CUDA tensor")
     src = t.contiguous()
@@ -251,11 +253,12 @@ def _readable(blob: torch.Tensor) -> bool:
 
 
 def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True, stream=None,
-               device=None) -> torch.Tensor:
+               device=None, packed: bool = False) -> torch.Tensor:
     """Restore the exact tensor (dtype and shape from the blob header). The
     blob is a CUDA tensor or a page-locked CPU tensor, which the kernel reads
     directly; the tensor is made on the blob's device (CUDA blob) or on
-    ``device`` (default: the current CUDA device)."""
+    ``device`` (default: the current CUDA device). ``packed`` as in
+    compress()."""
     if not _readable(blob):
         raise ZcError(EINVAL, "decompress expects a CUDA or page-locked CPU blob")
     info = read_info(blob) if info is None else info
@@ -264,7 +267,7 @@ def decompress(blob: torch.Tensor, info: dict | None = None, verify: bool = True
     dt = _CODE_TO_TORCH[info["dtype"]]
     out = torch.empty(info["shape"], dtype=dt, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    decompress_into(blob, info, out, status, verify, stream)
+    decompress_into(blob, info, out, status, verify, stream, packed)
     _check(int(status.item()), "zc_decompress (device)")
     return out
 
@@ -317,10 +320,11 @@ def compress_delta(base: torch.Tensor, new: torch.Tensor, chunk_bytes: int = DEF
 
 
 def decompress_delta_into(blob: torch.Tensor, info: dict, base: torch.Tensor, out: torch.Tensor,
-                          status: torch.Tensor, verify: bool = True, stream=None) -> None:
+                          status: torch.Tensor, verify: bool = True, stream=None, packed: bool = False) -> None:
     """Launch decompression of a difference blob XOR-ed with base into out."""
     st = lib().zc_decompress_delta(blob.data_ptr(), ctypes.byref(_info_struct(info)), base.data_ptr(),
-                                   out.data_ptr(), out.numel() * out.element_size(), 0 if verify else NO_VERIFY,
+                                   out.data_ptr(), out.numel() * out.element_size(),
+                                   (0 if verify else NO_VERIFY) | (PACKED if packed else 0),
                                    status.data_ptr(), _stream(stream))
     _check(st, "zc_decompress_delta")
 

@@ -88,3 +88,14 @@ def test_packed_calls_on_several_streams(zco, version):
         assert int(st[1].item()) == 0 and torch.equal(out, src)
         want = zco.compress(src.cpu().numpy(), wl.BF16, tuple(sh), 131072, 0.95, version)
         assert got.cpu().numpy().tobytes() == want
+
+
+def test_packed_python_api():
+    """compress(..., packed=True) makes the same blob as without, and
+    decompress(..., packed=True) restores the tensor."""
+    t = wl.llama8b_tensor(3, "layers.0.v", (1024, 4096), DEV)
+    for kw in ({}, {"lane_words": True}, {"shared_tables": True}):
+        a = zc.compress(t, **kw)
+        b = zc.compress(t, packed=True, **kw)
+        assert torch.equal(a, b), kw
+        assert torch.equal(zc.decompress(b, packed=True).view(torch.int16), t.view(torch.int16)), kw
