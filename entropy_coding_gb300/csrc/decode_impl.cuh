@@ -63,7 +63,9 @@ struct PairSmem {
     uint32_t big[kBig ? kM : 1];     // one-level table (kBig)
     alignas(16) uint8_t stage[kStages][256];  // decoded symbols, row k = step k of a group (read as uint2)
     unsigned long long full[kStages], empty[kStages], start;
+    unsigned long long crc_bar;      // kBig: the second CRC warp's half is in crc_part
     uint32_t flag;                   // producer -> consumer: 1 when the main stream is ready
+    uint32_t crc_part;
 };
 
 // Shared memory of one warp pair in format v2: the decoding tables are the
@@ -917,12 +919,32 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
     }
     const uint8_t *p = blob + off;
     const bool verify = !(a.flags & ZC_NO_VERIFY);
-    if (role == 2) {
-        // CRC warp: the stored bytes, 8 pieces of 16 bytes in flight per
-        // lane, then the last stored % 16 bytes one at a time
+    if (role >= 2) {
+        // the two CRC warps: the stored bytes' first and second half of the
+        // 16-byte pieces (8 in flight per lane), each register taken from
+        // zero; the second warp hands its register over through shared
+        // memory, the first appends it (linearity) and the last stored % 16
+        // bytes one at a time
         if (!verify) return;
-        const uint32_t main = stored & ~15u;
-        uint32_t reg = shift_bytes_small(0xFFFFFFFFu, main) ^ warp_crc16<C, false, 8>(p, main, crc_rep, gap496);
+        const uint32_t main = stored & ~15u, half = kCrcWarp ? (main >> 5) << 4 : main;
+        if constexpr (kCrcWarp) {
+            if (role == 3) {
+                const uint32_t r1 = warp_crc16<C, false, 8>(p + half, main - half, crc_rep, gap496);
+                if (lane == 0) ps.crc_part = r1;
+                __syncwarp();
+                mbar_arrive(&ps.crc_bar);
+                return;
+            }
+        }
+        uint32_t reg = warp_crc16<C, false, 8>(p, half, crc_rep, gap496);
+        if constexpr (kCrcWarp) {
+            if (!mbar_wait(&ps.crc_bar, 0, a.wait_cycles)) {
+                if (lane == 0) status_or(a.d_status, ZC_ETIMEOUT);
+                return;
+            }
+            reg = shift_bytes_small(reg, main - half) ^ ps.crc_part;
+        }
+        reg ^= shift_bytes_small(0xFFFFFFFFu, main);
         const uint32_t *row = crc_row<C>(crc_rep);
         for (uint32_t i = main; i < stored; i++) reg = crc_rep_byte<C>(reg, __ldg(p + i), row);
         if ((reg ^ 0xFFFFFFFFu) != ent.w && lane == 0) status_or(a.d_status, ZC_ECRC);
@@ -984,10 +1006,11 @@ __device__ void decode_chunk(const DecodeArgs &a, const BlobDesc &bd, uint32_t c
 // table per pair) the CRC tables have 8 copies; with two-level tables (up
 // to 16 pairs) they have 16, so fewer lanes meet on a bank.
 // Warps per chunk: with one-level tables (few chunks per SM, so the pair's
-// chains are latency-bound) a third warp checks the chunk's CRC; with up to
-// 16 pairs per CTA there is no room for it and the consumer takes the CRC.
+// chains are latency-bound) two more warps check the chunk's CRC, half of
+// the stored bytes each; with up to 16 pairs per CTA there is no room for
+// them and the consumer takes the CRC.
 template <bool kBig>
-constexpr int warps_per_chunk() { return kBig ? 3 : 2; }
+constexpr int warps_per_chunk() { return kBig ? 4 : 2; }
 
 template <int DT, bool kBig, bool kDelta, bool kLanes>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
@@ -1012,15 +1035,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
             mbar_init(&ps.empty[k], 32);
         }
         mbar_init(&ps.start, 32);
+        mbar_init(&ps.crc_bar, 32);
     }
     __syncthreads();
-    const uint32_t slot = uint32_t(warp) / kWpc;
+    // warp w has role w / pairs_per_cta for chunk slot w % pairs_per_cta: the
+    // warps of one role are consecutive, so they spread over the SM's four
+    // schedulers (warp w issues from scheduler w % 4) instead of piling one
+    // role onto one of them
+    const uint32_t slot = uint32_t(warp) % pairs_per_cta;
+    const int role = int(uint32_t(warp) / pairs_per_cta);
     const uint32_t g = blockIdx.x * pairs_per_cta + slot;
     if (g >= a.total_chunks) return;
     // the blob of this call-wide chunk index
     const BlobDesc bd = a.n_blobs == 1 ? a.one : a.blobs[owner_of(a.blobs, a.n_blobs, g)];
-    decode_chunk<DT, kBig, kDelta, false, C, kLanes, kBig>(a, bd, g - bd.chunk_base, int(uint32_t(warp) % kWpc),
-                                                           pairs[slot], crc_rep, gshift, gap496, nullptr);
+    decode_chunk<DT, kBig, kDelta, false, C, kLanes, kBig>(a, bd, g - bd.chunk_base, role, pairs[slot], crc_rep,
+                                                           gshift, gap496, nullptr);
 }
 
 // Format v2 (shared plane tables): a CTA decodes up to a.pairs consecutive
@@ -1126,13 +1155,15 @@ __global__ void __launch_bounds__(kV2Threads, 1) decode_v2_kernel(DecodeArgs a) 
         big[i] = sy | (e & 0xFFFu) << 8 | (slot - (e >> 12)) << 20;
     }
     __syncthreads();
-    const uint32_t pair = uint32_t(warp >> 1);
+    // warp w: role w / pairs_per_cta for pair w % pairs_per_cta (the roles
+    // spread over the SM's schedulers)
+    const uint32_t pair = uint32_t(warp) % pairs_per_cta;
     if (first + pair >= bd.n_chunks) return;
     const uint32_t *pbig[4] = {nullptr, nullptr, nullptr, nullptr};
 #pragma unroll
     for (int j = 0; j < W; j++) pbig[j] = pvalid[j] ? big + j * kM : nullptr;
-    decode_chunk<DT, true, kDelta, true, C, false, false>(a, bd, first + pair, warp & 1, pairs[pair], crc_rep,
-                                                          gshift, gap496, pbig);
+    decode_chunk<DT, true, kDelta, true, C, false, false>(a, bd, first + pair, int(uint32_t(warp) / pairs_per_cta),
+                                                          pairs[pair], crc_rep, gshift, gap496, pbig);
 }
 
 template <int DT, bool kBig, bool kDelta, bool kLanes>
