@@ -624,9 +624,10 @@ def run_model(a, world, rank, local, dev, stream):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_ach / hbm, 4),
                      "frac_of_nominal": round(dom_ach / NOMINAL_HBM_GBS, 4),
                      "traffic": profiled_traffic(dom_kernel, a.workload, format_version(a), packed),
-                     "algorithmic_bytes_per_launch": alg if batched else None,
-                     "note": ("compression" if enc_dom else "decompression") + " phase of the whole model: its "
-                             "algorithmic bytes (original + blob) over its time"},
+                     "algorithmic_bytes_per_launch": alg,
+                     "note": ("compression" if enc_dom else "decompression") + " phase of the whole model ("
+                             + ("one batched call" if batched else f"{n} calls on {n_streams} streams") + "): its "
+                             "algorithmic bytes (original + blob) over its time; traffic likewise per phase"},
         "clocks": clk.summary(),
         "e2e": {"value": round(N * e2e_steps / t_hb / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": hb_h2d // e2e_steps, "d2h_bytes_per_step": hb_d2h // e2e_steps,
